@@ -1,0 +1,168 @@
+"""fp64 CPU oracle for HYPIC's linear-layer state path (test infrastructure only).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+import this package. The product path (the CUDA library and its Python binding) never
+does, and the two share no code: this package compiles and calls ``hypic_oracle.c``,
+a token-by-token fp64 program written from the definitions on the pages (see the header
+of that file for the passages it follows).
+
+Every array goes in and out as C-contiguous float64 numpy arrays; the caller converts
+bf16 / fp32 inputs to float64 exactly (every bf16 and fp32 value is a float64 value).
+
+Parity pins: every function here is pinned in ``tests/test_oracle.py`` against closed
+forms, invariants and brute force; no function is left "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "hypic_oracle.c")
+_LIB = os.path.join(_HERE, "libhypic_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+FAMILIES = {"linear": 0, "scalar": 1, "diag": 2, "delta": 3, "gdn": 4}
+
+
+def build(force: bool = False) -> str:
+    """Compile hypic_oracle.c into libhypic_oracle.so beside it (plain gcc, OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+               "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            I64 = ctypes.c_int64
+            lib.oracle_build.argtypes = [I, I, P, I, I, I, I, P, P, P, P, P, P, P, I]
+            lib.oracle_run.argtypes = [I, I, P, I, I, I, I, P, P, P, P, P, P, P, I]
+            lib.oracle_compose_scan.argtypes = [I, I64, I, I, P, P, P, P, I]
+            lib.oracle_materialize_T.argtypes = [I, I64, I, P, P, P]
+            for f in (lib.oracle_build, lib.oracle_run, lib.oracle_compose_scan,
+                      lib.oracle_materialize_T):
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(a):
+    if a is None:
+        return None
+    a = np.ascontiguousarray(a, dtype=np.float64)
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _family(family):
+    return FAMILIES[family] if isinstance(family, str) else int(family)
+
+
+def build_segments(family, seg_offsets, k, v, log_gate=None, log_gamma=None, beta=None,
+                   H_k=None, H_v=None, want_T=True, nthreads=0):
+    """(S(C|0), T_C) per segment and value head, fp64.
+
+    k [N, H_k, d_k], v [N, H_v, d_v]; returns S [n_seg, H_v, d_k, d_v] and
+    T [n_seg, H_v, d_k, d_k] (None when want_T is False).
+    """
+    lib = _load()
+    offs = np.ascontiguousarray(seg_offsets, dtype=np.int64)
+    k, v = _f64(k), _f64(v)
+    log_gate, log_gamma, beta = _f64(log_gate), _f64(log_gamma), _f64(beta)
+    N, Hk, dk = k.shape
+    _, Hv, dv = v.shape
+    n_seg = len(offs) - 1
+    assert offs[0] == 0 and offs[-1] == N
+    S = np.zeros((n_seg, Hv, dk, dv))
+    T = np.zeros((n_seg, Hv, dk, dk)) if want_T else None
+    rc = lib.oracle_build(_family(family), n_seg, _ptr(offs), Hk, Hv, dk, dv, _ptr(k), _ptr(v),
+                          _ptr(log_gate), _ptr(log_gamma), _ptr(beta), _ptr(S), _ptr(T),
+                          nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_build failed ({rc})")
+    return S, T
+
+
+def run_sequential(family, seg_offsets, k, v, log_gate=None, log_gamma=None, beta=None,
+                   S0=None, nthreads=0):
+    """State after every segment of one sequential pass, fp64: [n_seg, H_v, d_k, d_v]."""
+    lib = _load()
+    offs = np.ascontiguousarray(seg_offsets, dtype=np.int64)
+    k, v = _f64(k), _f64(v)
+    log_gate, log_gamma, beta, S0 = _f64(log_gate), _f64(log_gamma), _f64(beta), _f64(S0)
+    N, Hk, dk = k.shape
+    _, Hv, dv = v.shape
+    n_seg = len(offs) - 1
+    out = np.zeros((n_seg, Hv, dk, dv))
+    rc = lib.oracle_run(_family(family), n_seg, _ptr(offs), Hk, Hv, dk, dv, _ptr(k), _ptr(v),
+                        _ptr(log_gate), _ptr(log_gamma), _ptr(beta), _ptr(S0), _ptr(out),
+                        nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_run failed ({rc})")
+    return out
+
+
+def compose_scan(T, S, S0=None, nthreads=0):
+    """prefix_j = T_j prefix_{j-1} + S_j; T [n_seg, U, d_k, d_k], S [n_seg, U, d_k, d_v]."""
+    lib = _load()
+    T, S, S0 = _f64(T), _f64(S), _f64(S0)
+    n_seg, U, dk, dv = S.shape
+    assert T.shape == (n_seg, U, dk, dk)
+    out = np.zeros_like(S)
+    rc = lib.oracle_compose_scan(n_seg, U, dk, dv, _ptr(T), _ptr(S), _ptr(S0), _ptr(out),
+                                 nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_compose_scan failed ({rc})")
+    return out
+
+
+def materialize_T(family, lam, P=None, d_k=None):
+    """Dense fp64 T from the library's log-scaled storage T = exp(lam) P.
+
+    lam has shape [..., ] (scalar families, GDN, DeltaNet) or [..., d_k] (DIAG);
+    P [..., d_k, d_k] for DELTA / GDN. Returns [..., d_k, d_k].
+    """
+    lib = _load()
+    fam = _family(family)
+    lam = _f64(lam)
+    if fam == FAMILIES["diag"]:
+        d_k = lam.shape[-1]
+        lead = lam.shape[:-1]
+    elif fam in (FAMILIES["delta"], FAMILIES["gdn"]):
+        P = _f64(P)
+        d_k = P.shape[-1]
+        lead = P.shape[:-2]
+    else:
+        assert d_k is not None
+        lead = lam.shape
+    n = int(np.prod(lead)) if len(lead) else 1
+    out = np.zeros(lead + (d_k, d_k))
+    rc = lib.oracle_materialize_T(fam, n, d_k, _ptr(lam), _ptr(P), _ptr(out))
+    if rc != 0:
+        raise RuntimeError(f"oracle_materialize_T failed ({rc})")
+    return out

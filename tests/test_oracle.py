@@ -1,0 +1,327 @@
+"""Pins for the fp64 oracle: each check ties it to something other than itself.
+
+What pins what (a plausible mistake anywhere in the oracle fails at least one check):
+
+* hand-derived fixtures under tests/golden (exact decimals, derivation in the file);
+* closed forms: plain linear attention (S = K^T V, T = I), scalar decay
+  (T = gamma^L I, S = decayed sum), diagonal gates (T = Diag(prod g)), one-token GDN;
+* delta-rule semantics: with b = 1 and |k| = 1 the last write is retrieved exactly
+  (k^T S = v^T) and the last key is annihilated by T (k^T T = 0);
+* invariants: det T = prod_t a_t^d (1 - b_t |k_t|^2); S(C|S0) - S(C|0) = T S0;
+* brute force on tiny inputs in exact rational arithmetic (sympy), with the transition
+  factors formed as dense matrices and multiplied out;
+* the composition theorem against the oracle's own sequential run, and the failure of
+  naive end-state addition for RetNet (but not for plain linear attention).
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_attention_state_gdn_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f64(t):
+    return None if t is None else t.double().numpy()
+
+
+def run_build(inp, want_T=True):
+    return oracle.build_segments(inp.family, inp.seg_offsets, f64(inp.k), f64(inp.v),
+                                 f64(inp.log_gate), f64(inp.log_gamma), f64(inp.beta),
+                                 want_T=want_T)
+
+
+def run_seq(inp, S0=None):
+    return oracle.run_sequential(inp.family, inp.seg_offsets, f64(inp.k), f64(inp.v),
+                                 f64(inp.log_gate), f64(inp.log_gamma), f64(inp.beta), S0=S0)
+
+
+def relF(a, b):
+    return np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300)
+
+
+# ------------------------------------------------------------------ hand-derived fixtures
+
+def test_golden_gdn_two_segments():
+    g = json.load(open(os.path.join(GOLDEN, "gdn_d2_two_segments.json")))
+    k = np.array(g["k"])[:, None, :]
+    v = np.array(g["v"])[:, None, :]
+    beta = np.array(g["beta"])[:, None]
+    log_a = np.log(np.array(g["alpha"]))[:, None]
+    offs = np.array(g["seg_offsets"])
+    S, T = oracle.build_segments("gdn", offs, k, v, log_gate=log_a, beta=beta)
+    np.testing.assert_allclose(S[0, 0], g["S_C1"], atol=1e-14)
+    np.testing.assert_allclose(T[0, 0], g["T_C1"], atol=1e-14)
+    np.testing.assert_allclose(S[1, 0], g["S_C2"], atol=1e-14)
+    np.testing.assert_allclose(T[1, 0], g["T_C2"], atol=1e-14)
+    pref = oracle.compose_scan(T, S)
+    np.testing.assert_allclose(pref[1, 0], g["S_C1C2"], atol=1e-14)
+    seq = oracle.run_sequential("gdn", offs, k, v, log_gate=log_a, beta=beta)
+    np.testing.assert_allclose(seq[1, 0], g["S_C1C2"], atol=1e-14)
+    np.testing.assert_allclose(S[0, 0] + S[1, 0], g["naive_add"], atol=1e-14)
+
+
+def test_golden_retnet_scalar():
+    g = json.load(open(os.path.join(GOLDEN, "retnet_d1_hand.json")))
+    k = np.array(g["k"])[:, None, None]
+    v = np.array(g["v"])[:, None, None]
+    offs = np.array(g["seg_offsets"])
+    log_gamma = np.array([np.log(g["gamma"])])
+    S, T = oracle.build_segments("scalar", offs, k, v, log_gamma=log_gamma)
+    assert S[0, 0, 0, 0] == pytest.approx(g["S_C1"], abs=1e-14)
+    assert T[0, 0, 0, 0] == pytest.approx(g["T_C1"], abs=1e-14)
+    assert S[1, 0, 0, 0] == pytest.approx(g["S_C2"], abs=1e-14)
+    assert T[1, 0, 0, 0] == pytest.approx(g["T_C2"], abs=1e-14)
+    pref = oracle.compose_scan(T, S)
+    assert pref[1, 0, 0, 0] == pytest.approx(g["S_C1C2"], abs=1e-14)
+    assert S[0, 0, 0, 0] + S[1, 0, 0, 0] == pytest.approx(g["naive_add"], abs=1e-14)
+
+
+# ------------------------------------------------------------------ closed forms
+
+def _segments(inp):
+    o = inp.seg_offsets
+    return [(int(o[j]), int(o[j + 1])) for j in range(inp.n_seg)]
+
+
+def test_linear_closed_form():
+    inp = synth.make_inputs("linear", 2, 4, 8, [5, 0, 17, 3], torch.float32, seed=1)
+    S, T = run_build(inp)
+    k, v = f64(inp.k), f64(inp.v)
+    for j, (a, b) in enumerate(_segments(inp)):
+        for h in range(4):
+            ref = k[a:b, h // 2].T @ v[a:b, h]
+            np.testing.assert_allclose(S[j, h], ref, atol=1e-13)
+            assert np.array_equal(T[j, h], np.eye(8))
+
+
+@pytest.mark.parametrize("per_token", [False, True])
+def test_scalar_closed_form(per_token):
+    inp = synth.make_inputs("scalar", 3, 3, 8, [7, 1, 12], torch.float32, seed=2,
+                            per_token_scalar=per_token, gla_div=2.0)
+    S, T = run_build(inp)
+    k, v = f64(inp.k), f64(inp.v)
+    for j, (a, b) in enumerate(_segments(inp)):
+        for h in range(3):
+            if per_token:
+                lg = f64(inp.log_gate)[a:b, h]
+            else:
+                lg = np.full(b - a, f64(inp.log_gamma)[h])
+            # weight of token t = product of the gates of the tokens after it
+            w = np.exp(np.concatenate([np.cumsum(lg[::-1])[::-1][1:], [0.0]]))
+            ref = (k[a:b, h] * w[:, None]).T @ v[a:b, h]
+            np.testing.assert_allclose(S[j, h], ref, rtol=1e-12, atol=1e-14)
+            np.testing.assert_allclose(T[j, h], np.exp(lg.sum()) * np.eye(8), rtol=1e-12)
+
+
+def test_diag_closed_form():
+    inp = synth.make_inputs("diag", 2, 2, 6, [9, 4], torch.float32, seed=3, gla_div=1.0)
+    S, T = run_build(inp)
+    k, v, lg = f64(inp.k), f64(inp.v), f64(inp.log_gate)
+    for j, (a, b) in enumerate(_segments(inp)):
+        for h in range(2):
+            g = lg[a:b, h]                                   # [L, d_k]
+            after = np.concatenate([np.cumsum(g[::-1], 0)[::-1][1:], np.zeros((1, 6))], 0)
+            ref = (k[a:b, h] * np.exp(after)).T @ v[a:b, h]
+            np.testing.assert_allclose(S[j, h], ref, rtol=1e-12, atol=1e-14)
+            np.testing.assert_allclose(T[j, h], np.diag(np.exp(g.sum(0))), rtol=1e-12)
+
+
+def test_gdn_one_token_closed_form():
+    inp = synth.make_inputs("gdn", 1, 2, 5, [1, 1], torch.float32, seed=4, alpha_scale=0.7)
+    S, T = run_build(inp)
+    k, v, b, la = f64(inp.k), f64(inp.v), f64(inp.beta), f64(inp.log_gate)
+    for t in range(2):
+        for h in range(2):
+            kk = k[t, 0]
+            np.testing.assert_allclose(
+                T[t, h], np.exp(la[t, h]) * (np.eye(5) - b[t, h] * np.outer(kk, kk)), atol=1e-15)
+            np.testing.assert_allclose(S[t, h], b[t, h] * np.outer(kk, v[t, h]), atol=1e-15)
+
+
+def test_gdn_beta_zero_is_pure_decay():
+    inp = synth.make_inputs("gdn", 2, 2, 8, [33, 10], torch.float32, seed=5)
+    inp.beta.zero_()
+    S, T = run_build(inp)
+    assert np.all(S == 0)
+    la = f64(inp.log_gate)
+    for j, (a, b) in enumerate(_segments(inp)):
+        for h in range(2):
+            np.testing.assert_allclose(T[j, h], np.exp(la[a:b, h].sum()) * np.eye(8), rtol=1e-12)
+
+
+def test_empty_segment_is_identity():
+    inp = synth.make_inputs("gdn", 1, 1, 4, [3, 0, 2], torch.float32, seed=6)
+    S, T = run_build(inp)
+    assert np.all(S[1] == 0) and np.array_equal(T[1, 0], np.eye(4))
+
+
+# ------------------------------------------------------------------ delta-rule semantics
+
+@pytest.mark.parametrize("family", ["delta", "gdn"])
+def test_delta_rule_retrieves_last_write(family):
+    """b_L = 1 and |k_L| = 1 (exactly, in binary): k_L^T S = v_L^T and k_L^T T = 0."""
+    inp = synth.make_inputs(family, 1, 1, 4, [6], torch.float64, seed=7)
+    kl = np.array([0.6, 0.0, -0.8, 0.0])    # |kl| = 1 up to one rounding
+    inp.k[-1, 0] = torch.from_numpy(kl)
+    inp.beta[-1, 0] = 1.0
+    S, T = run_build(inp)
+    np.testing.assert_allclose(kl @ S[0, 0], f64(inp.v)[-1, 0], atol=1e-14)
+    np.testing.assert_allclose(kl @ T[0, 0], np.zeros(4), atol=1e-15)
+
+
+# ------------------------------------------------------------------ invariants
+
+@pytest.mark.parametrize("family", ["delta", "gdn"])
+def test_det_invariant(family):
+    inp = synth.make_inputs(family, 1, 1, 6, [11], torch.float64, seed=8, l2norm_k=False,
+                            k_scale=0.5, alpha_scale=0.3)
+    S, T = run_build(inp)
+    k, b = f64(inp.k)[:, 0], f64(inp.beta)[:, 0]
+    sign, logdet = np.linalg.slogdet(T[0, 0])
+    la = f64(inp.log_gate)[:, 0].sum() if family == "gdn" else 0.0
+    expect = 6 * la + np.sum(np.log(np.abs(1 - b * (k * k).sum(1))))
+    assert sign == np.prod(np.sign(1 - b * (k * k).sum(1)))
+    assert logdet == pytest.approx(expect, rel=1e-12, abs=1e-12)
+
+
+@pytest.mark.parametrize("family", ["linear", "scalar", "diag", "delta", "gdn"])
+def test_T_is_the_jacobian_of_the_end_state(family):
+    inp = synth.make_inputs(family, 2, 4, 8, [40], torch.float32, seed=9, gla_div=4.0)
+    S, T = run_build(inp)
+    S0 = np.random.default_rng(0).standard_normal((4, 8, 8))
+    with_s0 = run_seq(inp, S0=S0)
+    for h in range(4):
+        np.testing.assert_allclose(with_s0[0, h] - S[0, h], T[0, h] @ S0[h], rtol=1e-11,
+                                   atol=1e-12)
+
+
+# ------------------------------------------------------------------ brute force (exact)
+
+def _exact_affine(k, v, a, b):
+    """Exact rationals: S_t = F_t S_{t-1} + b_t k_t v_t^T with F_t = a_t (I - b_t k_t k_t^T)
+    formed as a dense matrix; T = F_L ... F_1 multiplied out one dense product at a time."""
+    import sympy
+    d = len(k[0])
+    S = sympy.zeros(d, d)
+    T = sympy.eye(d)
+    for kt, vt, at, bt in zip(k, v, a, b):
+        K = sympy.Matrix(kt)
+        F = at * (sympy.eye(d) - bt * K * K.T)
+        S = F * S + bt * K * sympy.Matrix(vt).T
+        T = F * T
+    return S, T
+
+
+def test_bruteforce_exact_rational_gdn():
+    sympy = pytest.importorskip("sympy")
+    rng = np.random.default_rng(11)
+    d, L = 4, 9
+    # dyadic rationals are exact in binary floating point
+    k = rng.integers(-8, 9, size=(L, d)) / 8.0
+    v = rng.integers(-8, 9, size=(L, d)) / 4.0
+    b = rng.integers(1, 9, size=L) / 16.0
+    a = rng.integers(8, 17, size=L) / 16.0
+    S_ex, T_ex = _exact_affine([[Fraction(x) for x in r] for r in k],
+                               [[Fraction(x) for x in r] for r in v],
+                               [Fraction(x) for x in a], [Fraction(x) for x in b])
+    S, T = oracle.build_segments("gdn", [0, L], k[:, None], v[:, None],
+                                 log_gate=np.log(a)[:, None], beta=b[:, None])
+    S_ex = np.array(S_ex.tolist(), dtype=np.float64)
+    T_ex = np.array(T_ex.tolist(), dtype=np.float64)
+    assert relF(S[0, 0], S_ex) < 1e-13
+    assert relF(T[0, 0], T_ex) < 1e-13
+
+
+def test_bruteforce_dense_products_random():
+    for L in (1, 2, 7, 16):
+        inp = synth.make_inputs("gdn", 1, 1, 4, [L], torch.float64, seed=100 + L,
+                                alpha_scale=0.5)
+        S, T = run_build(inp)
+        k, v = f64(inp.k)[:, 0], f64(inp.v)[:, 0]
+        a, b = np.exp(f64(inp.log_gate)[:, 0]), f64(inp.beta)[:, 0]
+        Tb, Sb = np.eye(4), np.zeros((4, 4))
+        for t in range(L):
+            F = a[t] * (np.eye(4) - b[t] * np.outer(k[t], k[t]))
+            Sb = F @ Sb + b[t] * np.outer(k[t], v[t])
+            Tb = F @ Tb
+        assert relF(T[0, 0], Tb) < 1e-13 and relF(S[0, 0], Sb) < 1e-13
+
+
+# ------------------------------------------------------------------ composition theorem
+
+@pytest.mark.parametrize("family", ["linear", "scalar", "diag", "delta", "gdn"])
+def test_composition_equals_sequential(family):
+    inp = synth.make_inputs(family, 2, 4, 16, [70, 1, 0, 129, 64, 33], torch.bfloat16,
+                            seed=20, gla_div=8.0, alpha_scale=0.02)
+    S, T = run_build(inp)
+    pref = oracle.compose_scan(T.reshape(inp.n_seg, 4, 16, 16), S)
+    seq = run_seq(inp)
+    for j in range(inp.n_seg):
+        for h in range(4):
+            if np.linalg.norm(seq[j, h]) == 0:
+                assert np.linalg.norm(pref[j, h]) == 0
+            else:
+                assert relF(pref[j, h], seq[j, h]) < 1e-12
+
+
+def test_compose_scan_with_initial_state_matches_matmul_chain():
+    c = synth.make_compose_inputs("gdn", 5, 3, 8, seed=21, with_S0=True)
+    T = oracle.materialize_T("gdn", c.lam.double().numpy(), c.P.double().numpy())
+    S, S0 = c.S.double().numpy(), c.S0.double().numpy()
+    pref = oracle.compose_scan(T, S, S0)
+    for u in range(3):
+        cur = S0[u]
+        for j in range(5):
+            cur = np.matmul(T[j, u], cur) + S[j, u]
+            assert relF(pref[j, u], cur) < 1e-13
+
+
+def test_composition_is_associative():
+    c = synth.make_compose_inputs("gdn", 3, 1, 6, seed=22)
+    T = oracle.materialize_T("gdn", c.lam.double().numpy(), c.P.double().numpy())[:, 0]
+    S = c.S.double().numpy()[:, 0]
+    # ((3 o 2) o 1) and (3 o (2 o 1)) as pairs (T, S), then applied to zero
+    T32, S32 = T[2] @ T[1], T[2] @ S[1] + S[2]
+    S21 = T[1] @ S[0] + S[1]
+    left = T32 @ S[0] + S32
+    right = T[2] @ S21 + S[2]
+    pref = oracle.compose_scan(T[:, None], S[:, None])[2, 0]
+    assert relF(left, right) < 1e-13 and relF(pref, right) < 1e-13
+
+
+def test_materialize_T_forms():
+    lam = np.array([[-0.5, 0.0]])
+    np.testing.assert_allclose(oracle.materialize_T("scalar", lam, d_k=3)[0, 0],
+                               np.exp(-0.5) * np.eye(3))
+    np.testing.assert_array_equal(oracle.materialize_T("linear", lam, d_k=3)[0, 1], np.eye(3))
+    lv = np.array([[[-1.0, 0.25]]])
+    np.testing.assert_allclose(oracle.materialize_T("diag", lv)[0, 0], np.diag(np.exp([-1, .25])))
+    P = np.arange(4.0).reshape(1, 1, 2, 2)
+    np.testing.assert_allclose(oracle.materialize_T("gdn", np.array([[np.log(2.0)]]), P)[0, 0],
+                               2 * P[0, 0])
+
+
+# ------------------------------------------------------------------ naive addition
+
+def test_naive_add_exact_for_linear_only():
+    inp = synth.make_inputs("linear", 1, 1, 8, [50, 60, 70], torch.float32, seed=30)
+    S, _ = run_build(inp, want_T=False)
+    seq = run_seq(inp)
+    np.testing.assert_allclose(S.sum(0), seq[-1], rtol=1e-12, atol=1e-13)
+
+
+def test_naive_add_fails_for_retnet_by_the_predicted_amount():
+    inp = synth.make_inputs("scalar", 1, 1, 8, [50, 60], torch.float32, seed=31)
+    S, T = run_build(inp)
+    seq = run_seq(inp)
+    g = np.exp(f64(inp.log_gamma)[0])
+    naive = S[0, 0] + S[1, 0]
+    np.testing.assert_allclose(naive - seq[1, 0], (1 - g ** 60) * S[0, 0], rtol=1e-11, atol=1e-13)
+    assert relF(naive, seq[1, 0]) > 1e-2
