@@ -1,0 +1,562 @@
+#!/usr/bin/env python
+"""Benchmark of the HYPIC linear-layer state path on one GB300 (or N replicas).
+
+One step = the whole hot path on the GDN workload: one hybrid linear layer with 32 value /
+16 key heads, d_k = d_v = 128, one 32768-token cold prompt split into 16 segments of 2048
+tokens (bf16 k L2-normalised, bf16 v, fp32 gates and beta), built into all 512
+(S(C|0), T_C) pairs in one launch, then prefix-scan composed across the 16 segments in a
+second launch. `value` is build+compose tokens/s of that step with the inputs resident in
+device memory; `e2e` is the same metric through the public API with the inputs copied in
+from pinned host memory and every output copied back, inside the timed region.
+
+The other workloads (RetNet scalar build + compose, GLA diagonal build + compose, the
+48-layer x 64-segment GDN compose) are measured after the main timed region and reported
+under "sections". `--impl reference` times the fp64 CPU oracle instead (a bounded sample
+of the same workload per step, on the host cores).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hypic|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN (S,T_C) build tokens/s + compose/scan GB/s, % of GB300 roofline"
+UNIT = "tokens/s"
+CHUNK = 64
+L2_FLUSH_BYTES = 256 << 20
+
+# algorithmic work per token per value head of the chunked (C = 64) WY/UT GDN build:
+# gram 2Cd + W 2Cd + U 2Cd + X = W[S|P] 2d(2d) + state update 2d(2d)
+GDN_FLOP_PER_TOKEN_HEAD = 6 * CHUNK * 128 + 8 * 128 * 128   # 180,224
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"),
+                    sm_max_mhz=d.get("sm_max_mhz", 2070.0), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0,
+                sm_max_mhz=2070.0, source="fallback")
+
+
+def fp32_alu_peak_tflops(sm_mhz):
+    """FFMA peak: 152 SMs x 128 fp32 lanes x 2 flop x clock."""
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world > 1 and not torch.distributed.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank: float, max_seconds: float, world: int) -> float:
+    """Whole-job throughput: units processed by all ranks / the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+def src_hash(*names):
+    h = hashlib.sha1()
+    for n in names:
+        with open(os.path.join(ROOT, "linear_attention_state_gdn_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+def recorded_traffic(kernel: str, source_files):
+    """DRAM bytes per launch recorded from an ncu capture of this exact kernel source
+    (profiles/traffic.json); None when absent or when the source changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(kernel)
+    if not rec or rec.get("src") != src_hash(*source_files):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index=0):
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            ident = str(self.dev)
+            try:
+                u = torch.cuda.get_device_properties(self.dev).uuid
+                ident = "GPU-" + str(u)
+            except Exception:
+                pass
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", ident, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"],
+                        samples=0)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, p in zip(names, parts[4:8]):
+                if p.lower().startswith("active"):
+                    reasons.add(n)
+        return dict(sm_mhz=statistics.median(sm) if sm else None,
+                    sm_max_mhz=max(smax) if smax else None, reasons=sorted(reasons),
+                    samples=len(sm))
+
+
+# ----------------------------------------------------------------------------- workloads
+
+def gdn_algorithmic_bytes(n_tok, H_k, H_v, d, n_seg):
+    """Bytes the GDN build must move: k, v (bf16), log a and beta (fp32) in; S and P
+    (fp32) and lam out."""
+    inputs = n_tok * (H_k * d * 2 + H_v * d * 2 + H_v * 8)
+    outputs = n_seg * H_v * (2 * d * d * 4 + 4)
+    return inputs + outputs
+
+
+def compose_algorithmic_bytes(n_seg, units, d, dense, diag=False, s0=False):
+    """Compose scan bytes: read S_j and lam_j (and P_j for j >= 1 when dense), write
+    prefix_j."""
+    st = d * d * 4
+    per_unit = n_seg * (2 * st + (d * 4 if diag else 4))
+    if dense:
+        per_unit += (n_seg - 1 + (1 if s0 else 0)) * st
+    if s0:
+        per_unit += st
+    return per_unit * units
+
+
+class Step:
+    """Device buffers and the two launches of one step of a workload."""
+
+    def __init__(self, inp, device):
+        import linear_attention_state_gdn_gb300 as hy
+        self.hy = hy
+        self.inp = inp
+        self.dev = {n: t.to(device) for n, t in inp.tensors().items()}
+        self.S, self.lam, self.P = hy.build_outputs(inp.family, inp.n_seg, inp.H_v, inp.d_v,
+                                                    device)
+        self.prefix = torch.empty_like(self.S)
+
+    def build(self):
+        d = self.dev
+        self.hy.hypic_build_segments(self.inp.family, d["k"], d["v"], self.inp.seg_offsets,
+                                     log_gate=d.get("log_gate"), log_gamma=d.get("log_gamma"),
+                                     beta=d.get("beta"), S=self.S, lam=self.lam, P=self.P)
+
+    def compose(self):
+        self.hy.hypic_compose_scan(self.inp.family, self.S, self.lam, self.P,
+                                   prefix=self.prefix)
+
+    def kernel_names(self):
+        d = self.dev
+        b = self.hy.hypic_build_kernel_name(self.inp.family, d["k"], d["v"], self.inp.seg_offsets,
+                                            log_gate=d.get("log_gate"),
+                                            log_gamma=d.get("log_gamma"), beta=d.get("beta"),
+                                            S=self.S, lam=self.lam, P=self.P)
+        c = self.hy.hypic_compose_kernel_name(self.inp.family, self.S, self.lam, self.P)
+        return b, c
+
+
+def time_loop(fns, steps, warmup, flush):
+    """Run `steps` iterations of the launches in `fns` after `warmup` untimed ones, with an
+    L2 flush between iterations (outside the events). Returns per-function lists of
+    milliseconds and the per-iteration totals."""
+    for _ in range(warmup):
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in fns] for _ in range(steps)]
+    for it in range(steps):
+        flush.zero_()
+        for (a, b), f in zip(ev[it], fns):
+            a.record()
+            f()
+            b.record()
+    torch.cuda.synchronize()
+    per_fn = [[ev[it][i][0].elapsed_time(ev[it][i][1]) for it in range(steps)]
+              for i in range(len(fns))]
+    totals = [sum(per_fn[i][it] for i in range(len(fns))) for it in range(steps)]
+    return per_fn, totals
+
+
+def build_gdn_compose_cache(layers=48, device="cuda"):
+    """The 48-layer x 32-head x 64-segment GDN cache: every layer drawn on the device and
+    built into unit slice [layer*32, layer*32+32) of one [64, 1536, 128, 128] cache."""
+    import ctypes
+    import linear_attention_state_gdn_gb300 as hy
+    from linear_attention_state_gdn_gb300 import synth
+    info = synth.workload_info("gdn_compose")
+    H, d, n_seg = info["H_v"], info["d"], len(info["seg_lens"])
+    units = layers * H
+    S, lam, P = hy.build_outputs("gdn", n_seg, units, d, device)
+    lib = hy.load_library()
+    stream = torch.cuda.current_stream().cuda_stream
+    for layer in range(layers):
+        inp = synth.make_workload_device("gdn_compose", layer, device)
+        a = hy.make_build_args("gdn", inp.k, inp.v, inp.seg_offsets, inp.log_gate, None,
+                               inp.beta, None, None, None, out_seg_stride=units)
+        a.S = S.data_ptr() + layer * H * d * d * 4
+        a.lam = lam.data_ptr() + layer * H * 4
+        a.P = P.data_ptr() + layer * H * d * d * 4
+        st = lib.hypic_build_segments(ctypes.byref(a), stream)
+        if st != 0:
+            raise hy.HypicError(st, "hypic_build_segments (gdn_compose cache)")
+        del inp
+    torch.cuda.synchronize()
+    return S, lam, P, dict(info, units=units)
+
+
+# ----------------------------------------------------------------------------- sections
+
+def section_family(name, flush, peak, steps=20, warmup=3):
+    from linear_attention_state_gdn_gb300 import synth
+    inp = synth.make_workload(name)
+    st = Step(inp, "cuda")
+    (tb, tc), _ = time_loop([st.build, st.compose], steps, warmup, flush)
+    b_ms, c_ms = statistics.mean(tb), statistics.mean(tc)
+    n_tok, d = inp.n_tok, inp.d_k
+    gate_bytes = n_tok * inp.H_v * (d if inp.family == "diag" else 1) * 4 \
+        if inp.log_gate is not None else 0
+    b_bytes = n_tok * (inp.H_k + inp.H_v) * d * 2 + gate_bytes + \
+        inp.n_seg * inp.H_v * (d * d * 4 + (d * 4 if inp.family == "diag" else 4))
+    c_bytes = compose_algorithmic_bytes(inp.n_seg, inp.H_v, d, False, inp.family == "diag")
+    bk, ck = st.kernel_names()
+    b_gbs, c_gbs = b_bytes / b_ms / 1e6, c_bytes / c_ms / 1e6
+    return {"build_kernel": bk, "build_ms": round(b_ms, 4),
+            "build_tokens_per_s": round(n_tok / b_ms * 1e3, 1),
+            "build_gbs": round(b_gbs, 1), "build_hbm_frac": round(b_gbs / peak["hbm_gbs"], 4),
+            "build_bytes": b_bytes, "compose_kernel": ck, "compose_ms": round(c_ms, 4),
+            "compose_gbs": round(c_gbs, 1), "compose_hbm_frac": round(c_gbs / peak["hbm_gbs"], 4),
+            "compose_bytes": c_bytes}
+
+
+def section_gdn_compose(flush, peak, steps=10, warmup=3, layers=48):
+    import linear_attention_state_gdn_gb300 as hy
+    S, lam, P, info = build_gdn_compose_cache(layers)
+    prefix = torch.empty_like(S)
+    f = lambda: hy.hypic_compose_scan("gdn", S, lam, P, prefix=prefix)
+    (tc,), _ = time_loop([f], steps, warmup, flush)
+    ms = statistics.mean(tc)
+    nbytes = compose_algorithmic_bytes(S.shape[0], S.shape[1], S.shape[2], True)
+    gbs = nbytes / ms / 1e6
+    out = {"compose_kernel": hy.hypic_compose_kernel_name("gdn", S, lam, P),
+           "units": int(S.shape[1]), "n_seg": int(S.shape[0]), "compose_ms": round(ms, 4),
+           "compose_bytes": nbytes, "compose_gbs": round(gbs, 1),
+           "compose_hbm_frac": round(gbs / peak["hbm_gbs"], 4)}
+    del S, lam, P, prefix
+    torch.cuda.empty_cache()
+    return out
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_step_sample(inp, heads, nthreads):
+    """One oracle step on a sample: all segments of the first `heads` value heads
+    (with their key heads): fp64 build of (S, T) plus the fp64 compose scan."""
+    import oracle
+    g = inp.H_v // inp.H_k
+    hk = max(1, math.ceil(heads / g))
+    f = lambda t: None if t is None else t.double().numpy()
+    k = np.ascontiguousarray(f(inp.k)[:, :hk])
+    v = np.ascontiguousarray(f(inp.v)[:, :heads])
+    lg = None if inp.log_gate is None else np.ascontiguousarray(f(inp.log_gate)[:, :heads])
+    b = None if inp.beta is None else np.ascontiguousarray(f(inp.beta)[:, :heads])
+    lgam = None if inp.log_gamma is None else np.ascontiguousarray(f(inp.log_gamma)[:heads])
+    t0 = time.perf_counter()
+    S, T = oracle.build_segments(inp.family, inp.seg_offsets, k, v, lg, lgam, b,
+                                 nthreads=nthreads)
+    oracle.compose_scan(T, S, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp, budget_s=12.0):
+    """The oracle as it stands, on the host cores, on a bounded sample of the workload
+    sized to roughly `budget_s` seconds; reported as tokens/s of the whole workload."""
+    import oracle
+    threads = oracle.default_threads()
+    # calibration: one value head (n_seg units); h heads take about h times as long
+    t1 = max(oracle_step_sample(inp, 1, threads), 1e-3)
+    heads = max(1, min(inp.H_v, int(budget_s / t1)))
+    dt = oracle_step_sample(inp, heads, threads)
+    tok_per_s = inp.n_tok * heads / inp.H_v / dt
+    return {"value": round(tok_per_s, 2), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"fp64 oracle build (S, T) + compose of all {inp.n_seg} segments x "
+                      f"{heads} of {inp.H_v} value heads ({inp.n_tok} tokens each); "
+                      f"tokens/s scaled by {heads}/{inp.H_v}"}
+
+
+def run_reference(args):
+    """--impl reference: the fp64 oracle on the host cores, same metric and workload."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from linear_attention_state_gdn_gb300 import synth
+    inp = synth.make_workload("gdn")
+    threads = oracle.default_threads()
+    t1 = oracle_step_sample(inp, 1, threads)
+    # size each step so that warmup + steps end within ~150 s
+    per_step_budget = 150.0 / max(1, args.steps + args.warmup)
+    heads = max(1, min(inp.H_v, int(per_step_budget / max(t1, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_step_sample(inp, heads, threads)
+    times = [oracle_step_sample(inp, heads, threads) for _ in range(args.steps)]
+    total = sum(times)
+    tok = inp.n_tok * heads / inp.H_v
+    value = tok * args.steps / total
+    sample = (f"fp64 oracle build (S, T) + compose of all {inp.n_seg} segments x {heads} of "
+              f"{inp.H_v} value heads per step; tokens/s scaled by {heads}/{inp.H_v}")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(),
+            "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config():
+    return {"workload": "gdn: one GDN linear layer, 32 value / 16 key heads, d_k=d_v=128, "
+                        "one 32768-token cold prompt as 16 segments x 2048 tokens; bf16 k "
+                        "(L2-normalised) and v, fp32 log-gates and beta, fp32 S and T; "
+                        "build all 512 (S,T) pairs in one launch + 16-segment prefix-scan "
+                        "compose",
+            "tokens_per_step": 32768, "segments": 16, "heads_v": 32, "heads_k": 16, "d": 128,
+            "l2": "inputs (411 MB) exceed L2; 256 MB L2 flush between timed steps",
+            "parallelism": "replicas (one independent workload per GPU)"}
+
+
+# ----------------------------------------------------------------------------- main arm
+
+def e2e_measure(inp, steps=5, warmup=2):
+    """Through the public API from pinned host buffers: H2D of k, v, log a, beta; build;
+    compose; D2H of S, lam, P and the prefix states, all inside the events."""
+    import linear_attention_state_gdn_gb300 as hy
+    host = {n: t.pin_memory() for n, t in inp.tensors().items()}
+    dev = {n: torch.empty_like(t, device="cuda") for n, t in host.items()}
+    S, lam, P = hy.build_outputs(inp.family, inp.n_seg, inp.H_v, inp.d_v, "cuda")
+    prefix = torch.empty_like(S)
+    outs = [S, lam, P, prefix]
+    host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+
+    def one():
+        for n in host:
+            dev[n].copy_(host[n], non_blocking=True)
+        hy.hypic_build_segments(inp.family, dev["k"], dev["v"], inp.seg_offsets,
+                                log_gate=dev.get("log_gate"), log_gamma=dev.get("log_gamma"),
+                                beta=dev.get("beta"), S=S, lam=lam, P=P)
+        hy.hypic_compose_scan(inp.family, S, lam, P, prefix=prefix)
+        for h, d in zip(host_out, outs):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        one()
+        b.record()
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    m = statistics.mean(ms)
+    return {"value": round(inp.n_tok / m * 1e3, 1), "unit": UNIT, "ms_per_step": round(m, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def run_main(args):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    import linear_attention_state_gdn_gb300 as hy
+    from linear_attention_state_gdn_gb300 import synth
+    hy.load_library()
+    pk = peaks()
+    inp = synth.make_workload("gdn")
+    st = Step(inp, "cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    bk, ck = st.kernel_names()
+
+    # warm-up, then exactly K timed steps bracketed by barrier + synchronize
+    for _ in range(args.warmup):
+        st.build()
+        st.compose()
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(2)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for it in range(args.steps):
+        flush.zero_()
+        (b0, b1), (c0, c1) = ev[it]
+        b0.record()
+        st.build()
+        b1.record()
+        c0.record()
+        st.compose()
+        c1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    assert hy.hypic_get_device_status() == 0
+    build_ms = [ev[i][0][0].elapsed_time(ev[i][0][1]) for i in range(args.steps)]
+    comp_ms = [ev[i][1][0].elapsed_time(ev[i][1][1]) for i in range(args.steps)]
+    step_ms = [b + c for b, c in zip(build_ms, comp_ms)]
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world, "cuda")
+    value = aggregate_throughput(inp.n_tok * args.steps, total_s, world)
+    ms_per_step = total_s / args.steps * 1e3
+    b_ms, c_ms = statistics.mean(build_ms), statistics.mean(comp_ms)
+
+    # roofline of the dominant kernel (the build)
+    flops = GDN_FLOP_PER_TOKEN_HEAD * inp.n_tok * inp.H_v
+    nbytes = gdn_algorithmic_bytes(inp.n_tok, inp.H_k, inp.H_v, inp.d_k, inp.n_seg)
+    tensor_path = bk.endswith("_tc")
+    if tensor_path:
+        achieved = flops / (b_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 2), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "peak_source": f"{pk['source']} bf16 dense (burst)"}
+    else:
+        achieved = flops / (b_ms * 1e-3) / 1e12
+        alu = fp32_alu_peak_tflops(pk["sm_max_mhz"])
+        roof = {"bound": "alu", "achieved": round(achieved, 2), "peak": round(alu, 1),
+                "unit": "TFLOP/s",
+                "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 flop x max SM clock"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["kernel"] = bk
+    roof["algorithmic_flop_per_launch"] = flops
+    roof["algorithmic_bytes_per_launch"] = nbytes
+    roof["achieved_gbs"] = round(nbytes / (b_ms * 1e-3) / 1e9, 1)
+    roof["traffic"] = recorded_traffic(bk, ["build_gdn_tc.cu"] if tensor_path else
+                                       ["build_simt.cu"])
+    comp_bytes = compose_algorithmic_bytes(inp.n_seg, inp.H_v, inp.d_k, True)
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if tensor_path else "f32", "data": "synthetic",
+            "config": workload_config(), "roofline": roof,
+            "build_ms": round(b_ms, 4), "compose_ms": round(c_ms, 4),
+            "compose_gbs": round(comp_bytes / (c_ms * 1e-3) / 1e9, 1),
+            "compose_hbm_frac": round(comp_bytes / (c_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+            "kernels": {"build": bk, "compose": ck},
+            "gpu_launches": 2 * args.steps,
+            "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
+            "clock_samples": clocks["samples"], "wall_s_timed_region": round(wall, 3),
+            "peaks": pk}
+
+    if not args.quick:
+        line["e2e"] = e2e_measure(inp)
+        del st
+        torch.cuda.empty_cache()
+        sections = {}
+        for name in ("retnet", "gla"):
+            sections[name] = section_family(name, flush, pk)
+        sections["gdn_compose"] = section_gdn_compose(flush, pk, layers=args.compose_layers)
+        line["sections"] = sections
+        if rank == 0 and world == 1:
+            line["cpu_baseline"] = cpu_baseline(inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["hypic", "reference"], default="hypic")
+    ap.add_argument("--quick", action="store_true",
+                    help="main timed region only (no e2e, sections or CPU baseline)")
+    ap.add_argument("--compose-layers", type=int, default=48)
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_main(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

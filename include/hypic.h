@@ -1,0 +1,198 @@
+/*
+ * hypic.h -- C ABI of the GB300 (sm_103a) library for HYPIC's linear-layer state path.
+ *
+ * Two operations, both from the linear-layer half of HYPIC:
+ *
+ *  hypic_build_segments  prefill every cached prompt segment C of one layer into the pair
+ *                        (S(C|0), T_C): the zero-initial end state and the segment-cumulative
+ *                        transition operator.
+ *                        Source: "Cut First-Token Latency by 3.25x: Introducing HYPIC for
+ *                        Position-Independent Caching in Hybrid-Attention LLMs" (besthub.dev),
+ *                        paragraph "For linear layers" (HYPIC stores the pair (T_C, S(C|0))
+ *                        during the first prefill) and "HYPIC: Cache Acceleration for Hybrid
+ *                        Attention Models" (agihunt.info), "Core Approach", Linear Layers.
+ *
+ *  hypic_compose_scan    chain cached segments algebraically: the inclusive prefix scan
+ *                        prefix_j = T_j . prefix_{j-1} + S_j over n segments, for many
+ *                        (layer, head) units at once.
+ *                        Source: same besthub.dev paragraph (reuse composes
+ *                        T_C2 . S(C1) + S(C2) in O(1) time), the agihunt.info "Core Approach"
+ *                        (states combine in constant time for any prefix) and the besthub.dev
+ *                        paragraph on segment parallelism (a combine worker assembles the
+ *                        final state from the segments' results).
+ *
+ * State convention: per value head the state S is a d_k x d_v fp32 matrix (row = key
+ * channel); T_C is d_k x d_k and acts on the left. Families and their step
+ * (the pages name the families but print no equations; these are the standard forms):
+ *
+ *   HYPIC_FAM_LINEAR  S_t = S_{t-1} + k_t v_t^T                                T_C = I
+ *   HYPIC_FAM_SCALAR  S_t = g_t S_{t-1} + k_t v_t^T   (RetNet, Mamba2)        T_C = (prod g_t) I
+ *   HYPIC_FAM_DIAG    S_t = Diag(g_t) S_{t-1} + k_t v_t^T   (GLA)             T_C = Diag(prod g_t)
+ *   HYPIC_FAM_DELTA   S_t = (I - b_t k_t k_t^T) S_{t-1} + b_t k_t v_t^T       T_C = prod (I - b k k^T)
+ *   HYPIC_FAM_GDN     S_t = a_t (I - b_t k_t k_t^T) S_{t-1} + b_t k_t v_t^T   T_C = prod a_t (I - b k k^T)
+ *
+ * with products ordered latest step leftmost (GDN: "Gated Delta Networks: Improving Mamba2
+ * with Delta Rule", reference 7 of the episode-companion page "Hypic: Position-Independent
+ * KV Caching for Hybrid-Attention LLM Serving").
+ *
+ * Log-scaled transition storage. The gates of long segments drive T_C below the fp32
+ * range (a 2048-token GDN segment with log a ~ -0.04 per token has |T_C| ~ 1e-36), so
+ * T_C is stored as T_C = exp(lam) . P:
+ *   LINEAR           lam = 0 (written), no P
+ *   SCALAR           lam = sum_t log g_t                        [seg][head]
+ *   DIAG             lam = sum_t log g_t (per key channel)      [seg][head][d_k]
+ *   DELTA / GDN      lam = sum_t log a_t (0 for DELTA)          [seg][head]
+ *                    P = prod_t (I - b_t k_t k_t^T), gate-free  [seg][head][d_k][d_k] fp32
+ *
+ * Conventions shared by every call:
+ *   - Ownership: the caller allocates and owns every buffer. The library allocates no
+ *     memory on any call; it keeps per-device state of its own (a 4-byte status word per
+ *     device that has run a kernel).
+ *   - Memory: tensors are device pointers (cudaMalloc / torch CUDA tensors), row-major
+ *     and contiguous; seg_offsets is a HOST array. Every tensor pointer must be 16-byte
+ *     aligned (HYPIC_ERR_ALIGNMENT otherwise), except the fp32 gate / beta arrays
+ *     (4-byte).
+ *   - Asynchrony: calls enqueue work on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and return without synchronising. Outputs may not alias inputs.
+ *   - Errors: argument problems are detected on the host before anything is launched and
+ *     returned as a status; nothing is written then. Faults the host cannot see (a wait
+ *     that exceeded its iteration limit, a gate that leaves the supported range) are
+ *     recorded in the device status word; hypic_get_device_status() reads and clears it.
+ *   - Shapes: d_k == d_v, one of 32, 64, 128; H_v a multiple of H_k (grouped-query keys:
+ *     value head h reads key head h / (H_v / H_k)); at most HYPIC_MAX_SEGMENTS segments.
+ */
+#ifndef HYPIC_H
+#define HYPIC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HYPIC_MAX_SEGMENTS 1024
+
+typedef enum {
+    HYPIC_OK = 0,
+    HYPIC_ERR_INVALID_ARG = 1,  /* NULL / missing tensor, bad count or offsets, host pointer */
+    HYPIC_ERR_ALIGNMENT = 2,    /* a tensor pointer is not 16-byte (gates: 4-byte) aligned  */
+    HYPIC_ERR_UNSUPPORTED = 3,  /* valid request outside what is built (head size, dtype)   */
+    HYPIC_ERR_RANGE = 4,        /* a gate outside the supported range (device-detected)     */
+    HYPIC_ERR_CUDA = 5,         /* a CUDA runtime call failed (launch, attribute query)     */
+    HYPIC_ERR_TIMEOUT = 6       /* a kernel wait ran out of its iteration limit             */
+} hypic_status;
+
+typedef enum {
+    HYPIC_FAM_LINEAR = 0,
+    HYPIC_FAM_SCALAR = 1,
+    HYPIC_FAM_DIAG = 2,
+    HYPIC_FAM_DELTA = 3,
+    HYPIC_FAM_GDN = 4
+} hypic_family;
+
+typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
+
+/* Arguments of hypic_build_segments (one linear layer).
+ *
+ *   family, dtype     hypic_family, hypic_dtype of k and v (gates and beta are fp32)
+ *   n_seg             number of segments, 0 <= n_seg <= HYPIC_MAX_SEGMENTS (0: no-op)
+ *   H_k, H_v          key heads, value heads (H_v % H_k == 0)
+ *   d_k, d_v          head sizes (equal; 32, 64 or 128)
+ *   seg_offsets       HOST int64 [n_seg + 1]: 0 = o_0 <= o_1 <= ... <= o_n = N_tok; segment
+ *                     j is tokens [o_j, o_{j+1}); empty segments give S = 0, T = I
+ *   out_seg_stride    units between consecutive segments in S / lam / P, 0 = H_v (lets a
+ *                     caller write layer l of a multi-layer cache at unit offset l * H_v)
+ *   k                 [N_tok][H_k][d_k]  dtype
+ *   v                 [N_tok][H_v][d_v]  dtype
+ *   log_gate          SCALAR: [N_tok][H_v] log g_t (or NULL when log_gamma is given);
+ *                     DIAG: [N_tok][H_v][d_k] log g_t; GDN: [N_tok][H_v] log a_t;
+ *                     LINEAR, DELTA: NULL
+ *   log_gamma         SCALAR with a constant per-head decay: [H_v] log gamma_h; else NULL
+ *   beta              DELTA, GDN: [N_tok][H_v] b_t; else NULL
+ *   S                 out [n_seg][H_v][d_k][d_v] fp32 (segment stride out_seg_stride units)
+ *   lam               out [n_seg][H_v] fp32, DIAG [n_seg][H_v][d_k]
+ *   P                 out DELTA / GDN: [n_seg][H_v][d_k][d_k] fp32; else NULL
+ *   workspace         device scratch of hypic_build_workspace_bytes() bytes (NULL if 0)
+ */
+typedef struct {
+    int32_t family;
+    int32_t dtype;
+    int32_t n_seg;
+    int32_t H_k;
+    int32_t H_v;
+    int32_t d_k;
+    int32_t d_v;
+    int32_t reserved0;
+    int64_t out_seg_stride;
+    const int64_t *seg_offsets;
+    const void *k;
+    const void *v;
+    const float *log_gate;
+    const float *log_gamma;
+    const float *beta;
+    float *S;
+    float *lam;
+    float *P;
+    void *workspace;
+    size_t workspace_bytes;
+} hypic_build_args;
+
+/* Arguments of hypic_compose_scan.
+ *
+ *   family       hypic_family of the cached entries
+ *   n_seg        segments to chain, in order (0: no-op)
+ *   n_units      independent (layer, head) units scanned side by side
+ *   d_k, d_v     head sizes (equal; 32, 64 or 128)
+ *   S            [n_seg][n_units][d_k][d_v] fp32: S(C_j|0) of every segment
+ *   lam          [n_seg][n_units] fp32 (DIAG: [n_seg][n_units][d_k]); NULL for LINEAR
+ *   P            DELTA / GDN: [n_seg][n_units][d_k][d_k] fp32; else NULL
+ *   S0           optional initial state [n_units][d_k][d_v] fp32; NULL = zero state
+ *   prefix       out [n_seg][n_units][d_k][d_v] fp32: prefix[j] = state after segments
+ *                0..j, i.e. exp(lam_j) P_j prefix[j-1] + S_j with prefix[-1] = S0
+ */
+typedef struct {
+    int32_t family;
+    int32_t n_seg;
+    int64_t n_units;
+    int32_t d_k;
+    int32_t d_v;
+    const float *S;
+    const float *lam;
+    const float *P;
+    const float *S0;
+    float *prefix;
+} hypic_compose_args;
+
+/* Build (S(C|0), T_C) for every segment and value head of one layer in one launch.
+ * Segments run in parallel, longest first. Returns HYPIC_OK once the work is enqueued. */
+hypic_status hypic_build_segments(const hypic_build_args *args, void *stream);
+
+/* Inclusive prefix scan of the composition over n_seg segments for n_units units. */
+hypic_status hypic_compose_scan(const hypic_compose_args *args, void *stream);
+
+/* Device scratch bytes hypic_build_segments needs for these arguments (host-only query;
+ * reads the shapes and seg_offsets, never the tensors). 0 means no workspace. */
+size_t hypic_build_workspace_bytes(const hypic_build_args *args);
+
+/* Name of the kernel hypic_build_segments / hypic_compose_scan would launch for these
+ * arguments (host-only query, no device access; "none" for an empty request, NULL for
+ * arguments the call would reject on shape or family). Static strings. */
+const char *hypic_build_kernel_name(const hypic_build_args *args);
+const char *hypic_compose_kernel_name(const hypic_compose_args *args);
+
+/* Synchronise `stream`, then read and clear the current device's status word: HYPIC_OK,
+ * HYPIC_ERR_TIMEOUT or HYPIC_ERR_RANGE; HYPIC_ERR_CUDA if the synchronisation failed. */
+hypic_status hypic_get_device_status(void *stream);
+
+/* Static, NUL-terminated description of a status code. */
+const char *hypic_status_string(hypic_status status);
+
+/* Library ABI version (incremented on any change to the structs above). */
+int32_t hypic_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HYPIC_H */

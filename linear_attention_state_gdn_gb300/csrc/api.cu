@@ -1,0 +1,305 @@
+// api.cu -- the C ABI of libhypic (include/hypic.h): argument validation on the host,
+// launch-table construction (segments in longest-first order) and kernel dispatch.
+//
+// Nothing here allocates device memory. The only device state the library keeps is one
+// 4-byte status word per device (a file-scope __device__ variable), which kernels set
+// when a bounded wait runs out or a gate leaves the supported range.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.cuh"
+
+using namespace hypic;
+
+namespace {
+
+__device__ unsigned g_status_word;
+
+constexpr int kMaxDevices = 64;
+unsigned *g_status_addr[kMaxDevices];
+std::mutex g_status_mu;
+
+// Device address of this device's status word. Host code may not use &g_status_word
+// (it names the host-side shadow), so the address is looked up once per device with
+// that device current.
+unsigned *status_word(int *dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (dev_out) *dev_out = dev;
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (!g_status_addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_status_word) != cudaSuccess) return nullptr;
+        g_status_addr[dev] = static_cast<unsigned *>(ptr);
+    }
+    return g_status_addr[dev];
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// True if p is memory the current device can read with plain loads (device or managed).
+bool on_device(const void *p) {
+    if (!p) return false;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (at.type == cudaMemoryTypeManaged) return true;
+    return at.type == cudaMemoryTypeDevice && at.device == dev;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const char *pa = static_cast<const char *>(a), *pb = static_cast<const char *>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+bool head_size_ok(int d_k, int d_v) {
+    return d_k == d_v && (d_k == 32 || d_k == 64 || d_k == 128);
+}
+
+hypic_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA; }
+
+enum class BuildPath { None, GatedSimt, DeltaSeq };
+enum class ComposePath { None, Scaled, DenseSimt };
+
+// Kernel selection for a build (shape/family/dtype only; no pointer checks).
+BuildPath pick_build(const hypic_build_args *a) {
+    if (a->n_seg == 0) return BuildPath::None;
+    const bool delta = a->family == HYPIC_FAM_DELTA || a->family == HYPIC_FAM_GDN;
+    return delta ? BuildPath::DeltaSeq : BuildPath::GatedSimt;
+}
+
+ComposePath pick_compose(const hypic_compose_args *a) {
+    if (a->n_seg == 0 || a->n_units == 0) return ComposePath::None;
+    const bool dense = a->family == HYPIC_FAM_DELTA || a->family == HYPIC_FAM_GDN;
+    return dense ? ComposePath::DenseSimt : ComposePath::Scaled;
+}
+
+bool build_shape_ok(const hypic_build_args *a) {
+    return a && a->family >= HYPIC_FAM_LINEAR && a->family <= HYPIC_FAM_GDN &&
+           (a->dtype == HYPIC_BF16 || a->dtype == HYPIC_F32) && a->n_seg >= 0 &&
+           a->n_seg <= HYPIC_MAX_SEGMENTS && a->H_k > 0 && a->H_v > 0 && a->H_v % a->H_k == 0 &&
+           head_size_ok(a->d_k, a->d_v);
+}
+
+bool compose_shape_ok(const hypic_compose_args *a) {
+    return a && a->family >= HYPIC_FAM_LINEAR && a->family <= HYPIC_FAM_GDN && a->n_seg >= 0 &&
+           a->n_units >= 0 && head_size_ok(a->d_k, a->d_v);
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t hypic_abi_version(void) { return 1; }
+
+const char *hypic_status_string(hypic_status s) {
+    switch (s) {
+    case HYPIC_OK: return "ok";
+    case HYPIC_ERR_INVALID_ARG: return "invalid argument";
+    case HYPIC_ERR_ALIGNMENT: return "misaligned tensor pointer";
+    case HYPIC_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case HYPIC_ERR_RANGE: return "gate outside the supported range";
+    case HYPIC_ERR_CUDA: return "CUDA runtime error";
+    case HYPIC_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+size_t hypic_build_workspace_bytes(const hypic_build_args *a) {
+    (void)a;
+    return 0;
+}
+
+hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
+    if (!a) return HYPIC_ERR_INVALID_ARG;
+    const int fam = a->family;
+    if (fam < HYPIC_FAM_LINEAR || fam > HYPIC_FAM_GDN) return HYPIC_ERR_INVALID_ARG;
+    if (a->dtype != HYPIC_BF16 && a->dtype != HYPIC_F32) return HYPIC_ERR_INVALID_ARG;
+    if (a->n_seg < 0 || a->n_seg > HYPIC_MAX_SEGMENTS) return HYPIC_ERR_INVALID_ARG;
+    if (a->H_k <= 0 || a->H_v <= 0 || a->H_v % a->H_k != 0) return HYPIC_ERR_INVALID_ARG;
+    if (a->d_k <= 0 || a->d_v <= 0) return HYPIC_ERR_INVALID_ARG;
+    if (!head_size_ok(a->d_k, a->d_v)) return HYPIC_ERR_UNSUPPORTED;
+    if (a->out_seg_stride < 0 || (a->out_seg_stride != 0 && a->out_seg_stride < a->H_v))
+        return HYPIC_ERR_INVALID_ARG;
+    if (a->n_seg == 0) return HYPIC_OK;
+    if (!a->seg_offsets || a->seg_offsets[0] != 0) return HYPIC_ERR_INVALID_ARG;
+    int max_len = 0;
+    for (int j = 0; j < a->n_seg; ++j) {
+        const int64_t len = a->seg_offsets[j + 1] - a->seg_offsets[j];
+        if (len < 0) return HYPIC_ERR_INVALID_ARG;
+        max_len = (int)std::min<int64_t>(std::max<int64_t>(max_len, len), INT32_MAX);
+    }
+    const int64_t n_tok = a->seg_offsets[a->n_seg];
+    if (n_tok > INT32_MAX) return HYPIC_ERR_UNSUPPORTED;
+
+    // required / forbidden tensors per family
+    const bool delta = fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GDN;
+    const bool need_gate = fam == HYPIC_FAM_DIAG || fam == HYPIC_FAM_GDN;
+    if (!a->S || !a->lam) return HYPIC_ERR_INVALID_ARG;
+    if (delta && (!a->P || !a->beta)) return HYPIC_ERR_INVALID_ARG;
+    if (need_gate && !a->log_gate) return HYPIC_ERR_INVALID_ARG;
+    if (fam == HYPIC_FAM_SCALAR && (!a->log_gate) == (!a->log_gamma)) return HYPIC_ERR_INVALID_ARG;
+    if (n_tok > 0 && (!a->k || !a->v)) return HYPIC_ERR_INVALID_ARG;
+
+    // alignment (16 B for tensors read or written with vector / bulk accesses)
+    const void *v16[] = {a->k, a->v, a->S, a->P};
+    for (const void *p : v16)
+        if (p && !aligned(p, 16)) return HYPIC_ERR_ALIGNMENT;
+    const void *v4[] = {a->log_gate, a->log_gamma, a->beta, a->lam};
+    for (const void *p : v4)
+        if (p && !aligned(p, 4)) return HYPIC_ERR_ALIGNMENT;
+
+    // every tensor the kernels touch must be device memory of the current device
+    const void *dev_ptrs[] = {a->S, a->lam, a->P, a->log_gamma};
+    for (const void *p : dev_ptrs)
+        if (p && !on_device(p)) return HYPIC_ERR_INVALID_ARG;
+    if (n_tok > 0) {
+        const void *in_ptrs[] = {a->k, a->v, a->log_gate, a->beta};
+        for (const void *p : in_ptrs)
+            if (p && !on_device(p)) return HYPIC_ERR_INVALID_ARG;
+    }
+    if (hypic_build_workspace_bytes(a) > a->workspace_bytes) return HYPIC_ERR_INVALID_ARG;
+
+    unsigned *err = status_word(nullptr);
+    if (!err) return HYPIC_ERR_CUDA;
+
+    static thread_local BuildParams p;   // ~12 KB: kept off the stack
+    std::memset(&p, 0, sizeof(p));
+    p.family = fam;
+    p.dtype = a->dtype;
+    p.n_seg = a->n_seg;
+    p.H_k = a->H_k;
+    p.H_v = a->H_v;
+    p.D = a->d_k;
+    p.gqa = a->H_v / a->H_k;
+    p.max_len = max_len;
+    p.seg_stride = a->out_seg_stride ? a->out_seg_stride : a->H_v;
+    p.k = a->k;
+    p.v = a->v;
+    p.log_gate = a->log_gate;
+    p.log_gamma = a->log_gamma;
+    p.beta = a->beta;
+    p.S = a->S;
+    p.lam = a->lam;
+    p.P = a->P;
+    p.workspace = a->workspace;
+    p.err = err;
+    std::vector<int> order(a->n_seg);
+    for (int j = 0; j < a->n_seg; ++j) order[j] = j;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+        return a->seg_offsets[x + 1] - a->seg_offsets[x] > a->seg_offsets[y + 1] - a->seg_offsets[y];
+    });
+    for (int r = 0; r < a->n_seg; ++r) {
+        const int j = order[r];
+        p.seg[r].start = (int32_t)a->seg_offsets[j];
+        p.seg[r].len = (int32_t)(a->seg_offsets[j + 1] - a->seg_offsets[j]);
+        p.seg[r].idx = j;
+    }
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (pick_build(a)) {
+    case BuildPath::DeltaSeq: return from_cuda(launch_build_delta_seq(p, s));
+    case BuildPath::GatedSimt: return from_cuda(launch_build_gated_simt(p, s));
+    case BuildPath::None: break;
+    }
+    return HYPIC_OK;
+}
+
+hypic_status hypic_compose_scan(const hypic_compose_args *a, void *stream) {
+    if (!a) return HYPIC_ERR_INVALID_ARG;
+    const int fam = a->family;
+    if (fam < HYPIC_FAM_LINEAR || fam > HYPIC_FAM_GDN) return HYPIC_ERR_INVALID_ARG;
+    if (a->n_seg < 0 || a->n_units < 0) return HYPIC_ERR_INVALID_ARG;
+    if (a->d_k <= 0 || a->d_v <= 0) return HYPIC_ERR_INVALID_ARG;
+    if (!head_size_ok(a->d_k, a->d_v)) return HYPIC_ERR_UNSUPPORTED;
+    if (a->n_seg == 0 || a->n_units == 0) return HYPIC_OK;
+    if (a->n_units > (int64_t)INT32_MAX / 16) return HYPIC_ERR_UNSUPPORTED;
+    const bool dense = fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GDN;
+    if (!a->S || !a->prefix) return HYPIC_ERR_INVALID_ARG;
+    if (fam != HYPIC_FAM_LINEAR && !a->lam) return HYPIC_ERR_INVALID_ARG;
+    if (dense && !a->P) return HYPIC_ERR_INVALID_ARG;
+    const void *v16[] = {a->S, a->P, a->S0, a->prefix};
+    for (const void *p : v16)
+        if (p && !aligned(p, 16)) return HYPIC_ERR_ALIGNMENT;
+    if (a->lam && !aligned(a->lam, 4)) return HYPIC_ERR_ALIGNMENT;
+    const void *dev_ptrs[] = {a->S, a->P, a->S0, a->prefix, fam == HYPIC_FAM_LINEAR ? nullptr : a->lam};
+    for (const void *p : dev_ptrs)
+        if (p && !on_device(p)) return HYPIC_ERR_INVALID_ARG;
+
+    const size_t D = (size_t)a->d_k;
+    const size_t state_bytes = (size_t)a->n_seg * a->n_units * D * D * sizeof(float);
+    const size_t lam_bytes = (size_t)a->n_seg * a->n_units * (fam == HYPIC_FAM_DIAG ? D : 1) * 4;
+    if (overlaps(a->prefix, state_bytes, a->S, state_bytes) ||
+        overlaps(a->prefix, state_bytes, a->P, dense ? state_bytes : 0) ||
+        overlaps(a->prefix, state_bytes, a->lam, lam_bytes) ||
+        overlaps(a->prefix, state_bytes, a->S0, (size_t)a->n_units * D * D * 4))
+        return HYPIC_ERR_INVALID_ARG;
+
+    unsigned *err = status_word(nullptr);
+    if (!err) return HYPIC_ERR_CUDA;
+    ComposeParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.family = fam;
+    p.n_seg = a->n_seg;
+    p.n_units = a->n_units;
+    p.D = a->d_k;
+    p.S = a->S;
+    p.lam = a->lam;
+    p.P = a->P;
+    p.S0 = a->S0;
+    p.prefix = a->prefix;
+    p.err = err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    switch (pick_compose(a)) {
+    case ComposePath::DenseSimt: return from_cuda(launch_compose_dense_simt(p, s));
+    case ComposePath::Scaled: return from_cuda(launch_compose_scaled(p, s));
+    case ComposePath::None: break;
+    }
+    return HYPIC_OK;
+}
+
+const char *hypic_build_kernel_name(const hypic_build_args *a) {
+    if (!build_shape_ok(a)) return nullptr;
+    switch (pick_build(a)) {
+    case BuildPath::DeltaSeq: return "build_delta_seq";
+    case BuildPath::GatedSimt: return "build_gated_simt";
+    case BuildPath::None: break;
+    }
+    return "none";
+}
+
+const char *hypic_compose_kernel_name(const hypic_compose_args *a) {
+    if (!compose_shape_ok(a)) return nullptr;
+    switch (pick_compose(a)) {
+    case ComposePath::DenseSimt: return "compose_dense_simt";
+    case ComposePath::Scaled: return "compose_scaled";
+    case ComposePath::None: break;
+    }
+    return "none";
+}
+
+hypic_status hypic_get_device_status(void *stream) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return HYPIC_ERR_CUDA;
+    unsigned *w = status_word(nullptr);
+    if (!w) return HYPIC_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return HYPIC_ERR_CUDA;
+    if (v) {
+        const unsigned zero = 0;
+        if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return HYPIC_ERR_CUDA;
+    }
+    if (v & kErrTimeout) return HYPIC_ERR_TIMEOUT;
+    if (v & kErrRange) return HYPIC_ERR_RANGE;
+    return HYPIC_OK;
+}
+
+}  // extern "C"

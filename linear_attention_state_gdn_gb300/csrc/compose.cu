@@ -1,0 +1,180 @@
+// compose.cu -- prefix scan of the composition prefix_j = T_j prefix_{j-1} + S_j over the
+// cached segments of many (layer, head) units ("Cut First-Token Latency by 3.25x:
+// Introducing HYPIC ..." (besthub.dev), paragraph "For linear layers": reuse composes
+// T_C2 . S(C1) + S(C2); paragraph on segment parallelism: the combine worker assembles the
+// final state).
+//
+// compose_scaled: scalar and diagonal transitions, T_j = exp(lam_j) (per unit or per row).
+//   A pure element-wise stream: each thread carries 4 consecutive state elements of one
+//   unit through all segments, with the next segments' S loads issued ahead.
+// compose_dense_simt: dense transitions T_j = exp(lam_j) P_j on CUDA cores, used for head
+//   sizes below 128 (the d = 128 case runs on the tensor cores, compose_tc.cu).
+#include "internal.cuh"
+
+namespace hypic {
+namespace {
+
+constexpr int kScaledThreads = 256;
+constexpr int kAhead = 4;
+
+__device__ __forceinline__ float4 ldg_stream(const float *p) {
+    float4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void stg_stream(float *p, float4 v) {
+    asm volatile("st.global.cs.v4.f32 [%0], {%1,%2,%3,%4};" ::"l"(p), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kScaledThreads)
+compose_scaled_kernel(const __grid_constant__ ComposeParams p) {
+    const int D = p.D;
+    const int n4 = D * D / 4;
+    const int bpu = (n4 + kScaledThreads - 1) / kScaledThreads;   // blocks per unit
+    const int64_t u = blockIdx.x / bpu;
+    const int e4 = (blockIdx.x % bpu) * kScaledThreads + threadIdx.x;
+    if (e4 >= n4) return;
+    const int row = (e4 * 4) / D;
+    const int64_t DD = (int64_t)D * D;
+    const bool diag = p.family == HYPIC_FAM_DIAG;
+    const bool has_lam = p.family != HYPIC_FAM_LINEAR && p.lam != nullptr;
+
+    float4 cur = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.S0) cur = ldg_stream(p.S0 + u * DD + e4 * 4);
+
+    float4 ring[kAhead];
+#pragma unroll
+    for (int a = 0; a < kAhead; ++a)
+        if (a < p.n_seg) ring[a] = ldg_stream(p.S + ((int64_t)a * p.n_units + u) * DD + e4 * 4);
+
+    for (int j0 = 0; j0 < p.n_seg; j0 += kAhead) {
+#pragma unroll
+        for (int a = 0; a < kAhead; ++a) {
+            const int j = j0 + a;
+            if (j < p.n_seg) {
+                const float4 x = ring[a];
+                const int jn = j + kAhead;
+                if (jn < p.n_seg) ring[a] = ldg_stream(p.S + ((int64_t)jn * p.n_units + u) * DD + e4 * 4);
+                float sc = 1.f;
+                if (has_lam) sc = expf(diag ? p.lam[((int64_t)j * p.n_units + u) * D + row]
+                                            : p.lam[(int64_t)j * p.n_units + u]);
+                cur.x = fmaf(sc, cur.x, x.x);
+                cur.y = fmaf(sc, cur.y, x.y);
+                cur.z = fmaf(sc, cur.z, x.z);
+                cur.w = fmaf(sc, cur.w, x.w);
+                stg_stream(p.prefix + ((int64_t)j * p.n_units + u) * DD + e4 * 4, cur);
+            }
+        }
+    }
+}
+
+constexpr int kDenseThreads = 256;
+constexpr int kDenseCols = 32;
+
+// One CTA per (unit, block of 32 state columns). The column block X of prefix_{j-1} stays
+// in shared memory; P_j is staged whole; each thread forms RPT x 4 outputs.
+template <int D>
+__global__ void __launch_bounds__(kDenseThreads)
+compose_dense_simt_kernel(const __grid_constant__ ComposeParams p) {
+    constexpr int LDA = D + 4;
+    constexpr int RPT = D * kDenseCols / kDenseThreads / 4;   // rows per thread
+    extern __shared__ __align__(16) float smem[];
+    float *A = smem;                   // [D][LDA]
+    float *X = smem + D * LDA;         // [D][kDenseCols]
+
+    const int64_t u = blockIdx.x / (D / kDenseCols);
+    const int cb = (blockIdx.x % (D / kDenseCols)) * kDenseCols;
+    const int tid = threadIdx.x;
+    const int tx = tid % (kDenseCols / 4);   // 4-column group
+    const int ty = tid / (kDenseCols / 4);   // row group
+    const int64_t DD = (int64_t)D * D;
+
+    bool have_state = p.S0 != nullptr;
+    if (have_state)
+        for (int e = tid; e < D * kDenseCols; e += kDenseThreads)
+            X[e] = p.S0[u * DD + (int64_t)(e / kDenseCols) * D + cb + e % kDenseCols];
+
+    for (int j = 0; j < p.n_seg; ++j) {
+        const int64_t base = ((int64_t)j * p.n_units + u) * DD;
+        float acc[RPT][4];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
+        if (have_state) {
+            __syncthreads();
+            for (int e = tid; e < D * D / 4; e += kDenseThreads) {
+                const int r = (e * 4) / D, c = (e * 4) % D;
+                const float4 a = *reinterpret_cast<const float4 *>(p.P + base + (int64_t)r * D + c);
+                *reinterpret_cast<float4 *>(&A[r * LDA + c]) = a;
+            }
+            __syncthreads();
+#pragma unroll 4
+            for (int m = 0; m < D; ++m) {
+                const float4 x = *reinterpret_cast<const float4 *>(&X[m * kDenseCols + tx * 4]);
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const float a = A[(ty * RPT + r) * LDA + m];
+                    acc[r][0] = fmaf(a, x.x, acc[r][0]);
+                    acc[r][1] = fmaf(a, x.y, acc[r][1]);
+                    acc[r][2] = fmaf(a, x.z, acc[r][2]);
+                    acc[r][3] = fmaf(a, x.w, acc[r][3]);
+                }
+            }
+        }
+        const float sc = have_state ? expf(p.lam[(int64_t)j * p.n_units + u]) : 0.f;
+        __syncthreads();   // every thread is done reading X
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int row = ty * RPT + r;
+            const int64_t off = base + (int64_t)row * D + cb + tx * 4;
+            const float4 s = *reinterpret_cast<const float4 *>(p.S + off);
+            float4 o;
+            o.x = fmaf(sc, acc[r][0], s.x);
+            o.y = fmaf(sc, acc[r][1], s.y);
+            o.z = fmaf(sc, acc[r][2], s.z);
+            o.w = fmaf(sc, acc[r][3], s.w);
+            *reinterpret_cast<float4 *>(p.prefix + off) = o;
+            *reinterpret_cast<float4 *>(&X[row * kDenseCols + tx * 4]) = o;
+        }
+        have_state = true;
+    }
+}
+
+template <int D>
+cudaError_t launch_dense(const ComposeParams &p, cudaStream_t s) {
+    const size_t smem = sizeof(float) * (D * (D + 4) + D * kDenseCols);
+    cudaError_t e = cudaFuncSetAttribute(compose_dense_simt_kernel<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)(p.n_units * (D / kDenseCols)));
+    compose_dense_simt_kernel<D><<<grid, kDenseThreads, smem, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_compose_scaled(const ComposeParams &p, cudaStream_t s) {
+    if (p.n_seg == 0 || p.n_units == 0) return cudaSuccess;
+    const int n4 = p.D * p.D / 4;
+    dim3 grid((unsigned)(p.n_units * ((n4 + kScaledThreads - 1) / kScaledThreads)));
+    compose_scaled_kernel<<<grid, kScaledThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_compose_dense_simt(const ComposeParams &p, cudaStream_t s) {
+    if (p.n_seg == 0 || p.n_units == 0) return cudaSuccess;
+    switch (p.D) {
+    case 32: return launch_dense<32>(p, s);
+    case 64: return launch_dense<64>(p, s);
+    case 128: return launch_dense<128>(p, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace hypic

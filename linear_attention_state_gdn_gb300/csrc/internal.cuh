@@ -1,0 +1,79 @@
+// internal.cuh -- launch parameter blocks and launcher prototypes shared by the
+// translation units of libhypic (not part of the public ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/hypic.h"
+
+namespace hypic {
+
+// Device status word bits (set by kernels, read by hypic_get_device_status).
+enum : unsigned { kErrTimeout = 1u, kErrRange = 2u };
+
+// One segment of the launch table. The table is ordered longest first (LPT order:
+// "Hypic: Position-Independent KV Caching ..." episode companion, "Segment parallelism:
+// LPT scheduling across workers"); idx is the segment's position in the caller's order.
+struct SegEntry {
+    int32_t start;
+    int32_t len;
+    int32_t idx;
+};
+
+struct BuildParams {
+    int32_t family;
+    int32_t dtype;
+    int32_t n_seg;
+    int32_t H_k;
+    int32_t H_v;
+    int32_t D;          // d_k == d_v
+    int32_t gqa;        // H_v / H_k
+    int32_t max_len;    // longest segment
+    int64_t seg_stride; // output units between segments
+    const void *k;
+    const void *v;
+    const float *log_gate;
+    const float *log_gamma;
+    const float *beta;
+    float *S;
+    float *lam;
+    float *P;
+    void *workspace;
+    unsigned *err;
+    SegEntry seg[HYPIC_MAX_SEGMENTS];
+};
+
+struct ComposeParams {
+    int32_t family;
+    int32_t n_seg;
+    int64_t n_units;
+    int32_t D;
+    int32_t pad;
+    const float *S;
+    const float *lam;
+    const float *P;
+    const float *S0;
+    float *prefix;
+    unsigned *err;
+};
+
+// Launchers (return the launch's cudaError_t).
+cudaError_t launch_build_gated_simt(const BuildParams &p, cudaStream_t s);
+cudaError_t launch_build_delta_seq(const BuildParams &p, cudaStream_t s);
+cudaError_t launch_compose_scaled(const ComposeParams &p, cudaStream_t s);
+cudaError_t launch_compose_dense_simt(const ComposeParams &p, cudaStream_t s);
+
+// fp32 view of one input element (bf16 or fp32 storage).
+__device__ __forceinline__ float load_in(const void *base, int64_t idx, int dtype) {
+    if (dtype == HYPIC_BF16)
+        return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(base)[idx]);
+    return reinterpret_cast<const float *>(base)[idx];
+}
+
+__device__ __forceinline__ void raise_error(unsigned *err, unsigned bit) {
+    if (err) atomicOr(err, bit);
+}
+
+}  // namespace hypic

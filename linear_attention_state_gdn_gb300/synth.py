@@ -249,3 +249,50 @@ def make_compose_inputs(family: str, n_seg: int, n_units: int, d: int, seed: int
     S0 = _normal(rng, (n_units, d, d)) if with_S0 else None
     t = lambda x: None if x is None else torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
     return ComposeInputs(family, n_seg, n_units, d, d, t(lam), t(S), t(P), t(S0))
+
+
+# --------------------------------------------------------------------------------------
+# Device-side draws for the 48-layer workload (host draws of ~12 G values would take
+# minutes). torch's seeded generator on the target device draws the same recipe; a test
+# that checks a sample on the host copies the drawn tensors back, so both sides still see
+# identical bytes.
+
+def make_inputs_device(family: str, H_k: int, H_v: int, d: int, seg_lens, dtype, seed: int,
+                       device="cuda", alpha_scale: float = 0.05) -> SegmentInputs:
+    """GDN / DELTA inputs drawn with torch.Generator(device) (recipe as make_inputs)."""
+    assert family in ("gdn", "delta")
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    offs = offsets_from_lengths(seg_lens)
+    N = int(offs[-1])
+    k = torch.randn((N, H_k, d), generator=g, device=device, dtype=torch.float32)
+    k = k / k.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+    v = torch.randn((N, H_v, d), generator=g, device=device, dtype=torch.float32)
+    inp = SegmentInputs(family, dtype, H_k, H_v, d, d, offs, k.to(dtype), v.to(dtype))
+    if family == "gdn":
+        x = torch.randn((N, H_v), generator=g, device=device, dtype=torch.float32)
+        inp.log_gate = (-alpha_scale * torch.nn.functional.softplus(x.double())).float()
+    x = torch.randn((N, H_v), generator=g, device=device, dtype=torch.float32)
+    inp.beta = torch.sigmoid(x.double()).float()
+    return inp
+
+
+def make_workload_device(name: str, layer: int = 0, device="cuda") -> SegmentInputs:
+    """A named GDN workload drawn on `device` (used for the 48-layer gdn_compose cache)."""
+    info = workload_info(name)
+    assert info["family"] == "gdn" and info["dtype"] == "bf16"
+    seed = WORKLOAD_SEEDS[name] * 1000 + layer
+    inp = make_inputs_device("gdn", info["H_k"], info["H_v"], info["d"], info["seg_lens"],
+                             torch.bfloat16, seed, device=device, alpha_scale=0.05)
+    inp.meta = dict(workload=name, layer=layer, seed=seed, drawn_on=str(device), **info)
+    return inp
+
+
+def to_host(inp: SegmentInputs) -> SegmentInputs:
+    """Copy of a SegmentInputs with every tensor moved to the host."""
+    out = SegmentInputs(inp.family, inp.dtype, inp.H_k, inp.H_v, inp.d_k, inp.d_v,
+                        inp.seg_offsets, inp.k.cpu(), inp.v.cpu(), meta=dict(inp.meta))
+    for n in ("log_gate", "log_gamma", "beta"):
+        t = getattr(inp, n)
+        setattr(out, n, None if t is None else t.cpu())
+    return out

@@ -1,0 +1,232 @@
+"""CUDA path vs the fp64 oracle on identical seeded inputs (needs a GPU).
+
+Small ragged cases span several 64-token chunks, partial chunks, 1-token and empty
+segments; the named workloads run at full size in the same launch configuration as the
+benchmark. Every S, every T (materialised in fp64 from the stored (lam, P)) and every
+composed prefix state is compared matrix by matrix: relative Frobenius error <= 1e-4 for
+fp32 inputs and <= 2e-2 for bf16 inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_attention_state_gdn_gb300 import synth
+from tests.helpers import (COMPOSE_TOL, TOL, assert_close, f64, gpu_T, gpu_build, oracle_build,
+                           oracle_seq, slice_heads)
+
+pytestmark = pytest.mark.gpu
+
+RAGGED = [200, 64, 1, 0, 129, 300, 63]
+FAMILIES = ["linear", "scalar", "diag", "delta", "gdn"]
+
+
+def _hy():
+    import linear_attention_state_gdn_gb300 as hy
+    return hy
+
+
+def check_build(inp, tol=None):
+    tol = tol or TOL[inp.dtype]
+    S, lam, P = gpu_build(inp)
+    So, To = oracle_build(inp)
+    eS = assert_close(f64(S), So, tol, "S")
+    eT = assert_close(gpu_T(inp.family, lam, P, inp.d_k), To, tol, "T")
+    return S, lam, P, eS, eT
+
+
+@pytest.mark.parametrize("family", FAMILIES)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("d", [32, 64, 128])
+def test_build_parity_ragged(family, dtype, d):
+    inp = synth.make_inputs(family, 2, 4, d, RAGGED, dtype, seed=40 + d, gla_div=8.0,
+                            alpha_scale=0.05)
+    check_build(inp)
+
+
+def test_build_scalar_per_token_gate():
+    inp = synth.make_inputs("scalar", 2, 2, 128, [300, 77], torch.bfloat16, seed=41,
+                            per_token_scalar=True)
+    check_build(inp)
+
+
+def test_build_lam_closed_forms():
+    """lam is the plain sum of the log gates (scalar: L * log gamma)."""
+    inp = synth.make_inputs("scalar", 4, 4, 64, [100, 7, 0], torch.bfloat16, seed=42)
+    _, lam, _ = gpu_build(inp)
+    lg = f64(inp.log_gamma)
+    ref = np.array([[L * lg[h] for h in range(4)] for L in (100, 7, 0)])
+    np.testing.assert_allclose(f64(lam), ref, rtol=1e-6, atol=1e-7)
+    inp = synth.make_inputs("linear", 1, 2, 32, [5, 9], torch.float32, seed=43)
+    _, lam, _ = gpu_build(inp)
+    assert np.all(f64(lam) == 0)
+
+
+def test_build_empty_segment_is_identity():
+    inp = synth.make_inputs("gdn", 1, 2, 128, [65, 0, 3], torch.bfloat16, seed=44)
+    S, lam, P = gpu_build(inp)
+    assert torch.all(S[1] == 0)
+    assert torch.all(lam[1] == 0)
+    eye = torch.eye(128, device=P.device).expand(2, 128, 128)
+    assert torch.equal(P[1], eye)
+
+
+def test_build_out_seg_stride_writes_a_layer_slice():
+    """out_seg_stride lets two layers write interleaved into one [n_seg, 2*H_v] cache."""
+    hy = _hy()
+    inp = synth.make_inputs("gdn", 2, 4, 64, [70, 130], torch.bfloat16, seed=45)
+    d = {n: t.cuda() for n, t in inp.tensors().items()}
+    S, lam, P = hy.build_outputs("gdn", 2, 4, 64, "cuda", out_seg_stride=8)
+    S.fill_(7.0)
+    # a [n_seg, 8, ...] slice is not contiguous: pass the base pointers of unit 4 instead
+    ref_S, ref_lam, ref_P = gpu_build(inp)
+    a = hy.make_build_args("gdn", d["k"], d["v"], inp.seg_offsets, d["log_gate"], None,
+                           d["beta"], None, None, None, out_seg_stride=8)
+    a.S = S.data_ptr() + 4 * 64 * 64 * 4
+    a.lam = lam.data_ptr() + 4 * 4
+    a.P = P.data_ptr() + 4 * 64 * 64 * 4
+    import ctypes
+    st = hy.load_library().hypic_build_segments(ctypes.byref(a),
+                                               torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(S[:, 4:], ref_S) and torch.equal(P[:, 4:], ref_P)
+    assert torch.equal(lam[:, 4:], ref_lam)
+    assert torch.all(S[:, :4] == 7.0)
+
+
+# ------------------------------------------------------------------ compose scan
+
+@pytest.mark.parametrize("family", FAMILIES)
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("with_S0", [False, True])
+def test_compose_parity(family, d, with_S0):
+    hy = _hy()
+    c = synth.make_compose_inputs(family, 9, 5, d, seed=50 + d, with_S0=with_S0)
+    dev = lambda t: None if t is None else t.cuda()
+    pref = hy.hypic_compose_scan(family, dev(c.S), dev(c.lam), dev(c.P), dev(c.S0))
+    torch.cuda.synchronize()
+    T = oracle.materialize_T(family, f64(c.lam), f64(c.P), d_k=d)
+    ref = oracle.compose_scan(T, f64(c.S), f64(c.S0))
+    assert_close(f64(pref), ref, COMPOSE_TOL, "prefix")
+    # the carried term T_j prefix_{j-1} on its own (O(1) here, so not masked by S_j)
+    assert_close(f64(pref) - f64(c.S), ref - f64(c.S), COMPOSE_TOL * 10, "carried term")
+
+
+def test_compose_single_segment_is_S_plus_carry():
+    hy = _hy()
+    c = synth.make_compose_inputs("gdn", 1, 3, 128, seed=51)
+    pref = hy.hypic_compose_scan("gdn", c.S.cuda(), c.lam.cuda(), c.P.cuda())
+    assert torch.equal(pref.cpu(), c.S)     # zero initial state: prefix_0 = S_0 exactly
+
+
+# ------------------------------------------------------------------ build -> compose chain
+
+@pytest.mark.parametrize("family", FAMILIES)
+def test_chain_matches_sequential(family):
+    hy = _hy()
+    inp = synth.make_inputs(family, 2, 4, 128, RAGGED, torch.bfloat16, seed=60, gla_div=64.0,
+                            alpha_scale=0.002, beta_shift=-2.0)
+    S, lam, P = gpu_build(inp)
+    pref = hy.hypic_compose_scan(family, S, lam, P)
+    torch.cuda.synchronize()
+    seq = oracle_seq(inp)
+    assert_close(f64(pref), seq, TOL[inp.dtype], "prefix vs sequential")
+
+
+# ------------------------------------------------------------------ stress: O(1) transitions
+
+@pytest.mark.parametrize("case", ["deltanet", "gla_slow", "retnet_slow"])
+def test_stress_carried_term(case):
+    """Transitions near the identity make T_j prefix_{j-1} as large as S_j, so a compose
+    that dropped or transposed T would fail here (the workload gates hide it)."""
+    hy = _hy()
+    if case == "deltanet":
+        inp = synth.make_inputs("delta", 2, 4, 128, [300, 129, 64, 200], torch.bfloat16,
+                                seed=70, beta_shift=-3.0)
+    elif case == "gla_slow":
+        inp = synth.make_inputs("diag", 4, 4, 128, [300, 129, 64, 200], torch.bfloat16,
+                                seed=71, gla_div=256.0)
+    else:
+        inp = synth.make_inputs("scalar", 4, 4, 128, [300, 129, 64, 200], torch.bfloat16,
+                                seed=72, retnet_gammas=False)
+    S, lam, P = gpu_build(inp)
+    pref = hy.hypic_compose_scan(inp.family, S, lam, P)
+    torch.cuda.synchronize()
+    seq = oracle_seq(inp)
+    So, To = oracle_build(inp)
+    carried_ref = seq[1:] - So[1:]
+    assert np.linalg.norm(carried_ref) > 0.3 * np.linalg.norm(So[1:])
+    tol = TOL[inp.dtype]
+    assert_close(f64(pref), seq, tol, "prefix")
+    assert_close(f64(pref)[1:] - f64(S)[1:], carried_ref, tol, "carried term")
+    assert_close(gpu_T(inp.family, lam, P, 128), To, tol, "T")
+
+
+# ------------------------------------------------------------------ named workloads
+
+def _workload_chain(name):
+    hy = _hy()
+    inp = synth.make_workload(name)
+    S, lam, P, eS, eT = check_build(inp)
+    pref = hy.hypic_compose_scan(inp.family, S, lam, P)
+    torch.cuda.synchronize()
+    seq = oracle_seq(inp)
+    eP = assert_close(f64(pref), seq, TOL[inp.dtype], "prefix")
+    return eS, eT, eP
+
+
+def test_workload_gdn_tiny_fp32():
+    eS, eT, eP = _workload_chain("gdn_tiny")
+    assert max(eS, eT, eP) <= 1e-4
+
+
+def test_workload_retnet():
+    _workload_chain("retnet")
+
+
+def test_workload_gla():
+    _workload_chain("gla")
+
+
+def test_workload_gdn():
+    _workload_chain("gdn")
+
+
+def test_workload_gdn_compose_sampled():
+    """48 layers x 32 heads x 64 ragged segments, built layer by layer into one
+    [64, 1536] cache exactly as the benchmark does, then one compose launch over all 1536
+    units. The oracle rebuilds and runs sequentially a sample of (layer, head) units from
+    the same drawn bytes (copied back to the host)."""
+    from bench import build_gdn_compose_cache
+    hy = _hy()
+    S, lam, P, info = build_gdn_compose_cache(layers=48)
+    pref = hy.hypic_compose_scan("gdn", S, lam, P)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(5)
+    H = info["H_v"]
+    for layer in sorted(rng.choice(48, size=3, replace=False)):
+        layer = int(layer)
+        heads = [int(h) for h in sorted(rng.choice(H, size=2, replace=False))]
+        inp = slice_heads(synth.to_host(synth.make_workload_device("gdn_compose", layer)), heads)
+        seq = oracle_seq(inp)
+        So, To = oracle_build(inp)
+        for i, h in enumerate(heads):
+            u = layer * H + h
+            assert_close(f64(pref[:, u]), seq[:, i], 2e-2, f"prefix layer {layer} head {h}")
+            assert_close(f64(S[:, u]), So[:, i], 2e-2, "S")
+            assert_close(gpu_T("gdn", lam[:, u], P[:, u], 128), To[:, i], 2e-2, "T")
+
+
+def test_workload_gdn_compose_full_size_compose_only():
+    """The compose launch at full size (64 segments x 1536 units) on fp32 cached entries
+    drawn directly (O(1) transitions): 1e-4 on sampled units."""
+    hy = _hy()
+    c = synth.make_compose_inputs("gdn", 64, 1536, 128, seed=80)
+    pref = hy.hypic_compose_scan("gdn", c.S.cuda(), c.lam.cuda(), c.P.cuda())
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(6)
+    units = sorted(rng.choice(1536, size=6, replace=False))
+    T = oracle.materialize_T("gdn", f64(c.lam[:, units]), f64(c.P[:, units]))
+    ref = oracle.compose_scan(T, f64(c.S[:, units]))
+    assert_close(f64(pref[:, units]), ref, COMPOSE_TOL, "prefix")
