@@ -66,7 +66,7 @@ bool head_size_ok(int d_k, int d_v) {
 hypic_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA; }
 
 enum class BuildPath { None, GatedSimt, DeltaSeq };
-enum class ComposePath { None, Scaled, DenseSimt };
+enum class ComposePath { None, Scaled, DenseSimt, DenseTc };
 
 // Kernel selection for a build (shape/family/dtype only; no pointer checks).
 BuildPath pick_build(const hypic_build_args *a) {
@@ -78,7 +78,12 @@ BuildPath pick_build(const hypic_build_args *a) {
 ComposePath pick_compose(const hypic_compose_args *a) {
     if (a->n_seg == 0 || a->n_units == 0) return ComposePath::None;
     const bool dense = a->family == HYPIC_FAM_DELTA || a->family == HYPIC_FAM_GDN;
-    return dense ? ComposePath::DenseSimt : ComposePath::Scaled;
+    if (!dense) return ComposePath::Scaled;
+    ComposeParams q{};
+    q.D = a->d_k;
+    q.n_seg = a->n_seg;
+    q.n_units = a->n_units;
+    return compose_dense_tc_supported(q) ? ComposePath::DenseTc : ComposePath::DenseSimt;
 }
 
 bool build_shape_ok(const hypic_build_args *a) {
@@ -258,6 +263,7 @@ hypic_status hypic_compose_scan(const hypic_compose_args *a, void *stream) {
     p.err = err;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (pick_compose(a)) {
+    case ComposePath::DenseTc: return from_cuda(launch_compose_dense_tc(p, s));
     case ComposePath::DenseSimt: return from_cuda(launch_compose_dense_simt(p, s));
     case ComposePath::Scaled: return from_cuda(launch_compose_scaled(p, s));
     case ComposePath::None: break;
@@ -278,6 +284,7 @@ const char *hypic_build_kernel_name(const hypic_build_args *a) {
 const char *hypic_compose_kernel_name(const hypic_compose_args *a) {
     if (!compose_shape_ok(a)) return nullptr;
     switch (pick_compose(a)) {
+    case ComposePath::DenseTc: return "compose_dense_tc";
     case ComposePath::DenseSimt: return "compose_dense_simt";
     case ComposePath::Scaled: return "compose_scaled";
     case ComposePath::None: break;

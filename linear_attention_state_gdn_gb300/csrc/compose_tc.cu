@@ -1,0 +1,324 @@
+// compose_tc.cu -- dense compose prefix scan on the 5th-generation tensor cores (d = 128).
+//
+// For every (layer, head) unit: prefix_j = exp(lam_j) P_j prefix_{j-1} + S_j over the
+// cached segments j ("Cut First-Token Latency by 3.25x: Introducing HYPIC ..."
+// (besthub.dev), paragraph "For linear layers": reuse composes T_C2 . S(C1) + S(C2), with
+// T_C stored as exp(lam) P; paragraph on segment parallelism: a combine worker assembles
+// the final state from the segments' results).
+//
+// Precision. fp32-accurate products from three tf32 MMAs (hi/lo split of both operands:
+// A_hi B_hi + A_lo B_hi + A_hi B_lo, error ~2^-21 relative), fp32 accumulation. The hi
+// parts are truncated to tf32 explicitly, so the result does not depend on how the tensor
+// core rounds fp32 operands.
+//
+// Data flow of one CTA (persistent over units, one unit at a time):
+//   * the transposed running state prefix_{j-1}^T, scaled by exp(lam_j) and split into
+//     (hi, lo), lives in TMEM as the A operand (lane = state column n, column = row k);
+//   * P_j streams in by TMA (128B-swizzled, K-major: rows m, k contiguous) into one of two
+//     64 KB stages; the epilogue warps truncate it to tf32 in place and write its low part
+//     into a two-slot ring of 16 KB k-blocks, so the MMAs of block b overlap the split of
+//     block b+1;
+//   * D^T = A P_j^T accumulates in TMEM (lane n, column m) = (P_j prefix_{j-1})[:, n];
+//   * S_j arrives by TMA into shared memory; the epilogue thread of state column n forms
+//     prefix_j[:, n] = D^T[n, :] + S_j[:, n], stores it (coalesced across the warp) and
+//     writes the next A operand.
+// Roles: warps 0-3 epilogue (one TMEM lane each), warp 4 TMA producer, warp 5 MMA issuer.
+// Every wait is bounded; on expiry the CTA records HYPIC_ERR_TIMEOUT, lets its in-flight
+// copies and MMAs finish (bounded), frees its TMEM and returns.
+#include <algorithm>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+#include "tmap.cuh"
+
+namespace hypic {
+namespace {
+
+using namespace ptx;
+
+constexpr int D = 128;
+constexpr int kEpiWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kThreads = 6 * 32;
+constexpr uint32_t kTile = D * D * 4;          // one fp32 128x128 matrix: 64 KB
+constexpr uint32_t kBlock = D * 32 * 4;        // one 32-column k-block of P: 16 KB
+constexpr uint32_t kOffP = 0;                  // two P stages
+constexpr uint32_t kOffLo = 2 * kTile;         // two low-part k-block slots
+constexpr uint32_t kOffS = 2 * kTile + 2 * kBlock;
+constexpr uint32_t kSmemBytes = kOffS + kTile + 1024;   // + alignment slack
+constexpr uint32_t kTmemCols = 512;            // A_hi [0,128) A_lo [128,256) D [256,384)
+
+struct Bars {
+    uint64_t p_full[2], p_empty[2], lo_full[2], lo_empty[2];
+    uint64_t s_full, s_empty, a_full, d_full, fin;
+};
+
+__device__ __forceinline__ float tf32_trunc(float x) {
+    return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
+__device__ __forceinline__ void st_stream(float *p, float v) {
+    asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
+                        const __grid_constant__ CUtensorMap tmP,
+                        const __grid_constant__ CUtensorMap tmS) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    __shared__ Bars bars;
+    __shared__ uint32_t tslot;
+    __shared__ volatile int abort_flag;
+
+    const int warp = warp_id(), lane = lane_id();
+    const int U = (int)p.n_units, NS = p.n_seg;
+    const bool has_s0 = p.S0 != nullptr;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.p_full[i], 1);
+            mbar_init(&bars.p_empty[i], 1);
+            mbar_init(&bars.lo_full[i], kEpiWarps * 32);
+            mbar_init(&bars.lo_empty[i], 1);
+        }
+        mbar_init(&bars.s_full, 1);
+        mbar_init(&bars.s_empty, kEpiWarps * 32);
+        mbar_init(&bars.a_full, kEpiWarps * 32);
+        mbar_init(&bars.d_full, 1);
+        mbar_init(&bars.fin, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&tslot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tslot;
+    const uint32_t tA_hi = tmem, tA_lo = tmem + 128, tD = tmem + 256;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            prefetch_tmap(&tmP);
+            prefetch_tmap(&tmS);
+            uint32_t pc = 0, sc = 0;
+            for (int u = blockIdx.x; u < U && !abort_flag; u += gridDim.x) {
+                for (int j = 0; j < NS; ++j) {
+                    const int32_t row = (int32_t)(((int64_t)j * U + u) * D);
+                    if (j > 0 || has_s0) {
+                        const uint32_t st = pc & 1, use = pc >> 1;
+                        if (use >= 1 && !mbar_wait_or_abort(&bars.p_empty[st], (use - 1) & 1, p.err,
+                                                            kErrTimeout, &abort_flag))
+                            goto producer_done;
+                        mbar_arrive_expect_tx(&bars.p_full[st], kTile);
+                        for (int b = 0; b < 4; ++b)
+                            tma_load_2d(smem + kOffP + st * kTile + b * kBlock, &tmP, &bars.p_full[st],
+                                        32 * b, row);
+                        ++pc;
+                    }
+                    if (sc >= 1 && !mbar_wait_or_abort(&bars.s_empty, (sc - 1) & 1, p.err,
+                                                       kErrTimeout, &abort_flag))
+                        goto producer_done;
+                    mbar_arrive_expect_tx(&bars.s_full, kTile);
+                    tma_load_2d(smem + kOffS, &tmS, &bars.s_full, 0, row);
+                    ++sc;
+                }
+            }
+        producer_done:
+            if (abort_flag) {
+                // let the loads still in flight land before the CTA leaves (bounded)
+                for (uint32_t q = pc > 2 ? pc - 2 : 0; q < pc; ++q)
+                    mbar_wait(&bars.p_full[q & 1], (q >> 1) & 1, p.err, kErrTimeout);
+                if (sc) mbar_wait(&bars.s_full, (sc - 1) & 1, p.err, kErrTimeout);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            constexpr uint32_t id = idesc(kFmtTF32, kFmtTF32, false, false, 128, 128);
+            uint32_t pc = 0, lb = 0, ac = 0;
+            for (int u = blockIdx.x; u < U && !abort_flag; u += gridDim.x) {
+                for (int j = 0; j < NS; ++j) {
+                    if (!(j > 0 || has_s0)) continue;
+                    const uint32_t st = pc & 1;
+                    if (!mbar_wait_or_abort(&bars.a_full, ac & 1, p.err, kErrTimeout, &abort_flag))
+                        goto mma_done;
+                    ++ac;
+                    tc_fence_after();
+                    for (int b = 0; b < 4; ++b) {
+                        const uint32_t slot = lb & 1, use = lb >> 1;
+                        if (!mbar_wait_or_abort(&bars.lo_full[slot], use & 1, p.err, kErrTimeout,
+                                                &abort_flag))
+                            goto mma_done;
+                        tc_fence_after();
+                        const uint64_t dhi =
+                            sdesc(smem_u32(smem + kOffP + st * kTile + b * kBlock), 16, 1024, kSwizzle128B);
+                        const uint64_t dlo =
+                            sdesc(smem_u32(smem + kOffLo + slot * kBlock), 16, 1024, kSwizzle128B);
+#pragma unroll
+                        for (int s = 0; s < 4; ++s) {
+                            const uint32_t kc = (uint32_t)(32 * b + 8 * s);   // A column of this k-step
+                            mma_tf32_ta(tD, tA_hi + kc, dhi + 2 * s, id, (b | s) != 0);
+                            mma_tf32_ta(tD, tA_lo + kc, dhi + 2 * s, id, 1);
+                            mma_tf32_ta(tD, tA_hi + kc, dlo + 2 * s, id, 1);
+                        }
+                        mma_commit(&bars.lo_empty[slot]);
+                        ++lb;
+                    }
+                    mma_commit(&bars.p_empty[st]);
+                    mma_commit(&bars.d_full);
+                    ++pc;
+                }
+            }
+        mma_done:
+            if (abort_flag) {
+                // every MMA issued so far completes before TMEM is released (bounded)
+                mma_commit(&bars.fin);
+                mbar_wait(&bars.fin, 0, p.err, kErrTimeout);
+            }
+        }
+    } else {
+        // epilogue: thread n owns state column n = TMEM lane n
+        const int n = threadIdx.x;
+        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        uint32_t pc = 0, sc = 0, lb = 0, dc = 0;
+        const float *Ssm = reinterpret_cast<const float *>(smem + kOffS);
+        for (int u = blockIdx.x; u < U && !abort_flag; u += gridDim.x) {
+            if (has_s0) {
+                // A = split(exp(lam_0) S0^T) for the first step
+                const float sc0 = expf(p.lam[u]);
+                const float *s0 = p.S0 + (int64_t)u * D * D + n;
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t hi[16], lo[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float x = s0[(16 * c + i) * D] * sc0;
+                        const float h = tf32_trunc(x);
+                        hi[i] = __float_as_uint(h);
+                        lo[i] = __float_as_uint(x - h);
+                    }
+                    tmem_st16(tA_hi + lane_off + 16 * c, hi);
+                    tmem_st16(tA_lo + lane_off + 16 * c, lo);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bars.a_full);
+            }
+            for (int j = 0; j < NS; ++j) {
+                const bool mma = j > 0 || has_s0;
+                if (mma) {
+                    const uint32_t st = pc & 1, use = pc >> 1;
+                    if (!mbar_wait_or_abort(&bars.p_full[st], use & 1, p.err, kErrTimeout, &abort_flag))
+                        goto epi_done;
+                    for (int b = 0; b < 4; ++b) {
+                        const uint32_t slot = lb & 1, luse = lb >> 1;
+                        if (luse >= 1 && !mbar_wait_or_abort(&bars.lo_empty[slot], (luse - 1) & 1,
+                                                             p.err, kErrTimeout, &abort_flag))
+                            goto epi_done;
+                        float4 *src = reinterpret_cast<float4 *>(smem + kOffP + st * kTile + b * kBlock);
+                        float4 *dst = reinterpret_cast<float4 *>(smem + kOffLo + slot * kBlock);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int idx = n + 128 * q;
+                            const float4 x = src[idx];
+                            float4 h, l;
+                            h.x = tf32_trunc(x.x); l.x = x.x - h.x;
+                            h.y = tf32_trunc(x.y); l.y = x.y - h.y;
+                            h.z = tf32_trunc(x.z); l.z = x.z - h.z;
+                            h.w = tf32_trunc(x.w); l.w = x.w - h.w;
+                            src[idx] = h;
+                            dst[idx] = l;
+                        }
+                        fence_async_shared();
+                        mbar_arrive(&bars.lo_full[slot]);
+                        ++lb;
+                    }
+                    ++pc;
+                    if (!mbar_wait_or_abort(&bars.d_full, dc & 1, p.err, kErrTimeout, &abort_flag))
+                        goto epi_done;
+                    ++dc;
+                    tc_fence_after();
+                }
+                if (!mbar_wait_or_abort(&bars.s_full, sc & 1, p.err, kErrTimeout, &abort_flag))
+                    goto epi_done;
+                ++sc;
+                {
+                    const bool next = j + 1 < NS;
+                    const float scale_next = next ? expf(p.lam[(int64_t)(j + 1) * U + u]) : 0.f;
+                    float *out = p.prefix + ((int64_t)j * U + u) * D * D + n;
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t r[16];
+                        if (mma) {
+                            tmem_ld16(tD + lane_off + 16 * c, r);
+                            tmem_ld_wait();
+                        }
+                        uint32_t hi[16], lo[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int m = 16 * c + i;
+                            const float v = (mma ? __uint_as_float(r[i]) : 0.f) + Ssm[m * D + n];
+                            st_stream(out + (int64_t)m * D, v);
+                            const float x = v * scale_next;
+                            const float h = tf32_trunc(x);
+                            hi[i] = __float_as_uint(h);
+                            lo[i] = __float_as_uint(x - h);
+                        }
+                        if (next) {
+                            tmem_st16(tA_hi + lane_off + 16 * c, hi);
+                            tmem_st16(tA_lo + lane_off + 16 * c, lo);
+                        }
+                    }
+                    mbar_arrive(&bars.s_empty);
+                    if (next) {
+                        tmem_st_wait();
+                        tc_fence_before();
+                        mbar_arrive(&bars.a_full);
+                    }
+                }
+            }
+        }
+    epi_done:;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+bool compose_dense_tc_supported(const ComposeParams &p) {
+    return p.D == D && (int64_t)p.n_seg * p.n_units * D <= INT32_MAX;
+}
+
+cudaError_t launch_compose_dense_tc(const ComposeParams &p, cudaStream_t s) {
+    if (p.n_seg == 0 || p.n_units == 0) return cudaSuccess;
+    const uint64_t rows = (uint64_t)p.n_seg * p.n_units * D;
+    CUtensorMap tmP, tmS;
+    // P is only read for steps with a carried state; any valid base serves otherwise
+    const float *pbase = p.P ? p.P : p.S;
+    if (!make_tmap_2d(&tmP, pbase, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, rows, D * 4, 32, 128,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&tmS, p.S, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, rows, D * 4, 128, 128,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(compose_dense_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = (int)std::min<int64_t>(p.n_units, sm_count());
+    compose_dense_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, tmP, tmS);
+    return cudaGetLastError();
+}
+
+}  // namespace hypic

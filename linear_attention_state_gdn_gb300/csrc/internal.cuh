@@ -64,6 +64,8 @@ cudaError_t launch_build_gated_simt(const BuildParams &p, cudaStream_t s);
 cudaError_t launch_build_delta_seq(const BuildParams &p, cudaStream_t s);
 cudaError_t launch_compose_scaled(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_dense_simt(const ComposeParams &p, cudaStream_t s);
+cudaError_t launch_compose_dense_tc(const ComposeParams &p, cudaStream_t s);
+bool compose_dense_tc_supported(const ComposeParams &p);
 
 // fp32 view of one input element (bf16 or fp32 storage).
 __device__ __forceinline__ float load_in(const void *base, int64_t idx, int dtype) {
