@@ -65,14 +65,19 @@ bool head_size_ok(int d_k, int d_v) {
 
 hypic_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA; }
 
-enum class BuildPath { None, GatedSimt, DeltaSeq };
+enum class BuildPath { None, GatedSimt, GatedTc, DeltaSeq };
 enum class ComposePath { None, Scaled, DenseSimt, DenseTc };
 
 // Kernel selection for a build (shape/family/dtype only; no pointer checks).
 BuildPath pick_build(const hypic_build_args *a) {
     if (a->n_seg == 0) return BuildPath::None;
     const bool delta = a->family == HYPIC_FAM_DELTA || a->family == HYPIC_FAM_GDN;
-    return delta ? BuildPath::DeltaSeq : BuildPath::GatedSimt;
+    if (delta) return BuildPath::DeltaSeq;
+    BuildParams q{};
+    q.family = a->family;
+    q.dtype = a->dtype;
+    q.D = a->d_k;
+    return build_gated_tc_supported(q) ? BuildPath::GatedTc : BuildPath::GatedSimt;
 }
 
 ComposePath pick_compose(const hypic_compose_args *a) {
@@ -185,6 +190,7 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
     p.D = a->d_k;
     p.gqa = a->H_v / a->H_k;
     p.max_len = max_len;
+    p.n_tok = (int32_t)n_tok;
     p.seg_stride = a->out_seg_stride ? a->out_seg_stride : a->H_v;
     p.k = a->k;
     p.v = a->v;
@@ -211,6 +217,7 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (pick_build(a)) {
     case BuildPath::DeltaSeq: return from_cuda(launch_build_delta_seq(p, s));
+    case BuildPath::GatedTc: return from_cuda(launch_build_gated_tc(p, s));
     case BuildPath::GatedSimt: return from_cuda(launch_build_gated_simt(p, s));
     case BuildPath::None: break;
     }
@@ -275,6 +282,7 @@ const char *hypic_build_kernel_name(const hypic_build_args *a) {
     if (!build_shape_ok(a)) return nullptr;
     switch (pick_build(a)) {
     case BuildPath::DeltaSeq: return "build_delta_seq";
+    case BuildPath::GatedTc: return "build_gated_tc";
     case BuildPath::GatedSimt: return "build_gated_simt";
     case BuildPath::None: break;
     }

@@ -1,0 +1,296 @@
+// build_gated_tc.cu -- segment build for plain linear attention, scalar decay (RetNet,
+// Mamba2) and diagonal gates (GLA) on the 5th-generation tensor cores (bf16 k / v, d = 128).
+//
+// What is computed: for every cached segment C and value head, S(C|0) and lam with
+// T_C = exp(lam) (scalar) or Diag(exp(lam)) (diagonal) ("Cut First-Token Latency by 3.25x:
+// Introducing HYPIC ..." (besthub.dev), paragraph "For linear layers"; "Hypic:
+// Position-Independent KV Caching for Hybrid-Attention LLM Serving", "Family comparison:
+// scalar -> diagonal -> dense").
+//
+// Chunked form (exact algebra of S_t = Diag(g_t) S_{t-1} + k_t v_t^T): over a chunk of C
+// tokens with channel log-gates l_t,
+//     S <- Diag(exp(sum_t l_t)) S + Khat^T V,   Khat[t][i] = k_t[i] exp(sum_{s>t} l_s[i]),
+// so every chunk is one C-deep bf16 contraction with fp32 accumulation, and no factor
+// exceeds 1 (no overflow for any segment length).
+//
+// Data flow of one CTA (one (segment, value head) unit; two CTAs per SM):
+//   * warp 8 streams k, v (and the per-channel log-gates) chunk by chunk by TMA into a
+//     3-stage ring; k and v land 128B-swizzled with channels contiguous, which is directly
+//     the MN-major operand layout of both MMA operands;
+//   * warps 0-7 (two threads per key channel i, one per token half of the chunk) scale k
+//     in place into Khat (suffix products of the gates, masked past the segment end) and
+//     hand the stage to the MMA warp;
+//   * warp 9 issues dS_c = Khat^T V into one of two TMEM accumulators (lane i, column n);
+//   * warps 0-7 fold dS_c into the fp32 state they hold in registers (64 columns each):
+//     S[i][:] = exp(sum_t l_t[i]) S[i][:] + dS_c[i][:].
+// Every wait is bounded (HYPIC_ERR_TIMEOUT on expiry, after which the CTA winds down).
+#include <algorithm>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+#include "tmap.cuh"
+
+namespace hypic {
+namespace {
+
+using namespace ptx;
+
+constexpr int D = 128;
+constexpr int kThreads = 320;        // 8 state/decay warps, producer, MMA issuer
+constexpr int kEpi = 256;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kStages = 3;
+constexpr uint32_t kTmemCols = 256;   // two 128-column accumulators
+
+enum { kLinear = 0, kScalar = 1, kDiag = 2 };
+
+template <int KIND>
+struct Geo {
+    static constexpr int C = KIND == kDiag ? 32 : 64;          // tokens per chunk
+    static constexpr uint32_t kHalf = C * 128;                  // 64 channels x C tokens, bf16
+    static constexpr uint32_t kKV = 2 * kHalf;                  // one k (or v) chunk
+    static constexpr uint32_t kG = KIND == kDiag ? C * D * 4 : 0;
+    static constexpr uint32_t kStage = 2 * kKV + kG;
+    static constexpr uint32_t kSmem = kStages * kStage + 1024;
+};
+
+struct Bars {
+    uint64_t full[kStages], kready[kStages], empty[kStages], dfull[2], dfree[2], fin;
+};
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 2)
+build_gated_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG) {
+    using G = Geo<KIND>;
+    constexpr int C = G::C;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    __shared__ Bars bars;
+    __shared__ uint32_t tslot;
+    __shared__ volatile int abort_flag;
+
+    const int warp = warp_id(), lane = lane_id();
+    const SegEntry seg = p.seg[blockIdx.x / p.H_v];
+    const int h = blockIdx.x % p.H_v;
+    const int hk = h / p.gqa;
+    const int nchunks = (seg.len + C - 1) / C;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars.full[s], 1);
+            mbar_init(&bars.kready[s], kEpi);
+            mbar_init(&bars.empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&bars.dfull[b], 1);
+            mbar_init(&bars.dfree[b], kEpi);
+        }
+        mbar_init(&bars.fin, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&tslot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tslot;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            if (KIND == kDiag) prefetch_tmap(&tmG);
+            int c = 0;
+            for (; c < nchunks; ++c) {
+                const int s = c % kStages, use = c / kStages;
+                if (use >= 1 && !mbar_wait_or_abort(&bars.empty[s], (use - 1) & 1, p.err, kErrTimeout,
+                                                    &abort_flag))
+                    break;
+                uint8_t *st = smem + s * G::kStage;
+                const int32_t t0 = seg.start + c * C;
+                mbar_arrive_expect_tx(&bars.full[s], G::kStage);
+                tma_load_3d(st, &tmK, &bars.full[s], 0, hk, t0);
+                tma_load_3d(st + G::kHalf, &tmK, &bars.full[s], 64, hk, t0);
+                tma_load_3d(st + G::kKV, &tmV, &bars.full[s], 0, h, t0);
+                tma_load_3d(st + G::kKV + G::kHalf, &tmV, &bars.full[s], 64, h, t0);
+                if (KIND == kDiag) tma_load_3d(st + 2 * G::kKV, &tmG, &bars.full[s], 0, h, t0);
+            }
+            if (abort_flag)   // let the copies in flight land before leaving (bounded)
+                for (int q = (c > kStages ? c - kStages : 0); q < c; ++q)
+                    mbar_wait(&bars.full[q % kStages], (q / kStages) & 1, p.err, kErrTimeout);
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            constexpr uint32_t id = idesc(kFmtBF16, kFmtBF16, true, true, 128, 128);
+            for (int c = 0; c < nchunks; ++c) {
+                const int s = c % kStages, use = c / kStages, b = c & 1, buse = c >> 1;
+                if (!mbar_wait_or_abort(&bars.kready[s], use & 1, p.err, kErrTimeout, &abort_flag))
+                    break;
+                if (buse >= 1 && !mbar_wait_or_abort(&bars.dfree[b], (buse - 1) & 1, p.err,
+                                                     kErrTimeout, &abort_flag))
+                    break;
+                tc_fence_after();
+                const uint32_t ka = smem_u32(smem + s * G::kStage);
+                const uint32_t va = ka + G::kKV;
+#pragma unroll
+                for (int k = 0; k < C / 16; ++k)
+                    mma_bf16(tmem + b * 128, sdesc(ka + k * 2048, G::kHalf, 1024, kSwizzle128B),
+                             sdesc(va + k * 2048, G::kHalf, 1024, kSwizzle128B), id, k > 0);
+                mma_commit(&bars.empty[s]);
+                mma_commit(&bars.dfull[b]);
+            }
+            if (abort_flag) {
+                mma_commit(&bars.fin);
+                mbar_wait(&bars.fin, 0, p.err, kErrTimeout);
+            }
+        }
+    } else {
+        // thread t: key channel i = t % 128 (= TMEM lane), state columns [64 hc, 64 hc + 64)
+        // and, for the decay, the tokens of its half hc of each chunk
+        const int t = threadIdx.x;
+        const int i = t & 127, hc = t >> 7;
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        float S[64];
+#pragma unroll
+        for (int n = 0; n < 64; ++n) S[n] = 0.f;
+        float lam = 0.f;
+        float gsum[2] = {0.f, 0.f};
+        const float lgam = (KIND == kScalar && p.log_gamma) ? p.log_gamma[h] : 0.f;
+        const float gam = expf(lgam);
+        const uint32_t kcol = (uint32_t)(i >> 6) * G::kHalf;
+        const uint32_t kbyte = (uint32_t)(i & 63) * 2;
+
+        // log-gate of token tt of chunk c for channel i (0 past the segment end)
+        auto gate = [&](const float *gt, int64_t tok0, int valid, int tt) -> float {
+            if (tt >= valid) return 0.f;
+            if (KIND == kDiag) return gt[tt * D + i];
+            if (KIND == kScalar) return p.log_gamma ? lgam : p.log_gate[(tok0 + tt) * p.H_v + h];
+            return 0.f;
+        };
+        auto decay = [&](int c) -> bool {
+            const int s = c % kStages;
+            if (!mbar_wait_or_abort(&bars.full[s], (c / kStages) & 1, p.err, kErrTimeout, &abort_flag))
+                return false;
+            uint8_t *kt = smem + s * G::kStage + kcol;
+            const float *gt = reinterpret_cast<const float *>(smem + s * G::kStage + 2 * G::kKV);
+            const int valid = min(C, seg.len - c * C);
+            const int64_t tok0 = (int64_t)seg.start + c * C;
+            // the other half's gates: needed for the chunk total, and (first half) for the
+            // suffix product entering this half
+            float other = 0.f;
+#pragma unroll 4
+            for (int tt = (1 - hc) * (C / 2); tt < (2 - hc) * (C / 2); ++tt) other += gate(gt, tok0, valid, tt);
+            float r = hc == 0 ? expf(other) : 1.f, own = 0.f;
+#pragma unroll 4
+            for (int tt = hc * (C / 2) + C / 2 - 1; tt >= hc * (C / 2); --tt) {
+                __nv_bfloat16 *kp = reinterpret_cast<__nv_bfloat16 *>(kt + sw128(tt, kbyte));
+                if (tt >= valid) {
+                    *kp = __float2bfloat16(0.f);
+                    continue;
+                }
+                if (KIND != kLinear) *kp = __float2bfloat16(__bfloat162float(*kp) * r);
+                const float l = gate(gt, tok0, valid, tt);
+                if (KIND != kLinear) r *= (KIND == kScalar && p.log_gamma) ? gam : expf(l);
+                own += l;
+            }
+            gsum[c & 1] = own + other;
+            lam += own + other;
+            fence_async_shared();
+            mbar_arrive(&bars.kready[s]);
+            return true;
+        };
+        auto fold = [&](int c) -> bool {
+            const int b = c & 1;
+            if (!mbar_wait_or_abort(&bars.dfull[b], (c >> 1) & 1, p.err, kErrTimeout, &abort_flag))
+                return false;
+            tc_fence_after();
+            const float e = (KIND == kLinear) ? 1.f : expf(gsum[b]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t r[16];
+                tmem_ld16(tmem + lane_off + b * 128 + 64 * hc + 16 * q, r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) S[16 * q + j] = fmaf(e, S[16 * q + j], __uint_as_float(r[j]));
+            }
+            tc_fence_before();
+            mbar_arrive(&bars.dfree[b]);
+            return true;
+        };
+
+        bool ok = true;
+        if (nchunks > 0) ok = decay(0);
+        for (int c = 1; ok && c < nchunks; ++c) ok = decay(c) && fold(c - 1);
+        if (ok && nchunks > 0) ok = fold(nchunks - 1);
+
+        const int64_t unit = (int64_t)seg.idx * p.seg_stride + h;
+        float4 *out = reinterpret_cast<float4 *>(p.S + unit * D * D + (int64_t)i * D + 64 * hc);
+#pragma unroll
+        for (int n = 0; n < 64; n += 4) out[n / 4] = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
+        if (hc == 0) {
+            if (KIND == kDiag) {
+                p.lam[unit * D + i] = lam;
+            } else if (i == 0) {
+                float l = 0.f;
+                if (KIND == kScalar) l = p.log_gamma ? (float)seg.len * lgam : lam;
+                p.lam[unit] = l;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int KIND>
+cudaError_t launch_kind(const BuildParams &p, cudaStream_t s) {
+    using G = Geo<KIND>;
+    const int64_t N = p.n_tok > 0 ? p.n_tok : 1;
+    CUtensorMap tmK, tmV, tmG;
+    if (!make_tmap_3d(&tmK, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_k, N, (uint64_t)D * 2,
+                      (uint64_t)p.H_k * D * 2, 64, 1, G::C, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_3d(&tmV, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_v, N, (uint64_t)D * 2,
+                      (uint64_t)p.H_v * D * 2, 64, 1, G::C, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    if (KIND == kDiag) {
+        if (!make_tmap_3d(&tmG, p.log_gate, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, p.H_v, N,
+                          (uint64_t)D * 4, (uint64_t)p.H_v * D * 4, D, 1, G::C,
+                          CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    } else {
+        tmG = tmV;   // unused
+    }
+    cudaError_t e = cudaFuncSetAttribute(build_gated_tc_kernel<KIND>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
+    if (e != cudaSuccess) return e;
+    const int blocks = p.n_seg * p.H_v;
+    if (blocks == 0) return cudaSuccess;
+    build_gated_tc_kernel<KIND><<<blocks, kThreads, G::kSmem, s>>>(p, tmK, tmV, tmG);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool build_gated_tc_supported(const BuildParams &p) {
+    return p.D == D && p.dtype == HYPIC_BF16 &&
+           (p.family == HYPIC_FAM_LINEAR || p.family == HYPIC_FAM_SCALAR ||
+            p.family == HYPIC_FAM_DIAG);
+}
+
+cudaError_t launch_build_gated_tc(const BuildParams &p, cudaStream_t s) {
+    switch (p.family) {
+    case HYPIC_FAM_LINEAR: return launch_kind<kLinear>(p, s);
+    case HYPIC_FAM_SCALAR: return launch_kind<kScalar>(p, s);
+    case HYPIC_FAM_DIAG: return launch_kind<kDiag>(p, s);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace hypic

@@ -31,6 +31,8 @@ struct BuildParams {
     int32_t D;          // d_k == d_v
     int32_t gqa;        // H_v / H_k
     int32_t max_len;    // longest segment
+    int32_t n_tok;      // tokens in k / v (the last segment offset)
+    int32_t pad0;
     int64_t seg_stride; // output units between segments
     const void *k;
     const void *v;
@@ -66,6 +68,8 @@ cudaError_t launch_compose_scaled(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_dense_simt(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_dense_tc(const ComposeParams &p, cudaStream_t s);
 bool compose_dense_tc_supported(const ComposeParams &p);
+cudaError_t launch_build_gated_tc(const BuildParams &p, cudaStream_t s);
+bool build_gated_tc_supported(const BuildParams &p);
 
 // fp32 view of one input element (bf16 or fp32 storage).
 __device__ __forceinline__ float load_in(const void *base, int64_t idx, int dtype) {

@@ -230,3 +230,31 @@ def test_workload_gdn_compose_full_size_compose_only():
     T = oracle.materialize_T("gdn", f64(c.lam[:, units]), f64(c.P[:, units]))
     ref = oracle.compose_scan(T, f64(c.S[:, units]))
     assert_close(f64(pref[:, units]), ref, COMPOSE_TOL, "prefix")
+
+
+# ------------------------------------------------------------------ kernel selection
+
+@pytest.mark.parametrize("family,dtype,d,expect", [
+    ("linear", torch.bfloat16, 128, "build_gated_tc"), ("scalar", torch.bfloat16, 128, "build_gated_tc"),
+    ("diag", torch.bfloat16, 128, "build_gated_tc"), ("diag", torch.float32, 128, "build_gated_simt"),
+    ("scalar", torch.bfloat16, 64, "build_gated_simt"), ("gdn", torch.float32, 32, "build_delta_seq"),
+])
+def test_build_kernel_selection(family, dtype, d, expect):
+    """bf16 inputs with d = 128 run on the tensor cores; fp32 inputs and smaller heads run the
+    exact CUDA-core kernels (the parity cases above cover both)."""
+    hy = _hy()
+    inp = synth.make_inputs(family, 2, 2, d, [70, 3], dtype, seed=90)
+    dd = {n: t.cuda() for n, t in inp.tensors().items()}
+    name = hy.hypic_build_kernel_name(family, dd["k"], dd["v"], inp.seg_offsets,
+                                      log_gate=dd.get("log_gate"), log_gamma=dd.get("log_gamma"),
+                                      beta=dd.get("beta"))
+    assert name == expect
+
+
+@pytest.mark.parametrize("family,d,expect", [("gdn", 128, "compose_dense_tc"),
+                                             ("delta", 64, "compose_dense_simt"),
+                                             ("diag", 128, "compose_scaled")])
+def test_compose_kernel_selection(family, d, expect):
+    hy = _hy()
+    c = synth.make_compose_inputs(family, 2, 2, d, seed=91)
+    assert hy.hypic_compose_kernel_name(family, c.S) == expect
