@@ -283,11 +283,13 @@ def section_family(name, flush, peak, steps=20, warmup=3):
     (tb, tc), _ = time_loop([st.build, st.compose], steps, warmup, flush)
     b_ms, c_ms = statistics.mean(tb), statistics.mean(tc)
     n_tok, d = inp.n_tok, inp.d_k
+    dense = inp.family in ("gdn", "delta")
     gate_bytes = n_tok * inp.H_v * (d if inp.family == "diag" else 1) * 4 \
         if inp.log_gate is not None else 0
-    b_bytes = n_tok * (inp.H_k + inp.H_v) * d * 2 + gate_bytes + \
-        inp.n_seg * inp.H_v * (d * d * 4 + (d * 4 if inp.family == "diag" else 4))
-    c_bytes = compose_algorithmic_bytes(inp.n_seg, inp.H_v, d, False, inp.family == "diag")
+    beta_bytes = n_tok * inp.H_v * 4 if inp.beta is not None else 0
+    b_bytes = n_tok * (inp.H_k + inp.H_v) * d * 2 + gate_bytes + beta_bytes + \
+        inp.n_seg * inp.H_v * (d * d * 4 * (2 if dense else 1) + (d * 4 if inp.family == "diag" else 4))
+    c_bytes = compose_algorithmic_bytes(inp.n_seg, inp.H_v, d, dense, inp.family == "diag")
     bk, ck = st.kernel_names()
     b_gbs, c_gbs = b_bytes / b_ms / 1e6, c_bytes / c_ms / 1e6
     return {"build_kernel": bk, "build_ms": round(b_ms, 4),
@@ -542,6 +544,25 @@ def run_main(args):
     return 0
 
 
+def run_only(args):
+    """Time one workload's launches alone (for profiling runs): build + compose for the
+    named workload, or the compose scan alone for gdn_compose."""
+    import linear_attention_state_gdn_gb300 as hy
+    from linear_attention_state_gdn_gb300 import synth
+    torch.cuda.set_device(0)
+    hy.load_library()
+    pk = peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    if args.only == "gdn_compose":
+        out = section_gdn_compose(flush, pk, steps=args.steps, warmup=args.warmup,
+                                  layers=args.compose_layers)
+    else:
+        out = section_family(args.only, flush, pk, steps=args.steps, warmup=args.warmup)
+    assert hy.hypic_get_device_status() == 0
+    print(json.dumps({"only": args.only, **out}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -551,10 +572,14 @@ def main(argv=None):
     ap.add_argument("--quick", action="store_true",
                     help="main timed region only (no e2e, sections or CPU baseline)")
     ap.add_argument("--compose-layers", type=int, default=48)
+    ap.add_argument("--only", choices=["gdn", "retnet", "gla", "gdn_tiny", "gdn_compose"],
+                    help="time one workload's launches alone (profiling helper; no contract line)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
     if args.impl == "reference":
         return run_reference(args)
+    if args.only:
+        return run_only(args)
     return run_main(args)
 
 
