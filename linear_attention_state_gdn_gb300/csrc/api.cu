@@ -65,18 +65,18 @@ bool head_size_ok(int d_k, int d_v) {
 
 hypic_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA; }
 
-enum class BuildPath { None, GatedSimt, GatedTc, DeltaSeq };
+enum class BuildPath { None, GatedSimt, GatedTc, DeltaSeq, GdnTc };
 enum class ComposePath { None, Scaled, DenseSimt, DenseTc };
 
 // Kernel selection for a build (shape/family/dtype only; no pointer checks).
 BuildPath pick_build(const hypic_build_args *a) {
     if (a->n_seg == 0) return BuildPath::None;
     const bool delta = a->family == HYPIC_FAM_DELTA || a->family == HYPIC_FAM_GDN;
-    if (delta) return BuildPath::DeltaSeq;
     BuildParams q{};
     q.family = a->family;
     q.dtype = a->dtype;
     q.D = a->d_k;
+    if (delta) return build_gdn_tc_supported(q) ? BuildPath::GdnTc : BuildPath::DeltaSeq;
     return build_gated_tc_supported(q) ? BuildPath::GatedTc : BuildPath::GatedSimt;
 }
 
@@ -216,6 +216,7 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (pick_build(a)) {
+    case BuildPath::GdnTc: return from_cuda(launch_build_gdn_tc(p, s));
     case BuildPath::DeltaSeq: return from_cuda(launch_build_delta_seq(p, s));
     case BuildPath::GatedTc: return from_cuda(launch_build_gated_tc(p, s));
     case BuildPath::GatedSimt: return from_cuda(launch_build_gated_simt(p, s));
@@ -281,6 +282,7 @@ hypic_status hypic_compose_scan(const hypic_compose_args *a, void *stream) {
 const char *hypic_build_kernel_name(const hypic_build_args *a) {
     if (!build_shape_ok(a)) return nullptr;
     switch (pick_build(a)) {
+    case BuildPath::GdnTc: return "build_gdn_tc";
     case BuildPath::DeltaSeq: return "build_delta_seq";
     case BuildPath::GatedTc: return "build_gated_tc";
     case BuildPath::GatedSimt: return "build_gated_simt";

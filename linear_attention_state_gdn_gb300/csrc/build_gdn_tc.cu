@@ -1,0 +1,508 @@
+// build_gdn_tc.cu -- DeltaNet / Gated DeltaNet segment build on the 5th-generation tensor
+// cores (bf16 k / v, d_k = d_v = 128, fp32 state).
+//
+// What is computed: for every cached segment C and value head the pair (S(C|0), T_C) with
+// T_C = exp(lam) P, P = prod_t (I - b_t k_t k_t^T) (latest factor leftmost), lam = sum log a_t
+// ("Cut First-Token Latency by 3.25x: Introducing HYPIC ..." (besthub.dev), paragraph "For
+// linear layers": HYPIC stores (T_C, S(C|0)) for DeltaNet / GDN layers; GDN recurrence from
+// "Gated Delta Networks: Improving Mamba2 with Delta Rule", reference 7 of the episode
+// companion page "Hypic: Position-Independent KV Caching for Hybrid-Attention LLM Serving").
+//
+// Chunked form (exact algebra, chunks of C = 64 tokens, c_t = sum_{s<=t} log a_s inside
+// the chunk, A_ts = b_t (k_t . k_s) exp(c_t - c_s) for s < t, M = (I + A)^-1):
+//     W = M Diag(b e^c) K,  U = M Diag(b) V,  X = W [S | P],
+//     S <- e^{c_C} (S + K^T Diag(e^-c) (U - X_S)),   P <- P - K^T Diag(e^-c) X_P.
+// The state is carried as Z = [S~ | P] with S = exp(Lam) S~ (Lam a running log-scale,
+// renormalised into S~ when it drops below -20), so every chunk only adds to Z:
+//     Z <- Z + K^T D',   D' = Diag(e^-c) [exp(-Lam) U - X_S | -X_P].
+//
+// Layout (one CTA = one (segment, value head) unit, 320 threads, all 512 TMEM columns):
+//   TMEM  Z^T   [0,256)   lane = state column n (S~ half, then P half), column = key row i
+//         X^T   [256,384) lane n, column t          (X^T = Z^T W^T, two M = 128 halves)
+//         G/W^T [384,448) gram (M = 64 layout), then W^T (lane i, column t)
+//         U^T   [448,512) lane n, column t
+//   SMEM  two TMA stages of (k, v) chunks (128B-swizzled, channels contiguous), the bf16 A
+//         operands Z^T and D'^T (K-major), W (MN-major), M Diag(b e^c) and M Diag(b)
+//         (K-major), the fp32 A matrix for the inversion, per-chunk gate vectors.
+// Roles: warps 0-3 carry the chain (Z^T -> bf16, D' formation; thread n = TMEM lane n),
+// warps 4-7 prepare the next chunk (gates, A, M by column forward substitution in fp32,
+// W^T -> W), warp 8 issues TMA, warp 9 issues the MMAs. Every wait is bounded.
+#include <algorithm>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+#include "tmap.cuh"
+
+namespace hypic {
+namespace {
+
+using namespace ptx;
+
+constexpr int D = 128;
+constexpr int C = 64;
+constexpr int kThreads = 320;
+constexpr int kPrepWarp0 = 4;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr float kRenorm = -20.f;     // fold exp(Lam) into S~ below this log-scale
+constexpr float kMinChunkLogDecay = -60.f;
+
+// shared-memory map (offsets from the 1024-aligned base)
+constexpr uint32_t kKTile = C * 256;                  // k chunk: two 64-channel halves, 16 KB
+constexpr uint32_t kStage = 2 * kKTile;               // k + v
+constexpr uint32_t kOffStage = 0;                     // 2 stages: 64 KB
+constexpr uint32_t kOffAX = 2 * kStage;               // Z^T bf16, 2 K-blocks x 256 rows x 128 B
+constexpr uint32_t kOffAD = kOffAX + 65536;           // D'^T bf16, 256 rows x 128 B
+constexpr uint32_t kOffBW = kOffAD + 32768;           // W, MN-major: 128 rows i x 128 B
+constexpr uint32_t kOffMp = kOffBW + 16384;           // M Diag(b e^c): 64 rows t x 128 B
+constexpr uint32_t kOffMpp = kOffMp + 8192;           // M Diag(b)
+constexpr uint32_t kOffA32 = kOffMpp + 8192;          // fp32 A, 64 x 64
+constexpr uint32_t kOffVec = kOffA32 + 16384;         // per-chunk vectors (2 slots)
+constexpr uint32_t kVecSlot = 5 * C * 4 + 16;
+constexpr uint32_t kSmemBytes = kOffVec + 2 * kVecSlot + 1024;
+
+constexpr uint32_t kTZ = 0, kTX = 256, kTGW = 384, kTU = 448;
+
+struct Vec {   // one slot of per-chunk vectors
+    float beta[C], c[C], ecp[C], ecm[C], bec[C];
+    float cC;  // chunk total log decay
+    float pad[3];
+};
+
+struct Bars {
+    uint64_t kv_full[2], kv_empty[2];
+    uint64_t gfull, mready, wfull, wready, zbf_ready, xfull, dready, zfull, fin;
+};
+
+__device__ __forceinline__ void bar_prep() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t bf2(float lo, float hi) { return pack_bf16x2(lo, hi); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~uintptr_t(1023));
+    __shared__ Bars bars;
+    __shared__ uint32_t tslot;
+    __shared__ volatile int abort_flag;
+    __shared__ float scan_tmp[2];
+    __shared__ int prep_flag[2];
+
+    const int warp = warp_id(), lane = lane_id();
+    const SegEntry seg = p.seg[blockIdx.x / p.H_v];
+    const int h = blockIdx.x % p.H_v;
+    const int hk = h / p.gqa;
+    const int nch = (seg.len + C - 1) / C;
+    const bool gdn = p.family == HYPIC_FAM_GDN;
+    Vec *vec = reinterpret_cast<Vec *>(smem + kOffVec);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars.kv_full[s], 1);
+            mbar_init(&bars.kv_empty[s], 1);
+        }
+        mbar_init(&bars.gfull, 1);
+        mbar_init(&bars.mready, 128);
+        mbar_init(&bars.wfull, 1);
+        mbar_init(&bars.wready, 128);
+        mbar_init(&bars.zbf_ready, 128);
+        mbar_init(&bars.xfull, 1);
+        mbar_init(&bars.dready, 128);
+        mbar_init(&bars.zfull, 1);
+        mbar_init(&bars.fin, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&tslot, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tslot;
+    auto wait = [&](uint64_t *b, uint32_t par) {
+        return mbar_wait_or_abort(b, par, p.err, kErrTimeout, &abort_flag);
+    };
+
+    if (warp == kProducerWarp) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tmK);
+            prefetch_tmap(&tmV);
+            int c = 0;
+            for (; c < nch; ++c) {
+                const int s = c & 1, use = c >> 1;
+                if (use >= 1 && !wait(&bars.kv_empty[s], (use - 1) & 1)) break;
+                uint8_t *st = smem + kOffStage + s * kStage;
+                const int32_t t0 = seg.start + c * C;
+                mbar_arrive_expect_tx(&bars.kv_full[s], kStage);
+                tma_load_3d(st, &tmK, &bars.kv_full[s], 0, hk, t0);
+                tma_load_3d(st + kKTile / 2, &tmK, &bars.kv_full[s], 64, hk, t0);
+                tma_load_3d(st + kKTile, &tmV, &bars.kv_full[s], 0, h, t0);
+                tma_load_3d(st + kKTile + kKTile / 2, &tmV, &bars.kv_full[s], 64, h, t0);
+            }
+            if (abort_flag)
+                for (int q = (c > 2 ? c - 2 : 0); q < c; ++q)
+                    mbar_wait(&bars.kv_full[q & 1], (q >> 1) & 1, p.err, kErrTimeout);
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------------------------------------------------------- MMA issuer
+        if (lane == 0 && nch > 0) {
+            constexpr uint32_t idG = idesc(kFmtBF16, kFmtBF16, false, false, 64, 64);
+            constexpr uint32_t idWU = idesc(kFmtBF16, kFmtBF16, true, false, 128, 64);
+            constexpr uint32_t idX = idesc(kFmtBF16, kFmtBF16, false, true, 128, 64);
+            constexpr uint32_t idZ = idesc(kFmtBF16, kFmtBF16, false, true, 128, 128);
+            const uint32_t sb = smem_u32(smem);
+            auto issue_gram = [&](int c) -> bool {
+                if (!wait(&bars.kv_full[c & 1], (c >> 1) & 1)) return false;
+                if (c >= 1 && !wait(&bars.wready, (c - 1) & 1)) return false;   // G/W slot free
+                tc_fence_after();
+                const uint32_t k = sb + kOffStage + (c & 1) * kStage;
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t a = k + (s >> 2) * (kKTile / 2) + (s & 3) * 32;
+                    mma_bf16(tmem + kTGW, sdesc(a, 16, 1024, kSwizzle128B),
+                             sdesc(a, 16, 1024, kSwizzle128B), idG, s > 0);
+                }
+                mma_commit(&bars.gfull);
+                return true;
+            };
+            auto issue_wu = [&](int c) -> bool {
+                if (!wait(&bars.mready, c & 1)) return false;
+                if (c >= 1 && !wait(&bars.dready, (c - 1) & 1)) return false;   // U slot free
+                tc_fence_after();
+                const uint32_t k = sb + kOffStage + (c & 1) * kStage, v = k + kKTile;
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tmem + kTGW, sdesc(k + s * 2048, kKTile / 2, 1024, kSwizzle128B),
+                             sdesc(sb + kOffMp + s * 32, 16, 1024, kSwizzle128B), idWU, s > 0);
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_bf16(tmem + kTU, sdesc(v + s * 2048, kKTile / 2, 1024, kSwizzle128B),
+                             sdesc(sb + kOffMpp + s * 32, 16, 1024, kSwizzle128B), idWU, s > 0);
+                mma_commit(&bars.wfull);
+                return true;
+            };
+            bool ok = issue_gram(0) && issue_wu(0);
+            for (int c = 0; ok && c < nch; ++c) {
+                // X^T = Z^T W^T for the S~ and P halves
+                ok = wait(&bars.wready, c & 1) && wait(&bars.zbf_ready, c & 1);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t a = sb + kOffAX + (s >> 2) * 32768 + hf * 16384 + (s & 3) * 32;
+                        const uint32_t b = sb + kOffBW + s * 2048;
+                        mma_bf16(tmem + kTX + 64 * hf, sdesc(a, 16, 1024, kSwizzle128B),
+                                 sdesc(b, 8192, 1024, kSwizzle128B), idX, s > 0);
+                    }
+                mma_commit(&bars.xfull);
+                if (c + 1 < nch && !(ok = issue_gram(c + 1))) break;
+                // Z^T += D'^T K
+                if (!(ok = wait(&bars.dready, c & 1))) break;
+                tc_fence_after();
+                const uint32_t k = sb + kOffStage + (c & 1) * kStage;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        mma_bf16(tmem + kTZ + 128 * hf,
+                                 sdesc(sb + kOffAD + hf * 16384 + s * 32, 16, 1024, kSwizzle128B),
+                                 sdesc(k + s * 2048, kKTile / 2, 1024, kSwizzle128B), idZ, 1);
+                mma_commit(&bars.zfull);
+                mma_commit(&bars.kv_empty[c & 1]);
+                if (c + 1 < nch && !(ok = issue_wu(c + 1))) break;
+            }
+            if (abort_flag) {
+                mma_commit(&bars.fin);
+                mbar_wait(&bars.fin, 0, p.err, kErrTimeout);
+            }
+        }
+    } else if (warp >= kPrepWarp0) {
+        // ---------------------------------------------------------------- prep warps 4-7
+        const int q = threadIdx.x - 128;          // 0..127
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        float *A32 = reinterpret_cast<float *>(smem + kOffA32);
+        // one elected thread waits; the outcome reaches the other 127 through the named
+        // barrier, so every prep thread takes the same branch (no thread is left behind
+        // at a barrier when a wait gives up)
+        uint32_t nw = 0;
+        auto pwait = [&](uint64_t *b, uint32_t par) -> bool {
+            volatile int *f = &prep_flag[nw & 1];
+            if (q == 0) *f = wait(b, par) ? 1 : 0;
+            bar_prep();
+            const bool r = *f != 0;
+            ++nw;
+            return r;
+        };
+        for (int c = 0; c < nch; ++c) {   // leaves only through a broadcast pwait outcome
+            Vec &v = vec[c & 1];
+            // (a) gates of chunk c. The slot was last read by the chain for chunk c-2, which
+            //     finished before W of chunk c-1 was issued (waited on in (d) below).
+            const int valid = min(C, seg.len - c * C);
+            if (q < C) {
+                const int64_t tok = (int64_t)seg.start + c * C + q;
+                const bool in = q < valid;
+                const float b = in ? p.beta[tok * p.H_v + h] : 0.f;
+                const float la = (in && gdn) ? p.log_gate[tok * p.H_v + h] : 0.f;
+                float x = la;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
+                }
+                if (lane == 31) scan_tmp[q >> 5] = x;
+                v.beta[q] = b;
+                v.c[q] = x;   // finished below for the upper half
+            }
+            bar_prep();
+            if (q < C) {
+                const float cc = q >= 32 ? v.c[q] + scan_tmp[0] : v.c[q];
+                v.c[q] = cc;
+                v.ecp[q] = expf(cc);
+                v.ecm[q] = expf(-cc);
+                v.bec[q] = v.beta[q] * expf(cc);
+                if (q == C - 1) {
+                    v.cC = cc;
+                    if (cc < kMinChunkLogDecay) atomicOr(p.err, kErrRange);
+                }
+            }
+            // (b) gram -> A (rows t = 16 (warp - 4) + lane for lanes < 16)
+            if (!pwait(&bars.gfull, c & 1)) break;
+            tc_fence_after();
+            {
+                const int t = 16 * (warp - kPrepWarp0) + lane;
+                uint32_t g[64];
+                tmem_ld32(tmem + lane_off + kTGW, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
+                tmem_ld32(tmem + lane_off + kTGW + 32, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
+                tmem_ld_wait();
+                if (lane < 16) {
+                    const float bt = v.beta[t], et = v.ecp[t];
+                    float4 *row = reinterpret_cast<float4 *>(A32 + t * C);
+#pragma unroll
+                    for (int s = 0; s < C; s += 4) {
+                        float4 a;
+                        a.x = s + 0 < t ? bt * __uint_as_float(g[s + 0]) * et * v.ecm[s + 0] : 0.f;
+                        a.y = s + 1 < t ? bt * __uint_as_float(g[s + 1]) * et * v.ecm[s + 1] : 0.f;
+                        a.z = s + 2 < t ? bt * __uint_as_float(g[s + 2]) * et * v.ecm[s + 2] : 0.f;
+                        a.w = s + 3 < t ? bt * __uint_as_float(g[s + 3]) * et * v.ecm[s + 3] : 0.f;
+                        row[s / 4] = a;
+                    }
+                }
+            }
+            tc_fence_before();
+            bar_prep();
+            // (c) M = (I + A)^-1 by column forward substitution (thread q < 64: column q),
+            //     then M Diag(b e^c) and M Diag(b) as bf16 K-major rows
+            if (q < C) {
+                float x[C];
+#pragma unroll
+                for (int t = 0; t < C; ++t) {
+                    float acc = (t == q) ? 1.f : 0.f;
+                    const float4 *row = reinterpret_cast<const float4 *>(A32 + t * C);
+#pragma unroll
+                    for (int r = 0; r < t; r += 4) {
+                        const float4 a = row[r / 4];
+                        acc = fmaf(-a.x, x[r], acc);
+                        if (r + 1 < t) acc = fmaf(-a.y, x[r + 1], acc);
+                        if (r + 2 < t) acc = fmaf(-a.z, x[r + 2], acc);
+                        if (r + 3 < t) acc = fmaf(-a.w, x[r + 3], acc);
+                    }
+                    x[t] = acc;
+                }
+                const float s1 = v.bec[q], s2 = v.beta[q];
+                uint8_t *mp = smem + kOffMp, *mpp = smem + kOffMpp;
+#pragma unroll
+                for (int t = 0; t < C; ++t) {
+                    *reinterpret_cast<__nv_bfloat16 *>(mp + sw128(t, 2 * q)) = __float2bfloat16(x[t] * s1);
+                    *reinterpret_cast<__nv_bfloat16 *>(mpp + sw128(t, 2 * q)) = __float2bfloat16(x[t] * s2);
+                }
+            }
+            fence_async_shared();
+            mbar_arrive(&bars.mready);
+            // (d) W^T (lane i) -> W, MN-major rows i; B_W is free once X of chunk c-1 is done
+            if (!pwait(&bars.wfull, c & 1)) break;
+            if (c >= 1 && !pwait(&bars.xfull, (c - 1) & 1)) break;
+            tc_fence_after();
+            {
+                uint32_t w[64];
+                tmem_ld32(tmem + lane_off + kTGW, *reinterpret_cast<uint32_t(*)[32]>(&w[0]));
+                tmem_ld32(tmem + lane_off + kTGW + 32, *reinterpret_cast<uint32_t(*)[32]>(&w[32]));
+                tmem_ld_wait();
+                uint8_t *bw = smem + kOffBW;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint4 pk;
+                    pk.x = bf2(__uint_as_float(w[8 * j + 0]), __uint_as_float(w[8 * j + 1]));
+                    pk.y = bf2(__uint_as_float(w[8 * j + 2]), __uint_as_float(w[8 * j + 3]));
+                    pk.z = bf2(__uint_as_float(w[8 * j + 4]), __uint_as_float(w[8 * j + 5]));
+                    pk.w = bf2(__uint_as_float(w[8 * j + 6]), __uint_as_float(w[8 * j + 7]));
+                    *reinterpret_cast<uint4 *>(bw + sw128(q, 16 * j)) = pk;
+                }
+            }
+            fence_async_shared();
+            tc_fence_before();
+            mbar_arrive(&bars.wready);
+        }
+    } else {
+        // ---------------------------------------------------------------- chain warps 0-3
+        const int n = threadIdx.x;   // state column (and TMEM lane)
+        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        float Lam = 0.f, lam_total = 0.f;
+        // Z^T = [0 | I]
+        {
+            uint32_t z[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) z[j] = 0u;
+#pragma unroll
+            for (int c0 = 0; c0 < 256; c0 += 16) tmem_st16(tmem + lane_off + kTZ + c0, z);
+            tmem_st_wait();
+            // identity in the P half: every lane stores every column group (the TMEM
+            // address of a warp-wide store must be the same in all lanes)
+#pragma unroll
+            for (int c0 = 0; c0 < 128; c0 += 16) {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) z[j] = (c0 + j == n) ? __float_as_uint(1.f) : 0u;
+                tmem_st16(tmem + lane_off + kTZ + 128 + c0, z);
+            }
+            tmem_st_wait();
+        }
+        uint8_t *ax = smem + kOffAX, *ad = smem + kOffAD;
+        bool ok = true;
+        for (int c = 0; ok && c < nch; ++c) {
+            // (1) Z^T -> bf16 A operand (renormalising S~ when the log-scale got small)
+            if (c >= 1 && !(ok = wait(&bars.zfull, (c - 1) & 1))) break;
+            tc_fence_after();
+            const bool renorm = Lam < kRenorm;
+            const float sc = renorm ? expf(Lam) : 1.f;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll
+                for (int c0 = 0; c0 < 128; c0 += 16) {
+                    uint32_t z[16];
+                    tmem_ld16(tmem + lane_off + kTZ + 128 * hf + c0, z);
+                    tmem_ld_wait();
+                    if (hf == 0 && renorm) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) z[j] = __float_as_uint(__uint_as_float(z[j]) * sc);
+                        tmem_st16(tmem + lane_off + kTZ + c0, z);
+                    }
+                    uint4 lo, hi;
+                    lo.x = bf2(__uint_as_float(z[0]), __uint_as_float(z[1]));
+                    lo.y = bf2(__uint_as_float(z[2]), __uint_as_float(z[3]));
+                    lo.z = bf2(__uint_as_float(z[4]), __uint_as_float(z[5]));
+                    lo.w = bf2(__uint_as_float(z[6]), __uint_as_float(z[7]));
+                    hi.x = bf2(__uint_as_float(z[8]), __uint_as_float(z[9]));
+                    hi.y = bf2(__uint_as_float(z[10]), __uint_as_float(z[11]));
+                    hi.z = bf2(__uint_as_float(z[12]), __uint_as_float(z[13]));
+                    hi.w = bf2(__uint_as_float(z[14]), __uint_as_float(z[15]));
+                    // row (128 hf + n) of the K-major tile, key rows c0..c0+15 in K-block c0 / 64
+                    uint8_t *rowb = ax + (c0 >> 6) * 32768;
+                    const uint32_t r = 128 * hf + n, b = (c0 & 63) * 2;
+                    *reinterpret_cast<uint4 *>(rowb + sw128(r, b)) = lo;
+                    *reinterpret_cast<uint4 *>(rowb + sw128(r, b + 16)) = hi;
+                }
+            }
+            if (renorm) {
+                tmem_st_wait();
+                Lam = 0.f;
+            }
+            fence_async_shared();
+            tc_fence_before();
+            mbar_arrive(&bars.zbf_ready);
+            // (3) D'^T = Diag(e^-c) [e^-Lam U - X_S | -X_P], rows n and 128 + n of the K-major tile
+            if (!(ok = wait(&bars.xfull, c & 1))) break;
+            tc_fence_after();
+            const Vec &v = vec[c & 1];
+            const float cC = v.cC;
+            const float eL = expf(-Lam);
+#pragma unroll
+            for (int c0 = 0; c0 < C; c0 += 16) {
+                uint32_t xs[16], xp[16], u[16];
+                tmem_ld16(tmem + lane_off + kTX + c0, xs);
+                tmem_ld16(tmem + lane_off + kTX + 64 + c0, xp);
+                tmem_ld16(tmem + lane_off + kTU + c0, u);
+                tmem_ld_wait();
+                float ds[16], dp[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float e = v.ecm[c0 + j];
+                    ds[j] = e * fmaf(eL, __uint_as_float(u[j]), -__uint_as_float(xs[j]));
+                    dp[j] = -e * __uint_as_float(xp[j]);
+                }
+                uint4 a, b2, d, e2;
+                a = make_uint4(bf2(ds[0], ds[1]), bf2(ds[2], ds[3]), bf2(ds[4], ds[5]), bf2(ds[6], ds[7]));
+                b2 = make_uint4(bf2(ds[8], ds[9]), bf2(ds[10], ds[11]), bf2(ds[12], ds[13]), bf2(ds[14], ds[15]));
+                d = make_uint4(bf2(dp[0], dp[1]), bf2(dp[2], dp[3]), bf2(dp[4], dp[5]), bf2(dp[6], dp[7]));
+                e2 = make_uint4(bf2(dp[8], dp[9]), bf2(dp[10], dp[11]), bf2(dp[12], dp[13]), bf2(dp[14], dp[15]));
+                const uint32_t bo = c0 * 2;
+                *reinterpret_cast<uint4 *>(ad + sw128(n, bo)) = a;
+                *reinterpret_cast<uint4 *>(ad + sw128(n, bo + 16)) = b2;
+                *reinterpret_cast<uint4 *>(ad + sw128(128 + n, bo)) = d;
+                *reinterpret_cast<uint4 *>(ad + sw128(128 + n, bo + 16)) = e2;
+            }
+            fence_async_shared();
+            tc_fence_before();
+            mbar_arrive(&bars.dready);
+            Lam += cC;
+            lam_total += cC;
+        }
+        // outputs: S = exp(Lam) S~ (column n), P (column n), lam
+        if (ok && nch > 0) ok = wait(&bars.zfull, (nch - 1) & 1);
+        tc_fence_after();
+        const int64_t unit = (int64_t)seg.idx * p.seg_stride + h;
+        float *So = p.S + unit * D * D + n;
+        float *Po = p.P + unit * D * D + n;
+        const float sc = expf(Lam);
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int c0 = 0; c0 < 128; c0 += 16) {
+                uint32_t z[16];
+                tmem_ld16(tmem + lane_off + kTZ + 128 * hf + c0, z);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float val = __uint_as_float(z[j]);
+                    if (hf == 0) So[(int64_t)(c0 + j) * D] = val * sc;
+                    else Po[(int64_t)(c0 + j) * D] = val;
+                }
+            }
+        if (n == 0) p.lam[unit] = lam_total;
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+bool build_gdn_tc_supported(const BuildParams &p) {
+    return p.D == D && p.dtype == HYPIC_BF16 &&
+           (p.family == HYPIC_FAM_GDN || p.family == HYPIC_FAM_DELTA);
+}
+
+cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s) {
+    const int64_t N = p.n_tok > 0 ? p.n_tok : 1;
+    CUtensorMap tmK, tmV;
+    if (!make_tmap_3d(&tmK, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_k, N, (uint64_t)D * 2,
+                      (uint64_t)p.H_k * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_3d(&tmV, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_v, N, (uint64_t)D * 2,
+                      (uint64_t)p.H_v * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(build_gdn_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int blocks = p.n_seg * p.H_v;
+    if (blocks == 0) return cudaSuccess;
+    build_gdn_tc_kernel<<<blocks, kThreads, kSmemBytes, s>>>(p, tmK, tmV);
+    return cudaGetLastError();
+}
+
+}  // namespace hypic

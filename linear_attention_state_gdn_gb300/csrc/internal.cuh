@@ -70,6 +70,8 @@ cudaError_t launch_compose_dense_tc(const ComposeParams &p, cudaStream_t s);
 bool compose_dense_tc_supported(const ComposeParams &p);
 cudaError_t launch_build_gated_tc(const BuildParams &p, cudaStream_t s);
 bool build_gated_tc_supported(const BuildParams &p);
+cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s);
+bool build_gdn_tc_supported(const BuildParams &p);
 
 // fp32 view of one input element (bf16 or fp32 storage).
 __device__ __forceinline__ float load_in(const void *base, int64_t idx, int dtype) {

@@ -276,6 +276,11 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// TMEM address of (lane, column) relative to an allocation base.
+__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
+    return base + (lane << 16) + col;
+}
+
 // ------------------------------------------------------------------------------ layouts
 
 // Byte offset of (row, byte-in-row) inside a tile stored with the 128-byte swizzle: rows of

@@ -238,6 +238,8 @@ def test_workload_gdn_compose_full_size_compose_only():
     ("linear", torch.bfloat16, 128, "build_gated_tc"), ("scalar", torch.bfloat16, 128, "build_gated_tc"),
     ("diag", torch.bfloat16, 128, "build_gated_tc"), ("diag", torch.float32, 128, "build_gated_simt"),
     ("scalar", torch.bfloat16, 64, "build_gated_simt"), ("gdn", torch.float32, 32, "build_delta_seq"),
+    ("gdn", torch.bfloat16, 128, "build_gdn_tc"), ("delta", torch.bfloat16, 128, "build_gdn_tc"),
+    ("gdn", torch.float32, 128, "build_delta_seq"), ("gdn", torch.bfloat16, 64, "build_delta_seq"),
 ])
 def test_build_kernel_selection(family, dtype, d, expect):
     """bf16 inputs with d = 128 run on the tensor cores; fp32 inputs and smaller heads run the
