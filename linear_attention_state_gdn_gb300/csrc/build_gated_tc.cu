@@ -66,8 +66,9 @@ build_gated_tc_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     using G = Geo<KIND>;
     constexpr int C = G::C;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    // 1024-aligned base, derived by offsetting the shared array itself so that the
+    // compiler keeps the shared address space (plain ld/st.shared, not generic accesses)
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ Bars bars;
     __shared__ uint32_t tslot;
     __shared__ volatile int abort_flag;

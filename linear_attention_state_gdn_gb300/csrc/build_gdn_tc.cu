@@ -56,10 +56,15 @@ constexpr uint32_t kOffAD = kOffAX + 65536;           // D'^T bf16, 256 rows x 1
 constexpr uint32_t kOffBW = kOffAD + 32768;           // W, MN-major: 128 rows i x 128 B
 constexpr uint32_t kOffMp = kOffBW + 16384;           // M Diag(b e^c): 64 rows t x 128 B
 constexpr uint32_t kOffMpp = kOffMp + 8192;           // M Diag(b)
-constexpr uint32_t kOffA32 = kOffMpp + 8192;          // fp32 A, 64 x 64
-constexpr uint32_t kOffVec = kOffA32 + 16384;         // per-chunk vectors (2 slots)
+constexpr uint32_t kLDA = 68;                         // padded row stride of the fp32 A (16-B rows)
+constexpr uint32_t kOffA32 = kOffMpp + 8192;          // fp32 A, 64 x 65
+constexpr uint32_t kOffT = kOffA32 + 64 * kLDA * 4;   // fp32 block products, 3 x 16 x 16
+constexpr uint32_t kOffVec = kOffT + 3 * 256 * 4;     // per-chunk vectors (2 slots)
 constexpr uint32_t kVecSlot = 5 * C * 4 + 16;
 constexpr uint32_t kSmemBytes = kOffVec + 2 * kVecSlot + 1024;
+// M = (I + A)^-1 is formed in fp32 in the 16 KB spanned by the M Diag(b e^c) / M Diag(b)
+// tiles (free then: the MMAs of the previous chunk that read them have completed) and
+// converted in place once complete.
 
 constexpr uint32_t kTZ = 0, kTX = 256, kTGW = 384, kTU = 448;
 
@@ -78,12 +83,76 @@ __device__ __forceinline__ void bar_prep() { asm volatile("bar.sync 1, 128;" :::
 
 __device__ __forceinline__ uint32_t bf2(float lo, float hi) { return pack_bf16x2(lo, hi); }
 
+// One level of the blocked inverse M = (I + A)^-1 (64 x 64, 16 x 16 blocks): the NB = 4 - L
+// blocks (a, b) with a - b = L, from M_ab = -M_aa sum_{k=b}^{a-1} A_ak M_kb. Prep thread q
+// owns entries (row r0 + 8h, column j) of every block, r0 = q / 16, j = q % 16, h = 0, 1;
+// all loops are compile-time so the independent dot products interleave.
+template <int L>
+__device__ __forceinline__ void inverse_level(const float *A32, float *M32, float *T32, int q) {
+    constexpr int NB = 4 - L;
+    const int j = q & 15, r0 = q >> 4;
+    float t[2 * NB];
+#pragma unroll
+    for (int m = 0; m < 2 * NB; ++m) t[m] = 0.f;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+#pragma unroll
+        for (int k = b; k < b + L; ++k) {
+            float mc[16];
+#pragma unroll
+            for (int s = 0; s < 16; ++s) mc[s] = M32[(16 * k + s) * C + 16 * b + j];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float4 *ar = reinterpret_cast<const float4 *>(A32 + (16 * (b + L) + r0 + 8 * hh) * kLDA + 16 * k);
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    const float4 x = ar[s4];
+                    float &acc = t[2 * b + hh];
+                    acc = fmaf(x.x, mc[4 * s4 + 0], acc);
+                    acc = fmaf(x.y, mc[4 * s4 + 1], acc);
+                    acc = fmaf(x.z, mc[4 * s4 + 2], acc);
+                    acc = fmaf(x.w, mc[4 * s4 + 3], acc);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) T32[b * 256 + (r0 + 8 * hh) * 16 + j] = t[2 * b + hh];
+    bar_prep();
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        const int a = b + L;
+        float tc[16];
+#pragma unroll
+        for (int s = 0; s < 16; ++s) tc[s] = T32[b * 256 + s * 16 + j];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int r = r0 + 8 * hh;
+            const float4 *mr = reinterpret_cast<const float4 *>(M32 + (16 * a + r) * C + 16 * a);
+            float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+                const float4 x = mr[s4];
+                acc0 = fmaf(x.x, tc[4 * s4 + 0], acc0);
+                acc1 = fmaf(x.y, tc[4 * s4 + 1], acc1);
+                acc0 = fmaf(x.z, tc[4 * s4 + 2], acc0);
+                acc1 = fmaf(x.w, tc[4 * s4 + 3], acc1);
+            }
+            M32[(16 * a + r) * C + 16 * b + j] = -(acc0 + acc1);
+        }
+    }
+    bar_prep();
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~uintptr_t(1023));
+    // 1024-aligned base, derived by offsetting the shared array itself so that the
+    // compiler keeps the shared address space (plain ld/st.shared, not generic accesses)
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ Bars bars;
     __shared__ uint32_t tslot;
     __shared__ volatile int abort_flag;
@@ -225,6 +294,15 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
         const int q = threadIdx.x - 128;          // 0..127
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         float *A32 = reinterpret_cast<float *>(smem + kOffA32);
+        float *M32 = reinterpret_cast<float *>(smem + kOffMp);
+        float *T32 = reinterpret_cast<float *>(smem + kOffT);
+        float b_next = 0.f, la_next = 0.f;   // gates of the next chunk (thread q < 64: token q)
+        if (q < C && nch > 0) {
+            const int64_t tok = (int64_t)seg.start + q;
+            const bool in = q < min(C, seg.len);
+            b_next = in ? p.beta[tok * p.H_v + h] : 0.f;
+            la_next = (in && gdn) ? p.log_gate[tok * p.H_v + h] : 0.f;
+        }
         // one elected thread waits; the outcome reaches the other 127 through the named
         // barrier, so every prep thread takes the same branch (no thread is left behind
         // at a barrier when a wait gives up)
@@ -239,22 +317,25 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
         };
         for (int c = 0; c < nch; ++c) {   // leaves only through a broadcast pwait outcome
             Vec &v = vec[c & 1];
-            // (a) gates of chunk c. The slot was last read by the chain for chunk c-2, which
-            //     finished before W of chunk c-1 was issued (waited on in (d) below).
+            // (a) gates of chunk c (loaded one chunk ahead into registers), prefix sums
             const int valid = min(C, seg.len - c * C);
+            float b_cur = b_next, la_cur = la_next;
+            if (q < C && c + 1 < nch) {   // next chunk's gates: latency hidden behind this one
+                const int64_t tok = (int64_t)seg.start + (c + 1) * C + q;
+                const bool in = q < min(C, seg.len - (c + 1) * C);
+                b_next = in ? p.beta[tok * p.H_v + h] : 0.f;
+                la_next = (in && gdn) ? p.log_gate[tok * p.H_v + h] : 0.f;
+            }
             if (q < C) {
-                const int64_t tok = (int64_t)seg.start + c * C + q;
-                const bool in = q < valid;
-                const float b = in ? p.beta[tok * p.H_v + h] : 0.f;
-                const float la = (in && gdn) ? p.log_gate[tok * p.H_v + h] : 0.f;
-                float x = la;
+                if (q >= valid) b_cur = la_cur = 0.f;
+                float x = la_cur;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const float y = __shfl_up_sync(0xffffffffu, x, o);
                     if (lane >= o) x += y;
                 }
                 if (lane == 31) scan_tmp[q >> 5] = x;
-                v.beta[q] = b;
+                v.beta[q] = b_cur;
                 v.c[q] = x;   // finished below for the upper half
             }
             bar_prep();
@@ -269,7 +350,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                     if (cc < kMinChunkLogDecay) atomicOr(p.err, kErrRange);
                 }
             }
-            // (b) gram -> A (rows t = 16 (warp - 4) + lane for lanes < 16)
+            // (b) gram -> A (rows t = 16 (warp - 4) + lane for lanes < 16), padded rows
             if (!pwait(&bars.gfull, c & 1)) break;
             tc_fence_after();
             {
@@ -279,45 +360,59 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 tmem_ld32(tmem + lane_off + kTGW + 32, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
                 tmem_ld_wait();
                 if (lane < 16) {
-                    const float bt = v.beta[t], et = v.ecp[t];
-                    float4 *row = reinterpret_cast<float4 *>(A32 + t * C);
+                    const float bt = v.beta[t] * v.ecp[t];
+                    float *row = A32 + t * kLDA;
 #pragma unroll
-                    for (int s = 0; s < C; s += 4) {
-                        float4 a;
-                        a.x = s + 0 < t ? bt * __uint_as_float(g[s + 0]) * et * v.ecm[s + 0] : 0.f;
-                        a.y = s + 1 < t ? bt * __uint_as_float(g[s + 1]) * et * v.ecm[s + 1] : 0.f;
-                        a.z = s + 2 < t ? bt * __uint_as_float(g[s + 2]) * et * v.ecm[s + 2] : 0.f;
-                        a.w = s + 3 < t ? bt * __uint_as_float(g[s + 3]) * et * v.ecm[s + 3] : 0.f;
-                        row[s / 4] = a;
-                    }
+                    for (int s2 = 0; s2 < C; ++s2)
+                        row[s2] = s2 < t ? bt * __uint_as_float(g[s2]) * v.ecm[s2] : 0.f;
                 }
             }
             tc_fence_before();
             bar_prep();
-            // (c) M = (I + A)^-1 by column forward substitution (thread q < 64: column q),
-            //     then M Diag(b e^c) and M Diag(b) as bf16 K-major rows
+            // (c) M = (I + A)^-1 by 16 x 16 blocks: diagonal blocks by forward substitution
+            //     (thread = one column of one block), then the blocks below the diagonal level
+            //     by level, M_ab = -M_aa sum_{k=b}^{a-1} A_ak M_kb (independent dot products).
             if (q < C) {
-                float x[C];
+                const int a = q >> 4, j = q & 15;
+                float x[16];
 #pragma unroll
-                for (int t = 0; t < C; ++t) {
-                    float acc = (t == q) ? 1.f : 0.f;
-                    const float4 *row = reinterpret_cast<const float4 *>(A32 + t * C);
+                for (int r = 0; r < 16; ++r) {
+                    const float *Ar = A32 + (16 * a + r) * kLDA + 16 * a;
+                    float acc0 = (r == j) ? 1.f : 0.f, acc1 = 0.f;
 #pragma unroll
-                    for (int r = 0; r < t; r += 4) {
-                        const float4 a = row[r / 4];
-                        acc = fmaf(-a.x, x[r], acc);
-                        if (r + 1 < t) acc = fmaf(-a.y, x[r + 1], acc);
-                        if (r + 2 < t) acc = fmaf(-a.z, x[r + 2], acc);
-                        if (r + 3 < t) acc = fmaf(-a.w, x[r + 3], acc);
+                    for (int s2 = 0; s2 < r; ++s2) {
+                        if (s2 & 1) acc1 = fmaf(-Ar[s2], x[s2], acc1);
+                        else acc0 = fmaf(-Ar[s2], x[s2], acc0);
                     }
-                    x[t] = acc;
+                    x[r] = acc0 + acc1;
                 }
-                const float s1 = v.bec[q], s2 = v.beta[q];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) M32[(16 * a + r) * C + 16 * a + j] = x[r];
+            } else {
+                // zero the six blocks above the diagonal
+                for (int e = q - C; e < 6 * 256; e += C) {
+                    const int blk = e >> 8, r = (e >> 4) & 15, j = e & 15;
+                    const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                    const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                    M32[(16 * a + r) * C + 16 * b + j] = 0.f;
+                }
+            }
+            bar_prep();
+            inverse_level<1>(A32, M32, T32, q);
+            inverse_level<2>(A32, M32, T32, q);
+            inverse_level<3>(A32, M32, T32, q);
+            // M Diag(b e^c) and M Diag(b) as bf16 K-major rows t, in place of M
+            {
+                float mv[32];
+#pragma unroll
+                for (int m = 0; m < 32; ++m) mv[m] = M32[q + 128 * m];
+                bar_prep();
                 uint8_t *mp = smem + kOffMp, *mpp = smem + kOffMpp;
 #pragma unroll
-                for (int t = 0; t < C; ++t) {
-                    *reinterpret_cast<__nv_bfloat16 *>(mp + sw128(t, 2 * q)) = __float2bfloat16(x[t] * s1);
-                    *reinterpret_cast<__nv_bfloat16 *>(mpp + sw128(t, 2 * q)) = __float2bfloat16(x[t] * s2);
+                for (int m = 0; m < 32; ++m) {
+                    const int e = q + 128 * m, t = e >> 6, s2 = e & 63;
+                    *reinterpret_cast<__nv_bfloat16 *>(mp + sw128(t, 2 * s2)) = __float2bfloat16(mv[m] * v.bec[s2]);
+                    *reinterpret_cast<__nv_bfloat16 *>(mpp + sw128(t, 2 * s2)) = __float2bfloat16(mv[m] * v.beta[s2]);
                 }
             }
             fence_async_shared();
@@ -380,29 +475,30 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-                for (int c0 = 0; c0 < 128; c0 += 16) {
-                    uint32_t z[16];
-                    tmem_ld16(tmem + lane_off + kTZ + 128 * hf + c0, z);
+                for (int cb = 0; cb < 2; ++cb) {   // 64 key rows per batch: K-block cb
+                    uint32_t z[64];
+                    const uint32_t col = kTZ + 128 * hf + 64 * cb;
+                    tmem_ld32(tmem + lane_off + col, *reinterpret_cast<uint32_t(*)[32]>(&z[0]));
+                    tmem_ld32(tmem + lane_off + col + 32, *reinterpret_cast<uint32_t(*)[32]>(&z[32]));
                     tmem_ld_wait();
                     if (hf == 0 && renorm) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) z[j] = __float_as_uint(__uint_as_float(z[j]) * sc);
-                        tmem_st16(tmem + lane_off + kTZ + c0, z);
+                        for (int j = 0; j < 64; ++j) z[j] = __float_as_uint(__uint_as_float(z[j]) * sc);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            tmem_st16(tmem + lane_off + col + 16 * j, *reinterpret_cast<uint32_t(*)[16]>(&z[16 * j]));
                     }
-                    uint4 lo, hi;
-                    lo.x = bf2(__uint_as_float(z[0]), __uint_as_float(z[1]));
-                    lo.y = bf2(__uint_as_float(z[2]), __uint_as_float(z[3]));
-                    lo.z = bf2(__uint_as_float(z[4]), __uint_as_float(z[5]));
-                    lo.w = bf2(__uint_as_float(z[6]), __uint_as_float(z[7]));
-                    hi.x = bf2(__uint_as_float(z[8]), __uint_as_float(z[9]));
-                    hi.y = bf2(__uint_as_float(z[10]), __uint_as_float(z[11]));
-                    hi.z = bf2(__uint_as_float(z[12]), __uint_as_float(z[13]));
-                    hi.w = bf2(__uint_as_float(z[14]), __uint_as_float(z[15]));
-                    // row (128 hf + n) of the K-major tile, key rows c0..c0+15 in K-block c0 / 64
-                    uint8_t *rowb = ax + (c0 >> 6) * 32768;
-                    const uint32_t r = 128 * hf + n, b = (c0 & 63) * 2;
-                    *reinterpret_cast<uint4 *>(rowb + sw128(r, b)) = lo;
-                    *reinterpret_cast<uint4 *>(rowb + sw128(r, b + 16)) = hi;
+                    uint8_t *rowb = ax + cb * 32768;
+                    const uint32_t r = 128 * hf + n;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint4 pk;
+                        pk.x = bf2(__uint_as_float(z[8 * j + 0]), __uint_as_float(z[8 * j + 1]));
+                        pk.y = bf2(__uint_as_float(z[8 * j + 2]), __uint_as_float(z[8 * j + 3]));
+                        pk.z = bf2(__uint_as_float(z[8 * j + 4]), __uint_as_float(z[8 * j + 5]));
+                        pk.w = bf2(__uint_as_float(z[8 * j + 6]), __uint_as_float(z[8 * j + 7]));
+                        *reinterpret_cast<uint4 *>(rowb + sw128(r, 16 * j)) = pk;
+                    }
                 }
             }
             if (renorm) {
@@ -419,29 +515,28 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             const float cC = v.cC;
             const float eL = expf(-Lam);
 #pragma unroll
-            for (int c0 = 0; c0 < C; c0 += 16) {
-                uint32_t xs[16], xp[16], u[16];
-                tmem_ld16(tmem + lane_off + kTX + c0, xs);
-                tmem_ld16(tmem + lane_off + kTX + 64 + c0, xp);
-                tmem_ld16(tmem + lane_off + kTU + c0, u);
+            for (int c0 = 0; c0 < C; c0 += 32) {
+                uint32_t xs[32], xp[32], u[32];
+                tmem_ld32(tmem + lane_off + kTX + c0, xs);
+                tmem_ld32(tmem + lane_off + kTX + 64 + c0, xp);
+                tmem_ld32(tmem + lane_off + kTU + c0, u);
                 tmem_ld_wait();
-                float ds[16], dp[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float e = v.ecm[c0 + j];
-                    ds[j] = e * fmaf(eL, __uint_as_float(u[j]), -__uint_as_float(xs[j]));
-                    dp[j] = -e * __uint_as_float(xp[j]);
+                for (int j8 = 0; j8 < 4; ++j8) {
+                    float ds[8], dp[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int jj = 8 * j8 + j;
+                        const float e = v.ecm[c0 + jj];
+                        ds[j] = e * fmaf(eL, __uint_as_float(u[jj]), -__uint_as_float(xs[jj]));
+                        dp[j] = -e * __uint_as_float(xp[jj]);
+                    }
+                    const uint32_t bo = (c0 + 8 * j8) * 2;
+                    *reinterpret_cast<uint4 *>(ad + sw128(n, bo)) =
+                        make_uint4(bf2(ds[0], ds[1]), bf2(ds[2], ds[3]), bf2(ds[4], ds[5]), bf2(ds[6], ds[7]));
+                    *reinterpret_cast<uint4 *>(ad + sw128(128 + n, bo)) =
+                        make_uint4(bf2(dp[0], dp[1]), bf2(dp[2], dp[3]), bf2(dp[4], dp[5]), bf2(dp[6], dp[7]));
                 }
-                uint4 a, b2, d, e2;
-                a = make_uint4(bf2(ds[0], ds[1]), bf2(ds[2], ds[3]), bf2(ds[4], ds[5]), bf2(ds[6], ds[7]));
-                b2 = make_uint4(bf2(ds[8], ds[9]), bf2(ds[10], ds[11]), bf2(ds[12], ds[13]), bf2(ds[14], ds[15]));
-                d = make_uint4(bf2(dp[0], dp[1]), bf2(dp[2], dp[3]), bf2(dp[4], dp[5]), bf2(dp[6], dp[7]));
-                e2 = make_uint4(bf2(dp[8], dp[9]), bf2(dp[10], dp[11]), bf2(dp[12], dp[13]), bf2(dp[14], dp[15]));
-                const uint32_t bo = c0 * 2;
-                *reinterpret_cast<uint4 *>(ad + sw128(n, bo)) = a;
-                *reinterpret_cast<uint4 *>(ad + sw128(n, bo + 16)) = b2;
-                *reinterpret_cast<uint4 *>(ad + sw128(128 + n, bo)) = d;
-                *reinterpret_cast<uint4 *>(ad + sw128(128 + n, bo + 16)) = e2;
             }
             fence_async_shared();
             tc_fence_before();
