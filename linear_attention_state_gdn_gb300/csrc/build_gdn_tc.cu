@@ -10,23 +10,26 @@
 //
 // Chunked form (exact algebra, chunks of C = 64 tokens, c_t = sum_{s<=t} log a_s inside
 // the chunk, A_ts = b_t (k_t . k_s) exp(c_t - c_s) for s < t, M = (I + A)^-1):
-//     W = M Diag(b e^c) K,  U = M Diag(b) V,  X = W [S | P],
-//     S <- e^{c_C} (S + K^T Diag(e^-c) (U - X_S)),   P <- P - K^T Diag(e^-c) X_P.
-// The state is carried as Z = [S~ | P] with S = exp(Lam) S~ (Lam a running log-scale,
-// renormalised into S~ when it drops below -20), so every chunk only adds to Z:
-//     Z <- Z + K^T D',   D' = Diag(e^-c) [exp(-Lam) U - X_S | -X_P].
+//     S <- e^{c_C} (S + K^T Diag(e^-c) M Diag(b) (V - Diag(e^c) K S)),
+//     P <- P - K^T Diag(e^-c) M Diag(b e^c) K P,
+// i.e. with Y = K [S | P] and R = Diag(b) [V - Diag(e^c) Y_S | -Diag(e^c) Y_P] every chunk
+// adds K^T Diag(e^-c) M R to the state. The state is carried as Z = [S~ | P] with
+// S = exp(Lam) S~ (Lam a running log-scale, folded into S~ when it drops below -20):
+//     Y = K Z,  R = Diag(b) [exp(-Lam) V - Diag(e^c) Y_S | -Diag(e^c) Y_P],
+//     Z <- Z + K^T D',  D' = Diag(e^-c) M R.
+// Only M depends on the chunk's gram; everything that touches the state is three MMAs
+// (Y, M R, K^T D') plus two per-lane transforms.
 //
-// Layout (one CTA = one (segment, value head) unit, 320 threads, all 512 TMEM columns):
-//   TMEM  Z^T   [0,256)   lane = state column n (S~ half, then P half), column = key row i
-//         X^T   [256,384) lane n, column t          (X^T = Z^T W^T, two M = 128 halves)
-//         G/W^T [384,448) gram (M = 64 layout), then W^T (lane i, column t)
-//         U^T   [448,512) lane n, column t
-//   SMEM  two TMA stages of (k, v) chunks (128B-swizzled, channels contiguous), the bf16 A
-//         operands Z^T and D'^T (K-major), W (MN-major), M Diag(b e^c) and M Diag(b)
-//         (K-major), the fp32 A matrix for the inversion, per-chunk gate vectors.
-// Roles: warps 0-3 carry the chain (Z^T -> bf16, D' formation; thread n = TMEM lane n),
-// warps 4-7 prepare the next chunk (gates, A, M by column forward substitution in fp32,
-// W^T -> W), warp 8 issues TMA, warp 9 issues the MMAs. Every wait is bounded.
+// Layout (one CTA = one (segment, value head) unit, 320 threads):
+//   TMEM  Z^T      [0,256)   lane = state column n (S~ half, then P half), column = key row i
+//         Y^T/D^T  [256,384) lane n, column t: Y^T = Z^T K^T, then (M R)^T in the same place
+//         G        [384,512) two gram slots (M = 64 layout), one per chunk parity
+//   SMEM  two TMA stages of (k, v) chunks (128B-swizzled, channels contiguous); the bf16
+//         K-major operands Z^T (A of Y), R^T then D'^T (A of M R, then of the update) and M
+//         (B of M R); the fp32 A and M of the inversion; per-chunk gate vectors (3 slots).
+// Roles: warps 0-3 carry the chain (Z^T -> bf16, R, D'; thread n = TMEM lane n), warps 4-7
+// prepare M for the next chunk (gates, A from the gram, 16 x 16-blocked inverse in fp32),
+// warp 8 issues TMA, warp 9 issues the MMAs. Every wait is bounded.
 #include <algorithm>
 
 #include "internal.cuh"
@@ -51,32 +54,28 @@ constexpr float kMinChunkLogDecay = -60.f;
 constexpr uint32_t kKTile = C * 256;                  // k chunk: two 64-channel halves, 16 KB
 constexpr uint32_t kStage = 2 * kKTile;               // k + v
 constexpr uint32_t kOffStage = 0;                     // 2 stages: 64 KB
-constexpr uint32_t kOffAX = 2 * kStage;               // Z^T bf16, 2 K-blocks x 256 rows x 128 B
-constexpr uint32_t kOffAD = kOffAX + 65536;           // D'^T bf16, 256 rows x 128 B
-constexpr uint32_t kOffBW = kOffAD + 32768;           // W, MN-major: 128 rows i x 128 B
-constexpr uint32_t kOffMp = kOffBW + 16384;           // M Diag(b e^c): 64 rows t x 128 B
-constexpr uint32_t kOffMpp = kOffMp + 8192;           // M Diag(b)
+constexpr uint32_t kOffAZ = 2 * kStage;               // Z^T bf16, 2 K-blocks x 256 rows x 128 B
+constexpr uint32_t kOffAR = kOffAZ + 65536;           // R^T / D'^T bf16, 256 rows x 128 B
+constexpr uint32_t kOffBM = kOffAR + 32768;           // M bf16, 64 rows t x 128 B
 constexpr uint32_t kLDA = 68;                         // padded row stride of the fp32 A (16-B rows)
-constexpr uint32_t kOffA32 = kOffMpp + 8192;          // fp32 A, 64 x 65
-constexpr uint32_t kOffT = kOffA32 + 64 * kLDA * 4;   // fp32 block products, 3 x 16 x 16
-constexpr uint32_t kOffVec = kOffT + 3 * 256 * 4;     // per-chunk vectors (2 slots)
-constexpr uint32_t kVecSlot = 5 * C * 4 + 16;
-constexpr uint32_t kSmemBytes = kOffVec + 2 * kVecSlot + 1024;
-// M = (I + A)^-1 is formed in fp32 in the 16 KB spanned by the M Diag(b e^c) / M Diag(b)
-// tiles (free then: the MMAs of the previous chunk that read them have completed) and
-// converted in place once complete.
+constexpr uint32_t kOffA32 = kOffBM + 8192;           // fp32 A, 64 x 68
+constexpr uint32_t kOffM32 = kOffA32 + 64 * kLDA * 4; // fp32 M, 64 x 64
+constexpr uint32_t kOffT = kOffM32 + 64 * 64 * 4;     // fp32 block products, 3 x 16 x 16
+constexpr uint32_t kOffVec = kOffT + 3 * 256 * 4;     // per-chunk vectors (3 slots)
 
-constexpr uint32_t kTZ = 0, kTX = 256, kTGW = 384, kTU = 448;
+constexpr uint32_t kTZ = 0, kTY = 256, kTG = 384;
 
 struct Vec {   // one slot of per-chunk vectors
     float beta[C], c[C], ecp[C], ecm[C], bec[C];
     float cC;  // chunk total log decay
     float pad[3];
 };
+constexpr uint32_t kSmemBytes = kOffVec + 3 * sizeof(Vec) + 1024;
 
 struct Bars {
     uint64_t kv_full[2], kv_empty[2];
-    uint64_t gfull, mready, wfull, wready, zbf_ready, xfull, dready, zfull, fin;
+    uint64_t gfull[2];   // one per gram slot, so a wait can never alias a later phase
+    uint64_t vready, mready, zbf_ready, yfull, rready, dfull, dready, zfull, fin;
 };
 
 __device__ __forceinline__ void bar_prep() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -121,6 +120,7 @@ __device__ __forceinline__ void inverse_level(const float *A32, float *M32, floa
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) T32[b * 256 + (r0 + 8 * hh) * 16 + j] = t[2 * b + hh];
     bar_prep();
+    float res[2 * NB];   // all loads first, then the stores (no load/store interleaving)
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
         const int a = b + L;
@@ -140,9 +140,13 @@ __device__ __forceinline__ void inverse_level(const float *A32, float *M32, floa
                 acc0 = fmaf(x.z, tc[4 * s4 + 2], acc0);
                 acc1 = fmaf(x.w, tc[4 * s4 + 3], acc1);
             }
-            M32[(16 * a + r) * C + 16 * b + j] = -(acc0 + acc1);
+            res[2 * b + hh] = -(acc0 + acc1);
         }
     }
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) M32[(16 * (b + L) + r0 + 8 * hh) * C + 16 * b + j] = res[2 * b + hh];
     bar_prep();
 }
 
@@ -172,12 +176,14 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             mbar_init(&bars.kv_full[s], 1);
             mbar_init(&bars.kv_empty[s], 1);
         }
-        mbar_init(&bars.gfull, 1);
+        mbar_init(&bars.gfull[0], 1);
+        mbar_init(&bars.gfull[1], 1);
+        mbar_init(&bars.vready, 128);
         mbar_init(&bars.mready, 128);
-        mbar_init(&bars.wfull, 1);
-        mbar_init(&bars.wready, 128);
         mbar_init(&bars.zbf_ready, 128);
-        mbar_init(&bars.xfull, 1);
+        mbar_init(&bars.yfull, 1);
+        mbar_init(&bars.rready, 128);
+        mbar_init(&bars.dfull, 1);
         mbar_init(&bars.dready, 128);
         mbar_init(&bars.zfull, 1);
         mbar_init(&bars.fin, 1);
@@ -218,71 +224,63 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0 && nch > 0) {
             constexpr uint32_t idG = idesc(kFmtBF16, kFmtBF16, false, false, 64, 64);
-            constexpr uint32_t idWU = idesc(kFmtBF16, kFmtBF16, true, false, 128, 64);
-            constexpr uint32_t idX = idesc(kFmtBF16, kFmtBF16, false, true, 128, 64);
+            constexpr uint32_t idKK = idesc(kFmtBF16, kFmtBF16, false, false, 128, 64);
             constexpr uint32_t idZ = idesc(kFmtBF16, kFmtBF16, false, true, 128, 128);
             const uint32_t sb = smem_u32(smem);
             auto issue_gram = [&](int c) -> bool {
                 if (!wait(&bars.kv_full[c & 1], (c >> 1) & 1)) return false;
-                if (c >= 1 && !wait(&bars.wready, (c - 1) & 1)) return false;   // G/W slot free
                 tc_fence_after();
                 const uint32_t k = sb + kOffStage + (c & 1) * kStage;
 #pragma unroll
                 for (int s = 0; s < 8; ++s) {
                     const uint32_t a = k + (s >> 2) * (kKTile / 2) + (s & 3) * 32;
-                    mma_bf16(tmem + kTGW, sdesc(a, 16, 1024, kSwizzle128B),
+                    mma_bf16(tmem + kTG + 64 * (c & 1), sdesc(a, 16, 1024, kSwizzle128B),
                              sdesc(a, 16, 1024, kSwizzle128B), idG, s > 0);
                 }
-                mma_commit(&bars.gfull);
+                mma_commit(&bars.gfull[c & 1]);
                 return true;
             };
-            auto issue_wu = [&](int c) -> bool {
-                if (!wait(&bars.mready, c & 1)) return false;
-                if (c >= 1 && !wait(&bars.dready, (c - 1) & 1)) return false;   // U slot free
-                tc_fence_after();
-                const uint32_t k = sb + kOffStage + (c & 1) * kStage, v = k + kKTile;
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_bf16(tmem + kTGW, sdesc(k + s * 2048, kKTile / 2, 1024, kSwizzle128B),
-                             sdesc(sb + kOffMp + s * 32, 16, 1024, kSwizzle128B), idWU, s > 0);
-#pragma unroll
-                for (int s = 0; s < 4; ++s)
-                    mma_bf16(tmem + kTU, sdesc(v + s * 2048, kKTile / 2, 1024, kSwizzle128B),
-                             sdesc(sb + kOffMpp + s * 32, 16, 1024, kSwizzle128B), idWU, s > 0);
-                mma_commit(&bars.wfull);
-                return true;
-            };
-            bool ok = issue_gram(0) && issue_wu(0);
+            bool ok = issue_gram(0);
             for (int c = 0; ok && c < nch; ++c) {
-                // X^T = Z^T W^T for the S~ and P halves
-                ok = wait(&bars.wready, c & 1) && wait(&bars.zbf_ready, c & 1);
-                if (!ok) break;
+                const uint32_t k = sb + kOffStage + (c & 1) * kStage;
+                // Y^T = Z^T K^T (S~ and P halves)
+                if (!(ok = wait(&bars.zbf_ready, c & 1))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
                     for (int s = 0; s < 8; ++s) {
-                        const uint32_t a = sb + kOffAX + (s >> 2) * 32768 + hf * 16384 + (s & 3) * 32;
-                        const uint32_t b = sb + kOffBW + s * 2048;
-                        mma_bf16(tmem + kTX + 64 * hf, sdesc(a, 16, 1024, kSwizzle128B),
-                                 sdesc(b, 8192, 1024, kSwizzle128B), idX, s > 0);
+                        const uint32_t a = sb + kOffAZ + (s >> 2) * 32768 + hf * 16384 + (s & 3) * 32;
+                        const uint32_t b = k + (s >> 2) * (kKTile / 2) + (s & 3) * 32;
+                        mma_bf16(tmem + kTY + 64 * hf, sdesc(a, 16, 1024, kSwizzle128B),
+                                 sdesc(b, 16, 1024, kSwizzle128B), idKK, s > 0);
                     }
-                mma_commit(&bars.xfull);
+                mma_commit(&bars.yfull);
+                // the next chunk's gram, into the other slot
                 if (c + 1 < nch && !(ok = issue_gram(c + 1))) break;
+                // (M R)^T = R^T M^T
+                if (!(ok = wait(&bars.rready, c & 1) && wait(&bars.mready, c & 1))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        mma_bf16(tmem + kTY + 64 * hf,
+                                 sdesc(sb + kOffAR + hf * 16384 + s * 32, 16, 1024, kSwizzle128B),
+                                 sdesc(sb + kOffBM + s * 32, 16, 1024, kSwizzle128B), idKK, s > 0);
+                mma_commit(&bars.dfull);
                 // Z^T += D'^T K
                 if (!(ok = wait(&bars.dready, c & 1))) break;
                 tc_fence_after();
-                const uint32_t k = sb + kOffStage + (c & 1) * kStage;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
                         mma_bf16(tmem + kTZ + 128 * hf,
-                                 sdesc(sb + kOffAD + hf * 16384 + s * 32, 16, 1024, kSwizzle128B),
+                                 sdesc(sb + kOffAR + hf * 16384 + s * 32, 16, 1024, kSwizzle128B),
                                  sdesc(k + s * 2048, kKTile / 2, 1024, kSwizzle128B), idZ, 1);
                 mma_commit(&bars.zfull);
                 mma_commit(&bars.kv_empty[c & 1]);
-                if (c + 1 < nch && !(ok = issue_wu(c + 1))) break;
             }
             if (abort_flag) {
                 mma_commit(&bars.fin);
@@ -294,7 +292,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
         const int q = threadIdx.x - 128;          // 0..127
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         float *A32 = reinterpret_cast<float *>(smem + kOffA32);
-        float *M32 = reinterpret_cast<float *>(smem + kOffMp);
+        float *M32 = reinterpret_cast<float *>(smem + kOffM32);
         float *T32 = reinterpret_cast<float *>(smem + kOffT);
         float b_next = 0.f, la_next = 0.f;   // gates of the next chunk (thread q < 64: token q)
         if (q < C && nch > 0) {
@@ -316,11 +314,12 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             return r;
         };
         for (int c = 0; c < nch; ++c) {   // leaves only through a broadcast pwait outcome
-            Vec &v = vec[c & 1];
-            // (a) gates of chunk c (loaded one chunk ahead into registers), prefix sums
+            // (a) gates of chunk c (loaded one chunk ahead into registers), prefix sums.
+            //     Slot c % 3 was last read by the chain for chunk c - 3, long finished.
+            Vec &v = vec[c % 3];
             const int valid = min(C, seg.len - c * C);
             float b_cur = b_next, la_cur = la_next;
-            if (q < C && c + 1 < nch) {   // next chunk's gates: latency hidden behind this one
+            if (q < C && c + 1 < nch) {
                 const int64_t tok = (int64_t)seg.start + (c + 1) * C + q;
                 const bool in = q < min(C, seg.len - (c + 1) * C);
                 b_next = in ? p.beta[tok * p.H_v + h] : 0.f;
@@ -336,55 +335,76 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 }
                 if (lane == 31) scan_tmp[q >> 5] = x;
                 v.beta[q] = b_cur;
-                v.c[q] = x;   // finished below for the upper half
+                v.c[q] = x;
             }
             bar_prep();
             if (q < C) {
                 const float cc = q >= 32 ? v.c[q] + scan_tmp[0] : v.c[q];
+                const float e = expf(cc);
                 v.c[q] = cc;
-                v.ecp[q] = expf(cc);
+                v.ecp[q] = e;
                 v.ecm[q] = expf(-cc);
-                v.bec[q] = v.beta[q] * expf(cc);
+                v.bec[q] = v.beta[q] * e;
                 if (q == C - 1) {
                     v.cC = cc;
                     if (cc < kMinChunkLogDecay) atomicOr(p.err, kErrRange);
                 }
             }
+            mbar_arrive(&bars.vready);
             // (b) gram -> A (rows t = 16 (warp - 4) + lane for lanes < 16), padded rows
-            if (!pwait(&bars.gfull, c & 1)) break;
+            if (!pwait(&bars.gfull[c & 1], (c >> 1) & 1)) break;
             tc_fence_after();
             {
                 const int t = 16 * (warp - kPrepWarp0) + lane;
                 uint32_t g[64];
-                tmem_ld32(tmem + lane_off + kTGW, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
-                tmem_ld32(tmem + lane_off + kTGW + 32, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
+                const uint32_t gcol = kTG + 64 * (c & 1);
+                tmem_ld32(tmem + lane_off + gcol, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
+                tmem_ld32(tmem + lane_off + gcol + 32, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
                 tmem_ld_wait();
                 if (lane < 16) {
+                    // all loads before any store (stores to A may not pass loads from the
+                    // same shared memory, so interleaving them would serialise the loop)
                     const float bt = v.beta[t] * v.ecp[t];
-                    float *row = A32 + t * kLDA;
+                    float em[C];
 #pragma unroll
-                    for (int s2 = 0; s2 < C; ++s2)
-                        row[s2] = s2 < t ? bt * __uint_as_float(g[s2]) * v.ecm[s2] : 0.f;
+                    for (int s4 = 0; s4 < C / 4; ++s4) {
+                        const float4 e4 = reinterpret_cast<const float4 *>(v.ecm)[s4];
+                        em[4 * s4] = e4.x, em[4 * s4 + 1] = e4.y, em[4 * s4 + 2] = e4.z, em[4 * s4 + 3] = e4.w;
+                    }
+                    float4 *row = reinterpret_cast<float4 *>(A32 + t * kLDA);
+#pragma unroll
+                    for (int s4 = 0; s4 < C / 4; ++s4) {
+                        float4 a4;
+                        const int s2 = 4 * s4;
+                        a4.x = s2 + 0 < t ? bt * __uint_as_float(g[s2 + 0]) * em[s2 + 0] : 0.f;
+                        a4.y = s2 + 1 < t ? bt * __uint_as_float(g[s2 + 1]) * em[s2 + 1] : 0.f;
+                        a4.z = s2 + 2 < t ? bt * __uint_as_float(g[s2 + 2]) * em[s2 + 2] : 0.f;
+                        a4.w = s2 + 3 < t ? bt * __uint_as_float(g[s2 + 3]) * em[s2 + 3] : 0.f;
+                        row[s4] = a4;
+                    }
                 }
             }
             tc_fence_before();
             bar_prep();
             // (c) M = (I + A)^-1 by 16 x 16 blocks: diagonal blocks by forward substitution
-            //     (thread = one column of one block), then the blocks below the diagonal level
-            //     by level, M_ab = -M_aa sum_{k=b}^{a-1} A_ak M_kb (independent dot products).
+            //     (thread = one column of one block, each row's A entries loaded ahead),
+            //     then the blocks below the diagonal level by level.
             if (q < C) {
                 const int a = q >> 4, j = q & 15;
                 float x[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
-                    const float *Ar = A32 + (16 * a + r) * kLDA + 16 * a;
-                    float acc0 = (r == j) ? 1.f : 0.f, acc1 = 0.f;
+                    const float4 *Ar = reinterpret_cast<const float4 *>(A32 + (16 * a + r) * kLDA + 16 * a);
+                    float ar[16];
 #pragma unroll
-                    for (int s2 = 0; s2 < r; ++s2) {
-                        if (s2 & 1) acc1 = fmaf(-Ar[s2], x[s2], acc1);
-                        else acc0 = fmaf(-Ar[s2], x[s2], acc0);
+                    for (int s4 = 0; s4 < 4; ++s4) {
+                        const float4 t4 = Ar[s4];
+                        ar[4 * s4] = t4.x, ar[4 * s4 + 1] = t4.y, ar[4 * s4 + 2] = t4.z, ar[4 * s4 + 3] = t4.w;
                     }
-                    x[r] = acc0 + acc1;
+                    float acc[4] = {(r == j) ? 1.f : 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int s2 = 0; s2 < r; ++s2) acc[s2 & 3] = fmaf(-ar[s2], x[s2], acc[s2 & 3]);
+                    x[r] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
                 }
 #pragma unroll
                 for (int r = 0; r < 16; ++r) M32[(16 * a + r) * C + 16 * a + j] = x[r];
@@ -401,45 +421,22 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             inverse_level<1>(A32, M32, T32, q);
             inverse_level<2>(A32, M32, T32, q);
             inverse_level<3>(A32, M32, T32, q);
-            // M Diag(b e^c) and M Diag(b) as bf16 K-major rows t, in place of M
+            // (d) M as bf16 K-major rows t, once the M R product of chunk c - 1 has read it
+            if (c >= 1 && !pwait(&bars.dfull, (c - 1) & 1)) break;
             {
-                float mv[32];
+                uint8_t *bm = smem + kOffBM;
 #pragma unroll
-                for (int m = 0; m < 32; ++m) mv[m] = M32[q + 128 * m];
-                bar_prep();
-                uint8_t *mp = smem + kOffMp, *mpp = smem + kOffMpp;
-#pragma unroll
-                for (int m = 0; m < 32; ++m) {
-                    const int e = q + 128 * m, t = e >> 6, s2 = e & 63;
-                    *reinterpret_cast<__nv_bfloat16 *>(mp + sw128(t, 2 * s2)) = __float2bfloat16(mv[m] * v.bec[s2]);
-                    *reinterpret_cast<__nv_bfloat16 *>(mpp + sw128(t, 2 * s2)) = __float2bfloat16(mv[m] * v.beta[s2]);
+                for (int m = 0; m < 4; ++m) {
+                    const int e8 = q + 128 * m;            // 8 consecutive entries of row t
+                    const int t = e8 >> 3, s8 = (e8 & 7) * 8;
+                    const float4 lo = reinterpret_cast<const float4 *>(M32 + t * C + s8)[0];
+                    const float4 hi = reinterpret_cast<const float4 *>(M32 + t * C + s8)[1];
+                    *reinterpret_cast<uint4 *>(bm + sw128(t, 2 * s8)) =
+                        make_uint4(bf2(lo.x, lo.y), bf2(lo.z, lo.w), bf2(hi.x, hi.y), bf2(hi.z, hi.w));
                 }
             }
             fence_async_shared();
             mbar_arrive(&bars.mready);
-            // (d) W^T (lane i) -> W, MN-major rows i; B_W is free once X of chunk c-1 is done
-            if (!pwait(&bars.wfull, c & 1)) break;
-            if (c >= 1 && !pwait(&bars.xfull, (c - 1) & 1)) break;
-            tc_fence_after();
-            {
-                uint32_t w[64];
-                tmem_ld32(tmem + lane_off + kTGW, *reinterpret_cast<uint32_t(*)[32]>(&w[0]));
-                tmem_ld32(tmem + lane_off + kTGW + 32, *reinterpret_cast<uint32_t(*)[32]>(&w[32]));
-                tmem_ld_wait();
-                uint8_t *bw = smem + kOffBW;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint4 pk;
-                    pk.x = bf2(__uint_as_float(w[8 * j + 0]), __uint_as_float(w[8 * j + 1]));
-                    pk.y = bf2(__uint_as_float(w[8 * j + 2]), __uint_as_float(w[8 * j + 3]));
-                    pk.z = bf2(__uint_as_float(w[8 * j + 4]), __uint_as_float(w[8 * j + 5]));
-                    pk.w = bf2(__uint_as_float(w[8 * j + 6]), __uint_as_float(w[8 * j + 7]));
-                    *reinterpret_cast<uint4 *>(bw + sw128(q, 16 * j)) = pk;
-                }
-            }
-            fence_async_shared();
-            tc_fence_before();
-            mbar_arrive(&bars.wready);
         }
     } else {
         // ---------------------------------------------------------------- chain warps 0-3
@@ -464,7 +461,8 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             }
             tmem_st_wait();
         }
-        uint8_t *ax = smem + kOffAX, *ad = smem + kOffAD;
+        uint8_t *az = smem + kOffAZ, *ar = smem + kOffAR;
+        const uint32_t vhalf = (uint32_t)(n >> 6) * (kKTile / 2), vbyte = (uint32_t)(n & 63) * 2;
         bool ok = true;
         for (int c = 0; ok && c < nch; ++c) {
             // (1) Z^T -> bf16 A operand (renormalising S~ when the log-scale got small)
@@ -488,7 +486,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                         for (int j = 0; j < 4; ++j)
                             tmem_st16(tmem + lane_off + col + 16 * j, *reinterpret_cast<uint32_t(*)[16]>(&z[16 * j]));
                     }
-                    uint8_t *rowb = ax + cb * 32768;
+                    uint8_t *rowb = az + cb * 32768;
                     const uint32_t r = 128 * hf + n;
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -508,34 +506,67 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             fence_async_shared();
             tc_fence_before();
             mbar_arrive(&bars.zbf_ready);
-            // (3) D'^T = Diag(e^-c) [e^-Lam U - X_S | -X_P], rows n and 128 + n of the K-major tile
-            if (!(ok = wait(&bars.xfull, c & 1))) break;
+            // (2) R^T[n][t] = b_t (exp(-Lam) V[t][n] - e^{c_t} Y_S^T[n][t]), -b_t e^{c_t} Y_P^T[n][t]
+            if (!(ok = wait(&bars.vready, c & 1) && wait(&bars.yfull, c & 1))) break;
             tc_fence_after();
-            const Vec &v = vec[c & 1];
-            const float cC = v.cC;
+            const Vec &v = vec[c % 3];
             const float eL = expf(-Lam);
+            const uint8_t *vt = smem + kOffStage + (c & 1) * kStage + kKTile + vhalf;
 #pragma unroll
             for (int c0 = 0; c0 < C; c0 += 32) {
-                uint32_t xs[32], xp[32], u[32];
-                tmem_ld32(tmem + lane_off + kTX + c0, xs);
-                tmem_ld32(tmem + lane_off + kTX + 64 + c0, xp);
-                tmem_ld32(tmem + lane_off + kTU + c0, u);
+                uint32_t ys[32], yp[32];
+                tmem_ld32(tmem + lane_off + kTY + c0, ys);
+                tmem_ld32(tmem + lane_off + kTY + 64 + c0, yp);
+                float vv[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    vv[j] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vt + sw128(c0 + j, vbyte)));
                 tmem_ld_wait();
 #pragma unroll
                 for (int j8 = 0; j8 < 4; ++j8) {
-                    float ds[8], dp[8];
+                    float rs[8], rp[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int jj = 8 * j8 + j, t = c0 + jj;
+                        const float b = v.beta[t], be = v.bec[t];
+                        rs[j] = fmaf(b * eL, vv[jj], -be * __uint_as_float(ys[jj]));
+                        rp[j] = -be * __uint_as_float(yp[jj]);
+                    }
+                    const uint32_t bo = (c0 + 8 * j8) * 2;
+                    *reinterpret_cast<uint4 *>(ar + sw128(n, bo)) =
+                        make_uint4(bf2(rs[0], rs[1]), bf2(rs[2], rs[3]), bf2(rs[4], rs[5]), bf2(rs[6], rs[7]));
+                    *reinterpret_cast<uint4 *>(ar + sw128(128 + n, bo)) =
+                        make_uint4(bf2(rp[0], rp[1]), bf2(rp[2], rp[3]), bf2(rp[4], rp[5]), bf2(rp[6], rp[7]));
+                }
+            }
+            fence_async_shared();
+            tc_fence_before();
+            mbar_arrive(&bars.rready);
+            // (3) D'^T[n][t] = e^{-c_t} (M R)^T[n][t], into the same operand tile
+            if (!(ok = wait(&bars.dfull, c & 1))) break;
+            tc_fence_after();
+            const float cC = v.cC;
+#pragma unroll
+            for (int c0 = 0; c0 < C; c0 += 32) {
+                uint32_t ds[32], dp[32];
+                tmem_ld32(tmem + lane_off + kTY + c0, ds);
+                tmem_ld32(tmem + lane_off + kTY + 64 + c0, dp);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j8 = 0; j8 < 4; ++j8) {
+                    float a8[8], b8[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int jj = 8 * j8 + j;
                         const float e = v.ecm[c0 + jj];
-                        ds[j] = e * fmaf(eL, __uint_as_float(u[jj]), -__uint_as_float(xs[jj]));
-                        dp[j] = -e * __uint_as_float(xp[jj]);
+                        a8[j] = e * __uint_as_float(ds[jj]);
+                        b8[j] = e * __uint_as_float(dp[jj]);
                     }
                     const uint32_t bo = (c0 + 8 * j8) * 2;
-                    *reinterpret_cast<uint4 *>(ad + sw128(n, bo)) =
-                        make_uint4(bf2(ds[0], ds[1]), bf2(ds[2], ds[3]), bf2(ds[4], ds[5]), bf2(ds[6], ds[7]));
-                    *reinterpret_cast<uint4 *>(ad + sw128(128 + n, bo)) =
-                        make_uint4(bf2(dp[0], dp[1]), bf2(dp[2], dp[3]), bf2(dp[4], dp[5]), bf2(dp[6], dp[7]));
+                    *reinterpret_cast<uint4 *>(ar + sw128(n, bo)) =
+                        make_uint4(bf2(a8[0], a8[1]), bf2(a8[2], a8[3]), bf2(a8[4], a8[5]), bf2(a8[6], a8[7]));
+                    *reinterpret_cast<uint4 *>(ar + sw128(128 + n, bo)) =
+                        make_uint4(bf2(b8[0], b8[1]), bf2(b8[2], b8[3]), bf2(b8[4], b8[5]), bf2(b8[6], b8[7]));
                 }
             }
             fence_async_shared();
@@ -554,12 +585,12 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
-            for (int c0 = 0; c0 < 128; c0 += 16) {
-                uint32_t z[16];
-                tmem_ld16(tmem + lane_off + kTZ + 128 * hf + c0, z);
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+                uint32_t z[32];
+                tmem_ld32(tmem + lane_off + kTZ + 128 * hf + c0, z);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
+                for (int j = 0; j < 32; ++j) {
                     const float val = __uint_as_float(z[j]);
                     if (hf == 0) So[(int64_t)(c0 + j) * D] = val * sc;
                     else Po[(int64_t)(c0 + j) * D] = val;
