@@ -75,10 +75,21 @@ constexpr uint32_t kSmemBytes = kOffVec + 3 * sizeof(Vec) + 1024;
 struct Bars {
     uint64_t kv_full[2], kv_empty[2];
     uint64_t gfull[2];   // one per gram slot, so a wait can never alias a later phase
-    uint64_t vready, mready, zbf_ready, yfull, rready, dfull, dready, zfull, fin;
+    // one per gate-vector slot: the prep may run two chunks ahead of the chain's wait on
+    // these (its progress past chunk c + 1 only needs the chain's step 2 of chunk c), so
+    // a single barrier could be two phases ahead and alias the awaited parity
+    uint64_t vready[3];
+    uint64_t mready, zbf_ready, yfull, rready, dfull, dready, zfull, fin;
 };
 
-__device__ __forceinline__ void bar_prep() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named barrier of the 128 prep threads. The non-aligned form counts threads, not warps,
+// so it stays correct when the lanes of a warp reach it at different times (for example
+// lane 0 returning later from an mbarrier wait than its warp-mates); __syncwarp first
+// reconverges the warp anyway.
+__device__ __forceinline__ void bar_prep() {
+    __syncwarp();
+    asm volatile("barrier.sync 1, 128;" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t bf2(float lo, float hi) { return pack_bf16x2(lo, hi); }
 
@@ -178,7 +189,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
         }
         mbar_init(&bars.gfull[0], 1);
         mbar_init(&bars.gfull[1], 1);
-        mbar_init(&bars.vready, 128);
+        for (int s = 0; s < 3; ++s) mbar_init(&bars.vready[s], 128);
         mbar_init(&bars.mready, 128);
         mbar_init(&bars.zbf_ready, 128);
         mbar_init(&bars.yfull, 1);
@@ -350,7 +361,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                     if (cc < kMinChunkLogDecay) atomicOr(p.err, kErrRange);
                 }
             }
-            mbar_arrive(&bars.vready);
+            mbar_arrive(&bars.vready[c % 3]);
             // (b) gram -> A (rows t = 16 (warp - 4) + lane for lanes < 16), padded rows
             if (!pwait(&bars.gfull[c & 1], (c >> 1) & 1)) break;
             tc_fence_after();
@@ -507,7 +518,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             tc_fence_before();
             mbar_arrive(&bars.zbf_ready);
             // (2) R^T[n][t] = b_t (exp(-Lam) V[t][n] - e^{c_t} Y_S^T[n][t]), -b_t e^{c_t} Y_P^T[n][t]
-            if (!(ok = wait(&bars.vready, c & 1) && wait(&bars.yfull, c & 1))) break;
+            if (!(ok = wait(&bars.vready[c % 3], (c / 3) & 1) && wait(&bars.yfull, c & 1))) break;
             tc_fence_after();
             const Vec &v = vec[c % 3];
             const float eL = expf(-Lam);
@@ -517,20 +528,27 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 uint32_t ys[32], yp[32];
                 tmem_ld32(tmem + lane_off + kTY + c0, ys);
                 tmem_ld32(tmem + lane_off + kTY + 64 + c0, yp);
-                float vv[32];
+                // every shared-memory load of the batch before its stores
+                float vv[32], bb[32], be[32];
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
                     vv[j] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vt + sw128(c0 + j, vbyte)));
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 b4 = reinterpret_cast<const float4 *>(v.beta + c0)[j4];
+                    const float4 e4 = reinterpret_cast<const float4 *>(v.bec + c0)[j4];
+                    bb[4 * j4] = b4.x, bb[4 * j4 + 1] = b4.y, bb[4 * j4 + 2] = b4.z, bb[4 * j4 + 3] = b4.w;
+                    be[4 * j4] = e4.x, be[4 * j4 + 1] = e4.y, be[4 * j4 + 2] = e4.z, be[4 * j4 + 3] = e4.w;
+                }
                 tmem_ld_wait();
 #pragma unroll
                 for (int j8 = 0; j8 < 4; ++j8) {
                     float rs[8], rp[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const int jj = 8 * j8 + j, t = c0 + jj;
-                        const float b = v.beta[t], be = v.bec[t];
-                        rs[j] = fmaf(b * eL, vv[jj], -be * __uint_as_float(ys[jj]));
-                        rp[j] = -be * __uint_as_float(yp[jj]);
+                        const int jj = 8 * j8 + j;
+                        rs[j] = fmaf(bb[jj] * eL, vv[jj], -be[jj] * __uint_as_float(ys[jj]));
+                        rp[j] = -be[jj] * __uint_as_float(yp[jj]);
                     }
                     const uint32_t bo = (c0 + 8 * j8) * 2;
                     *reinterpret_cast<uint4 *>(ar + sw128(n, bo)) =
@@ -551,6 +569,12 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 uint32_t ds[32], dp[32];
                 tmem_ld32(tmem + lane_off + kTY + c0, ds);
                 tmem_ld32(tmem + lane_off + kTY + 64 + c0, dp);
+                float em[32];
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const float4 e4 = reinterpret_cast<const float4 *>(v.ecm + c0)[j4];
+                    em[4 * j4] = e4.x, em[4 * j4 + 1] = e4.y, em[4 * j4 + 2] = e4.z, em[4 * j4 + 3] = e4.w;
+                }
                 tmem_ld_wait();
 #pragma unroll
                 for (int j8 = 0; j8 < 4; ++j8) {
@@ -558,7 +582,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int jj = 8 * j8 + j;
-                        const float e = v.ecm[c0 + jj];
+                        const float e = em[jj];
                         a8[j] = e * __uint_as_float(ds[jj]);
                         b8[j] = e * __uint_as_float(dp[jj]);
                     }

@@ -260,3 +260,26 @@ def test_compose_kernel_selection(family, d, expect):
     hy = _hy()
     c = synth.make_compose_inputs(family, 2, 2, d, seed=91)
     assert hy.hypic_compose_kernel_name(family, c.S) == expect
+
+
+# ------------------------------------------------------------------ determinism / liveness
+
+def test_gdn_build_is_deterministic_with_clean_status():
+    """Two builds of the same 16 layers of the 64-segment workload (ragged 256-1024-token
+    segments) are bitwise identical and no launch reports a timed-out wait: the build has
+    no data race and no wait that can miss its phase, whatever the relative speed of its
+    roles."""
+    hy = _hy()
+    outs = []
+    for rep in range(2):
+        res = []
+        for layer in range(16):
+            inp = synth.make_workload_device("gdn_compose", layer, "cuda")
+            torch.cuda.synchronize()
+            S, lam, P = hy.hypic_build_segments("gdn", inp.k, inp.v, inp.seg_offsets,
+                                                log_gate=inp.log_gate, beta=inp.beta)
+            assert hy.hypic_get_device_status() == 0, f"layer {layer}: device status not OK"
+            res.append((S, lam, P))
+        outs.append(res)
+    for (S1, l1, P1), (S2, l2, P2) in zip(*outs):
+        assert torch.equal(S1, S2) and torch.equal(P1, P2) and torch.equal(l1, l2)
