@@ -192,6 +192,14 @@ def compose_algorithmic_bytes(n_seg, units, d, dense, diag=False, s0=False):
     return per_unit * units
 
 
+def make_workspace(hy, inp, dev, device):
+    """The build's device scratch (allocated once, outside every timed region), or None."""
+    need = hy.hypic_build_workspace_bytes(inp.family, dev["k"], dev["v"], inp.seg_offsets,
+                                          log_gate=dev.get("log_gate"),
+                                          log_gamma=dev.get("log_gamma"), beta=dev.get("beta"))
+    return torch.empty(need, dtype=torch.uint8, device=device) if need else None
+
+
 class Step:
     """Device buffers and the two launches of one step of a workload."""
 
@@ -203,12 +211,14 @@ class Step:
         self.S, self.lam, self.P = hy.build_outputs(inp.family, inp.n_seg, inp.H_v, inp.d_v,
                                                     device)
         self.prefix = torch.empty_like(self.S)
+        self.workspace = make_workspace(hy, inp, self.dev, device)
 
     def build(self):
         d = self.dev
         self.hy.hypic_build_segments(self.inp.family, d["k"], d["v"], self.inp.seg_offsets,
                                      log_gate=d.get("log_gate"), log_gamma=d.get("log_gamma"),
-                                     beta=d.get("beta"), S=self.S, lam=self.lam, P=self.P)
+                                     beta=d.get("beta"), S=self.S, lam=self.lam, P=self.P,
+                                     workspace=self.workspace)
 
     def compose(self):
         self.hy.hypic_compose_scan(self.inp.family, self.S, self.lam, self.P,
@@ -259,6 +269,7 @@ def build_gdn_compose_cache(layers=48, device="cuda"):
     S, lam, P = hy.build_outputs("gdn", n_seg, units, d, device)
     lib = hy.load_library()
     stream = torch.cuda.current_stream().cuda_stream
+    ws = None
     for layer in range(layers):
         inp = synth.make_workload_device("gdn_compose", layer, device)
         a = hy.make_build_args("gdn", inp.k, inp.v, inp.seg_offsets, inp.log_gate, None,
@@ -266,6 +277,12 @@ def build_gdn_compose_cache(layers=48, device="cuda"):
         a.S = S.data_ptr() + layer * H * d * d * 4
         a.lam = lam.data_ptr() + layer * H * 4
         a.P = P.data_ptr() + layer * H * d * d * 4
+        need = int(lib.hypic_build_workspace_bytes(ctypes.byref(a)))
+        if need and (ws is None or ws.numel() < need):
+            torch.cuda.synchronize()   # the previous layer's build may still read the old one
+            ws = torch.empty(need, dtype=torch.uint8, device=device)
+        if need:
+            a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
         st = lib.hypic_build_segments(ctypes.byref(a), stream)
         if st != 0:
             raise hy.HypicError(st, "hypic_build_segments (gdn_compose cache)")
@@ -416,6 +433,7 @@ def e2e_measure(inp, steps=5, warmup=2):
     dev = {n: torch.empty_like(t, device="cuda") for n, t in host.items()}
     S, lam, P = hy.build_outputs(inp.family, inp.n_seg, inp.H_v, inp.d_v, "cuda")
     prefix = torch.empty_like(S)
+    workspace = make_workspace(hy, inp, dev, "cuda")
     outs = [S, lam, P, prefix]
     host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -426,7 +444,7 @@ def e2e_measure(inp, steps=5, warmup=2):
             dev[n].copy_(host[n], non_blocking=True)
         hy.hypic_build_segments(inp.family, dev["k"], dev["v"], inp.seg_offsets,
                                 log_gate=dev.get("log_gate"), log_gamma=dev.get("log_gamma"),
-                                beta=dev.get("beta"), S=S, lam=lam, P=P)
+                                beta=dev.get("beta"), S=S, lam=lam, P=P, workspace=workspace)
         hy.hypic_compose_scan(inp.family, S, lam, P, prefix=prefix)
         for h, d in zip(host_out, outs):
             h.copy_(d, non_blocking=True)

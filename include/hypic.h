@@ -113,7 +113,13 @@ typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  *   S                 out [n_seg][H_v][d_k][d_v] fp32 (segment stride out_seg_stride units)
  *   lam               out [n_seg][H_v] fp32, DIAG [n_seg][H_v][d_k]
  *   P                 out DELTA / GDN: [n_seg][H_v][d_k][d_k] fp32; else NULL
- *   workspace         device scratch of hypic_build_workspace_bytes() bytes (NULL if 0)
+ *   workspace         device scratch, at least hypic_build_workspace_bytes() bytes, 16-byte
+ *                     aligned (NULL when that is 0). DELTA / GDN with bf16 k, v and
+ *                     d = 128 use 8 KB per (segment, value head, 64-token chunk): the
+ *                     chunk matrices (I + Diag(b) L)^-1 Diag(b) that the chain kernel reads
+ *                     back. The caller owns it; its contents are undefined after the call and
+ *                     it may be reused by the next call on the same stream, but not by a call
+ *                     still running on another stream. It must not overlap any argument.
  */
 typedef struct {
     int32_t family;
@@ -172,7 +178,8 @@ hypic_status hypic_build_segments(const hypic_build_args *args, void *stream);
 hypic_status hypic_compose_scan(const hypic_compose_args *args, void *stream);
 
 /* Device scratch bytes hypic_build_segments needs for these arguments (host-only query;
- * reads the shapes and seg_offsets, never the tensors). 0 means no workspace. */
+ * reads the shapes and seg_offsets, never the tensors). 0 means no workspace; 0 also for
+ * NULL or malformed arguments, which hypic_build_segments then rejects. */
 size_t hypic_build_workspace_bytes(const hypic_build_args *args);
 
 /* Name of the kernel hypic_build_segments / hypic_compose_scan would launch for these

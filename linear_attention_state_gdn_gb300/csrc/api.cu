@@ -91,6 +91,17 @@ ComposePath pick_compose(const hypic_compose_args *a) {
     return compose_dense_tc_supported(q) ? ComposePath::DenseTc : ComposePath::DenseSimt;
 }
 
+// Workspace records of the GDN / DeltaNet tensor-core build: one per (segment, value head,
+// 64-token chunk). Negative segment lengths count as empty (they are rejected elsewhere).
+int64_t gdn_records(const hypic_build_args *a) {
+    int64_t records = 0;
+    for (int j = 0; j < a->n_seg; ++j) {
+        const int64_t len = a->seg_offsets[j + 1] - a->seg_offsets[j];
+        if (len > 0) records += (int64_t)a->H_v * ((len + kGdnChunk - 1) / kGdnChunk);
+    }
+    return records;
+}
+
 bool build_shape_ok(const hypic_build_args *a) {
     return a && a->family >= HYPIC_FAM_LINEAR && a->family <= HYPIC_FAM_GDN &&
            (a->dtype == HYPIC_BF16 || a->dtype == HYPIC_F32) && a->n_seg >= 0 &&
@@ -123,8 +134,9 @@ const char *hypic_status_string(hypic_status s) {
 }
 
 size_t hypic_build_workspace_bytes(const hypic_build_args *a) {
-    (void)a;
-    return 0;
+    if (!build_shape_ok(a) || a->n_seg == 0 || !a->seg_offsets) return 0;
+    if (pick_build(a) != BuildPath::GdnTc) return 0;
+    return (size_t)gdn_records(a) * (size_t)kGdnRecordBytes;
 }
 
 hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
@@ -175,6 +187,16 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
         for (const void *p : in_ptrs)
             if (p && !on_device(p)) return HYPIC_ERR_INVALID_ARG;
     }
+    const BuildPath path = pick_build(a);
+    if (path == BuildPath::GdnTc) {
+        // records are addressed as 64-row blocks of a 2D tensor map with int32 coordinates
+        if (gdn_records(a) > (int64_t)(INT32_MAX / 64)) return HYPIC_ERR_UNSUPPORTED;
+        if (gdn_records(a) > 0) {
+            if (!a->workspace) return HYPIC_ERR_INVALID_ARG;
+            if (!aligned(a->workspace, 16)) return HYPIC_ERR_ALIGNMENT;
+            if (!on_device(a->workspace)) return HYPIC_ERR_INVALID_ARG;
+        }
+    }
     if (hypic_build_workspace_bytes(a) > a->workspace_bytes) return HYPIC_ERR_INVALID_ARG;
 
     unsigned *err = status_word(nullptr);
@@ -207,15 +229,19 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
     std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
         return a->seg_offsets[x + 1] - a->seg_offsets[x] > a->seg_offsets[y + 1] - a->seg_offsets[y];
     });
+    int64_t wsb = 0;
     for (int r = 0; r < a->n_seg; ++r) {
         const int j = order[r];
         p.seg[r].start = (int32_t)a->seg_offsets[j];
         p.seg[r].len = (int32_t)(a->seg_offsets[j + 1] - a->seg_offsets[j]);
         p.seg[r].idx = j;
+        p.seg[r].wsb = (int32_t)wsb;   // bounded by the record check above on the GDN path
+        wsb = std::min<int64_t>(wsb + (int64_t)a->H_v * ((p.seg[r].len + kGdnChunk - 1) / kGdnChunk),
+                                INT32_MAX);
     }
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    switch (pick_build(a)) {
+    switch (path) {
     case BuildPath::GdnTc: return from_cuda(launch_build_gdn_tc(p, s));
     case BuildPath::DeltaSeq: return from_cuda(launch_build_delta_seq(p, s));
     case BuildPath::GatedTc: return from_cuda(launch_build_gated_tc(p, s));

@@ -1,0 +1,326 @@
+// build_gdn_prep.cu -- chunk preparation of the DeltaNet / GDN segment build (bf16 k,
+// d_k = d_v = 128, chunks of 64 tokens): for every (segment, value head, chunk) the matrix
+//     M2 = N Diag(b),   N = (I + Diag(b) L)^-1,   L_ts = k_t . k_s for s < t (0 otherwise),
+// rounded to bf16 and written as one 8 KB record (64 rows t' x 64 columns t, row-major) into
+// the caller's workspace. The chain kernel (build_gdn_tc.cu) reads the records back.
+//
+// Why N carries everything the chain needs: with c_t = sum_{s<=t} log a_s inside the chunk,
+// the chunked recurrence of "Gated Delta Networks: Improving Mamba2 with Delta Rule"
+// (reference 7 of the episode-companion page "Hypic: Position-Independent KV Caching for
+// Hybrid-Attention LLM Serving") needs M = (I + A)^-1 with A_ts = b_t (k_t . k_s) e^{c_t - c_s}
+// (s < t). A = Diag(b e^c) L Diag(e^-c), so I + A = Diag(e^c) (I + Diag(b) L) Diag(e^-c) and
+// M = Diag(e^c) N Diag(e^-c): the inverse itself never sees the gates a_t. The chain applies
+// them as diagonal scalings of M2. The product of the chunk's transitions
+// prod_t (I - b_t k_t k_t^T) (latest leftmost) equals I - K^T M2 K, the transition part of
+// the pair (S(C|0), T_C) that "Cut First-Token Latency by 3.25x: Introducing HYPIC ..."
+// (besthub.dev), paragraph "For linear layers", stores for DeltaNet / GDN layers.
+//
+// Persistent CTAs of 128 threads, two per SM, each walking a strided list of records: the k
+// tile of a record is requested three records ahead (a ring of four) and its gram is issued
+// one record ahead (two TMEM buffers), so loads and grams overlap the inversions.
+//   1. TMA the chunk's k (two 128B-swizzled 64-channel halves); b masked past the segment end.
+//   2. One thread issues the gram K K^T (M = 64 tcgen05 MMA, fp32 accumulator in TMEM).
+//   3. A = Diag(b) L in fp32 shared memory (rows padded to 68 floats).
+//   4. N by 16 x 16 blocks: the four diagonal blocks by forward substitution (one warp each),
+//      then the blocks below level by level, N_ab = -N_aa sum_{k=b}^{a-1} A_ak N_kb, as
+//      16 x 8 half-blocks spread over the four warps. The 16 x 16 x 16 products run on the
+//      warp-level tensor-core MMA (m16n8k8, tf32 inputs, fp32 accumulation): tcgen05's
+//      smallest tile (M = 64) would waste most of its work on products this small and
+//      each would need a round trip through TMEM.
+//   5. Columns scaled by b_t, rounded to bf16, stored (16-byte coalesced stores).
+// Tokens past the segment end have b = 0, so their rows and columns of M2 are zero.
+#include <algorithm>
+
+#include "internal.cuh"
+#include "ptx.cuh"
+#include "tmap.cuh"
+
+namespace hypic {
+namespace {
+
+using namespace ptx;
+
+constexpr int D = 128;
+constexpr int C = kGdnChunk;
+constexpr int kThreads = 128;
+constexpr uint32_t kLDA = 68;                            // padded fp32 row stride
+constexpr int kKBufs = 4;                                // k tiles requested 3 records ahead
+constexpr uint32_t kOffK = 0;                            // k tiles, 4 x 16 KB
+constexpr uint32_t kOffA32 = kKBufs * 16384;             // fp32 Diag(b) L, 64 x 68
+constexpr uint32_t kOffN32 = kOffA32 + 64 * kLDA * 4;    // fp32 N, 64 x 68
+constexpr uint32_t kLDT = 12;                            // per-warp 16 x 8 scratch, padded rows
+constexpr uint32_t kOffT = kOffN32 + 64 * kLDA * 4;      // 4 warps x 16 x 12 fp32
+constexpr uint32_t kSmemBytes = kOffT + 4 * 16 * kLDT * 4 + 1024;
+constexpr int kCtasPerSm = 2;
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// c (16 x 8, m16n8 accumulator layout) += X[xr.., xc..] (16 x 16) * Y[yr.., yc..] (16 x 8);
+// X and Y row-major fp32 in shared memory with row strides ldx, ldy.
+__device__ __forceinline__ void mma16x8x16(float (&c)[4], const float *X, int ldx, const float *Y, int ldy,
+                                           int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        const uint32_t a0 = to_tf32(X[g * ldx + 8 * ks + t]);
+        const uint32_t a1 = to_tf32(X[(g + 8) * ldx + 8 * ks + t]);
+        const uint32_t a2 = to_tf32(X[g * ldx + 8 * ks + t + 4]);
+        const uint32_t a3 = to_tf32(X[(g + 8) * ldx + 8 * ks + t + 4]);
+        const uint32_t b0 = to_tf32(Y[(8 * ks + t) * ldy + g]);
+        const uint32_t b1 = to_tf32(Y[(8 * ks + t + 4) * ldy + g]);
+        asm volatile(
+            "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+}
+
+// Half-block (a, b, hh) of N: columns 16 b + 8 hh .. + 7 of block row a, from the blocks of
+// N already computed: T = sum_{k=b}^{a-1} A_ak N_kb[:, half], N_ab[:, half] = -N_aa T.
+__device__ __forceinline__ void half_block(const float *A32, float *N32, float *Tw, int a, int b, int hh,
+                                           int lane) {
+    const int g = lane >> 2, t = lane & 3;
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k = b; k < a; ++k)
+        mma16x8x16(c, A32 + 16 * a * kLDA + 16 * k, kLDA, N32 + 16 * k * kLDA + 16 * b + 8 * hh, kLDA, lane);
+    Tw[g * kLDT + 2 * t] = c[0];
+    Tw[g * kLDT + 2 * t + 1] = c[1];
+    Tw[(g + 8) * kLDT + 2 * t] = c[2];
+    Tw[(g + 8) * kLDT + 2 * t + 1] = c[3];
+    __syncwarp();
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    mma16x8x16(d, N32 + 16 * a * kLDA + 16 * a, kLDA, Tw, kLDT, lane);
+    float *o = N32 + 16 * a * kLDA + 16 * b + 8 * hh;
+    o[g * kLDA + 2 * t] = -d[0];
+    o[g * kLDA + 2 * t + 1] = -d[1];
+    o[(g + 8) * kLDA + 2 * t] = -d[2];
+    o[(g + 8) * kLDA + 2 * t + 1] = -d[3];
+    __syncwarp();   // Tw is reused by this warp's next half-block
+}
+
+// Records are visited in the order (segment, chunk, head), so the value heads that share a
+// key head read the same k tile back to back (from L2).
+struct RecPos {
+    int r, c, h, nch;
+    bool valid;
+};
+__device__ __forceinline__ RecPos rec_pos(const BuildParams &p, int max_nch, int v) {
+    RecPos q;
+    q.h = v % p.H_v;
+    const int rc = v / p.H_v;
+    q.c = rc % max_nch;
+    q.r = rc / max_nch;
+    q.nch = (p.seg[q.r].len + C - 1) / C;
+    q.valid = q.c < q.nch;
+    return q;
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ uint64_t kfull[kKBufs], gfull[2];
+    __shared__ uint32_t tslot;
+    __shared__ int s_ok;
+    __shared__ __align__(16) float vb[2][C];
+
+    const int max_nch = (p.max_len + C - 1) / C;
+    const int total = p.n_seg * max_nch * p.H_v;
+    auto next_valid = [&](int v) {
+        while (v < total && !rec_pos(p, max_nch, v).valid) v += gridDim.x;
+        return v;
+    };
+    int v = next_valid(blockIdx.x);
+    if (v >= total) return;   // uniform: the whole CTA leaves before any set-up
+    const int q = threadIdx.x, warp = q >> 5, lane = q & 31;
+    float *A32 = reinterpret_cast<float *>(smem + kOffA32);
+    float *N32 = reinterpret_cast<float *>(smem + kOffN32);
+    float *Tw = reinterpret_cast<float *>(smem + kOffT) + warp * 16 * kLDT;
+
+    if (q == 0) {
+        for (int s = 0; s < kKBufs; ++s) mbar_init(&kfull[s], 1);
+        for (int s = 0; s < 2; ++s) mbar_init(&gfull[s], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&tslot, 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tslot;
+    constexpr uint32_t idG = idesc(kFmtBF16, kFmtBF16, false, false, 64, 64);
+    int kiss[kKBufs] = {}, kwait[kKBufs] = {}, giss[2] = {}, gwait[2] = {};   // thread 0
+    auto load_k = [&](int vv, int b) {   // thread 0
+        ++kiss[b];
+        const RecPos r = rec_pos(p, max_nch, vv);
+        const int32_t t0 = p.seg[r.r].start + r.c * C;
+        uint8_t *kt = smem + kOffK + b * 16384;
+        mbar_arrive_expect_tx(&kfull[b], 16384);
+        tma_load_3d(kt, &tmK, &kfull[b], 0, r.h / p.gqa, t0);
+        tma_load_3d(kt + 8192, &tmK, &kfull[b], 64, r.h / p.gqa, t0);
+    };
+    auto gram = [&](int kb, int b) -> bool {   // thread 0: k buffer kb -> TMEM buffer b
+        if (!mbar_wait(&kfull[kb], kwait[kb] & 1, p.err, kErrTimeout)) return false;
+        ++kwait[kb];
+        ++giss[b];
+        tc_fence_after();
+        const uint32_t k = smem_u32(smem + kOffK + kb * 16384);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const uint32_t a = k + (s >> 2) * 8192 + (s & 3) * 32;
+            mma_bf16(tmem + 64 * b, sdesc(a, 16, 1024, kSwizzle128B), sdesc(a, 16, 1024, kSwizzle128B), idG,
+                     s > 0);
+        }
+        mma_commit(&gfull[b]);
+        return true;
+    };
+    bool ok = true;
+    // the next three records (total when there are none)
+    int vn = next_valid(v + gridDim.x);
+    int vn2 = vn < total ? next_valid(vn + gridDim.x) : total;
+    int vn3 = vn2 < total ? next_valid(vn2 + gridDim.x) : total;
+    if (q == 0) {
+        prefetch_tmap(&tmK);
+        load_k(v, 0);
+        if (vn < total) load_k(vn, 1);
+        if (vn2 < total) load_k(vn2, 2);
+        ok = gram(0, 0);
+    }
+    for (int i = 0; v < total; ++i) {
+        const int b = i & 1;
+        const RecPos r = rec_pos(p, max_nch, v);
+        const SegEntry seg = p.seg[r.r];
+        // k ring slot (i + 3) % 4 held record i - 1, whose gram has completed
+        if (q == 0 && ok && vn3 < total) load_k(vn3, (i + 3) % kKBufs);
+        const int valid = min(C, seg.len - r.c * C);
+        if (q < C) vb[b][q] = q < valid ? p.beta[((int64_t)seg.start + r.c * C + q) * p.H_v + r.h] : 0.f;
+        if (q == 0) {
+            ok = ok && mbar_wait(&gfull[b], gwait[b] & 1, p.err, kErrTimeout);
+            if (ok) ++gwait[b];
+            s_ok = ok ? 1 : 0;
+        }
+        __syncthreads();
+        if (!s_ok) break;   // uniform
+        tc_fence_after();
+        {   // gram rows t = 16 warp + lane (lanes < 16, M = 64 accumulator layout) -> A rows
+            uint32_t gr[64];
+            const uint32_t taddr = tmem + 64 * b + ((uint32_t)(32 * warp) << 16);
+            tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&gr[0]));
+            tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&gr[32]));
+            tmem_ld_wait();
+            if (lane < 16) {
+                const int t = 16 * warp + lane;
+                const float bt = vb[b][t];
+                float4 *row = reinterpret_cast<float4 *>(A32 + t * kLDA);
+#pragma unroll
+                for (int s4 = 0; s4 < C / 4; ++s4) {
+                    const int s = 4 * s4;
+                    float4 a4;
+                    a4.x = s + 0 < t ? bt * __uint_as_float(gr[s + 0]) : 0.f;
+                    a4.y = s + 1 < t ? bt * __uint_as_float(gr[s + 1]) : 0.f;
+                    a4.z = s + 2 < t ? bt * __uint_as_float(gr[s + 2]) : 0.f;
+                    a4.w = s + 3 < t ? bt * __uint_as_float(gr[s + 3]) : 0.f;
+                    row[s4] = a4;
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        // diagonal block `warp`: lane j < 16 solves column j by forward substitution
+        if (lane < 16) {
+            const int a = warp, j = lane;
+            float x[16];
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                const float4 *Ar = reinterpret_cast<const float4 *>(A32 + (16 * a + rr) * kLDA + 16 * a);
+                float ar[16];
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    const float4 t4 = Ar[s4];
+                    ar[4 * s4] = t4.x, ar[4 * s4 + 1] = t4.y, ar[4 * s4 + 2] = t4.z, ar[4 * s4 + 3] = t4.w;
+                }
+                float acc[4] = {(rr == j) ? 1.f : 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int s = 0; s < rr; ++s) acc[s & 3] = fmaf(-ar[s], x[s], acc[s & 3]);
+                x[rr] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            }
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) N32[(16 * a + rr) * kLDA + 16 * a + j] = x[rr];
+        }
+        __syncthreads();
+        // level 1: (1,0), (2,1), (3,2) as six half-blocks; level 2: (2,0), (3,1); level 3: (3,0)
+        half_block(A32, N32, Tw, 1 + (warp >> 1), warp >> 1, warp & 1, lane);
+        if (warp < 2) half_block(A32, N32, Tw, 3, 2, warp, lane);
+        // the gram of the next record into the other TMEM buffer (last read two records ago);
+        // its k tile was requested at the top of this iteration
+        if (q == 0 && ok && vn < total) ok = gram((i + 1) % kKBufs, b ^ 1);
+        __syncthreads();
+        half_block(A32, N32, Tw, 2 + (warp >> 1), warp >> 1, warp & 1, lane);
+        __syncthreads();
+        if (warp < 2) half_block(A32, N32, Tw, 3, 0, warp, lane);
+        __syncthreads();
+        // record: N Diag(b) as bf16 rows t' (blocks above the diagonal are zero)
+        uint8_t *dst = static_cast<uint8_t *>(p.workspace) +
+                       ((int64_t)seg.wsb + (int64_t)r.h * r.nch + r.c) * (int64_t)kGdnRecordBytes;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const int e8 = q + 128 * m;   // 8 consecutive entries of row t'
+            const int tp = e8 >> 3, s8 = (e8 & 7) * 8;
+            uint4 pk = make_uint4(0u, 0u, 0u, 0u);
+            if ((s8 >> 4) <= (tp >> 4)) {
+                const float4 lo = reinterpret_cast<const float4 *>(N32 + tp * kLDA + s8)[0];
+                const float4 hi = reinterpret_cast<const float4 *>(N32 + tp * kLDA + s8)[1];
+                const float4 b0 = reinterpret_cast<const float4 *>(vb[b] + s8)[0];
+                const float4 b1 = reinterpret_cast<const float4 *>(vb[b] + s8)[1];
+                pk = make_uint4(pack_bf16x2(lo.x * b0.x, lo.y * b0.y), pack_bf16x2(lo.z * b0.z, lo.w * b0.w),
+                                pack_bf16x2(hi.x * b1.x, hi.y * b1.y), pack_bf16x2(hi.z * b1.z, hi.w * b1.w));
+            }
+            *reinterpret_cast<uint4 *>(dst + tp * 128 + s8 * 2) = pk;
+        }
+        v = vn;
+        vn = vn2;
+        vn2 = vn3;
+        vn3 = vn3 < total ? next_valid(vn3 + gridDim.x) : total;
+    }
+    if (q == 0) {   // after a wait gave up: let every copy and MMA in flight land first
+        for (int b = 0; b < kKBufs; ++b)
+            for (; kwait[b] < kiss[b]; ++kwait[b]) mbar_wait(&kfull[b], kwait[b] & 1, nullptr, 0);
+        for (int b = 0; b < 2; ++b)
+            for (; gwait[b] < giss[b]; ++gwait[b]) mbar_wait(&gfull[b], gwait[b] & 1, nullptr, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_build_gdn_prep(const BuildParams &p, cudaStream_t s) {
+    const int max_nch = (p.max_len + C - 1) / C;
+    const int64_t total = (int64_t)p.n_seg * max_nch * p.H_v;
+    if (total == 0) return cudaSuccess;
+    if (total > INT32_MAX / 2) return cudaErrorInvalidValue;
+    const int64_t N = p.n_tok > 0 ? p.n_tok : 1;
+    CUtensorMap tmK;
+    if (!make_tmap_3d(&tmK, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_k, N, (uint64_t)D * 2,
+                      (uint64_t)p.H_k * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(build_gdn_prep_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int grid = (int)std::min<int64_t>(total, (int64_t)sms * kCtasPerSm);
+    build_gdn_prep_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, tmK);
+    return cudaGetLastError();
+}
+
+}  // namespace hypic

@@ -1,5 +1,7 @@
 // build_gdn_tc.cu -- DeltaNet / Gated DeltaNet segment build on the 5th-generation tensor
-// cores (bf16 k / v, d_k = d_v = 128, fp32 state).
+// cores (bf16 k / v, d_k = d_v = 128, fp32 state): the serial chunk chain. It runs after
+// build_gdn_prep.cu, which leaves one bf16 matrix M2 = N Diag(b) per 64-token chunk in the
+// workspace (N = (I + Diag(b) L)^-1, L the strictly lower part of the chunk's gram K K^T).
 //
 // What is computed: for every cached segment C and value head the pair (S(C|0), T_C) with
 // T_C = exp(lam) P, P = prod_t (I - b_t k_t k_t^T) (latest factor leftmost), lam = sum log a_t
@@ -8,28 +10,40 @@
 // "Gated Delta Networks: Improving Mamba2 with Delta Rule", reference 7 of the episode
 // companion page "Hypic: Position-Independent KV Caching for Hybrid-Attention LLM Serving").
 //
-// Chunked form (exact algebra, chunks of C = 64 tokens, c_t = sum_{s<=t} log a_s inside
-// the chunk, A_ts = b_t (k_t . k_s) exp(c_t - c_s) for s < t, M = (I + A)^-1):
-//     S <- e^{c_C} (S + K^T Diag(e^-c) M Diag(b) (V - Diag(e^c) K S)),
-//     P <- P - K^T Diag(e^-c) M Diag(b e^c) K P,
-// i.e. with Y = K [S | P] and R = Diag(b) [V - Diag(e^c) Y_S | -Diag(e^c) Y_P] every chunk
-// adds K^T Diag(e^-c) M R to the state. The state is carried as Z = [S~ | P] with
-// S = exp(Lam) S~ (Lam a running log-scale, folded into S~ when it drops below -20):
-//     Y = K Z,  R = Diag(b) [exp(-Lam) V - Diag(e^c) Y_S | -Diag(e^c) Y_P],
-//     Z <- Z + K^T D',  D' = Diag(e^-c) M R.
-// Only M depends on the chunk's gram; everything that touches the state is three MMAs
-// (Y, M R, K^T D') plus two per-lane transforms.
+// Chunked form (exact algebra; c_t = sum_{s<=t} log a_s inside the chunk, c_C = c_63):
+//     W = M2 K,   U = M2 Diag(e^-c) V,
+//     S <- e^{c_C} (S + K^T (U - W S)),     P <- P + K^T (-W P).
+// W and U do not depend on the state. The state is carried as Z = [S~ | P] with
+// S = exp(Lam) S~, Lam a running log-scale reset to 0 whenever Lam + c_C < -30 (S~ is then
+// multiplied by exp(Lam) first), so every chunk is
+//     D_S = exp(-Lam) U - W S~,   D_P = -W P,   Z <- Z + K^T [D_S | D_P],   Lam += c_C,
+// two dependent MMA groups per half with a bf16 rounding of Z and of D in between.
 //
-// Layout (one CTA = one (segment, value head) unit, 320 threads):
-//   TMEM  Z^T      [0,256)   lane = state column n (S~ half, then P half), column = key row i
-//         Y^T/D^T  [256,384) lane n, column t: Y^T = Z^T K^T, then (M R)^T in the same place
-//         G        [384,512) two gram slots (M = 64 layout), one per chunk parity
-//   SMEM  two TMA stages of (k, v) chunks (128B-swizzled, channels contiguous); the bf16
-//         K-major operands Z^T (A of Y), R^T then D'^T (A of M R, then of the update) and M
-//         (B of M R); the fp32 A and M of the inversion; per-chunk gate vectors (3 slots).
-// Roles: warps 0-3 carry the chain (Z^T -> bf16, R, D'; thread n = TMEM lane n), warps 4-7
-// prepare M for the next chunk (gates, A from the gram, 16 x 16-blocked inverse in fp32),
-// warp 8 issues TMA, warp 9 issues the MMAs. Every wait is bounded.
+// The chain is bound by shared-memory bandwidth when its operands go through shared memory,
+// so both dependent products take their A operand from TMEM: the state and the D
+// accumulators are rounded to bf16 in place in TMEM (tcgen05.ld / st, two values per
+// column), and only the B operands (-W^T and the k chunk) are read from shared memory.
+//
+// Layout (one CTA = one (segment, value head) unit, 480 threads, one CTA per SM):
+//   TMEM  [0,128) Z_S^T, [128,256) Z_P^T   fp32 state, lane n = state column, column = key row
+//         [256,320) D_S^T, [320,384) D_P^T fp32 accumulators (lane n, column t); the bf16 D^T
+//                                         (A of the update) is written over their first half
+//         [384,448) bf16 Z_S^T (A of d_S); between d_S(c) and the next Z pass it holds the
+//                   fp32 W^T(c+1) accumulator (lane i, column t')
+//         [448,512) bf16 Z_P^T (A of d_P)
+//   SMEM  a ring of three k chunks and a ring of two {v chunk, M2 record} (TMA,
+//         128B-swizzled); -W^T bf16 (MN-major B of d, two slots); M1 = M2 Diag(exp(-Lam - c))
+//         bf16 (K-major B of U, two slots).
+// Roles: warps 0-3 carry the S~ half and warps 4-7 the P half (thread = TMEM lane = state
+// column: Z^T -> bf16, D^T -> bf16), warps 8-11 prepare the state-independent operands
+// (gates, M1, -W^T -> bf16), warp 12 issues TMA, warp 13 the S~ half's MMAs and the state-
+// independent ones, warp 14 the P half's MMAs:
+//     warp 13, per chunk c:  d_S(c): D_S += Z_S^T (-W^T);  W(c+1): W^T = K^T M2^T;
+//                            f_S(c): Z_S^T += D_S^T K;     U(c+1): D_S = V^T M1^T
+//     warp 14, per chunk c:  d_P(c): D_P = Z_P^T (-W^T);   f_P(c): Z_P^T += D_P^T K
+// Two issuers keep the tensor pipe fed: it queues only a few instructions, so while one half
+// waits for its operands the other half's products run.
+// Every wait is bounded; a wait that runs out sets the status word and the CTA drains.
 #include <algorithm>
 
 #include "internal.cuh"
@@ -42,137 +56,103 @@ namespace {
 using namespace ptx;
 
 constexpr int D = 128;
-constexpr int C = 64;
-constexpr int kThreads = 320;
-constexpr int kPrepWarp0 = 4;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr float kRenorm = -20.f;     // fold exp(Lam) into S~ below this log-scale
-constexpr float kMinChunkLogDecay = -60.f;
+constexpr int C = kGdnChunk;
+constexpr int kThreads = 480;
+constexpr int kAuxWarp0 = 8;
+constexpr int kProducerWarp = 12;
+constexpr int kMmaWarpS = 13;   // issues the S~ half's products and W, U
+constexpr int kMmaWarpP = 14;   // issues the P half's products
+constexpr float kRenormBelow = -30.f;       // reset Lam when Lam + c_C would drop below this
+constexpr float kMinChunkLogDecay = -60.f;  // supported range of c_C
 
 // shared-memory map (offsets from the 1024-aligned base)
-constexpr uint32_t kKTile = C * 256;                  // k chunk: two 64-channel halves, 16 KB
-constexpr uint32_t kStage = 2 * kKTile;               // k + v
-constexpr uint32_t kOffStage = 0;                     // 2 stages: 64 KB
-constexpr uint32_t kOffAZ = 2 * kStage;               // Z^T bf16, 2 K-blocks x 256 rows x 128 B
-constexpr uint32_t kOffAR = kOffAZ + 65536;           // R^T / D'^T bf16, 256 rows x 128 B
-constexpr uint32_t kOffBM = kOffAR + 32768;           // M bf16, 64 rows t x 128 B
-constexpr uint32_t kLDA = 68;                         // padded row stride of the fp32 A (16-B rows)
-constexpr uint32_t kOffA32 = kOffBM + 8192;           // fp32 A, 64 x 68
-constexpr uint32_t kOffM32 = kOffA32 + 64 * kLDA * 4; // fp32 M, 64 x 64
-constexpr uint32_t kOffT = kOffM32 + 64 * 64 * 4;     // fp32 block products, 3 x 16 x 16
-constexpr uint32_t kOffVec = kOffT + 3 * 256 * 4;     // per-chunk vectors (3 slots)
+constexpr uint32_t kHalf = 64 * 128;          // 64 rows x 128 B: one 64-channel half of a chunk
+constexpr uint32_t kKV = 2 * kHalf;           // k (or v) chunk, 16 KB
+constexpr uint32_t kRec = 64 * 128;           // M2 record, 8 KB
+constexpr uint32_t kVR = kKV + kRec;          // v chunk + M2 record, 24 KB
+constexpr int kKSlots = 3;                    // k is read until the lagging half's update
+constexpr uint32_t kOffK = 0;                 // k ring: 3 x 16 KB
+constexpr uint32_t kOffVR = kKSlots * kKV;    // {v, M2} ring: 2 x 24 KB
+constexpr uint32_t kOffWop = kOffVR + 2 * kVR;  // -W^T bf16: 2 slots x [128 rows i][128 B]
+constexpr uint32_t kOffM1 = kOffWop + 2 * kKV;  // M1: 2 slots x 8 KB
+constexpr uint32_t kSmemBytes = kOffM1 + 2 * kRec + 1024;
 
-constexpr uint32_t kTZ = 0, kTY = 256, kTG = 384;
+constexpr uint32_t kTZ = 0, kTD = 256, kTZK = 384;
 
-struct Vec {   // one slot of per-chunk vectors
-    float beta[C], c[C], ecp[C], ecm[C], bec[C];
-    float cC;  // chunk total log decay
-    float pad[3];
+struct Slot {   // per-chunk values from the operand warps (two slots)
+    float ex[C];      // exp(-Lam_start - c_t)
+    float rscale;     // exp(Lam) before the reset (used when renorm)
+    int renorm;       // S~ is multiplied by rscale before this chunk
+    float lam_after;  // Lam after this chunk
+    float lam_sum;    // sum of c_C up to and including this chunk
 };
-constexpr uint32_t kSmemBytes = kOffVec + 3 * sizeof(Vec) + 1024;
 
 struct Bars {
-    uint64_t kv_full[2], kv_empty[2];
-    uint64_t gfull[2];   // one per gram slot, so a wait can never alias a later phase
-    // one per gate-vector slot: the prep may run two chunks ahead of the chain's wait on
-    // these (its progress past chunk c + 1 only needs the chain's step 2 of chunk c), so
-    // a single barrier could be two phases ahead and alias the awaited parity
-    uint64_t vready[3];
-    uint64_t mready, zbf_ready, yfull, rready, dfull, dready, zfull, fin;
+    uint64_t kfull[kKSlots], kempty[kKSlots];   // k ring
+    uint64_t vfull[2], vempty[2];               // {v, M2} ring
+    uint64_t wfull;               // W^T accumulated
+    // -W^T operand of a chunk written (and the W^T TMEM columns free), one per operand slot:
+    // the P half's issuer may lag, so one barrier could be two phases ahead of its wait
+    uint64_t wready[2];
+    uint64_t wfree[2];            // d_P has read a -W^T slot (d_S is ordered by wfull)
+    uint64_t m1ready[2];          // M1 (and the slot) of a chunk, one barrier per slot
+    uint64_t zready[2], dfull[2], dready[2], zfull[2];   // per half
+    uint64_t fin[2];
 };
 
-// Named barrier of the 128 prep threads. The non-aligned form counts threads, not warps,
-// so it stays correct when the lanes of a warp reach it at different times (for example
-// lane 0 returning later from an mbarrier wait than its warp-mates); __syncwarp first
-// reconverges the warp anyway.
-__device__ __forceinline__ void bar_prep() {
+// Named barrier of the 128 operand-warp threads, and the same with an AND of a predicate
+// (every thread leaves with the same outcome). Non-aligned forms: the lanes of a warp may
+// arrive at different times.
+__device__ __forceinline__ void bar_aux() {
     __syncwarp();
-    asm volatile("barrier.sync 1, 128;" ::: "memory");
+    asm volatile("barrier.sync 2, 128;" ::: "memory");
+}
+__device__ __forceinline__ bool bar_aux_and(bool v) {
+    uint32_t r;
+    __syncwarp();
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "barrier.red.and.pred po, 2, 128, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ uint32_t bf2(float lo, float hi) { return pack_bf16x2(lo, hi); }
 
-// One level of the blocked inverse M = (I + A)^-1 (64 x 64, 16 x 16 blocks): the NB = 4 - L
-// blocks (a, b) with a - b = L, from M_ab = -M_aa sum_{k=b}^{a-1} A_ak M_kb. Prep thread q
-// owns entries (row r0 + 8h, column j) of every block, r0 = q / 16, j = q % 16, h = 0, 1;
-// all loops are compile-time so the independent dot products interleave.
-template <int L>
-__device__ __forceinline__ void inverse_level(const float *A32, float *M32, float *T32, int q) {
-    constexpr int NB = 4 - L;
-    const int j = q & 15, r0 = q >> 4;
-    float t[2 * NB];
+__device__ __forceinline__ void ld64(uint32_t taddr, uint32_t (&z)[64]) {
+    tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&z[0]));
+    tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&z[32]));
+}
+
+// 64 fp32 values of this lane -> 32 TMEM columns of bf16 pairs (even element in the low
+// half), the A-operand form of a kind::f16 MMA with A in TMEM.
+__device__ __forceinline__ void st_bf16x64(uint32_t taddr, const uint32_t (&z)[64]) {
 #pragma unroll
-    for (int m = 0; m < 2 * NB; ++m) t[m] = 0.f;
+    for (int g = 0; g < 2; ++g) {
+        uint32_t pk[16];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-#pragma unroll
-        for (int k = b; k < b + L; ++k) {
-            float mc[16];
-#pragma unroll
-            for (int s = 0; s < 16; ++s) mc[s] = M32[(16 * k + s) * C + 16 * b + j];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const float4 *ar = reinterpret_cast<const float4 *>(A32 + (16 * (b + L) + r0 + 8 * hh) * kLDA + 16 * k);
-#pragma unroll
-                for (int s4 = 0; s4 < 4; ++s4) {
-                    const float4 x = ar[s4];
-                    float &acc = t[2 * b + hh];
-                    acc = fmaf(x.x, mc[4 * s4 + 0], acc);
-                    acc = fmaf(x.y, mc[4 * s4 + 1], acc);
-                    acc = fmaf(x.z, mc[4 * s4 + 2], acc);
-                    acc = fmaf(x.w, mc[4 * s4 + 3], acc);
-                }
-            }
-        }
+        for (int j = 0; j < 16; ++j)
+            pk[j] = bf2(__uint_as_float(z[32 * g + 2 * j]), __uint_as_float(z[32 * g + 2 * j + 1]));
+        tmem_st16(taddr + 16 * g, pk);
     }
-#pragma unroll
-    for (int b = 0; b < NB; ++b)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) T32[b * 256 + (r0 + 8 * hh) * 16 + j] = t[2 * b + hh];
-    bar_prep();
-    float res[2 * NB];   // all loads first, then the stores (no load/store interleaving)
-#pragma unroll
-    for (int b = 0; b < NB; ++b) {
-        const int a = b + L;
-        float tc[16];
-#pragma unroll
-        for (int s = 0; s < 16; ++s) tc[s] = T32[b * 256 + s * 16 + j];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int r = r0 + 8 * hh;
-            const float4 *mr = reinterpret_cast<const float4 *>(M32 + (16 * a + r) * C + 16 * a);
-            float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4) {
-                const float4 x = mr[s4];
-                acc0 = fmaf(x.x, tc[4 * s4 + 0], acc0);
-                acc1 = fmaf(x.y, tc[4 * s4 + 1], acc1);
-                acc0 = fmaf(x.z, tc[4 * s4 + 2], acc0);
-                acc1 = fmaf(x.w, tc[4 * s4 + 3], acc1);
-            }
-            res[2 * b + hh] = -(acc0 + acc1);
-        }
-    }
-#pragma unroll
-    for (int b = 0; b < NB; ++b)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) M32[(16 * (b + L) + r0 + 8 * hh) * C + 16 * b + j] = res[2 * b + hh];
-    bar_prep();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmR) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-aligned base, derived by offsetting the shared array itself so that the
     // compiler keeps the shared address space (plain ld/st.shared, not generic accesses)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ Bars bars;
+    __shared__ __align__(16) Slot slots[2];
     __shared__ uint32_t tslot;
     __shared__ volatile int abort_flag;
     __shared__ float scan_tmp[2];
-    __shared__ int prep_flag[2];
 
     const int warp = warp_id(), lane = lane_id();
     const SegEntry seg = p.seg[blockIdx.x / p.H_v];
@@ -180,24 +160,26 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
     const int hk = h / p.gqa;
     const int nch = (seg.len + C - 1) / C;
     const bool gdn = p.family == HYPIC_FAM_GDN;
-    Vec *vec = reinterpret_cast<Vec *>(smem + kOffVec);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars.kv_full[s], 1);
-            mbar_init(&bars.kv_empty[s], 1);
+        for (int s = 0; s < kKSlots; ++s) {
+            mbar_init(&bars.kfull[s], 1);
+            mbar_init(&bars.kempty[s], 2);   // both halves' updates read the k chunk
         }
-        mbar_init(&bars.gfull[0], 1);
-        mbar_init(&bars.gfull[1], 1);
-        for (int s = 0; s < 3; ++s) mbar_init(&bars.vready[s], 128);
-        mbar_init(&bars.mready, 128);
-        mbar_init(&bars.zbf_ready, 128);
-        mbar_init(&bars.yfull, 1);
-        mbar_init(&bars.rready, 128);
-        mbar_init(&bars.dfull, 1);
-        mbar_init(&bars.dready, 128);
-        mbar_init(&bars.zfull, 1);
-        mbar_init(&bars.fin, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars.vfull[s], 1);
+            mbar_init(&bars.vempty[s], 1);
+            mbar_init(&bars.m1ready[s], 128);
+            mbar_init(&bars.zready[s], 128);
+            mbar_init(&bars.dfull[s], 1);
+            mbar_init(&bars.dready[s], 128);
+            mbar_init(&bars.zfull[s], 1);
+            mbar_init(&bars.wfree[s], 1);
+            mbar_init(&bars.wready[s], 128);
+        }
+        mbar_init(&bars.wfull, 1);
+        mbar_init(&bars.fin[0], 1);
+        mbar_init(&bars.fin[1], 1);
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -209,418 +191,326 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
     auto wait = [&](uint64_t *b, uint32_t par) {
         return mbar_wait_or_abort(b, par, p.err, kErrTimeout, &abort_flag);
     };
+    // every lane waits; the warp leaves with one outcome (tcgen05.ld / st are warp-wide)
+    auto wwait = [&](uint64_t *b, uint32_t par) { return __all_sync(0xffffffffu, wait(b, par)) != 0; };
 
     if (warp == kProducerWarp) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
-            int c = 0;
+            prefetch_tmap(&tmR);
+            int c = 0, kc = 0;   // chunks whose {v, M2} / k loads were issued
             for (; c < nch; ++c) {
-                const int s = c & 1, use = c >> 1;
-                if (use >= 1 && !wait(&bars.kv_empty[s], (use - 1) & 1)) break;
-                uint8_t *st = smem + kOffStage + s * kStage;
                 const int32_t t0 = seg.start + c * C;
-                mbar_arrive_expect_tx(&bars.kv_full[s], kStage);
-                tma_load_3d(st, &tmK, &bars.kv_full[s], 0, hk, t0);
-                tma_load_3d(st + kKTile / 2, &tmK, &bars.kv_full[s], 64, hk, t0);
-                tma_load_3d(st + kKTile, &tmV, &bars.kv_full[s], 0, h, t0);
-                tma_load_3d(st + kKTile + kKTile / 2, &tmV, &bars.kv_full[s], 64, h, t0);
+                const int ks = c % kKSlots, kuse = c / kKSlots;
+                if (kuse >= 1 && !wait(&bars.kempty[ks], (kuse - 1) & 1)) break;
+                uint8_t *kt = smem + kOffK + ks * kKV;
+                mbar_arrive_expect_tx(&bars.kfull[ks], kKV);
+                tma_load_3d(kt, &tmK, &bars.kfull[ks], 0, hk, t0);
+                tma_load_3d(kt + kHalf, &tmK, &bars.kfull[ks], 64, hk, t0);
+                kc = c + 1;
+                const int vs = c & 1, vuse = c >> 1;
+                if (vuse >= 1 && !wait(&bars.vempty[vs], (vuse - 1) & 1)) break;
+                uint8_t *vt = smem + kOffVR + vs * kVR;
+                const int32_t rrow = (seg.wsb + h * nch + c) * 64;
+                mbar_arrive_expect_tx(&bars.vfull[vs], kVR);
+                tma_load_3d(vt, &tmV, &bars.vfull[vs], 0, h, t0);
+                tma_load_3d(vt + kHalf, &tmV, &bars.vfull[vs], 64, h, t0);
+                tma_load_2d(vt + kKV, &tmR, &bars.vfull[vs], 0, rrow);
             }
-            if (abort_flag)
+            if (abort_flag) {   // let the loads in flight land before the CTA exits
+                for (int q = (kc > kKSlots ? kc - kKSlots : 0); q < kc; ++q)
+                    mbar_wait(&bars.kfull[q % kKSlots], (q / kKSlots) & 1, p.err, kErrTimeout);
                 for (int q = (c > 2 ? c - 2 : 0); q < c; ++q)
-                    mbar_wait(&bars.kv_full[q & 1], (q >> 1) & 1, p.err, kErrTimeout);
+                    mbar_wait(&bars.vfull[q & 1], (q >> 1) & 1, p.err, kErrTimeout);
+            }
         }
-    } else if (warp == kMmaWarp) {
-        // ---------------------------------------------------------------- MMA issuer
+    } else if (warp == kMmaWarpS || warp == kMmaWarpP) {
+        // ---------------------------------------------------------------- MMA issuers
+        // Two issuing threads, one per state half: the tensor pipe queues only a few
+        // instructions, so a thread that waits between its groups leaves it idle unless the
+        // other half has work queued. Every descriptor is built once; an MMA then costs a
+        // 64-bit add and the issue itself.
         if (lane == 0 && nch > 0) {
-            constexpr uint32_t idG = idesc(kFmtBF16, kFmtBF16, false, false, 64, 64);
-            constexpr uint32_t idKK = idesc(kFmtBF16, kFmtBF16, false, false, 128, 64);
-            constexpr uint32_t idZ = idesc(kFmtBF16, kFmtBF16, false, true, 128, 128);
-            const uint32_t sb = smem_u32(smem);
-            auto issue_gram = [&](int c) -> bool {
-                if (!wait(&bars.kv_full[c & 1], (c >> 1) & 1)) return false;
-                tc_fence_after();
-                const uint32_t k = sb + kOffStage + (c & 1) * kStage;
-#pragma unroll
-                for (int s = 0; s < 8; ++s) {
-                    const uint32_t a = k + (s >> 2) * (kKTile / 2) + (s & 3) * 32;
-                    mma_bf16(tmem + kTG + 64 * (c & 1), sdesc(a, 16, 1024, kSwizzle128B),
-                             sdesc(a, 16, 1024, kSwizzle128B), idG, s > 0);
-                }
-                mma_commit(&bars.gfull[c & 1]);
-                return true;
+            auto wait = [&](uint64_t *b, uint32_t par) {
+                return mbar_wait_or_abort(b, par, p.err, kErrTimeout, &abort_flag, true);
             };
-            bool ok = issue_gram(0);
-            for (int c = 0; ok && c < nch; ++c) {
-                const uint32_t k = sb + kOffStage + (c & 1) * kStage;
-                // Y^T = Z^T K^T (S~ and P halves)
-                if (!(ok = wait(&bars.zbf_ready, c & 1))) break;
-                tc_fence_after();
+            constexpr uint32_t idA = idesc(kFmtBF16, kFmtBF16, true, false, 128, 64);
+            constexpr uint32_t idD = idesc(kFmtBF16, kFmtBF16, false, true, 128, 64);
+            constexpr uint32_t idF = idesc(kFmtBF16, kFmtBF16, false, true, 128, 128);
+            const uint32_t sb = smem_u32(smem);
+            const uint64_t dK = sdesc(sb + kOffK, kHalf, 1024, kSwizzle128B);         // MN-major
+            const uint64_t dV = sdesc(sb + kOffVR, kHalf, 1024, kSwizzle128B);        // MN-major
+            const uint64_t dR = sdesc(sb + kOffVR + kKV, 16, 1024, kSwizzle128B);     // K-major
+            const uint64_t dW = sdesc(sb + kOffWop, kHalf, 1024, kSwizzle128B);       // MN-major
+            const uint64_t dM = sdesc(sb + kOffM1, 16, 1024, kSwizzle128B);           // K-major
+            constexpr uint64_t kRow16 = 2048 >> 4;   // 16 rows of 128 B (MN-major K step)
+            constexpr uint64_t kCol16 = 32 >> 4;     // 16 bf16 columns (K-major K step)
+            const int hf = warp == kMmaWarpS ? 0 : 1;
+            // D^T(hf) += Z^T(hf) (-W^T) with A = bf16 Z^T in TMEM (the P half starts from zero)
+            auto issue_d = [&](int c) {
+                const uint64_t b = dW + (((c & 1) * kKV) >> 4);
+                const uint32_t d = tmem + kTD + 64 * hf, a = tmem + kTZK + 64 * hf;
+                mma_bf16_ta(d, a, b, idD, hf == 0 ? 1u : 0u);
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
+                for (int s = 1; s < 8; ++s) mma_bf16_ta(d, a + 8 * s, b + s * kRow16, idD, 1u);
+                mma_commit(&bars.dfull[hf]);
+            };
+            // Z^T(hf) += D^T(hf) K(c) with A = bf16 D^T in TMEM; with the other half's update
+            // it frees the k slot
+            auto issue_f = [&](int c) {
+                const uint64_t b = dK + (((c % kKSlots) * kKV) >> 4);
+                const uint32_t d = tmem + kTZ + 128 * hf, a = tmem + kTD + 64 * hf;
 #pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        const uint32_t a = sb + kOffAZ + (s >> 2) * 32768 + hf * 16384 + (s & 3) * 32;
-                        const uint32_t b = k + (s >> 2) * (kKTile / 2) + (s & 3) * 32;
-                        mma_bf16(tmem + kTY + 64 * hf, sdesc(a, 16, 1024, kSwizzle128B),
-                                 sdesc(b, 16, 1024, kSwizzle128B), idKK, s > 0);
+                for (int s = 0; s < 4; ++s) mma_bf16_ta(d, a + 8 * s, b + s * kRow16, idF, 1u);
+                mma_commit(&bars.zfull[hf]);
+                mma_commit(&bars.kempty[c % kKSlots]);
+            };
+            bool ok = true;
+            if (hf == 0) {
+                // W^T(c) = K^T M2^T into the S~ half's bf16-Z^T columns (A: the k chunk read
+                // MN-major, B: the M2 record K-major)
+                auto issue_w = [&](int c) {
+                    const uint64_t a = dK + (((c % kKSlots) * kKV) >> 4), b = dR + (((c & 1) * kVR) >> 4);
+                    mma_bf16(tmem + kTZK, a, b, idA, 0u);
+#pragma unroll
+                    for (int s = 1; s < 4; ++s) mma_bf16(tmem + kTZK, a + s * kRow16, b + s * kCol16, idA, 1u);
+                    mma_commit(&bars.wfull);
+                };
+                // D_S^T(c) = V^T M1^T (A: the v chunk read MN-major, B: M1 K-major); frees the
+                // {v, M2} slot of chunk c
+                auto issue_u = [&](int c) {
+                    const uint64_t a = dV + (((c & 1) * kVR) >> 4), b = dM + (((c & 1) * kRec) >> 4);
+                    mma_bf16(tmem + kTD, a, b, idA, 0u);
+#pragma unroll
+                    for (int s = 1; s < 4; ++s) mma_bf16(tmem + kTD, a + s * kRow16, b + s * kCol16, idA, 1u);
+                    mma_commit(&bars.vempty[c & 1]);
+                };
+                // per chunk: d_S(c), W(c+1), f_S(c), U(c+1). W(c+1) overwrites the columns
+                // d_S(c) reads as A and U(c+1) the D_S columns f_S(c) reads as A, so each is
+                // issued only once that product's completion has been observed.
+                ok = wait(&bars.kfull[0], 0) && wait(&bars.vfull[0], 0);
+                if (ok) {
+                    tc_fence_after();
+                    issue_w(0);
+                    if ((ok = wait(&bars.m1ready[0], 0))) {
+                        tc_fence_after();
+                        issue_u(0);
                     }
-                mma_commit(&bars.yfull);
-                // the next chunk's gram, into the other slot
-                if (c + 1 < nch && !(ok = issue_gram(c + 1))) break;
-                // (M R)^T = R^T M^T
-                if (!(ok = wait(&bars.rready, c & 1) && wait(&bars.mready, c & 1))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        mma_bf16(tmem + kTY + 64 * hf,
-                                 sdesc(sb + kOffAR + hf * 16384 + s * 32, 16, 1024, kSwizzle128B),
-                                 sdesc(sb + kOffBM + s * 32, 16, 1024, kSwizzle128B), idKK, s > 0);
-                mma_commit(&bars.dfull);
-                // Z^T += D'^T K
-                if (!(ok = wait(&bars.dready, c & 1))) break;
-                tc_fence_after();
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        mma_bf16(tmem + kTZ + 128 * hf,
-                                 sdesc(sb + kOffAR + hf * 16384 + s * 32, 16, 1024, kSwizzle128B),
-                                 sdesc(k + s * 2048, kKTile / 2, 1024, kSwizzle128B), idZ, 1);
-                mma_commit(&bars.zfull);
-                mma_commit(&bars.kv_empty[c & 1]);
+                }
+                for (int c = 0; ok && c < nch; ++c) {
+                    const bool more = c + 1 < nch;
+                    if (!(ok = wait(&bars.wready[c & 1], (c >> 1) & 1) && wait(&bars.zready[0], c & 1))) break;
+                    tc_fence_after();
+                    issue_d(c);
+                    if (more) {
+                        if (!(ok = wait(&bars.dfull[0], c & 1) && wait(&bars.kfull[(c + 1) % kKSlots], ((c + 1) / kKSlots) & 1) &&
+                                   wait(&bars.vfull[(c + 1) & 1], ((c + 1) >> 1) & 1)))
+                            break;
+                        tc_fence_after();
+                        issue_w(c + 1);
+                    }
+                    if (!(ok = wait(&bars.dready[0], c & 1))) break;
+                    tc_fence_after();
+                    issue_f(c);
+                    if (more) {
+                        if (!(ok = wait(&bars.zfull[0], c & 1) && wait(&bars.m1ready[(c + 1) & 1], ((c + 1) >> 1) & 1)))
+                            break;
+                        tc_fence_after();
+                        issue_u(c + 1);
+                    }
+                }
+            } else {
+                // per chunk: d_P(c) (frees the -W^T slot for the operand warps), f_P(c).
+                // zready_P(c) implies f_P(c-1) is complete (the P half waited for it).
+                for (int c = 0; ok && c < nch; ++c) {
+                    if (!(ok = wait(&bars.wready[c & 1], (c >> 1) & 1) && wait(&bars.zready[1], c & 1))) break;
+                    tc_fence_after();
+                    issue_d(c);
+                    mma_commit(&bars.wfree[c & 1]);
+                    if (!(ok = wait(&bars.dready[1], c & 1))) break;
+                    tc_fence_after();
+                    issue_f(c);
+                }
             }
-            if (abort_flag) {
-                mma_commit(&bars.fin);
-                mbar_wait(&bars.fin, 0, p.err, kErrTimeout);
+            if (!ok) {   // let this thread's MMAs in flight finish before the CTA exits
+                mma_commit(&bars.fin[hf]);
+                mbar_wait(&bars.fin[hf], 0, p.err, kErrTimeout);
             }
         }
-    } else if (warp >= kPrepWarp0) {
-        // ---------------------------------------------------------------- prep warps 4-7
-        const int q = threadIdx.x - 128;          // 0..127
+    } else if (warp >= kAuxWarp0 && warp < kProducerWarp) {
+        // ---------------------------------------------------------------- operand warps 8-11
+        const int q = threadIdx.x - 32 * kAuxWarp0;    // 0..127 = TMEM lane of W^T
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-        float *A32 = reinterpret_cast<float *>(smem + kOffA32);
-        float *M32 = reinterpret_cast<float *>(smem + kOffM32);
-        float *T32 = reinterpret_cast<float *>(smem + kOffT);
-        float b_next = 0.f, la_next = 0.f;   // gates of the next chunk (thread q < 64: token q)
-        if (q < C && nch > 0) {
+        float Lam = 0.f, lam_sum = 0.f;
+        float la_next = 0.f;   // log-gate of the next chunk (thread q < 64: token q)
+        if (q < C && nch > 0 && gdn) {
             const int64_t tok = (int64_t)seg.start + q;
-            const bool in = q < min(C, seg.len);
-            b_next = in ? p.beta[tok * p.H_v + h] : 0.f;
-            la_next = (in && gdn) ? p.log_gate[tok * p.H_v + h] : 0.f;
+            la_next = q < min(C, seg.len) ? p.log_gate[tok * p.H_v + h] : 0.f;
         }
-        // one elected thread waits; the outcome reaches the other 127 through the named
-        // barrier, so every prep thread takes the same branch (no thread is left behind
-        // at a barrier when a wait gives up)
-        uint32_t nw = 0;
-        auto pwait = [&](uint64_t *b, uint32_t par) -> bool {
-            volatile int *f = &prep_flag[nw & 1];
-            if (q == 0) *f = wait(b, par) ? 1 : 0;
-            bar_prep();
-            const bool r = *f != 0;
-            ++nw;
-            return r;
-        };
-        for (int c = 0; c < nch; ++c) {   // leaves only through a broadcast pwait outcome
-            // (a) gates of chunk c (loaded one chunk ahead into registers), prefix sums.
-            //     Slot c % 3 was last read by the chain for chunk c - 3, long finished.
-            Vec &v = vec[c % 3];
-            const int valid = min(C, seg.len - c * C);
-            float b_cur = b_next, la_cur = la_next;
-            if (q < C && c + 1 < nch) {
+        for (int c = 0; c < nch; ++c) {
+            Slot &sl = slots[c & 1];
+            // (1) gates: prefix sums c_t, chunk total c_C, the log-scale bookkeeping.
+            //     Slot c % 2 was last read for chunk c - 2, whose W product has been issued.
+            float x = la_next;
+            if (q < C && gdn && c + 1 < nch) {
                 const int64_t tok = (int64_t)seg.start + (c + 1) * C + q;
-                const bool in = q < min(C, seg.len - (c + 1) * C);
-                b_next = in ? p.beta[tok * p.H_v + h] : 0.f;
-                la_next = (in && gdn) ? p.log_gate[tok * p.H_v + h] : 0.f;
+                la_next = q < min(C, seg.len - (c + 1) * C) ? p.log_gate[tok * p.H_v + h] : 0.f;
             }
             if (q < C) {
-                if (q >= valid) b_cur = la_cur = 0.f;
-                float x = la_cur;
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const float y = __shfl_up_sync(0xffffffffu, x, o);
                     if (lane >= o) x += y;
                 }
                 if (lane == 31) scan_tmp[q >> 5] = x;
-                v.beta[q] = b_cur;
-                v.c[q] = x;
             }
-            bar_prep();
-            if (q < C) {
-                const float cc = q >= 32 ? v.c[q] + scan_tmp[0] : v.c[q];
-                const float e = expf(cc);
-                v.c[q] = cc;
-                v.ecp[q] = e;
-                v.ecm[q] = expf(-cc);
-                v.bec[q] = v.beta[q] * e;
-                if (q == C - 1) {
-                    v.cC = cc;
-                    if (cc < kMinChunkLogDecay) atomicOr(p.err, kErrRange);
-                }
+            bar_aux();
+            const float cC = scan_tmp[0] + scan_tmp[1];
+            const bool renorm = Lam + cC < kRenormBelow;
+            const float lam0 = renorm ? 0.f : Lam;
+            if (q < C) sl.ex[q] = expf(-lam0 - (q >= 32 ? x + scan_tmp[0] : x));
+            if (q == 0) {
+                sl.renorm = renorm ? 1 : 0;
+                sl.rscale = expf(Lam);
+                sl.lam_after = lam0 + cC;
+                sl.lam_sum = lam_sum + cC;
+                if (cC < kMinChunkLogDecay) atomicOr(p.err, kErrRange);
             }
-            mbar_arrive(&bars.vready[c % 3]);
-            // (b) gram -> A (rows t = 16 (warp - 4) + lane for lanes < 16), padded rows
-            if (!pwait(&bars.gfull[c & 1], (c >> 1) & 1)) break;
-            tc_fence_after();
+            Lam = lam0 + cC;
+            lam_sum += cC;
+            bar_aux();   // ex visible; every read of scan_tmp done before the next writes
+            // (2) M1[t'][t] = M2[t'][t] exp(-Lam_start - c_t), same swizzled layout
+            if (!bar_aux_and(wait(&bars.vfull[c & 1], (c >> 1) & 1))) break;
             {
-                const int t = 16 * (warp - kPrepWarp0) + lane;
-                uint32_t g[64];
-                const uint32_t gcol = kTG + 64 * (c & 1);
-                tmem_ld32(tmem + lane_off + gcol, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
-                tmem_ld32(tmem + lane_off + gcol + 32, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
-                tmem_ld_wait();
-                if (lane < 16) {
-                    // all loads before any store (stores to A may not pass loads from the
-                    // same shared memory, so interleaving them would serialise the loop)
-                    const float bt = v.beta[t] * v.ecp[t];
-                    float em[C];
-#pragma unroll
-                    for (int s4 = 0; s4 < C / 4; ++s4) {
-                        const float4 e4 = reinterpret_cast<const float4 *>(v.ecm)[s4];
-                        em[4 * s4] = e4.x, em[4 * s4 + 1] = e4.y, em[4 * s4 + 2] = e4.z, em[4 * s4 + 3] = e4.w;
-                    }
-                    float4 *row = reinterpret_cast<float4 *>(A32 + t * kLDA);
-#pragma unroll
-                    for (int s4 = 0; s4 < C / 4; ++s4) {
-                        float4 a4;
-                        const int s2 = 4 * s4;
-                        a4.x = s2 + 0 < t ? bt * __uint_as_float(g[s2 + 0]) * em[s2 + 0] : 0.f;
-                        a4.y = s2 + 1 < t ? bt * __uint_as_float(g[s2 + 1]) * em[s2 + 1] : 0.f;
-                        a4.z = s2 + 2 < t ? bt * __uint_as_float(g[s2 + 2]) * em[s2 + 2] : 0.f;
-                        a4.w = s2 + 3 < t ? bt * __uint_as_float(g[s2 + 3]) * em[s2 + 3] : 0.f;
-                        row[s4] = a4;
-                    }
-                }
-            }
-            tc_fence_before();
-            bar_prep();
-            // (c) M = (I + A)^-1 by 16 x 16 blocks: diagonal blocks by forward substitution
-            //     (thread = one column of one block, each row's A entries loaded ahead),
-            //     then the blocks below the diagonal level by level.
-            if (q < C) {
-                const int a = q >> 4, j = q & 15;
-                float x[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const float4 *Ar = reinterpret_cast<const float4 *>(A32 + (16 * a + r) * kLDA + 16 * a);
-                    float ar[16];
-#pragma unroll
-                    for (int s4 = 0; s4 < 4; ++s4) {
-                        const float4 t4 = Ar[s4];
-                        ar[4 * s4] = t4.x, ar[4 * s4 + 1] = t4.y, ar[4 * s4 + 2] = t4.z, ar[4 * s4 + 3] = t4.w;
-                    }
-                    float acc[4] = {(r == j) ? 1.f : 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int s2 = 0; s2 < r; ++s2) acc[s2 & 3] = fmaf(-ar[s2], x[s2], acc[s2 & 3]);
-                    x[r] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-                }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) M32[(16 * a + r) * C + 16 * a + j] = x[r];
-            } else {
-                // zero the six blocks above the diagonal
-                for (int e = q - C; e < 6 * 256; e += C) {
-                    const int blk = e >> 8, r = (e >> 4) & 15, j = e & 15;
-                    const int a = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                    const int b = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                    M32[(16 * a + r) * C + 16 * b + j] = 0.f;
-                }
-            }
-            bar_prep();
-            inverse_level<1>(A32, M32, T32, q);
-            inverse_level<2>(A32, M32, T32, q);
-            inverse_level<3>(A32, M32, T32, q);
-            // (d) M as bf16 K-major rows t, once the M R product of chunk c - 1 has read it
-            if (c >= 1 && !pwait(&bars.dfull, (c - 1) & 1)) break;
-            {
-                uint8_t *bm = smem + kOffBM;
+                const uint8_t *rec = smem + kOffVR + (c & 1) * kVR + kKV;
+                uint8_t *m1 = smem + kOffM1 + (c & 1) * kRec;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
-                    const int e8 = q + 128 * m;            // 8 consecutive entries of row t
-                    const int t = e8 >> 3, s8 = (e8 & 7) * 8;
-                    const float4 lo = reinterpret_cast<const float4 *>(M32 + t * C + s8)[0];
-                    const float4 hi = reinterpret_cast<const float4 *>(M32 + t * C + s8)[1];
-                    *reinterpret_cast<uint4 *>(bm + sw128(t, 2 * s8)) =
-                        make_uint4(bf2(lo.x, lo.y), bf2(lo.z, lo.w), bf2(hi.x, hi.y), bf2(hi.z, hi.w));
+                    const int e = q + 128 * m;   // 16-byte piece: row t', columns 8 t8 .. 8 t8 + 7
+                    const int tp = e >> 3, t8 = e & 7;
+                    const uint32_t off = sw128(tp, 16 * t8);
+                    const uint4 r = *reinterpret_cast<const uint4 *>(rec + off);
+                    const float4 e0 = reinterpret_cast<const float4 *>(sl.ex + 8 * t8)[0];
+                    const float4 e1 = reinterpret_cast<const float4 *>(sl.ex + 8 * t8)[1];
+                    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+                    float f[8];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        f[2 * j] = __uint_as_float(w[j] << 16);
+                        f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+                    }
+                    *reinterpret_cast<uint4 *>(m1 + off) =
+                        make_uint4(bf2(f[0] * e0.x, f[1] * e0.y), bf2(f[2] * e0.z, f[3] * e0.w),
+                                   bf2(f[4] * e1.x, f[5] * e1.y), bf2(f[6] * e1.z, f[7] * e1.w));
                 }
             }
             fence_async_shared();
-            mbar_arrive(&bars.mready);
+            mbar_arrive(&bars.m1ready[c & 1]);
+            // (3) W^T(c) -> -W^T bf16, MN-major B operand (row i = this thread's lane). The
+            //     slot was last read by d_S(c-2) (ordered before W(c) by its issuer) and by
+            //     d_P(c-2), whose completion is signalled on wfree.
+            if (!bar_aux_and(wait(&bars.wfull, c & 1) &&
+                             (c < 2 || wait(&bars.wfree[c & 1], ((c - 2) >> 1) & 1))))
+                break;
+            tc_fence_after();
+            {
+                uint32_t z[64];
+                ld64(tmem + lane_off + kTZK, z);
+                tmem_ld_wait();
+                uint8_t *wop = smem + kOffWop + (c & 1) * kKV;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint4 pk;
+                    pk.x = bf2(-__uint_as_float(z[8 * j + 0]), -__uint_as_float(z[8 * j + 1]));
+                    pk.y = bf2(-__uint_as_float(z[8 * j + 2]), -__uint_as_float(z[8 * j + 3]));
+                    pk.z = bf2(-__uint_as_float(z[8 * j + 4]), -__uint_as_float(z[8 * j + 5]));
+                    pk.w = bf2(-__uint_as_float(z[8 * j + 6]), -__uint_as_float(z[8 * j + 7]));
+                    *reinterpret_cast<uint4 *>(wop + sw128((uint32_t)q, 16 * j)) = pk;
+                }
+            }
+            fence_async_shared();
+            tc_fence_before();
+            mbar_arrive(&bars.wready[c & 1]);
         }
     } else {
-        // ---------------------------------------------------------------- chain warps 0-3
-        const int n = threadIdx.x;   // state column (and TMEM lane)
-        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        float Lam = 0.f, lam_total = 0.f;
-        // Z^T = [0 | I]
-        {
+        // ---------------------------------------------------------------- chain warps 0-7
+        const int hf = warp >> 2;                  // 0: S~ half, 1: P half
+        const int n = threadIdx.x & 127;           // state column = TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t zcol = kTZ + 128 * hf, dcol = kTD + 64 * hf, zkcol = kTZK + 64 * hf;
+        {   // Z^T = 0 (S~ half) or I (P half); the TMEM address of a warp-wide store must be
+            // the same in all lanes, so every lane stores every column group
             uint32_t z[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) z[j] = 0u;
-#pragma unroll
-            for (int c0 = 0; c0 < 256; c0 += 16) tmem_st16(tmem + lane_off + kTZ + c0, z);
-            tmem_st_wait();
-            // identity in the P half: every lane stores every column group (the TMEM
-            // address of a warp-wide store must be the same in all lanes)
 #pragma unroll
             for (int c0 = 0; c0 < 128; c0 += 16) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) z[j] = (c0 + j == n) ? __float_as_uint(1.f) : 0u;
-                tmem_st16(tmem + lane_off + kTZ + 128 + c0, z);
+                for (int j = 0; j < 16; ++j) z[j] = (hf == 1 && c0 + j == n) ? __float_as_uint(1.f) : 0u;
+                tmem_st16(tmem + lane_off + zcol + c0, z);
             }
             tmem_st_wait();
         }
-        uint8_t *az = smem + kOffAZ, *ar = smem + kOffAR;
-        const uint32_t vhalf = (uint32_t)(n >> 6) * (kKTile / 2), vbyte = (uint32_t)(n & 63) * 2;
         bool ok = true;
         for (int c = 0; ok && c < nch; ++c) {
-            // (1) Z^T -> bf16 A operand (renormalising S~ when the log-scale got small)
-            if (c >= 1 && !(ok = wait(&bars.zfull, (c - 1) & 1))) break;
-            tc_fence_after();
-            const bool renorm = Lam < kRenorm;
-            const float sc = renorm ? expf(Lam) : 1.f;
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-#pragma unroll
-                for (int cb = 0; cb < 2; ++cb) {   // 64 key rows per batch: K-block cb
-                    uint32_t z[64];
-                    const uint32_t col = kTZ + 128 * hf + 64 * cb;
-                    tmem_ld32(tmem + lane_off + col, *reinterpret_cast<uint32_t(*)[32]>(&z[0]));
-                    tmem_ld32(tmem + lane_off + col + 32, *reinterpret_cast<uint32_t(*)[32]>(&z[32]));
-                    tmem_ld_wait();
-                    if (hf == 0 && renorm) {
-#pragma unroll
-                        for (int j = 0; j < 64; ++j) z[j] = __float_as_uint(__uint_as_float(z[j]) * sc);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            tmem_st16(tmem + lane_off + col + 16 * j, *reinterpret_cast<uint32_t(*)[16]>(&z[16 * j]));
-                    }
-                    uint8_t *rowb = az + cb * 32768;
-                    const uint32_t r = 128 * hf + n;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        uint4 pk;
-                        pk.x = bf2(__uint_as_float(z[8 * j + 0]), __uint_as_float(z[8 * j + 1]));
-                        pk.y = bf2(__uint_as_float(z[8 * j + 2]), __uint_as_float(z[8 * j + 3]));
-                        pk.z = bf2(__uint_as_float(z[8 * j + 4]), __uint_as_float(z[8 * j + 5]));
-                        pk.w = bf2(__uint_as_float(z[8 * j + 6]), __uint_as_float(z[8 * j + 7]));
-                        *reinterpret_cast<uint4 *>(rowb + sw128(r, 16 * j)) = pk;
-                    }
-                }
+            // (1) Z^T -> bf16 A operand in TMEM (S~ half: multiplied by exp(Lam) first on a
+            //     reset). The S~ half's bf16 columns hold W^T(c) until its pass has read it.
+            if (c >= 1 && !(ok = wwait(&bars.zfull[hf], (c - 1) & 1))) break;
+            bool renorm = false;
+            float rs = 1.f;
+            if (hf == 0) {
+                if (!(ok = wwait(&bars.m1ready[c & 1], (c >> 1) & 1) && wwait(&bars.wready[c & 1], (c >> 1) & 1)))
+                    break;
+                renorm = slots[c & 1].renorm != 0;
+                rs = slots[c & 1].rscale;
             }
-            if (renorm) {
-                tmem_st_wait();
-                Lam = 0.f;
-            }
-            fence_async_shared();
-            tc_fence_before();
-            mbar_arrive(&bars.zbf_ready);
-            // (2) R^T[n][t] = b_t (exp(-Lam) V[t][n] - e^{c_t} Y_S^T[n][t]), -b_t e^{c_t} Y_P^T[n][t]
-            if (!(ok = wait(&bars.vready[c % 3], (c / 3) & 1) && wait(&bars.yfull, c & 1))) break;
             tc_fence_after();
-            const Vec &v = vec[c % 3];
-            const float eL = expf(-Lam);
-            const uint8_t *vt = smem + kOffStage + (c & 1) * kStage + kKTile + vhalf;
 #pragma unroll
-            for (int c0 = 0; c0 < C; c0 += 32) {
-                uint32_t ys[32], yp[32];
-                tmem_ld32(tmem + lane_off + kTY + c0, ys);
-                tmem_ld32(tmem + lane_off + kTY + 64 + c0, yp);
-                // every shared-memory load of the batch before its stores
-                float vv[32], bb[32], be[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    vv[j] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(vt + sw128(c0 + j, vbyte)));
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 b4 = reinterpret_cast<const float4 *>(v.beta + c0)[j4];
-                    const float4 e4 = reinterpret_cast<const float4 *>(v.bec + c0)[j4];
-                    bb[4 * j4] = b4.x, bb[4 * j4 + 1] = b4.y, bb[4 * j4 + 2] = b4.z, bb[4 * j4 + 3] = b4.w;
-                    be[4 * j4] = e4.x, be[4 * j4 + 1] = e4.y, be[4 * j4 + 2] = e4.z, be[4 * j4 + 3] = e4.w;
-                }
+            for (int cb = 0; cb < 2; ++cb) {
+                uint32_t z[64];
+                ld64(tmem + lane_off + zcol + 64 * cb, z);
                 tmem_ld_wait();
+                if (renorm) {
 #pragma unroll
-                for (int j8 = 0; j8 < 4; ++j8) {
-                    float rs[8], rp[8];
+                    for (int j = 0; j < 64; ++j) z[j] = __float_as_uint(__uint_as_float(z[j]) * rs);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int jj = 8 * j8 + j;
-                        rs[j] = fmaf(bb[jj] * eL, vv[jj], -be[jj] * __uint_as_float(ys[jj]));
-                        rp[j] = -be[jj] * __uint_as_float(yp[jj]);
-                    }
-                    const uint32_t bo = (c0 + 8 * j8) * 2;
-                    *reinterpret_cast<uint4 *>(ar + sw128(n, bo)) =
-                        make_uint4(bf2(rs[0], rs[1]), bf2(rs[2], rs[3]), bf2(rs[4], rs[5]), bf2(rs[6], rs[7]));
-                    *reinterpret_cast<uint4 *>(ar + sw128(128 + n, bo)) =
-                        make_uint4(bf2(rp[0], rp[1]), bf2(rp[2], rp[3]), bf2(rp[4], rp[5]), bf2(rp[6], rp[7]));
+                    for (int j = 0; j < 4; ++j)
+                        tmem_st16(tmem + lane_off + zcol + 64 * cb + 16 * j,
+                                  *reinterpret_cast<uint32_t(*)[16]>(&z[16 * j]));
                 }
+                st_bf16x64(tmem + lane_off + zkcol + 32 * cb, z);
             }
-            fence_async_shared();
+            tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&bars.rready);
-            // (3) D'^T[n][t] = e^{-c_t} (M R)^T[n][t], into the same operand tile
-            if (!(ok = wait(&bars.dfull, c & 1))) break;
+            mbar_arrive(&bars.zready[hf]);
+            // (2) D^T -> bf16 A operand of the update, over the accumulator's first columns
+            if (!(ok = wwait(&bars.dfull[hf], c & 1))) break;
             tc_fence_after();
-            const float cC = v.cC;
-#pragma unroll
-            for (int c0 = 0; c0 < C; c0 += 32) {
-                uint32_t ds[32], dp[32];
-                tmem_ld32(tmem + lane_off + kTY + c0, ds);
-                tmem_ld32(tmem + lane_off + kTY + 64 + c0, dp);
-                float em[32];
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 e4 = reinterpret_cast<const float4 *>(v.ecm + c0)[j4];
-                    em[4 * j4] = e4.x, em[4 * j4 + 1] = e4.y, em[4 * j4 + 2] = e4.z, em[4 * j4 + 3] = e4.w;
-                }
+            {
+                uint32_t z[64];
+                ld64(tmem + lane_off + dcol, z);
                 tmem_ld_wait();
-#pragma unroll
-                for (int j8 = 0; j8 < 4; ++j8) {
-                    float a8[8], b8[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int jj = 8 * j8 + j;
-                        const float e = em[jj];
-                        a8[j] = e * __uint_as_float(ds[jj]);
-                        b8[j] = e * __uint_as_float(dp[jj]);
-                    }
-                    const uint32_t bo = (c0 + 8 * j8) * 2;
-                    *reinterpret_cast<uint4 *>(ar + sw128(n, bo)) =
-                        make_uint4(bf2(a8[0], a8[1]), bf2(a8[2], a8[3]), bf2(a8[4], a8[5]), bf2(a8[6], a8[7]));
-                    *reinterpret_cast<uint4 *>(ar + sw128(128 + n, bo)) =
-                        make_uint4(bf2(b8[0], b8[1]), bf2(b8[2], b8[3]), bf2(b8[4], b8[5]), bf2(b8[6], b8[7]));
-                }
+                st_bf16x64(tmem + lane_off + dcol, z);
             }
-            fence_async_shared();
+            tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&bars.dready);
-            Lam += cC;
-            lam_total += cC;
+            mbar_arrive(&bars.dready[hf]);
         }
-        // outputs: S = exp(Lam) S~ (column n), P (column n), lam
-        if (ok && nch > 0) ok = wait(&bars.zfull, (nch - 1) & 1);
+        // outputs: S = exp(Lam) S~ (column n) or P (column n), and lam
+        if (ok && nch > 0) ok = wwait(&bars.zfull[hf], (nch - 1) & 1);
         tc_fence_after();
         const int64_t unit = (int64_t)seg.idx * p.seg_stride + h;
-        float *So = p.S + unit * D * D + n;
-        float *Po = p.P + unit * D * D + n;
-        const float sc = expf(Lam);
+        float *O = (hf == 0 ? p.S : p.P) + unit * D * D + n;
+        const float sc = (hf == 0 && nch > 0) ? expf(slots[(nch - 1) & 1].lam_after) : 1.f;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t z[32];
+            tmem_ld32(tmem + lane_off + zcol + c0, z);
+            tmem_ld_wait();
 #pragma unroll
-            for (int c0 = 0; c0 < 128; c0 += 32) {
-                uint32_t z[32];
-                tmem_ld32(tmem + lane_off + kTZ + 128 * hf + c0, z);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float val = __uint_as_float(z[j]);
-                    if (hf == 0) So[(int64_t)(c0 + j) * D] = val * sc;
-                    else Po[(int64_t)(c0 + j) * D] = val;
-                }
-            }
-        if (n == 0) p.lam[unit] = lam_total;
+            for (int j = 0; j < 32; ++j) O[(int64_t)(c0 + j) * D] = __uint_as_float(z[j]) * sc;
+        }
+        if (hf == 0 && n == 0) p.lam[unit] = nch > 0 ? slots[(nch - 1) & 1].lam_sum : 0.f;
     }
 
     tc_fence_before();
@@ -639,19 +529,30 @@ bool build_gdn_tc_supported(const BuildParams &p) {
 }
 
 cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s) {
+    const int blocks = p.n_seg * p.H_v;
+    if (blocks == 0) return cudaSuccess;
+    int64_t records = 0;
+    for (int r = 0; r < p.n_seg; ++r) records += (int64_t)p.H_v * ((p.seg[r].len + C - 1) / C);
     const int64_t N = p.n_tok > 0 ? p.n_tok : 1;
-    CUtensorMap tmK, tmV;
+    CUtensorMap tmK, tmV, tmR;
     if (!make_tmap_3d(&tmK, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_k, N, (uint64_t)D * 2,
                       (uint64_t)p.H_k * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_3d(&tmV, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_v, N, (uint64_t)D * 2,
                       (uint64_t)p.H_v * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(build_gdn_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (records > 0) {
+        if (!p.workspace ||
+            !make_tmap_2d(&tmR, p.workspace, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64, (uint64_t)records * 64,
+                          128, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    } else {
+        tmR = tmK;   // no chunk anywhere: the kernel issues no load
+    }
+    cudaError_t e = launch_build_gdn_prep(p, s);
     if (e != cudaSuccess) return e;
-    const int blocks = p.n_seg * p.H_v;
-    if (blocks == 0) return cudaSuccess;
-    build_gdn_tc_kernel<<<blocks, kThreads, kSmemBytes, s>>>(p, tmK, tmV);
+    e = cudaFuncSetAttribute(build_gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    build_gdn_tc_kernel<<<blocks, kThreads, kSmemBytes, s>>>(p, tmK, tmV, tmR);
     return cudaGetLastError();
 }
 

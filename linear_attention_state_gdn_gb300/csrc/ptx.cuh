@@ -74,6 +74,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity,
     return ok != 0;
 }
 
+// Non-blocking test of the phase (no suspension): true if the phase with this parity has
+// completed. Lets a thread start the check early and consume the answer later.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete, for at most `limit_ns` of wall
 // time. On expiry sets `bit` in *err and returns false.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned *err,
@@ -90,15 +104,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsign
     }
 }
 
+// One probe of the phase without a suspend-time hint (the hardware picks a short window).
+__device__ __forceinline__ bool mbar_try_wait_short(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait that also gives up as soon as another role of the CTA has given up
 // (*abort_flag set); on its own expiry it sets `bit` in *err and raises the flag.
+// With `prompt`, the probes carry no suspend hint: for a thread whose reaction time matters
+// more than the issue slots it takes while waiting (an MMA issuer).
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, unsigned *err,
-                                                   unsigned bit, volatile int *abort_flag) {
+                                                   unsigned bit, volatile int *abort_flag,
+                                                   bool prompt = false) {
     const uint32_t a = smem_u32(bar);
-    if (mbar_try_wait(a, parity)) return true;
+    if (prompt ? mbar_try_wait_short(a, parity) : mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(a, parity)) return true;
+        if (prompt ? mbar_try_wait_short(a, parity) : mbar_try_wait(a, parity)) return true;
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > 2000000000ull) {
             if (err) atomicOr(err, bit);
