@@ -15,9 +15,9 @@
 // the pair (S(C|0), T_C) that "Cut First-Token Latency by 3.25x: Introducing HYPIC ..."
 // (besthub.dev), paragraph "For linear layers", stores for DeltaNet / GDN layers.
 //
-// Persistent CTAs of 128 threads, two per SM, each walking a strided list of records: the k
-// tile of a record is requested three records ahead (a ring of four) and its gram is issued
-// one record ahead (two TMEM buffers), so loads and grams overlap the inversions.
+// Persistent CTAs of 128 threads, three per SM, each walking a strided list of records: the
+// k tile and the b values of a record are requested one record ahead and its gram is issued
+// half a record ahead (two TMEM buffers), so loads and grams overlap the inversions.
 //   1. TMA the chunk's k (two 128B-swizzled 64-channel halves); b masked past the segment end.
 //   2. One thread issues the gram K K^T (M = 64 tcgen05 MMA, fp32 accumulator in TMEM).
 //   3. A = Diag(b) L in fp32 shared memory (rows padded to 68 floats).
@@ -44,14 +44,15 @@ constexpr int D = 128;
 constexpr int C = kGdnChunk;
 constexpr int kThreads = 128;
 constexpr uint32_t kLDA = 68;                            // padded fp32 row stride
-constexpr int kKBufs = 4;                                // k tiles requested 3 records ahead
-constexpr uint32_t kOffK = 0;                            // k tiles, 4 x 16 KB
+constexpr int kKBufs = 2;                                // k tiles requested a record ahead
+constexpr uint32_t kOffK = 0;                            // k tiles, 2 x 16 KB
 constexpr uint32_t kOffA32 = kKBufs * 16384;             // fp32 Diag(b) L, 64 x 68
 constexpr uint32_t kOffN32 = kOffA32 + 64 * kLDA * 4;    // fp32 N, 64 x 68
 constexpr uint32_t kLDT = 12;                            // per-warp 16 x 8 scratch, padded rows
 constexpr uint32_t kOffT = kOffN32 + 64 * kLDA * 4;      // 4 warps x 16 x 12 fp32
 constexpr uint32_t kSmemBytes = kOffT + 4 * 16 * kLDT * 4 + 1024;
-constexpr int kCtasPerSm = 2;
+constexpr int kCtasPerSm = 3;
+constexpr int kCtl = 96;   // warp 3 lane 0: loads, grams (warp 3 has the least level-1 work)
 
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
@@ -181,24 +182,28 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     bool ok = true;
     // the next three records (total when there are none)
     int vn = next_valid(v + gridDim.x);
-    int vn2 = vn < total ? next_valid(vn + gridDim.x) : total;
-    int vn3 = vn2 < total ? next_valid(vn2 + gridDim.x) : total;
-    if (q == 0) {
+    // b of the current record (thread q < 64: token q), loaded one record ahead
+    auto load_beta = [&](int vv) -> float {
+        if (q >= C || vv >= total) return 0.f;
+        const RecPos r = rec_pos(p, max_nch, vv);
+        const SegEntry sg = p.seg[r.r];
+        return q < min(C, sg.len - r.c * C) ? p.beta[((int64_t)sg.start + r.c * C + q) * p.H_v + r.h] : 0.f;
+    };
+    float beta_cur = load_beta(v);
+    if (q == kCtl) {
         prefetch_tmap(&tmK);
         load_k(v, 0);
-        if (vn < total) load_k(vn, 1);
-        if (vn2 < total) load_k(vn2, 2);
         ok = gram(0, 0);
     }
     for (int i = 0; v < total; ++i) {
         const int b = i & 1;
         const RecPos r = rec_pos(p, max_nch, v);
         const SegEntry seg = p.seg[r.r];
-        // k ring slot (i + 3) % 4 held record i - 1, whose gram has completed
-        if (q == 0 && ok && vn3 < total) load_k(vn3, (i + 3) % kKBufs);
-        const int valid = min(C, seg.len - r.c * C);
-        if (q < C) vb[b][q] = q < valid ? p.beta[((int64_t)seg.start + r.c * C + q) * p.H_v + r.h] : 0.f;
-        if (q == 0) {
+        // the other k slot held record i - 1, whose gram has completed
+        if (q == kCtl && ok && vn < total) load_k(vn, (i + 1) % kKBufs);
+        if (q < C) vb[b][q] = beta_cur;
+        const float beta_next = load_beta(vn);
+        if (q == kCtl) {
             ok = ok && mbar_wait(&gfull[b], gwait[b] & 1, p.err, kErrTimeout);
             if (ok) ++gwait[b];
             s_ok = ok ? 1 : 0;
@@ -257,7 +262,7 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         if (warp < 2) half_block(A32, N32, Tw, 3, 2, warp, lane);
         // the gram of the next record into the other TMEM buffer (last read two records ago);
         // its k tile was requested at the top of this iteration
-        if (q == 0 && ok && vn < total) ok = gram((i + 1) % kKBufs, b ^ 1);
+        if (q == kCtl && ok && vn < total) ok = gram((i + 1) % kKBufs, b ^ 1);
         __syncthreads();
         half_block(A32, N32, Tw, 2 + (warp >> 1), warp >> 1, warp & 1, lane);
         __syncthreads();
@@ -282,11 +287,10 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
             *reinterpret_cast<uint4 *>(dst + tp * 128 + s8 * 2) = pk;
         }
         v = vn;
-        vn = vn2;
-        vn2 = vn3;
-        vn3 = vn3 < total ? next_valid(vn3 + gridDim.x) : total;
+        vn = vn < total ? next_valid(vn + gridDim.x) : total;
+        beta_cur = beta_next;
     }
-    if (q == 0) {   // after a wait gave up: let every copy and MMA in flight land first
+    if (q == kCtl) {   // after a wait gave up: let every copy and MMA in flight land first
         for (int b = 0; b < kKBufs; ++b)
             for (; kwait[b] < kiss[b]; ++kwait[b]) mbar_wait(&kfull[b], kwait[b] & 1, nullptr, 0);
         for (int b = 0; b < 2; ++b)
