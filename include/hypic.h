@@ -174,6 +174,21 @@ typedef struct {
  * Segments run in parallel, longest first. Returns HYPIC_OK once the work is enqueued. */
 hypic_status hypic_build_segments(const hypic_build_args *args, void *stream);
 
+/* hypic_build_segments with library-owned scratch instead of args->workspace (which is
+ * ignored): a file-scope device array of HYPIC_STATIC_WS_BYTES bytes, reserved when the
+ * library's device code is loaded, so the call itself allocates nothing. The pages describe
+ * no counterpart; it exists for callers that must not allocate device memory per call.
+ *   - Requests whose hypic_build_workspace_bytes() exceeds HYPIC_STATIC_WS_BYTES return
+ *     HYPIC_ERR_UNSUPPORTED before any device work (use hypic_build_segments then).
+ *   - The scratch is one buffer per device: calls that overlap in time (two streams, or
+ *     two host threads) race on it and give undefined results. Serialise them.
+ *   - The first call on a device looks the buffer up (cudaGetSymbolAddress, once per
+ *     device); make that first call before any stream capture.
+ *   - No part of the scratch needs to start at zero.
+ * Other arguments, results and errors are those of hypic_build_segments. */
+#define HYPIC_STATIC_WS_BYTES (64u << 20)
+hypic_status hypic_build_segments_static_ws(const hypic_build_args *args, void *stream);
+
 /* Inclusive prefix scan of the composition over n_seg segments for n_units units. */
 hypic_status hypic_compose_scan(const hypic_compose_args *args, void *stream);
 

@@ -69,6 +69,8 @@ def load_library(path: str = LIB_PATH):
             lib = ctypes.CDLL(path)
             lib.hypic_build_segments.argtypes = [ctypes.POINTER(BuildArgs), ctypes.c_void_p]
             lib.hypic_build_segments.restype = ctypes.c_int
+            lib.hypic_build_segments_static_ws.argtypes = [ctypes.POINTER(BuildArgs), ctypes.c_void_p]
+            lib.hypic_build_segments_static_ws.restype = ctypes.c_int
             lib.hypic_compose_scan.argtypes = [ctypes.POINTER(ComposeArgs), ctypes.c_void_p]
             lib.hypic_compose_scan.restype = ctypes.c_int
             lib.hypic_build_workspace_bytes.argtypes = [ctypes.POINTER(BuildArgs)]
@@ -173,6 +175,25 @@ def hypic_build_segments(family, k, v, seg_offsets, log_gate=None, log_gamma=Non
     return S, lam, P
 
 
+def hypic_build_segments_static_ws(family, k, v, seg_offsets, log_gate=None, log_gamma=None,
+                                   beta=None, S=None, lam=None, P=None, out_seg_stride=0,
+                                   stream=None):
+    """hypic_build_segments with the library's own device scratch (HYPIC_STATIC_WS_BYTES,
+    64 MiB): no per-call allocation. Calls that overlap in time race on that scratch."""
+    lib = load_library()
+    n_seg = len(_offsets(seg_offsets)) - 1
+    if S is None:
+        S, lam, P = build_outputs(family, n_seg, v.shape[1], v.shape[2], v.device)
+    a = make_build_args(family, k, v, seg_offsets, log_gate, log_gamma, beta, S, lam, P,
+                        out_seg_stride)
+    _check(lib.hypic_build_segments_static_ws(ctypes.byref(a), _stream(stream)),
+           "hypic_build_segments_static_ws")
+    return S, lam, P
+
+
+STATIC_WS_BYTES = 64 << 20   # HYPIC_STATIC_WS_BYTES in include/hypic.h
+
+
 def make_compose_args(family, S, lam, P=None, S0=None, prefix=None):
     fam = FAMILY[family] if isinstance(family, str) else int(family)
     a = ComposeArgs()
@@ -218,7 +239,8 @@ def hypic_status_string(status: int) -> str:
     return load_library().hypic_status_string(status).decode()
 
 
-__all__ = ["hypic_build_segments", "hypic_compose_scan", "hypic_build_workspace_bytes",
+__all__ = ["hypic_build_segments", "hypic_build_segments_static_ws", "hypic_compose_scan",
+           "hypic_build_workspace_bytes",
            "hypic_build_kernel_name", "hypic_compose_kernel_name",
            "hypic_get_device_status", "hypic_status_string", "load_library", "HypicError",
            "build_outputs", "FAMILY"]

@@ -37,6 +37,25 @@ unsigned *status_word(int *dev_out) {
     return g_status_addr[dev];
 }
 
+// Library-owned build scratch for hypic_build_segments_static_ws: a file-scope device array
+// (reserved when the module loads; nothing is allocated at call time), located once per
+// device like the status word. No part of it needs to start at zero: the build overwrites
+// every record it later reads.
+__device__ __align__(256) unsigned char g_static_ws[HYPIC_STATIC_WS_BYTES];
+void *g_static_ws_addr[kMaxDevices];
+
+void *static_workspace() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (!g_static_ws_addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_ws) != cudaSuccess) return nullptr;
+        g_static_ws_addr[dev] = ptr;
+    }
+    return g_static_ws_addr[dev];
+}
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // True if p is memory the current device can read with plain loads (device or managed).
@@ -249,6 +268,22 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
     case BuildPath::None: break;
     }
     return HYPIC_OK;
+}
+
+hypic_status hypic_build_segments_static_ws(const hypic_build_args *a, void *stream) {
+    if (!a) return HYPIC_ERR_INVALID_ARG;
+    const size_t need = hypic_build_workspace_bytes(a);
+    if (need > (size_t)HYPIC_STATIC_WS_BYTES) return HYPIC_ERR_UNSUPPORTED;
+    hypic_build_args b = *a;
+    b.workspace = nullptr;
+    b.workspace_bytes = 0;
+    if (need) {
+        void *ws = static_workspace();
+        if (!ws) return HYPIC_ERR_CUDA;
+        b.workspace = ws;
+        b.workspace_bytes = (size_t)HYPIC_STATIC_WS_BYTES;
+    }
+    return hypic_build_segments(&b, stream);
 }
 
 hypic_status hypic_compose_scan(const hypic_compose_args *a, void *stream) {

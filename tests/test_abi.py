@@ -201,3 +201,27 @@ def test_binding_refuses_cpu_tensors():
     lam = torch.zeros(1, 1)
     with pytest.raises(ValueError):
         hypic_build_segments("linear", k, v, [0, 8], S=S, lam=lam)
+
+
+def test_workspace_bytes_of_the_tensor_core_gdn_build(lib):
+    # bf16, d = 128, DeltaNet / GDN: 8 KB per (segment, value head, 64-token chunk)
+    a = good_build(lens=(64, 130))
+    assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == 4 * (1 + 3) * 8192
+    a.d_k = a.d_v = 64                      # exact fp32-state path: no workspace
+    assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == 0
+    b = good_build(family=2)                # gated families: no workspace
+    assert lib.hypic_build_workspace_bytes(ctypes.byref(b)) == 0
+
+
+def test_build_rejects_a_short_workspace(lib):
+    a = good_build()
+    a.workspace, a.workspace_bytes = FAKE + 0x7000000, 100
+    assert call_build(lib, a) == 1
+
+
+def test_static_workspace_build_rejects_null_and_oversized_requests(lib):
+    assert lib.hypic_build_segments_static_ws(None, None) == 1
+    # 4 heads x 2049 chunks x 8 KB > 64 MiB: refused before any device work
+    a = good_build(n_seg=1, lens=(2049 * 64,))
+    assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) > (64 << 20)
+    assert lib.hypic_build_segments_static_ws(ctypes.byref(a), None) == 3
