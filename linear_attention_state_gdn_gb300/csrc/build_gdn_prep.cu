@@ -15,9 +15,10 @@
 // the pair (S(C|0), T_C) that "Cut First-Token Latency by 3.25x: Introducing HYPIC ..."
 // (besthub.dev), paragraph "For linear layers", stores for DeltaNet / GDN layers.
 //
-// Persistent CTAs of 128 threads, three per SM, each walking a strided list of records: the
-// k tile and the b values of a record are requested one record ahead and its gram is issued
-// half a record ahead (two TMEM buffers), so loads and grams overlap the inversions.
+// Persistent CTAs of 128 threads, four per SM, each walking a strided list of records: the
+// k tile of the next record is requested as soon as the current gram has read the single k
+// buffer, its gram is issued while two warps finish the current inverse (two TMEM buffers),
+// and b is loaded a record ahead, so loads and grams overlap the inversions.
 //   1. TMA the chunk's k (two 128B-swizzled 64-channel halves); b masked past the segment end.
 //   2. One thread issues the gram K K^T (M = 64 tcgen05 MMA, fp32 accumulator in TMEM).
 //   3. A = Diag(b) L in fp32 shared memory (rows padded to 68 floats).
@@ -44,15 +45,14 @@ constexpr int D = 128;
 constexpr int C = kGdnChunk;
 constexpr int kThreads = 128;
 constexpr uint32_t kLDA = 68;                            // padded fp32 row stride
-constexpr int kKBufs = 2;                                // k tiles requested a record ahead
-constexpr uint32_t kOffK = 0;                            // k tiles, 2 x 16 KB
-constexpr uint32_t kOffA32 = kKBufs * 16384;             // fp32 Diag(b) L, 64 x 68
+constexpr uint32_t kOffK = 0;                            // k tile, 16 KB
+constexpr uint32_t kOffA32 = 16384;                      // fp32 Diag(b) L, 64 x 68
 constexpr uint32_t kOffN32 = kOffA32 + 64 * kLDA * 4;    // fp32 N, 64 x 68
 constexpr uint32_t kLDT = 12;                            // per-warp 16 x 8 scratch, padded rows
 constexpr uint32_t kOffT = kOffN32 + 64 * kLDA * 4;      // 4 warps x 16 x 12 fp32
 constexpr uint32_t kSmemBytes = kOffT + 4 * 16 * kLDT * 4 + 1024;
-constexpr int kCtasPerSm = 3;
-constexpr int kCtl = 96;   // warp 3 lane 0: loads, grams (warp 3 has the least level-1 work)
+constexpr int kCtasPerSm = 4;
+constexpr int kCtl = 96;   // warp 3 lane 0 issues loads and grams (warp 3 has the least level work)
 
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
@@ -105,47 +105,53 @@ __device__ __forceinline__ void half_block(const float *A32, float *N32, float *
 }
 
 // Records are visited in the order (segment, chunk, head), so the value heads that share a
-// key head read the same k tile back to back (from L2).
-struct RecPos {
-    int r, c, h, nch;
-    bool valid;
+// key head read the same k tile back to back (from L2). A CTA walks every gridDim.x-th
+// record; the position is advanced in mixed radix (head, chunk, segment) without divisions.
+struct Walk {
+    int r, c, h;   // segment rank, chunk, value head; r == n_seg when past the end
 };
-__device__ __forceinline__ RecPos rec_pos(const BuildParams &p, int max_nch, int v) {
-    RecPos q;
-    q.h = v % p.H_v;
-    const int rc = v / p.H_v;
-    q.c = rc % max_nch;
-    q.r = rc / max_nch;
-    q.nch = (p.seg[q.r].len + C - 1) / C;
-    q.valid = q.c < q.nch;
-    return q;
-}
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ uint64_t kfull[kKBufs], gfull[2];
+    __shared__ uint64_t kfull, gfull[2];
     __shared__ uint32_t tslot;
     __shared__ int s_ok;
     __shared__ __align__(16) float vb[2][C];
 
     const int max_nch = (p.max_len + C - 1) / C;
-    const int total = p.n_seg * max_nch * p.H_v;
-    auto next_valid = [&](int v) {
-        while (v < total && !rec_pos(p, max_nch, v).valid) v += gridDim.x;
-        return v;
+    const int stride = gridDim.x;
+    const int sh = stride % p.H_v, sc = (stride / p.H_v) % max_nch, sr = stride / (p.H_v * max_nch);
+    auto nch_of = [&](int r) { return (p.seg[r].len + C - 1) / C; };
+    auto valid = [&](const Walk &w) { return w.r < p.n_seg && w.c < nch_of(w.r); };
+    auto step = [&](Walk w) {   // next record of this CTA (skipping chunks past a segment's end)
+        do {
+            w.h += sh;
+            int carry = w.h >= p.H_v;
+            w.h -= carry ? p.H_v : 0;
+            w.c += sc + carry;
+            carry = w.c >= max_nch;
+            w.c -= carry ? max_nch : 0;
+            w.r += sr + carry;
+        } while (w.r < p.n_seg && w.c >= nch_of(w.r));
+        return w;
     };
-    int v = next_valid(blockIdx.x);
-    if (v >= total) return;   // uniform: the whole CTA leaves before any set-up
+    Walk cur;
+    cur.h = blockIdx.x % p.H_v;
+    cur.c = (blockIdx.x / p.H_v) % max_nch;
+    cur.r = blockIdx.x / (p.H_v * max_nch);
+    if (cur.r < p.n_seg && !valid(cur)) cur = step(cur);
+    if (cur.r >= p.n_seg) return;   // uniform: the whole CTA leaves before any set-up
     const int q = threadIdx.x, warp = q >> 5, lane = q & 31;
     float *A32 = reinterpret_cast<float *>(smem + kOffA32);
     float *N32 = reinterpret_cast<float *>(smem + kOffN32);
     float *Tw = reinterpret_cast<float *>(smem + kOffT) + warp * 16 * kLDT;
 
     if (q == 0) {
-        for (int s = 0; s < kKBufs; ++s) mbar_init(&kfull[s], 1);
-        for (int s = 0; s < 2; ++s) mbar_init(&gfull[s], 1);
+        mbar_init(&kfull, 1);
+        mbar_init(&gfull[0], 1);
+        mbar_init(&gfull[1], 1);
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(&tslot, 128);
@@ -154,22 +160,20 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = tslot;
     constexpr uint32_t idG = idesc(kFmtBF16, kFmtBF16, false, false, 64, 64);
-    int kiss[kKBufs] = {}, kwait[kKBufs] = {}, giss[2] = {}, gwait[2] = {};   // thread 0
-    auto load_k = [&](int vv, int b) {   // thread 0
-        ++kiss[b];
-        const RecPos r = rec_pos(p, max_nch, vv);
-        const int32_t t0 = p.seg[r.r].start + r.c * C;
-        uint8_t *kt = smem + kOffK + b * 16384;
-        mbar_arrive_expect_tx(&kfull[b], 16384);
-        tma_load_3d(kt, &tmK, &kfull[b], 0, r.h / p.gqa, t0);
-        tma_load_3d(kt + 8192, &tmK, &kfull[b], 64, r.h / p.gqa, t0);
+    int kiss = 0, kwait = 0, giss[2] = {0, 0}, gwait[2] = {0, 0};   // thread kCtl
+    auto load_k = [&](const Walk &w) {   // thread kCtl
+        ++kiss;
+        const int32_t t0 = p.seg[w.r].start + w.c * C;
+        mbar_arrive_expect_tx(&kfull, 16384);
+        tma_load_3d(smem + kOffK, &tmK, &kfull, 0, w.h / p.gqa, t0);
+        tma_load_3d(smem + kOffK + 8192, &tmK, &kfull, 64, w.h / p.gqa, t0);
     };
-    auto gram = [&](int kb, int b) -> bool {   // thread 0: k buffer kb -> TMEM buffer b
-        if (!mbar_wait(&kfull[kb], kwait[kb] & 1, p.err, kErrTimeout)) return false;
-        ++kwait[kb];
+    auto gram = [&](int b) -> bool {   // thread kCtl: the k tile -> TMEM buffer b
+        if (!mbar_wait(&kfull, kwait & 1, p.err, kErrTimeout)) return false;
+        ++kwait;
         ++giss[b];
         tc_fence_after();
-        const uint32_t k = smem_u32(smem + kOffK + kb * 16384);
+        const uint32_t k = smem_u32(smem + kOffK);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
             const uint32_t a = k + (s >> 2) * 8192 + (s & 3) * 32;
@@ -179,33 +183,33 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         mma_commit(&gfull[b]);
         return true;
     };
-    bool ok = true;
-    // the next three records (total when there are none)
-    int vn = next_valid(v + gridDim.x);
-    // b of the current record (thread q < 64: token q), loaded one record ahead
-    auto load_beta = [&](int vv) -> float {
-        if (q >= C || vv >= total) return 0.f;
-        const RecPos r = rec_pos(p, max_nch, vv);
-        const SegEntry sg = p.seg[r.r];
-        return q < min(C, sg.len - r.c * C) ? p.beta[((int64_t)sg.start + r.c * C + q) * p.H_v + r.h] : 0.f;
+    // b of a record (thread q < 64: token q), loaded one record ahead
+    auto load_beta = [&](const Walk &w) -> float {
+        if (q >= C || w.r >= p.n_seg) return 0.f;
+        const SegEntry sg = p.seg[w.r];
+        return q < min(C, sg.len - w.c * C) ? p.beta[((int64_t)sg.start + w.c * C + q) * p.H_v + w.h] : 0.f;
     };
-    float beta_cur = load_beta(v);
+    bool ok = true;
+    Walk nxt = step(cur);
+    float beta_cur = load_beta(cur);
     if (q == kCtl) {
         prefetch_tmap(&tmK);
-        load_k(v, 0);
-        ok = gram(0, 0);
+        load_k(cur);
+        ok = gram(0);
     }
-    for (int i = 0; v < total; ++i) {
+    for (int i = 0; cur.r < p.n_seg; ++i) {
         const int b = i & 1;
-        const RecPos r = rec_pos(p, max_nch, v);
-        const SegEntry seg = p.seg[r.r];
-        // the other k slot held record i - 1, whose gram has completed
-        if (q == kCtl && ok && vn < total) load_k(vn, (i + 1) % kKBufs);
+        const SegEntry seg = p.seg[cur.r];
+        const int nch = nch_of(cur.r);
         if (q < C) vb[b][q] = beta_cur;
-        const float beta_next = load_beta(vn);
+        const float beta_next = load_beta(nxt);
+        // gram(i) done: the k tile is free for the next record
         if (q == kCtl) {
             ok = ok && mbar_wait(&gfull[b], gwait[b] & 1, p.err, kErrTimeout);
-            if (ok) ++gwait[b];
+            if (ok) {
+                ++gwait[b];
+                if (nxt.r < p.n_seg) load_k(nxt);
+            }
             s_ok = ok ? 1 : 0;
         }
         __syncthreads();
@@ -257,20 +261,21 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
             for (int rr = 0; rr < 16; ++rr) N32[(16 * a + rr) * kLDA + 16 * a + j] = x[rr];
         }
         __syncthreads();
-        // level 1: (1,0), (2,1), (3,2) as six half-blocks; level 2: (2,0), (3,1); level 3: (3,0)
+        // level 1: (1,0), (2,1), (3,2) as six half-blocks; level 2: (2,0), (3,1); level 3: (3,0).
+        // Warps 0-1 take one half-block per level, warps 2-3 two in level 1 and none in level 3.
         half_block(A32, N32, Tw, 1 + (warp >> 1), warp >> 1, warp & 1, lane);
-        if (warp < 2) half_block(A32, N32, Tw, 3, 2, warp, lane);
-        // the gram of the next record into the other TMEM buffer (last read two records ago);
-        // its k tile was requested at the top of this iteration
-        if (q == kCtl && ok && vn < total) ok = gram((i + 1) % kKBufs, b ^ 1);
+        if (warp >= 2) half_block(A32, N32, Tw, 3, 2, warp & 1, lane);
         __syncthreads();
         half_block(A32, N32, Tw, 2 + (warp >> 1), warp >> 1, warp & 1, lane);
         __syncthreads();
         if (warp < 2) half_block(A32, N32, Tw, 3, 0, warp, lane);
+        // warps 2-3 have no level-3 work: the next record's gram (its k tile was requested at
+        // the top of this iteration) into the other TMEM buffer, last read a record ago
+        if (q == kCtl && ok && nxt.r < p.n_seg) ok = gram(b ^ 1);
         __syncthreads();
         // record: N Diag(b) as bf16 rows t' (blocks above the diagonal are zero)
         uint8_t *dst = static_cast<uint8_t *>(p.workspace) +
-                       ((int64_t)seg.wsb + (int64_t)r.h * r.nch + r.c) * (int64_t)kGdnRecordBytes;
+                       ((int64_t)seg.wsb + (int64_t)cur.h * nch + cur.c) * (int64_t)kGdnRecordBytes;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             const int e8 = q + 128 * m;   // 8 consecutive entries of row t'
@@ -286,13 +291,12 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
             }
             *reinterpret_cast<uint4 *>(dst + tp * 128 + s8 * 2) = pk;
         }
-        v = vn;
-        vn = vn < total ? next_valid(vn + gridDim.x) : total;
+        cur = nxt;
+        nxt = cur.r < p.n_seg ? step(cur) : cur;
         beta_cur = beta_next;
     }
     if (q == kCtl) {   // after a wait gave up: let every copy and MMA in flight land first
-        for (int b = 0; b < kKBufs; ++b)
-            for (; kwait[b] < kiss[b]; ++kwait[b]) mbar_wait(&kfull[b], kwait[b] & 1, nullptr, 0);
+        for (; kwait < kiss; ++kwait) mbar_wait(&kfull, kwait & 1, nullptr, 0);
         for (int b = 0; b < 2; ++b)
             for (; gwait[b] < giss[b]; ++gwait[b]) mbar_wait(&gfull[b], gwait[b] & 1, nullptr, 0);
     }

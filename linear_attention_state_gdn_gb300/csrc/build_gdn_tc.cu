@@ -31,7 +31,7 @@
 //         [384,448) bf16 Z_S^T (A of d_S); between d_S(c) and the next Z pass it holds the
 //                   fp32 W^T(c+1) accumulator (lane i, column t')
 //         [448,512) bf16 Z_P^T (A of d_P)
-//   SMEM  a ring of three k chunks and a ring of two {v chunk, M2 record} (TMA,
+//   SMEM  a ring of three k chunks and a ring of three {v chunk, M2 record} (TMA,
 //         128B-swizzled); -W^T bf16 (MN-major B of d, two slots); M1 = M2 Diag(exp(-Lam - c))
 //         bf16 (K-major B of U, two slots).
 // Roles: warps 0-3 carry the S~ half and warps 4-7 the P half (thread = TMEM lane = state
@@ -71,9 +71,10 @@ constexpr uint32_t kKV = 2 * kHalf;           // k (or v) chunk, 16 KB
 constexpr uint32_t kRec = 64 * 128;           // M2 record, 8 KB
 constexpr uint32_t kVR = kKV + kRec;          // v chunk + M2 record, 24 KB
 constexpr int kKSlots = 3;                    // k is read until the lagging half's update
+constexpr int kVSlots = 3;                    // {v, M2} slots: loads requested two chunks ahead
 constexpr uint32_t kOffK = 0;                 // k ring: 3 x 16 KB
-constexpr uint32_t kOffVR = kKSlots * kKV;    // {v, M2} ring: 2 x 24 KB
-constexpr uint32_t kOffWop = kOffVR + 2 * kVR;  // -W^T bf16: 2 slots x [128 rows i][128 B]
+constexpr uint32_t kOffVR = kKSlots * kKV;    // {v, M2} ring: 3 x 24 KB
+constexpr uint32_t kOffWop = kOffVR + kVSlots * kVR;  // -W^T bf16: 2 slots x [128 rows i][128 B]
 constexpr uint32_t kOffM1 = kOffWop + 2 * kKV;  // M1: 2 slots x 8 KB
 constexpr uint32_t kSmemBytes = kOffM1 + 2 * kRec + 1024;
 
@@ -89,7 +90,7 @@ struct Slot {   // per-chunk values from the operand warps (two slots)
 
 struct Bars {
     uint64_t kfull[kKSlots], kempty[kKSlots];   // k ring
-    uint64_t vfull[2], vempty[2];               // {v, M2} ring
+    uint64_t vfull[kVSlots], vempty[kVSlots];   // {v, M2} ring
     uint64_t wfull;               // W^T accumulated
     // -W^T operand of a chunk written (and the W^T TMEM columns free), one per operand slot:
     // the P half's issuer may lag, so one barrier could be two phases ahead of its wait
@@ -166,9 +167,11 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             mbar_init(&bars.kfull[s], 1);
             mbar_init(&bars.kempty[s], 2);   // both halves' updates read the k chunk
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kVSlots; ++s) {
             mbar_init(&bars.vfull[s], 1);
             mbar_init(&bars.vempty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(&bars.m1ready[s], 128);
             mbar_init(&bars.zready[s], 128);
             mbar_init(&bars.dfull[s], 1);
@@ -210,7 +213,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 tma_load_3d(kt, &tmK, &bars.kfull[ks], 0, hk, t0);
                 tma_load_3d(kt + kHalf, &tmK, &bars.kfull[ks], 64, hk, t0);
                 kc = c + 1;
-                const int vs = c & 1, vuse = c >> 1;
+                const int vs = c % kVSlots, vuse = c / kVSlots;
                 if (vuse >= 1 && !wait(&bars.vempty[vs], (vuse - 1) & 1)) break;
                 uint8_t *vt = smem + kOffVR + vs * kVR;
                 const int32_t rrow = (seg.wsb + h * nch + c) * 64;
@@ -222,8 +225,8 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             if (abort_flag) {   // let the loads in flight land before the CTA exits
                 for (int q = (kc > kKSlots ? kc - kKSlots : 0); q < kc; ++q)
                     mbar_wait(&bars.kfull[q % kKSlots], (q / kKSlots) & 1, p.err, kErrTimeout);
-                for (int q = (c > 2 ? c - 2 : 0); q < c; ++q)
-                    mbar_wait(&bars.vfull[q & 1], (q >> 1) & 1, p.err, kErrTimeout);
+                for (int q = (c > kVSlots ? c - kVSlots : 0); q < c; ++q)
+                    mbar_wait(&bars.vfull[q % kVSlots], (q / kVSlots) & 1, p.err, kErrTimeout);
             }
         }
     } else if (warp == kMmaWarpS || warp == kMmaWarpP) {
@@ -272,7 +275,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 // W^T(c) = K^T M2^T into the S~ half's bf16-Z^T columns (A: the k chunk read
                 // MN-major, B: the M2 record K-major)
                 auto issue_w = [&](int c) {
-                    const uint64_t a = dK + (((c % kKSlots) * kKV) >> 4), b = dR + (((c & 1) * kVR) >> 4);
+                    const uint64_t a = dK + (((c % kKSlots) * kKV) >> 4), b = dR + (((c % kVSlots) * kVR) >> 4);
                     mma_bf16(tmem + kTZK, a, b, idA, 0u);
 #pragma unroll
                     for (int s = 1; s < 4; ++s) mma_bf16(tmem + kTZK, a + s * kRow16, b + s * kCol16, idA, 1u);
@@ -281,11 +284,11 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 // D_S^T(c) = V^T M1^T (A: the v chunk read MN-major, B: M1 K-major); frees the
                 // {v, M2} slot of chunk c
                 auto issue_u = [&](int c) {
-                    const uint64_t a = dV + (((c & 1) * kVR) >> 4), b = dM + (((c & 1) * kRec) >> 4);
+                    const uint64_t a = dV + (((c % kVSlots) * kVR) >> 4), b = dM + (((c & 1) * kRec) >> 4);
                     mma_bf16(tmem + kTD, a, b, idA, 0u);
 #pragma unroll
                     for (int s = 1; s < 4; ++s) mma_bf16(tmem + kTD, a + s * kRow16, b + s * kCol16, idA, 1u);
-                    mma_commit(&bars.vempty[c & 1]);
+                    mma_commit(&bars.vempty[c % kVSlots]);
                 };
                 // per chunk: d_S(c), W(c+1), f_S(c), U(c+1). W(c+1) overwrites the columns
                 // d_S(c) reads as A and U(c+1) the D_S columns f_S(c) reads as A, so each is
@@ -306,7 +309,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                     issue_d(c);
                     if (more) {
                         if (!(ok = wait(&bars.dfull[0], c & 1) && wait(&bars.kfull[(c + 1) % kKSlots], ((c + 1) / kKSlots) & 1) &&
-                                   wait(&bars.vfull[(c + 1) & 1], ((c + 1) >> 1) & 1)))
+                                   wait(&bars.vfull[(c + 1) % kVSlots], ((c + 1) / kVSlots) & 1)))
                             break;
                         tc_fence_after();
                         issue_w(c + 1);
@@ -382,9 +385,9 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             lam_sum += cC;
             bar_aux();   // ex visible; every read of scan_tmp done before the next writes
             // (2) M1[t'][t] = M2[t'][t] exp(-Lam_start - c_t), same swizzled layout
-            if (!bar_aux_and(wait(&bars.vfull[c & 1], (c >> 1) & 1))) break;
+            if (!bar_aux_and(wait(&bars.vfull[c % kVSlots], (c / kVSlots) & 1))) break;
             {
-                const uint8_t *rec = smem + kOffVR + (c & 1) * kVR + kKV;
+                const uint8_t *rec = smem + kOffVR + (c % kVSlots) * kVR + kKV;
                 uint8_t *m1 = smem + kOffM1 + (c & 1) * kRec;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
