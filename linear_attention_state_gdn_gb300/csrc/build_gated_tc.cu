@@ -17,9 +17,10 @@
 //   * warp 8 streams k, v (and the per-channel log-gates) chunk by chunk by TMA into a
 //     3-stage ring; k and v land 128B-swizzled with channels contiguous, which is directly
 //     the MN-major operand layout of both MMA operands;
-//   * warps 0-7 (two threads per key channel i, one per token half of the chunk) scale k
-//     in place into Khat (suffix products of the gates, masked past the segment end) and
-//     hand the stage to the MMA warp;
+//   * warps 0-7 turn the chunk's gates into decay factors (one per token for linear /
+//     scalar decay, one per token and channel for diagonal gates, written over the gate
+//     tile; 0 past the segment end), then scale k in place into Khat with 16-byte vector
+//     accesses and hand the stage to the MMA warp;
 //   * warp 9 issues dS_c = Khat^T V into one of two TMEM accumulators (lane i, column n);
 //   * warps 0-7 fold dS_c into the fp32 state they hold in registers (64 columns each):
 //     S[i][:] = exp(sum_t l_t[i]) S[i][:] + dS_c[i][:].
@@ -59,6 +60,26 @@ struct Bars {
     uint64_t full[kStages], kready[kStages], empty[kStages], dfull[2], dfree[2], fin;
 };
 
+// Named barrier of the 256 decay / state threads, plain and with an AND of a predicate (every
+// thread leaves with the same outcome). Non-aligned forms: lanes may arrive at different times.
+__device__ __forceinline__ void bar_state() {
+    __syncwarp();
+    asm volatile("barrier.sync 1, 256;" ::: "memory");
+}
+__device__ __forceinline__ bool bar_state_and(bool v) {
+    uint32_t r;
+    __syncwarp();
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "barrier.red.and.pred po, 1, 256, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 2)
 build_gated_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK,
@@ -72,6 +93,9 @@ build_gated_tc_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     __shared__ Bars bars;
     __shared__ uint32_t tslot;
     __shared__ volatile int abort_flag;
+    __shared__ __align__(16) float fac[kStages][64];   // per-token decay factors (linear / scalar)
+    __shared__ float gtot[2][D];                        // chunk log-decay (per channel for diagonal)
+    __shared__ float scan_tmp[2];
 
     const int warp = warp_id(), lane = lane_id();
     const SegEntry seg = p.seg[blockIdx.x / p.H_v];
@@ -160,52 +184,97 @@ build_gated_tc_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         float lam = 0.f;
         float gsum[2] = {0.f, 0.f};
         const float lgam = (KIND == kScalar && p.log_gamma) ? p.log_gamma[h] : 0.f;
-        const float gam = expf(lgam);
-        const uint32_t kcol = (uint32_t)(i >> 6) * G::kHalf;
-        const uint32_t kbyte = (uint32_t)(i & 63) * 2;
 
-        // log-gate of token tt of chunk c for channel i (0 past the segment end)
-        auto gate = [&](const float *gt, int64_t tok0, int valid, int tt) -> float {
-            if (tt >= valid) return 0.f;
-            if (KIND == kDiag) return gt[tt * D + i];
-            if (KIND == kScalar) return p.log_gamma ? lgam : p.log_gate[(tok0 + tt) * p.H_v + h];
-            return 0.f;
-        };
         auto decay = [&](int c) -> bool {
             const int s = c % kStages;
-            if (!mbar_wait_or_abort(&bars.full[s], (c / kStages) & 1, p.err, kErrTimeout, &abort_flag))
+            if (!bar_state_and(mbar_wait_or_abort(&bars.full[s], (c / kStages) & 1, p.err, kErrTimeout,
+                                                  &abort_flag)))
                 return false;
-            uint8_t *kt = smem + s * G::kStage + kcol;
-            const float *gt = reinterpret_cast<const float *>(smem + s * G::kStage + 2 * G::kKV);
+            uint8_t *kt = smem + s * G::kStage;
+            float *gt = reinterpret_cast<float *>(smem + s * G::kStage + 2 * G::kKV);
             const int valid = min(C, seg.len - c * C);
-            const int64_t tok0 = (int64_t)seg.start + c * C;
-            // the other half's gates: needed for the chunk total, and (first half) for the
-            // suffix product entering this half
-            float other = 0.f;
-#pragma unroll 4
-            for (int tt = (1 - hc) * (C / 2); tt < (2 - hc) * (C / 2); ++tt) other += gate(gt, tok0, valid, tt);
-            float r = hc == 0 ? expf(other) : 1.f, own = 0.f;
-#pragma unroll 4
-            for (int tt = hc * (C / 2) + C / 2 - 1; tt >= hc * (C / 2); --tt) {
-                __nv_bfloat16 *kp = reinterpret_cast<__nv_bfloat16 *>(kt + sw128(tt, kbyte));
-                if (tt >= valid) {
-                    *kp = __float2bfloat16(0.f);
-                    continue;
+            // (1) decay factors: exp of the log-gates after each token inside the chunk. They
+            //     only scale bf16 operands (relative rounding 2^-9), so the fast exponential
+            //     (relative error near 2^-22 over this range) is exact enough; the fp32 state's
+            //     per-chunk decay below keeps expf.
+            if (KIND == kDiag) {
+                // thread t < 128 walks channel t from the last token, writing the factor of each
+                // token over its gate (same thread, same address: read before write)
+                if (t < D) {
+                    float suf = 0.f;
+#pragma unroll 8
+                    for (int tt = C - 1; tt >= 0; --tt) {
+                        const float l = tt < valid ? gt[tt * D + t] : 0.f;
+                        gt[tt * D + t] = tt < valid ? __expf(suf) : 0.f;
+                        suf += l;
+                    }
+                    gtot[c & 1][t] = suf;
                 }
-                if (KIND != kLinear) *kp = __float2bfloat16(__bfloat162float(*kp) * r);
-                const float l = gate(gt, tok0, valid, tt);
-                if (KIND != kLinear) r *= (KIND == kScalar && p.log_gamma) ? gam : expf(l);
-                own += l;
+            } else if (KIND == kScalar && p.log_gamma) {
+                if (t < C) fac[s][t] = t < valid ? expf(lgam * (float)(valid - 1 - t)) : 0.f;
+                if (t == 0) gtot[c & 1][0] = lgam * (float)valid;
+            } else if (KIND == kScalar) {
+                // threads 0-63: inclusive scan of the per-token log-gates, suffix = total - scan
+                float l = 0.f, x = 0.f;
+                if (t < C) {
+                    l = t < valid ? p.log_gate[((int64_t)seg.start + c * C + t) * p.H_v + h] : 0.f;
+                    x = l;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, x, o);
+                        if (lane >= o) x += y;
+                    }
+                    if (lane == 31) scan_tmp[t >> 5] = x;
+                }
+                bar_state();
+                if (t < C) {
+                    const float total = scan_tmp[0] + scan_tmp[1];
+                    const float incl = t >= 32 ? x + scan_tmp[0] : x;
+                    fac[s][t] = t < valid ? __expf(total - incl) : 0.f;
+                    if (t == 0) gtot[c & 1][0] = total;
+                }
+            } else {
+                if (t < C) fac[s][t] = t < valid ? 1.f : 0.f;
+                if (t == 0) gtot[c & 1][0] = 0.f;
             }
-            gsum[c & 1] = own + other;
-            lam += own + other;
+            bar_state();
+            gsum[c & 1] = KIND == kDiag ? gtot[c & 1][i] : gtot[c & 1][0];
+            lam += gsum[c & 1];
+            // (2) Khat = factors * k, 16 bytes (8 channels of one token) per access. Row tok of
+            //     a 64-channel half holds physical 16-byte chunk pc = logical chunk ^ (tok % 8).
+            if (KIND != kLinear || valid < C) {
+#pragma unroll 1
+                for (int m = 0; m < C * 16 / kEpi; ++m) {
+                    const int e = t + kEpi * m;
+                    const int tok = e >> 4, hf = (e >> 3) & 1, pc = e & 7;
+                    uint4 *ptr = reinterpret_cast<uint4 *>(kt + hf * G::kHalf + tok * 128 + pc * 16);
+                    const uint4 w = *ptr;
+                    auto scale2 = [](uint32_t wj, float f0, float f1) {
+                        return pack_bf16x2(__uint_as_float(wj << 16) * f0, __uint_as_float(wj & 0xffff0000u) * f1);
+                    };
+                    uint4 o;
+                    if (KIND == kDiag) {
+                        const int ch = 64 * hf + 8 * (pc ^ (tok & 7));
+                        const float4 f0 = *reinterpret_cast<const float4 *>(gt + tok * D + ch);
+                        const float4 f1 = *reinterpret_cast<const float4 *>(gt + tok * D + ch + 4);
+                        o = make_uint4(scale2(w.x, f0.x, f0.y), scale2(w.y, f0.z, f0.w), scale2(w.z, f1.x, f1.y),
+                                       scale2(w.w, f1.z, f1.w));
+                    } else {
+                        const float ft = fac[s][tok];
+                        o = make_uint4(scale2(w.x, ft, ft), scale2(w.y, ft, ft), scale2(w.z, ft, ft),
+                                       scale2(w.w, ft, ft));
+                    }
+                    *ptr = o;
+                }
+            }
             fence_async_shared();
             mbar_arrive(&bars.kready[s]);
             return true;
         };
         auto fold = [&](int c) -> bool {
             const int b = c & 1;
-            if (!mbar_wait_or_abort(&bars.dfull[b], (c >> 1) & 1, p.err, kErrTimeout, &abort_flag))
+            if (!bar_state_and(mbar_wait_or_abort(&bars.dfull[b], (c >> 1) & 1, p.err, kErrTimeout,
+                                                  &abort_flag)))
                 return false;
             tc_fence_after();
             const float e = (KIND == kLinear) ? 1.f : expf(gsum[b]);
