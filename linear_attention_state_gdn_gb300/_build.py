@@ -24,6 +24,16 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"]
 
 
+# Translation units compiled as relocatable device code (-rdc=true) and device-linked into
+# the library. Chosen by measurement on GB300: the GDN chain kernel runs 10% faster compiled
+# this way; the gated build runs 30% slower, and the other units are unaffected.
+RDC_SOURCES = {"build_gdn_tc.cu"}
+
+
+def _flags(src: str):
+    return NVCC_FLAGS + (["-rdc=true"] if src in RDC_SOURCES else [])
+
+
 def nvcc() -> str:
     for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
         if cand and os.path.exists(cand):
@@ -47,6 +57,10 @@ def _stale(target: str, deps) -> bool:
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(OBJ, exist_ok=True)
     cc = nvcc()
+    stamp = os.path.join(OBJ, "flags.txt")   # objects built with other flags are rebuilt
+    flags = " ".join(NVCC_FLAGS + list(extra_flags) + sorted(RDC_SOURCES))
+    if not os.path.exists(stamp) or open(stamp).read() != flags:
+        force = True
     headers = _headers()
     objs, jobs = [], []
     for src in SOURCES:
@@ -54,7 +68,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         o = os.path.join(OBJ, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + headers):
-            jobs.append([cc, *NVCC_FLAGS, *extra_flags, "-c", s, "-o", o])
+            jobs.append([cc, *_flags(src), *extra_flags, "-c", s, "-o", o])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -68,8 +82,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         list(ex.map(run, jobs))
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        run([cc, *ARCH, "-shared", "-o", tmp, *objs, "-Xlinker", "-soname,libhypic.so"])
+        run([cc, *ARCH, "-rdc=true", "-shared", "-o", tmp, *objs, "-Xlinker", "-soname,libhypic.so"])
         os.replace(tmp, LIB)
+    with open(stamp, "w") as f:
+        f.write(flags)
     return LIB
 
 
