@@ -117,7 +117,8 @@ typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  *                     aligned (NULL when that is 0). DELTA / GDN with bf16 k, v and
  *                     d = 128 use 8 KB per (segment, value head, 64-token chunk): the
  *                     chunk matrices (I + Diag(b) L)^-1 Diag(b) that the chain kernel reads
- *                     back. The caller owns it; its contents are undefined after the call and
+ *                     back, plus 256 bytes of work-distribution counter (set by the call
+ *                     itself; no part needs to start at zero). The caller owns it; its contents are undefined after the call and
  *                     it may be reused by the next call on the same stream, but not by a call
  *                     still running on another stream. It must not overlap any argument.
  */

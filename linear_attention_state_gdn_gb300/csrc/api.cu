@@ -155,7 +155,8 @@ const char *hypic_status_string(hypic_status s) {
 size_t hypic_build_workspace_bytes(const hypic_build_args *a) {
     if (!build_shape_ok(a) || a->n_seg == 0 || !a->seg_offsets) return 0;
     if (pick_build(a) != BuildPath::GdnTc) return 0;
-    return (size_t)gdn_records(a) * (size_t)kGdnRecordBytes;
+    const int64_t records = gdn_records(a);
+    return records > 0 ? (size_t)records * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail : 0;
 }
 
 hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {

@@ -15,10 +15,15 @@
 // the pair (S(C|0), T_C) that "Cut First-Token Latency by 3.25x: Introducing HYPIC ..."
 // (besthub.dev), paragraph "For linear layers", stores for DeltaNet / GDN layers.
 //
-// Persistent CTAs of 128 threads, four per SM, each walking a strided list of records: the
-// k tile of the next record is requested as soon as the current gram has read the single k
-// buffer, its gram is issued while two warps finish the current inverse (two TMEM buffers),
-// and b is loaded a record ahead, so loads and grams overlap the inversions.
+// Persistent CTAs of 128 threads, four per SM. Records are handed out as tickets: a CTA
+// starts with two fixed records and takes each further one from a counter in the workspace
+// (zeroed before the launch), so CTAs that run faster take more records and all CTAs finish
+// within about one record of each other. The k tile of the next record is requested as soon
+// as the current gram has read the single k buffer, its gram is issued while two warps
+// finish the current inverse (two TMEM buffers), and b is loaded a record ahead, so loads
+// and grams overlap the inversions. A CTA that has drawn its last ticket lets the chain
+// kernel launch (programmatic dependent launch); the chain waits for this grid's completion
+// before it reads any record.
 //   1. TMA the chunk's k (two 128B-swizzled 64-channel halves); b masked past the segment end.
 //   2. One thread issues the gram K K^T (M = 64 tcgen05 MMA, fp32 accumulator in TMEM).
 //   3. A = Diag(b) L in fp32 shared memory (rows padded to 68 floats).
@@ -104,12 +109,34 @@ __device__ __forceinline__ void half_block(const float *A32, float *N32, float *
     __syncwarp();   // Tw is reused by this warp's next half-block
 }
 
-// Records are visited in the order (segment, chunk, head), so the value heads that share a
-// key head read the same k tile back to back (from L2). A CTA walks every gridDim.x-th
-// record; the position is advanced in mixed radix (head, chunk, segment) without divisions.
+// Records are numbered in the order (segment rank, chunk, value head), so the value heads
+// that share a key head read the same k tile back to back (from L2); segment rank r owns
+// numbers [wsb_r, wsb_r + H_v nch_r). A number is turned back into its record by a binary
+// search over the segment table.
 struct Walk {
-    int r, c, h;   // segment rank, chunk, value head; r == n_seg when past the end
+    int r, c, h;   // segment rank, chunk, value head; r == n_seg: no record
 };
+
+__device__ __forceinline__ Walk decode(const BuildParams &p, int64_t t, int64_t total) {
+    Walk w{p.n_seg, 0, 0};
+    if (t >= total) return w;
+    int lo = 0, hi = p.n_seg - 1;   // the last rank with wsb <= t (empty segments come last)
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.seg[mid].wsb <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    const int local = (int)(t - p.seg[lo].wsb);
+    w.r = lo;
+    w.c = local / p.H_v;
+    w.h = local - w.c * p.H_v;
+    return w;
+}
+
+__device__ __forceinline__ int64_t total_records(const BuildParams &p) {
+    const SegEntry &l = p.seg[p.n_seg - 1];
+    return (int64_t)l.wsb + (int64_t)p.H_v * ((l.len + C - 1) / C);
+}
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK) {
@@ -118,30 +145,13 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     __shared__ uint64_t kfull, gfull[2];
     __shared__ uint32_t tslot;
     __shared__ int s_ok;
+    __shared__ Walk s_n2[2];   // the record after `nxt`, drawn by thread kCtl (two slots)
     __shared__ __align__(16) float vb[2][C];
 
-    const int max_nch = (p.max_len + C - 1) / C;
-    const int stride = gridDim.x;
-    const int sh = stride % p.H_v, sc = (stride / p.H_v) % max_nch, sr = stride / (p.H_v * max_nch);
+    const int64_t total = total_records(p);
+    unsigned *tickets = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(p.workspace) + total * kGdnRecordBytes);
     auto nch_of = [&](int r) { return (p.seg[r].len + C - 1) / C; };
-    auto valid = [&](const Walk &w) { return w.r < p.n_seg && w.c < nch_of(w.r); };
-    auto step = [&](Walk w) {   // next record of this CTA (skipping chunks past a segment's end)
-        do {
-            w.h += sh;
-            int carry = w.h >= p.H_v;
-            w.h -= carry ? p.H_v : 0;
-            w.c += sc + carry;
-            carry = w.c >= max_nch;
-            w.c -= carry ? max_nch : 0;
-            w.r += sr + carry;
-        } while (w.r < p.n_seg && w.c >= nch_of(w.r));
-        return w;
-    };
-    Walk cur;
-    cur.h = blockIdx.x % p.H_v;
-    cur.c = (blockIdx.x / p.H_v) % max_nch;
-    cur.r = blockIdx.x / (p.H_v * max_nch);
-    if (cur.r < p.n_seg && !valid(cur)) cur = step(cur);
+    Walk cur = decode(p, blockIdx.x, total);
     if (cur.r >= p.n_seg) return;   // uniform: the whole CTA leaves before any set-up
     const int q = threadIdx.x, warp = q >> 5, lane = q & 31;
     float *A32 = reinterpret_cast<float *>(smem + kOffA32);
@@ -190,7 +200,8 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         return q < min(C, sg.len - w.c * C) ? p.beta[((int64_t)sg.start + w.c * C + q) * p.H_v + w.h] : 0.f;
     };
     bool ok = true;
-    Walk nxt = step(cur);
+    int64_t ticket = 0;   // thread kCtl
+    Walk nxt = decode(p, (int64_t)gridDim.x + blockIdx.x, total);
     float beta_cur = load_beta(cur);
     if (q == kCtl) {
         prefetch_tmap(&tmK);
@@ -211,6 +222,9 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
                 if (nxt.r < p.n_seg) load_k(nxt);
             }
             s_ok = ok ? 1 : 0;
+            // the ticket of the record after `nxt` (the counter's answer is used only at
+            // level 3 below, so its latency overlaps this record's inverse)
+            if (nxt.r < p.n_seg) ticket = 2 * (int64_t)gridDim.x + atomicAdd(tickets, 1u);
         }
         __syncthreads();
         if (!s_ok) break;   // uniform
@@ -271,8 +285,14 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         if (warp < 2) half_block(A32, N32, Tw, 3, 0, warp, lane);
         // warps 2-3 have no level-3 work: the next record's gram (its k tile was requested at
         // the top of this iteration) into the other TMEM buffer, last read a record ago
-        if (q == kCtl && ok && nxt.r < p.n_seg) ok = gram(b ^ 1);
+        // and the ticket of the record after it
+        if (q == kCtl) {
+            if (ok && nxt.r < p.n_seg) ok = gram(b ^ 1);
+            s_n2[b] = nxt.r < p.n_seg ? decode(p, ticket, total) : nxt;
+        }
         __syncthreads();
+        const Walk n2 = s_n2[b];   // slot b is written again two records later
+        if (n2.r >= p.n_seg) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         // record: N Diag(b) as bf16 rows t' (blocks above the diagonal are zero)
         uint8_t *dst = static_cast<uint8_t *>(p.workspace) +
                        ((int64_t)seg.wsb + (int64_t)cur.h * nch + cur.c) * (int64_t)kGdnRecordBytes;
@@ -292,7 +312,7 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
             *reinterpret_cast<uint4 *>(dst + tp * 128 + s8 * 2) = pk;
         }
         cur = nxt;
-        nxt = cur.r < p.n_seg ? step(cur) : cur;
+        nxt = n2;
         beta_cur = beta_next;
     }
     if (q == kCtl) {   // after a wait gave up: let every copy and MMA in flight land first
@@ -311,8 +331,9 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
 }  // namespace
 
 cudaError_t launch_build_gdn_prep(const BuildParams &p, cudaStream_t s) {
-    const int max_nch = (p.max_len + C - 1) / C;
-    const int64_t total = (int64_t)p.n_seg * max_nch * p.H_v;
+    if (p.n_seg == 0) return cudaSuccess;
+    const SegEntry &l = p.seg[p.n_seg - 1];
+    const int64_t total = (int64_t)l.wsb + (int64_t)p.H_v * ((l.len + C - 1) / C);
     if (total == 0) return cudaSuccess;
     if (total > INT32_MAX / 2) return cudaErrorInvalidValue;
     const int64_t N = p.n_tok > 0 ? p.n_tok : 1;
@@ -326,6 +347,9 @@ cudaError_t launch_build_gdn_prep(const BuildParams &p, cudaStream_t s) {
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    // the ticket counter after the records (the workspace tail), zeroed for this launch
+    e = cudaMemsetAsync(static_cast<uint8_t *>(p.workspace) + total * kGdnRecordBytes, 0, sizeof(unsigned), s);
+    if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(total, (int64_t)sms * kCtasPerSm);
     build_gdn_prep_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, tmK);
     return cudaGetLastError();

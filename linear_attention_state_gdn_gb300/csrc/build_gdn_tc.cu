@@ -213,6 +213,10 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 tma_load_3d(kt, &tmK, &bars.kfull[ks], 0, hk, t0);
                 tma_load_3d(kt + kHalf, &tmK, &bars.kfull[ks], 64, hk, t0);
                 kc = c + 1;
+                // the records are written by the preparation kernel, which may still be
+                // running (this grid is a programmatic dependent launch): wait for it to
+                // complete before the first record load (k and v above are inputs)
+                if (c == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
                 const int vs = c % kVSlots, vuse = c / kVSlots;
                 if (vuse >= 1 && !wait(&bars.vempty[vs], (vuse - 1) & 1)) break;
                 uint8_t *vt = smem + kOffVR + vs * kVR;
@@ -555,8 +559,24 @@ cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(build_gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    build_gdn_tc_kernel<<<blocks, kThreads, kSmemBytes, s>>>(p, tmK, tmV, tmR);
-    return cudaGetLastError();
+    if (records == 0) {
+        build_gdn_tc_kernel<<<blocks, kThreads, kSmemBytes, s>>>(p, tmK, tmV, tmR);
+        return cudaGetLastError();
+    }
+    // launched as a programmatic dependent of the preparation kernel: CTAs may start (set-up,
+    // k / v loads) on SMs the preparation has left, and wait for its completion before
+    // reading its records
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, build_gdn_tc_kernel, p, tmK, tmV, tmR);
 }
 
 }  // namespace hypic

@@ -27,6 +27,7 @@ struct SegEntry {
 // (segment, value head, 64-token chunk).
 constexpr int kGdnChunk = 64;
 constexpr int64_t kGdnRecordBytes = kGdnChunk * kGdnChunk * 2;
+constexpr int64_t kGdnWorkspaceTail = 256;   // after the records: the preparation's ticket counter
 
 struct BuildParams {
     int32_t family;

@@ -204,9 +204,10 @@ def test_binding_refuses_cpu_tensors():
 
 
 def test_workspace_bytes_of_the_tensor_core_gdn_build(lib):
-    # bf16, d = 128, DeltaNet / GDN: 8 KB per (segment, value head, 64-token chunk)
+    # bf16, d = 128, DeltaNet / GDN: 8 KB per (segment, value head, 64-token chunk) and a
+    # 256-byte tail (the preparation kernel's ticket counter)
     a = good_build(lens=(64, 130))
-    assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == 4 * (1 + 3) * 8192
+    assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == 4 * (1 + 3) * 8192 + 256
     a.d_k = a.d_v = 64                      # exact fp32-state path: no workspace
     assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == 0
     b = good_build(family=2)                # gated families: no workspace
