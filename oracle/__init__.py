@@ -54,8 +54,9 @@ def _load():
             lib.oracle_run.argtypes = [I, I, P, I, I, I, I, P, P, P, P, P, P, P, I]
             lib.oracle_compose_scan.argtypes = [I, I64, I, I, P, P, P, P, I]
             lib.oracle_materialize_T.argtypes = [I, I64, I, P, P, P]
+            lib.oracle_compose_transitions.argtypes = [I, I, I64, I, P, P, P, P, I]
             for f in (lib.oracle_build, lib.oracle_run, lib.oracle_compose_scan,
-                      lib.oracle_materialize_T):
+                      lib.oracle_materialize_T, lib.oracle_compose_transitions):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -139,6 +140,36 @@ def compose_scan(T, S, S0=None, nthreads=0):
     if rc != 0:
         raise RuntimeError(f"oracle_compose_scan failed ({rc})")
     return out
+
+
+def compose_transitions(family, lam, P=None, d_k=None):
+    """Transition of the entry composed from n_seg consecutive segments, log-scaled:
+    lam_total = sum_j lam_j and (delta / gdn) P_total = P_{n-1} ... P_0, fp64.
+
+    lam [n_seg, U] (diag [n_seg, U, d_k]; ignored for linear, pass d_k and a [n_seg, U]
+    array of zeros or any values), P [n_seg, U, d_k, d_k] for delta / gdn. Returns
+    (lam_total [U] or [U, d_k], P_total [U, d_k, d_k] or None).
+    """
+    lib = _load()
+    fam = _family(family)
+    lam = _f64(lam)
+    dense = fam in (FAMILIES["delta"], FAMILIES["gdn"])
+    if fam == FAMILIES["diag"]:
+        n_seg, U, d_k = lam.shape
+    else:
+        n_seg, U = lam.shape[:2]
+    if dense:
+        P = _f64(P)
+        d_k = P.shape[-1]
+        assert P.shape == (n_seg, U, d_k, d_k)
+    assert d_k is not None
+    lam_total = np.zeros((U, d_k) if fam == FAMILIES["diag"] else (U,))
+    P_total = np.zeros((U, d_k, d_k)) if dense else None
+    rc = lib.oracle_compose_transitions(fam, n_seg, U, d_k, _ptr(lam), _ptr(P), _ptr(lam_total),
+                                        _ptr(P_total), default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_compose_transitions failed ({rc})")
+    return lam_total, P_total
 
 
 def materialize_T(family, lam, P=None, d_k=None):

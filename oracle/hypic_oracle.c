@@ -23,7 +23,7 @@
  *
  *  - The composition scan prefix_j = T_j . prefix_{j-1} + S_j (besthub.dev paragraph
  *    "For linear layers": reuse composes T_C2 . S(C1) + S(C2)), with explicit dense
- *    matrix products.
+ *    matrix products, and the transition of the composed entry, T_{n-1} ... T_0.
  *
  * The pages name the families (plain linear attention, RetNet, Mamba2, GLA, DeltaNet,
  * GDN) but print no equation. The recurrences below are the standard published forms,
@@ -284,4 +284,54 @@ int oracle_materialize_T(int family, int64_t n, int d_k, const double *lam, cons
     return 0;
 }
 
-int oracle_version(void) { return 1; }
+/* The transition of consecutive segments composed into one cache entry, in the log-scaled
+ * storage of the library: T(C_0 ... C_{n-1}) = T_{n-1} ... T_0 (latest segment leftmost;
+ * "Cut First-Token Latency by 3.25x: Introducing HYPIC ..." (besthub.dev), paragraph "For
+ * linear layers": an entry is the pair (T_C, S(C|0)) and entries compose as
+ * T_C2 . S(C1) + S(C2), whose transition is T_C2 T_C1). With T_j = exp(lam_j) P_j:
+ *   lam_total = sum_j lam_j                      [n_units] (DIAG: [n_units][d_k])
+ *   P_total   = P_{n-1} ... P_0                  DELTA / GDN: [n_units][d_k][d_k]
+ * lam [n_seg][n_units] (DIAG [n_seg][n_units][d_k]; unused for LINEAR, whose lam_total is
+ * 0), P [n_seg][n_units][d_k][d_k]. Explicit dense products, one segment at a time. */
+int oracle_compose_transitions(int family, int n_seg, int64_t n_units, int d_k, const double *lam,
+                               const double *P, double *lam_total, double *P_total, int nthreads) {
+    if (family < FAM_LINEAR || family > FAM_GDN || n_seg < 1 || n_units < 0 || d_k <= 0) return -1;
+    const int dense = family == FAM_DELTA || family == FAM_GDN;
+    const int nl = family == FAM_DIAG ? d_k : 1;
+    set_threads(nthreads);
+    int err = 0;
+#pragma omp parallel
+    {
+        double *nxt = dense ? (double *)malloc(sizeof(double) * d_k * d_k) : NULL;
+        if (dense && !nxt) {
+#pragma omp atomic write
+            err = -2;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t u = 0; u < n_units; ++u) {
+            for (int i = 0; i < nl; ++i) {
+                double acc = 0.0;
+                if (family != FAM_LINEAR)
+                    for (int j = 0; j < n_seg; ++j) acc += lam[((size_t)j * n_units + u) * nl + i];
+                lam_total[(size_t)u * nl + i] = acc;
+            }
+            if (!dense || !nxt) continue;
+            double *cur = P_total + (size_t)u * d_k * d_k;
+            memcpy(cur, P + (size_t)u * d_k * d_k, sizeof(double) * d_k * d_k);
+            for (int j = 1; j < n_seg; ++j) {
+                const double *Pj = P + ((size_t)j * n_units + u) * d_k * d_k;
+                for (int i = 0; i < d_k; ++i)
+                    for (int c = 0; c < d_k; ++c) {
+                        double acc = 0.0;
+                        for (int m = 0; m < d_k; ++m) acc += Pj[(size_t)i * d_k + m] * cur[(size_t)m * d_k + c];
+                        nxt[(size_t)i * d_k + c] = acc;
+                    }
+                memcpy(cur, nxt, sizeof(double) * d_k * d_k);
+            }
+        }
+        free(nxt);
+    }
+    return err;
+}
+
+int oracle_version(void) { return 2; }

@@ -11,7 +11,9 @@ What pins what (a plausible mistake anywhere in the oracle fails at least one ch
 * brute force on tiny inputs in exact rational arithmetic (sympy), with the transition
   factors formed as dense matrices and multiplied out;
 * the composition theorem against the oracle's own sequential run, and the failure of
-  naive end-state addition for RetNet (but not for plain linear attention).
+  naive end-state addition for RetNet (but not for plain linear attention);
+* the composed transition of consecutive segments against the transition of the same
+  tokens built as one segment.
 """
 import json
 import os
@@ -306,6 +308,59 @@ def test_materialize_T_forms():
     P = np.arange(4.0).reshape(1, 1, 2, 2)
     np.testing.assert_allclose(oracle.materialize_T("gdn", np.array([[np.log(2.0)]]), P)[0, 0],
                                2 * P[0, 0])
+
+
+# ------------------------------------------------------------------ composed entries
+
+def segment_log_scale(inp):
+    """lam of every (segment, value head) from the gates alone: the sum of the log-gates
+    over the segment (L log gamma for a constant decay, 0 without gates)."""
+    offs = inp.seg_offsets
+    n, H, d = inp.n_seg, inp.H_v, inp.d_k
+    lam = np.zeros((n, H, d) if inp.family == "diag" else (n, H))
+    for j in range(n):
+        a, b = offs[j], offs[j + 1]
+        if inp.log_gate is not None:
+            lam[j] = f64(inp.log_gate)[a:b].sum(0)
+        elif inp.log_gamma is not None:
+            lam[j] = (b - a) * f64(inp.log_gamma)
+    return lam
+
+
+@pytest.mark.parametrize("family,per_token", [("linear", False), ("scalar", False), ("scalar", True),
+                                              ("diag", False), ("delta", False), ("gdn", False)])
+def test_composed_transition_is_the_transition_of_the_concatenation(family, per_token):
+    # segments built one by one, their transitions composed, against the same tokens built
+    # as one segment: T(C_0 ... C_4) = T_4 ... T_0, through the log-scaled storage
+    inp = synth.make_inputs(family, 2, 4, 8, [9, 0, 13, 1, 6], torch.float32, seed=23,
+                            gla_div=8.0, alpha_scale=0.1, per_token_scalar=per_token)
+    _, T = run_build(inp)
+    lam = segment_log_scale(inp)
+    dense = family in ("delta", "gdn")
+    P = T * np.exp(-lam)[..., None, None] if dense else None
+    lam_t, P_t = oracle.compose_transitions(family, lam, P, d_k=8)
+    T_t = oracle.materialize_T(family, lam_t, P_t, d_k=8)
+    N = int(inp.seg_offsets[-1])
+    _, T_whole = oracle.build_segments(family, [0, N], f64(inp.k), f64(inp.v), f64(inp.log_gate),
+                                       f64(inp.log_gamma), f64(inp.beta))
+    for h in range(4):
+        assert relF(T_t[h], T_whole[0, h]) < 1e-12
+    if dense:
+        # the order is what the check above fixes: the reversed product is far off
+        rev = P[0, 0]
+        for j in range(1, inp.n_seg):
+            rev = rev @ P[j, 0]
+        assert relF(np.exp(lam_t[0]) * rev, T_whole[0, 0]) > 1e-3
+
+
+def test_composed_transition_of_one_segment_is_that_segment():
+    c = synth.make_compose_inputs("gdn", 1, 3, 8, seed=24)
+    lam, P = c.lam.double().numpy(), c.P.double().numpy()
+    lam_t, P_t = oracle.compose_transitions("gdn", lam, P)
+    np.testing.assert_array_equal(lam_t, lam[0])
+    np.testing.assert_array_equal(P_t, P[0])
+    lam_l, P_l = oracle.compose_transitions("linear", lam, None, d_k=8)
+    assert P_l is None and not lam_l.any()
 
 
 # ------------------------------------------------------------------ naive addition
