@@ -330,7 +330,20 @@ def section_gdn_compose(flush, peak, steps=10, warmup=3, layers=48):
            "units": int(S.shape[1]), "n_seg": int(S.shape[0]), "compose_ms": round(ms, 4),
            "compose_bytes": nbytes, "compose_gbs": round(gbs, 1),
            "compose_hbm_frac": round(gbs / peak["hbm_gbs"], 4)}
-    del S, lam, P, prefix
+    # the same launch also composing the 64 entries of every unit into one: lam_total and
+    # P_total = P_63 ... P_0. Algorithmic bytes add P_0 read once and the totals written;
+    # the transition chain's second read of P_1 .. P_63 counts as overhead.
+    U, d = S.shape[1], S.shape[2]
+    lam_t = torch.empty(U, dtype=torch.float32, device=S.device)
+    P_t = torch.empty((U, d, d), dtype=torch.float32, device=S.device)
+    g = lambda: hy.hypic_compose_scan("gdn", S, lam, P, prefix=prefix, lam_total=lam_t, P_total=P_t)
+    (tt,), _ = time_loop([g], steps, warmup, flush)
+    ms_t = statistics.mean(tt)
+    nbytes_t = nbytes + U * (2 * d * d * 4 + 4)
+    out["with_totals"] = {"compose_ms": round(ms_t, 4), "compose_bytes": nbytes_t,
+                          "compose_gbs": round(nbytes_t / ms_t / 1e6, 1),
+                          "compose_hbm_frac": round(nbytes_t / ms_t / 1e6 / peak["hbm_gbs"], 4)}
+    del S, lam, P, prefix, lam_t, P_t
     torch.cuda.empty_cache()
     return out
 

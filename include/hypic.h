@@ -157,6 +157,16 @@ typedef struct {
  *   S0           optional initial state [n_units][d_k][d_v] fp32; NULL = zero state
  *   prefix       out [n_seg][n_units][d_k][d_v] fp32: prefix[j] = state after segments
  *                0..j, i.e. exp(lam_j) P_j prefix[j-1] + S_j with prefix[-1] = S0
+ *   lam_total    optional out (NULL = skip): the log-scale of the transition of all n_seg
+ *                segments composed, sum_j lam_j; [n_units] (DIAG: [n_units][d_k]); 0 for
+ *                LINEAR. 4-byte aligned.
+ *   P_total      optional out (NULL = skip), DELTA / GDN only (must be NULL otherwise):
+ *                P_{n-1} ... P_0 [n_units][d_k][d_k] fp32, latest segment leftmost.
+ *                16-byte aligned.
+ *   With S0 = NULL, (prefix[n-1], exp(lam_total) P_total) is the cache entry
+ *   (S(C|0), T_C) of the concatenation C = C_0 ... C_{n-1}: entries compose as
+ *   T_C2 . S(C1) + S(C2) with transition T_C2 T_C1 (besthub.dev, paragraph "For linear
+ *   layers"). Neither total may overlap an input or prefix.
  */
 typedef struct {
     int32_t family;
@@ -169,6 +179,8 @@ typedef struct {
     const float *P;
     const float *S0;
     float *prefix;
+    float *lam_total;
+    float *P_total;
 } hypic_compose_args;
 
 /* Build (S(C|0), T_C) for every segment and value head of one layer in one launch.
@@ -190,7 +202,8 @@ hypic_status hypic_build_segments(const hypic_build_args *args, void *stream);
 #define HYPIC_STATIC_WS_BYTES (64u << 20)
 hypic_status hypic_build_segments_static_ws(const hypic_build_args *args, void *stream);
 
-/* Inclusive prefix scan of the composition over n_seg segments for n_units units. */
+/* Inclusive prefix scan of the composition over n_seg segments for n_units units, and
+ * optionally the transition of all of them composed (lam_total, P_total). */
 hypic_status hypic_compose_scan(const hypic_compose_args *args, void *stream);
 
 /* Device scratch bytes hypic_build_segments needs for these arguments (host-only query;

@@ -50,7 +50,8 @@ class ComposeArgs(ctypes.Structure):
     _fields_ = [("family", ctypes.c_int32), ("n_seg", ctypes.c_int32),
                 ("n_units", ctypes.c_int64), ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
                 ("S", ctypes.c_void_p), ("lam", ctypes.c_void_p), ("P", ctypes.c_void_p),
-                ("S0", ctypes.c_void_p), ("prefix", ctypes.c_void_p)]
+                ("S0", ctypes.c_void_p), ("prefix", ctypes.c_void_p),
+                ("lam_total", ctypes.c_void_p), ("P_total", ctypes.c_void_p)]
 
 
 _lib = None
@@ -194,24 +195,29 @@ def hypic_build_segments_static_ws(family, k, v, seg_offsets, log_gate=None, log
 STATIC_WS_BYTES = 64 << 20   # HYPIC_STATIC_WS_BYTES in include/hypic.h
 
 
-def make_compose_args(family, S, lam, P=None, S0=None, prefix=None):
+def make_compose_args(family, S, lam, P=None, S0=None, prefix=None, lam_total=None, P_total=None):
     fam = FAMILY[family] if isinstance(family, str) else int(family)
     a = ComposeArgs()
     a.family = fam
     a.n_seg, a.n_units, a.d_k, a.d_v = S.shape[0], S.shape[1], S.shape[2], S.shape[3]
     a.S, a.lam, a.P, a.S0, a.prefix = _ptr(S), _ptr(lam), _ptr(P), _ptr(S0), _ptr(prefix)
+    a.lam_total, a.P_total = _ptr(lam_total), _ptr(P_total)
     return a
 
 
-def hypic_compose_scan(family, S, lam, P=None, S0=None, prefix=None, stream=None):
+def hypic_compose_scan(family, S, lam, P=None, S0=None, prefix=None, lam_total=None,
+                       P_total=None, stream=None):
     """Inclusive prefix scan prefix[j] = exp(lam_j) P_j prefix[j-1] + S_j over segments.
-    S [n_seg, U, d, d]; returns prefix of the same shape (allocated when not given)."""
+    S [n_seg, U, d, d]; returns prefix of the same shape (allocated when not given).
+    Optional outputs: lam_total [U] ([U, d] for "diag") = sum_j lam_j and, for "gdn" /
+    "delta", P_total [U, d, d] = P_{n-1} ... P_0 (the transition of all segments composed)."""
     lib = load_library()
     if prefix is None:
         prefix = torch.empty_like(S)
-    a = make_compose_args(family, S, lam, P, S0, prefix)
+    a = make_compose_args(family, S, lam, P, S0, prefix, lam_total, P_total)
     _check(lib.hypic_compose_scan(ctypes.byref(a), _stream(stream)), "hypic_compose_scan")
     return prefix
+
 
 
 def hypic_build_kernel_name(family, k, v, seg_offsets, **kw) -> str:

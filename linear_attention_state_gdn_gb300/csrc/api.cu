@@ -137,7 +137,7 @@ bool compose_shape_ok(const hypic_compose_args *a) {
 
 extern "C" {
 
-int32_t hypic_abi_version(void) { return 1; }
+int32_t hypic_abi_version(void) { return 2; }
 
 const char *hypic_status_string(hypic_status s) {
     switch (s) {
@@ -300,11 +300,14 @@ hypic_status hypic_compose_scan(const hypic_compose_args *a, void *stream) {
     if (!a->S || !a->prefix) return HYPIC_ERR_INVALID_ARG;
     if (fam != HYPIC_FAM_LINEAR && !a->lam) return HYPIC_ERR_INVALID_ARG;
     if (dense && !a->P) return HYPIC_ERR_INVALID_ARG;
-    const void *v16[] = {a->S, a->P, a->S0, a->prefix};
+    if (a->P_total && !dense) return HYPIC_ERR_INVALID_ARG;
+    const void *v16[] = {a->S, a->P, a->S0, a->prefix, a->P_total};
     for (const void *p : v16)
         if (p && !aligned(p, 16)) return HYPIC_ERR_ALIGNMENT;
     if (a->lam && !aligned(a->lam, 4)) return HYPIC_ERR_ALIGNMENT;
-    const void *dev_ptrs[] = {a->S, a->P, a->S0, a->prefix, fam == HYPIC_FAM_LINEAR ? nullptr : a->lam};
+    if (a->lam_total && !aligned(a->lam_total, 4)) return HYPIC_ERR_ALIGNMENT;
+    const void *dev_ptrs[] = {a->S, a->P, a->S0, a->prefix, fam == HYPIC_FAM_LINEAR ? nullptr : a->lam,
+                              a->lam_total, a->P_total};
     for (const void *p : dev_ptrs)
         if (p && !on_device(p)) return HYPIC_ERR_INVALID_ARG;
 
@@ -316,6 +319,16 @@ hypic_status hypic_compose_scan(const hypic_compose_args *a, void *stream) {
         overlaps(a->prefix, state_bytes, a->lam, lam_bytes) ||
         overlaps(a->prefix, state_bytes, a->S0, (size_t)a->n_units * D * D * 4))
         return HYPIC_ERR_INVALID_ARG;
+    // the totals overlap nothing: not the inputs, not prefix, not each other
+    const size_t unit_bytes = (size_t)a->n_units * D * D * 4;
+    const size_t lt_bytes = (size_t)a->n_units * (fam == HYPIC_FAM_DIAG ? D : 1) * 4;
+    const struct { const void *p; size_t n; } ins[] = {
+        {a->S, state_bytes}, {a->P, dense ? state_bytes : 0}, {a->lam, lam_bytes},
+        {a->S0, unit_bytes}, {a->prefix, state_bytes}};
+    for (const auto &in : ins)
+        if (overlaps(a->lam_total, lt_bytes, in.p, in.n) || overlaps(a->P_total, unit_bytes, in.p, in.n))
+            return HYPIC_ERR_INVALID_ARG;
+    if (overlaps(a->lam_total, lt_bytes, a->P_total, unit_bytes)) return HYPIC_ERR_INVALID_ARG;
 
     unsigned *err = status_word(nullptr);
     if (!err) return HYPIC_ERR_CUDA;
@@ -330,15 +343,19 @@ hypic_status hypic_compose_scan(const hypic_compose_args *a, void *stream) {
     p.P = a->P;
     p.S0 = a->S0;
     p.prefix = a->prefix;
+    p.lam_total = a->lam_total;
+    p.P_total = a->P_total;
     p.err = err;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
     switch (pick_compose(a)) {
-    case ComposePath::DenseTc: return from_cuda(launch_compose_dense_tc(p, s));
-    case ComposePath::DenseSimt: return from_cuda(launch_compose_dense_simt(p, s));
-    case ComposePath::Scaled: return from_cuda(launch_compose_scaled(p, s));
+    case ComposePath::DenseTc: e = launch_compose_dense_tc(p, s); break;
+    case ComposePath::DenseSimt: e = launch_compose_dense_simt(p, s); break;
+    case ComposePath::Scaled: e = launch_compose_scaled(p, s); break;
     case ComposePath::None: break;
     }
-    return HYPIC_OK;
+    if (e == cudaSuccess && a->lam_total) e = launch_compose_lam_total(p, s);
+    return from_cuda(e);
 }
 
 const char *hypic_build_kernel_name(const hypic_build_args *a) {

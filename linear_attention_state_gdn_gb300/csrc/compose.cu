@@ -8,7 +8,10 @@
 //   A pure element-wise stream: each thread carries 4 consecutive state elements of one
 //   unit through all segments, with the next segments' S loads issued ahead.
 // compose_dense_simt: dense transitions T_j = exp(lam_j) P_j on CUDA cores, used for head
-//   sizes below 128 (the d = 128 case runs on the tensor cores, compose_tc.cu).
+//   sizes below 128 (the d = 128 case runs on the tensor cores, compose_tc.cu). With P_total
+//   requested, units U .. 2U-1 of the grid carry the transition chain P_j ... P_0 instead.
+// compose_lam_total: the log-scale of the composed transition, sum_j lam_j (the transition
+//   of an entry composed from consecutive segments is T_{n-1} ... T_0).
 #include "internal.cuh"
 
 namespace hypic {
@@ -87,19 +90,25 @@ compose_dense_simt_kernel(const __grid_constant__ ComposeParams p) {
     float *A = smem;                   // [D][LDA]
     float *X = smem + D * LDA;         // [D][kDenseCols]
 
-    const int64_t u = blockIdx.x / (D / kDenseCols);
+    // units 0 .. U-1: the prefix scan; U .. 2U-1 (with P_total): the transition chain
+    // Q_j = P_j Q_{j-1}, Q_0 = P_0, of unit u - U, written once at the end
+    const int64_t ublk = blockIdx.x / (D / kDenseCols);
+    const bool trans = ublk >= p.n_units;
+    const int64_t u = trans ? ublk - p.n_units : ublk;
     const int cb = (blockIdx.x % (D / kDenseCols)) * kDenseCols;
     const int tid = threadIdx.x;
     const int tx = tid % (kDenseCols / 4);   // 4-column group
     const int ty = tid / (kDenseCols / 4);   // row group
     const int64_t DD = (int64_t)D * D;
 
-    bool have_state = p.S0 != nullptr;
-    if (have_state)
+    bool have_state = trans || p.S0 != nullptr;
+    if (have_state) {
+        const float *X0 = trans ? p.P + u * DD : p.S0 + u * DD;
         for (int e = tid; e < D * kDenseCols; e += kDenseThreads)
-            X[e] = p.S0[u * DD + (int64_t)(e / kDenseCols) * D + cb + e % kDenseCols];
+            X[e] = X0[(int64_t)(e / kDenseCols) * D + cb + e % kDenseCols];
+    }
 
-    for (int j = 0; j < p.n_seg; ++j) {
+    for (int j = trans ? 1 : 0; j < p.n_seg; ++j) {
         const int64_t base = ((int64_t)j * p.n_units + u) * DD;
         float acc[RPT][4];
 #pragma unroll
@@ -127,12 +136,17 @@ compose_dense_simt_kernel(const __grid_constant__ ComposeParams p) {
                 }
             }
         }
-        const float sc = have_state ? expf(p.lam[(int64_t)j * p.n_units + u]) : 0.f;
+        const float sc = trans ? 1.f : have_state ? expf(p.lam[(int64_t)j * p.n_units + u]) : 0.f;
         __syncthreads();   // every thread is done reading X
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
             const int row = ty * RPT + r;
             const int64_t off = base + (int64_t)row * D + cb + tx * 4;
+            if (trans) {
+                *reinterpret_cast<float4 *>(&X[row * kDenseCols + tx * 4]) =
+                    make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+                continue;
+            }
             const float4 s = *reinterpret_cast<const float4 *>(p.S + off);
             float4 o;
             o.x = fmaf(sc, acc[r][0], s.x);
@@ -144,6 +158,21 @@ compose_dense_simt_kernel(const __grid_constant__ ComposeParams p) {
         }
         have_state = true;
     }
+    if (trans) {
+        __syncthreads();
+        for (int e = tid; e < D * kDenseCols; e += kDenseThreads)
+            p.P_total[u * DD + (int64_t)(e / kDenseCols) * D + cb + e % kDenseCols] = X[e];
+    }
+}
+
+__global__ void __launch_bounds__(256) compose_lam_total_kernel(const __grid_constant__ ComposeParams p) {
+    const int nl = p.family == HYPIC_FAM_DIAG ? p.D : 1;
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // unit * nl + row
+    if (i >= p.n_units * nl) return;
+    float acc = 0.f;
+    if (p.family != HYPIC_FAM_LINEAR)
+        for (int j = 0; j < p.n_seg; ++j) acc += p.lam[(int64_t)j * p.n_units * nl + i];
+    p.lam_total[i] = acc;
 }
 
 template <int D>
@@ -152,7 +181,7 @@ cudaError_t launch_dense(const ComposeParams &p, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(compose_dense_simt_kernel<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)(p.n_units * (D / kDenseCols)));
+    dim3 grid((unsigned)(p.n_units * (p.P_total ? 2 : 1) * (D / kDenseCols)));
     compose_dense_simt_kernel<D><<<grid, kDenseThreads, smem, s>>>(p);
     return cudaGetLastError();
 }
@@ -164,6 +193,13 @@ cudaError_t launch_compose_scaled(const ComposeParams &p, cudaStream_t s) {
     const int n4 = p.D * p.D / 4;
     dim3 grid((unsigned)(p.n_units * ((n4 + kScaledThreads - 1) / kScaledThreads)));
     compose_scaled_kernel<<<grid, kScaledThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_compose_lam_total(const ComposeParams &p, cudaStream_t s) {
+    if (p.n_units == 0 || !p.lam_total) return cudaSuccess;
+    const int64_t n = p.n_units * (p.family == HYPIC_FAM_DIAG ? p.D : 1);
+    compose_lam_total_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(p);
     return cudaGetLastError();
 }
 

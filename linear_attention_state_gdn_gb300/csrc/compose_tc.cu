@@ -22,6 +22,10 @@
 //   * S_j arrives by TMA into shared memory; the epilogue thread of state column n forms
 //     prefix_j[:, n] = D^T[n, :] + S_j[:, n], stores it (coalesced across the warp) and
 //     writes the next A operand.
+// Transition units: with P_total requested, units U .. 2U-1 of the persistent loop carry
+// the chain Q_j = P_j Q_{j-1} from Q_0 = P_0 (loaded like an S tile) through the same
+// products, without S, without scaling, and write only Q_{n-1} = P_total of unit u - U:
+// the transition of the entry composed from all n segments is exp(sum_j lam_j) Q_{n-1}.
 // Roles: warps 0-3 epilogue (one TMEM lane each), warp 4 TMA producer, warp 5 MMA issuer.
 // Every wait is bounded; on expiry the CTA records HYPIC_ERR_TIMEOUT, lets its in-flight
 // copies and MMAs finish (bounded), frees its TMEM and returns.
@@ -65,7 +69,8 @@ __device__ __forceinline__ void st_stream(float *p, float v) {
 __global__ void __launch_bounds__(kThreads, 1)
 compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                         const __grid_constant__ CUtensorMap tmP,
-                        const __grid_constant__ CUtensorMap tmS) {
+                        const __grid_constant__ CUtensorMap tmS,
+                        const __grid_constant__ CUtensorMap tmQ) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-aligned base, derived by offsetting the shared array itself so that the
     // compiler keeps the shared address space (plain ld/st.shared, not generic accesses)
@@ -76,6 +81,7 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
 
     const int warp = warp_id(), lane = lane_id();
     const int U = (int)p.n_units, NS = p.n_seg;
+    const int UT = p.P_total ? 2 * U : U;   // units, then transition units
     const bool has_s0 = p.S0 != nullptr;
 
     if (threadIdx.x == 0) {
@@ -104,11 +110,14 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
         if (lane == 0) {
             prefetch_tmap(&tmP);
             prefetch_tmap(&tmS);
+            prefetch_tmap(&tmQ);
             uint32_t pc = 0, sc = 0;
-            for (int u = blockIdx.x; u < U && !abort_flag; u += gridDim.x) {
+            for (int ux = blockIdx.x; ux < UT && !abort_flag; ux += gridDim.x) {
+                const bool tr = ux >= U;
+                const int u = tr ? ux - U : ux;
                 for (int j = 0; j < NS; ++j) {
                     const int32_t row = (int32_t)(((int64_t)j * U + u) * D);
-                    if (j > 0 || has_s0) {
+                    if (j > 0 || (has_s0 && !tr)) {
                         const uint32_t st = pc & 1, use = pc >> 1;
                         if (use >= 1 && !mbar_wait_or_abort(&bars.p_empty[st], (use - 1) & 1, p.err,
                                                             kErrTimeout, &abort_flag))
@@ -119,11 +128,12 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                                         32 * b, row);
                         ++pc;
                     }
+                    if (tr && j > 0) continue;   // the transition chain adds no S
                     if (sc >= 1 && !mbar_wait_or_abort(&bars.s_empty, (sc - 1) & 1, p.err,
                                                        kErrTimeout, &abort_flag))
                         goto producer_done;
                     mbar_arrive_expect_tx(&bars.s_full, kTile);
-                    tma_load_2d(smem + kOffS, &tmS, &bars.s_full, 0, row);
+                    tma_load_2d(smem + kOffS, tr ? &tmQ : &tmS, &bars.s_full, 0, row);   // Q_0 = P_0
                     ++sc;
                 }
             }
@@ -139,9 +149,10 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
         if (lane == 0) {
             constexpr uint32_t id = idesc(kFmtTF32, kFmtTF32, false, false, 128, 128);
             uint32_t pc = 0, lb = 0, ac = 0;
-            for (int u = blockIdx.x; u < U && !abort_flag; u += gridDim.x) {
+            for (int ux = blockIdx.x; ux < UT && !abort_flag; ux += gridDim.x) {
+                const bool tr = ux >= U;
                 for (int j = 0; j < NS; ++j) {
-                    if (!(j > 0 || has_s0)) continue;
+                    if (!(j > 0 || (has_s0 && !tr))) continue;
                     const uint32_t st = pc & 1;
                     if (!mbar_wait_or_abort(&bars.a_full, ac & 1, p.err, kErrTimeout, &abort_flag))
                         goto mma_done;
@@ -185,8 +196,10 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
         const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
         uint32_t pc = 0, sc = 0, lb = 0, dc = 0;
         const float *Ssm = reinterpret_cast<const float *>(smem + kOffS);
-        for (int u = blockIdx.x; u < U && !abort_flag; u += gridDim.x) {
-            if (has_s0) {
+        for (int ux = blockIdx.x; ux < UT && !abort_flag; ux += gridDim.x) {
+            const bool tr = ux >= U;
+            const int u = tr ? ux - U : ux;
+            if (has_s0 && !tr) {
                 // A = split(exp(lam_0) S0^T) for the first step
                 const float sc0 = expf(p.lam[u]);
                 const float *s0 = p.S0 + (int64_t)u * D * D + n;
@@ -207,7 +220,7 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                 mbar_arrive(&bars.a_full);
             }
             for (int j = 0; j < NS; ++j) {
-                const bool mma = j > 0 || has_s0;
+                const bool mma = j > 0 || (has_s0 && !tr);
                 if (mma) {
                     const uint32_t st = pc & 1, use = pc >> 1;
                     if (!mbar_wait_or_abort(&bars.p_full[st], use & 1, p.err, kErrTimeout, &abort_flag))
@@ -241,13 +254,18 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                     ++dc;
                     tc_fence_after();
                 }
-                if (!mbar_wait_or_abort(&bars.s_full, sc & 1, p.err, kErrTimeout, &abort_flag))
-                    goto epi_done;
-                ++sc;
+                const bool has_s = !(tr && j > 0);   // S_j (Q_0 = P_0 for the transition chain)
+                if (has_s) {
+                    if (!mbar_wait_or_abort(&bars.s_full, sc & 1, p.err, kErrTimeout, &abort_flag))
+                        goto epi_done;
+                    ++sc;
+                }
                 {
                     const bool next = j + 1 < NS;
-                    const float scale_next = next ? expf(p.lam[(int64_t)(j + 1) * U + u]) : 0.f;
-                    float *out = p.prefix + ((int64_t)j * U + u) * D * D + n;
+                    const float scale_next = !next ? 0.f : tr ? 1.f : expf(p.lam[(int64_t)(j + 1) * U + u]);
+                    // prefix_j, or for the transition chain only its last state, P_total
+                    float *out = tr ? (next ? nullptr : p.P_total + (int64_t)u * D * D + n)
+                                    : p.prefix + ((int64_t)j * U + u) * D * D + n;
                     for (int c = 0; c < 8; ++c) {
                         uint32_t r[16];
                         if (mma) {
@@ -258,8 +276,8 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             const int m = 16 * c + i;
-                            const float v = (mma ? __uint_as_float(r[i]) : 0.f) + Ssm[m * D + n];
-                            st_stream(out + (int64_t)m * D, v);
+                            const float v = (mma ? __uint_as_float(r[i]) : 0.f) + (has_s ? Ssm[m * D + n] : 0.f);
+                            if (out) st_stream(out + (int64_t)m * D, v);
                             const float x = v * scale_next;
                             const float h = tf32_trunc(x);
                             hi[i] = __float_as_uint(h);
@@ -270,7 +288,7 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                             tmem_st16(tA_lo + lane_off + 16 * c, lo);
                         }
                     }
-                    mbar_arrive(&bars.s_empty);
+                    if (has_s) mbar_arrive(&bars.s_empty);
                     if (next) {
                         tmem_st_wait();
                         tc_fence_before();
@@ -306,19 +324,22 @@ bool compose_dense_tc_supported(const ComposeParams &p) {
 cudaError_t launch_compose_dense_tc(const ComposeParams &p, cudaStream_t s) {
     if (p.n_seg == 0 || p.n_units == 0) return cudaSuccess;
     const uint64_t rows = (uint64_t)p.n_seg * p.n_units * D;
-    CUtensorMap tmP, tmS;
+    CUtensorMap tmP, tmS, tmQ;
     // P is only read for steps with a carried state; any valid base serves otherwise
     const float *pbase = p.P ? p.P : p.S;
     if (!make_tmap_2d(&tmP, pbase, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, rows, D * 4, 32, 128,
                       CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_2d(&tmS, p.S, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, rows, D * 4, 128, 128,
-                      CU_TENSOR_MAP_SWIZZLE_NONE))
+                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tmap_2d(&tmQ, pbase, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, rows, D * 4, 128, 128,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))   // P_0 read whole, like an S tile
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(compose_dense_tc_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int grid = (int)std::min<int64_t>(p.n_units, sm_count());
-    compose_dense_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, tmP, tmS);
+    const int64_t units = p.n_units * (p.P_total ? 2 : 1);
+    const int grid = (int)std::min<int64_t>(units, sm_count());
+    compose_dense_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, tmP, tmS, tmQ);
     return cudaGetLastError();
 }
 

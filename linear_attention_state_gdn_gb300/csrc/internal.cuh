@@ -65,6 +65,8 @@ struct ComposeParams {
     const float *P;
     const float *S0;
     float *prefix;
+    float *lam_total;   // optional: sum_j lam_j per unit (per key row for DIAG)
+    float *P_total;     // optional, dense families: P_{n-1} ... P_0 per unit
     unsigned *err;
 };
 
@@ -72,6 +74,7 @@ struct ComposeParams {
 cudaError_t launch_build_gated_simt(const BuildParams &p, cudaStream_t s);
 cudaError_t launch_build_delta_seq(const BuildParams &p, cudaStream_t s);
 cudaError_t launch_compose_scaled(const ComposeParams &p, cudaStream_t s);
+cudaError_t launch_compose_lam_total(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_dense_simt(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_dense_tc(const ComposeParams &p, cudaStream_t s);
 bool compose_dense_tc_supported(const ComposeParams &p);

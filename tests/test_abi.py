@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.hypic_abi_version() == 1
+    assert lib.hypic_abi_version() == 2
     assert lib.hypic_status_string(0) == b"ok"
     assert lib.hypic_status_string(2) == b"misaligned tensor pointer"
     assert lib.hypic_status_string(99) == b"unknown status"
@@ -174,6 +174,19 @@ def test_compose_rejects_misaligned(lib):
     a = good_compose()
     a.prefix = a.prefix + 4
     assert lib.hypic_compose_scan(ctypes.byref(a), None) == 2
+
+
+@pytest.mark.parametrize("field,offset", [("P_total", 4), ("lam_total", 2)])
+def test_compose_rejects_misaligned_totals(lib, field, offset):
+    a = good_compose()
+    setattr(a, field, FAKE + 0x4000000 + offset)
+    assert lib.hypic_compose_scan(ctypes.byref(a), None) == 2
+
+
+def test_compose_args_layout():
+    # int32 family, n_seg; int64 n_units; int32 d_k, d_v; seven pointers
+    assert ctypes.sizeof(ComposeArgs) == 80
+    assert ComposeArgs.lam_total.offset == 64 and ComposeArgs.P_total.offset == 72
 
 
 def test_compose_empty_is_a_noop(lib):

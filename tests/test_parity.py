@@ -120,6 +120,69 @@ def test_compose_single_segment_is_S_plus_carry():
     assert torch.equal(pref.cpu(), c.S)     # zero initial state: prefix_0 = S_0 exactly
 
 
+# ------------------------------------------------------------------ composed entries
+
+def compose_with_totals(family, S, lam, P, S0=None):
+    hy = _hy()
+    U, d = S.shape[1], S.shape[2]
+    lam_t = torch.empty((U, d) if family == "diag" else (U,), dtype=torch.float32, device=S.device)
+    P_t = torch.empty((U, d, d), dtype=torch.float32, device=S.device) if P is not None else None
+    pref = hy.hypic_compose_scan(family, S, lam, P, S0, lam_total=lam_t, P_total=P_t)
+    torch.cuda.synchronize()
+    assert hy.hypic_get_device_status() == 0
+    return pref, lam_t, P_t
+
+
+@pytest.mark.parametrize("family", FAMILIES)
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("with_S0", [False, True])
+def test_compose_totals_parity(family, d, with_S0):
+    """lam_total = sum_j lam_j and P_total = P_{n-1} ... P_0 next to the prefix scan, whose
+    output must not change when the totals are requested."""
+    c = synth.make_compose_inputs(family, 9, 5, d, seed=150 + d, with_S0=with_S0)
+    dev = lambda t: None if t is None else t.cuda()
+    pref, lam_t, P_t = compose_with_totals(family, dev(c.S), dev(c.lam), dev(c.P), dev(c.S0))
+    T = oracle.materialize_T(family, f64(c.lam), f64(c.P), d_k=d)
+    assert_close(f64(pref), oracle.compose_scan(T, f64(c.S), f64(c.S0)), COMPOSE_TOL, "prefix")
+    lam_o, P_o = oracle.compose_transitions(family, f64(c.lam), f64(c.P), d_k=d)
+    np.testing.assert_allclose(f64(lam_t), lam_o, rtol=1e-5, atol=1e-6)
+    if P_o is not None:
+        assert_close(f64(P_t)[None], P_o[None], COMPOSE_TOL, "P_total")
+
+
+@pytest.mark.parametrize("family", FAMILIES)
+def test_composed_entry_is_the_entry_of_the_concatenation(family):
+    """Segments built on the GPU, composed into one entry (prefix[n-1], lam_total, P_total),
+    against the oracle's entry of the same tokens built as one segment (O(1) transitions,
+    so that T is compared at its own scale)."""
+    inp = synth.make_inputs(family, 2, 4, 128, RAGGED, torch.bfloat16, seed=61, gla_div=64.0,
+                            alpha_scale=0.002, beta_shift=-2.0)
+    S, lam, P = gpu_build(inp)
+    pref, lam_t, P_t = compose_with_totals(family, S, lam, P)
+    N = int(inp.seg_offsets[-1])
+    S_w, T_w = oracle.build_segments(family, [0, N], f64(inp.k), f64(inp.v), f64(inp.log_gate),
+                                     f64(inp.log_gamma), f64(inp.beta))
+    tol = TOL[inp.dtype]
+    assert_close(f64(pref[-1])[None], S_w, tol, "S of the concatenation")
+    assert_close(gpu_T(family, lam_t[None], None if P_t is None else P_t[None], 128), T_w, tol,
+                 "T of the concatenation")
+
+
+def test_compose_totals_are_validated():
+    hy = _hy()
+    c = synth.make_compose_inputs("scalar", 3, 2, 64, seed=152)
+    S, lam = c.S.cuda(), c.lam.cuda()
+    with pytest.raises(hy.HypicError):     # P_total exists for dense transitions only
+        hy.hypic_compose_scan("scalar", S, lam, P_total=torch.empty(2, 64, 64, device="cuda"))
+    g = synth.make_compose_inputs("gdn", 3, 2, 64, seed=153)
+    S, lam, P = g.S.cuda(), g.lam.cuda(), g.P.cuda()
+    prefix = torch.empty_like(S)
+    with pytest.raises(hy.HypicError):     # a total may not overlap prefix
+        hy.hypic_compose_scan("gdn", S, lam, P, prefix=prefix, P_total=prefix[0])
+    with pytest.raises(hy.HypicError):     # nor an input
+        hy.hypic_compose_scan("gdn", S, lam, P, lam_total=lam[0])
+
+
 # ------------------------------------------------------------------ build -> compose chain
 
 @pytest.mark.parametrize("family", FAMILIES)
@@ -230,6 +293,20 @@ def test_workload_gdn_compose_full_size_compose_only():
     T = oracle.materialize_T("gdn", f64(c.lam[:, units]), f64(c.P[:, units]))
     ref = oracle.compose_scan(T, f64(c.S[:, units]))
     assert_close(f64(pref[:, units]), ref, COMPOSE_TOL, "prefix")
+
+
+def test_workload_gdn_compose_full_size_with_totals():
+    """The composed-entry launch the benchmark times (64 segments x 1536 units, with
+    lam_total and P_total) on fp32 cached entries drawn directly: 1e-4 on sampled units."""
+    c = synth.make_compose_inputs("gdn", 64, 1536, 128, seed=81)
+    pref, lam_t, P_t = compose_with_totals("gdn", c.S.cuda(), c.lam.cuda(), c.P.cuda())
+    rng = np.random.default_rng(7)
+    units = sorted(rng.choice(1536, size=6, replace=False))
+    T = oracle.materialize_T("gdn", f64(c.lam[:, units]), f64(c.P[:, units]))
+    assert_close(f64(pref[:, units]), oracle.compose_scan(T, f64(c.S[:, units])), COMPOSE_TOL, "prefix")
+    lam_o, P_o = oracle.compose_transitions("gdn", f64(c.lam[:, units]), f64(c.P[:, units]))
+    np.testing.assert_allclose(f64(lam_t[units]), lam_o, rtol=1e-5, atol=1e-5)
+    assert_close(f64(P_t[units])[None], P_o[None], COMPOSE_TOL, "P_total")
 
 
 # ------------------------------------------------------------------ kernel selection
