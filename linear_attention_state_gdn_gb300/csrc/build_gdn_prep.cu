@@ -26,13 +26,18 @@
 // before it reads any record.
 //   1. TMA the chunk's k (two 128B-swizzled 64-channel halves); b masked past the segment end.
 //   2. One thread issues the gram K K^T (M = 64 tcgen05 MMA, fp32 accumulator in TMEM).
-//   3. A = Diag(b) L in fp32 shared memory (rows padded to 68 floats).
+//   3. The raw gram G = K K^T in shared memory (rows padded to 68 floats): the blocks left of
+//      the diagonal rounded to tf32 once (they are only ever MMA operands), the diagonal
+//      blocks exact (forward substitution); the blocks right of the diagonal are not stored.
+//      A = Diag(b) L is never formed: b scales rows inside the consumers, and the strictly
+//      lower mask is the consumers' index range.
 //   4. N by 16 x 16 blocks: the four diagonal blocks by forward substitution (one warp each),
-//      then the blocks below level by level, N_ab = -N_aa sum_{k=b}^{a-1} A_ak N_kb, as
-//      16 x 8 half-blocks spread over the four warps. The 16 x 16 x 16 products run on the
-//      warp-level tensor-core MMA (m16n8k8, tf32 inputs, fp32 accumulation): tcgen05's
-//      smallest tile (M = 64) would waste most of its work on products this small and
-//      each would need a round trip through TMEM.
+//      then the blocks below level by level, N_ab = -N_aa Diag(b_a) sum_{k=b}^{a-1} G_ak N_kb,
+//      as 16 x 8 half-blocks spread over the four warps. The 16 x 16 x 16 products run on
+//      the warp-level tensor-core MMA (m16n8k8, tf32 inputs, fp32 accumulation): tcgen05's
+//      smallest tile (M = 64) would waste most of its work on products this small and each
+//      would need a round trip through TMEM. Every MMA operand in shared memory is stored
+//      already rounded to tf32, so the fragments are loaded without conversions.
 //   5. Columns scaled by b_t, rounded to bf16, stored (16-byte coalesced stores).
 // Tokens past the segment end have b = 0, so their rows and columns of M2 are zero.
 #include <algorithm>
@@ -51,8 +56,8 @@ constexpr int C = kGdnChunk;
 constexpr int kThreads = 128;
 constexpr uint32_t kLDA = 68;                            // padded fp32 row stride
 constexpr uint32_t kOffK = 0;                            // k tile, 16 KB
-constexpr uint32_t kOffA32 = 16384;                      // fp32 Diag(b) L, 64 x 68
-constexpr uint32_t kOffN32 = kOffA32 + 64 * kLDA * 4;    // fp32 N, 64 x 68
+constexpr uint32_t kOffG32 = 16384;                      // the gram K K^T, 64 x 68
+constexpr uint32_t kOffN32 = kOffG32 + 64 * kLDA * 4;    // N (tf32-rounded), 64 x 68
 constexpr uint32_t kLDT = 12;                            // per-warp 16 x 8 scratch, padded rows
 constexpr uint32_t kOffT = kOffN32 + 64 * kLDA * 4;      // 4 warps x 16 x 12 fp32
 constexpr uint32_t kSmemBytes = kOffT + 4 * 16 * kLDT * 4 + 1024;
@@ -65,19 +70,22 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
     return r;
 }
 
+// x rounded to tf32 (round to nearest), kept as a float with the low 13 mantissa bits zero
+__device__ __forceinline__ float tf32r(float x) { return __uint_as_float(to_tf32(x)); }
+
 // c (16 x 8, m16n8 accumulator layout) += X[xr.., xc..] (16 x 16) * Y[yr.., yc..] (16 x 8);
-// X and Y row-major fp32 in shared memory with row strides ldx, ldy.
+// X and Y row-major in shared memory with row strides ldx, ldy, holding tf32-rounded values.
 __device__ __forceinline__ void mma16x8x16(float (&c)[4], const float *X, int ldx, const float *Y, int ldy,
                                            int lane) {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-        const uint32_t a0 = to_tf32(X[g * ldx + 8 * ks + t]);
-        const uint32_t a1 = to_tf32(X[(g + 8) * ldx + 8 * ks + t]);
-        const uint32_t a2 = to_tf32(X[g * ldx + 8 * ks + t + 4]);
-        const uint32_t a3 = to_tf32(X[(g + 8) * ldx + 8 * ks + t + 4]);
-        const uint32_t b0 = to_tf32(Y[(8 * ks + t) * ldy + g]);
-        const uint32_t b1 = to_tf32(Y[(8 * ks + t + 4) * ldy + g]);
+        const uint32_t a0 = __float_as_uint(X[g * ldx + 8 * ks + t]);
+        const uint32_t a1 = __float_as_uint(X[(g + 8) * ldx + 8 * ks + t]);
+        const uint32_t a2 = __float_as_uint(X[g * ldx + 8 * ks + t + 4]);
+        const uint32_t a3 = __float_as_uint(X[(g + 8) * ldx + 8 * ks + t + 4]);
+        const uint32_t b0 = __float_as_uint(Y[(8 * ks + t) * ldy + g]);
+        const uint32_t b1 = __float_as_uint(Y[(8 * ks + t + 4) * ldy + g]);
         asm volatile(
             "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
             "{%0,%1,%2,%3};"
@@ -87,25 +95,27 @@ __device__ __forceinline__ void mma16x8x16(float (&c)[4], const float *X, int ld
 }
 
 // Half-block (a, b, hh) of N: columns 16 b + 8 hh .. + 7 of block row a, from the blocks of
-// N already computed: T = sum_{k=b}^{a-1} A_ak N_kb[:, half], N_ab[:, half] = -N_aa T.
-__device__ __forceinline__ void half_block(const float *A32, float *N32, float *Tw, int a, int b, int hh,
-                                           int lane) {
+// N already computed: T = Diag(b_a) sum_{k=b}^{a-1} G_ak N_kb[:, half], N_ab[:, half] =
+// -N_aa T (bv: the chunk's b).
+__device__ __forceinline__ void half_block(const float *G32, float *N32, float *Tw, const float *bv, int a,
+                                           int b, int hh, int lane) {
     const int g = lane >> 2, t = lane & 3;
     float c[4] = {0.f, 0.f, 0.f, 0.f};
     for (int k = b; k < a; ++k)
-        mma16x8x16(c, A32 + 16 * a * kLDA + 16 * k, kLDA, N32 + 16 * k * kLDA + 16 * b + 8 * hh, kLDA, lane);
-    Tw[g * kLDT + 2 * t] = c[0];
-    Tw[g * kLDT + 2 * t + 1] = c[1];
-    Tw[(g + 8) * kLDT + 2 * t] = c[2];
-    Tw[(g + 8) * kLDT + 2 * t + 1] = c[3];
+        mma16x8x16(c, G32 + 16 * a * kLDA + 16 * k, kLDA, N32 + 16 * k * kLDA + 16 * b + 8 * hh, kLDA, lane);
+    const float b0 = bv[16 * a + g], b1 = bv[16 * a + g + 8];
+    Tw[g * kLDT + 2 * t] = tf32r(c[0] * b0);
+    Tw[g * kLDT + 2 * t + 1] = tf32r(c[1] * b0);
+    Tw[(g + 8) * kLDT + 2 * t] = tf32r(c[2] * b1);
+    Tw[(g + 8) * kLDT + 2 * t + 1] = tf32r(c[3] * b1);
     __syncwarp();
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     mma16x8x16(d, N32 + 16 * a * kLDA + 16 * a, kLDA, Tw, kLDT, lane);
     float *o = N32 + 16 * a * kLDA + 16 * b + 8 * hh;
-    o[g * kLDA + 2 * t] = -d[0];
-    o[g * kLDA + 2 * t + 1] = -d[1];
-    o[(g + 8) * kLDA + 2 * t] = -d[2];
-    o[(g + 8) * kLDA + 2 * t + 1] = -d[3];
+    o[g * kLDA + 2 * t] = tf32r(-d[0]);
+    o[g * kLDA + 2 * t + 1] = tf32r(-d[1]);
+    o[(g + 8) * kLDA + 2 * t] = tf32r(-d[2]);
+    o[(g + 8) * kLDA + 2 * t + 1] = tf32r(-d[3]);
     __syncwarp();   // Tw is reused by this warp's next half-block
 }
 
@@ -154,7 +164,7 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     Walk cur = decode(p, blockIdx.x, total);
     if (cur.r >= p.n_seg) return;   // uniform: the whole CTA leaves before any set-up
     const int q = threadIdx.x, warp = q >> 5, lane = q & 31;
-    float *A32 = reinterpret_cast<float *>(smem + kOffA32);
+    float *G32 = reinterpret_cast<float *>(smem + kOffG32);
     float *N32 = reinterpret_cast<float *>(smem + kOffN32);
     float *Tw = reinterpret_cast<float *>(smem + kOffT) + warp * 16 * kLDT;
 
@@ -229,7 +239,9 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         __syncthreads();
         if (!s_ok) break;   // uniform
         tc_fence_after();
-        {   // gram rows t = 16 warp + lane (lanes < 16, M = 64 accumulator layout) -> A rows
+        {   // gram rows t = 16 warp + lane (lanes < 16, M = 64 accumulator layout): row t lies
+            // in block row `warp`; its blocks left of the diagonal are stored tf32-rounded, its
+            // diagonal block exact, the rest not at all
             uint32_t gr[64];
             const uint32_t taddr = tmem + 64 * b + ((uint32_t)(32 * warp) << 16);
             tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&gr[0]));
@@ -237,52 +249,50 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
             tmem_ld_wait();
             if (lane < 16) {
                 const int t = 16 * warp + lane;
-                const float bt = vb[b][t];
-                float4 *row = reinterpret_cast<float4 *>(A32 + t * kLDA);
+                float4 *row = reinterpret_cast<float4 *>(G32 + t * kLDA);
 #pragma unroll
                 for (int s4 = 0; s4 < C / 4; ++s4) {
-                    const int s = 4 * s4;
-                    float4 a4;
-                    a4.x = s + 0 < t ? bt * __uint_as_float(gr[s + 0]) : 0.f;
-                    a4.y = s + 1 < t ? bt * __uint_as_float(gr[s + 1]) : 0.f;
-                    a4.z = s + 2 < t ? bt * __uint_as_float(gr[s + 2]) : 0.f;
-                    a4.w = s + 3 < t ? bt * __uint_as_float(gr[s + 3]) : 0.f;
-                    row[s4] = a4;
+                    if (s4 >= 4 * (warp + 1)) break;   // uniform
+                    float4 g4 = make_float4(__uint_as_float(gr[4 * s4]), __uint_as_float(gr[4 * s4 + 1]),
+                                            __uint_as_float(gr[4 * s4 + 2]), __uint_as_float(gr[4 * s4 + 3]));
+                    if (s4 < 4 * warp) g4 = make_float4(tf32r(g4.x), tf32r(g4.y), tf32r(g4.z), tf32r(g4.w));
+                    row[s4] = g4;
                 }
             }
         }
         tc_fence_before();
         __syncthreads();
-        // diagonal block `warp`: lane j < 16 solves column j by forward substitution
+        // diagonal block `warp`: lane j < 16 solves column j by forward substitution,
+        // x_r = [r == j] - b_r sum_{s<r} G_rs x_s (A = Diag(b) L restricted to the block)
         if (lane < 16) {
             const int a = warp, j = lane;
             float x[16];
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
-                const float4 *Ar = reinterpret_cast<const float4 *>(A32 + (16 * a + rr) * kLDA + 16 * a);
-                float ar[16];
+                const float4 *Gr = reinterpret_cast<const float4 *>(G32 + (16 * a + rr) * kLDA + 16 * a);
+                float gr[16];
 #pragma unroll
                 for (int s4 = 0; s4 < 4; ++s4) {
-                    const float4 t4 = Ar[s4];
-                    ar[4 * s4] = t4.x, ar[4 * s4 + 1] = t4.y, ar[4 * s4 + 2] = t4.z, ar[4 * s4 + 3] = t4.w;
+                    const float4 t4 = Gr[s4];
+                    gr[4 * s4] = t4.x, gr[4 * s4 + 1] = t4.y, gr[4 * s4 + 2] = t4.z, gr[4 * s4 + 3] = t4.w;
                 }
-                float acc[4] = {(rr == j) ? 1.f : 0.f, 0.f, 0.f, 0.f};
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int s = 0; s < rr; ++s) acc[s & 3] = fmaf(-ar[s], x[s], acc[s & 3]);
-                x[rr] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                for (int s = 0; s < rr; ++s) acc[s & 3] = fmaf(gr[s], x[s], acc[s & 3]);
+                x[rr] = fmaf(-vb[b][16 * a + rr], (acc[0] + acc[1]) + (acc[2] + acc[3]), (rr == j) ? 1.f : 0.f);
             }
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) N32[(16 * a + rr) * kLDA + 16 * a + j] = x[rr];
+            for (int rr = 0; rr < 16; ++rr) N32[(16 * a + rr) * kLDA + 16 * a + j] = tf32r(x[rr]);
         }
         __syncthreads();
         // level 1: (1,0), (2,1), (3,2) as six half-blocks; level 2: (2,0), (3,1); level 3: (3,0).
         // Warps 0-1 take one half-block per level, warps 2-3 two in level 1 and none in level 3.
-        half_block(A32, N32, Tw, 1 + (warp >> 1), warp >> 1, warp & 1, lane);
-        if (warp >= 2) half_block(A32, N32, Tw, 3, 2, warp & 1, lane);
+        half_block(G32, N32, Tw, vb[b], 1 + (warp >> 1), warp >> 1, warp & 1, lane);
+        if (warp >= 2) half_block(G32, N32, Tw, vb[b], 3, 2, warp & 1, lane);
         __syncthreads();
-        half_block(A32, N32, Tw, 2 + (warp >> 1), warp >> 1, warp & 1, lane);
+        half_block(G32, N32, Tw, vb[b], 2 + (warp >> 1), warp >> 1, warp & 1, lane);
         __syncthreads();
-        if (warp < 2) half_block(A32, N32, Tw, 3, 0, warp, lane);
+        if (warp < 2) half_block(G32, N32, Tw, vb[b], 3, 0, warp, lane);
         // warps 2-3 have no level-3 work: the next record's gram (its k tile was requested at
         // the top of this iteration) into the other TMEM buffer, last read a record ago
         // and the ticket of the record after it
