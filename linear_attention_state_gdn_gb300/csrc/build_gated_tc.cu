@@ -131,7 +131,7 @@ build_gated_tc_kernel(const __grid_constant__ BuildParams p, const __grid_consta
             int c = 0;
             for (; c < nchunks; ++c) {
                 const int s = c % kStages, use = c / kStages;
-                if (use >= 1 && !mbar_wait_or_abort(&bars.empty[s], (use - 1) & 1, p.err, kErrTimeout,
+                if (use >= 1 && !mbar_wait_or_abort_compact(&bars.empty[s], (use - 1) & 1, p.err, kErrTimeout,
                                                     &abort_flag))
                     break;
                 uint8_t *st = smem + s * G::kStage;
@@ -152,9 +152,9 @@ build_gated_tc_kernel(const __grid_constant__ BuildParams p, const __grid_consta
             constexpr uint32_t id = idesc(kFmtBF16, kFmtBF16, true, true, 128, 128);
             for (int c = 0; c < nchunks; ++c) {
                 const int s = c % kStages, use = c / kStages, b = c & 1, buse = c >> 1;
-                if (!mbar_wait_or_abort(&bars.kready[s], use & 1, p.err, kErrTimeout, &abort_flag))
+                if (!mbar_wait_or_abort_compact(&bars.kready[s], use & 1, p.err, kErrTimeout, &abort_flag))
                     break;
-                if (buse >= 1 && !mbar_wait_or_abort(&bars.dfree[b], (buse - 1) & 1, p.err,
+                if (buse >= 1 && !mbar_wait_or_abort_compact(&bars.dfree[b], (buse - 1) & 1, p.err,
                                                      kErrTimeout, &abort_flag))
                     break;
                 tc_fence_after();
@@ -187,7 +187,7 @@ build_gated_tc_kernel(const __grid_constant__ BuildParams p, const __grid_consta
 
         auto decay = [&](int c) -> bool {
             const int s = c % kStages;
-            if (!bar_state_and(mbar_wait_or_abort(&bars.full[s], (c / kStages) & 1, p.err, kErrTimeout,
+            if (!bar_state_and(mbar_wait_or_abort_compact(&bars.full[s], (c / kStages) & 1, p.err, kErrTimeout,
                                                   &abort_flag)))
                 return false;
             uint8_t *kt = smem + s * G::kStage;
@@ -273,7 +273,7 @@ build_gated_tc_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         };
         auto fold = [&](int c) -> bool {
             const int b = c & 1;
-            if (!bar_state_and(mbar_wait_or_abort(&bars.dfull[b], (c >> 1) & 1, p.err, kErrTimeout,
+            if (!bar_state_and(mbar_wait_or_abort_compact(&bars.dfull[b], (c >> 1) & 1, p.err, kErrTimeout,
                                                   &abort_flag)))
                 return false;
             tc_fence_after();

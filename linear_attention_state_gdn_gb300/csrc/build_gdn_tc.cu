@@ -192,7 +192,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = tslot;
     auto wait = [&](uint64_t *b, uint32_t par) {
-        return mbar_wait_or_abort(b, par, p.err, kErrTimeout, &abort_flag);
+        return mbar_wait_or_abort_compact(b, par, p.err, kErrTimeout, &abort_flag);
     };
     // every lane waits; the warp leaves with one outcome (tcgen05.ld / st are warp-wide)
     auto wwait = [&](uint64_t *b, uint32_t par) { return __all_sync(0xffffffffu, wait(b, par)) != 0; };

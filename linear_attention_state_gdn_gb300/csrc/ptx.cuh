@@ -138,6 +138,31 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parit
     }
 }
 
+// The same bounded wait with suspending probes, for kernels whose many wait sites compete
+// for the instruction cache: a suspending probe almost always ends the wait, so only that
+// probe is inlined and the clock and abort bookkeeping after it is one out-of-line function
+// per translation unit. Measured on GB300: the GDN chain and the gated builds run faster with
+// it, the dense compose slower (it keeps mbar_wait_or_abort).
+static __device__ __noinline__ bool mbar_wait_or_abort_slow(uint32_t a, uint32_t parity, unsigned *err,
+                                                            unsigned bit, volatile int *abort_flag) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(a, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > 2000000000ull) {
+            if (err) atomicOr(err, bit);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool mbar_wait_or_abort_compact(uint64_t *bar, uint32_t parity, unsigned *err,
+                                                           unsigned bit, volatile int *abort_flag) {
+    const uint32_t a = smem_u32(bar);
+    return mbar_try_wait(a, parity) || mbar_wait_or_abort_slow(a, parity, err, bit, abort_flag);
+}
+
 // ------------------------------------------------------------------------------ TMA
 
 // 2D / 3D tiled tensor loads into shared memory, completing on an mbarrier.

@@ -44,6 +44,17 @@ def test_build_parity_ragged(family, dtype, d):
     check_build(inp)
 
 
+@pytest.mark.parametrize("family", ["gdn", "delta"])
+def test_build_more_units_than_sms(family):
+    """More (segment, head) units than SMs, in several rounds per SM: 180 ragged segments
+    (empty, one-token, one-chunk and multi-chunk) x 2 value heads through the tensor-core
+    build, whose records of many short units interleave in the workspace."""
+    lens = [int(x) for x in np.random.default_rng(44).integers(0, 200, size=180)]
+    lens[:6] = [0, 1, 64, 65, 0, 130]
+    inp = synth.make_inputs(family, 1, 2, 128, lens, torch.bfloat16, seed=45, alpha_scale=0.05)
+    check_build(inp)
+
+
 def test_build_scalar_per_token_gate():
     inp = synth.make_inputs("scalar", 2, 2, 128, [300, 77], torch.bfloat16, seed=41,
                             per_token_scalar=True)
