@@ -9,9 +9,10 @@ second launch. `value` is build+compose tokens/s of that step with the inputs re
 device memory; `e2e` is the same metric through the public API with the inputs copied in
 from pinned host memory and every output copied back, inside the timed region.
 
-The other workloads (RetNet scalar build + compose, GLA diagonal build + compose, the
-48-layer x 64-segment GDN compose) are measured after the main timed region and reported
-under "sections". `--impl reference` times the fp64 CPU oracle instead (a bounded sample
+The other workloads (RetNet scalar build + compose, GLA diagonal build + compose, the same
+GDN prompt cached as one 32768-token segment, the 48-layer x 64-segment GDN compose with and
+without the composed entry) are measured after the main timed region and reported under
+"sections". `--impl reference` times the fp64 CPU oracle instead (a bounded sample
 of the same workload per step, on the host cores).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hypic|reference]
@@ -309,7 +310,11 @@ def section_family(name, flush, peak, steps=20, warmup=3):
     c_bytes = compose_algorithmic_bytes(inp.n_seg, inp.H_v, d, dense, inp.family == "diag")
     bk, ck = st.kernel_names()
     b_gbs, c_gbs = b_bytes / b_ms / 1e6, c_bytes / c_ms / 1e6
-    return {"build_kernel": bk, "build_ms": round(b_ms, 4),
+    extra = {}
+    if dense:   # tensor-bound: the chunked-form flops against the measured bf16 peak
+        tf = GDN_FLOP_PER_TOKEN_HEAD * n_tok * inp.H_v / (b_ms * 1e-3) / 1e12
+        extra = {"build_tflops": round(tf, 1), "build_tensor_frac": round(tf / peak["bf16_tflops"], 4)}
+    return {"build_kernel": bk, "build_ms": round(b_ms, 4), **extra,
             "build_tokens_per_s": round(n_tok / b_ms * 1e3, 1),
             "build_gbs": round(b_gbs, 1), "build_hbm_frac": round(b_gbs / peak["hbm_gbs"], 4),
             "build_bytes": b_bytes, "compose_kernel": ck, "compose_ms": round(c_ms, 4),
@@ -574,7 +579,7 @@ def run_main(args):
         del st
         torch.cuda.empty_cache()
         sections = {}
-        for name in ("retnet", "gla"):
+        for name in ("retnet", "gla", "gdn_one_segment"):
             sections[name] = section_family(name, flush, pk)
         sections["gdn_compose"] = section_gdn_compose(flush, pk, layers=args.compose_layers)
         line["sections"] = sections
@@ -615,7 +620,7 @@ def main(argv=None):
     ap.add_argument("--quick", action="store_true",
                     help="main timed region only (no e2e, sections or CPU baseline)")
     ap.add_argument("--compose-layers", type=int, default=48)
-    ap.add_argument("--only", choices=["gdn", "retnet", "gla", "gdn_tiny", "gdn_compose"],
+    ap.add_argument("--only", choices=["gdn", "retnet", "gla", "gdn_tiny", "gdn_compose", "gdn_one_segment"],
                     help="time one workload's launches alone (profiling helper; no contract line)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps

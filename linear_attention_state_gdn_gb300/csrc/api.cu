@@ -121,6 +121,68 @@ int64_t gdn_records(const hypic_build_args *a) {
     return records;
 }
 
+// Intra-segment split of the DeltaNet / GDN tensor-core build. Each (segment, value head)
+// unit is one serial chain of 64-token chunks, so a call with few units (one long prompt as a
+// single segment) leaves most SMs idle. When the units fill at most half of the SMs, every
+// segment is cut into up to kMaxPieces chunk-aligned pieces that build in parallel as
+// segments of their own; the pieces of a segment are then composed back into its entry, the
+// composition the pages state for consecutive cached segments ("Cut First-Token Latency by
+// 3.25x ..." (besthub.dev), paragraph "For linear layers": T_C2 S(C1) + S(C2), transition
+// T_C2 T_C1) applied inside one segment. The decision depends on the current device's SM
+// count; without a device there is no split.
+constexpr int kMaxPieces = 8;
+
+int gdn_split_m(const hypic_build_args *a) {
+    const int64_t units = (int64_t)a->n_seg * a->H_v;
+    if (units == 0) return 1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 1;
+    }
+    if (2 * units > sms) return 1;
+    return (int)std::min<int64_t>(kMaxPieces, sms / units);
+}
+
+// pieces of one segment of `len` tokens (1: built whole)
+int seg_pieces(int64_t len, int m) {
+    const int64_t nch = len > 0 ? (len + kGdnChunk - 1) / kGdnChunk : 0;
+    return (int)std::max<int64_t>(1, std::min<int64_t>(m, nch));
+}
+
+// Workspace of the split: piece outputs S, P [slots][H_v][d][d], lam [slots][H_v] (rounded to
+// 256 bytes), and one scan buffer [max pieces][H_v][d][d] for the composition.
+struct SplitLayout {
+    int m = 1, slots = 0, max_pieces = 1;
+    size_t off_S = 0, off_P = 0, off_lam = 0, off_prefix = 0, bytes = 0;
+};
+
+SplitLayout gdn_split_layout(const hypic_build_args *a, size_t base) {
+    SplitLayout L;
+    L.m = gdn_split_m(a);
+    if (L.m <= 1) return L;
+    for (int j = 0; j < a->n_seg; ++j) {
+        const int pj = seg_pieces(a->seg_offsets[j + 1] - a->seg_offsets[j], L.m);
+        if (pj > 1) {
+            L.slots += pj;
+            L.max_pieces = std::max(L.max_pieces, pj);
+        }
+    }
+    if (L.slots == 0) {
+        L.m = 1;
+        return L;
+    }
+    const size_t unit = (size_t)a->d_k * a->d_k * sizeof(float);
+    const size_t su = (size_t)L.slots * a->H_v;
+    L.off_S = base;
+    L.off_P = L.off_S + su * unit;
+    L.off_lam = L.off_P + su * unit;
+    L.off_prefix = L.off_lam + ((su * sizeof(float) + 255) & ~(size_t)255);
+    L.bytes = L.off_prefix + (size_t)L.max_pieces * a->H_v * unit - base;
+    return L;
+}
+
 bool build_shape_ok(const hypic_build_args *a) {
     return a && a->family >= HYPIC_FAM_LINEAR && a->family <= HYPIC_FAM_GDN &&
            (a->dtype == HYPIC_BF16 || a->dtype == HYPIC_F32) && a->n_seg >= 0 &&
@@ -156,7 +218,9 @@ size_t hypic_build_workspace_bytes(const hypic_build_args *a) {
     if (!build_shape_ok(a) || a->n_seg == 0 || !a->seg_offsets) return 0;
     if (pick_build(a) != BuildPath::GdnTc) return 0;
     const int64_t records = gdn_records(a);
-    return records > 0 ? (size_t)records * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail : 0;
+    if (records == 0) return 0;
+    const size_t base = (size_t)records * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail;
+    return base + gdn_split_layout(a, base).bytes;
 }
 
 hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
@@ -244,17 +308,43 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
     p.P = a->P;
     p.workspace = a->workspace;
     p.err = err;
-    std::vector<int> order(a->n_seg);
-    for (int j = 0; j < a->n_seg; ++j) order[j] = j;
-    std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
-        return a->seg_offsets[x + 1] - a->seg_offsets[x] > a->seg_offsets[y + 1] - a->seg_offsets[y];
-    });
+    // the launch table: whole segments, or the chunk-aligned pieces of split ones (piece k of
+    // a segment with n chunks in pj pieces covers chunks [k n / pj, (k + 1) n / pj))
+    SplitLayout split;
+    if (path == BuildPath::GdnTc) {
+        const size_t base = (size_t)gdn_records(a) * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail;
+        split = gdn_split_layout(a, base);
+        if (split.m > 1) {
+            uint8_t *ws = static_cast<uint8_t *>(a->workspace);
+            p.S_piece = reinterpret_cast<float *>(ws + split.off_S);
+            p.P_piece = reinterpret_cast<float *>(ws + split.off_P);
+            p.lam_piece = reinterpret_cast<float *>(ws + split.off_lam);
+        }
+    }
+    std::vector<SegEntry> table;
+    table.reserve(a->n_seg);
+    int32_t slot = 0;
+    for (int j = 0; j < a->n_seg; ++j) {
+        const int64_t st = a->seg_offsets[j], len = a->seg_offsets[j + 1] - st;
+        const int pj = split.m > 1 ? seg_pieces(len, split.m) : 1;
+        if (pj == 1) {
+            table.push_back(SegEntry{(int32_t)st, (int32_t)len, j, 0});
+            continue;
+        }
+        const int64_t nch = (len + kGdnChunk - 1) / kGdnChunk;
+        for (int k = 0; k < pj; ++k) {
+            const int64_t t0 = (k * nch / pj) * kGdnChunk;
+            const int64_t t1 = std::min<int64_t>(((k + 1) * nch / pj) * kGdnChunk, len);
+            table.push_back(SegEntry{(int32_t)(st + t0), (int32_t)(t1 - t0), -1 - slot, 0});
+            ++slot;
+        }
+    }
+    if ((int64_t)table.size() > HYPIC_MAX_SEGMENTS) return HYPIC_ERR_UNSUPPORTED;   // not reached: splits need few units
+    std::stable_sort(table.begin(), table.end(), [](const SegEntry &x, const SegEntry &y) { return x.len > y.len; });
+    p.n_seg = (int32_t)table.size();
     int64_t wsb = 0;
-    for (int r = 0; r < a->n_seg; ++r) {
-        const int j = order[r];
-        p.seg[r].start = (int32_t)a->seg_offsets[j];
-        p.seg[r].len = (int32_t)(a->seg_offsets[j + 1] - a->seg_offsets[j]);
-        p.seg[r].idx = j;
+    for (int r = 0; r < p.n_seg; ++r) {
+        p.seg[r] = table[r];
         p.seg[r].wsb = (int32_t)wsb;   // bounded by the record check above on the GDN path
         wsb = std::min<int64_t>(wsb + (int64_t)a->H_v * ((p.seg[r].len + kGdnChunk - 1) / kGdnChunk),
                                 INT32_MAX);
@@ -262,7 +352,40 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (path) {
-    case BuildPath::GdnTc: return from_cuda(launch_build_gdn_tc(p, s));
+    case BuildPath::GdnTc: {
+        cudaError_t e = launch_build_gdn_tc(p, s);
+        if (e != cudaSuccess || split.m <= 1) return from_cuda(e);
+        // compose the pieces of every split segment into its entry: S = the pieces' prefix
+        // scan from a zero state (its last state, copied out), lam = sum, P = product
+        const size_t unit = (size_t)a->d_k * a->d_k;
+        const int64_t stride = p.seg_stride;
+        float *prefix = reinterpret_cast<float *>(static_cast<uint8_t *>(a->workspace) + split.off_prefix);
+        int32_t slot0 = 0;
+        for (int j = 0; j < a->n_seg && e == cudaSuccess; ++j) {
+            const int pj = seg_pieces(a->seg_offsets[j + 1] - a->seg_offsets[j], split.m);
+            if (pj == 1) continue;
+            ComposeParams q;
+            std::memset(&q, 0, sizeof(q));
+            q.family = fam;
+            q.n_seg = pj;
+            q.n_units = a->H_v;
+            q.D = a->d_k;
+            q.S = p.S_piece + (size_t)slot0 * a->H_v * unit;
+            q.lam = p.lam_piece + (size_t)slot0 * a->H_v;
+            q.P = p.P_piece + (size_t)slot0 * a->H_v * unit;
+            q.prefix = prefix;
+            q.lam_total = a->lam + (size_t)j * stride;
+            q.P_total = a->P + (size_t)j * stride * unit;
+            q.err = err;
+            e = launch_compose_dense_tc(q, s);
+            if (e == cudaSuccess) e = launch_compose_lam_total(q, s);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(a->S + (size_t)j * stride * unit, prefix + (size_t)(pj - 1) * a->H_v * unit,
+                                    (size_t)a->H_v * unit * sizeof(float), cudaMemcpyDeviceToDevice, s);
+            slot0 += pj;
+        }
+        return from_cuda(e);
+    }
     case BuildPath::DeltaSeq: return from_cuda(launch_build_delta_seq(p, s));
     case BuildPath::GatedTc: return from_cuda(launch_build_gated_tc(p, s));
     case BuildPath::GatedSimt: return from_cuda(launch_build_gated_simt(p, s));

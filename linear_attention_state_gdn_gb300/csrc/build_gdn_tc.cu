@@ -506,8 +506,10 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
         // outputs: S = exp(Lam) S~ (column n) or P (column n), and lam
         if (ok && nch > 0) ok = wwait(&bars.zfull[hf], (nch - 1) & 1);
         tc_fence_after();
-        const int64_t unit = (int64_t)seg.idx * p.seg_stride + h;
-        float *O = (hf == 0 ? p.S : p.P) + unit * D * D + n;
+        // a piece of a split segment writes its own slot; a whole segment the caller's output
+        const bool piece = seg.idx < 0;
+        const int64_t unit = piece ? (int64_t)(-1 - seg.idx) * p.H_v + h : (int64_t)seg.idx * p.seg_stride + h;
+        float *O = (hf == 0 ? (piece ? p.S_piece : p.S) : (piece ? p.P_piece : p.P)) + unit * D * D + n;
         const float sc = (hf == 0 && nch > 0) ? expf(slots[(nch - 1) & 1].lam_after) : 1.f;
 #pragma unroll
         for (int c0 = 0; c0 < 128; c0 += 32) {
@@ -517,7 +519,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
 #pragma unroll
             for (int j = 0; j < 32; ++j) O[(int64_t)(c0 + j) * D] = __uint_as_float(z[j]) * sc;
         }
-        if (hf == 0 && n == 0) p.lam[unit] = nch > 0 ? slots[(nch - 1) & 1].lam_sum : 0.f;
+        if (hf == 0 && n == 0) (piece ? p.lam_piece : p.lam)[unit] = nch > 0 ? slots[(nch - 1) & 1].lam_sum : 0.f;
     }
 
     tc_fence_before();

@@ -15,7 +15,8 @@ enum : unsigned { kErrTimeout = 1u, kErrRange = 2u };
 
 // One segment of the launch table. The table is ordered longest first (LPT order:
 // "Hypic: Position-Independent KV Caching ..." episode companion, "Segment parallelism:
-// LPT scheduling across workers"); idx is the segment's position in the caller's order.
+// LPT scheduling across workers"); idx >= 0 is the segment's position in the caller's order,
+// idx < 0 marks a piece of a split segment whose outputs go to piece slot -1 - idx.
 struct SegEntry {
     int32_t start;
     int32_t len;
@@ -51,6 +52,11 @@ struct BuildParams {
     float *P;
     void *workspace;
     unsigned *err;
+    // outputs of segment pieces (SegEntry.idx < 0: slot -1 - idx, [slot][H_v] units) when a
+    // long segment is built as several pieces and composed afterwards; else unused
+    float *S_piece;
+    float *P_piece;
+    float *lam_piece;
     SegEntry seg[HYPIC_MAX_SEGMENTS];
 };
 

@@ -169,9 +169,10 @@ def make_inputs(family: str, H_k: int, H_v: int, d: int, seg_lens, dtype=torch.b
 # --------------------------------------------------------------------------------------
 # The five named workloads
 
-WORKLOADS = ("gdn_tiny", "retnet", "gla", "gdn", "gdn_compose")
+WORKLOADS = ("gdn_tiny", "retnet", "gla", "gdn", "gdn_compose", "gdn_one_segment")
 
-WORKLOAD_SEEDS = {"gdn_tiny": 1001, "retnet": 1002, "gla": 1003, "gdn": 1004, "gdn_compose": 1005}
+WORKLOAD_SEEDS = {"gdn_tiny": 1001, "retnet": 1002, "gla": 1003, "gdn": 1004, "gdn_compose": 1005,
+                  "gdn_one_segment": 1006}
 
 
 def workload_info(name: str) -> dict:
@@ -187,6 +188,8 @@ def workload_info(name: str) -> dict:
     if name == "gdn":
         return dict(family="gdn", dtype="bf16", H_k=16, H_v=32, d=128, seg_lens=[2048] * 16,
                     layers=1)
+    if name == "gdn_one_segment":   # the GDN prompt cached as one segment
+        return dict(family="gdn", dtype="bf16", H_k=16, H_v=32, d=128, seg_lens=[32768], layers=1)
     if name == "gdn_compose":
         lens = _rng(WORKLOAD_SEEDS[name]).integers(256, 1024, size=64, endpoint=True)
         return dict(family="gdn", dtype="bf16", H_k=16, H_v=32, d=128,

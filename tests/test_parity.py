@@ -55,6 +55,22 @@ def test_build_more_units_than_sms(family):
     check_build(inp)
 
 
+@pytest.mark.parametrize("family", ["gdn", "delta"])
+@pytest.mark.parametrize("lens", [[3000], [2500, 100, 0, 65]])
+def test_build_split_segments(family, lens):
+    """Few units (a long prompt as one or a few segments): the tensor-core build cuts each
+    segment into up to eight chunk-aligned pieces, builds them in parallel and composes them
+    back into the segment's entry. The result is the entry of the whole segment."""
+    hy = _hy()
+    inp = synth.make_inputs(family, 1, 2, 128, lens, torch.bfloat16, seed=46, alpha_scale=0.05)
+    d = {n: t.cuda() for n, t in inp.tensors().items()}
+    need = hy.hypic_build_workspace_bytes(family, d["k"], d["v"], inp.seg_offsets,
+                                          log_gate=d.get("log_gate"), beta=d.get("beta"))
+    chunks = sum((n + 63) // 64 for n in lens)
+    assert need > chunks * 2 * 8192 + 256      # records, tail, and the pieces' scratch
+    check_build(inp)
+
+
 def test_build_scalar_per_token_gate():
     inp = synth.make_inputs("scalar", 2, 2, 128, [300, 77], torch.bfloat16, seed=41,
                             per_token_scalar=True)
