@@ -10,7 +10,8 @@ device memory; `e2e` is the same metric through the public API with the inputs c
 from pinned host memory and every output copied back, inside the timed region.
 
 The other workloads (RetNet scalar build + compose, GLA diagonal build + compose, the same
-GDN prompt cached as one 32768-token segment, the 48-layer x 64-segment GDN compose with and
+GDN prompt cached as one 32768-token segment, the RetNet prompt as one 16384-token segment,
+the 48-layer x 64-segment GDN compose with and
 without the composed entry) are measured after the main timed region and reported under
 "sections". `--impl reference` times the fp64 CPU oracle instead (a bounded sample
 of the same workload per step, on the host cores).
@@ -579,7 +580,7 @@ def run_main(args):
         del st
         torch.cuda.empty_cache()
         sections = {}
-        for name in ("retnet", "gla", "gdn_one_segment"):
+        for name in ("retnet", "gla", "gdn_one_segment", "retnet_one_segment"):
             sections[name] = section_family(name, flush, pk)
         sections["gdn_compose"] = section_gdn_compose(flush, pk, layers=args.compose_layers)
         line["sections"] = sections
@@ -620,7 +621,8 @@ def main(argv=None):
     ap.add_argument("--quick", action="store_true",
                     help="main timed region only (no e2e, sections or CPU baseline)")
     ap.add_argument("--compose-layers", type=int, default=48)
-    ap.add_argument("--only", choices=["gdn", "retnet", "gla", "gdn_tiny", "gdn_compose", "gdn_one_segment"],
+    ap.add_argument("--only", choices=["gdn", "retnet", "gla", "gdn_tiny", "gdn_compose", "gdn_one_segment",
+                                       "retnet_one_segment"],
                     help="time one workload's launches alone (profiling helper; no contract line)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps

@@ -114,17 +114,19 @@ typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  *   lam               out [n_seg][H_v] fp32, DIAG [n_seg][H_v][d_k]
  *   P                 out DELTA / GDN: [n_seg][H_v][d_k][d_k] fp32; else NULL
  *   workspace         device scratch, at least hypic_build_workspace_bytes() bytes, 16-byte
- *                     aligned (NULL when that is 0). DELTA / GDN with bf16 k, v and
- *                     d = 128 use 8 KB per (segment, value head, 64-token chunk): the
- *                     chunk matrices (I + Diag(b) L)^-1 Diag(b) that the chain kernel reads
- *                     back, plus 256 bytes of work-distribution counter (set by the call
- *                     itself; no part needs to start at zero). When the call's (segment,
- *                     value head) units fill at most half of the current device's SMs, each
- *                     segment is built as up to 8 chunk-aligned pieces that are composed
- *                     back into its entry; the pieces' S, P and lam and one scan buffer then
- *                     follow in the workspace. The caller owns it; its contents are undefined after the call and
- *                     it may be reused by the next call on the same stream, but not by a call
- *                     still running on another stream. It must not overlap any argument.
+ *                     aligned (NULL when that is 0). What it holds:
+ *                     - DELTA / GDN with bf16 k, v and d = 128: 8 KB per (segment, value
+ *                       head, 64-token chunk), the chunk matrices (I + Diag(b) L)^-1 Diag(b)
+ *                       that the chain kernel reads back, and 256 bytes of work-distribution
+ *                       counter set by the call itself.
+ *                     - Any bf16, d = 128 build whose (segment, value head) units fill at most
+ *                       half of the current device's SMs: each segment is built as up to 8
+ *                       chunk-aligned pieces that are then composed back into its entry; the
+ *                       pieces' S, (P,) lam and one scan buffer follow.
+ *                     No part needs to start at zero. The caller owns it; its contents are
+ *                     undefined after the call and it may be reused by the next call on the
+ *                     same stream, but not by a call still running on another stream. It must
+ *                     not overlap any argument.
  */
 typedef struct {
     int32_t family;

@@ -121,9 +121,9 @@ int64_t gdn_records(const hypic_build_args *a) {
     return records;
 }
 
-// Intra-segment split of the DeltaNet / GDN tensor-core build. Each (segment, value head)
-// unit is one serial chain of 64-token chunks, so a call with few units (one long prompt as a
-// single segment) leaves most SMs idle. When the units fill at most half of the SMs, every
+// Intra-segment split of the tensor-core builds (DeltaNet / GDN, and the linear / scalar /
+// diagonal one). Each (segment, value head) unit is one serial chain of chunks, so a call with
+// few units (one long prompt as a single segment) leaves most SMs idle. When the units fill at most half of the SMs, every
 // segment is cut into up to kMaxPieces chunk-aligned pieces that build in parallel as
 // segments of their own; the pieces of a segment are then composed back into its entry, the
 // composition the pages state for consecutive cached segments ("Cut First-Token Latency by
@@ -151,8 +151,9 @@ int seg_pieces(int64_t len, int m) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(m, nch));
 }
 
-// Workspace of the split: piece outputs S, P [slots][H_v][d][d], lam [slots][H_v] (rounded to
-// 256 bytes), and one scan buffer [max pieces][H_v][d][d] for the composition.
+// Workspace of the split: piece outputs S, P (dense families only) [slots][H_v][d][d], lam
+// [slots][H_v] ([slots][H_v][d] for diagonal gates; rounded to 256 bytes), and one scan
+// buffer [max pieces][H_v][d][d] for the composition.
 struct SplitLayout {
     int m = 1, slots = 0, max_pieces = 1;
     size_t off_S = 0, off_P = 0, off_lam = 0, off_prefix = 0, bytes = 0;
@@ -175,10 +176,12 @@ SplitLayout gdn_split_layout(const hypic_build_args *a, size_t base) {
     }
     const size_t unit = (size_t)a->d_k * a->d_k * sizeof(float);
     const size_t su = (size_t)L.slots * a->H_v;
+    const bool dense = a->family == HYPIC_FAM_DELTA || a->family == HYPIC_FAM_GDN;
+    const size_t nl = a->family == HYPIC_FAM_DIAG ? (size_t)a->d_k : 1;
     L.off_S = base;
     L.off_P = L.off_S + su * unit;
-    L.off_lam = L.off_P + su * unit;
-    L.off_prefix = L.off_lam + ((su * sizeof(float) + 255) & ~(size_t)255);
+    L.off_lam = L.off_P + (dense ? su * unit : 0);
+    L.off_prefix = L.off_lam + ((su * nl * sizeof(float) + 255) & ~(size_t)255);
     L.bytes = L.off_prefix + (size_t)L.max_pieces * a->H_v * unit - base;
     return L;
 }
@@ -216,7 +219,9 @@ const char *hypic_status_string(hypic_status s) {
 
 size_t hypic_build_workspace_bytes(const hypic_build_args *a) {
     if (!build_shape_ok(a) || a->n_seg == 0 || !a->seg_offsets) return 0;
-    if (pick_build(a) != BuildPath::GdnTc) return 0;
+    const BuildPath path = pick_build(a);
+    if (path == BuildPath::GatedTc) return gdn_split_layout(a, 0).bytes;   // 0 without a split
+    if (path != BuildPath::GdnTc) return 0;
     const int64_t records = gdn_records(a);
     if (records == 0) return 0;
     const size_t base = (size_t)records * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail;
@@ -272,16 +277,15 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
             if (p && !on_device(p)) return HYPIC_ERR_INVALID_ARG;
     }
     const BuildPath path = pick_build(a);
-    if (path == BuildPath::GdnTc) {
-        // records are addressed as 64-row blocks of a 2D tensor map with int32 coordinates
-        if (gdn_records(a) > (int64_t)(INT32_MAX / 64)) return HYPIC_ERR_UNSUPPORTED;
-        if (gdn_records(a) > 0) {
-            if (!a->workspace) return HYPIC_ERR_INVALID_ARG;
-            if (!aligned(a->workspace, 16)) return HYPIC_ERR_ALIGNMENT;
-            if (!on_device(a->workspace)) return HYPIC_ERR_INVALID_ARG;
-        }
+    // records are addressed as 64-row blocks of a 2D tensor map with int32 coordinates
+    if (path == BuildPath::GdnTc && gdn_records(a) > (int64_t)(INT32_MAX / 64)) return HYPIC_ERR_UNSUPPORTED;
+    const size_t ws_need = hypic_build_workspace_bytes(a);
+    if (ws_need > 0) {
+        if (!a->workspace) return HYPIC_ERR_INVALID_ARG;
+        if (!aligned(a->workspace, 16)) return HYPIC_ERR_ALIGNMENT;
+        if (!on_device(a->workspace)) return HYPIC_ERR_INVALID_ARG;
     }
-    if (hypic_build_workspace_bytes(a) > a->workspace_bytes) return HYPIC_ERR_INVALID_ARG;
+    if (ws_need > a->workspace_bytes) return HYPIC_ERR_INVALID_ARG;
 
     unsigned *err = status_word(nullptr);
     if (!err) return HYPIC_ERR_CUDA;
@@ -311,8 +315,10 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
     // the launch table: whole segments, or the chunk-aligned pieces of split ones (piece k of
     // a segment with n chunks in pj pieces covers chunks [k n / pj, (k + 1) n / pj))
     SplitLayout split;
-    if (path == BuildPath::GdnTc) {
-        const size_t base = (size_t)gdn_records(a) * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail;
+    if (path == BuildPath::GdnTc || path == BuildPath::GatedTc) {
+        const size_t base = path == BuildPath::GdnTc
+                                ? (size_t)gdn_records(a) * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail
+                                : 0;
         split = gdn_split_layout(a, base);
         if (split.m > 1) {
             uint8_t *ws = static_cast<uint8_t *>(a->workspace);
@@ -352,12 +358,15 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (path) {
-    case BuildPath::GdnTc: {
-        cudaError_t e = launch_build_gdn_tc(p, s);
+    case BuildPath::GdnTc:
+    case BuildPath::GatedTc: {
+        cudaError_t e = path == BuildPath::GdnTc ? launch_build_gdn_tc(p, s) : launch_build_gated_tc(p, s);
         if (e != cudaSuccess || split.m <= 1) return from_cuda(e);
         // compose the pieces of every split segment into its entry: S = the pieces' prefix
         // scan from a zero state (its last state, copied out), lam = sum, P = product
+        const bool dense = fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GDN;
         const size_t unit = (size_t)a->d_k * a->d_k;
+        const size_t nl = fam == HYPIC_FAM_DIAG ? (size_t)a->d_k : 1;
         const int64_t stride = p.seg_stride;
         float *prefix = reinterpret_cast<float *>(static_cast<uint8_t *>(a->workspace) + split.off_prefix);
         int32_t slot0 = 0;
@@ -371,13 +380,13 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
             q.n_units = a->H_v;
             q.D = a->d_k;
             q.S = p.S_piece + (size_t)slot0 * a->H_v * unit;
-            q.lam = p.lam_piece + (size_t)slot0 * a->H_v;
-            q.P = p.P_piece + (size_t)slot0 * a->H_v * unit;
+            q.lam = p.lam_piece + (size_t)slot0 * a->H_v * nl;
+            q.P = dense ? p.P_piece + (size_t)slot0 * a->H_v * unit : nullptr;
             q.prefix = prefix;
-            q.lam_total = a->lam + (size_t)j * stride;
-            q.P_total = a->P + (size_t)j * stride * unit;
+            q.lam_total = a->lam + (size_t)j * stride * nl;
+            q.P_total = dense ? a->P + (size_t)j * stride * unit : nullptr;
             q.err = err;
-            e = launch_compose_dense_tc(q, s);
+            e = dense ? launch_compose_dense_tc(q, s) : launch_compose_scaled(q, s);
             if (e == cudaSuccess) e = launch_compose_lam_total(q, s);
             if (e == cudaSuccess)
                 e = cudaMemcpyAsync(a->S + (size_t)j * stride * unit, prefix + (size_t)(pj - 1) * a->H_v * unit,
@@ -387,7 +396,6 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
         return from_cuda(e);
     }
     case BuildPath::DeltaSeq: return from_cuda(launch_build_delta_seq(p, s));
-    case BuildPath::GatedTc: return from_cuda(launch_build_gated_tc(p, s));
     case BuildPath::GatedSimt: return from_cuda(launch_build_gated_simt(p, s));
     case BuildPath::None: break;
     }

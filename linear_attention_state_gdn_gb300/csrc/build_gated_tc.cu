@@ -296,17 +296,20 @@ build_gated_tc_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         for (int c = 1; ok && c < nchunks; ++c) ok = decay(c) && fold(c - 1);
         if (ok && nchunks > 0) ok = fold(nchunks - 1);
 
-        const int64_t unit = (int64_t)seg.idx * p.seg_stride + h;
-        float4 *out = reinterpret_cast<float4 *>(p.S + unit * D * D + (int64_t)i * D + 64 * hc);
+        // a piece of a split segment writes its own slot; a whole segment the caller's output
+        const bool piece = seg.idx < 0;
+        const int64_t unit = piece ? (int64_t)(-1 - seg.idx) * p.H_v + h : (int64_t)seg.idx * p.seg_stride + h;
+        float *lam_out = piece ? p.lam_piece : p.lam;
+        float4 *out = reinterpret_cast<float4 *>((piece ? p.S_piece : p.S) + unit * D * D + (int64_t)i * D + 64 * hc);
 #pragma unroll
         for (int n = 0; n < 64; n += 4) out[n / 4] = make_float4(S[n], S[n + 1], S[n + 2], S[n + 3]);
         if (hc == 0) {
             if (KIND == kDiag) {
-                p.lam[unit * D + i] = lam;
+                lam_out[unit * D + i] = lam;
             } else if (i == 0) {
                 float l = 0.f;
                 if (KIND == kScalar) l = p.log_gamma ? (float)seg.len * lgam : lam;
-                p.lam[unit] = l;
+                lam_out[unit] = l;
             }
         }
     }

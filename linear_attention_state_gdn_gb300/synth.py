@@ -169,10 +169,10 @@ def make_inputs(family: str, H_k: int, H_v: int, d: int, seg_lens, dtype=torch.b
 # --------------------------------------------------------------------------------------
 # The five named workloads
 
-WORKLOADS = ("gdn_tiny", "retnet", "gla", "gdn", "gdn_compose", "gdn_one_segment")
+WORKLOADS = ("gdn_tiny", "retnet", "gla", "gdn", "gdn_compose", "gdn_one_segment", "retnet_one_segment")
 
 WORKLOAD_SEEDS = {"gdn_tiny": 1001, "retnet": 1002, "gla": 1003, "gdn": 1004, "gdn_compose": 1005,
-                  "gdn_one_segment": 1006}
+                  "gdn_one_segment": 1006, "retnet_one_segment": 1007}
 
 
 def workload_info(name: str) -> dict:
@@ -187,6 +187,9 @@ def workload_info(name: str) -> dict:
                     layers=1)
     if name == "gdn":
         return dict(family="gdn", dtype="bf16", H_k=16, H_v=32, d=128, seg_lens=[2048] * 16,
+                    layers=1)
+    if name == "retnet_one_segment":   # the RetNet prompt cached as one segment
+        return dict(family="scalar", dtype="bf16", H_k=16, H_v=16, d=128, seg_lens=[16384],
                     layers=1)
     if name == "gdn_one_segment":   # the GDN prompt cached as one segment
         return dict(family="gdn", dtype="bf16", H_k=16, H_v=32, d=128, seg_lens=[32768], layers=1)
@@ -204,7 +207,7 @@ def make_workload(name: str, layer: int = 0) -> SegmentInputs:
     fam, d = info["family"], info["d"]
     if name == "gdn_tiny":
         inp = make_inputs("gdn", 2, 2, 32, info["seg_lens"], torch.float32, seed, alpha_scale=0.1)
-    elif name == "retnet":
+    elif name in ("retnet", "retnet_one_segment"):
         inp = make_inputs("scalar", 16, 16, d, info["seg_lens"], torch.bfloat16, seed)
     elif name == "gla":
         inp = make_inputs("diag", 16, 16, d, info["seg_lens"], torch.bfloat16, seed)

@@ -55,19 +55,23 @@ def test_build_more_units_than_sms(family):
     check_build(inp)
 
 
-@pytest.mark.parametrize("family", ["gdn", "delta"])
+@pytest.mark.parametrize("family,per_token", [("gdn", False), ("delta", False), ("linear", False),
+                                              ("scalar", False), ("scalar", True), ("diag", False)])
 @pytest.mark.parametrize("lens", [[3000], [2500, 100, 0, 65]])
-def test_build_split_segments(family, lens):
-    """Few units (a long prompt as one or a few segments): the tensor-core build cuts each
-    segment into up to eight chunk-aligned pieces, builds them in parallel and composes them
+def test_build_split_segments(family, per_token, lens):
+    """Few units (a long prompt as one or a few segments): the tensor-core builds cut each
+    segment into up to eight chunk-aligned pieces, build them in parallel and compose them
     back into the segment's entry. The result is the entry of the whole segment."""
     hy = _hy()
-    inp = synth.make_inputs(family, 1, 2, 128, lens, torch.bfloat16, seed=46, alpha_scale=0.05)
+    inp = synth.make_inputs(family, 1, 2, 128, lens, torch.bfloat16, seed=46, alpha_scale=0.05,
+                            gla_div=8.0, per_token_scalar=per_token)
     d = {n: t.cuda() for n, t in inp.tensors().items()}
     need = hy.hypic_build_workspace_bytes(family, d["k"], d["v"], inp.seg_offsets,
-                                          log_gate=d.get("log_gate"), beta=d.get("beta"))
+                                          log_gate=d.get("log_gate"), log_gamma=d.get("log_gamma"),
+                                          beta=d.get("beta"))
     chunks = sum((n + 63) // 64 for n in lens)
-    assert need > chunks * 2 * 8192 + 256      # records, tail, and the pieces' scratch
+    records = chunks * 2 * 8192 + 256 if family in ("gdn", "delta") else 0
+    assert need > records      # (records and tail, and) the pieces' scratch
     check_build(inp)
 
 
