@@ -7,7 +7,8 @@ tokens (bf16 k L2-normalised, bf16 v, fp32 gates and beta), built into all 512
 (S(C|0), T_C) pairs in one launch, then prefix-scan composed across the 16 segments in a
 second launch. `value` is build+compose tokens/s of that step with the inputs resident in
 device memory; `e2e` is the same metric through the public API with the inputs copied in
-from pinned host memory and every output copied back, inside the timed region.
+from pinned host memory and every output copied back, inside the timed region (the segments
+in four groups, so that each group's copies overlap the previous group's build).
 
 The other workloads (RetNet scalar build + compose, GLA diagonal build + compose, the same
 GDN prompt cached as one 32768-token segment, the RetNet prompt as one 16384-token segment,
@@ -444,44 +445,86 @@ def workload_config():
 
 # ----------------------------------------------------------------------------- main arm
 
-def e2e_measure(inp, steps=5, warmup=2):
-    """Through the public API from pinned host buffers: H2D of k, v, log a, beta; build;
-    compose; D2H of S, lam, P and the prefix states, all inside the events."""
+def e2e_measure(inp, steps=5, warmup=2, groups=4):
+    """Through the public API from pinned host buffers, inside the events: H2D of k, v, log a,
+    beta; build; compose; D2H of S, lam, P and the prefix states. The prompt's segments go in
+    `groups` consecutive groups so that transfers overlap compute: group g's inputs copy in on
+    one stream while group g - 1 builds, and each group's S, lam, P copy out on a third stream
+    as soon as it is built (each unit's result does not depend on the grouping). The compose
+    over all segments follows the last build; its prefix states copy out last."""
     import linear_attention_state_gdn_gb300 as hy
     host = {n: t.pin_memory() for n, t in inp.tensors().items()}
     dev = {n: torch.empty_like(t, device="cuda") for n, t in host.items()}
     S, lam, P = hy.build_outputs(inp.family, inp.n_seg, inp.H_v, inp.d_v, "cuda")
     prefix = torch.empty_like(S)
-    workspace = make_workspace(hy, inp, dev, "cuda")
     outs = [S, lam, P, prefix]
     host_out = [torch.empty_like(t, device="cpu").pin_memory() for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in outs)
+    offs = np.asarray(inp.seg_offsets, dtype=np.int64)
+    bounds = [round(g * inp.n_seg / groups) for g in range(groups + 1)]
+    grp = [(s0, s1, int(offs[s0]), int(offs[s1])) for s0, s1 in zip(bounds[:-1], bounds[1:]) if s1 > s0]
+    sub = lambda d, t0, t1: {n: t[t0:t1] for n, t in d.items()}
+    need = max(hy.hypic_build_workspace_bytes(inp.family, dev["k"][t0:t1], dev["v"][t0:t1],
+                                              offs[s0:s1 + 1] - t0, log_gate=dev.get("log_gate"),
+                                              beta=dev.get("beta")) for s0, s1, t0, t1 in grp)
+    workspace = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
+    comp = torch.cuda.current_stream()
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def one():
-        for n in host:
-            dev[n].copy_(host[n], non_blocking=True)
-        hy.hypic_build_segments(inp.family, dev["k"], dev["v"], inp.seg_offsets,
-                                log_gate=dev.get("log_gate"), log_gamma=dev.get("log_gamma"),
-                                beta=dev.get("beta"), S=S, lam=lam, P=P, workspace=workspace)
+    def one(start_ev):
+        cin.wait_event(start_ev)
+        cout.wait_event(start_ev)
+        loaded = []
+        for s0, s1, t0, t1 in grp:            # every group's inputs, in order, on the copy-in stream
+            with torch.cuda.stream(cin):
+                for n in host:
+                    dev[n][t0:t1].copy_(host[n][t0:t1], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(cin)
+            loaded.append(ev)
+        for (s0, s1, t0, t1), ev in zip(grp, loaded):
+            comp.wait_event(ev)
+            d = sub(dev, t0, t1)
+            hy.hypic_build_segments(inp.family, d["k"], d["v"], offs[s0:s1 + 1] - t0,
+                                    log_gate=d.get("log_gate"), log_gamma=dev.get("log_gamma"),
+                                    beta=d.get("beta"), S=S[s0:s1], lam=lam[s0:s1], P=P[s0:s1],
+                                    workspace=workspace)
+            built = torch.cuda.Event()
+            built.record(comp)
+            cout.wait_event(built)
+            with torch.cuda.stream(cout):
+                for h, t in zip(host_out[:3], outs[:3]):
+                    if t is not None:
+                        h[s0:s1].copy_(t[s0:s1], non_blocking=True)
         hy.hypic_compose_scan(inp.family, S, lam, P, prefix=prefix)
-        for h, d in zip(host_out, outs):
-            h.copy_(d, non_blocking=True)
+        composed = torch.cuda.Event()
+        composed.record(comp)
+        cout.wait_event(composed)
+        with torch.cuda.stream(cout):
+            host_out[3].copy_(prefix, non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(cout)
+        comp.wait_event(done)
 
     for _ in range(warmup):
-        one()
+        ev = torch.cuda.Event()
+        ev.record(comp)
+        one(ev)
     torch.cuda.synchronize()
     ms = []
     for _ in range(steps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        one()
-        b.record()
+        a.record(comp)
+        one(a)
+        b.record(comp)
         b.synchronize()
         ms.append(a.elapsed_time(b))
     m = statistics.mean(ms)
+    # the copied-out results are the device results
+    assert torch.equal(host_out[0], S.cpu()) and torch.equal(host_out[3], prefix.cpu())
     return {"value": round(inp.n_tok / m * 1e3, 1), "unit": UNIT, "ms_per_step": round(m, 4),
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "groups": len(grp)}
 
 
 def build_launches(kernel_name):
