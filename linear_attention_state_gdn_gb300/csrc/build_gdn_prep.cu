@@ -55,13 +55,19 @@ constexpr int D = 128;
 constexpr int C = kGdnChunk;
 constexpr int kThreads = 128;
 constexpr uint32_t kLDA = 68;                            // padded fp32 row stride
-constexpr uint32_t kOffK = 0;                            // k tile, 16 KB
-constexpr uint32_t kOffG32 = 16384;                      // the gram K K^T, 64 x 68
-constexpr uint32_t kOffN32 = kOffG32 + 64 * kLDA * 4;    // N (tf32-rounded), 64 x 68
 constexpr uint32_t kLDT = 12;                            // per-warp 16 x 8 scratch, padded rows
-constexpr uint32_t kOffT = kOffN32 + 64 * kLDA * 4;      // 4 warps x 16 x 12 fp32
-constexpr uint32_t kSmemBytes = kOffT + 4 * 16 * kLDT * 4 + 1024;
-constexpr int kCtasPerSm = 4;
+// R records per iteration: the value heads h, h + 1 that share a key head (R = 2, when the
+// grouped-query factor is even) share the k tile, the gram and its shared-memory copy, and
+// their two inverses run side by side; R = 1 otherwise.
+template <int R>
+struct PrepGeo {
+    static constexpr uint32_t kOffK = 0;                              // k tile, 16 KB
+    static constexpr uint32_t kOffG32 = 16384;                        // the gram K K^T, 64 x 68
+    static constexpr uint32_t kOffN32 = kOffG32 + 64 * kLDA * 4;      // R x N (tf32-rounded), 64 x 68
+    static constexpr uint32_t kOffT = kOffN32 + R * 64 * kLDA * 4;    // 4 warps x 16 x 12 fp32
+    static constexpr uint32_t kSmemBytes = kOffT + 4 * 16 * kLDT * 4 + 1024;
+    static constexpr int kCtasPerSm = R == 1 ? 4 : 3;
+};
 constexpr int kCtl = 96;   // warp 3 lane 0 issues loads and grams (warp 3 has the least level work)
 
 __device__ __forceinline__ uint32_t to_tf32(float x) {
@@ -119,27 +125,28 @@ __device__ __forceinline__ void half_block(const float *G32, float *N32, float *
     __syncwarp();   // Tw is reused by this warp's next half-block
 }
 
-// Records are numbered in the order (segment rank, chunk, value head), so the value heads
-// that share a key head read the same k tile back to back (from L2); segment rank r owns
-// numbers [wsb_r, wsb_r + H_v nch_r). A number is turned back into its record by a binary
-// search over the segment table.
+// Work units (R records each) are numbered in the order (segment rank, chunk, value heads
+// h .. h + R - 1), so the units that share a key head read the same k tile back to back
+// (from L2); segment rank r owns numbers [wsb_r / R, (wsb_r + H_v nch_r) / R). A number is
+// turned back into its unit by a binary search over the segment table.
 struct Walk {
-    int r, c, h;   // segment rank, chunk, value head; r == n_seg: no record
+    int r, c, h;   // segment rank, chunk, first value head; r == n_seg: no unit
 };
 
-__device__ __forceinline__ Walk decode(const BuildParams &p, int64_t t, int64_t total) {
+template <int R>
+__device__ __forceinline__ Walk decode(const BuildParams &p, int64_t t, int64_t units) {
     Walk w{p.n_seg, 0, 0};
-    if (t >= total) return w;
-    int lo = 0, hi = p.n_seg - 1;   // the last rank with wsb <= t (empty segments come last)
+    if (t >= units) return w;
+    int lo = 0, hi = p.n_seg - 1;   // the last rank with wsb / R <= t (empty segments come last)
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (p.seg[mid].wsb <= t) lo = mid;
+        if (p.seg[mid].wsb / R <= t) lo = mid;
         else hi = mid - 1;
     }
-    const int local = (int)(t - p.seg[lo].wsb);
+    const int local = (int)(t - p.seg[lo].wsb / R), per_chunk = p.H_v / R;
     w.r = lo;
-    w.c = local / p.H_v;
-    w.h = local - w.c * p.H_v;
+    w.c = local / per_chunk;
+    w.h = R * (local - w.c * per_chunk);
     return w;
 }
 
@@ -148,25 +155,27 @@ __device__ __forceinline__ int64_t total_records(const BuildParams &p) {
     return (int64_t)l.wsb + (int64_t)p.H_v * ((l.len + C - 1) / C);
 }
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+template <int R>
+__global__ void __launch_bounds__(kThreads, PrepGeo<R>::kCtasPerSm)
 build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK) {
+    using G = PrepGeo<R>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ uint64_t kfull, gfull[2];
     __shared__ uint32_t tslot;
     __shared__ int s_ok;
-    __shared__ Walk s_n2[2];   // the record after `nxt`, drawn by thread kCtl (two slots)
-    __shared__ __align__(16) float vb[2][C];
+    __shared__ Walk s_n2[2];   // the unit after `nxt`, drawn by thread kCtl (two slots)
+    __shared__ __align__(16) float vb[2][R][C];
 
-    const int64_t total = total_records(p);
+    const int64_t total = total_records(p), units = total / R;
     unsigned *tickets = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(p.workspace) + total * kGdnRecordBytes);
     auto nch_of = [&](int r) { return (p.seg[r].len + C - 1) / C; };
-    Walk cur = decode(p, blockIdx.x, total);
+    Walk cur = decode<R>(p, blockIdx.x, units);
     if (cur.r >= p.n_seg) return;   // uniform: the whole CTA leaves before any set-up
     const int q = threadIdx.x, warp = q >> 5, lane = q & 31;
-    float *G32 = reinterpret_cast<float *>(smem + kOffG32);
-    float *N32 = reinterpret_cast<float *>(smem + kOffN32);
-    float *Tw = reinterpret_cast<float *>(smem + kOffT) + warp * 16 * kLDT;
+    float *G32 = reinterpret_cast<float *>(smem + G::kOffG32);
+    float *N32 = reinterpret_cast<float *>(smem + G::kOffN32);   // record rr at N32 + rr * 64 * kLDA
+    float *Tw = reinterpret_cast<float *>(smem + G::kOffT) + warp * 16 * kLDT;
 
     if (q == 0) {
         mbar_init(&kfull, 1);
@@ -185,15 +194,15 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         ++kiss;
         const int32_t t0 = p.seg[w.r].start + w.c * C;
         mbar_arrive_expect_tx(&kfull, 16384);
-        tma_load_3d(smem + kOffK, &tmK, &kfull, 0, w.h / p.gqa, t0);
-        tma_load_3d(smem + kOffK + 8192, &tmK, &kfull, 64, w.h / p.gqa, t0);
+        tma_load_3d(smem + G::kOffK, &tmK, &kfull, 0, w.h / p.gqa, t0);
+        tma_load_3d(smem + G::kOffK + 8192, &tmK, &kfull, 64, w.h / p.gqa, t0);
     };
     auto gram = [&](int b) -> bool {   // thread kCtl: the k tile -> TMEM buffer b
         if (!mbar_wait(&kfull, kwait & 1, p.err, kErrTimeout)) return false;
         ++kwait;
         ++giss[b];
         tc_fence_after();
-        const uint32_t k = smem_u32(smem + kOffK);
+        const uint32_t k = smem_u32(smem + G::kOffK);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
             const uint32_t a = k + (s >> 2) * 8192 + (s & 3) * 32;
@@ -203,15 +212,16 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         mma_commit(&gfull[b]);
         return true;
     };
-    // b of a record (thread q < 64: token q), loaded one record ahead
+    // b of a unit's records (thread q < 64 R: token q % 64 of record q / 64), a unit ahead
     auto load_beta = [&](const Walk &w) -> float {
-        if (q >= C || w.r >= p.n_seg) return 0.f;
+        const int tq = q & (C - 1), rr = q / C;
+        if (rr >= R || w.r >= p.n_seg) return 0.f;
         const SegEntry sg = p.seg[w.r];
-        return q < min(C, sg.len - w.c * C) ? p.beta[((int64_t)sg.start + w.c * C + q) * p.H_v + w.h] : 0.f;
+        return tq < min(C, sg.len - w.c * C) ? p.beta[((int64_t)sg.start + w.c * C + tq) * p.H_v + w.h + rr] : 0.f;
     };
     bool ok = true;
     int64_t ticket = 0;   // thread kCtl
-    Walk nxt = decode(p, (int64_t)gridDim.x + blockIdx.x, total);
+    Walk nxt = decode<R>(p, (int64_t)gridDim.x + blockIdx.x, units);
     float beta_cur = load_beta(cur);
     if (q == kCtl) {
         prefetch_tmap(&tmK);
@@ -222,7 +232,7 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         const int b = i & 1;
         const SegEntry seg = p.seg[cur.r];
         const int nch = nch_of(cur.r);
-        if (q < C) vb[b][q] = beta_cur;
+        if (q < R * C) vb[b][q / C][q & (C - 1)] = beta_cur;
         const float beta_next = load_beta(nxt);
         // gram(i) done: the k tile is free for the next record
         if (q == kCtl) {
@@ -262,10 +272,13 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         }
         tc_fence_before();
         __syncthreads();
-        // diagonal block `warp`: lane j < 16 solves column j by forward substitution,
+        // diagonal block `warp`: lane j < 16 solves column j of record 0 (lanes 16-31 that of
+        // record 1 when R = 2) by forward substitution,
         // x_r = [r == j] - b_r sum_{s<r} G_rs x_s (A = Diag(b) L restricted to the block)
-        if (lane < 16) {
-            const int a = warp, j = lane;
+        if (R == 2 || lane < 16) {
+            const int a = warp, j = lane & 15, rr_ = lane >> 4;
+            const float *bv = vb[b][rr_];
+            float *Nr = N32 + rr_ * 64 * kLDA;
             float x[16];
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
@@ -279,43 +292,54 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int s = 0; s < rr; ++s) acc[s & 3] = fmaf(gr[s], x[s], acc[s & 3]);
-                x[rr] = fmaf(-vb[b][16 * a + rr], (acc[0] + acc[1]) + (acc[2] + acc[3]), (rr == j) ? 1.f : 0.f);
+                x[rr] = fmaf(-bv[16 * a + rr], (acc[0] + acc[1]) + (acc[2] + acc[3]), (rr == j) ? 1.f : 0.f);
             }
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) N32[(16 * a + rr) * kLDA + 16 * a + j] = tf32r(x[rr]);
+            for (int rr = 0; rr < 16; ++rr) Nr[(16 * a + rr) * kLDA + 16 * a + j] = tf32r(x[rr]);
         }
         __syncthreads();
         // level 1: (1,0), (2,1), (3,2) as six half-blocks; level 2: (2,0), (3,1); level 3: (3,0).
         // Warps 0-1 take one half-block per level, warps 2-3 two in level 1 and none in level 3.
-        half_block(G32, N32, Tw, vb[b], 1 + (warp >> 1), warp >> 1, warp & 1, lane);
-        if (warp >= 2) half_block(G32, N32, Tw, vb[b], 3, 2, warp & 1, lane);
+        // Each half-block is done for every record of the unit.
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr) {
+            half_block(G32, N32 + rr * 64 * kLDA, Tw, vb[b][rr], 1 + (warp >> 1), warp >> 1, warp & 1, lane);
+            if (warp >= 2) half_block(G32, N32 + rr * 64 * kLDA, Tw, vb[b][rr], 3, 2, warp & 1, lane);
+        }
         __syncthreads();
-        half_block(G32, N32, Tw, vb[b], 2 + (warp >> 1), warp >> 1, warp & 1, lane);
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr)
+            half_block(G32, N32 + rr * 64 * kLDA, Tw, vb[b][rr], 2 + (warp >> 1), warp >> 1, warp & 1, lane);
         __syncthreads();
-        if (warp < 2) half_block(G32, N32, Tw, vb[b], 3, 0, warp, lane);
+        if (warp < 2) {
+#pragma unroll
+            for (int rr = 0; rr < R; ++rr) half_block(G32, N32 + rr * 64 * kLDA, Tw, vb[b][rr], 3, 0, warp, lane);
+        }
         // warps 2-3 have no level-3 work: the next record's gram (its k tile was requested at
         // the top of this iteration) into the other TMEM buffer, last read a record ago
         // and the ticket of the record after it
         if (q == kCtl) {
             if (ok && nxt.r < p.n_seg) ok = gram(b ^ 1);
-            s_n2[b] = nxt.r < p.n_seg ? decode(p, ticket, total) : nxt;
+            s_n2[b] = nxt.r < p.n_seg ? decode<R>(p, ticket, units) : nxt;
         }
         __syncthreads();
         const Walk n2 = s_n2[b];   // slot b is written again two records later
         if (n2.r >= p.n_seg) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        // record: N Diag(b) as bf16 rows t' (blocks above the diagonal are zero)
-        uint8_t *dst = static_cast<uint8_t *>(p.workspace) +
-                       ((int64_t)seg.wsb + (int64_t)cur.h * nch + cur.c) * (int64_t)kGdnRecordBytes;
+        // records: N Diag(b) as bf16 rows t' (blocks above the diagonal are zero)
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int e8 = q + 128 * m;   // 8 consecutive entries of row t'
+        for (int m = 0; m < 4 * R; ++m) {
+            const int rr = m / 4;
+            uint8_t *dst = static_cast<uint8_t *>(p.workspace) +
+                           ((int64_t)seg.wsb + (int64_t)(cur.h + rr) * nch + cur.c) * (int64_t)kGdnRecordBytes;
+            const float *Nr = N32 + rr * 64 * kLDA;
+            const int e8 = q + 128 * (m & 3);   // 8 consecutive entries of row t'
             const int tp = e8 >> 3, s8 = (e8 & 7) * 8;
             uint4 pk = make_uint4(0u, 0u, 0u, 0u);
             if ((s8 >> 4) <= (tp >> 4)) {
-                const float4 lo = reinterpret_cast<const float4 *>(N32 + tp * kLDA + s8)[0];
-                const float4 hi = reinterpret_cast<const float4 *>(N32 + tp * kLDA + s8)[1];
-                const float4 b0 = reinterpret_cast<const float4 *>(vb[b] + s8)[0];
-                const float4 b1 = reinterpret_cast<const float4 *>(vb[b] + s8)[1];
+                const float4 lo = reinterpret_cast<const float4 *>(Nr + tp * kLDA + s8)[0];
+                const float4 hi = reinterpret_cast<const float4 *>(Nr + tp * kLDA + s8)[1];
+                const float4 b0 = reinterpret_cast<const float4 *>(vb[b][rr] + s8)[0];
+                const float4 b1 = reinterpret_cast<const float4 *>(vb[b][rr] + s8)[1];
                 pk = make_uint4(pack_bf16x2(lo.x * b0.x, lo.y * b0.y), pack_bf16x2(lo.z * b0.z, lo.w * b0.w),
                                 pack_bf16x2(hi.x * b1.x, hi.y * b1.y), pack_bf16x2(hi.z * b1.z, hi.w * b1.w));
             }
@@ -338,6 +362,17 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     }
 }
 
+template <int R>
+cudaError_t launch_prep(const BuildParams &p, int64_t total, const CUtensorMap &tmK, int sms, cudaStream_t s) {
+    using G = PrepGeo<R>;
+    cudaError_t e = cudaFuncSetAttribute(build_gdn_prep_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         G::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = (int)std::min<int64_t>(total / R, (int64_t)sms * G::kCtasPerSm);
+    build_gdn_prep_kernel<R><<<grid, kThreads, G::kSmemBytes, s>>>(p, tmK);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_build_gdn_prep(const BuildParams &p, cudaStream_t s) {
@@ -351,18 +386,15 @@ cudaError_t launch_build_gdn_prep(const BuildParams &p, cudaStream_t s) {
     if (!make_tmap_3d(&tmK, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_k, N, (uint64_t)D * 2,
                       (uint64_t)p.H_k * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(build_gdn_prep_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
+    cudaError_t e;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     // the ticket counter after the records (the workspace tail), zeroed for this launch
     e = cudaMemsetAsync(static_cast<uint8_t *>(p.workspace) + total * kGdnRecordBytes, 0, sizeof(unsigned), s);
     if (e != cudaSuccess) return e;
-    const int grid = (int)std::min<int64_t>(total, (int64_t)sms * kCtasPerSm);
-    build_gdn_prep_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, tmK);
-    return cudaGetLastError();
+    // pairs of value heads share a key head when the grouped-query factor is even
+    return p.gqa % 2 == 0 ? launch_prep<2>(p, total, tmK, sms, s) : launch_prep<1>(p, total, tmK, sms, s);
 }
 
 }  // namespace hypic

@@ -45,6 +45,16 @@ def test_build_parity_ragged(family, dtype, d):
 
 
 @pytest.mark.parametrize("family", ["gdn", "delta"])
+@pytest.mark.parametrize("H_k,H_v", [(3, 3), (1, 4), (2, 6)])
+def test_build_key_head_sharing(family, H_k, H_v):
+    """Grouped-query factors 1, 4 and 3: the tensor-core build's chunk preparation handles
+    the value heads of one key head two at a time when the factor is even, one at a time
+    otherwise."""
+    inp = synth.make_inputs(family, H_k, H_v, 128, RAGGED, torch.bfloat16, seed=47, alpha_scale=0.05)
+    check_build(inp)
+
+
+@pytest.mark.parametrize("family", ["gdn", "delta"])
 def test_build_more_units_than_sms(family):
     """More (segment, head) units than SMs, in several rounds per SM: 180 ragged segments
     (empty, one-token, one-chunk and multi-chunk) x 2 value heads through the tensor-core
