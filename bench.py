@@ -98,10 +98,17 @@ def aggregate_throughput(units_per_rank: float, max_seconds: float, world: int) 
 
 
 def src_hash(*names):
+    """Hash of the code of the named kernel sources: comments and blank lines do not count,
+    so that a recorded measurement stays valid across comment-only edits."""
+    import re
     h = hashlib.sha1()
     for n in names:
-        with open(os.path.join(ROOT, "linear_attention_state_gdn_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "linear_attention_state_gdn_gb300", "csrc", n)) as f:
+            text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+        for line in text.splitlines():
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()[:12]
 
 

@@ -15,13 +15,16 @@
 // the pair (S(C|0), T_C) that "Cut First-Token Latency by 3.25x: Introducing HYPIC ..."
 // (besthub.dev), paragraph "For linear layers", stores for DeltaNet / GDN layers.
 //
-// Persistent CTAs of 128 threads, four per SM. Records are handed out as tickets: a CTA
-// starts with two fixed records and takes each further one from a counter in the workspace
-// (zeroed before the launch), so CTAs that run faster take more records and all CTAs finish
-// within about one record of each other. The k tile of the next record is requested as soon
-// as the current gram has read the single k buffer, its gram is issued while two warps
-// finish the current inverse (two TMEM buffers), and b is loaded a record ahead, so loads
-// and grams overlap the inversions. A CTA that has drawn its last ticket lets the chain
+// Persistent CTAs of 128 threads. A unit of work is R records of one (segment, chunk): with
+// an even grouped-query factor R = 2, the two value heads of one key head, which share the k
+// tile, the gram and its shared-memory copy, and whose two inverses run side by side (three
+// CTAs per SM); otherwise R = 1 (four CTAs per SM). Units are handed out as tickets: a CTA
+// starts with two fixed units and takes each further one from a counter in the workspace
+// (zeroed before the launch), so CTAs that run faster take more units and all CTAs finish
+// within about one unit of each other. The k tile of the next unit is requested as soon as
+// the current gram has read the single k buffer, its gram is issued while the current
+// inverses finish (two TMEM buffers), and b is loaded a unit ahead, so loads and grams
+// overlap the inversions. A CTA that has drawn its last ticket lets the chain
 // kernel launch (programmatic dependent launch); the chain waits for this grid's completion
 // before it reads any record.
 //   1. TMA the chunk's k (two 128B-swizzled 64-channel halves); b masked past the segment end.
@@ -31,7 +34,8 @@
 //      blocks exact (forward substitution); the blocks right of the diagonal are not stored.
 //      A = Diag(b) L is never formed: b scales rows inside the consumers, and the strictly
 //      lower mask is the consumers' index range.
-//   4. N by 16 x 16 blocks: the four diagonal blocks by forward substitution (one warp each),
+//   4. N by 16 x 16 blocks: the four diagonal blocks by forward substitution (one warp each;
+//      lanes 0-15 solve the first record's columns, lanes 16-31 the second's),
 //      then the blocks below level by level, N_ab = -N_aa Diag(b_a) sum_{k=b}^{a-1} G_ak N_kb,
 //      as 16 x 8 half-blocks spread over the four warps. The 16 x 16 x 16 products run on
 //      the warp-level tensor-core MMA (m16n8k8, tf32 inputs, fp32 accumulation): tcgen05's
