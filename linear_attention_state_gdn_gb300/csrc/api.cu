@@ -152,27 +152,75 @@ int seg_pieces(int64_t len, int m) {
 }
 
 // Workspace of the split: piece outputs S, P (dense families only) [slots][H_v][d][d], lam
-// [slots][H_v] ([slots][H_v][d] for diagonal gates; rounded to 256 bytes), and one scan
-// buffer [max pieces][H_v][d][d] for the composition.
+// [slots][H_v] ([slots][H_v][d] for diagonal gates; rounded to 256 bytes), and for the scaled
+// families one scan buffer [max pieces][H_v][d][d] for the composition.
+//
+// A second, narrower case: a DeltaNet / GDN call whose units take several rounds of SMs with
+// a last round at most half full (16 segments x 32 heads on 152 SMs: 56 units in round four).
+// Its trailing segments (the shortest, equal in length, last in the caller's order, outputs
+// adjacent) are cut in two, so the last round runs half-length pieces, and all of their
+// pieces are composed back in one batched launch (pieces laid out [piece][segment][head]).
 struct SplitLayout {
     int m = 1, slots = 0, max_pieces = 1;
+    int tail_first = -1, tail_count = 0;   // batched halving of segments [first, first + count)
     size_t off_S = 0, off_P = 0, off_lam = 0, off_prefix = 0, bytes = 0;
+    int pieces(const hypic_build_args *a, int j) const {
+        if (tail_count > 0) return j >= tail_first && j < tail_first + tail_count ? 2 : 1;
+        return m > 1 ? seg_pieces(a->seg_offsets[j + 1] - a->seg_offsets[j], m) : 1;
+    }
 };
+
+// the trailing segments to halve, or 0 (see above)
+int gdn_tail_split(const hypic_build_args *a, int *first) {
+    if (a->family != HYPIC_FAM_DELTA && a->family != HYPIC_FAM_GDN) return 0;
+    if (a->out_seg_stride != 0 && a->out_seg_stride != a->H_v) return 0;
+    const int64_t units = (int64_t)a->n_seg * a->H_v;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (units <= sms) return 0;
+    const int64_t last = units - ((units + sms - 1) / sms - 1) * sms;   // units of the last round
+    if (2 * last > sms) return 0;
+    const int cnt = (int)((last + a->H_v - 1) / a->H_v);
+    if (cnt >= a->n_seg) return 0;
+    const int j0 = a->n_seg - cnt;
+    const int64_t len = a->seg_offsets[j0 + 1] - a->seg_offsets[j0];
+    if ((len + kGdnChunk - 1) / kGdnChunk < 2) return 0;
+    for (int j = 0; j < a->n_seg; ++j) {
+        const int64_t lj = a->seg_offsets[j + 1] - a->seg_offsets[j];
+        if (j >= j0 ? lj != len : lj < len) return 0;
+    }
+    *first = j0;
+    return cnt;
+}
 
 SplitLayout gdn_split_layout(const hypic_build_args *a, size_t base) {
     SplitLayout L;
     L.m = gdn_split_m(a);
-    if (L.m <= 1) return L;
-    for (int j = 0; j < a->n_seg; ++j) {
-        const int pj = seg_pieces(a->seg_offsets[j + 1] - a->seg_offsets[j], L.m);
-        if (pj > 1) {
-            L.slots += pj;
-            L.max_pieces = std::max(L.max_pieces, pj);
-        }
-    }
-    if (L.slots == 0) {
+    size_t prefix_units = 0;
+    if (L.m <= 1) {
         L.m = 1;
-        return L;
+        L.tail_count = gdn_tail_split(a, &L.tail_first);
+        if (L.tail_count == 0) return L;
+        L.slots = 2 * L.tail_count;
+        L.max_pieces = 2;
+        prefix_units = (size_t)L.slots * a->H_v;
+    } else {
+        for (int j = 0; j < a->n_seg; ++j) {
+            const int pj = seg_pieces(a->seg_offsets[j + 1] - a->seg_offsets[j], L.m);
+            if (pj > 1) {
+                L.slots += pj;
+                L.max_pieces = std::max(L.max_pieces, pj);
+            }
+        }
+        if (L.slots == 0) {
+            L.m = 1;
+            return L;
+        }
+        prefix_units = (size_t)L.max_pieces * a->H_v;
     }
     const size_t unit = (size_t)a->d_k * a->d_k * sizeof(float);
     const size_t su = (size_t)L.slots * a->H_v;
@@ -182,7 +230,9 @@ SplitLayout gdn_split_layout(const hypic_build_args *a, size_t base) {
     L.off_P = L.off_S + su * unit;
     L.off_lam = L.off_P + (dense ? su * unit : 0);
     L.off_prefix = L.off_lam + ((su * nl * sizeof(float) + 255) & ~(size_t)255);
-    L.bytes = L.off_prefix + (size_t)L.max_pieces * a->H_v * unit - base;
+    // dense pieces are composed straight into the outputs; only the scaled compose needs a
+    // scan buffer
+    L.bytes = L.off_prefix + (dense ? 0 : prefix_units * unit) - base;
     return L;
 }
 
@@ -320,7 +370,7 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
                                 ? (size_t)gdn_records(a) * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail
                                 : 0;
         split = gdn_split_layout(a, base);
-        if (split.m > 1) {
+        if (split.slots > 0) {
             uint8_t *ws = static_cast<uint8_t *>(a->workspace);
             p.S_piece = reinterpret_cast<float *>(ws + split.off_S);
             p.P_piece = reinterpret_cast<float *>(ws + split.off_P);
@@ -332,7 +382,7 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
     int32_t slot = 0;
     for (int j = 0; j < a->n_seg; ++j) {
         const int64_t st = a->seg_offsets[j], len = a->seg_offsets[j + 1] - st;
-        const int pj = split.m > 1 ? seg_pieces(len, split.m) : 1;
+        const int pj = split.pieces(a, j);
         if (pj == 1) {
             table.push_back(SegEntry{(int32_t)st, (int32_t)len, j, 0});
             continue;
@@ -341,8 +391,9 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
         for (int k = 0; k < pj; ++k) {
             const int64_t t0 = (k * nch / pj) * kGdnChunk;
             const int64_t t1 = std::min<int64_t>(((k + 1) * nch / pj) * kGdnChunk, len);
-            table.push_back(SegEntry{(int32_t)(st + t0), (int32_t)(t1 - t0), -1 - slot, 0});
-            ++slot;
+            // batched tail halves: slot [piece][segment]; otherwise a segment's pieces in a row
+            const int32_t sl = split.tail_count > 0 ? k * split.tail_count + (j - split.tail_first) : slot++;
+            table.push_back(SegEntry{(int32_t)(st + t0), (int32_t)(t1 - t0), -1 - sl, 0});
         }
     }
     if ((int64_t)table.size() > HYPIC_MAX_SEGMENTS) return HYPIC_ERR_UNSUPPORTED;   // not reached: splits need few units
@@ -361,7 +412,7 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
     case BuildPath::GdnTc:
     case BuildPath::GatedTc: {
         cudaError_t e = path == BuildPath::GdnTc ? launch_build_gdn_tc(p, s) : launch_build_gated_tc(p, s);
-        if (e != cudaSuccess || split.m <= 1) return from_cuda(e);
+        if (e != cudaSuccess || split.slots == 0) return from_cuda(e);
         // compose the pieces of every split segment into its entry: S = the pieces' prefix
         // scan from a zero state (its last state, copied out), lam = sum, P = product
         const bool dense = fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GDN;
@@ -369,9 +420,26 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
         const size_t nl = fam == HYPIC_FAM_DIAG ? (size_t)a->d_k : 1;
         const int64_t stride = p.seg_stride;
         float *prefix = reinterpret_cast<float *>(static_cast<uint8_t *>(a->workspace) + split.off_prefix);
+        if (split.tail_count > 0) {   // one launch for all halved segments (adjacent outputs)
+            const int64_t nu = (int64_t)split.tail_count * a->H_v;
+            ComposeParams q;
+            std::memset(&q, 0, sizeof(q));
+            q.family = fam;
+            q.n_seg = 2;
+            q.n_units = nu;
+            q.D = a->d_k;
+            q.S = p.S_piece;
+            q.lam = p.lam_piece;
+            q.P = p.P_piece;
+            q.prefix_last = a->S + (size_t)split.tail_first * a->H_v * unit;   // the segments' S
+            q.lam_total = a->lam + (size_t)split.tail_first * a->H_v;
+            q.P_total = a->P + (size_t)split.tail_first * a->H_v * unit;
+            q.err = err;
+            return from_cuda(launch_compose_dense_tc(q, s));
+        }
         int32_t slot0 = 0;
         for (int j = 0; j < a->n_seg && e == cudaSuccess; ++j) {
-            const int pj = seg_pieces(a->seg_offsets[j + 1] - a->seg_offsets[j], split.m);
+            const int pj = split.pieces(a, j);
             if (pj == 1) continue;
             ComposeParams q;
             std::memset(&q, 0, sizeof(q));
@@ -386,11 +454,16 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
             q.lam_total = a->lam + (size_t)j * stride * nl;
             q.P_total = dense ? a->P + (size_t)j * stride * unit : nullptr;
             q.err = err;
-            e = dense ? launch_compose_dense_tc(q, s) : launch_compose_scaled(q, s);
-            if (e == cudaSuccess) e = launch_compose_lam_total(q, s);
-            if (e == cudaSuccess)
-                e = cudaMemcpyAsync(a->S + (size_t)j * stride * unit, prefix + (size_t)(pj - 1) * a->H_v * unit,
-                                    (size_t)a->H_v * unit * sizeof(float), cudaMemcpyDeviceToDevice, s);
+            if (dense) {   // one launch: the last state straight into S, lam_total summed inside
+                q.prefix_last = a->S + (size_t)j * stride * unit;
+                e = launch_compose_dense_tc(q, s);
+            } else {
+                e = launch_compose_scaled(q, s);
+                if (e == cudaSuccess) e = launch_compose_lam_total(q, s);
+                if (e == cudaSuccess)
+                    e = cudaMemcpyAsync(a->S + (size_t)j * stride * unit, prefix + (size_t)(pj - 1) * a->H_v * unit,
+                                        (size_t)a->H_v * unit * sizeof(float), cudaMemcpyDeviceToDevice, s);
+            }
             slot0 += pj;
         }
         return from_cuda(e);
@@ -485,7 +558,8 @@ hypic_status hypic_compose_scan(const hypic_compose_args *a, void *stream) {
     case ComposePath::Scaled: e = launch_compose_scaled(p, s); break;
     case ComposePath::None: break;
     }
-    if (e == cudaSuccess && a->lam_total) e = launch_compose_lam_total(p, s);
+    // the dense tensor-core kernel sums lam_total itself
+    if (e == cudaSuccess && a->lam_total && pick_compose(a) != ComposePath::DenseTc) e = launch_compose_lam_total(p, s);
     return from_cuda(e);
 }
 

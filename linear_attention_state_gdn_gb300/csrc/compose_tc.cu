@@ -26,6 +26,8 @@
 // the chain Q_j = P_j Q_{j-1} from Q_0 = P_0 (loaded like an S tile) through the same
 // products, without S, without scaling, and write only Q_{n-1} = P_total of unit u - U:
 // the transition of the entry composed from all n segments is exp(sum_j lam_j) Q_{n-1}.
+// lam_total of the normal units is summed by their epilogue (thread 0, segment order). With
+// prefix_last (a build composing the pieces of its segments), only the last state is written.
 // Roles: warps 0-3 epilogue (one TMEM lane each), warp 4 TMA producer, warp 5 MMA issuer.
 // Every wait is bounded; on expiry the CTA records HYPIC_ERR_TIMEOUT, lets its in-flight
 // copies and MMAs finish (bounded), frees its TMEM and returns.
@@ -199,6 +201,7 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
         for (int ux = blockIdx.x; ux < UT && !abort_flag; ux += gridDim.x) {
             const bool tr = ux >= U;
             const int u = tr ? ux - U : ux;
+            float lsum = 0.f;   // thread 0 of a normal unit: sum of lam over the segments
             if (has_s0 && !tr) {
                 // A = split(exp(lam_0) S0^T) for the first step
                 const float sc0 = expf(p.lam[u]);
@@ -263,9 +266,12 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                 {
                     const bool next = j + 1 < NS;
                     const float scale_next = !next ? 0.f : tr ? 1.f : expf(p.lam[(int64_t)(j + 1) * U + u]);
-                    // prefix_j, or for the transition chain only its last state, P_total
+                    if (!tr && n == 0 && p.lam_total) lsum += p.lam[(int64_t)j * U + u];
+                    // prefix_j (only the last one with prefix_last), or for the transition chain
+                    // only its last state, P_total
                     float *out = tr ? (next ? nullptr : p.P_total + (int64_t)u * D * D + n)
-                                    : p.prefix + ((int64_t)j * U + u) * D * D + n;
+                               : p.prefix_last ? (next ? nullptr : p.prefix_last + (int64_t)u * D * D + n)
+                                               : p.prefix + ((int64_t)j * U + u) * D * D + n;
                     for (int c = 0; c < 8; ++c) {
                         uint32_t r[16];
                         if (mma) {
@@ -296,6 +302,7 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                     }
                 }
             }
+            if (!tr && n == 0 && p.lam_total) p.lam_total[u] = lsum;
         }
     epi_done:;
     }

@@ -73,6 +73,8 @@ struct ComposeParams {
     float *prefix;
     float *lam_total;   // optional: sum_j lam_j per unit (per key row for DIAG)
     float *P_total;     // optional, dense families: P_{n-1} ... P_0 per unit
+    float *prefix_last; // dense tensor-core compose, internal use: write only the last state,
+                        // [n_units][d][d], instead of prefix
     unsigned *err;
 };
 

@@ -85,6 +85,15 @@ def test_build_split_segments(family, per_token, lens):
     check_build(inp)
 
 
+@pytest.mark.parametrize("family", ["gdn", "delta"])
+def test_build_halved_trailing_segments(family):
+    """A call whose units take two rounds of SMs with a nearly empty second round (80 equal
+    segments x 2 heads = 160 units): its last segments are built as halves and composed back
+    in one batched launch."""
+    inp = synth.make_inputs(family, 1, 2, 128, [130] * 80, torch.bfloat16, seed=48, alpha_scale=0.05)
+    check_build(inp)
+
+
 def test_build_scalar_per_token_gate():
     inp = synth.make_inputs("scalar", 2, 2, 128, [300, 77], torch.bfloat16, seed=41,
                             per_token_scalar=True)
