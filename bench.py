@@ -38,6 +38,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GDN (S,T_C) build tokens/s + compose/scan GB/s, % of GB300 roofline"
+# sources whose code the recorded build traffic belongs to (the launches and how the call
+# splits and merges segments)
+TRAFFIC_SOURCES = ["build_gdn_prep.cu", "build_gdn_tc.cu", "compose_tc.cu", "api.cu"]
 UNIT = "tokens/s"
 CHUNK = 64
 L2_FLUSH_BYTES = 256 << 20
@@ -534,9 +537,23 @@ def e2e_measure(inp, steps=5, warmup=2, groups=4):
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "groups": len(grp)}
 
 
-def build_launches(kernel_name):
-    """Kernel launches of one hypic_build_segments call on the path `kernel_name`."""
-    return 2 if kernel_name == "build_gdn_tc" else 1
+def build_split(hy, inp, dev):
+    """True when the tensor-core GDN build of `inp` splits segments into pieces (its workspace
+    then holds more than the chunk records and their 256-byte tail)."""
+    need = hy.hypic_build_workspace_bytes(inp.family, dev["k"], dev["v"], inp.seg_offsets,
+                                          log_gate=dev.get("log_gate"), beta=dev.get("beta"))
+    records = sum((int(b - a) + CHUNK - 1) // CHUNK for a, b in
+                  zip(inp.seg_offsets[:-1], inp.seg_offsets[1:])) * inp.H_v
+    return need > records * CHUNK * CHUNK * 2 + 256
+
+
+def build_launches(kernel_name, split=False):
+    """Kernel launches of one hypic_build_segments call on the path `kernel_name`: the GDN
+    tensor-core build is the chunk preparation and the chain, plus one compose launch that
+    merges pieces when the call splits segments (the 16-segment workload halves its last two)."""
+    if kernel_name == "build_gdn_tc":
+        return 3 if split else 2
+    return 1
 
 
 def run_main(args):
@@ -601,14 +618,16 @@ def run_main(args):
                 "unit": "TFLOP/s",
                 "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 flop x max SM clock"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    # the tensor-core GDN build is one call of two launches (chunk preparation, then the
-    # chain); the events bracket the call, so the roofline covers both
-    roof["kernel"] = "build_gdn_prep + build_gdn_tc" if bk == "build_gdn_tc" else bk
+    # the tensor-core GDN build is one call of two or three launches (chunk preparation, the
+    # chain, and the compose merging halved segments); the events bracket the call, so the
+    # roofline covers all of them
+    split = tensor_path and build_split(hy, inp, st.dev)
+    roof["kernel"] = ("build_gdn_prep + build_gdn_tc" + (" + compose_dense_tc (merge)" if split else "")
+                      if bk == "build_gdn_tc" else bk)
     roof["algorithmic_flop_per_launch"] = flops
     roof["algorithmic_bytes_per_launch"] = nbytes
     roof["achieved_gbs"] = round(nbytes / (b_ms * 1e-3) / 1e9, 1)
-    roof["traffic"] = recorded_traffic(bk, ["build_gdn_prep.cu", "build_gdn_tc.cu"] if tensor_path else
-                                       ["build_simt.cu"])
+    roof["traffic"] = recorded_traffic(bk, TRAFFIC_SOURCES if tensor_path else ["build_simt.cu"])
     comp_bytes = compose_algorithmic_bytes(inp.n_seg, inp.H_v, inp.d_k, True)
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -620,7 +639,7 @@ def run_main(args):
             "compose_gbs": round(comp_bytes / (c_ms * 1e-3) / 1e9, 1),
             "compose_hbm_frac": round(comp_bytes / (c_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
             "kernels": {"build": bk, "compose": ck},
-            "gpu_launches": (build_launches(bk) + 1) * args.steps,
+            "gpu_launches": (build_launches(bk, split) + 1) * args.steps,
             "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
             "clock_samples": clocks["samples"], "wall_s_timed_region": round(wall, 3),
             "peaks": pk}
