@@ -68,6 +68,9 @@ __device__ __forceinline__ void st_stream(float *p, float v) {
     asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
+// FUSED: lam_total summed here and prefix_last honoured (compiled separately, so that the
+// plain scan's code is unchanged)
+template <bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
 compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                         const __grid_constant__ CUtensorMap tmP,
@@ -266,11 +269,11 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                 {
                     const bool next = j + 1 < NS;
                     const float scale_next = !next ? 0.f : tr ? 1.f : expf(p.lam[(int64_t)(j + 1) * U + u]);
-                    if (!tr && n == 0 && p.lam_total) lsum += p.lam[(int64_t)j * U + u];
+                    if (FUSED && !tr && n == 0 && p.lam_total) lsum += p.lam[(int64_t)j * U + u];
                     // prefix_j (only the last one with prefix_last), or for the transition chain
                     // only its last state, P_total
                     float *out = tr ? (next ? nullptr : p.P_total + (int64_t)u * D * D + n)
-                               : p.prefix_last ? (next ? nullptr : p.prefix_last + (int64_t)u * D * D + n)
+                               : (FUSED && p.prefix_last) ? (next ? nullptr : p.prefix_last + (int64_t)u * D * D + n)
                                                : p.prefix + ((int64_t)j * U + u) * D * D + n;
                     for (int c = 0; c < 8; ++c) {
                         uint32_t r[16];
@@ -302,7 +305,7 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                     }
                 }
             }
-            if (!tr && n == 0 && p.lam_total) p.lam_total[u] = lsum;
+            if (FUSED && !tr && n == 0 && p.lam_total) p.lam_total[u] = lsum;
         }
     epi_done:;
     }
@@ -341,12 +344,14 @@ cudaError_t launch_compose_dense_tc(const ComposeParams &p, cudaStream_t s) {
         !make_tmap_2d(&tmQ, pbase, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, rows, D * 4, 128, 128,
                       CU_TENSOR_MAP_SWIZZLE_NONE))   // P_0 read whole, like an S tile
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(compose_dense_tc_kernel,
+    const bool fused = p.lam_total != nullptr || p.prefix_last != nullptr;
+    auto kern = fused ? compose_dense_tc_kernel<true> : compose_dense_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     const int64_t units = p.n_units * (p.P_total ? 2 : 1);
     const int grid = (int)std::min<int64_t>(units, sm_count());
-    compose_dense_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(p, tmP, tmS, tmQ);
+    kern<<<grid, kThreads, kSmemBytes, s>>>(p, tmP, tmS, tmQ);
     return cudaGetLastError();
 }
 
