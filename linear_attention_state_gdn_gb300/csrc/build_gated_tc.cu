@@ -41,23 +41,26 @@ constexpr int kThreads = 320;        // 8 state/decay warps, producer, MMA issue
 constexpr int kEpi = 256;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kStages = 3;
+// TMA ring depth: 3 stages at two CTAs per SM; 6 at one CTA per SM (calls with at most one
+// unit per SM), whose single CTA needs more bytes in flight to keep HBM busy
+// (RetNet, 128 units: 47.9 -> 42.0 us).
 constexpr uint32_t kTmemCols = 256;   // two 128-column accumulators
 
 enum { kLinear = 0, kScalar = 1, kDiag = 2 };
 
-template <int KIND>
+template <int KIND, int STAGES>
 struct Geo {
     static constexpr int C = KIND == kDiag ? 32 : 64;          // tokens per chunk
     static constexpr uint32_t kHalf = C * 128;                  // 64 channels x C tokens, bf16
     static constexpr uint32_t kKV = 2 * kHalf;                  // one k (or v) chunk
     static constexpr uint32_t kG = KIND == kDiag ? C * D * 4 : 0;
     static constexpr uint32_t kStage = 2 * kKV + kG;
-    static constexpr uint32_t kSmem = kStages * kStage + 1024;
+    static constexpr uint32_t kSmem = STAGES * kStage + 1024;
 };
 
+template <int STAGES>
 struct Bars {
-    uint64_t full[kStages], kready[kStages], empty[kStages], dfull[2], dfree[2], fin;
+    uint64_t full[STAGES], kready[STAGES], empty[STAGES], dfull[2], dfree[2], fin;
 };
 
 // Named barrier of the 256 decay / state threads, plain and with an AND of a predicate (every
@@ -80,17 +83,18 @@ __device__ __forceinline__ bool bar_state_and(bool v) {
     return r != 0;
 }
 
-template <int KIND>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int KIND, int STAGES>
+__global__ void __launch_bounds__(kThreads, STAGES == 3 ? 2 : 1)
 build_gated_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG) {
-    using G = Geo<KIND>;
+    constexpr int kStages = STAGES;
+    using G = Geo<KIND, STAGES>;
     constexpr int C = G::C;
     extern __shared__ uint8_t smem_raw[];
     // 1024-aligned base, derived by offsetting the shared array itself so that the
     // compiler keeps the shared address space (plain ld/st.shared, not generic accesses)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    __shared__ Bars bars;
+    __shared__ Bars<STAGES> bars;
     __shared__ uint32_t tslot;
     __shared__ volatile int abort_flag;
     __shared__ __align__(16) float fac[kStages][64];   // per-token decay factors (linear / scalar)
@@ -322,9 +326,9 @@ build_gated_tc_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     }
 }
 
-template <int KIND>
+template <int KIND, int STAGES>
 cudaError_t launch_kind(const BuildParams &p, cudaStream_t s) {
-    using G = Geo<KIND>;
+    using G = Geo<KIND, STAGES>;
     const int64_t N = p.n_tok > 0 ? p.n_tok : 1;
     CUtensorMap tmK, tmV, tmG;
     if (!make_tmap_3d(&tmK, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_k, N, (uint64_t)D * 2,
@@ -340,12 +344,12 @@ cudaError_t launch_kind(const BuildParams &p, cudaStream_t s) {
     } else {
         tmG = tmV;   // unused
     }
-    cudaError_t e = cudaFuncSetAttribute(build_gated_tc_kernel<KIND>,
+    cudaError_t e = cudaFuncSetAttribute(build_gated_tc_kernel<KIND, STAGES>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, G::kSmem);
     if (e != cudaSuccess) return e;
     const int blocks = p.n_seg * p.H_v;
     if (blocks == 0) return cudaSuccess;
-    build_gated_tc_kernel<KIND><<<blocks, kThreads, G::kSmem, s>>>(p, tmK, tmV, tmG);
+    build_gated_tc_kernel<KIND, STAGES><<<blocks, kThreads, G::kSmem, s>>>(p, tmK, tmV, tmG);
     return cudaGetLastError();
 }
 
@@ -358,10 +362,15 @@ bool build_gated_tc_supported(const BuildParams &p) {
 }
 
 cudaError_t launch_build_gated_tc(const BuildParams &p, cudaStream_t s) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const bool deep = (int64_t)p.n_seg * p.H_v <= sms;   // at most one unit per SM
     switch (p.family) {
-    case HYPIC_FAM_LINEAR: return launch_kind<kLinear>(p, s);
-    case HYPIC_FAM_SCALAR: return launch_kind<kScalar>(p, s);
-    case HYPIC_FAM_DIAG: return launch_kind<kDiag>(p, s);
+    case HYPIC_FAM_LINEAR: return deep ? launch_kind<kLinear, 6>(p, s) : launch_kind<kLinear, 3>(p, s);
+    case HYPIC_FAM_SCALAR: return deep ? launch_kind<kScalar, 6>(p, s) : launch_kind<kScalar, 3>(p, s);
+    case HYPIC_FAM_DIAG: return deep ? launch_kind<kDiag, 6>(p, s) : launch_kind<kDiag, 3>(p, s);
     }
     return cudaErrorInvalidValue;
 }
