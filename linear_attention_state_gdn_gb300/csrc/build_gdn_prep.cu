@@ -58,8 +58,16 @@ using namespace ptx;
 constexpr int D = 128;
 constexpr int C = kGdnChunk;
 constexpr int kThreads = 128;
-constexpr uint32_t kLDA = 68;                            // padded fp32 row stride
-constexpr uint32_t kLDT = 12;                            // per-warp 16 x 8 scratch, padded rows
+// Shared-memory layouts, chosen so that the warp-level MMA fragments, the 16 x 8 result stores
+// and the record stores touch 32 distinct banks:
+//   G (only ever an A operand): rows padded to 68 floats;
+//   N (A operand for its diagonal blocks, B operand below them): rows of 72 floats with element
+//   (r, c) at column c ^ (r & 4), and the second record 16 banks after the first;
+//   the per-warp 16 x 8 scratch (a B operand): unpadded rows of 8.
+constexpr uint32_t kLDA = 68;
+constexpr uint32_t kLDN = 72;
+constexpr uint32_t kNRec = 64 * kLDN + 16;
+constexpr uint32_t kLDT = 8;
 // R records per iteration: the value heads h, h + 1 that share a key head (R = 2, when the
 // grouped-query factor is even) share the k tile, the gram and its shared-memory copy, and
 // their two inverses run side by side; R = 1 otherwise.
@@ -67,8 +75,8 @@ template <int R>
 struct PrepGeo {
     static constexpr uint32_t kOffK = 0;                              // k tile, 16 KB
     static constexpr uint32_t kOffG32 = 16384;                        // the gram K K^T, 64 x 68
-    static constexpr uint32_t kOffN32 = kOffG32 + 64 * kLDA * 4;      // R x N (tf32-rounded), 64 x 68
-    static constexpr uint32_t kOffT = kOffN32 + R * 64 * kLDA * 4;    // 4 warps x 16 x 12 fp32
+    static constexpr uint32_t kOffN32 = kOffG32 + 64 * kLDA * 4;      // R x N (tf32-rounded), kNRec each
+    static constexpr uint32_t kOffT = kOffN32 + R * kNRec * 4;        // 4 warps x 16 x 8 fp32
     static constexpr uint32_t kSmemBytes = kOffT + 4 * 16 * kLDT * 4 + 1024;
     static constexpr int kCtasPerSm = R == 1 ? 4 : 3;
 };
@@ -83,19 +91,23 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
 // x rounded to tf32 (round to nearest), kept as a float with the low 13 mantissa bits zero
 __device__ __forceinline__ float tf32r(float x) { return __uint_as_float(to_tf32(x)); }
 
-// c (16 x 8, m16n8 accumulator layout) += X[xr.., xc..] (16 x 16) * Y[yr.., yc..] (16 x 8);
-// X and Y row-major in shared memory with row strides ldx, ldy, holding tf32-rounded values.
+// c (16 x 8, m16n8 accumulator layout) += X (16 x 16) * Y (16 x 8); X and Y row-major in shared
+// memory with row strides ldx, ldy, holding tf32-rounded values, each at a block offset that is
+// a multiple of 8 rows and 8 columns; XS / YS: that matrix has N's column swizzle (c ^ (r & 4)).
+template <bool XS, bool YS>
 __device__ __forceinline__ void mma16x8x16(float (&c)[4], const float *X, int ldx, const float *Y, int ldy,
                                            int lane) {
     const int g = lane >> 2, t = lane & 3;
+    const int sx = XS ? (g & 4) : 0;   // rows g and g + 8 share it
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-        const uint32_t a0 = __float_as_uint(X[g * ldx + 8 * ks + t]);
-        const uint32_t a1 = __float_as_uint(X[(g + 8) * ldx + 8 * ks + t]);
-        const uint32_t a2 = __float_as_uint(X[g * ldx + 8 * ks + t + 4]);
-        const uint32_t a3 = __float_as_uint(X[(g + 8) * ldx + 8 * ks + t + 4]);
-        const uint32_t b0 = __float_as_uint(Y[(8 * ks + t) * ldy + g]);
-        const uint32_t b1 = __float_as_uint(Y[(8 * ks + t + 4) * ldy + g]);
+        const int c0 = (8 * ks + t) ^ sx, c1 = (8 * ks + t + 4) ^ sx;
+        const uint32_t a0 = __float_as_uint(X[g * ldx + c0]);
+        const uint32_t a1 = __float_as_uint(X[(g + 8) * ldx + c0]);
+        const uint32_t a2 = __float_as_uint(X[g * ldx + c1]);
+        const uint32_t a3 = __float_as_uint(X[(g + 8) * ldx + c1]);
+        const uint32_t b0 = __float_as_uint(Y[(8 * ks + t) * ldy + g]);                    // r & 4 == 0
+        const uint32_t b1 = __float_as_uint(Y[(8 * ks + t + 4) * ldy + (YS ? g ^ 4 : g)]);  // r & 4 == 4
         asm volatile(
             "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
             "{%0,%1,%2,%3};"
@@ -112,20 +124,17 @@ __device__ __forceinline__ void half_block(const float *G32, float *N32, float *
     const int g = lane >> 2, t = lane & 3;
     float c[4] = {0.f, 0.f, 0.f, 0.f};
     for (int k = b; k < a; ++k)
-        mma16x8x16(c, G32 + 16 * a * kLDA + 16 * k, kLDA, N32 + 16 * k * kLDA + 16 * b + 8 * hh, kLDA, lane);
+        mma16x8x16<false, true>(c, G32 + 16 * a * kLDA + 16 * k, kLDA, N32 + 16 * k * kLDN + 16 * b + 8 * hh, kLDN,
+                                lane);
     const float b0 = bv[16 * a + g], b1 = bv[16 * a + g + 8];
-    Tw[g * kLDT + 2 * t] = tf32r(c[0] * b0);
-    Tw[g * kLDT + 2 * t + 1] = tf32r(c[1] * b0);
-    Tw[(g + 8) * kLDT + 2 * t] = tf32r(c[2] * b1);
-    Tw[(g + 8) * kLDT + 2 * t + 1] = tf32r(c[3] * b1);
+    *reinterpret_cast<float2 *>(Tw + g * kLDT + 2 * t) = make_float2(tf32r(c[0] * b0), tf32r(c[1] * b0));
+    *reinterpret_cast<float2 *>(Tw + (g + 8) * kLDT + 2 * t) = make_float2(tf32r(c[2] * b1), tf32r(c[3] * b1));
     __syncwarp();
     float d[4] = {0.f, 0.f, 0.f, 0.f};
-    mma16x8x16(d, N32 + 16 * a * kLDA + 16 * a, kLDA, Tw, kLDT, lane);
-    float *o = N32 + 16 * a * kLDA + 16 * b + 8 * hh;
-    o[g * kLDA + 2 * t] = tf32r(-d[0]);
-    o[g * kLDA + 2 * t + 1] = tf32r(-d[1]);
-    o[(g + 8) * kLDA + 2 * t] = tf32r(-d[2]);
-    o[(g + 8) * kLDA + 2 * t + 1] = tf32r(-d[3]);
+    mma16x8x16<true, false>(d, N32 + 16 * a * kLDN + 16 * a, kLDN, Tw, kLDT, lane);
+    float *o = N32 + 16 * a * kLDN + 16 * b + 8 * hh + ((2 * t) ^ (g & 4));
+    *reinterpret_cast<float2 *>(o + g * kLDN) = make_float2(tf32r(-d[0]), tf32r(-d[1]));
+    *reinterpret_cast<float2 *>(o + (g + 8) * kLDN) = make_float2(tf32r(-d[2]), tf32r(-d[3]));
     __syncwarp();   // Tw is reused by this warp's next half-block
 }
 
@@ -169,7 +178,7 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     __shared__ uint32_t tslot;
     __shared__ int s_ok;
     __shared__ Walk s_n2[2];   // the unit after `nxt`, drawn by thread kCtl (two slots)
-    __shared__ __align__(16) float vb[2][R][C];
+    __shared__ __align__(16) float vb[2][R][C + 4];   // padded: the two records' b in different banks
 
     const int64_t total = total_records(p), units = total / R;
     unsigned *tickets = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(p.workspace) + total * kGdnRecordBytes);
@@ -178,7 +187,7 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     if (cur.r >= p.n_seg) return;   // uniform: the whole CTA leaves before any set-up
     const int q = threadIdx.x, warp = q >> 5, lane = q & 31;
     float *G32 = reinterpret_cast<float *>(smem + G::kOffG32);
-    float *N32 = reinterpret_cast<float *>(smem + G::kOffN32);   // record rr at N32 + rr * 64 * kLDA
+    float *N32 = reinterpret_cast<float *>(smem + G::kOffN32);   // record rr at N32 + rr * kNRec
     float *Tw = reinterpret_cast<float *>(smem + G::kOffT) + warp * 16 * kLDT;
 
     if (q == 0) {
@@ -282,7 +291,7 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         if (R == 2 || lane < 16) {
             const int a = warp, j = lane & 15, rr_ = lane >> 4;
             const float *bv = vb[b][rr_];
-            float *Nr = N32 + rr_ * 64 * kLDA;
+            float *Nr = N32 + rr_ * kNRec;
             float x[16];
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
@@ -299,7 +308,7 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
                 x[rr] = fmaf(-bv[16 * a + rr], (acc[0] + acc[1]) + (acc[2] + acc[3]), (rr == j) ? 1.f : 0.f);
             }
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) Nr[(16 * a + rr) * kLDA + 16 * a + j] = tf32r(x[rr]);
+            for (int rr = 0; rr < 16; ++rr) Nr[(16 * a + rr) * kLDN + ((16 * a + j) ^ (rr & 4))] = tf32r(x[rr]);
         }
         __syncthreads();
         // level 1: (1,0), (2,1), (3,2) as six half-blocks; level 2: (2,0), (3,1); level 3: (3,0).
@@ -307,17 +316,17 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         // Each half-block is done for every record of the unit.
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
-            half_block(G32, N32 + rr * 64 * kLDA, Tw, vb[b][rr], 1 + (warp >> 1), warp >> 1, warp & 1, lane);
-            if (warp >= 2) half_block(G32, N32 + rr * 64 * kLDA, Tw, vb[b][rr], 3, 2, warp & 1, lane);
+            half_block(G32, N32 + rr * kNRec, Tw, vb[b][rr], 1 + (warp >> 1), warp >> 1, warp & 1, lane);
+            if (warp >= 2) half_block(G32, N32 + rr * kNRec, Tw, vb[b][rr], 3, 2, warp & 1, lane);
         }
         __syncthreads();
 #pragma unroll
         for (int rr = 0; rr < R; ++rr)
-            half_block(G32, N32 + rr * 64 * kLDA, Tw, vb[b][rr], 2 + (warp >> 1), warp >> 1, warp & 1, lane);
+            half_block(G32, N32 + rr * kNRec, Tw, vb[b][rr], 2 + (warp >> 1), warp >> 1, warp & 1, lane);
         __syncthreads();
         if (warp < 2) {
 #pragma unroll
-            for (int rr = 0; rr < R; ++rr) half_block(G32, N32 + rr * 64 * kLDA, Tw, vb[b][rr], 3, 0, warp, lane);
+            for (int rr = 0; rr < R; ++rr) half_block(G32, N32 + rr * kNRec, Tw, vb[b][rr], 3, 0, warp, lane);
         }
         // warps 2-3 have no level-3 work: the next record's gram (its k tile was requested at
         // the top of this iteration) into the other TMEM buffer, last read a record ago
@@ -335,17 +344,21 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
             const int rr = m / 4;
             uint8_t *dst = static_cast<uint8_t *>(p.workspace) +
                            ((int64_t)seg.wsb + (int64_t)(cur.h + rr) * nch + cur.c) * (int64_t)kGdnRecordBytes;
-            const float *Nr = N32 + rr * 64 * kLDA;
+            const float *Nr = N32 + rr * kNRec;
             const int e8 = q + 128 * (m & 3);   // 8 consecutive entries of row t'
             const int tp = e8 >> 3, s8 = (e8 & 7) * 8;
             uint4 pk = make_uint4(0u, 0u, 0u, 0u);
             if ((s8 >> 4) <= (tp >> 4)) {
-                const float4 lo = reinterpret_cast<const float4 *>(Nr + tp * kLDA + s8)[0];
-                const float4 hi = reinterpret_cast<const float4 *>(Nr + tp * kLDA + s8)[1];
-                const float4 b0 = reinterpret_cast<const float4 *>(vb[b][rr] + s8)[0];
-                const float4 b1 = reinterpret_cast<const float4 *>(vb[b][rr] + s8)[1];
-                pk = make_uint4(pack_bf16x2(lo.x * b0.x, lo.y * b0.y), pack_bf16x2(lo.z * b0.z, lo.w * b0.w),
-                                pack_bf16x2(hi.x * b1.x, hi.y * b1.y), pack_bf16x2(hi.z * b1.z, hi.w * b1.w));
+                // the eight lanes of a row read the two halves of their 8 entries in opposite
+                // orders, so that each load instruction covers all 32 banks
+                const int h0 = e8 & 4, h1 = h0 ^ 4, sw = tp & 4;
+                const float4 x0 = *reinterpret_cast<const float4 *>(Nr + tp * kLDN + ((s8 + h0) ^ sw));
+                const float4 x1 = *reinterpret_cast<const float4 *>(Nr + tp * kLDN + ((s8 + h1) ^ sw));
+                const float4 b0 = *reinterpret_cast<const float4 *>(vb[b][rr] + s8 + h0);
+                const float4 b1 = *reinterpret_cast<const float4 *>(vb[b][rr] + s8 + h1);
+                const uint32_t p0 = pack_bf16x2(x0.x * b0.x, x0.y * b0.y), p1 = pack_bf16x2(x0.z * b0.z, x0.w * b0.w);
+                const uint32_t p2 = pack_bf16x2(x1.x * b1.x, x1.y * b1.y), p3 = pack_bf16x2(x1.z * b1.z, x1.w * b1.w);
+                pk = h0 == 0 ? make_uint4(p0, p1, p2, p3) : make_uint4(p2, p3, p0, p1);
             }
             *reinterpret_cast<uint4 *>(dst + tp * 128 + s8 * 2) = pk;
         }
