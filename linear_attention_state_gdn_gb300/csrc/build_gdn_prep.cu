@@ -17,8 +17,9 @@
 //
 // Persistent CTAs of 128 threads. A unit of work is R records of one (segment, chunk): with
 // an even grouped-query factor R = 2, the two value heads of one key head, which share the k
-// tile, the gram and its shared-memory copy, and whose two inverses run side by side (three
-// CTAs per SM); otherwise R = 1 (four CTAs per SM). Units are handed out as tickets: a CTA
+// tile, the gram and its shared-memory copy, and whose two inverses run side by side;
+// otherwise R = 1. Four CTAs per SM (all 512 TMEM columns, about 52 KB of shared memory and at
+// most 128 registers each). Units are handed out as tickets: a CTA
 // starts with two fixed units and takes each further one from a counter in the workspace
 // (zeroed before the launch), so CTAs that run faster take more units and all CTAs finish
 // within about one unit of each other. The k tile of the next unit is requested as soon as
@@ -29,9 +30,9 @@
 // before it reads any record.
 //   1. TMA the chunk's k (two 128B-swizzled 64-channel halves); b masked past the segment end.
 //   2. One thread issues the gram K K^T (M = 64 tcgen05 MMA, fp32 accumulator in TMEM).
-//   3. The raw gram G = K K^T in shared memory (rows padded to 68 floats): the blocks left of
-//      the diagonal rounded to tf32 once (they are only ever MMA operands), the diagonal
-//      blocks exact (forward substitution); the blocks right of the diagonal are not stored.
+//   3. The raw gram G = K K^T in shared memory, 16 x 16 blocks: the blocks left of the
+//      diagonal rounded to tf32 once (they are only ever MMA operands), the diagonal blocks
+//      exact (forward substitution); the blocks right of the diagonal are not stored.
 //      A = Diag(b) L is never formed: b scales rows inside the consumers, and the strictly
 //      lower mask is the consumers' index range.
 //   4. N by 16 x 16 blocks: the four diagonal blocks by forward substitution (one warp each;
@@ -58,27 +59,34 @@ using namespace ptx;
 constexpr int D = 128;
 constexpr int C = kGdnChunk;
 constexpr int kThreads = 128;
-// Shared-memory layouts, chosen so that the warp-level MMA fragments, the 16 x 8 result stores
-// and the record stores touch 32 distinct banks:
-//   G (only ever an A operand): rows padded to 68 floats;
-//   N (A operand for its diagonal blocks, B operand below them): rows of 72 floats with element
-//   (r, c) at column c ^ (r & 4), and the second record 16 banks after the first;
-//   the per-warp 16 x 8 scratch (a B operand): unpadded rows of 8.
-constexpr uint32_t kLDA = 68;
-constexpr uint32_t kLDN = 72;
-constexpr uint32_t kNRec = 64 * kLDN + 16;
-constexpr uint32_t kLDT = 8;
+// Shared-memory layout of G and N: only the ten 16 x 16 blocks on and below the diagonal are
+// stored, block (a, b) at word kBlk (a (a + 1) / 2 + b), and element (r, c) of a block at
+// 16 r + (c ^ sw(r)). The swizzle makes the warp-level MMA's A fragments (8 rows x 4 columns),
+// its B fragments (4 rows x 8 columns), the 16 x 8 result stores and the row-wise accesses
+// each touch 32 distinct banks. The 8 words after each block put the blocks of one row in
+// different banks (record stage) and start N's second record 16 banks after the first (the two
+// records' diagonal solves store side by side). The per-warp 16 x 8 scratch (a B operand) has
+// unpadded rows of 8.
+constexpr int kBlk = 264;
+constexpr int kTri = 10 * kBlk;   // one matrix
+constexpr int kLDT = 8;
+__device__ __forceinline__ int sw(int r) { return ((r << 2) & 8) | (r & 4); }
+__device__ __forceinline__ int blk(int a, int b) { return kBlk * (a * (a + 1) / 2 + b); }
+// b of a record: entry e at vbi(e), 16 words of padding after the first 32 entries, so that the
+// record stage's loads of b touch distinct banks
+constexpr int kVb = 80;
+__device__ __forceinline__ int vbi(int e) { return e + ((e >> 5) << 4); }
 // R records per iteration: the value heads h, h + 1 that share a key head (R = 2, when the
 // grouped-query factor is even) share the k tile, the gram and its shared-memory copy, and
 // their two inverses run side by side; R = 1 otherwise.
 template <int R>
 struct PrepGeo {
     static constexpr uint32_t kOffK = 0;                              // k tile, 16 KB
-    static constexpr uint32_t kOffG32 = 16384;                        // the gram K K^T, 64 x 68
-    static constexpr uint32_t kOffN32 = kOffG32 + 64 * kLDA * 4;      // R x N (tf32-rounded), kNRec each
-    static constexpr uint32_t kOffT = kOffN32 + R * kNRec * 4;        // 4 warps x 16 x 8 fp32
+    static constexpr uint32_t kOffG32 = 16384;                        // the gram K K^T, 10 blocks
+    static constexpr uint32_t kOffN32 = kOffG32 + kTri * 4;           // R x N (tf32-rounded), 10 blocks each
+    static constexpr uint32_t kOffT = kOffN32 + R * kTri * 4;         // 4 warps x 16 x 8 fp32
     static constexpr uint32_t kSmemBytes = kOffT + 4 * 16 * kLDT * 4 + 1024;
-    static constexpr int kCtasPerSm = R == 1 ? 4 : 3;
+    static constexpr int kCtasPerSm = 4;                              // 4 x 128 TMEM columns
 };
 constexpr int kCtl = 96;   // warp 3 lane 0 issues loads and grams (warp 3 has the least level work)
 
@@ -91,23 +99,24 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
 // x rounded to tf32 (round to nearest), kept as a float with the low 13 mantissa bits zero
 __device__ __forceinline__ float tf32r(float x) { return __uint_as_float(to_tf32(x)); }
 
-// c (16 x 8, m16n8 accumulator layout) += X (16 x 16) * Y (16 x 8); X and Y row-major in shared
-// memory with row strides ldx, ldy, holding tf32-rounded values, each at a block offset that is
-// a multiple of 8 rows and 8 columns; XS / YS: that matrix has N's column swizzle (c ^ (r & 4)).
-template <bool XS, bool YS>
-__device__ __forceinline__ void mma16x8x16(float (&c)[4], const float *X, int ldx, const float *Y, int ldy,
-                                           int lane) {
+// c (16 x 8, m16n8 accumulator layout) += X (16 x 16) * Y[:, yc .. yc + 7] (16 x 8), holding
+// tf32-rounded values: X a swizzled block; Y a swizzled block (YS) or the unswizzled 16 x 8
+// scratch (row stride kLDT, yc = 0).
+template <bool YS>
+__device__ __forceinline__ void mma16x8x16(float (&c)[4], const float *X, const float *Y, int yc, int lane) {
     const int g = lane >> 2, t = lane & 3;
-    const int sx = XS ? (g & 4) : 0;   // rows g and g + 8 share it
+    const int sx = sw(g);   // rows g and g + 8 share it
+    constexpr int ldy = YS ? 16 : kLDT;
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
         const int c0 = (8 * ks + t) ^ sx, c1 = (8 * ks + t + 4) ^ sx;
-        const uint32_t a0 = __float_as_uint(X[g * ldx + c0]);
-        const uint32_t a1 = __float_as_uint(X[(g + 8) * ldx + c0]);
-        const uint32_t a2 = __float_as_uint(X[g * ldx + c1]);
-        const uint32_t a3 = __float_as_uint(X[(g + 8) * ldx + c1]);
-        const uint32_t b0 = __float_as_uint(Y[(8 * ks + t) * ldy + g]);                    // r & 4 == 0
-        const uint32_t b1 = __float_as_uint(Y[(8 * ks + t + 4) * ldy + (YS ? g ^ 4 : g)]);  // r & 4 == 4
+        const int r0 = 8 * ks + t, r1 = r0 + 4;
+        const uint32_t a0 = __float_as_uint(X[g * 16 + c0]);
+        const uint32_t a1 = __float_as_uint(X[(g + 8) * 16 + c0]);
+        const uint32_t a2 = __float_as_uint(X[g * 16 + c1]);
+        const uint32_t a3 = __float_as_uint(X[(g + 8) * 16 + c1]);
+        const uint32_t b0 = __float_as_uint(Y[r0 * ldy + ((yc + g) ^ (YS ? sw(r0) : 0))]);
+        const uint32_t b1 = __float_as_uint(Y[r1 * ldy + ((yc + g) ^ (YS ? sw(r1) : 0))]);
         asm volatile(
             "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
             "{%0,%1,%2,%3};"
@@ -123,18 +132,16 @@ __device__ __forceinline__ void half_block(const float *G32, float *N32, float *
                                            int b, int hh, int lane) {
     const int g = lane >> 2, t = lane & 3;
     float c[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k = b; k < a; ++k)
-        mma16x8x16<false, true>(c, G32 + 16 * a * kLDA + 16 * k, kLDA, N32 + 16 * k * kLDN + 16 * b + 8 * hh, kLDN,
-                                lane);
-    const float b0 = bv[16 * a + g], b1 = bv[16 * a + g + 8];
+    for (int k = b; k < a; ++k) mma16x8x16<true>(c, G32 + blk(a, k), N32 + blk(k, b), 8 * hh, lane);
+    const float b0 = bv[vbi(16 * a + g)], b1 = bv[vbi(16 * a + g + 8)];
     *reinterpret_cast<float2 *>(Tw + g * kLDT + 2 * t) = make_float2(tf32r(c[0] * b0), tf32r(c[1] * b0));
     *reinterpret_cast<float2 *>(Tw + (g + 8) * kLDT + 2 * t) = make_float2(tf32r(c[2] * b1), tf32r(c[3] * b1));
     __syncwarp();
     float d[4] = {0.f, 0.f, 0.f, 0.f};
-    mma16x8x16<true, false>(d, N32 + 16 * a * kLDN + 16 * a, kLDN, Tw, kLDT, lane);
-    float *o = N32 + 16 * a * kLDN + 16 * b + 8 * hh + ((2 * t) ^ (g & 4));
-    *reinterpret_cast<float2 *>(o + g * kLDN) = make_float2(tf32r(-d[0]), tf32r(-d[1]));
-    *reinterpret_cast<float2 *>(o + (g + 8) * kLDN) = make_float2(tf32r(-d[2]), tf32r(-d[3]));
+    mma16x8x16<false>(d, N32 + blk(a, a), Tw, 0, lane);
+    float *o = N32 + blk(a, b) + ((8 * hh + 2 * t) ^ sw(g));   // rows g and g + 8 share the swizzle
+    *reinterpret_cast<float2 *>(o + g * 16) = make_float2(tf32r(-d[0]), tf32r(-d[1]));
+    *reinterpret_cast<float2 *>(o + (g + 8) * 16) = make_float2(tf32r(-d[2]), tf32r(-d[3]));
     __syncwarp();   // Tw is reused by this warp's next half-block
 }
 
@@ -178,7 +185,7 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     __shared__ uint32_t tslot;
     __shared__ int s_ok;
     __shared__ Walk s_n2[2];   // the unit after `nxt`, drawn by thread kCtl (two slots)
-    __shared__ __align__(16) float vb[2][R][C + 4];   // padded: the two records' b in different banks
+    __shared__ __align__(16) float vb[2][R][kVb];   // the records' b at vbi(token)
 
     const int64_t total = total_records(p), units = total / R;
     unsigned *tickets = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(p.workspace) + total * kGdnRecordBytes);
@@ -187,7 +194,7 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     if (cur.r >= p.n_seg) return;   // uniform: the whole CTA leaves before any set-up
     const int q = threadIdx.x, warp = q >> 5, lane = q & 31;
     float *G32 = reinterpret_cast<float *>(smem + G::kOffG32);
-    float *N32 = reinterpret_cast<float *>(smem + G::kOffN32);   // record rr at N32 + rr * kNRec
+    float *N32 = reinterpret_cast<float *>(smem + G::kOffN32);   // record rr at N32 + rr * kTri
     float *Tw = reinterpret_cast<float *>(smem + G::kOffT) + warp * 16 * kLDT;
 
     if (q == 0) {
@@ -245,7 +252,7 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         const int b = i & 1;
         const SegEntry seg = p.seg[cur.r];
         const int nch = nch_of(cur.r);
-        if (q < R * C) vb[b][q / C][q & (C - 1)] = beta_cur;
+        if (q < R * C) vb[b][q / C][vbi(q & (C - 1))] = beta_cur;
         const float beta_next = load_beta(nxt);
         // gram(i) done: the k tile is free for the next record
         if (q == kCtl) {
@@ -262,24 +269,28 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         __syncthreads();
         if (!s_ok) break;   // uniform
         tc_fence_after();
-        {   // gram rows t = 16 warp + lane (lanes < 16, M = 64 accumulator layout): row t lies
-            // in block row `warp`; its blocks left of the diagonal are stored tf32-rounded, its
-            // diagonal block exact, the rest not at all
-            uint32_t gr[64];
+        {   // gram rows 16 warp + lane (lanes < 16, M = 64 accumulator layout): row `lane` of
+            // block row `warp`; its blocks left of the diagonal are stored tf32-rounded, its
+            // diagonal block exact, the blocks right of it not at all. Columns in two halves of
+            // 32 (warps 0-1 need only the first).
             const uint32_t taddr = tmem + 64 * b + ((uint32_t)(32 * warp) << 16);
-            tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(&gr[0]));
-            tmem_ld32(taddr + 32, *reinterpret_cast<uint32_t(*)[32]>(&gr[32]));
-            tmem_ld_wait();
-            if (lane < 16) {
-                const int t = 16 * warp + lane;
-                float4 *row = reinterpret_cast<float4 *>(G32 + t * kLDA);
+            const int r = lane & 15;
 #pragma unroll
-                for (int s4 = 0; s4 < C / 4; ++s4) {
-                    if (s4 >= 4 * (warp + 1)) break;   // uniform
-                    float4 g4 = make_float4(__uint_as_float(gr[4 * s4]), __uint_as_float(gr[4 * s4 + 1]),
-                                            __uint_as_float(gr[4 * s4 + 2]), __uint_as_float(gr[4 * s4 + 3]));
-                    if (s4 < 4 * warp) g4 = make_float4(tf32r(g4.x), tf32r(g4.y), tf32r(g4.z), tf32r(g4.w));
-                    row[s4] = g4;
+            for (int hc = 0; hc < 2; ++hc) {
+                if (hc == 1 && warp < 2) break;   // uniform
+                uint32_t gr[32];
+                tmem_ld32(taddr + 32 * hc, gr);
+                tmem_ld_wait();
+                if (lane < 16) {
+#pragma unroll
+                    for (int s4 = 0; s4 < 8; ++s4) {
+                        const int k = 2 * hc + (s4 >> 2), cb = 4 * (s4 & 3);
+                        if (k > warp) break;   // uniform
+                        float4 g4 = make_float4(__uint_as_float(gr[4 * s4]), __uint_as_float(gr[4 * s4 + 1]),
+                                                __uint_as_float(gr[4 * s4 + 2]), __uint_as_float(gr[4 * s4 + 3]));
+                        if (k < warp) g4 = make_float4(tf32r(g4.x), tf32r(g4.y), tf32r(g4.z), tf32r(g4.w));
+                        *reinterpret_cast<float4 *>(G32 + blk(warp, k) + 16 * r + (cb ^ sw(r))) = g4;
+                    }
                 }
             }
         }
@@ -291,24 +302,24 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         if (R == 2 || lane < 16) {
             const int a = warp, j = lane & 15, rr_ = lane >> 4;
             const float *bv = vb[b][rr_];
-            float *Nr = N32 + rr_ * kNRec;
+            const float *Gd = G32 + blk(a, a);
+            float *Nd = N32 + rr_ * kTri + blk(a, a);
             float x[16];
 #pragma unroll
             for (int rr = 0; rr < 16; ++rr) {
-                const float4 *Gr = reinterpret_cast<const float4 *>(G32 + (16 * a + rr) * kLDA + 16 * a);
                 float gr[16];
 #pragma unroll
                 for (int s4 = 0; s4 < 4; ++s4) {
-                    const float4 t4 = Gr[s4];
+                    const float4 t4 = *reinterpret_cast<const float4 *>(Gd + 16 * rr + ((4 * s4) ^ sw(rr)));
                     gr[4 * s4] = t4.x, gr[4 * s4 + 1] = t4.y, gr[4 * s4 + 2] = t4.z, gr[4 * s4 + 3] = t4.w;
                 }
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int s = 0; s < rr; ++s) acc[s & 3] = fmaf(gr[s], x[s], acc[s & 3]);
-                x[rr] = fmaf(-bv[16 * a + rr], (acc[0] + acc[1]) + (acc[2] + acc[3]), (rr == j) ? 1.f : 0.f);
+                x[rr] = fmaf(-bv[vbi(16 * a + rr)], (acc[0] + acc[1]) + (acc[2] + acc[3]), (rr == j) ? 1.f : 0.f);
             }
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) Nr[(16 * a + rr) * kLDN + ((16 * a + j) ^ (rr & 4))] = tf32r(x[rr]);
+            for (int rr = 0; rr < 16; ++rr) Nd[16 * rr + (j ^ sw(rr))] = tf32r(x[rr]);
         }
         __syncthreads();
         // level 1: (1,0), (2,1), (3,2) as six half-blocks; level 2: (2,0), (3,1); level 3: (3,0).
@@ -316,17 +327,17 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         // Each half-block is done for every record of the unit.
 #pragma unroll
         for (int rr = 0; rr < R; ++rr) {
-            half_block(G32, N32 + rr * kNRec, Tw, vb[b][rr], 1 + (warp >> 1), warp >> 1, warp & 1, lane);
-            if (warp >= 2) half_block(G32, N32 + rr * kNRec, Tw, vb[b][rr], 3, 2, warp & 1, lane);
+            half_block(G32, N32 + rr * kTri, Tw, vb[b][rr], 1 + (warp >> 1), warp >> 1, warp & 1, lane);
+            if (warp >= 2) half_block(G32, N32 + rr * kTri, Tw, vb[b][rr], 3, 2, warp & 1, lane);
         }
         __syncthreads();
 #pragma unroll
         for (int rr = 0; rr < R; ++rr)
-            half_block(G32, N32 + rr * kNRec, Tw, vb[b][rr], 2 + (warp >> 1), warp >> 1, warp & 1, lane);
+            half_block(G32, N32 + rr * kTri, Tw, vb[b][rr], 2 + (warp >> 1), warp >> 1, warp & 1, lane);
         __syncthreads();
         if (warp < 2) {
 #pragma unroll
-            for (int rr = 0; rr < R; ++rr) half_block(G32, N32 + rr * kNRec, Tw, vb[b][rr], 3, 0, warp, lane);
+            for (int rr = 0; rr < R; ++rr) half_block(G32, N32 + rr * kTri, Tw, vb[b][rr], 3, 0, warp, lane);
         }
         // warps 2-3 have no level-3 work: the next record's gram (its k tile was requested at
         // the top of this iteration) into the other TMEM buffer, last read a record ago
@@ -344,18 +355,20 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
             const int rr = m / 4;
             uint8_t *dst = static_cast<uint8_t *>(p.workspace) +
                            ((int64_t)seg.wsb + (int64_t)(cur.h + rr) * nch + cur.c) * (int64_t)kGdnRecordBytes;
-            const float *Nr = N32 + rr * kNRec;
+            const float *Nr = N32 + rr * kTri;
             const int e8 = q + 128 * (m & 3);   // 8 consecutive entries of row t'
             const int tp = e8 >> 3, s8 = (e8 & 7) * 8;
+            const int ba = tp >> 4, bb = s8 >> 4, r = tp & 15;   // block (ba, bb), row r in it
             uint4 pk = make_uint4(0u, 0u, 0u, 0u);
-            if ((s8 >> 4) <= (tp >> 4)) {
-                // the eight lanes of a row read the two halves of their 8 entries in opposite
-                // orders, so that each load instruction covers all 32 banks
-                const int h0 = e8 & 4, h1 = h0 ^ 4, sw = tp & 4;
-                const float4 x0 = *reinterpret_cast<const float4 *>(Nr + tp * kLDN + ((s8 + h0) ^ sw));
-                const float4 x1 = *reinterpret_cast<const float4 *>(Nr + tp * kLDN + ((s8 + h1) ^ sw));
-                const float4 b0 = *reinterpret_cast<const float4 *>(vb[b][rr] + s8 + h0);
-                const float4 b1 = *reinterpret_cast<const float4 *>(vb[b][rr] + s8 + h1);
+            if (bb <= ba) {
+                // the eight lanes of a row read the two halves of their 8 entries in an order
+                // chosen per lane, so that each load of N and of b touches distinct banks
+                const int h0 = 4 * ((bb & 1) ^ ((sw(r) >> 2) & 1)), h1 = h0 ^ 4;
+                const float *src = Nr + blk(ba, bb) + 16 * r;
+                const float4 x0 = *reinterpret_cast<const float4 *>(src + (((s8 & 15) + h0) ^ sw(r)));
+                const float4 x1 = *reinterpret_cast<const float4 *>(src + (((s8 & 15) + h1) ^ sw(r)));
+                const float4 b0 = *reinterpret_cast<const float4 *>(vb[b][rr] + vbi(s8 + h0));
+                const float4 b1 = *reinterpret_cast<const float4 *>(vb[b][rr] + vbi(s8 + h1));
                 const uint32_t p0 = pack_bf16x2(x0.x * b0.x, x0.y * b0.y), p1 = pack_bf16x2(x0.z * b0.z, x0.w * b0.w);
                 const uint32_t p2 = pack_bf16x2(x1.x * b1.x, x1.y * b1.y), p3 = pack_bf16x2(x1.z * b1.z, x1.w * b1.w);
                 pk = h0 == 0 ? make_uint4(p0, p1, p2, p3) : make_uint4(p2, p3, p0, p1);
