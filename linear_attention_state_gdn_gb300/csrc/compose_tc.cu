@@ -110,6 +110,9 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
     tc_fence_after();
     const uint32_t tmem = tslot;
     const uint32_t tA_hi = tmem, tA_lo = tmem + 128, tD = tmem + 256;
+    // launched as a programmatic dependent of the previous kernel on the stream: the set-up
+    // above may overlap its tail; every global access comes after its completion
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
@@ -351,8 +354,19 @@ cudaError_t launch_compose_dense_tc(const ComposeParams &p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const int64_t units = p.n_units * (p.P_total ? 2 : 1);
     const int grid = (int)std::min<int64_t>(units, sm_count());
-    kern<<<grid, kThreads, kSmemBytes, s>>>(p, tmP, tmS, tmQ);
-    return cudaGetLastError();
+    // a programmatic dependent launch: CTAs may set up while the previous kernel finishes
+    // (the chain of a build call, whose pieces this merges) and wait for it before any access
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, tmP, tmS, tmQ);
 }
 
 }  // namespace hypic
