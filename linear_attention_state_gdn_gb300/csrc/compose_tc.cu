@@ -28,7 +28,9 @@
 // the transition of the entry composed from all n segments is exp(sum_j lam_j) Q_{n-1}.
 // lam_total of the normal units is summed by their epilogue (thread 0, segment order). With
 // prefix_last (a build composing the pieces of its segments), only the last state is written.
-// Roles: warps 0-3 epilogue (one TMEM lane each), warp 4 TMA producer, warp 5 MMA issuer.
+// Roles: warps 0-7 epilogue (warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31, one state
+// column per lane, and each take half of the column's rows and of every P split), warp 8 TMA
+// producer, warp 9 MMA issuer.
 // Every wait is bounded; on expiry the CTA records HYPIC_ERR_TIMEOUT, lets its in-flight
 // copies and MMAs finish (bounded), frees its TMEM and returns.
 #include <algorithm>
@@ -43,10 +45,11 @@ namespace {
 using namespace ptx;
 
 constexpr int D = 128;
-constexpr int kEpiWarps = 4;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kThreads = 6 * 32;
+constexpr int kEpiWarps = 8;
+constexpr int kEpi = kEpiWarps * 32;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 10 * 32;
 constexpr uint32_t kTile = D * D * 4;          // one fp32 128x128 matrix: 64 KB
 constexpr uint32_t kBlock = D * 32 * 4;        // one 32-column k-block of P: 16 KB
 constexpr uint32_t kOffP = 0;                  // two P stages
@@ -199,9 +202,10 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
             }
         }
     } else {
-        // epilogue: thread n owns state column n = TMEM lane n
-        const int n = threadIdx.x;
-        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+        // epilogue: thread t owns state column n = t % 128 = TMEM lane n, rows (and TMEM
+        // columns) [64 eh, 64 eh + 64) with eh = t / 128
+        const int t = threadIdx.x, n = t & 127, eh = t >> 7;
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         uint32_t pc = 0, sc = 0, lb = 0, dc = 0;
         const float *Ssm = reinterpret_cast<const float *>(smem + kOffS);
         for (int ux = blockIdx.x; ux < UT && !abort_flag; ux += gridDim.x) {
@@ -212,7 +216,7 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                 // A = split(exp(lam_0) S0^T) for the first step
                 const float sc0 = expf(p.lam[u]);
                 const float *s0 = p.S0 + (int64_t)u * D * D + n;
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 4 * eh; c < 4 * eh + 4; ++c) {
                     uint32_t hi[16], lo[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -242,8 +246,8 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                         float4 *src = reinterpret_cast<float4 *>(smem + kOffP + st * kTile + b * kBlock);
                         float4 *dst = reinterpret_cast<float4 *>(smem + kOffLo + slot * kBlock);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const int idx = n + 128 * q;
+                        for (int q = 0; q < 1024 / kEpi; ++q) {
+                            const int idx = t + kEpi * q;
                             const float4 x = src[idx];
                             float4 h, l;
                             h.x = tf32_trunc(x.x); l.x = x.x - h.x;
@@ -272,13 +276,13 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                 {
                     const bool next = j + 1 < NS;
                     const float scale_next = !next ? 0.f : tr ? 1.f : expf(p.lam[(int64_t)(j + 1) * U + u]);
-                    if (FUSED && !tr && n == 0 && p.lam_total) lsum += p.lam[(int64_t)j * U + u];
+                    if (FUSED && !tr && t == 0 && p.lam_total) lsum += p.lam[(int64_t)j * U + u];
                     // prefix_j (only the last one with prefix_last), or for the transition chain
                     // only its last state, P_total
                     float *out = tr ? (next ? nullptr : p.P_total + (int64_t)u * D * D + n)
                                : (FUSED && p.prefix_last) ? (next ? nullptr : p.prefix_last + (int64_t)u * D * D + n)
                                                : p.prefix + ((int64_t)j * U + u) * D * D + n;
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 4 * eh; c < 4 * eh + 4; ++c) {
                         uint32_t r[16];
                         if (mma) {
                             tmem_ld16(tD + lane_off + 16 * c, r);
@@ -308,7 +312,7 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                     }
                 }
             }
-            if (FUSED && !tr && n == 0 && p.lam_total) p.lam_total[u] = lsum;
+            if (FUSED && !tr && t == 0 && p.lam_total) p.lam_total[u] = lsum;
         }
     epi_done:;
     }
