@@ -121,8 +121,11 @@ typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  *                       counter set by the call itself.
  *                     - Any bf16, d = 128 build whose (segment, value head) units fill at most
  *                       half of the current device's SMs: each segment is built as up to 8
- *                       chunk-aligned pieces that are then composed back into its entry; the
- *                       pieces' S, (P,) lam and one scan buffer follow.
+ *                       chunk-aligned pieces that are then composed back into its entry. A
+ *                       DELTA / GDN build whose last round of units fills at most half of the
+ *                       SMs builds its trailing equal-length segments as two halves each. The
+ *                       pieces' S, (P,) lam follow, and for LINEAR / SCALAR / DIAG one scan
+ *                       buffer.
  *                     No part needs to start at zero. The caller owns it; its contents are
  *                     undefined after the call and it may be reused by the next call on the
  *                     same stream, but not by a call still running on another stream. It must
