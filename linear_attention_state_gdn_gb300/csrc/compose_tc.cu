@@ -56,11 +56,11 @@ constexpr uint32_t kOffP = 0;                  // two P stages
 constexpr uint32_t kOffLo = 2 * kTile;         // two low-part k-block slots
 constexpr uint32_t kOffS = 2 * kTile + 2 * kBlock;
 constexpr uint32_t kSmemBytes = kOffS + kTile + 1024;   // + alignment slack
-constexpr uint32_t kTmemCols = 512;            // A_hi [0,128) A_lo [128,256) D [256,384)
+constexpr uint32_t kTmemCols = 512;            // A_hi [0,128) A_lo [128,256) D 2 x [256,384)
 
 struct Bars {
     uint64_t p_full[2], p_empty[2], lo_full[2], lo_empty[2];
-    uint64_t s_full, s_empty, a_full, d_full, fin;
+    uint64_t s_full, s_empty, a_full[2], d_full, fin;
 };
 
 __device__ __forceinline__ float tf32_trunc(float x) {
@@ -101,7 +101,8 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
         }
         mbar_init(&bars.s_full, 1);
         mbar_init(&bars.s_empty, kEpiWarps * 32);
-        mbar_init(&bars.a_full, kEpiWarps * 32);
+        mbar_init(&bars.a_full[0], kEpiWarps * 32);
+        mbar_init(&bars.a_full[1], kEpiWarps * 32);
         mbar_init(&bars.d_full, 1);
         mbar_init(&bars.fin, 1);
         abort_flag = 0;
@@ -165,11 +166,14 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                 for (int j = 0; j < NS; ++j) {
                     if (!(j > 0 || (has_s0 && !tr))) continue;
                     const uint32_t st = pc & 1;
-                    if (!mbar_wait_or_abort(&bars.a_full, ac & 1, p.err, kErrTimeout, &abort_flag))
-                        goto mma_done;
-                    ++ac;
-                    tc_fence_after();
+                    const uint32_t dacc = tD + 128 * (pc & 1);   // the two D buffers alternate by step
                     for (int b = 0; b < 4; ++b) {
+                        if ((b & 1) == 0) {   // A's k-blocks 0-1, then 2-3, as the epilogue writes them
+                            if (!mbar_wait_or_abort(&bars.a_full[b >> 1], ac & 1, p.err, kErrTimeout,
+                                                    &abort_flag))
+                                goto mma_done;
+                            tc_fence_after();
+                        }
                         const uint32_t slot = lb & 1, use = lb >> 1;
                         if (!mbar_wait_or_abort(&bars.lo_full[slot], use & 1, p.err, kErrTimeout,
                                                 &abort_flag))
@@ -182,13 +186,14 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
 #pragma unroll
                         for (int s = 0; s < 4; ++s) {
                             const uint32_t kc = (uint32_t)(32 * b + 8 * s);   // A column of this k-step
-                            mma_tf32_ta(tD, tA_hi + kc, dhi + 2 * s, id, (b | s) != 0);
-                            mma_tf32_ta(tD, tA_lo + kc, dhi + 2 * s, id, 1);
-                            mma_tf32_ta(tD, tA_hi + kc, dlo + 2 * s, id, 1);
+                            mma_tf32_ta(dacc, tA_hi + kc, dhi + 2 * s, id, (b | s) != 0);
+                            mma_tf32_ta(dacc, tA_lo + kc, dhi + 2 * s, id, 1);
+                            mma_tf32_ta(dacc, tA_hi + kc, dlo + 2 * s, id, 1);
                         }
                         mma_commit(&bars.lo_empty[slot]);
                         ++lb;
                     }
+                    ++ac;
                     mma_commit(&bars.p_empty[st]);
                     mma_commit(&bars.d_full);
                     ++pc;
@@ -202,12 +207,47 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
             }
         }
     } else {
-        // epilogue: thread t owns state column n = t % 128 = TMEM lane n, rows (and TMEM
-        // columns) [64 eh, 64 eh + 64) with eh = t / 128
+        // epilogue: thread t owns state column n = t % 128 = TMEM lane n. A step's rows are
+        // written in two parts, A's k-blocks 0-1 (rows 0-63) and then 2-3 (rows 64-127); in each
+        // part half eh = t / 128 of the threads takes 32 rows. After each part the threads split
+        // the matching k-blocks of the next step's P, so that the next step's products on those
+        // k-blocks (into the other D buffer) run while the second part is still being written.
         const int t = threadIdx.x, n = t & 127, eh = t >> 7;
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         uint32_t pc = 0, sc = 0, lb = 0, dc = 0;
         const float *Ssm = reinterpret_cast<const float *>(smem + kOffS);
+        // hi / lo split of k-blocks [b0, b1) of the next P stage to be consumed (pc), in place
+        // and into the low-part ring; block 0 waits for the stage, block 3 retires it
+        auto split = [&](int b0, int b1) -> bool {
+            const uint32_t st = pc & 1, use = pc >> 1;
+            if (b0 == 0 && !mbar_wait_or_abort(&bars.p_full[st], use & 1, p.err, kErrTimeout, &abort_flag))
+                return false;
+            for (int b = b0; b < b1; ++b) {
+                const uint32_t slot = lb & 1, luse = lb >> 1;
+                if (luse >= 1 && !mbar_wait_or_abort(&bars.lo_empty[slot], (luse - 1) & 1,
+                                                     p.err, kErrTimeout, &abort_flag))
+                    return false;
+                float4 *src = reinterpret_cast<float4 *>(smem + kOffP + st * kTile + b * kBlock);
+                float4 *dst = reinterpret_cast<float4 *>(smem + kOffLo + slot * kBlock);
+#pragma unroll
+                for (int q = 0; q < 1024 / kEpi; ++q) {
+                    const int idx = t + kEpi * q;
+                    const float4 x = src[idx];
+                    float4 h, l;
+                    h.x = tf32_trunc(x.x); l.x = x.x - h.x;
+                    h.y = tf32_trunc(x.y); l.y = x.y - h.y;
+                    h.z = tf32_trunc(x.z); l.z = x.z - h.z;
+                    h.w = tf32_trunc(x.w); l.w = x.w - h.w;
+                    src[idx] = h;
+                    dst[idx] = l;
+                }
+                fence_async_shared();
+                mbar_arrive(&bars.lo_full[slot]);
+                ++lb;
+            }
+            if (b1 == 4) ++pc;
+            return true;
+        };
         for (int ux = blockIdx.x; ux < UT && !abort_flag; ux += gridDim.x) {
             const bool tr = ux >= U;
             const int u = tr ? ux - U : ux;
@@ -230,38 +270,16 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                 }
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&bars.a_full);
+                mbar_arrive(&bars.a_full[0]);
+                mbar_arrive(&bars.a_full[1]);
             }
+            bool split_ahead = false;   // this step's P was split during the previous step
             for (int j = 0; j < NS; ++j) {
                 const bool mma = j > 0 || (has_s0 && !tr);
+                uint32_t dacc = tD;
                 if (mma) {
-                    const uint32_t st = pc & 1, use = pc >> 1;
-                    if (!mbar_wait_or_abort(&bars.p_full[st], use & 1, p.err, kErrTimeout, &abort_flag))
-                        goto epi_done;
-                    for (int b = 0; b < 4; ++b) {
-                        const uint32_t slot = lb & 1, luse = lb >> 1;
-                        if (luse >= 1 && !mbar_wait_or_abort(&bars.lo_empty[slot], (luse - 1) & 1,
-                                                             p.err, kErrTimeout, &abort_flag))
-                            goto epi_done;
-                        float4 *src = reinterpret_cast<float4 *>(smem + kOffP + st * kTile + b * kBlock);
-                        float4 *dst = reinterpret_cast<float4 *>(smem + kOffLo + slot * kBlock);
-#pragma unroll
-                        for (int q = 0; q < 1024 / kEpi; ++q) {
-                            const int idx = t + kEpi * q;
-                            const float4 x = src[idx];
-                            float4 h, l;
-                            h.x = tf32_trunc(x.x); l.x = x.x - h.x;
-                            h.y = tf32_trunc(x.y); l.y = x.y - h.y;
-                            h.z = tf32_trunc(x.z); l.z = x.z - h.z;
-                            h.w = tf32_trunc(x.w); l.w = x.w - h.w;
-                            src[idx] = h;
-                            dst[idx] = l;
-                        }
-                        fence_async_shared();
-                        mbar_arrive(&bars.lo_full[slot]);
-                        ++lb;
-                    }
-                    ++pc;
+                    if (!split_ahead && !split(0, 4)) goto epi_done;
+                    dacc = tD + 128 * (dc & 1);
                     if (!mbar_wait_or_abort(&bars.d_full, dc & 1, p.err, kErrTimeout, &abort_flag))
                         goto epi_done;
                     ++dc;
@@ -273,19 +291,19 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                         goto epi_done;
                     ++sc;
                 }
-                {
-                    const bool next = j + 1 < NS;
-                    const float scale_next = !next ? 0.f : tr ? 1.f : expf(p.lam[(int64_t)(j + 1) * U + u]);
-                    if (FUSED && !tr && t == 0 && p.lam_total) lsum += p.lam[(int64_t)j * U + u];
-                    // prefix_j (only the last one with prefix_last), or for the transition chain
-                    // only its last state, P_total
-                    float *out = tr ? (next ? nullptr : p.P_total + (int64_t)u * D * D + n)
-                               : (FUSED && p.prefix_last) ? (next ? nullptr : p.prefix_last + (int64_t)u * D * D + n)
-                                               : p.prefix + ((int64_t)j * U + u) * D * D + n;
-                    for (int c = 4 * eh; c < 4 * eh + 4; ++c) {
+                const bool next = j + 1 < NS;
+                const float scale_next = !next ? 0.f : tr ? 1.f : expf(p.lam[(int64_t)(j + 1) * U + u]);
+                if (FUSED && !tr && t == 0 && p.lam_total) lsum += p.lam[(int64_t)j * U + u];
+                // prefix_j (only the last one with prefix_last), or for the transition chain
+                // only its last state, P_total
+                float *out = tr ? (next ? nullptr : p.P_total + (int64_t)u * D * D + n)
+                           : (FUSED && p.prefix_last) ? (next ? nullptr : p.prefix_last + (int64_t)u * D * D + n)
+                                           : p.prefix + ((int64_t)j * U + u) * D * D + n;
+                for (int part = 0; part < 2; ++part) {
+                    for (int c = 4 * part + 2 * eh; c < 4 * part + 2 * eh + 2; ++c) {
                         uint32_t r[16];
                         if (mma) {
-                            tmem_ld16(tD + lane_off + 16 * c, r);
+                            tmem_ld16(dacc + lane_off + 16 * c, r);
                             tmem_ld_wait();
                         }
                         uint32_t hi[16], lo[16];
@@ -304,13 +322,15 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                             tmem_st16(tA_lo + lane_off + 16 * c, lo);
                         }
                     }
-                    if (has_s) mbar_arrive(&bars.s_empty);
+                    if (part == 1 && has_s) mbar_arrive(&bars.s_empty);
                     if (next) {
                         tmem_st_wait();
                         tc_fence_before();
-                        mbar_arrive(&bars.a_full);
+                        mbar_arrive(&bars.a_full[part]);
+                        if (!split(2 * part, 2 * part + 2)) goto epi_done;
                     }
                 }
+                split_ahead = next;
             }
             if (FUSED && !tr && t == 0 && p.lam_total) p.lam_total[u] = lsum;
         }
