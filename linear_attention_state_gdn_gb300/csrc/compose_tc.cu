@@ -18,10 +18,12 @@
 //     64 KB stages; the epilogue warps truncate it to tf32 in place and write its low part
 //     into a two-slot ring of 16 KB k-blocks, so the MMAs of block b overlap the split of
 //     block b+1;
-//   * D^T = A P_j^T accumulates in TMEM (lane n, column m) = (P_j prefix_{j-1})[:, n];
+//   * D^T = A P_j^T accumulates in TMEM (lane n, column m) = (P_j prefix_{j-1})[:, n], in one
+//     of two accumulators that alternate by step;
 //   * S_j arrives by TMA into shared memory; the epilogue thread of state column n forms
 //     prefix_j[:, n] = D^T[n, :] + S_j[:, n], stores it (coalesced across the warp) and
-//     writes the next A operand.
+//     writes the next A operand, in two halves of A's K range: after the first half the next
+//     step's products on it start (into the other accumulator) while the second is written.
 // Transition units: with P_total requested, units U .. 2U-1 of the persistent loop carry
 // the chain Q_j = P_j Q_{j-1} from Q_0 = P_0 (loaded like an S tile) through the same
 // products, without S, without scaling, and write only Q_{n-1} = P_total of unit u - U:
