@@ -7,7 +7,9 @@ What pins what (a plausible mistake anywhere in the oracle fails at least one ch
   (T = gamma^L I, S = decayed sum), diagonal gates (T = Diag(prod g)), one-token GDN;
 * delta-rule semantics: with b = 1 and |k| = 1 the last write is retrieved exactly
   (k^T S = v^T) and the last key is annihilated by T (k^T T = 0);
-* invariants: det T = prod_t a_t^d (1 - b_t |k_t|^2); S(C|S0) - S(C|0) = T S0;
+* invariants: det T = prod_t a_t^d (1 - b_t |k_t|^2); S(C|S0) - S(C|0) = T S0; |T|_2 <= 1
+  for b |k|^2 in [0, 2]; with b_t = 2 / |k_t|^2 (Householder reflections) T is orthogonal and
+  the last key is flipped by the leftmost factor;
 * brute force on tiny inputs in exact rational arithmetic (sympy), with the transition
   factors formed as dense matrices and multiplied out;
 * the composition theorem against the oracle's own sequential run, and the failure of
@@ -191,6 +193,36 @@ def test_det_invariant(family):
     expect = 6 * la + np.sum(np.log(np.abs(1 - b * (k * k).sum(1))))
     assert sign == np.prod(np.sign(1 - b * (k * k).sum(1)))
     assert logdet == pytest.approx(expect, rel=1e-12, abs=1e-12)
+
+
+@pytest.mark.parametrize("family", ["delta", "gdn"])
+def test_transition_is_a_contraction(family):
+    """With b_t |k_t|^2 in [0, 2] every factor a_t (I - b_t k_t k_t^T) is symmetric with
+    eigenvalues a_t and a_t (1 - b_t |k_t|^2), all in [-1, 1], so |T|_2 <= 1 (a flipped sign in
+    the factor, I + b k k^T, breaks it)."""
+    inp = synth.make_inputs(family, 1, 2, 8, [64], torch.float64, seed=13)
+    S, T = run_build(inp)
+    for h in range(2):
+        assert np.linalg.norm(T[0, h], 2) <= 1 + 1e-12
+
+
+def test_reflection_product_is_orthogonal():
+    """With b_t = 2 / |k_t|^2 every DeltaNet factor is the Householder reflection through the
+    plane orthogonal to k_t: T is orthogonal with det (-1)^L, and each k_t is flipped by its own
+    factor, so the last key satisfies k_L^T T = -k_L^T F_{L-1} ... F_1."""
+    L, d = 9, 5
+    inp = synth.make_inputs("delta", 1, 1, d, [L], torch.float64, seed=12, l2norm_k=False)
+    k = f64(inp.k)[:, 0]
+    inp.beta = torch.from_numpy((2.0 / (k * k).sum(1))[:, None])
+    S, T = run_build(inp)
+    Tm = T[0, 0]
+    np.testing.assert_allclose(Tm.T @ Tm, np.eye(d), atol=1e-12)
+    assert np.linalg.det(Tm) == pytest.approx((-1.0) ** L, abs=1e-10)
+    inp_head = synth.make_inputs("delta", 1, 1, d, [L - 1], torch.float64, seed=12, l2norm_k=False)
+    inp_head.k, inp_head.v = inp.k[: L - 1], inp.v[: L - 1]
+    inp_head.beta = inp.beta[: L - 1]
+    _, T_head = run_build(inp_head)
+    np.testing.assert_allclose(k[-1] @ Tm, -(k[-1] @ T_head[0, 0]), atol=1e-12)
 
 
 @pytest.mark.parametrize("family", ["linear", "scalar", "diag", "delta", "gdn"])
