@@ -2,7 +2,8 @@
 
 What pins what (a plausible mistake anywhere in the oracle fails at least one check):
 
-* hand-derived fixtures under tests/golden (exact decimals, derivation in the file);
+* hand-derived fixtures under tests/golden (exact decimals, derivation in the file): GDN,
+  RetNet and GLA;
 * closed forms: plain linear attention (S = K^T V, T = I), scalar decay
   (T = gamma^L I, S = decayed sum), diagonal gates (T = Diag(prod g)), one-token GDN;
 * delta-rule semantics: with b = 1 and |k| = 1 the last write is retrieved exactly
@@ -85,6 +86,24 @@ def test_golden_retnet_scalar():
     pref = oracle.compose_scan(T, S)
     assert pref[1, 0, 0, 0] == pytest.approx(g["S_C1C2"], abs=1e-14)
     assert S[0, 0, 0, 0] + S[1, 0, 0, 0] == pytest.approx(g["naive_add"], abs=1e-14)
+
+
+def test_golden_gla_diagonal():
+    g = json.load(open(os.path.join(GOLDEN, "gla_d2_hand.json")))
+    k = np.array(g["k"])[:, None, :]
+    v = np.array(g["v"])[:, None, :]
+    log_g = np.log(np.array(g["g"]))[:, None, :]
+    offs = np.array(g["seg_offsets"])
+    S, T = oracle.build_segments("diag", offs, k, v, log_gate=log_g)
+    np.testing.assert_allclose(S[0, 0], g["S_C1"], atol=1e-14)
+    np.testing.assert_allclose(T[0, 0], g["T_C1"], atol=1e-14)
+    np.testing.assert_allclose(S[1, 0], g["S_C2"], atol=1e-14)
+    np.testing.assert_allclose(T[1, 0], g["T_C2"], atol=1e-14)
+    pref = oracle.compose_scan(T, S)
+    np.testing.assert_allclose(pref[1, 0], g["S_C1C2"], atol=1e-14)
+    seq = oracle.run_sequential("diag", offs, k, v, log_gate=log_g)
+    np.testing.assert_allclose(seq[1, 0], g["S_C1C2"], atol=1e-14)
+    np.testing.assert_allclose(S[0, 0] + S[1, 0], g["naive_add"], atol=1e-14)
 
 
 # ------------------------------------------------------------------ closed forms
