@@ -306,7 +306,7 @@ def build_gdn_compose_cache(layers=48, device="cuda"):
 
 # ----------------------------------------------------------------------------- sections
 
-def section_family(name, flush, peak, steps=20, warmup=3):
+def section_family(name, flush, peak, steps=20, warmup=3, oracle_budget_s=0.0):
     from linear_attention_state_gdn_gb300 import synth
     inp = synth.make_workload(name)
     st = Step(inp, "cuda")
@@ -326,15 +326,21 @@ def section_family(name, flush, peak, steps=20, warmup=3):
     if dense:   # tensor-bound: the chunked-form flops against the measured bf16 peak
         tf = GDN_FLOP_PER_TOKEN_HEAD * n_tok * inp.H_v / (b_ms * 1e-3) / 1e12
         extra = {"build_tflops": round(tf, 1), "build_tensor_frac": round(tf / peak["bf16_tflops"], 4)}
-    return {"build_kernel": bk, "build_ms": round(b_ms, 4), **extra,
-            "build_tokens_per_s": round(n_tok / b_ms * 1e3, 1),
-            "build_gbs": round(b_gbs, 1), "build_hbm_frac": round(b_gbs / peak["hbm_gbs"], 4),
-            "build_bytes": b_bytes, "compose_kernel": ck, "compose_ms": round(c_ms, 4),
-            "compose_gbs": round(c_gbs, 1), "compose_hbm_frac": round(c_gbs / peak["hbm_gbs"], 4),
-            "compose_bytes": c_bytes}
+    out = {"build_kernel": bk, "build_ms": round(b_ms, 4), **extra,
+           "build_tokens_per_s": round(n_tok / b_ms * 1e3, 1),
+           "build_gbs": round(b_gbs, 1), "build_hbm_frac": round(b_gbs / peak["hbm_gbs"], 4),
+           "build_bytes": b_bytes, "compose_kernel": ck, "compose_ms": round(c_ms, 4),
+           "compose_gbs": round(c_gbs, 1), "compose_hbm_frac": round(c_gbs / peak["hbm_gbs"], 4),
+           "compose_bytes": c_bytes}
+    if oracle_budget_s:
+        torch.cuda.synchronize()
+        out["cpu_baseline"] = cpu_baseline(inp, gpu=(st.S, st.lam, st.P, st.prefix),
+                                           budget_s=oracle_budget_s)
+        out["parity"] = out["cpu_baseline"].pop("parity")
+    return out
 
 
-def section_gdn_compose(flush, peak, steps=10, warmup=3, layers=48):
+def section_gdn_compose(flush, peak, steps=10, warmup=3, layers=48, oracle_units=0):
     import linear_attention_state_gdn_gb300 as hy
     S, lam, P, info = build_gdn_compose_cache(layers)
     prefix = torch.empty_like(S)
@@ -360,19 +366,50 @@ def section_gdn_compose(flush, peak, steps=10, warmup=3, layers=48):
     out["with_totals"] = {"compose_ms": round(ms_t, 4), "compose_bytes": nbytes_t,
                           "compose_gbs": round(nbytes_t / ms_t / 1e6, 1),
                           "compose_hbm_frac": round(nbytes_t / ms_t / 1e6 / peak["hbm_gbs"], 4)}
+    if oracle_units:
+        # one unit per layer, each a different head, spread over the whole cache
+        H = info["H_v"]
+        units = [l * H + (7 * l) % H for l in range(S.shape[1] // H)][:oracle_units]
+        torch.cuda.synchronize()
+        out["cpu_baseline"] = compose_cpu_baseline(S, lam, P, prefix, units, lam_t, P_t)
+        out["parity"] = out["cpu_baseline"].pop("parity")
     del S, lam, P, prefix, lam_t, P_t
     torch.cuda.empty_cache()
     return out
 
 
 # ----------------------------------------------------------------------------- CPU oracle
+# The cpu_baseline legs below are the only places this file executes the oracle: they time
+# it on the host cores and, from the same pass, report how far the GPU results of the timed
+# workload are from it (max relative Frobenius error per matrix, computed in fp64).
 
-def oracle_step_sample(inp, heads, nthreads):
-    """One oracle step on a sample: all segments of the first `heads` value heads
-    (with their key heads): fp64 build of (S, T) plus the fp64 compose scan."""
-    import oracle
+def rel_frob_max(got, ref):
+    """Largest relative Frobenius error over the matrices (last two axes) of `got` against
+    `ref`, in fp64; a matrix whose reference is exactly zero counts its absolute norm."""
+    g = np.asarray(got, dtype=np.float64)
+    r = np.asarray(ref, dtype=np.float64)
+    assert g.shape == r.shape, (g.shape, r.shape)
+    g = g.reshape(-1, g.shape[-2] * g.shape[-1])
+    r = r.reshape(-1, r.shape[-2] * r.shape[-1])
+    num = np.linalg.norm(g - r, axis=1)
+    den = np.linalg.norm(r, axis=1)
+    e = np.where(den > 0, num / np.where(den > 0, den, 1.0), num)
+    return float(e.max()) if e.size else 0.0
+
+
+def sample_heads(inp, heads):
+    """Value heads [0, heads) rounded down to whole key-head groups (at least one group)."""
     g = inp.H_v // inp.H_k
-    hk = max(1, math.ceil(heads / g))
+    return max(g, min(inp.H_v, heads) // g * g)
+
+
+def oracle_step_sample(inp, heads, nthreads, want=False):
+    """One oracle step on a sample: all segments of the first `heads` value heads (a whole
+    number of key-head groups, with their key heads): fp64 build of (S, T) plus the fp64
+    compose scan. Returns the seconds taken and, with `want`, (S, T, prefix)."""
+    import oracle
+    heads = sample_heads(inp, heads)
+    hk = heads // (inp.H_v // inp.H_k)
     f = lambda t: None if t is None else t.double().numpy()
     k = np.ascontiguousarray(f(inp.k)[:, :hk])
     v = np.ascontiguousarray(f(inp.v)[:, :heads])
@@ -382,30 +419,88 @@ def oracle_step_sample(inp, heads, nthreads):
     t0 = time.perf_counter()
     S, T = oracle.build_segments(inp.family, inp.seg_offsets, k, v, lg, lgam, b,
                                  nthreads=nthreads)
-    oracle.compose_scan(T, S, nthreads=nthreads)
-    return time.perf_counter() - t0
+    pref = oracle.compose_scan(T, S, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return (dt, (S, T, pref)) if want else dt
 
 
-def cpu_baseline(inp, budget_s=12.0):
+def build_parity(inp, heads, ref, gpu):
+    """Errors of the GPU's S, T (= exp(lam) P materialised in fp64) and prefix states for
+    value heads [0, heads) against the oracle's (S, T, prefix) of the same heads."""
+    import oracle
+    S_o, T_o, pref_o = ref
+    S, lam, P, prefix = gpu
+    d = inp.d_k
+    h = slice(0, heads)
+    f = lambda t: None if t is None else t[:, h].double().cpu().numpy()
+    T = oracle.materialize_T(inp.family, f(lam), f(P), d_k=d)
+    out = {"S": rel_frob_max(f(S), S_o), "T": rel_frob_max(T, T_o)}
+    if prefix is not None:
+        out["prefix"] = rel_frob_max(f(prefix), pref_o)
+    tol = 1e-4 if inp.dtype == torch.float32 else 2e-2
+    out = {k: float(f"{v:.3e}") for k, v in out.items()}
+    out.update({"tol": tol, "ok": all(v <= tol for v in out.values()),
+                "units": f"{inp.n_seg} segments x {heads} of {inp.H_v} value heads"})
+    return out
+
+
+def cpu_baseline(inp, gpu=None, budget_s=12.0, min_passes=1):
     """The oracle as it stands, on the host cores, on a bounded sample of the workload
-    sized to roughly `budget_s` seconds; reported as tokens/s of the whole workload."""
+    sized to roughly `budget_s` seconds; reported as tokens/s of the whole workload. With
+    the GPU's outputs of the same inputs (S, lam, P, prefix), the last pass's oracle results
+    also give the parity of those outputs on the sampled heads."""
     import oracle
     threads = oracle.default_threads()
-    # calibration: one value head (n_seg units); h heads take about h times as long
+    # calibration: one key-head group (n_seg units each); h heads take about h times as long
     t1 = max(oracle_step_sample(inp, 1, threads), 1e-3)
-    heads = max(1, min(inp.H_v, int(budget_s / t1)))
+    g = inp.H_v // inp.H_k
+    heads = sample_heads(inp, int(budget_s / t1 * g))
     # whole passes over the sample until the budget is used (the full workload can take
     # less than the budget on many cores)
-    dt, passes = 0.0, 0
-    while passes == 0 or dt < budget_s:
-        dt += oracle_step_sample(inp, heads, threads)
+    dt, passes, ref = 0.0, 0, None
+    while passes < min_passes or dt < budget_s:
+        t, ref = oracle_step_sample(inp, heads, threads, want=True)
+        dt += t
         passes += 1
     tok_per_s = inp.n_tok * heads / inp.H_v * passes / dt
-    return {"value": round(tok_per_s, 2), "unit": UNIT, "cores": threads, "kind": "oracle",
-            "seconds": round(dt, 2),
-            "sample": f"fp64 oracle build (S, T) + compose of all {inp.n_seg} segments x "
-                      f"{heads} of {inp.H_v} value heads ({inp.n_tok} tokens each), "
-                      f"{passes} pass(es); tokens/s scaled by {heads}/{inp.H_v}"}
+    out = {"value": round(tok_per_s, 2), "unit": UNIT, "cores": threads, "kind": "oracle",
+           "seconds": round(dt, 2),
+           "sample": f"fp64 oracle build (S, T) + compose of all {inp.n_seg} segments x "
+                     f"{heads} of {inp.H_v} value heads ({inp.n_tok} tokens each), "
+                     f"{passes} pass(es); tokens/s scaled by {heads}/{inp.H_v}"}
+    if gpu is not None:
+        out["parity"] = build_parity(inp, heads, ref, gpu)
+    return out
+
+
+def compose_cpu_baseline(S, lam, P, prefix, units, lam_t=None, P_t=None):
+    """The oracle's compose scan of the GPU-built fp32 entries (lam, P, S) of the sampled
+    units, consumed as data; timed on the host cores (GB/s of the algorithmic compose bytes
+    of the sample) and compared with the GPU's prefix states (and composed transitions) of
+    the same units."""
+    import oracle
+    threads = oracle.default_threads()
+    f = lambda t: t[:, units].double().cpu().numpy()
+    Sd, lamd, Pd = f(S), f(lam), f(P)
+    t0 = time.perf_counter()
+    T = oracle.materialize_T("gdn", lamd, Pd)
+    pref_o = oracle.compose_scan(T, Sd, nthreads=threads)
+    dt = time.perf_counter() - t0
+    n_seg, U, d = Sd.shape[0], Sd.shape[1], Sd.shape[2]
+    nbytes = compose_algorithmic_bytes(n_seg, U, d, True)
+    par = {"prefix": float(f"{rel_frob_max(f(prefix), pref_o):.3e}")}
+    if lam_t is not None:
+        lt_o, Pt_o = oracle.compose_transitions("gdn", lamd, Pd)
+        lt = lam_t[units].double().cpu().numpy()
+        par["lam_total"] = float(f"{float(np.max(np.abs(lt - lt_o) / np.maximum(np.abs(lt_o), 1e-30))):.3e}")
+        par["P_total"] = float(f"{rel_frob_max(P_t[units].double().cpu().numpy()[None], Pt_o[None]):.3e}")
+    par.update({"tol": 1e-4, "ok": all(v <= 1e-4 for v in par.values()),
+                "units": f"{n_seg} segments x {U} sampled units"})
+    return {"value": round(nbytes / dt / 1e9, 3), "unit": "GB/s", "cores": threads,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"fp64 oracle compose scan of {U} of {S.shape[1]} units x {n_seg} segments "
+                      f"(the GPU-built fp32 entries as data); GB/s of the sample's algorithmic bytes",
+            "parity": par}
 
 
 def run_reference(args):
@@ -420,7 +515,8 @@ def run_reference(args):
     t1 = oracle_step_sample(inp, 1, threads)
     # size each step so that warmup + steps end within ~150 s
     per_step_budget = 150.0 / max(1, args.steps + args.warmup)
-    heads = max(1, min(inp.H_v, int(per_step_budget / max(t1, 1e-3))))
+    g = inp.H_v // inp.H_k
+    heads = sample_heads(inp, int(per_step_budget / max(t1, 1e-3) * g))
     for _ in range(args.warmup):
         oracle_step_sample(inp, heads, threads)
     times = [oracle_step_sample(inp, heads, threads) for _ in range(args.steps)]
@@ -645,16 +741,21 @@ def run_main(args):
             "peaks": pk}
 
     if not args.quick:
+        # the last timed step's outputs, for the oracle leg's parity check
+        gpu_out = tuple(None if t is None else t.cpu() for t in (st.S, st.lam, st.P, st.prefix))
         line["e2e"] = e2e_measure(inp)
         del st
         torch.cuda.empty_cache()
+        oracle_leg = rank == 0 and world == 1
         sections = {}
         for name in ("retnet", "gla", "gdn_one_segment", "retnet_one_segment"):
-            sections[name] = section_family(name, flush, pk)
-        sections["gdn_compose"] = section_gdn_compose(flush, pk, layers=args.compose_layers)
+            sections[name] = section_family(name, flush, pk, oracle_budget_s=4.0 if oracle_leg else 0.0)
+        sections["gdn_compose"] = section_gdn_compose(flush, pk, layers=args.compose_layers,
+                                                      oracle_units=96 if oracle_leg else 0)
         line["sections"] = sections
-        if rank == 0 and world == 1:
-            line["cpu_baseline"] = cpu_baseline(inp)
+        if oracle_leg:
+            line["cpu_baseline"] = cpu_baseline(inp, gpu=gpu_out)
+            line["parity"] = line["cpu_baseline"].pop("parity")
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -230,6 +230,18 @@ const char *hypic_compose_kernel_name(const hypic_compose_args *args);
  * HYPIC_ERR_TIMEOUT or HYPIC_ERR_RANGE; HYPIC_ERR_CUDA if the synchronisation failed. */
 hypic_status hypic_get_device_status(void *stream);
 
+/* Diagnostic for the kernels' failure path, so that it can be exercised on a GPU without
+ * making any real kernel hang. The pages have no counterpart. Launches one CTA per SM of
+ * the current device; each allocates tensor memory the way the build and compose kernels
+ * do, waits on an mbarrier that nothing ever arrives at with the library's bounded wait
+ * and a wall-clock limit of limit_us microseconds (1 .. 1,000,000), records
+ * HYPIC_ERR_TIMEOUT in the device status word when the limit runs out (always, by
+ * construction), passes the give-up on to a second wait through the CTA's abort flag as
+ * the multi-role kernels do, frees its tensor memory and returns. Asynchronous on `stream`;
+ * hypic_get_device_status() then reports HYPIC_ERR_TIMEOUT. Returns HYPIC_ERR_INVALID_ARG
+ * for a limit outside the range, HYPIC_ERR_CUDA if the launch fails. */
+hypic_status hypic_probe_wait_timeout(uint32_t limit_us, void *stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char *hypic_status_string(hypic_status status);
 

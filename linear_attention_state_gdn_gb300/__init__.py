@@ -84,6 +84,8 @@ def load_library(path: str = LIB_PATH):
                          (lib.hypic_compose_kernel_name, ComposeArgs)):
                 f.argtypes = [ctypes.POINTER(t)]
                 f.restype = ctypes.c_char_p
+            lib.hypic_probe_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
+            lib.hypic_probe_wait_timeout.restype = ctypes.c_int
             lib.hypic_abi_version.argtypes = []
             lib.hypic_abi_version.restype = ctypes.c_int32
             _lib = lib
@@ -149,6 +151,30 @@ def build_outputs(family, n_seg, H_v, d, device, out_seg_stride=0):
     return S, lam, P
 
 
+def _outputs(family, n_seg, v, S, lam, P, out_seg_stride):
+    """The build's output tensors: allocated (with the segment stride the call writes at)
+    when S is not given; checked to hold every unit the call writes when they are. Segment j
+    of the call writes units j * stride .. j * stride + H_v - 1 of S, lam and P."""
+    H_v, d = v.shape[1], v.shape[2]
+    if S is None:
+        if lam is not None or P is not None:
+            raise ValueError("give S, lam (and P) together, or none of them")
+        return build_outputs(family, n_seg, H_v, d, v.device, out_seg_stride)
+    stride = out_seg_stride or H_v
+    units = (n_seg - 1) * stride + H_v if n_seg > 0 else 0
+    dense = family in ("gdn", "delta") or family in (FAMILY["gdn"], FAMILY["delta"])
+    diag = family in ("diag", FAMILY["diag"])
+    need = [(S, units * d * d, "S"), (lam, units * (d if diag else 1), "lam")]
+    if dense:
+        need.append((P, units * d * d, "P"))
+    for t, n, name in need:
+        if t is None:
+            raise ValueError(f"{name} missing")
+        if not t.is_contiguous() or t.dtype != torch.float32 or t.numel() < n:
+            raise ValueError(f"{name} must be a contiguous fp32 tensor of at least {n} elements")
+    return S, lam, P
+
+
 def hypic_build_workspace_bytes(family, k, v, seg_offsets, **kw) -> int:
     lib = load_library()
     a = make_build_args(family, k, v, seg_offsets, **kw)
@@ -163,15 +189,15 @@ def hypic_build_segments(family, k, v, seg_offsets, log_gate=None, log_gamma=Non
     Outputs are allocated when not given. Asynchronous on `stream`."""
     lib = load_library()
     n_seg = len(_offsets(seg_offsets)) - 1
-    if S is None:
-        S, lam, P = build_outputs(family, n_seg, v.shape[1], v.shape[2], v.device)
+    S, lam, P = _outputs(family, n_seg, v, S, lam, P, out_seg_stride)
     a = make_build_args(family, k, v, seg_offsets, log_gate, log_gamma, beta, S, lam, P,
                         out_seg_stride)
     need = int(lib.hypic_build_workspace_bytes(ctypes.byref(a)))
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=v.device)
     if workspace is not None:
-        a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel()
+        a.workspace = _ptr(workspace)
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
     _check(lib.hypic_build_segments(ctypes.byref(a), _stream(stream)), "hypic_build_segments")
     return S, lam, P
 
@@ -183,8 +209,7 @@ def hypic_build_segments_static_ws(family, k, v, seg_offsets, log_gate=None, log
     64 MiB): no per-call allocation. Calls that overlap in time race on that scratch."""
     lib = load_library()
     n_seg = len(_offsets(seg_offsets)) - 1
-    if S is None:
-        S, lam, P = build_outputs(family, n_seg, v.shape[1], v.shape[2], v.device)
+    S, lam, P = _outputs(family, n_seg, v, S, lam, P, out_seg_stride)
     a = make_build_args(family, k, v, seg_offsets, log_gate, log_gamma, beta, S, lam, P,
                         out_seg_stride)
     _check(lib.hypic_build_segments_static_ws(ctypes.byref(a), _stream(stream)),
@@ -241,6 +266,14 @@ def hypic_get_device_status(stream=None) -> int:
     return int(load_library().hypic_get_device_status(_stream(stream)))
 
 
+def hypic_probe_wait_timeout(limit_us: int, stream=None) -> None:
+    """Run the library's bounded-wait failure path on every SM (a wait that nothing ends runs
+    out after limit_us microseconds); hypic_get_device_status() then reports
+    HYPIC_ERR_TIMEOUT. Diagnostic only: no real kernel is made to hang."""
+    _check(load_library().hypic_probe_wait_timeout(int(limit_us), _stream(stream)),
+           "hypic_probe_wait_timeout")
+
+
 def hypic_status_string(status: int) -> str:
     return load_library().hypic_status_string(status).decode()
 
@@ -248,5 +281,6 @@ def hypic_status_string(status: int) -> str:
 __all__ = ["hypic_build_segments", "hypic_build_segments_static_ws", "hypic_compose_scan",
            "hypic_build_workspace_bytes",
            "hypic_build_kernel_name", "hypic_compose_kernel_name",
-           "hypic_get_device_status", "hypic_status_string", "load_library", "HypicError",
+           "hypic_get_device_status", "hypic_probe_wait_timeout", "hypic_status_string",
+           "load_library", "HypicError",
            "build_outputs", "FAMILY"]

@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "internal.cuh"
+#include "ptx.cuh"
 
 using namespace hypic;
 
@@ -54,6 +55,35 @@ void *static_workspace() {
         g_static_ws_addr[dev] = ptr;
     }
     return g_static_ws_addr[dev];
+}
+
+// hypic_probe_wait_timeout: one warp per CTA allocates tensor memory as the kernels do; its
+// first thread waits with the bounded wait on a barrier nothing arrives at (the limit runs
+// out and sets kErrTimeout), raises the CTA's abort flag as a multi-role kernel's timed-out
+// role does, and checks that a second wait gives up on that flag at once instead of sitting
+// out its own limit; the warp then frees the tensor memory.
+__global__ void __launch_bounds__(32) wait_probe_kernel(unsigned *err, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tslot;
+    __shared__ volatile int abort_flag;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(&bar, 1);
+        abort_flag = 0;
+        ptx::fence_mbar_init();
+    }
+    ptx::tmem_alloc(&tslot, 32);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = tslot;
+    if (threadIdx.x == 0 && !ptx::mbar_wait(&bar, 0, err, kErrTimeout, limit_ns)) {
+        abort_flag = 1;
+        ptx::mbar_wait_or_abort(&bar, 0, err, kErrTimeout, &abort_flag);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 32);
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -561,6 +591,17 @@ hypic_status hypic_compose_scan(const hypic_compose_args *a, void *stream) {
     // the dense tensor-core kernel sums lam_total itself
     if (e == cudaSuccess && a->lam_total && pick_compose(a) != ComposePath::DenseTc) e = launch_compose_lam_total(p, s);
     return from_cuda(e);
+}
+
+hypic_status hypic_probe_wait_timeout(uint32_t limit_us, void *stream) {
+    if (limit_us < 1 || limit_us > 1000000u) return HYPIC_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    unsigned *err = status_word(&dev);
+    if (!err) return HYPIC_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return HYPIC_ERR_CUDA;
+    wait_probe_kernel<<<sms, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, (uint64_t)limit_us * 1000u);
+    return from_cuda(cudaGetLastError());
 }
 
 const char *hypic_build_kernel_name(const hypic_build_args *a) {

@@ -82,3 +82,23 @@ def slice_heads(inp, heads):
     if inp.log_gamma is not None:
         out.log_gamma = inp.log_gamma[heads].contiguous()
     return out
+
+
+def kernel_code_hash(name):
+    """Hash of the code of a kernel source under csrc/ (comments and blank lines do not
+    count). The host models of a kernel's protocol or layout record the hash of the source
+    they were checked against, so that an edit to the kernel fails them until the model has
+    been re-checked against the new code and the recorded hash updated."""
+    import hashlib
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    path = os.path.join(root, "linear_attention_state_gdn_gb300", "csrc", name)
+    with open(path) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    h = hashlib.sha1()
+    for line in text.splitlines():
+        code = line.split("//", 1)[0].rstrip()
+        if code:
+            h.update(code.encode() + b"\n")
+    return h.hexdigest()[:12]

@@ -239,3 +239,9 @@ def test_static_workspace_build_rejects_null_and_oversized_requests(lib):
     a = good_build(n_seg=1, lens=(2049 * 64,))
     assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) > (64 << 20)
     assert lib.hypic_build_segments_static_ws(ctypes.byref(a), None) == 3
+
+
+def test_wait_probe_rejects_limits_out_of_range(lib):
+    # checked before the library touches the device
+    assert lib.hypic_probe_wait_timeout(0, None) == 1
+    assert lib.hypic_probe_wait_timeout(1000001, None) == 1

@@ -315,3 +315,15 @@ def test_chain_protocol_model_catches_planted_mistakes(mistake):
             continue
         hits += r != "ok"
     assert hits > 0
+
+
+# The kernel source this model was last checked against (code only; comments do not count).
+MODELLED_SOURCE = ("build_gdn_tc.cu", "9702cefe1f3e")
+
+
+def test_model_is_checked_against_the_current_kernel_source():
+    from tests.helpers import kernel_code_hash
+    name, recorded = MODELLED_SOURCE
+    assert kernel_code_hash(name) == recorded, (
+        f"{name} changed since this model was checked against it: re-check the model "
+        f"against the new code, then record the new hash {kernel_code_hash(name)}")

@@ -228,3 +228,15 @@ def test_compose_protocol_model_catches_planted_mistakes(mistake, expect):
             assert any(e in str(h) for e in expect), str(h)
             hits += 1
     assert hits > 0
+
+
+# The kernel source this model was last checked against (code only; comments do not count).
+MODELLED_SOURCE = ("compose_tc.cu", "dca88169bc5c")
+
+
+def test_model_is_checked_against_the_current_kernel_source():
+    from tests.helpers import kernel_code_hash
+    name, recorded = MODELLED_SOURCE
+    assert kernel_code_hash(name) == recorded, (
+        f"{name} changed since this model was checked against it: re-check the model "
+        f"against the new code, then record the new hash {kernel_code_hash(name)}")

@@ -136,3 +136,15 @@ def test_planted_unswizzled_layout_conflicts():
     worst = max(wavefronts(addrs, width) - {1: 1, 2: 2}[width]
                 for _, addrs, width in fragment_accesses(swizzle=lambda r: 0))
     assert worst > 0
+
+
+# The kernel source this model was last checked against (code only; comments do not count).
+MODELLED_SOURCE = ("build_gdn_prep.cu", "e619cdf67e60")
+
+
+def test_model_is_checked_against_the_current_kernel_source():
+    from tests.helpers import kernel_code_hash
+    name, recorded = MODELLED_SOURCE
+    assert kernel_code_hash(name) == recorded, (
+        f"{name} changed since this model was checked against it: re-check the model "
+        f"against the new code, then record the new hash {kernel_code_hash(name)}")
