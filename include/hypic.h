@@ -167,11 +167,16 @@ typedef struct {
  *   prefix       out [n_seg][n_units][d_k][d_v] fp32: prefix[j] = state after segments
  *                0..j, i.e. exp(lam_j) P_j prefix[j-1] + S_j with prefix[-1] = S0
  *   lam_total    optional out (NULL = skip): the log-scale of the transition of all n_seg
- *                segments composed, sum_j lam_j; [n_units] (DIAG: [n_units][d_k]); 0 for
- *                LINEAR. 4-byte aligned.
- *   P_total      optional out (NULL = skip), DELTA / GDN only (must be NULL otherwise):
- *                P_{n-1} ... P_0 [n_units][d_k][d_k] fp32, latest segment leftmost.
- *                16-byte aligned.
+ *                segments composed; [n_units] (DIAG: [n_units][d_k]); 4-byte aligned.
+ *                sum_j lam_j (0 for LINEAR), minus E ln 2 when P_total carries a scale 2^E.
+ *   P_total      optional out (NULL = skip), DELTA / GDN only (must be NULL otherwise, and
+ *                needs lam_total): 2^E P_{n-1} ... P_0 [n_units][d_k][d_k] fp32, latest
+ *                segment leftmost, 16-byte aligned. The product of many contractions leaves
+ *                the fp32 range (64 segments of a few hundred tokens: about 1e-49), so the
+ *                d = 128 kernel carries it scaled by powers of two and reports the exponent
+ *                E >= 0 in lam_total; E = 0 while the product stays above 2^-24 in its
+ *                largest entry, and always for d = 32, 64. exp(lam_total) P_total is the
+ *                composed transition either way.
  *   With S0 = NULL, (prefix[n-1], exp(lam_total) P_total) is the cache entry
  *   (S(C|0), T_C) of the concatenation C = C_0 ... C_{n-1}: entries compose as
  *   T_C2 . S(C1) + S(C2) with transition T_C2 T_C1 (besthub.dev, paragraph "For linear
@@ -245,7 +250,8 @@ hypic_status hypic_probe_wait_timeout(uint32_t limit_us, void *stream);
 /* Static, NUL-terminated description of a status code. */
 const char *hypic_status_string(hypic_status status);
 
-/* Library ABI version (incremented on any change to the structs above). */
+/* Library ABI version (incremented on any change to the structs above or to the meaning of
+ * their fields). 3: P_total needs lam_total and may carry a power-of-two scale. */
 int32_t hypic_abi_version(void);
 
 #ifdef __cplusplus

@@ -26,9 +26,16 @@
 //     step's products on it start (into the other accumulator) while the second is written.
 // Transition units: with P_total requested, units U .. 2U-1 of the persistent loop carry
 // the chain Q_j = P_j Q_{j-1} from Q_0 = P_0 (loaded like an S tile) through the same
-// products, without S, without scaling, and write only Q_{n-1} = P_total of unit u - U:
-// the transition of the entry composed from all n segments is exp(sum_j lam_j) Q_{n-1}.
-// lam_total of the normal units is summed by their epilogue (thread 0, segment order). With
+// products, without S, and write only Q_{n-1} = P_total of unit u - U: the transition of the
+// entry composed from all n segments is exp(sum_j lam_j) Q_{n-1}. Each P_j is a product of
+// contractions, so a long chain drives Q below the fp32 range (64 cached segments of a few
+// hundred tokens: about 1e-49). The chain is therefore carried scaled by powers of two: once
+// the largest entry of the carried matrix falls below 2^-24 (found by a max-reduction of the
+// previous step's values over the epilogue threads, on an mbarrier), the next operand is
+// multiplied by the power of two that brings it back into [1, 2); the exponents are summed
+// and P_total = 2^E Q_{n-1} is written with lam_total = sum_j lam_j - E ln 2 (the scaling is
+// exact, and E = 0 whenever the chain stays in range). The transition unit writes lam_total;
+// without P_total it is summed by the normal unit's epilogue (thread 0, segment order). With
 // prefix_last (a build composing the pieces of its segments), only the last state is written.
 // Roles: warps 0-7 epilogue (warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31, one state
 // column per lane, and each take half of the column's rows and of every P split), warp 8 TMA
@@ -63,7 +70,11 @@ constexpr uint32_t kTmemCols = 512;            // A_hi [0,128) A_lo [128,256) D 
 struct Bars {
     uint64_t p_full[2], p_empty[2], lo_full[2], lo_empty[2];
     uint64_t s_full, s_empty, a_full[2], d_full, fin;
+    uint64_t red;   // the epilogue threads' max-reduction of a transition unit's step
 };
+
+// The power-of-two exponent e with 2^e <= x < 2^(e+1), for a normal positive float x.
+__device__ __forceinline__ int exponent_of(float x) { return (int)((__float_as_uint(x) >> 23) & 0xFFu) - 127; }
 
 __device__ __forceinline__ float tf32_trunc(float x) {
     return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
@@ -88,6 +99,7 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
     __shared__ Bars bars;
     __shared__ uint32_t tslot;
     __shared__ volatile int abort_flag;
+    __shared__ unsigned red_max[3];   // largest |value| of a transition step (float bits), three slots
 
     const int warp = warp_id(), lane = lane_id();
     const int U = (int)p.n_units, NS = p.n_seg;
@@ -107,6 +119,8 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
         mbar_init(&bars.a_full[1], kEpiWarps * 32);
         mbar_init(&bars.d_full, 1);
         mbar_init(&bars.fin, 1);
+        mbar_init(&bars.red, kEpiWarps * 32);
+        red_max[0] = red_max[1] = red_max[2] = 0u;
         abort_flag = 0;
         fence_mbar_init();
     }
@@ -216,7 +230,7 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
         // k-blocks (into the other D buffer) run while the second part is still being written.
         const int t = threadIdx.x, n = t & 127, eh = t >> 7;
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-        uint32_t pc = 0, sc = 0, lb = 0, dc = 0;
+        uint32_t pc = 0, sc = 0, lb = 0, dc = 0, rc = 0;
         const float *Ssm = reinterpret_cast<const float *>(smem + kOffS);
         // hi / lo split of k-blocks [b0, b1) of the next P stage to be consumed (pc), in place
         // and into the low-part ring; block 0 waits for the stage, block 3 retires it
@@ -253,7 +267,11 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
         for (int ux = blockIdx.x; ux < UT && !abort_flag; ux += gridDim.x) {
             const bool tr = ux >= U;
             const int u = tr ? ux - U : ux;
-            float lsum = 0.f;   // thread 0 of a normal unit: sum of lam over the segments
+            float lsum = 0.f;   // thread 0: sum of lam over the segments (lam_total)
+            // transition units: the power of two the next operand is multiplied by, the sum of
+            // the exponents applied so far, and this thread's largest |value| of the step
+            float s_pow = 1.f, vmax = 0.f;
+            int e_sum = 0;
             if (has_s0 && !tr) {
                 // A = split(exp(lam_0) S0^T) for the first step
                 const float sc0 = expf(p.lam[u]);
@@ -286,6 +304,27 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                         goto epi_done;
                     ++dc;
                     tc_fence_after();
+                    if (FUSED && tr) {
+                        // the largest |entry| of the previous step's values over all epilogue
+                        // threads (non-negative floats order like their bit patterns), in slot
+                        // rc % 3. Thread 0 then clears slot (rc + 2) % 3: every thread read it
+                        // (reduction rc - 1) before arriving here, and none writes it before
+                        // reduction rc + 2, which needs thread 0's next arrival
+                        atomicMax(&red_max[rc % 3], __float_as_uint(vmax));
+                        mbar_arrive(&bars.red);
+                        if (!mbar_wait_or_abort(&bars.red, rc & 1, p.err, kErrTimeout, &abort_flag))
+                            goto epi_done;
+                        const float m = __uint_as_float(red_max[rc % 3]) * s_pow;   // largest |entry| of A_j
+                        if (t == 0) red_max[(rc + 2) % 3] = 0u;
+                        ++rc;
+                        s_pow = 1.f;
+                        if (m > 0.f && m < 0x1p-24f) {
+                            const int e = -exponent_of(m);   // m 2^e in [1, 2)
+                            s_pow = __uint_as_float((uint32_t)(127 + e) << 23);
+                            e_sum += e;
+                        }
+                        vmax = 0.f;
+                    }
                 }
                 const bool has_s = !(tr && j > 0);   // S_j (Q_0 = P_0 for the transition chain)
                 if (has_s) {
@@ -294,8 +333,8 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                     ++sc;
                 }
                 const bool next = j + 1 < NS;
-                const float scale_next = !next ? 0.f : tr ? 1.f : expf(p.lam[(int64_t)(j + 1) * U + u]);
-                if (FUSED && !tr && t == 0 && p.lam_total) lsum += p.lam[(int64_t)j * U + u];
+                const float scale_next = !next ? 0.f : tr ? s_pow : expf(p.lam[(int64_t)(j + 1) * U + u]);
+                if (FUSED && t == 0 && p.lam_total) lsum += p.lam[(int64_t)j * U + u];
                 // prefix_j (only the last one with prefix_last), or for the transition chain
                 // only its last state, P_total
                 float *out = tr ? (next ? nullptr : p.P_total + (int64_t)u * D * D + n)
@@ -314,6 +353,7 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                             const int m = 16 * c + i;
                             const float v = (mma ? __uint_as_float(r[i]) : 0.f) + (has_s ? Ssm[m * D + n] : 0.f);
                             if (out) st_stream(out + (int64_t)m * D, v);
+                            if (FUSED && tr) vmax = fmaxf(vmax, fabsf(v));
                             const float x = v * scale_next;
                             const float h = tf32_trunc(x);
                             hi[i] = __float_as_uint(h);
@@ -334,7 +374,10 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                 }
                 split_ahead = next;
             }
-            if (FUSED && !tr && t == 0 && p.lam_total) p.lam_total[u] = lsum;
+            // lam_total: by the transition unit when there is one (with the exponents of its
+            // scaling), else by the normal unit
+            if (FUSED && t == 0 && p.lam_total && tr == (p.P_total != nullptr))
+                p.lam_total[u] = lsum - (float)e_sum * 0.69314718055994531f;
         }
     epi_done:;
     }

@@ -201,6 +201,33 @@ def test_compose_totals_parity(family, d, with_S0):
         assert_close(f64(P_t)[None], P_o[None], COMPOSE_TOL, "P_total")
 
 
+def test_compose_totals_stay_in_range_on_long_chains():
+    """64 entries whose P_j have spectral norm about 0.1: the plain product (about 1e-64)
+    is below the fp32 range. The d = 128 kernel carries it scaled by powers of two and
+    reports the exponent in lam_total, so exp(lam_total) P_total is still the composed
+    transition (compared at its own scale, in fp64)."""
+    c = synth.make_compose_inputs("gdn", 64, 6, 128, seed=154, p_norm=0.1)
+    pref, lam_t, P_t = compose_with_totals("gdn", c.S.cuda(), c.lam.cuda(), c.P.cuda())
+    lam_o, P_o = oracle.compose_transitions("gdn", f64(c.lam), f64(c.P))
+    assert np.abs(P_o).max() < 1e-50            # out of fp32's range
+    E = (lam_o - f64(lam_t)) / np.log(2.0)       # the exponents applied
+    assert np.all(E > 100) and np.allclose(E, np.round(E), atol=1e-3)
+    got = f64(P_t) * np.exp(f64(lam_t) - lam_o)[:, None, None]
+    assert_close(got[None], P_o[None], COMPOSE_TOL, "scaled P_total")
+
+
+def test_long_deltanet_segment_keeps_its_transition():
+    """One 32768-token DeltaNet segment (no gates, lam = 0): its transition (about 1e-40) is
+    built as eight pieces composed back; the scaled composition keeps it in range, so T
+    matches the oracle's at its own scale."""
+    inp = synth.make_inputs("delta", 1, 2, 128, [32768], torch.bfloat16, seed=155)
+    S, lam, P = gpu_build(inp)
+    So, To = oracle_build(inp)
+    assert np.abs(To).max() < 1e-30
+    assert_close(f64(S), So, TOL[inp.dtype], "S")
+    assert_close(gpu_T("delta", lam, P, 128), To, TOL[inp.dtype], "T")
+
+
 @pytest.mark.parametrize("family", FAMILIES)
 def test_composed_entry_is_the_entry_of_the_concatenation(family):
     """Segments built on the GPU, composed into one entry (prefix[n-1], lam_total, P_total),
@@ -228,8 +255,11 @@ def test_compose_totals_are_validated():
     g = synth.make_compose_inputs("gdn", 3, 2, 64, seed=153)
     S, lam, P = g.S.cuda(), g.lam.cuda(), g.P.cuda()
     prefix = torch.empty_like(S)
+    lam_t = torch.empty(2, device="cuda")
     with pytest.raises(hy.HypicError):     # a total may not overlap prefix
-        hy.hypic_compose_scan("gdn", S, lam, P, prefix=prefix, P_total=prefix[0])
+        hy.hypic_compose_scan("gdn", S, lam, P, prefix=prefix, lam_total=lam_t, P_total=prefix[0])
+    with pytest.raises(hy.HypicError):     # P_total needs lam_total (its scale)
+        hy.hypic_compose_scan("gdn", S, lam, P, P_total=torch.empty(2, 64, 64, device="cuda"))
     with pytest.raises(hy.HypicError):     # nor an input
         hy.hypic_compose_scan("gdn", S, lam, P, lam_total=lam[0])
 
