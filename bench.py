@@ -40,7 +40,7 @@ sys.path.insert(0, ROOT)
 METRIC = "GDN (S,T_C) build tokens/s + compose/scan GB/s, % of GB300 roofline"
 # sources whose code the recorded build traffic belongs to (the launches and how the call
 # splits and merges segments)
-TRAFFIC_SOURCES = ["build_gdn_tc.cu", "gdn_chunk_inverse.cuh", "compose_tc.cu", "api.cu"]
+TRAFFIC_SOURCES = ["build_gdn_prep.cu", "build_gdn_tc.cu", "compose_tc.cu", "api.cu"]
 UNIT = "tokens/s"
 CHUNK = 64
 L2_FLUSH_BYTES = 256 << 20
@@ -636,20 +636,21 @@ def e2e_measure(inp, steps=5, warmup=2, groups=4):
 
 
 def build_split(hy, inp, dev):
-    """True when the tensor-core GDN build of `inp` splits segments into pieces (the pieces'
-    outputs are its only workspace)."""
+    """True when the tensor-core GDN build of `inp` splits segments into pieces (its workspace
+    then holds more than the chunk records and their 256-byte tail)."""
     need = hy.hypic_build_workspace_bytes(inp.family, dev["k"], dev["v"], inp.seg_offsets,
                                           log_gate=dev.get("log_gate"), beta=dev.get("beta"))
-    return need > 0
+    records = sum((int(b - a) + CHUNK - 1) // CHUNK for a, b in
+                  zip(inp.seg_offsets[:-1], inp.seg_offsets[1:])) * inp.H_v
+    return need > records * CHUNK * CHUNK * 2 + 256
 
 
 def build_launches(kernel_name, split=False):
     """Kernel launches of one hypic_build_segments call on the path `kernel_name`: the GDN
-    tensor-core build is one launch of the chain (which computes its chunk matrices itself),
-    plus one compose launch that merges pieces when the call splits segments (the 16-segment
-    workload halves its last two)."""
+    tensor-core build is the chunk preparation and the chain, plus one compose launch that
+    merges pieces when the call splits segments (the 16-segment workload halves its last two)."""
     if kernel_name == "build_gdn_tc":
-        return 2 if split else 1
+        return 3 if split else 2
     return 1
 
 
@@ -715,10 +716,11 @@ def run_main(args):
                 "unit": "TFLOP/s",
                 "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 flop x max SM clock"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
-    # the tensor-core GDN build is one call of one or two launches (the chain, and the compose
-    # merging halved segments); the events bracket the call, so the roofline covers both
+    # the tensor-core GDN build is one call of two or three launches (chunk preparation, the
+    # chain, and the compose merging halved segments); the events bracket the call, so the
+    # roofline covers all of them
     split = tensor_path and build_split(hy, inp, st.dev)
-    roof["kernel"] = ("build_gdn_tc" + (" + compose_dense_tc (merge)" if split else "")
+    roof["kernel"] = ("build_gdn_prep + build_gdn_tc" + (" + compose_dense_tc (merge)" if split else "")
                       if bk == "build_gdn_tc" else bk)
     roof["algorithmic_flop_per_launch"] = flops
     roof["algorithmic_bytes_per_launch"] = nbytes

@@ -140,6 +140,17 @@ ComposePath pick_compose(const hypic_compose_args *a) {
     return compose_dense_tc_supported(q) ? ComposePath::DenseTc : ComposePath::DenseSimt;
 }
 
+// Workspace records of the GDN / DeltaNet tensor-core build: one per (segment, value head,
+// 64-token chunk). Negative segment lengths count as empty (they are rejected elsewhere).
+int64_t gdn_records(const hypic_build_args *a) {
+    int64_t records = 0;
+    for (int j = 0; j < a->n_seg; ++j) {
+        const int64_t len = a->seg_offsets[j + 1] - a->seg_offsets[j];
+        if (len > 0) records += (int64_t)a->H_v * ((len + kGdnChunk - 1) / kGdnChunk);
+    }
+    return records;
+}
+
 // Intra-segment split of the tensor-core builds (DeltaNet / GDN, and the linear / scalar /
 // diagonal one). Each (segment, value head) unit is one serial chain of chunks, so a call with
 // few units (one long prompt as a single segment) leaves most SMs idle. When the units fill at most half of the SMs, every
@@ -289,9 +300,12 @@ const char *hypic_status_string(hypic_status s) {
 size_t hypic_build_workspace_bytes(const hypic_build_args *a) {
     if (!build_shape_ok(a) || a->n_seg == 0 || !a->seg_offsets) return 0;
     const BuildPath path = pick_build(a);
-    // only the tensor-core builds that split segments need scratch (0 without a split)
-    if (path == BuildPath::GatedTc || path == BuildPath::GdnTc) return gdn_split_layout(a, 0).bytes;
-    return 0;
+    if (path == BuildPath::GatedTc) return gdn_split_layout(a, 0).bytes;   // 0 without a split
+    if (path != BuildPath::GdnTc) return 0;
+    const int64_t records = gdn_records(a);
+    if (records == 0) return 0;
+    const size_t base = (size_t)records * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail;
+    return base + gdn_split_layout(a, base).bytes;
 }
 
 hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
@@ -343,6 +357,8 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
             if (p && !on_device(p)) return HYPIC_ERR_INVALID_ARG;
     }
     const BuildPath path = pick_build(a);
+    // records are addressed as 64-row blocks of a 2D tensor map with int32 coordinates
+    if (path == BuildPath::GdnTc && gdn_records(a) > (int64_t)(INT32_MAX / 64)) return HYPIC_ERR_UNSUPPORTED;
     const size_t ws_need = hypic_build_workspace_bytes(a);
     if (ws_need > 0) {
         if (!a->workspace) return HYPIC_ERR_INVALID_ARG;
@@ -380,7 +396,10 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
     // a segment with n chunks in pj pieces covers chunks [k n / pj, (k + 1) n / pj))
     SplitLayout split;
     if (path == BuildPath::GdnTc || path == BuildPath::GatedTc) {
-        split = gdn_split_layout(a, 0);
+        const size_t base = path == BuildPath::GdnTc
+                                ? (size_t)gdn_records(a) * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail
+                                : 0;
+        split = gdn_split_layout(a, base);
         if (split.slots > 0) {
             uint8_t *ws = static_cast<uint8_t *>(a->workspace);
             p.S_piece = reinterpret_cast<float *>(ws + split.off_S);
@@ -410,7 +429,13 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
     if ((int64_t)table.size() > HYPIC_MAX_SEGMENTS) return HYPIC_ERR_UNSUPPORTED;   // not reached: splits need few units
     std::stable_sort(table.begin(), table.end(), [](const SegEntry &x, const SegEntry &y) { return x.len > y.len; });
     p.n_seg = (int32_t)table.size();
-    for (int r = 0; r < p.n_seg; ++r) p.seg[r] = table[r];
+    int64_t wsb = 0;
+    for (int r = 0; r < p.n_seg; ++r) {
+        p.seg[r] = table[r];
+        p.seg[r].wsb = (int32_t)wsb;   // bounded by the record check above on the GDN path
+        wsb = std::min<int64_t>(wsb + (int64_t)a->H_v * ((p.seg[r].len + kGdnChunk - 1) / kGdnChunk),
+                                INT32_MAX);
+    }
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     switch (path) {

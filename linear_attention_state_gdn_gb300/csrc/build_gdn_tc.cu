@@ -1,9 +1,7 @@
 // build_gdn_tc.cu -- DeltaNet / Gated DeltaNet segment build on the 5th-generation tensor
-// cores (bf16 k / v, d_k = d_v = 128, fp32 state): the serial chunk chain, together with the
-// chunk matrices M2 = N Diag(b) it consumes (N = (I + Diag(b) L)^-1, L the strictly lower part
-// of the chunk's gram K K^T), which four warps of the same CTA compute from the chunk's k tile
-// a chunk or two ahead (gdn_chunk_inverse.cuh) and leave in shared memory: nothing goes
-// through global memory between the two, and the call is one launch.
+// cores (bf16 k / v, d_k = d_v = 128, fp32 state): the serial chunk chain. It runs after
+// build_gdn_prep.cu, which leaves one bf16 matrix M2 = N Diag(b) per 64-token chunk in the
+// workspace (N = (I + Diag(b) L)^-1, L the strictly lower part of the chunk's gram K K^T).
 //
 // What is computed: for every cached segment C and value head the pair (S(C|0), T_C) with
 // T_C = exp(lam) P, P = prod_t (I - b_t k_t k_t^T) (latest factor leftmost), lam = sum log a_t
@@ -33,15 +31,13 @@
 //         [384,448) bf16 Z_S^T (A of d_S); between d_S(c) and the next Z pass it holds the
 //                   fp32 W^T(c+1) accumulator (lane i, column t')
 //         [448,512) bf16 Z_P^T (A of d_P)
-//   SMEM  a ring of three k chunks and a ring of three {v chunk, M2} (k, v by TMA, M2 written by
-//         the chunk-inverse warps; 128B-swizzled); -W^T bf16 (MN-major B of d, two slots);
-//         M1 = M2 Diag(exp(-Lam - c)) bf16 (K-major B of U, two slots); the chunk-inverse
-//         warps' G, N and scratch.
+//   SMEM  a ring of three k chunks and a ring of three {v chunk, M2 record} (TMA,
+//         128B-swizzled); -W^T bf16 (MN-major B of d, two slots); M1 = M2 Diag(exp(-Lam - c))
+//         bf16 (K-major B of U, two slots).
 // Roles: warps 0-3 carry the S~ half and warps 4-7 the P half (thread = TMEM lane = state
 // column: Z^T -> bf16, D^T -> bf16), warps 8-11 prepare the state-independent operands
 // (gates, M1, -W^T -> bf16), warp 12 issues TMA, warp 13 the S~ half's MMAs and the state-
-// independent ones, warp 14 the P half's MMAs, warps 15-18 compute each chunk's M2 into its
-// ring slot (the slot's {v, M2} barrier counts their 128 arrivals beside the TMA's):
+// independent ones, warp 14 the P half's MMAs:
 //     warp 13, per chunk c:  d_S(c): D_S += Z_S^T (-W^T);  W(c+1): W^T = K^T M2^T;
 //                            f_S(c): Z_S^T += D_S^T K;     U(c+1): D_S = V^T M1^T
 //     warp 14, per chunk c:  d_P(c): D_P = Z_P^T (-W^T);   f_P(c): Z_P^T += D_P^T K
@@ -50,7 +46,6 @@
 // Every wait is bounded; a wait that runs out sets the status word and the CTA drains.
 #include <algorithm>
 
-#include "gdn_chunk_inverse.cuh"
 #include "internal.cuh"
 #include "ptx.cuh"
 #include "tmap.cuh"
@@ -62,12 +57,11 @@ using namespace ptx;
 
 constexpr int D = 128;
 constexpr int C = kGdnChunk;
-constexpr int kThreads = 608;
+constexpr int kThreads = 480;
 constexpr int kAuxWarp0 = 8;
 constexpr int kProducerWarp = 12;
 constexpr int kMmaWarpS = 13;   // issues the S~ half's products and W, U
 constexpr int kMmaWarpP = 14;   // issues the P half's products
-constexpr int kInvWarp0 = 15;   // warps 15-18: the chunk matrices M2
 constexpr float kRenormBelow = -30.f;       // reset Lam when Lam + c_C would drop below this
 constexpr float kMinChunkLogDecay = -60.f;  // supported range of c_C
 
@@ -82,8 +76,7 @@ constexpr uint32_t kOffK = 0;                 // k ring: 3 x 16 KB
 constexpr uint32_t kOffVR = kKSlots * kKV;    // {v, M2} ring: 3 x 24 KB
 constexpr uint32_t kOffWop = kOffVR + kVSlots * kVR;  // -W^T bf16: 2 slots x [128 rows i][128 B]
 constexpr uint32_t kOffM1 = kOffWop + 2 * kKV;  // M1: 2 slots x 8 KB
-constexpr uint32_t kOffInv = kOffM1 + 2 * kRec;  // chunk-inverse warps: G, N, 4 x 16 x 8 scratch
-constexpr uint32_t kSmemBytes = kOffInv + gdninv::kSmemBytes + 1024;
+constexpr uint32_t kSmemBytes = kOffM1 + 2 * kRec + 1024;
 
 constexpr uint32_t kTZ = 0, kTD = 256, kTZK = 384;
 
@@ -97,7 +90,7 @@ struct Slot {   // per-chunk values from the operand warps (two slots)
 
 struct Bars {
     uint64_t kfull[kKSlots], kempty[kKSlots];   // k ring
-    uint64_t vfull[kVSlots], vempty[kVSlots];   // {v, M2} ring (vfull: the TMA + 128 M2 writers)
+    uint64_t vfull[kVSlots], vempty[kVSlots];   // {v, M2} ring
     uint64_t wfull;               // W^T accumulated
     // -W^T operand of a chunk written (and the W^T TMEM columns free), one per operand slot:
     // the P half's issuer may lag, so one barrier could be two phases ahead of its wait
@@ -129,25 +122,6 @@ __device__ __forceinline__ bool bar_aux_and(bool v) {
     return r != 0;
 }
 
-// The same pair of barriers for the 128 chunk-inverse threads (named barrier 3).
-__device__ __forceinline__ void bar_inv() {
-    __syncwarp();
-    asm volatile("barrier.sync 3, 128;" ::: "memory");
-}
-__device__ __forceinline__ bool bar_inv_and(bool v) {
-    uint32_t r;
-    __syncwarp();
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "barrier.red.and.pred po, 3, 128, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-
 __device__ __forceinline__ uint32_t bf2(float lo, float hi) { return pack_bf16x2(lo, hi); }
 
 __device__ __forceinline__ void ld64(uint32_t taddr, uint32_t (&z)[64]) {
@@ -170,7 +144,7 @@ __device__ __forceinline__ void st_bf16x64(uint32_t taddr, const uint32_t (&z)[6
 
 __global__ void __launch_bounds__(kThreads, 1)
 build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmR) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-aligned base, derived by offsetting the shared array itself so that the
     // compiler keeps the shared address space (plain ld/st.shared, not generic accesses)
@@ -180,7 +154,6 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
     __shared__ uint32_t tslot;
     __shared__ volatile int abort_flag;
     __shared__ float scan_tmp[2];
-    __shared__ __align__(16) float vb[2][gdninv::kVb];   // b of a chunk at vbi(token), two slots
 
     const int warp = warp_id(), lane = lane_id();
     const SegEntry seg = p.seg[blockIdx.x / p.H_v];
@@ -195,7 +168,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             mbar_init(&bars.kempty[s], 2);   // both halves' updates read the k chunk
         }
         for (int s = 0; s < kVSlots; ++s) {
-            mbar_init(&bars.vfull[s], 1 + 128);
+            mbar_init(&bars.vfull[s], 1);
             mbar_init(&bars.vempty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
@@ -232,6 +205,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
         if (lane == 0) {
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
+            prefetch_tmap(&tmR);
             int c = 0, kc = 0;   // chunks whose {v, M2} / k loads were issued
             for (; c < nch; ++c) {
                 const int32_t t0 = seg.start + c * C;
@@ -242,12 +216,18 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 tma_load_3d(kt, &tmK, &bars.kfull[ks], 0, hk, t0);
                 tma_load_3d(kt + kHalf, &tmK, &bars.kfull[ks], 64, hk, t0);
                 kc = c + 1;
+                // the records are written by the preparation kernel, which may still be
+                // running (this grid is a programmatic dependent launch): wait for it to
+                // complete before the first record load (k and v above are inputs)
+                if (c == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
                 const int vs = c % kVSlots, vuse = c / kVSlots;
                 if (vuse >= 1 && !wait(&bars.vempty[vs], (vuse - 1) & 1)) break;
                 uint8_t *vt = smem + kOffVR + vs * kVR;
-                mbar_arrive_expect_tx(&bars.vfull[vs], kKV);
+                const int32_t rrow = (seg.wsb + h * nch + c) * 64;
+                mbar_arrive_expect_tx(&bars.vfull[vs], kVR);
                 tma_load_3d(vt, &tmV, &bars.vfull[vs], 0, h, t0);
                 tma_load_3d(vt + kHalf, &tmV, &bars.vfull[vs], 64, h, t0);
+                tma_load_2d(vt + kKV, &tmR, &bars.vfull[vs], 0, rrow);
             }
             if (abort_flag) {   // let the loads in flight land before the CTA exits
                 for (int q = (kc > kKSlots ? kc - kKSlots : 0); q < kc; ++q)
@@ -464,48 +444,6 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             tc_fence_before();
             mbar_arrive(&bars.wready[c & 1]);
         }
-    } else if (warp >= kInvWarp0) {
-        // ---------------------------------------------------------------- chunk-inverse warps 15-18
-        // Per chunk c: the gram of k(c) from its ring slot, N, then M2 = N Diag(b) into the
-        // M2 part of {v, M2} slot c % 3 once W and M1 of chunk c - 3 have read it (vempty).
-        // G, N, b and the scratch are reused chunk after chunk; the named barriers between the
-        // steps order every reuse (b has two slots: chunk c's is written before the barrier
-        // that chunk c - 1's last reader has passed).
-        using namespace gdninv;
-        const int q = threadIdx.x - 32 * kInvWarp0, w = q >> 5;
-        float *G32 = reinterpret_cast<float *>(smem + kOffInv);
-        float *N32 = G32 + kTri;
-        float *Tw = N32 + kTri + w * 16 * kLDT;
-        // b of token q of chunk c (0 past the segment end)
-        auto beta_of = [&](int c) -> float {
-            return (q < C && q < seg.len - c * C) ? p.beta[((int64_t)seg.start + c * C + q) * p.H_v + h] : 0.f;
-        };
-        float beta_next = nch > 0 ? beta_of(0) : 0.f;
-        for (int c = 0; c < nch; ++c) {
-            const float *bv = vb[c & 1];
-            if (q < C) vb[c & 1][vbi(q)] = beta_next;
-            if (c + 1 < nch) beta_next = beta_of(c + 1);
-            // the chunk's k tile has landed (and b is visible to the four warps)
-            if (!bar_inv_and(wait(&bars.kfull[c % kKSlots], (c / kKSlots) & 1))) break;
-            gram_blocks(smem_u32(smem + kOffK + (c % kKSlots) * kKV), G32, w, lane);
-            bar_inv();
-            diag_solve(G32, N32, bv, w, lane);
-            bar_inv();
-            // level 1: (1,0), (2,1), (3,2) as six half-blocks; level 2: (2,0), (3,1); level 3:
-            // (3,0). Warps 0-1 take one half-block per level, warps 2-3 two in level 1 and none
-            // in level 3.
-            half_block(G32, N32, Tw, bv, 1 + (w >> 1), w >> 1, w & 1, lane);
-            if (w >= 2) half_block(G32, N32, Tw, bv, 3, 2, w & 1, lane);
-            bar_inv();
-            half_block(G32, N32, Tw, bv, 2 + (w >> 1), w >> 1, w & 1, lane);
-            bar_inv();
-            if (w < 2) half_block(G32, N32, Tw, bv, 3, 0, w, lane);
-            const int vs = c % kVSlots, vuse = c / kVSlots;
-            if (!bar_inv_and(vuse < 1 || wait(&bars.vempty[vs], (vuse - 1) & 1))) break;
-            store_m2(N32, bv, smem + kOffVR + vs * kVR + kKV, q);
-            fence_async_shared();
-            mbar_arrive(&bars.vfull[vs]);
-        }
     } else {
         // ---------------------------------------------------------------- chain warps 0-7
         const int hf = warp >> 2;                  // 0: S~ half, 1: P half
@@ -605,17 +543,45 @@ bool build_gdn_tc_supported(const BuildParams &p) {
 cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s) {
     const int blocks = p.n_seg * p.H_v;
     if (blocks == 0) return cudaSuccess;
+    int64_t records = 0;
+    for (int r = 0; r < p.n_seg; ++r) records += (int64_t)p.H_v * ((p.seg[r].len + C - 1) / C);
     const int64_t N = p.n_tok > 0 ? p.n_tok : 1;
-    CUtensorMap tmK, tmV;
+    CUtensorMap tmK, tmV, tmR;
     if (!make_tmap_3d(&tmK, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_k, N, (uint64_t)D * 2,
                       (uint64_t)p.H_k * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_3d(&tmV, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_v, N, (uint64_t)D * 2,
                       (uint64_t)p.H_v * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(build_gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (records > 0) {
+        if (!p.workspace ||
+            !make_tmap_2d(&tmR, p.workspace, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64, (uint64_t)records * 64,
+                          128, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    } else {
+        tmR = tmK;   // no chunk anywhere: the kernel issues no load
+    }
+    cudaError_t e = launch_build_gdn_prep(p, s);
     if (e != cudaSuccess) return e;
-    build_gdn_tc_kernel<<<blocks, kThreads, kSmemBytes, s>>>(p, tmK, tmV);
-    return cudaGetLastError();
+    e = cudaFuncSetAttribute(build_gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (records == 0) {
+        build_gdn_tc_kernel<<<blocks, kThreads, kSmemBytes, s>>>(p, tmK, tmV, tmR);
+        return cudaGetLastError();
+    }
+    // launched as a programmatic dependent of the preparation kernel: CTAs may start (set-up,
+    // k / v loads) on SMs the preparation has left, and wait for its completion before
+    // reading its records
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, build_gdn_tc_kernel, p, tmK, tmV, tmR);
 }
 
 }  // namespace hypic

@@ -21,11 +21,14 @@ struct SegEntry {
     int32_t start;
     int32_t len;
     int32_t idx;
-    int32_t pad;
+    int32_t wsb;   // first workspace record of this segment (GDN / DeltaNet tensor-core build)
 };
 
-// Chunk length of the tensor-core builds (and the unit of their intra-segment splits).
+// Workspace record of the GDN / DeltaNet tensor-core build: one 64 x 64 bf16 matrix per
+// (segment, value head, 64-token chunk).
 constexpr int kGdnChunk = 64;
+constexpr int64_t kGdnRecordBytes = kGdnChunk * kGdnChunk * 2;
+constexpr int64_t kGdnWorkspaceTail = 256;   // after the records: the preparation's ticket counter
 
 struct BuildParams {
     int32_t family;
@@ -86,6 +89,7 @@ bool compose_dense_tc_supported(const ComposeParams &p);
 cudaError_t launch_build_gated_tc(const BuildParams &p, cudaStream_t s);
 bool build_gated_tc_supported(const BuildParams &p);
 cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s);
+cudaError_t launch_build_gdn_prep(const BuildParams &p, cudaStream_t s);
 bool build_gdn_tc_supported(const BuildParams &p);
 
 // fp32 view of one input element (bf16 or fp32 storage).

@@ -224,11 +224,10 @@ def test_binding_refuses_cpu_tensors():
 
 
 def test_workspace_bytes_of_the_tensor_core_gdn_build(lib):
-    # bf16, d = 128, DeltaNet / GDN: the chain computes its chunk matrices in shared memory,
-    # so the only scratch is the pieces' outputs of a split build, which depends on the
-    # device's SM count; without a device nothing is split and nothing is needed
+    # bf16, d = 128, DeltaNet / GDN: 8 KB per (segment, value head, 64-token chunk) and a
+    # 256-byte tail (the preparation kernel's ticket counter)
     a = good_build(lens=(64, 130))
-    assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == 0
+    assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == 4 * (1 + 3) * 8192 + 256
     a.d_k = a.d_v = 64                      # exact fp32-state path: no workspace
     assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == 0
     b = good_build(family=2)                # gated families: no workspace
@@ -241,8 +240,12 @@ def test_build_rejects_a_short_workspace(lib):
     assert call_build(lib, a) == 1
 
 
-def test_static_workspace_build_rejects_null_args(lib):
+def test_static_workspace_build_rejects_null_and_oversized_requests(lib):
     assert lib.hypic_build_segments_static_ws(None, None) == 1
+    # 4 heads x 2049 chunks x 8 KB > 64 MiB: refused before any device work
+    a = good_build(n_seg=1, lens=(2049 * 64,))
+    assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) > (64 << 20)
+    assert lib.hypic_build_segments_static_ws(ctypes.byref(a), None) == 3
 
 
 def test_wait_probe_rejects_limits_out_of_range(lib):

@@ -1,20 +1,16 @@
-"""Host model of the shared-memory layout of the chunk-inverse warps of the GDN chain kernel
-(csrc/gdn_chunk_inverse.cuh, used by csrc/build_gdn_tc.cu).
+"""Host model of the shared-memory layout of the chunk preparation (csrc/build_gdn_prep.cu).
 
-G (the chunk's gram) and N (its inverse) keep only their ten 16 x 16 blocks on and below the
-diagonal: block (a, b) starts at word 264 (a (a + 1) / 2 + b), and element (r, c) of a block
-sits at 16 r + (c ^ sw(r)) with sw(r) = 8 bit1(r) + 4 bit2(r). The b values of a chunk sit at
-e + 16 (e >> 5). The k tile is read from the chain's TMA ring (two 64-channel halves of 64
-rows x 128 bytes, 128-byte swizzle), and M2 is written into the ring's M2 slot in the same
-swizzled form. The tests restate those index functions and every access pattern of the code,
-and check that
+G (the chunk's gram) and N (the inverse, one per record of a unit) keep only their ten 16 x 16
+blocks on and below the diagonal: block (a, b) starts at word 264 (a (a + 1) / 2 + b), and
+element (r, c) of a block sits at 16 r + (c ^ sw(r)) with sw(r) = 8 bit1(r) + 4 bit2(r). The b
+values of a record sit at e + 16 (e >> 5). The tests restate those index functions and every
+access pattern of the kernel, and check that
 
 - every element has its own word, inside the allocation;
 - each warp-wide access needs no more shared-memory wavefronts than its width requires
-  (1 for 4-byte, 2 for 8-byte, 4 for 16-byte accesses by a full warp): the ldmatrix loads of
-  the k tile for the gram, the gram's and the level products' 16 x 8 result stores, the
-  warp-level MMA's A and B fragments, the diagonal solves' stores and reads of b, and the
-  record stage's loads of N and b and its stores of M2.
+  (1 for 4-byte, 2 for 8-byte, 4 for 16-byte accesses by a full warp): the warp-level MMA's A
+  and B fragments, the 16 x 8 result stores, the gram's row stores, the diagonal solves' stores
+  and reads of b, and the record stage's loads of N and b.
 
 A planted layout without the swizzle fails the fragment check.
 """
@@ -108,52 +104,20 @@ def test_fragments_and_result_stores_are_conflict_free():
         assert wavefronts(addrs, width) == {1: 1, 2: 2}[width], name
 
 
-def sw128(row, byte):
-    return row * 128 + (byte ^ ((row & 7) << 4))
-
-
-def ktile_off(t, i):
-    return (i >> 6) * 8192 + sw128(t, (i & 63) * 2)
-
-
-def test_gram_ldmatrix_loads_are_conflict_free():
-    """ldmatrix.x4 serves 8 lanes (one 8 x 8 matrix, one 16-byte row each) per phase: each
-    phase must cover 32 distinct banks."""
-    blocks = [[(0, 0), (1, 0), (1, 1)], [(2, 0), (2, 1), (2, 2)], [(3, 0), (3, 1)], [(3, 2), (3, 3)]]
-    for w in range(4):
-        for a, b in blocks[w]:
-            for ks in range(8):
-                A = [ktile_off(16 * a + (l & 7) + 8 * ((l >> 3) & 1), 16 * ks + 8 * (l >> 4)) for l in range(32)]
-                B = [ktile_off(16 * b + (l & 7) + 8 * (l >> 4), 16 * ks + 8 * ((l >> 3) & 1)) for l in range(32)]
-                for addrs in (A, B):
-                    assert all(x % 16 == 0 for x in addrs)
-                    assert wavefronts([x // 4 for x in addrs], 4) == 4
-
-
-def test_gram_result_stores_are_conflict_free():
-    for a in range(4):
-        for b in range(a + 1):
-            for n in range(2):
-                for rh in range(2):
-                    addrs = [el(a, b, (l >> 2) + 8 * rh, 8 * n + 2 * (l & 3)) for l in range(32)]
-                    assert wavefronts(addrs, 2) == 2
-
-
-def test_diagonal_solves_are_conflict_free():
-    for a in range(4):   # lane j < 16 solves column j of block (a, a)
+def test_row_accesses_are_conflict_free():
+    for w in range(4):   # gram row stores: lanes < 16 of warp w store row `lane` of block row w
+        for s4 in range(4 * (w + 1)):
+            k, c = s4 >> 2, 4 * (s4 & 3)
+            assert wavefronts([el(w, k, l, c) if l < 16 else None for l in range(32)], 4) == 2
+    for a in range(4):   # diagonal solves: lanes 0-15 record 0, 16-31 record 1
         for rr in range(16):
-            assert wavefronts([TRI + el(a, a, rr, l) if l < 16 else None for l in range(32)], 1) == 1
-            assert wavefronts([vbi(16 * a + rr) if l < 16 else None for l in range(32)], 1) == 1
+            assert wavefronts([(l >> 4) * TRI + el(a, a, rr, l & 15) for l in range(32)], 1) == 1
+            assert wavefronts([(l >> 4) * 80 + vbi(16 * a + rr) for l in range(32)], 1) == 1
 
 
 def test_record_stage_is_conflict_free():
     for m in range(4):
         for w in range(4):
-            st = []
-            for l in range(32):
-                e8 = 32 * w + l + 128 * m
-                st.append(sw128(e8 >> 3, (e8 & 7) * 16) // 4)
-            assert wavefronts(st, 4) == 4   # M2 stores: four full 128-byte rows
             for first in (True, False):
                 an, ab = [], []
                 for l in range(32):
@@ -163,7 +127,7 @@ def test_record_stage_is_conflict_free():
                     h0 = 4 * ((b & 1) ^ ((sw(r) >> 2) & 1))
                     h = h0 if first else h0 ^ 4
                     an.append(TRI + el(a, b, r, c0 + h) if b <= a else None)
-                    ab.append(vbi(8 * j + h) if b <= a else None)
+                    ab.append(80 + vbi(8 * j + h) if b <= a else None)
                 assert wavefronts(an, 4) == 4
                 assert wavefronts(ab, 4) <= 4
 
@@ -175,7 +139,7 @@ def test_planted_unswizzled_layout_conflicts():
 
 
 # The kernel source this model was last checked against (code only; comments do not count).
-MODELLED_SOURCE = ("gdn_chunk_inverse.cuh", "b72c9e833edf")
+MODELLED_SOURCE = ("build_gdn_prep.cu", "e619cdf67e60")
 
 
 def test_model_is_checked_against_the_current_kernel_source():
