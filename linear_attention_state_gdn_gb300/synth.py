@@ -5,11 +5,13 @@ describe (key/value tensors, gates, segment boundaries, cached (lam, P, S) tripl
 holds none of the recurrence or composition arithmetic, so both the CUDA path and the
 fp64 oracle can consume the same bytes from it.
 
-All draws use numpy's PCG64 with a fixed draw order (k, v, gate, beta, then lengths),
-are made in float32/float64 on the host and cast once (round-to-nearest-even) to the
-input dtype. The oracle receives exactly the cast values, converted to float64.
+All draws use numpy's PCG64 with a fixed draw order (k, v, gate, beta, then q when the
+outputs are wanted, then lengths), are made in float32/float64 on the host and cast once
+(round-to-nearest-even) to the input dtype. The oracle receives exactly the cast values,
+converted to float64. q is drawn last, so the other inputs of a seed do not depend on
+whether it is drawn: (S, T_C) does not read it, only the segment outputs do.
 
-Workloads (all synthetic; q is not drawn because (S, T_C) does not read it):
+Workloads (all synthetic):
 
   gdn_tiny      GDN, fp32, 2 heads, d_k=d_v=32, 4 segments x 128 tokens;
                 k ~ N(0,1) L2-normalised per token, v ~ N(0,1), beta = sigmoid(N(0,1)),
@@ -23,6 +25,10 @@ Workloads (all synthetic; q is not drawn because (S, T_C) does not read it):
                 log alpha = -0.05 softplus(N(0,1)).
   gdn_compose   48 layers x 32 heads, d=128, 64 segments with lengths uniform in
                 [256, 1024]; per layer the same draw recipe as ``gdn``.
+  kda           the channel-gated delta rule at the ``gdn`` shape (32 value / 16 key heads,
+                d=128, 16 x 2048 tokens, bf16); the same recipe with a per-channel
+                log alpha = -0.05 softplus(N(0,1)) [N, H_v, d_k].
+  q (outputs)   q ~ N(0,1)/sqrt(d) per element, in the input dtype, [N, H_k, d_k].
 """
 from __future__ import annotations
 
@@ -34,7 +40,8 @@ from typing import Optional
 import numpy as np
 import torch
 
-FAMILY_IDS = {"linear": 0, "scalar": 1, "diag": 2, "delta": 3, "gdn": 4}
+FAMILY_IDS = {"linear": 0, "scalar": 1, "diag": 2, "delta": 3, "gdn": 4, "kda": 5}
+DELTA_FAMILIES = ("gdn", "delta", "kda")
 
 
 @dataclass
@@ -49,9 +56,10 @@ class SegmentInputs:
     seg_offsets: np.ndarray                 # int64 [n_seg + 1]
     k: torch.Tensor                         # [N, H_k, d_k] dtype
     v: torch.Tensor                         # [N, H_v, d_v] dtype
-    log_gate: Optional[torch.Tensor] = None   # fp32: SCALAR [N,H_v] | DIAG [N,H_v,d_k] | GDN [N,H_v]
+    log_gate: Optional[torch.Tensor] = None   # fp32: SCALAR [N,H_v] | DIAG, KDA [N,H_v,d_k] | GDN [N,H_v]
     log_gamma: Optional[torch.Tensor] = None  # fp32 [H_v] (SCALAR constant gate)
     beta: Optional[torch.Tensor] = None       # fp32 [N, H_v]
+    q: Optional[torch.Tensor] = None          # [N, H_k, d_k] dtype (segment outputs only)
     meta: dict = field(default_factory=dict)
 
     @property
@@ -63,7 +71,7 @@ class SegmentInputs:
         return int(self.seg_offsets[-1])
 
     def tensors(self):
-        return {n: getattr(self, n) for n in ("k", "v", "log_gate", "log_gamma", "beta")
+        return {n: getattr(self, n) for n in ("k", "v", "log_gate", "log_gamma", "beta", "q")
                 if getattr(self, n) is not None}
 
 
@@ -122,35 +130,40 @@ def offsets_from_lengths(lengths) -> np.ndarray:
 def make_inputs(family: str, H_k: int, H_v: int, d: int, seg_lens, dtype=torch.bfloat16,
                 seed: int = 0, k_scale: Optional[float] = None, l2norm_k: Optional[bool] = None,
                 alpha_scale: float = 0.05, beta_shift: float = 0.0, gla_div: float = 16.0,
-                retnet_gammas: bool = True, per_token_scalar: bool = False) -> SegmentInputs:
+                retnet_gammas: bool = True, per_token_scalar: bool = False,
+                with_q: bool = False) -> SegmentInputs:
     """Draw one layer of inputs for any family at any size (tests use small ragged ones).
 
-    GDN / DELTA: k L2-normalised (default), v ~ N(0,1), beta = sigmoid(N(0,1) + beta_shift),
-                 GDN log alpha = -alpha_scale softplus(N(0,1)).
+    GDN / DELTA / KDA: k L2-normalised (default), v ~ N(0,1), beta = sigmoid(N(0,1) +
+                 beta_shift), GDN log alpha = -alpha_scale softplus(N(0,1)) per token, KDA
+                 the same per key channel.
     SCALAR:      k, v ~ N(0,1) * k_scale (default 1/sqrt(d)); constant per-head
                  gamma_h = 1 - 2^(-5 - 3h/15) (retnet_gammas) or, with per_token_scalar,
                  a per-token log gate logsigmoid(N(0,1))/gla_div.
     DIAG:        k, v ~ N(0,1) * k_scale; log g = logsigmoid(N(0,1))/gla_div per channel.
     LINEAR:      k, v ~ N(0,1) * k_scale.
+    with_q:      q ~ N(0,1) / sqrt(d), drawn after everything else.
     """
     rng = _rng(seed)
     offs = offsets_from_lengths(seg_lens)
     N = int(offs[-1])
     if l2norm_k is None:
-        l2norm_k = family in ("gdn", "delta")
+        l2norm_k = family in DELTA_FAMILIES
     if k_scale is None:
-        k_scale = 1.0 if family in ("gdn", "delta") else 1.0 / math.sqrt(d)
+        k_scale = 1.0 if family in DELTA_FAMILIES else 1.0 / math.sqrt(d)
     k = _normal(rng, (N, H_k, d))
     v = _normal(rng, (N, H_v, d))
     if l2norm_k:
         k = _l2norm_rows(k)
     else:
         k = k * k_scale
-    if family not in ("gdn", "delta"):
+    if family not in DELTA_FAMILIES:
         v = v * k_scale
     inp = SegmentInputs(family, dtype, H_k, H_v, d, d, offs, _to(k, dtype), _to(v, dtype))
     if family == "gdn":
         inp.log_gate = _to(-alpha_scale * _softplus(_normal(rng, (N, H_v))), torch.float32)
+    elif family == "kda":
+        inp.log_gate = _to(-alpha_scale * _softplus(_normal(rng, (N, H_v, d))), torch.float32)
     elif family == "diag":
         inp.log_gate = _to(_logsigmoid(_normal(rng, (N, H_v, d))) / gla_div, torch.float32)
     elif family == "scalar":
@@ -161,18 +174,21 @@ def make_inputs(family: str, H_k: int, H_v: int, d: int, seg_lens, dtype=torch.b
             inp.log_gamma = _to(np.log1p(-np.exp2(-5.0 - 3.0 * h / 15.0)), torch.float32)
         else:
             inp.log_gamma = _to(-np.abs(_normal(rng, (H_v,))) * 1e-3, torch.float32)
-    if family in ("gdn", "delta"):
+    if family in DELTA_FAMILIES:
         inp.beta = _to(_sigmoid(_normal(rng, (N, H_v)) + beta_shift), torch.float32)
+    if with_q:
+        inp.q = _to(_normal(rng, (N, H_k, d)) / math.sqrt(d), dtype)
     return inp
 
 
 # --------------------------------------------------------------------------------------
 # The five named workloads
 
-WORKLOADS = ("gdn_tiny", "retnet", "gla", "gdn", "gdn_compose", "gdn_one_segment", "retnet_one_segment")
+WORKLOADS = ("gdn_tiny", "retnet", "gla", "gdn", "gdn_compose", "gdn_one_segment", "retnet_one_segment",
+             "kda")
 
 WORKLOAD_SEEDS = {"gdn_tiny": 1001, "retnet": 1002, "gla": 1003, "gdn": 1004, "gdn_compose": 1005,
-                  "gdn_one_segment": 1006, "retnet_one_segment": 1007}
+                  "gdn_one_segment": 1006, "retnet_one_segment": 1007, "kda": 1008}
 
 
 def workload_info(name: str) -> dict:
@@ -191,6 +207,9 @@ def workload_info(name: str) -> dict:
     if name == "retnet_one_segment":   # the RetNet prompt cached as one segment
         return dict(family="scalar", dtype="bf16", H_k=16, H_v=16, d=128, seg_lens=[16384],
                     layers=1)
+    if name == "kda":   # the channel-gated delta rule at the GDN shape
+        return dict(family="kda", dtype="bf16", H_k=16, H_v=32, d=128, seg_lens=[2048] * 16,
+                    layers=1)
     if name == "gdn_one_segment":   # the GDN prompt cached as one segment
         return dict(family="gdn", dtype="bf16", H_k=16, H_v=32, d=128, seg_lens=[32768], layers=1)
     if name == "gdn_compose":
@@ -200,20 +219,22 @@ def workload_info(name: str) -> dict:
     raise KeyError(name)
 
 
-def make_workload(name: str, layer: int = 0) -> SegmentInputs:
-    """Draw the inputs of a named workload (one layer; gdn_compose takes layer in [0, 48))."""
+def make_workload(name: str, layer: int = 0, with_q: bool = False) -> SegmentInputs:
+    """Draw the inputs of a named workload (one layer; gdn_compose takes layer in [0, 48));
+    with_q also draws the queries the segment outputs read."""
     info = workload_info(name)
     seed = WORKLOAD_SEEDS[name] * 1000 + layer
     fam, d = info["family"], info["d"]
     if name == "gdn_tiny":
-        inp = make_inputs("gdn", 2, 2, 32, info["seg_lens"], torch.float32, seed, alpha_scale=0.1)
+        inp = make_inputs("gdn", 2, 2, 32, info["seg_lens"], torch.float32, seed, alpha_scale=0.1,
+                          with_q=with_q)
     elif name in ("retnet", "retnet_one_segment"):
-        inp = make_inputs("scalar", 16, 16, d, info["seg_lens"], torch.bfloat16, seed)
+        inp = make_inputs("scalar", 16, 16, d, info["seg_lens"], torch.bfloat16, seed, with_q=with_q)
     elif name == "gla":
-        inp = make_inputs("diag", 16, 16, d, info["seg_lens"], torch.bfloat16, seed)
+        inp = make_inputs("diag", 16, 16, d, info["seg_lens"], torch.bfloat16, seed, with_q=with_q)
     else:
-        inp = make_inputs("gdn", info["H_k"], info["H_v"], d, info["seg_lens"], torch.bfloat16,
-                          seed, alpha_scale=0.05)
+        inp = make_inputs(fam, info["H_k"], info["H_v"], d, info["seg_lens"], torch.bfloat16,
+                          seed, alpha_scale=0.05, with_q=with_q)
     inp.meta = dict(workload=name, layer=layer, seed=seed, **info)
     return inp
 
@@ -250,7 +271,7 @@ def make_compose_inputs(family: str, n_seg: int, n_units: int, d: int, seed: int
     if family == "linear":
         lam[:] = 0
     P = None
-    if family in ("gdn", "delta"):
+    if family in DELTA_FAMILIES:
         P = _normal(rng, (n_seg, n_units, d, d)) * np.float32(p_norm / (2.0 * math.sqrt(d)))
     S0 = _normal(rng, (n_units, d, d)) if with_S0 else None
     t = lambda x: None if x is None else torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))

@@ -27,7 +27,7 @@ _LIB = os.path.join(_HERE, "libhypic_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-FAMILIES = {"linear": 0, "scalar": 1, "diag": 2, "delta": 3, "gdn": 4}
+FAMILIES = {"linear": 0, "scalar": 1, "diag": 2, "delta": 3, "gdn": 4, "kda": 5}
 
 
 def build(force: bool = False) -> str:
@@ -55,8 +55,9 @@ def _load():
             lib.oracle_compose_scan.argtypes = [I, I64, I, I, P, P, P, P, I]
             lib.oracle_materialize_T.argtypes = [I, I64, I, P, P, P]
             lib.oracle_compose_transitions.argtypes = [I, I, I64, I, P, P, P, P, I]
+            lib.oracle_outputs.argtypes = [I, I, P, I, I, I, I, P, P, P, P, P, P, P, P, I]
             for f in (lib.oracle_build, lib.oracle_run, lib.oracle_compose_scan,
-                      lib.oracle_materialize_T, lib.oracle_compose_transitions):
+                      lib.oracle_materialize_T, lib.oracle_compose_transitions, lib.oracle_outputs):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -128,6 +129,27 @@ def run_sequential(family, seg_offsets, k, v, log_gate=None, log_gamma=None, bet
     return out
 
 
+def outputs(family, seg_offsets, k, v, q, log_gate=None, log_gamma=None, beta=None, S_init=None,
+            nthreads=0):
+    """o_t = S_t^T q_t for every token, fp64: [N_tok, H_v, d_v]. Each segment starts from
+    S_init[seg, h] ([n_seg, H_v, d_k, d_v]; None = zero state, the outputs O(C|0))."""
+    lib = _load()
+    offs = np.ascontiguousarray(seg_offsets, dtype=np.int64)
+    k, v, q = _f64(k), _f64(v), _f64(q)
+    log_gate, log_gamma, beta, S_init = _f64(log_gate), _f64(log_gamma), _f64(beta), _f64(S_init)
+    N, Hk, dk = k.shape
+    _, Hv, dv = v.shape
+    assert q.shape == k.shape
+    n_seg = len(offs) - 1
+    out = np.zeros((N, Hv, dv))
+    rc = lib.oracle_outputs(_family(family), n_seg, _ptr(offs), Hk, Hv, dk, dv, _ptr(k), _ptr(v),
+                            _ptr(q), _ptr(log_gate), _ptr(log_gamma), _ptr(beta), _ptr(S_init),
+                            _ptr(out), nthreads or default_threads())
+    if rc != 0:
+        raise RuntimeError(f"oracle_outputs failed ({rc})")
+    return out
+
+
 def compose_scan(T, S, S0=None, nthreads=0):
     """prefix_j = T_j prefix_{j-1} + S_j; T [n_seg, U, d_k, d_k], S [n_seg, U, d_k, d_v]."""
     lib = _load()
@@ -153,7 +175,7 @@ def compose_transitions(family, lam, P=None, d_k=None):
     lib = _load()
     fam = _family(family)
     lam = _f64(lam)
-    dense = fam in (FAMILIES["delta"], FAMILIES["gdn"])
+    dense = fam in (FAMILIES["delta"], FAMILIES["gdn"], FAMILIES["kda"])
     if fam == FAMILIES["diag"]:
         n_seg, U, d_k = lam.shape
     else:
@@ -184,7 +206,7 @@ def materialize_T(family, lam, P=None, d_k=None):
     if fam == FAMILIES["diag"]:
         d_k = lam.shape[-1]
         lead = lam.shape[:-1]
-    elif fam in (FAMILIES["delta"], FAMILIES["gdn"]):
+    elif fam in (FAMILIES["delta"], FAMILIES["gdn"], FAMILIES["kda"]):
         P = _f64(P)
         d_k = P.shape[-1]
         lead = P.shape[:-2]

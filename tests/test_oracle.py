@@ -431,3 +431,159 @@ def test_naive_add_fails_for_retnet_by_the_predicted_amount():
     naive = S[0, 0] + S[1, 0]
     np.testing.assert_allclose(naive - seq[1, 0], (1 - g ** 60) * S[0, 0], rtol=1e-11, atol=1e-13)
     assert relF(naive, seq[1, 0]) > 1e-2
+
+
+# ------------------------------------------------------------------ KDA (channel-gated delta rule)
+
+def _kda_inputs(L, d, seed, **kw):
+    return synth.make_inputs("kda", 1, 2, d, [L], torch.float64, seed=seed, alpha_scale=0.3, **kw)
+
+
+def test_golden_kda_outputs():
+    g = json.load(open(os.path.join(GOLDEN, "kda_d2_outputs.json")))
+    k = np.array(g["k"])[:, None, :]
+    v = np.array(g["v"])[:, None, :]
+    q = np.array(g["q"])[:, None, :]
+    beta = np.array(g["beta"])[:, None]
+    lg = np.log(np.array(g["alpha"]))[:, None, :]
+    S, T = oracle.build_segments("kda", g["seg_offsets"], k, v, lg, None, beta)
+    np.testing.assert_allclose(S[0, 0], g["S_C"], atol=1e-14)
+    np.testing.assert_allclose(T[0, 0], g["T_C"], atol=1e-14)
+    O = oracle.outputs("kda", g["seg_offsets"], k, v, q, lg, None, beta)
+    np.testing.assert_allclose(O[:, 0], g["O"], atol=1e-14)
+
+
+def test_kda_with_equal_channel_gates_is_gdn():
+    """A per-channel decay that is the same on every channel is the GDN scalar gate."""
+    inp = _kda_inputs(37, 6, seed=160)
+    a = f64(inp.log_gate)[:, :, 0]
+    inp.log_gate = torch.from_numpy(np.repeat(a[:, :, None], 6, axis=2))
+    gdn = synth.make_inputs("gdn", 1, 2, 6, [37], torch.float64, seed=160)
+    gdn.k, gdn.v, gdn.beta, gdn.log_gate = inp.k, inp.v, inp.beta, torch.from_numpy(a)
+    S1, T1 = run_build(inp)
+    S2, T2 = run_build(gdn)
+    assert relF(S1, S2) < 1e-13 and relF(T1, T2) < 1e-13
+
+
+def test_kda_with_beta_zero_is_the_diagonal_decay():
+    """b = 0 removes the delta update and the write: S = 0 and T = Diag(prod_t a_t), the GLA
+    transition of the same gates."""
+    inp = _kda_inputs(23, 5, seed=161)
+    inp.beta = torch.zeros_like(inp.beta)
+    S, T = run_build(inp)
+    assert np.all(S == 0)
+    diag = synth.make_inputs("diag", 1, 2, 5, [23], torch.float64, seed=161)
+    diag.log_gate = inp.log_gate
+    _, T_diag = run_build(diag)
+    np.testing.assert_allclose(T, T_diag, rtol=1e-13, atol=0)
+
+
+def test_kda_retrieves_last_write_so_the_gate_comes_first():
+    """b_L = 1, |k_L| = 1: k_L^T S = v_L^T and k_L^T T = 0 whatever the decays, which holds only
+    with the decay applied before the delta update, (I - k k^T) Diag(a), not after it."""
+    inp = _kda_inputs(6, 4, seed=162)
+    kl = np.array([0.6, 0.0, -0.8, 0.0])
+    inp.k[-1, 0] = torch.from_numpy(kl)
+    inp.beta[-1, :] = 1.0
+    S, T = run_build(inp)
+    for h in range(2):
+        np.testing.assert_allclose(kl @ S[0, h], f64(inp.v)[-1, h], atol=1e-14)
+        np.testing.assert_allclose(kl @ T[0, h], np.zeros(4), atol=1e-15)
+
+
+def test_kda_det_invariant():
+    """det T = prod_t (1 - b_t |k_t|^2) prod_i a_t[i]."""
+    inp = synth.make_inputs("kda", 1, 1, 6, [11], torch.float64, seed=163, l2norm_k=False,
+                            k_scale=0.5, alpha_scale=0.3)
+    S, T = run_build(inp)
+    k, b = f64(inp.k)[:, 0], f64(inp.beta)[:, 0]
+    sign, logdet = np.linalg.slogdet(T[0, 0])
+    expect = f64(inp.log_gate)[:, 0].sum() + np.sum(np.log(np.abs(1 - b * (k * k).sum(1))))
+    assert sign == np.prod(np.sign(1 - b * (k * k).sum(1)))
+    assert logdet == pytest.approx(expect, rel=1e-12, abs=1e-12)
+
+
+def test_kda_T_is_the_jacobian_and_segments_compose():
+    inp = synth.make_inputs("kda", 1, 2, 8, [30, 0, 17], torch.float64, seed=164, alpha_scale=0.3)
+    S, T = run_build(inp)
+    seq = run_seq(inp)
+    np.testing.assert_allclose(oracle.compose_scan(T, S), seq, rtol=1e-11, atol=1e-12)
+    S0 = np.random.default_rng(1).standard_normal((2, 8, 8))
+    with_s0 = run_seq(inp, S0=S0)
+    np.testing.assert_allclose(with_s0[-1] - seq[-1], np.einsum("hij,hjk->hik", T[2] @ T[1] @ T[0], S0),
+                               rtol=1e-10, atol=1e-12)
+
+
+# ------------------------------------------------------------------ segment outputs o_t = S_t^T q_t
+
+def _with_q(family, lens, d=6, seed=170, **kw):
+    return synth.make_inputs(family, 2, 4, d, lens, torch.float64, seed=seed, with_q=True, **kw)
+
+
+def run_out(inp, S_init=None):
+    return oracle.outputs(inp.family, inp.seg_offsets, f64(inp.k), f64(inp.v), f64(inp.q),
+                          f64(inp.log_gate), f64(inp.log_gamma), f64(inp.beta), S_init=S_init)
+
+
+def test_outputs_linear_closed_form():
+    """Plain linear attention: o_t = sum_{s <= t in the segment} (q_t . k_s) v_s."""
+    inp = _with_q("linear", [9, 0, 5])
+    O = run_out(inp)
+    k, v, q = f64(inp.k), f64(inp.v), f64(inp.q)
+    for j in range(inp.n_seg):
+        a, b = inp.seg_offsets[j], inp.seg_offsets[j + 1]
+        for t in range(a, b):
+            for h in range(4):
+                hk = h // 2
+                ref = sum((q[t, hk] @ k[s, hk]) * v[s, h] for s in range(a, t + 1))
+                np.testing.assert_allclose(O[t, h], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_outputs_scalar_decay_closed_form():
+    """RetNet: o_t = sum_{s <= t} gamma^(t - s) (q_t . k_s) v_s within the segment."""
+    inp = _with_q("scalar", [12, 7])
+    O = run_out(inp)
+    k, v, q, lg = f64(inp.k), f64(inp.v), f64(inp.q), f64(inp.log_gamma)
+    for j in range(inp.n_seg):
+        a, b = inp.seg_offsets[j], inp.seg_offsets[j + 1]
+        for t in range(a, b):
+            for h in range(4):
+                ref = sum(np.exp((t - s) * lg[h]) * (q[t, h // 2] @ k[s, h // 2]) * v[s, h]
+                          for s in range(a, t + 1))
+                np.testing.assert_allclose(O[t, h], ref, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("family", ["linear", "scalar", "diag", "delta", "gdn", "kda"])
+def test_last_output_reads_the_end_state(family):
+    """The output of a segment's last token is S(C|0)^T q_L, with S(C|0) from the build."""
+    inp = _with_q(family, [13, 1, 8], alpha_scale=0.3, gla_div=4.0)
+    O = run_out(inp)
+    S, _ = run_build(inp, want_T=False)
+    q = f64(inp.q)
+    for j in range(inp.n_seg):
+        t = inp.seg_offsets[j + 1] - 1
+        for h in range(4):
+            np.testing.assert_allclose(O[t, h], S[j, h].T @ q[t, h // 2], rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("family", ["linear", "scalar", "diag", "delta", "gdn", "kda"])
+def test_outputs_after_a_prefix_state_are_corrected_by_the_transition(family):
+    """Starting a segment from a prefix state S0 adds (T_{<=t} S0)^T q_t to every output,
+    T_{<=t} the transition of the segment's tokens up to t (the build's T of the prefix of the
+    segment that ends at t)."""
+    L = 10
+    inp = _with_q(family, [L], alpha_scale=0.3, gla_div=4.0)
+    S0 = np.random.default_rng(2).standard_normal((1, 4, 6, 6))
+    dO = run_out(inp, S_init=S0) - run_out(inp)
+    q = f64(inp.q)
+    for t in range(L):
+        part = synth.make_inputs(family, 2, 4, 6, [t + 1], torch.float64, seed=170, with_q=True,
+                                 alpha_scale=0.3, gla_div=4.0)
+        for n in ("k", "v", "q", "log_gate", "beta"):
+            if getattr(inp, n) is not None:
+                setattr(part, n, getattr(inp, n)[: t + 1])
+        part.log_gamma = inp.log_gamma
+        _, T = run_build(part)
+        for h in range(4):
+            np.testing.assert_allclose(dO[t, h], (T[0, h] @ S0[0, h]).T @ q[t, h // 2],
+                                       rtol=1e-10, atol=1e-12)
