@@ -5,7 +5,9 @@
  *
  *  hypic_build_segments  prefill every cached prompt segment C of one layer into the pair
  *                        (S(C|0), T_C): the zero-initial end state and the segment-cumulative
- *                        transition operator.
+ *                        transition operator; optionally also the segment's outputs
+ *                        o_t = S_t^T q_t for every token (the prefill's own outputs, from a
+ *                        zero state or from a given prefix state).
  *                        Source: "Cut First-Token Latency by 3.25x: Introducing HYPIC for
  *                        Position-Independent Caching in Hybrid-Attention LLMs" (besthub.dev),
  *                        paragraph "For linear layers" (HYPIC stores the pair (T_C, S(C|0))
@@ -30,6 +32,9 @@
  *   HYPIC_FAM_DIAG    S_t = Diag(g_t) S_{t-1} + k_t v_t^T   (GLA)             T_C = Diag(prod g_t)
  *   HYPIC_FAM_DELTA   S_t = (I - b_t k_t k_t^T) S_{t-1} + b_t k_t v_t^T       T_C = prod (I - b k k^T)
  *   HYPIC_FAM_GDN     S_t = a_t (I - b_t k_t k_t^T) S_{t-1} + b_t k_t v_t^T   T_C = prod a_t (I - b k k^T)
+ *   HYPIC_FAM_KDA     S_t = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} + b_t k_t v_t^T
+ *                                                            T_C = prod (I - b k k^T) Diag(a_t)
+ *                     (the channel-gated delta rule: a per-key-channel decay a_t)
  *
  * with products ordered latest step leftmost (GDN: "Gated Delta Networks: Improving Mamba2
  * with Delta Rule", reference 7 of the episode-companion page "Hypic: Position-Independent
@@ -43,6 +48,8 @@
  *   DIAG             lam = sum_t log g_t (per key channel)      [seg][head][d_k]
  *   DELTA / GDN      lam = sum_t log a_t (0 for DELTA)          [seg][head]
  *                    P = prod_t (I - b_t k_t k_t^T), gate-free  [seg][head][d_k][d_k] fp32
+ *   KDA              lam = sum_t max_i log a_t[i]              [seg][head]
+ *                    P = exp(-lam) T_C                          [seg][head][d_k][d_k] fp32
  *
  * Conventions shared by every call:
  *   - Ownership: the caller allocates and owns every buffer. The library allocates no
@@ -88,7 +95,8 @@ typedef enum {
     HYPIC_FAM_SCALAR = 1,
     HYPIC_FAM_DIAG = 2,
     HYPIC_FAM_DELTA = 3,
-    HYPIC_FAM_GDN = 4
+    HYPIC_FAM_GDN = 4,
+    HYPIC_FAM_KDA = 5
 } hypic_family;
 
 typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
@@ -107,12 +115,12 @@ typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  *   v                 [N_tok][H_v][d_v]  dtype
  *   log_gate          SCALAR: [N_tok][H_v] log g_t (or NULL when log_gamma is given);
  *                     DIAG: [N_tok][H_v][d_k] log g_t; GDN: [N_tok][H_v] log a_t;
- *                     LINEAR, DELTA: NULL
+ *                     KDA: [N_tok][H_v][d_k] log a_t; LINEAR, DELTA: NULL
  *   log_gamma         SCALAR with a constant per-head decay: [H_v] log gamma_h; else NULL
- *   beta              DELTA, GDN: [N_tok][H_v] b_t; else NULL
+ *   beta              DELTA, GDN, KDA: [N_tok][H_v] b_t; else NULL
  *   S                 out [n_seg][H_v][d_k][d_v] fp32 (segment stride out_seg_stride units)
  *   lam               out [n_seg][H_v] fp32, DIAG [n_seg][H_v][d_k]
- *   P                 out DELTA / GDN: [n_seg][H_v][d_k][d_k] fp32; else NULL
+ *   P                 out DELTA / GDN / KDA: [n_seg][H_v][d_k][d_k] fp32; else NULL
  *   workspace         device scratch, at least hypic_build_workspace_bytes() bytes, 16-byte
  *                     aligned (NULL when that is 0). What it holds:
  *                     - DELTA / GDN with bf16 k, v and d = 128: 8 KB per (segment, value
@@ -130,6 +138,21 @@ typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  *                     undefined after the call and it may be reused by the next call on the
  *                     same stream, but not by a call still running on another stream. It must
  *                     not overlap any argument.
+ *   q                 optional [N_tok][H_k][d_k] dtype, 16-byte aligned: the queries; given
+ *                     exactly when O is
+ *   O                 optional out [N_tok][H_v][d_v] dtype, 16-byte aligned: o_t = S_t^T q_t,
+ *                     the state after token t read with its query, for every token of every
+ *                     segment (besthub.dev, paragraph "For linear layers": the pair is stored
+ *                     during the first prefill, whose outputs these are; paragraph "Segment
+ *                     parallelism": cold segments are prefilled by scatter workers). It may
+ *                     not overlap k, v, q, S, lam or P.
+ *   S_init            optional [n_seg][H_v][d_k][d_v] fp32, 16-byte aligned: the state each
+ *                     segment starts from (NULL = zero). With it, S is S(C|S_init) and O the
+ *                     outputs of the segment reused after that prefix state; T_C does not
+ *                     change. (S_init is indexed by segment and head, stride H_v, whatever
+ *                     out_seg_stride is.)
+ *   A call with O or S_init, and every KDA call, runs the exact CUDA-core path (fp32
+ *   arithmetic, one thread per state column); the tensor-core builds compute neither.
  */
 typedef struct {
     int32_t family;
@@ -152,6 +175,9 @@ typedef struct {
     float *P;
     void *workspace;
     size_t workspace_bytes;
+    const void *q;          /* ABI 4 */
+    void *O;
+    const float *S_init;
 } hypic_build_args;
 
 /* Arguments of hypic_compose_scan.
@@ -162,14 +188,14 @@ typedef struct {
  *   d_k, d_v     head sizes (equal; 32, 64 or 128)
  *   S            [n_seg][n_units][d_k][d_v] fp32: S(C_j|0) of every segment
  *   lam          [n_seg][n_units] fp32 (DIAG: [n_seg][n_units][d_k]); NULL for LINEAR
- *   P            DELTA / GDN: [n_seg][n_units][d_k][d_k] fp32; else NULL
+ *   P            DELTA / GDN / KDA: [n_seg][n_units][d_k][d_k] fp32; else NULL
  *   S0           optional initial state [n_units][d_k][d_v] fp32; NULL = zero state
  *   prefix       out [n_seg][n_units][d_k][d_v] fp32: prefix[j] = state after segments
  *                0..j, i.e. exp(lam_j) P_j prefix[j-1] + S_j with prefix[-1] = S0
  *   lam_total    optional out (NULL = skip): the log-scale of the transition of all n_seg
  *                segments composed; [n_units] (DIAG: [n_units][d_k]); 4-byte aligned.
  *                sum_j lam_j (0 for LINEAR), minus E ln 2 when P_total carries a scale 2^E.
- *   P_total      optional out (NULL = skip), DELTA / GDN only (must be NULL otherwise, and
+ *   P_total      optional out (NULL = skip), DELTA / GDN / KDA only (must be NULL otherwise, and
  *                needs lam_total): 2^E P_{n-1} ... P_0 [n_units][d_k][d_k] fp32, latest
  *                segment leftmost, 16-byte aligned. The product of many contractions leaves
  *                the fp32 range (64 segments of a few hundred tokens: about 1e-49), so the
@@ -251,7 +277,8 @@ hypic_status hypic_probe_wait_timeout(uint32_t limit_us, void *stream);
 const char *hypic_status_string(hypic_status status);
 
 /* Library ABI version (incremented on any change to the structs above or to the meaning of
- * their fields). 3: P_total needs lam_total and may carry a power-of-two scale. */
+ * their fields). 3: P_total needs lam_total and may carry a power-of-two scale. 4: KDA; the
+ * build's q, O and S_init. */
 int32_t hypic_abi_version(void);
 
 #ifdef __cplusplus

@@ -21,7 +21,8 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libhypic.so")
 
-FAMILY = {"linear": 0, "scalar": 1, "diag": 2, "delta": 3, "gdn": 4}
+FAMILY = {"linear": 0, "scalar": 1, "diag": 2, "delta": 3, "gdn": 4, "kda": 5}
+DENSE = ("delta", "gdn", "kda")
 DTYPE = {torch.bfloat16: 0, torch.float32: 1}
 STATUS = {0: "HYPIC_OK", 1: "HYPIC_ERR_INVALID_ARG", 2: "HYPIC_ERR_ALIGNMENT",
           3: "HYPIC_ERR_UNSUPPORTED", 4: "HYPIC_ERR_RANGE", 5: "HYPIC_ERR_CUDA",
@@ -43,7 +44,8 @@ class BuildArgs(ctypes.Structure):
                 ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("log_gate", ctypes.c_void_p),
                 ("log_gamma", ctypes.c_void_p), ("beta", ctypes.c_void_p),
                 ("S", ctypes.c_void_p), ("lam", ctypes.c_void_p), ("P", ctypes.c_void_p),
-                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("q", ctypes.c_void_p), ("O", ctypes.c_void_p), ("S_init", ctypes.c_void_p)]
 
 
 class ComposeArgs(ctypes.Structure):
@@ -120,7 +122,8 @@ def _offsets(seg_offsets) -> np.ndarray:
 
 
 def make_build_args(family, k, v, seg_offsets, log_gate=None, log_gamma=None, beta=None,
-                    S=None, lam=None, P=None, out_seg_stride=0, workspace=None):
+                    S=None, lam=None, P=None, out_seg_stride=0, workspace=None, q=None, O=None,
+                    S_init=None):
     """Fill a BuildArgs struct (and keep the host offsets array alive with it)."""
     offs = _offsets(seg_offsets)
     fam = FAMILY[family] if isinstance(family, str) else int(family)
@@ -135,6 +138,7 @@ def make_build_args(family, k, v, seg_offsets, log_gate=None, log_gamma=None, be
     a.k, a.v = _ptr(k), _ptr(v)
     a.log_gate, a.log_gamma, a.beta = _ptr(log_gate), _ptr(log_gamma), _ptr(beta)
     a.S, a.lam, a.P = _ptr(S), _ptr(lam), _ptr(P)
+    a.q, a.O, a.S_init = _ptr(q), _ptr(O), _ptr(S_init)
     if workspace is not None:
         a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
     a._keep = offs
@@ -147,7 +151,7 @@ def build_outputs(family, n_seg, H_v, d, device, out_seg_stride=0):
     lam = torch.empty((n_seg, units, d) if family == "diag" else (n_seg, units),
                       dtype=torch.float32, device=device)
     P = (torch.empty((n_seg, units, d, d), dtype=torch.float32, device=device)
-         if family in ("gdn", "delta") else None)
+         if family in DENSE else None)
     return S, lam, P
 
 
@@ -162,7 +166,7 @@ def _outputs(family, n_seg, v, S, lam, P, out_seg_stride):
         return build_outputs(family, n_seg, H_v, d, v.device, out_seg_stride)
     stride = out_seg_stride or H_v
     units = (n_seg - 1) * stride + H_v if n_seg > 0 else 0
-    dense = family in ("gdn", "delta") or family in (FAMILY["gdn"], FAMILY["delta"])
+    dense = family in DENSE or family in tuple(FAMILY[f] for f in DENSE)
     diag = family in ("diag", FAMILY["diag"])
     need = [(S, units * d * d, "S"), (lam, units * (d if diag else 1), "lam")]
     if dense:
@@ -183,15 +187,20 @@ def hypic_build_workspace_bytes(family, k, v, seg_offsets, **kw) -> int:
 
 def hypic_build_segments(family, k, v, seg_offsets, log_gate=None, log_gamma=None, beta=None,
                          S=None, lam=None, P=None, out_seg_stride=0, workspace=None,
-                         stream=None):
+                         stream=None, q=None, O=None, S_init=None):
     """(S(C|0), lam, P) of every segment: S [n_seg, H_v, d, d], lam [n_seg, H_v]
-    ([n_seg, H_v, d] for "diag"), P [n_seg, H_v, d, d] for "gdn"/"delta" (else None).
-    Outputs are allocated when not given. Asynchronous on `stream`."""
+    ([n_seg, H_v, d] for "diag"), P [n_seg, H_v, d, d] for "gdn"/"delta"/"kda" (else None).
+    With queries q [N, H_k, d] also the segment outputs O [N, H_v, d] (dtype of v; allocated
+    when not given), returned fourth: (S, lam, P, O). S_init [n_seg, H_v, d, d] starts each
+    segment from that state instead of zero. Outputs are allocated when not given.
+    Asynchronous on `stream`."""
     lib = load_library()
     n_seg = len(_offsets(seg_offsets)) - 1
     S, lam, P = _outputs(family, n_seg, v, S, lam, P, out_seg_stride)
+    if q is not None and O is None:
+        O = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     a = make_build_args(family, k, v, seg_offsets, log_gate, log_gamma, beta, S, lam, P,
-                        out_seg_stride)
+                        out_seg_stride, q=q, O=O, S_init=S_init)
     need = int(lib.hypic_build_workspace_bytes(ctypes.byref(a)))
     if need and workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=v.device)
@@ -199,7 +208,7 @@ def hypic_build_segments(family, k, v, seg_offsets, log_gate=None, log_gamma=Non
         a.workspace = _ptr(workspace)
         a.workspace_bytes = workspace.numel() * workspace.element_size()
     _check(lib.hypic_build_segments(ctypes.byref(a), _stream(stream)), "hypic_build_segments")
-    return S, lam, P
+    return (S, lam, P) if q is None else (S, lam, P, O)
 
 
 def hypic_build_segments_static_ws(family, k, v, seg_offsets, log_gate=None, log_gamma=None,

@@ -114,24 +114,28 @@ bool head_size_ok(int d_k, int d_v) {
 
 hypic_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA; }
 
-enum class BuildPath { None, GatedSimt, GatedTc, DeltaSeq, GdnTc };
+enum class BuildPath { None, GatedSimt, GatedTc, Seq, GdnTc };
+
+bool dense_family(int fam) { return fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GDN || fam == HYPIC_FAM_KDA; }
 enum class ComposePath { None, Scaled, DenseSimt, DenseTc };
 
 // Kernel selection for a build (shape/family/dtype only; no pointer checks).
 BuildPath pick_build(const hypic_build_args *a) {
     if (a->n_seg == 0) return BuildPath::None;
+    // the segment outputs, a start state and the channel-gated delta rule: the exact path
+    if (a->O || a->S_init || a->family == HYPIC_FAM_KDA) return BuildPath::Seq;
     const bool delta = a->family == HYPIC_FAM_DELTA || a->family == HYPIC_FAM_GDN;
     BuildParams q{};
     q.family = a->family;
     q.dtype = a->dtype;
     q.D = a->d_k;
-    if (delta) return build_gdn_tc_supported(q) ? BuildPath::GdnTc : BuildPath::DeltaSeq;
+    if (delta) return build_gdn_tc_supported(q) ? BuildPath::GdnTc : BuildPath::Seq;
     return build_gated_tc_supported(q) ? BuildPath::GatedTc : BuildPath::GatedSimt;
 }
 
 ComposePath pick_compose(const hypic_compose_args *a) {
     if (a->n_seg == 0 || a->n_units == 0) return ComposePath::None;
-    const bool dense = a->family == HYPIC_FAM_DELTA || a->family == HYPIC_FAM_GDN;
+    const bool dense = dense_family(a->family);
     if (!dense) return ComposePath::Scaled;
     ComposeParams q{};
     q.D = a->d_k;
@@ -267,14 +271,14 @@ SplitLayout gdn_split_layout(const hypic_build_args *a, size_t base) {
 }
 
 bool build_shape_ok(const hypic_build_args *a) {
-    return a && a->family >= HYPIC_FAM_LINEAR && a->family <= HYPIC_FAM_GDN &&
+    return a && a->family >= HYPIC_FAM_LINEAR && a->family <= HYPIC_FAM_KDA &&
            (a->dtype == HYPIC_BF16 || a->dtype == HYPIC_F32) && a->n_seg >= 0 &&
            a->n_seg <= HYPIC_MAX_SEGMENTS && a->H_k > 0 && a->H_v > 0 && a->H_v % a->H_k == 0 &&
            head_size_ok(a->d_k, a->d_v);
 }
 
 bool compose_shape_ok(const hypic_compose_args *a) {
-    return a && a->family >= HYPIC_FAM_LINEAR && a->family <= HYPIC_FAM_GDN && a->n_seg >= 0 &&
+    return a && a->family >= HYPIC_FAM_LINEAR && a->family <= HYPIC_FAM_KDA && a->n_seg >= 0 &&
            a->n_units >= 0 && head_size_ok(a->d_k, a->d_v);
 }
 
@@ -282,7 +286,7 @@ bool compose_shape_ok(const hypic_compose_args *a) {
 
 extern "C" {
 
-int32_t hypic_abi_version(void) { return 3; }
+int32_t hypic_abi_version(void) { return 4; }
 
 const char *hypic_status_string(hypic_status s) {
     switch (s) {
@@ -311,7 +315,7 @@ size_t hypic_build_workspace_bytes(const hypic_build_args *a) {
 hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
     if (!a) return HYPIC_ERR_INVALID_ARG;
     const int fam = a->family;
-    if (fam < HYPIC_FAM_LINEAR || fam > HYPIC_FAM_GDN) return HYPIC_ERR_INVALID_ARG;
+    if (fam < HYPIC_FAM_LINEAR || fam > HYPIC_FAM_KDA) return HYPIC_ERR_INVALID_ARG;
     if (a->dtype != HYPIC_BF16 && a->dtype != HYPIC_F32) return HYPIC_ERR_INVALID_ARG;
     if (a->n_seg < 0 || a->n_seg > HYPIC_MAX_SEGMENTS) return HYPIC_ERR_INVALID_ARG;
     if (a->H_k <= 0 || a->H_v <= 0 || a->H_v % a->H_k != 0) return HYPIC_ERR_INVALID_ARG;
@@ -331,16 +335,17 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
     if (n_tok > INT32_MAX) return HYPIC_ERR_UNSUPPORTED;
 
     // required / forbidden tensors per family
-    const bool delta = fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GDN;
-    const bool need_gate = fam == HYPIC_FAM_DIAG || fam == HYPIC_FAM_GDN;
+    const bool delta = dense_family(fam);
+    const bool need_gate = fam == HYPIC_FAM_DIAG || fam == HYPIC_FAM_GDN || fam == HYPIC_FAM_KDA;
     if (!a->S || !a->lam) return HYPIC_ERR_INVALID_ARG;
+    if ((!a->q) != (!a->O)) return HYPIC_ERR_INVALID_ARG;   // queries exactly when outputs
     if (delta && (!a->P || !a->beta)) return HYPIC_ERR_INVALID_ARG;
     if (need_gate && !a->log_gate) return HYPIC_ERR_INVALID_ARG;
     if (fam == HYPIC_FAM_SCALAR && (!a->log_gate) == (!a->log_gamma)) return HYPIC_ERR_INVALID_ARG;
     if (n_tok > 0 && (!a->k || !a->v)) return HYPIC_ERR_INVALID_ARG;
 
     // alignment (16 B for tensors read or written with vector / bulk accesses)
-    const void *v16[] = {a->k, a->v, a->S, a->P};
+    const void *v16[] = {a->k, a->v, a->S, a->P, a->q, a->O, a->S_init};
     for (const void *p : v16)
         if (p && !aligned(p, 16)) return HYPIC_ERR_ALIGNMENT;
     const void *v4[] = {a->log_gate, a->log_gamma, a->beta, a->lam};
@@ -348,13 +353,26 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
         if (p && !aligned(p, 4)) return HYPIC_ERR_ALIGNMENT;
 
     // every tensor the kernels touch must be device memory of the current device
-    const void *dev_ptrs[] = {a->S, a->lam, a->P, a->log_gamma};
+    const void *dev_ptrs[] = {a->S, a->lam, a->P, a->log_gamma, a->S_init};
     for (const void *p : dev_ptrs)
         if (p && !on_device(p)) return HYPIC_ERR_INVALID_ARG;
     if (n_tok > 0) {
-        const void *in_ptrs[] = {a->k, a->v, a->log_gate, a->beta};
+        const void *in_ptrs[] = {a->k, a->v, a->log_gate, a->beta, a->q, a->O};
         for (const void *p : in_ptrs)
             if (p && !on_device(p)) return HYPIC_ERR_INVALID_ARG;
+    }
+    if (a->O && n_tok > 0) {   // the outputs overlap no input and no other output
+        const size_t el = a->dtype == HYPIC_BF16 ? 2 : 4;
+        const size_t nO = (size_t)n_tok * a->H_v * a->d_v * el;
+        const size_t nk = (size_t)n_tok * a->H_k * a->d_k * el, nv = (size_t)n_tok * a->H_v * a->d_v * el;
+        const int64_t stride = a->out_seg_stride ? a->out_seg_stride : a->H_v;
+        const size_t units = (size_t)((a->n_seg - 1) * stride + a->H_v);
+        const size_t nS = units * a->d_k * a->d_v * 4;
+        const size_t nl = units * (fam == HYPIC_FAM_DIAG ? a->d_k : 1) * 4;
+        if (overlaps(a->O, nO, a->k, nk) || overlaps(a->O, nO, a->v, nv) || overlaps(a->O, nO, a->q, nk) ||
+            overlaps(a->O, nO, a->S, nS) || overlaps(a->O, nO, a->P, delta ? nS : 0) ||
+            overlaps(a->O, nO, a->lam, nl))
+            return HYPIC_ERR_INVALID_ARG;
     }
     const BuildPath path = pick_build(a);
     // records are addressed as 64-row blocks of a 2D tensor map with int32 coordinates
@@ -391,6 +409,9 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
     p.lam = a->lam;
     p.P = a->P;
     p.workspace = a->workspace;
+    p.q = a->q;
+    p.O = a->O;
+    p.S_init = a->S_init;
     p.err = err;
     // the launch table: whole segments, or the chunk-aligned pieces of split ones (piece k of
     // a segment with n chunks in pj pieces covers chunks [k n / pj, (k + 1) n / pj))
@@ -445,7 +466,7 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
         if (e != cudaSuccess || split.slots == 0) return from_cuda(e);
         // compose the pieces of every split segment into its entry: S = the pieces' prefix
         // scan from a zero state (its last state, copied out), lam = sum, P = product
-        const bool dense = fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GDN;
+        const bool dense = dense_family(fam);
         const size_t unit = (size_t)a->d_k * a->d_k;
         const size_t nl = fam == HYPIC_FAM_DIAG ? (size_t)a->d_k : 1;
         const int64_t stride = p.seg_stride;
@@ -498,7 +519,7 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
         }
         return from_cuda(e);
     }
-    case BuildPath::DeltaSeq: return from_cuda(launch_build_delta_seq(p, s));
+    case BuildPath::Seq: return from_cuda(launch_build_seq(p, s));
     case BuildPath::GatedSimt: return from_cuda(launch_build_gated_simt(p, s));
     case BuildPath::None: break;
     }
@@ -524,13 +545,13 @@ hypic_status hypic_build_segments_static_ws(const hypic_build_args *a, void *str
 hypic_status hypic_compose_scan(const hypic_compose_args *a, void *stream) {
     if (!a) return HYPIC_ERR_INVALID_ARG;
     const int fam = a->family;
-    if (fam < HYPIC_FAM_LINEAR || fam > HYPIC_FAM_GDN) return HYPIC_ERR_INVALID_ARG;
+    if (fam < HYPIC_FAM_LINEAR || fam > HYPIC_FAM_KDA) return HYPIC_ERR_INVALID_ARG;
     if (a->n_seg < 0 || a->n_units < 0) return HYPIC_ERR_INVALID_ARG;
     if (a->d_k <= 0 || a->d_v <= 0) return HYPIC_ERR_INVALID_ARG;
     if (!head_size_ok(a->d_k, a->d_v)) return HYPIC_ERR_UNSUPPORTED;
     if (a->n_seg == 0 || a->n_units == 0) return HYPIC_OK;
     if (a->n_units > (int64_t)INT32_MAX / 16) return HYPIC_ERR_UNSUPPORTED;
-    const bool dense = fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GDN;
+    const bool dense = dense_family(fam);
     if (!a->S || !a->prefix) return HYPIC_ERR_INVALID_ARG;
     if (fam != HYPIC_FAM_LINEAR && !a->lam) return HYPIC_ERR_INVALID_ARG;
     if (dense && !a->P) return HYPIC_ERR_INVALID_ARG;
@@ -608,7 +629,7 @@ const char *hypic_build_kernel_name(const hypic_build_args *a) {
     if (!build_shape_ok(a)) return nullptr;
     switch (pick_build(a)) {
     case BuildPath::GdnTc: return "build_gdn_tc";
-    case BuildPath::DeltaSeq: return "build_delta_seq";
+    case BuildPath::Seq: return "build_seq";
     case BuildPath::GatedTc: return "build_gated_tc";
     case BuildPath::GatedSimt: return "build_gated_simt";
     case BuildPath::None: break;

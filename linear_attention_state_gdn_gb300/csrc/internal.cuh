@@ -57,6 +57,9 @@ struct BuildParams {
     float *S_piece;
     float *P_piece;
     float *lam_piece;
+    const void *q;        // segment outputs (exact path only): queries, outputs, start states
+    void *O;
+    const float *S_init;
     SegEntry seg[HYPIC_MAX_SEGMENTS];
 };
 
@@ -80,7 +83,7 @@ struct ComposeParams {
 
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_build_gated_simt(const BuildParams &p, cudaStream_t s);
-cudaError_t launch_build_delta_seq(const BuildParams &p, cudaStream_t s);
+cudaError_t launch_build_seq(const BuildParams &p, cudaStream_t s);
 cudaError_t launch_compose_scaled(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_lam_total(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_dense_simt(const ComposeParams &p, cudaStream_t s);

@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.hypic_abi_version() == 3
+    assert lib.hypic_abi_version() == 4
     assert lib.hypic_status_string(0) == b"ok"
     assert lib.hypic_status_string(2) == b"misaligned tensor pointer"
     assert lib.hypic_status_string(99) == b"unknown status"
@@ -252,3 +252,35 @@ def test_wait_probe_rejects_limits_out_of_range(lib):
     # checked before the library touches the device
     assert lib.hypic_probe_wait_timeout(0, None) == 1
     assert lib.hypic_probe_wait_timeout(1000001, None) == 1
+
+
+def test_build_args_layout():
+    # eight int32 and one int64; ten pointers; size_t; then (ABI 4) q, O, S_init
+    assert ctypes.sizeof(BuildArgs) == 152
+    assert BuildArgs.q.offset == 128 and BuildArgs.O.offset == 136 and BuildArgs.S_init.offset == 144
+
+
+def test_build_outputs_and_queries_come_together(lib):
+    a = good_build()
+    a.q = FAKE + 0x8000000
+    assert call_build(lib, a) == 1
+    a = good_build()
+    a.O = FAKE + 0x8000000
+    assert call_build(lib, a) == 1
+
+
+def test_kda_needs_gates_beta_and_P(lib):
+    for field in ("log_gate", "beta", "P"):
+        a = good_build(family=5)
+        setattr(a, field, None)
+        assert call_build(lib, a) == 1
+
+
+def test_kda_and_outputs_take_the_exact_path(lib):
+    a = good_build(family=5)
+    assert lib.hypic_build_kernel_name(ctypes.byref(a)) == b"build_seq"
+    a = good_build(family=4)
+    assert lib.hypic_build_kernel_name(ctypes.byref(a)) == b"build_gdn_tc"
+    a.q, a.O = FAKE + 0x8000000, FAKE + 0x9000000
+    assert lib.hypic_build_kernel_name(ctypes.byref(a)) == b"build_seq"
+    assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == 0

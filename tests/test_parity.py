@@ -18,7 +18,7 @@ from tests.helpers import (COMPOSE_TOL, TOL, assert_close, f64, gpu_T, gpu_build
 pytestmark = pytest.mark.gpu
 
 RAGGED = [200, 64, 1, 0, 129, 300, 63]
-FAMILIES = ["linear", "scalar", "diag", "delta", "gdn"]
+FAMILIES = ["linear", "scalar", "diag", "delta", "gdn", "kda"]
 
 
 def _hy():
@@ -325,6 +325,12 @@ def test_workload_gdn():
     _workload_chain("gdn")
 
 
+def test_workload_kda():
+    """The channel-gated delta rule at the GDN workload's shape (32 value / 16 key heads,
+    d = 128, 16 x 2048 tokens, bf16): every S, T and prefix state."""
+    _workload_chain("kda")
+
+
 def test_workload_gdn_compose_sampled():
     """48 layers x 32 heads x 64 ragged segments, built layer by layer into one
     [64, 1536] cache exactly as the benchmark does, then one compose launch over all 1536
@@ -374,8 +380,12 @@ def test_workload_gdn_compose_full_size_with_totals():
     T = oracle.materialize_T("gdn", f64(c.lam[:, units]), f64(c.P[:, units]))
     assert_close(f64(pref[:, units]), oracle.compose_scan(T, f64(c.S[:, units])), COMPOSE_TOL, "prefix")
     lam_o, P_o = oracle.compose_transitions("gdn", f64(c.lam[:, units]), f64(c.P[:, units]))
-    np.testing.assert_allclose(f64(lam_t[units]), lam_o, rtol=1e-5, atol=1e-5)
-    assert_close(f64(P_t[units])[None], P_o[None], COMPOSE_TOL, "P_total")
+    # the composed transition exp(lam_total) P_total at its own scale: P_total carries the
+    # power of two whose exponent lam_total reports
+    E = (lam_o - f64(lam_t[units])) / np.log(2.0)
+    assert np.allclose(E, np.round(E), atol=1e-3)
+    got = f64(P_t[units]) * np.exp(f64(lam_t[units]) - lam_o)[:, None, None]
+    assert_close(got[None], P_o[None], COMPOSE_TOL, "P_total")
 
 
 # ------------------------------------------------------------------ kernel selection
@@ -383,9 +393,10 @@ def test_workload_gdn_compose_full_size_with_totals():
 @pytest.mark.parametrize("family,dtype,d,expect", [
     ("linear", torch.bfloat16, 128, "build_gated_tc"), ("scalar", torch.bfloat16, 128, "build_gated_tc"),
     ("diag", torch.bfloat16, 128, "build_gated_tc"), ("diag", torch.float32, 128, "build_gated_simt"),
-    ("scalar", torch.bfloat16, 64, "build_gated_simt"), ("gdn", torch.float32, 32, "build_delta_seq"),
+    ("scalar", torch.bfloat16, 64, "build_gated_simt"), ("gdn", torch.float32, 32, "build_seq"),
     ("gdn", torch.bfloat16, 128, "build_gdn_tc"), ("delta", torch.bfloat16, 128, "build_gdn_tc"),
-    ("gdn", torch.float32, 128, "build_delta_seq"), ("gdn", torch.bfloat16, 64, "build_delta_seq"),
+    ("gdn", torch.float32, 128, "build_seq"), ("gdn", torch.bfloat16, 64, "build_seq"),
+    ("kda", torch.bfloat16, 128, "build_seq"), ("kda", torch.float32, 32, "build_seq"),
 ])
 def test_build_kernel_selection(family, dtype, d, expect):
     """bf16 inputs with d = 128 run on the tensor cores; fp32 inputs and smaller heads run the
