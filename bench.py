@@ -12,9 +12,10 @@ in four groups, so that each group's copies overlap the previous group's build).
 
 The other workloads (RetNet scalar build + compose, GLA diagonal build + compose, the same
 GDN prompt cached as one 32768-token segment, the RetNet prompt as one 16384-token segment,
-the 48-layer x 64-segment GDN compose with and
-without the composed entry) are measured after the main timed region and reported under
-"sections". `--impl reference` times the fp64 CPU oracle instead (a bounded sample
+the channel-gated delta rule (KDA) at the GDN shape, the GDN build that also returns the
+segment outputs O(C|0), the 48-layer x 64-segment GDN compose with and without the composed
+entry) are measured after the main timed region and reported under "sections", each with the
+oracle timed on the host cores beside it and the parity of its outputs against that oracle. `--impl reference` times the fp64 CPU oracle instead (a bounded sample
 of the same workload per step, on the host cores).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl hypic|reference]
@@ -48,6 +49,12 @@ L2_FLUSH_BYTES = 256 << 20
 # algorithmic work per token per value head of the chunked (C = 64) WY/UT GDN build:
 # gram 2Cd + W 2Cd + U 2Cd + X = W[S|P] 2d(2d) + state update 2d(2d)
 GDN_FLOP_PER_TOKEN_HEAD = 6 * CHUNK * 128 + 8 * 128 * 128   # 180,224
+# the exact sequential form (one thread per state column), per token per value head, d = 128:
+# the gate d^2 (a product per state element; KDA also on P), k^T z 2d^2 and the rank-1
+# update 2d^2 on each of the S and P halves, and o = S^T q 2d^2 when the outputs are read
+SEQ_D = 128
+SEQ_FLOP_PER_TOKEN_HEAD = {"kda": 2 * 5 * SEQ_D * SEQ_D, "gdn": (5 + 4) * SEQ_D * SEQ_D}
+SEQ_OUT_FLOP = 2 * SEQ_D * SEQ_D
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -313,8 +320,8 @@ def section_family(name, flush, peak, steps=20, warmup=3, oracle_budget_s=0.0):
     (tb, tc), _ = time_loop([st.build, st.compose], steps, warmup, flush)
     b_ms, c_ms = statistics.mean(tb), statistics.mean(tc)
     n_tok, d = inp.n_tok, inp.d_k
-    dense = inp.family in ("gdn", "delta")
-    gate_bytes = n_tok * inp.H_v * (d if inp.family == "diag" else 1) * 4 \
+    dense = inp.family in ("gdn", "delta", "kda")
+    gate_bytes = n_tok * inp.H_v * (d if inp.family in ("diag", "kda") else 1) * 4 \
         if inp.log_gate is not None else 0
     beta_bytes = n_tok * inp.H_v * 4 if inp.beta is not None else 0
     b_bytes = n_tok * (inp.H_k + inp.H_v) * d * 2 + gate_bytes + beta_bytes + \
@@ -323,9 +330,14 @@ def section_family(name, flush, peak, steps=20, warmup=3, oracle_budget_s=0.0):
     bk, ck = st.kernel_names()
     b_gbs, c_gbs = b_bytes / b_ms / 1e6, c_bytes / c_ms / 1e6
     extra = {}
-    if dense:   # tensor-bound: the chunked-form flops against the measured bf16 peak
+    if bk == "build_gdn_tc":   # tensor-bound: the chunked-form flops against the measured bf16 peak
         tf = GDN_FLOP_PER_TOKEN_HEAD * n_tok * inp.H_v / (b_ms * 1e-3) / 1e12
         extra = {"build_tflops": round(tf, 1), "build_tensor_frac": round(tf / peak["bf16_tflops"], 4)}
+    elif bk == "build_seq":    # fp32 CUDA-core bound: the sequential form against the FFMA peak
+        tf = SEQ_FLOP_PER_TOKEN_HEAD[inp.family] * n_tok * inp.H_v / (b_ms * 1e-3) / 1e12
+        alu = fp32_alu_peak_tflops(peak["sm_max_mhz"])
+        extra = {"build_tflops": round(tf, 2), "build_alu_frac": round(tf / alu, 4),
+                 "alu_peak_tflops": round(alu, 1)}
     out = {"build_kernel": bk, "build_ms": round(b_ms, 4), **extra,
            "build_tokens_per_s": round(n_tok / b_ms * 1e3, 1),
            "build_gbs": round(b_gbs, 1), "build_hbm_frac": round(b_gbs / peak["hbm_gbs"], 4),
@@ -336,6 +348,36 @@ def section_family(name, flush, peak, steps=20, warmup=3, oracle_budget_s=0.0):
         torch.cuda.synchronize()
         out["cpu_baseline"] = cpu_baseline(inp, gpu=(st.S, st.lam, st.P, st.prefix),
                                            budget_s=oracle_budget_s)
+        out["parity"] = out["cpu_baseline"].pop("parity")
+    return out
+
+
+def section_outputs(name, flush, peak, steps=10, warmup=3, oracle_budget_s=0.0):
+    """The build of a workload that also returns the segment outputs O(C|0) (queries drawn
+    with the workload): the exact sequential path, against the fp32 FFMA peak; the oracle
+    leg times oracle.outputs on a sample of heads and reports the parity of O there."""
+    import linear_attention_state_gdn_gb300 as hy
+    from linear_attention_state_gdn_gb300 import synth
+    inp = synth.make_workload(name, with_q=True)
+    dev = {n: t.cuda() for n, t in inp.tensors().items()}
+    S, lam, P = hy.build_outputs(inp.family, inp.n_seg, inp.H_v, inp.d_v, "cuda")
+    O = torch.empty_like(dev["v"])
+    kw = dict(log_gate=dev.get("log_gate"), log_gamma=dev.get("log_gamma"), beta=dev.get("beta"))
+    f = lambda: hy.hypic_build_segments(inp.family, dev["k"], dev["v"], inp.seg_offsets, S=S,
+                                        lam=lam, P=P, q=dev["q"], O=O, **kw)
+    (tb,), _ = time_loop([f], steps, warmup, flush)
+    ms = statistics.mean(tb)
+    flop = (SEQ_FLOP_PER_TOKEN_HEAD[inp.family] + SEQ_OUT_FLOP) * inp.n_tok * inp.H_v
+    tf = flop / (ms * 1e-3) / 1e12
+    alu = fp32_alu_peak_tflops(peak["sm_max_mhz"])
+    bk = hy.hypic_build_kernel_name(inp.family, dev["k"], dev["v"], inp.seg_offsets, S=S, lam=lam,
+                                    P=P, q=dev["q"], O=O, **kw)
+    out = {"build_kernel": bk, "build_ms": round(ms, 4), "build_tokens_per_s": round(inp.n_tok / ms * 1e3, 1),
+           "build_tflops": round(tf, 2), "build_alu_frac": round(tf / alu, 4),
+           "alu_peak_tflops": round(alu, 1)}
+    if oracle_budget_s:
+        torch.cuda.synchronize()
+        out["cpu_baseline"] = outputs_cpu_baseline(inp, O, oracle_budget_s)
         out["parity"] = out["cpu_baseline"].pop("parity")
     return out
 
@@ -471,6 +513,42 @@ def cpu_baseline(inp, gpu=None, budget_s=12.0, min_passes=1):
     if gpu is not None:
         out["parity"] = build_parity(inp, heads, ref, gpu)
     return out
+
+
+def outputs_cpu_baseline(inp, O, budget_s):
+    """oracle.outputs on the first value heads of the workload (a whole number of key-head
+    groups, about budget_s seconds), timed on the host cores, and the parity of the GPU's O
+    on those heads: the largest relative Frobenius error over the (segment, head) blocks."""
+    import oracle
+    threads = oracle.default_threads()
+    g = inp.H_v // inp.H_k
+    f = lambda t, hs: None if t is None else np.ascontiguousarray(t.double().numpy()[:, hs])
+
+    def run(heads):
+        hk = heads // g
+        t0 = time.perf_counter()
+        ref = oracle.outputs(inp.family, inp.seg_offsets, f(inp.k, slice(0, hk)), f(inp.v, slice(0, heads)),
+                             f(inp.q, slice(0, hk)), f(inp.log_gate, slice(0, heads)),
+                             None if inp.log_gamma is None else inp.log_gamma[:heads].double().numpy(),
+                             f(inp.beta, slice(0, heads)), nthreads=threads)
+        return time.perf_counter() - t0, ref
+    t1, _ = run(g)
+    heads = sample_heads(inp, int(budget_s / max(t1, 1e-3) * g))
+    dt, ref = run(heads)
+    got = O[:, :heads].double().cpu().numpy()
+    worst = 0.0
+    for j in range(inp.n_seg):
+        a, b = int(inp.seg_offsets[j]), int(inp.seg_offsets[j + 1])
+        for h in range(heads):
+            r = ref[a:b, h]
+            worst = max(worst, float(np.linalg.norm(got[a:b, h] - r) / max(np.linalg.norm(r), 1e-300)))
+    tol = 1e-4 if inp.dtype == torch.float32 else 2e-2
+    return {"value": round(inp.n_tok * heads / inp.H_v / dt, 2), "unit": UNIT, "cores": threads,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": f"fp64 oracle outputs of all {inp.n_seg} segments x {heads} of {inp.H_v} "
+                      f"value heads; tokens/s scaled by {heads}/{inp.H_v}",
+            "parity": {"O": float(f"{worst:.3e}"), "tol": tol, "ok": worst <= tol,
+                       "units": f"{inp.n_seg} segments x {heads} of {inp.H_v} value heads"}}
 
 
 def compose_cpu_baseline(S, lam, P, prefix, units, lam_t=None, P_t=None):
@@ -750,8 +828,9 @@ def run_main(args):
         torch.cuda.empty_cache()
         oracle_leg = rank == 0 and world == 1
         sections = {}
-        for name in ("retnet", "gla", "gdn_one_segment", "retnet_one_segment"):
+        for name in ("retnet", "gla", "gdn_one_segment", "retnet_one_segment", "kda"):
             sections[name] = section_family(name, flush, pk, oracle_budget_s=4.0 if oracle_leg else 0.0)
+        sections["gdn_outputs"] = section_outputs("gdn", flush, pk, oracle_budget_s=4.0 if oracle_leg else 0.0)
         sections["gdn_compose"] = section_gdn_compose(flush, pk, layers=args.compose_layers,
                                                       oracle_units=96 if oracle_leg else 0)
         line["sections"] = sections
@@ -777,6 +856,8 @@ def run_only(args):
     if args.only == "gdn_compose":
         out = section_gdn_compose(flush, pk, steps=args.steps, warmup=args.warmup,
                                   layers=args.compose_layers)
+    elif args.only == "gdn_outputs":
+        out = section_outputs("gdn", flush, pk, steps=args.steps, warmup=args.warmup)
     else:
         out = section_family(args.only, flush, pk, steps=args.steps, warmup=args.warmup)
     assert hy.hypic_get_device_status() == 0
@@ -794,7 +875,7 @@ def main(argv=None):
                     help="main timed region only (no e2e, sections or CPU baseline)")
     ap.add_argument("--compose-layers", type=int, default=48)
     ap.add_argument("--only", choices=["gdn", "retnet", "gla", "gdn_tiny", "gdn_compose", "gdn_one_segment",
-                                       "retnet_one_segment"],
+                                       "retnet_one_segment", "kda", "gdn_outputs"],
                     help="time one workload's launches alone (profiling helper; no contract line)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps

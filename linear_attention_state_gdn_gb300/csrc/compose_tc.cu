@@ -323,7 +323,8 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                         if (t == 0) red_max[(rc + 2) % 3] = 0u;
                         ++rc;
                         s_pow = 1.f;
-                        if (m > 0.f && m < 0x1p-24f) {
+                        // (the last step writes no next operand: no scale, no exponent)
+                        if (j + 1 < NS && m > 0.f && m < 0x1p-24f) {
                             const int e = -exponent_of(m);   // m 2^e in [1, 2)
                             s_pow = __uint_as_float((uint32_t)(127 + e) << 23);
                             e_sum += e;
