@@ -96,6 +96,27 @@ build_gated_simt_kernel(const __grid_constant__ BuildParams p) {
 
 constexpr int kSeqChunk = 16;
 
+// x . z over D elements (x in shared memory, z in registers) as eight independent partial
+// sums, so that the dependent chain is D / 8 fused multiply-adds long rather than D.
+template <int D>
+__device__ __forceinline__ float dot(const float *x, const float (&z)[D]) {
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < D; i += 8) {
+        const float4 x0 = *reinterpret_cast<const float4 *>(x + i);
+        const float4 x1 = *reinterpret_cast<const float4 *>(x + i + 4);
+        a[0] = fmaf(x0.x, z[i], a[0]);
+        a[1] = fmaf(x0.y, z[i + 1], a[1]);
+        a[2] = fmaf(x0.z, z[i + 2], a[2]);
+        a[3] = fmaf(x0.w, z[i + 3], a[3]);
+        a[4] = fmaf(x1.x, z[i + 4], a[4]);
+        a[5] = fmaf(x1.y, z[i + 5], a[5]);
+        a[6] = fmaf(x1.z, z[i + 6], a[6]);
+        a[7] = fmaf(x1.w, z[i + 7], a[7]);
+    }
+    return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+}
+
 // Every family, stepped token by token in fp32: thread n owns column n of the augmented state
 // Z = [S | P] (d_k rows in registers; P only for the dense families DELTA / GDN / KDA, whose
 // transition is not a scalar or a diagonal). Per token t, with the family's gate A_t:
@@ -203,15 +224,7 @@ build_seq_kernel(const __grid_constant__ BuildParams p) {
                 }
             }
             if (delta) {
-                float w = 0.f;
-#pragma unroll
-                for (int i = 0; i < D; i += 4) {
-                    const float4 kk = *reinterpret_cast<const float4 *>(&ks[tt][i]);
-                    w = fmaf(kk.x, z[i], w);
-                    w = fmaf(kk.y, z[i + 1], w);
-                    w = fmaf(kk.z, z[i + 2], w);
-                    w = fmaf(kk.w, z[i + 3], w);
-                }
+                const float w = dot<D>(ks[tt], z);
                 const float coef = bs[tt] * ((is_S ? vs[tt][n] : 0.f) - w);
 #pragma unroll
                 for (int i = 0; i < D; i += 4) {
@@ -233,15 +246,7 @@ build_seq_kernel(const __grid_constant__ BuildParams p) {
                 }
             }
             if (outs && is_S) {
-                float o = 0.f;
-#pragma unroll
-                for (int i = 0; i < D; i += 4) {
-                    const float4 qq = *reinterpret_cast<const float4 *>(&qs[tt][i]);
-                    o = fmaf(qq.x, z[i], o);
-                    o = fmaf(qq.y, z[i + 1], o);
-                    o = fmaf(qq.z, z[i + 2], o);
-                    o = fmaf(qq.w, z[i + 3], o);
-                }
+                const float o = dot<D>(qs[tt], z);
                 const int64_t oi = (tok * p.H_v + h) * D + n;
                 if (p.dtype == HYPIC_BF16) reinterpret_cast<__nv_bfloat16 *>(p.O)[oi] = __float2bfloat16_rn(o);
                 else reinterpret_cast<float *>(p.O)[oi] = o;
