@@ -96,30 +96,12 @@ build_gated_simt_kernel(const __grid_constant__ BuildParams p) {
 
 constexpr int kSeqChunk = 16;
 
-// x . z over D elements (x in shared memory, z in registers) as eight independent partial
-// sums, so that the dependent chain is D / 8 fused multiply-adds long rather than D.
-template <int D>
-__device__ __forceinline__ float dot(const float *x, const float (&z)[D]) {
-    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < D; i += 8) {
-        const float4 x0 = *reinterpret_cast<const float4 *>(x + i);
-        const float4 x1 = *reinterpret_cast<const float4 *>(x + i + 4);
-        a[0] = fmaf(x0.x, z[i], a[0]);
-        a[1] = fmaf(x0.y, z[i + 1], a[1]);
-        a[2] = fmaf(x0.z, z[i + 2], a[2]);
-        a[3] = fmaf(x0.w, z[i + 3], a[3]);
-        a[4] = fmaf(x1.x, z[i + 4], a[4]);
-        a[5] = fmaf(x1.y, z[i + 5], a[5]);
-        a[6] = fmaf(x1.z, z[i + 6], a[6]);
-        a[7] = fmaf(x1.w, z[i + 7], a[7]);
-    }
-    return ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
-}
-
-// Every family, stepped token by token in fp32: thread n owns column n of the augmented state
-// Z = [S | P] (d_k rows in registers; P only for the dense families DELTA / GDN / KDA, whose
-// transition is not a scalar or a diagonal). Per token t, with the family's gate A_t:
+// Every family, stepped token by token in fp32. One CTA carries one half of a unit's
+// augmented state Z = [S | P]: the S half, or the P half (only for the dense families DELTA /
+// GDN / KDA, whose transition is not a scalar or a diagonal). Column n of the half is held in
+// registers by TPC adjacent threads, RPT = D / TPC rows each; dot products over a column are
+// partial sums over a thread's rows combined by shuffles inside the group. Per token t, with
+// the family's gate A_t:
 //   S <- A_t S                 A_t = g I (SCALAR), Diag(g) (DIAG), a I (GDN), Diag(a) (KDA)
 //   S <- S + b k (v - k^T S)^T  (DELTA / GDN / KDA: the delta update)
 //   S <- S + k v^T              (LINEAR / SCALAR / DIAG: the write)
@@ -130,76 +112,109 @@ __device__ __forceinline__ float dot(const float *x, const float (&z)[D]) {
 // where a 1e-4 relative error budget rules out bf16 or tf32 tensor-core operands), the path
 // of the head sizes and families the tensor-core builds do not take (d = 32, 64; KDA), and
 // the path of every build that asks for the segment outputs.
-template <int D>
-__global__ void __launch_bounds__(2 * D)
+//
+// Shared-memory vectors (k, q, per-channel gates) keep the rows of thread part r in 4-element
+// chunks permuted by chunk ^ r, so that the TPC parts of a column group, which read the same
+// chunk index of different row ranges at once, hit different banks.
+template <int D, int TPC>
+__device__ __forceinline__ int sidx(int i) {
+    constexpr int RPT = D / TPC;
+    return (i / RPT) * RPT + ((((i % RPT) >> 2) ^ (i / RPT)) << 2) + (i & 3);
+}
+
+// Partial x . z over this thread's RPT rows (x a swizzled shared vector, part r), as four
+// independent sums, combined over the TPC threads of the column.
+template <int D, int TPC>
+__device__ __forceinline__ float col_dot(const float *x, const float (&z)[D / TPC], int r) {
+    constexpr int RPT = D / TPC;
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    const float *xr = x + r * RPT;
+#pragma unroll
+    for (int j = 0; j < RPT / 4; ++j) {
+        const float4 v = *reinterpret_cast<const float4 *>(xr + ((j ^ r) << 2));
+        a[0] = fmaf(v.x, z[4 * j], a[0]);
+        a[1] = fmaf(v.y, z[4 * j + 1], a[1]);
+        a[2] = fmaf(v.z, z[4 * j + 2], a[2]);
+        a[3] = fmaf(v.w, z[4 * j + 3], a[3]);
+    }
+    float w = (a[0] + a[1]) + (a[2] + a[3]);
+#pragma unroll
+    for (int o = 1; o < TPC; o <<= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+    return w;
+}
+
+template <int D, int TPC>
+__global__ void __launch_bounds__(D * TPC)
 build_seq_kernel(const __grid_constant__ BuildParams p) {
+    constexpr int RPT = D / TPC;
     __shared__ __align__(16) float ks[kSeqChunk][D];
     __shared__ __align__(16) float vs[kSeqChunk][D];
     __shared__ __align__(16) float qs[kSeqChunk][D];
-    __shared__ __align__(16) float gs[kSeqChunk][D];   // exp of the gate: per channel, or [tt][0]
+    __shared__ __align__(16) float gs[kSeqChunk][D];   // per-channel gates (log, then exp)
     __shared__ float lgs[kSeqChunk];                     // per-token log gate (SCALAR / GDN), KDA: m_t
     __shared__ float bs[kSeqChunk];
 
     const int fam = p.family;
-    const SegEntry seg = p.seg[blockIdx.x / p.H_v];
-    const int h = blockIdx.x % p.H_v;
-    const int hk = h / p.gqa;
-    const int n = threadIdx.x;
-    const bool is_S = n < D;
     const bool delta = fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GDN || fam == HYPIC_FAM_KDA;
+    const int halves = delta ? 2 : 1;
+    const int ux = blockIdx.x / halves;                       // (segment rank, value head)
+    const bool is_S = blockIdx.x % halves == 0;               // the S half, else the P half
+    const SegEntry seg = p.seg[ux / p.H_v];
+    const int h = ux % p.H_v;
+    const int hk = h / p.gqa;
+    const int n = threadIdx.x / TPC, r = threadIdx.x % TPC;   // column of the half, part of its rows
     const bool chan = fam == HYPIC_FAM_DIAG || fam == HYPIC_FAM_KDA;   // per-channel gates
     const bool tok_gate = fam == HYPIC_FAM_GDN || (fam == HYPIC_FAM_SCALAR && !p.log_gamma);
     const bool outs = p.O != nullptr;
     const int nthr = blockDim.x;
-    const int nwarp = nthr >> 5;
+    const int tid = threadIdx.x;
     const float const_lg = (fam == HYPIC_FAM_SCALAR && p.log_gamma) ? p.log_gamma[h] : 0.f;
     const float const_g = expf(const_lg);
     const int64_t unit = (int64_t)seg.idx * p.seg_stride + h;
 
-    float z[D];
+    float z[RPT];   // rows r RPT .. r RPT + RPT - 1 of column n
     if (is_S && p.S_init) {
-        const float *s0 = p.S_init + ((int64_t)seg.idx * p.H_v + h) * D * D + n;
+        const float *s0 = p.S_init + ((int64_t)seg.idx * p.H_v + h) * D * D + (int64_t)r * RPT * D + n;
 #pragma unroll
-        for (int i = 0; i < D; ++i) z[i] = s0[(int64_t)i * D];
+        for (int m = 0; m < RPT; ++m) z[m] = s0[(int64_t)m * D];
     } else {
 #pragma unroll
-        for (int i = 0; i < D; ++i) z[i] = (!is_S && i == n - D) ? 1.f : 0.f;
+        for (int m = 0; m < RPT; ++m) z[m] = (!is_S && r * RPT + m == n) ? 1.f : 0.f;
     }
-    float lam_acc = 0.f;   // thread 0: sum of the scalar log-gates; DIAG: thread n, channel n
+    float lam_acc = 0.f;   // thread 0: sum of the scalar log-gates; DIAG: part 0 of column n
 
     for (int t0 = 0; t0 < seg.len; t0 += kSeqChunk) {
         const int nt = min(kSeqChunk, seg.len - t0);
         __syncthreads();
-        for (int e = n; e < nt * D; e += nthr) {
+        for (int e = tid; e < nt * D; e += nthr) {
             const int tt = e / D, d = e % D;
             const int64_t tok = (int64_t)seg.start + t0 + tt;
-            ks[tt][d] = load_in(p.k, (tok * p.H_k + hk) * D + d, p.dtype);
+            const int sd = sidx<D, TPC>(d);
+            ks[tt][sd] = load_in(p.k, (tok * p.H_k + hk) * D + d, p.dtype);
             vs[tt][d] = load_in(p.v, (tok * p.H_v + h) * D + d, p.dtype);
-            if (outs) qs[tt][d] = load_in(p.q, (tok * p.H_k + hk) * D + d, p.dtype);
-            if (chan) gs[tt][d] = p.log_gate[(tok * p.H_v + h) * D + d];   // log, exponentiated below
+            if (outs) qs[tt][sd] = load_in(p.q, (tok * p.H_k + hk) * D + d, p.dtype);
+            if (chan) gs[tt][sd] = p.log_gate[(tok * p.H_v + h) * D + d];
         }
-        if (n < nt) {
-            const int64_t tok = (int64_t)seg.start + t0 + n;
-            bs[n] = delta ? p.beta[tok * p.H_v + h] : 0.f;
-            lgs[n] = tok_gate ? p.log_gate[tok * p.H_v + h] : const_lg;
+        if (tid < nt) {
+            const int64_t tok = (int64_t)seg.start + t0 + tid;
+            bs[tid] = delta ? p.beta[tok * p.H_v + h] : 0.f;
+            lgs[tid] = tok_gate ? p.log_gate[tok * p.H_v + h] : const_lg;
         }
         __syncthreads();
+        if (fam == HYPIC_FAM_DIAG && is_S && r == 0)   // lam of channel n: the chunk's log gates
+            for (int tt = 0; tt < nt; ++tt) lam_acc += gs[tt][sidx<D, TPC>(n)];
         if (fam == HYPIC_FAM_KDA) {   // m_t = max_i log a_t[i], one warp per token
-            for (int tt = n >> 5; tt < nt; tt += nwarp) {
+            for (int tt = tid >> 5; tt < nt; tt += nthr >> 5) {
                 float m = -INFINITY;
-                for (int d = n & 31; d < D; d += 32) m = fmaxf(m, gs[tt][d]);
+                for (int d = tid & 31; d < D; d += 32) m = fmaxf(m, gs[tt][d]);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                if ((n & 31) == 0) lgs[tt] = m;
+                if ((tid & 31) == 0) lgs[tt] = m;
             }
-            __syncthreads();
         }
+        __syncthreads();
         if (chan) {
-            for (int e = n; e < nt * D; e += nthr) {
-                const int tt = e / D, d = e % D;
-                const float lg = gs[tt][d];
-                gs[tt][d] = expf(lg);
-            }
+            for (int e = tid; e < nt * D; e += nthr) gs[e / D][e % D] = expf(gs[e / D][e % D]);
             __syncthreads();
         }
         for (int tt = 0; tt < nt; ++tt) {
@@ -208,62 +223,52 @@ build_seq_kernel(const __grid_constant__ BuildParams p) {
             if (fam == HYPIC_FAM_SCALAR || (fam == HYPIC_FAM_GDN && is_S)) {
                 const float g = (fam == HYPIC_FAM_SCALAR && p.log_gamma) ? const_g : expf(lgs[tt]);
 #pragma unroll
-                for (int i = 0; i < D; ++i) z[i] *= g;
-            } else if (fam == HYPIC_FAM_DIAG || (fam == HYPIC_FAM_KDA && is_S)) {
+                for (int m = 0; m < RPT; ++m) z[m] *= g;
+            } else if (fam == HYPIC_FAM_DIAG || fam == HYPIC_FAM_KDA) {
+                // S half: Diag(g); KDA's P half: Diag(a e^-m)
+                const float em = (fam == HYPIC_FAM_KDA && !is_S) ? expf(-lgs[tt]) : 1.f;
+                const float *gr = gs[tt] + r * RPT;
 #pragma unroll
-                for (int i = 0; i < D; i += 4) {
-                    const float4 g = *reinterpret_cast<const float4 *>(&gs[tt][i]);
-                    z[i] *= g.x, z[i + 1] *= g.y, z[i + 2] *= g.z, z[i + 3] *= g.w;
-                }
-            } else if (fam == HYPIC_FAM_KDA) {   // P half: Diag(a e^-m)
-                const float em = expf(-lgs[tt]);
-#pragma unroll
-                for (int i = 0; i < D; i += 4) {
-                    const float4 g = *reinterpret_cast<const float4 *>(&gs[tt][i]);
-                    z[i] *= g.x * em, z[i + 1] *= g.y * em, z[i + 2] *= g.z * em, z[i + 3] *= g.w * em;
+                for (int j = 0; j < RPT / 4; ++j) {
+                    const float4 g = *reinterpret_cast<const float4 *>(gr + ((j ^ r) << 2));
+                    z[4 * j] *= g.x * em, z[4 * j + 1] *= g.y * em, z[4 * j + 2] *= g.z * em,
+                        z[4 * j + 3] *= g.w * em;
                 }
             }
+            const float *kr = ks[tt] + r * RPT;
+            float coef;
             if (delta) {
-                const float w = dot<D>(ks[tt], z);
-                const float coef = bs[tt] * ((is_S ? vs[tt][n] : 0.f) - w);
-#pragma unroll
-                for (int i = 0; i < D; i += 4) {
-                    const float4 kk = *reinterpret_cast<const float4 *>(&ks[tt][i]);
-                    z[i] = fmaf(coef, kk.x, z[i]);
-                    z[i + 1] = fmaf(coef, kk.y, z[i + 1]);
-                    z[i + 2] = fmaf(coef, kk.z, z[i + 2]);
-                    z[i + 3] = fmaf(coef, kk.w, z[i + 3]);
-                }
+                const float w = col_dot<D, TPC>(ks[tt], z, r);
+                coef = bs[tt] * ((is_S ? vs[tt][n] : 0.f) - w);
             } else {
-                const float vn = vs[tt][n];
+                coef = vs[tt][n];
+            }
 #pragma unroll
-                for (int i = 0; i < D; i += 4) {
-                    const float4 kk = *reinterpret_cast<const float4 *>(&ks[tt][i]);
-                    z[i] = fmaf(kk.x, vn, z[i]);
-                    z[i + 1] = fmaf(kk.y, vn, z[i + 1]);
-                    z[i + 2] = fmaf(kk.z, vn, z[i + 2]);
-                    z[i + 3] = fmaf(kk.w, vn, z[i + 3]);
+            for (int j = 0; j < RPT / 4; ++j) {   // z += coef k (the delta update or the write)
+                const float4 kk = *reinterpret_cast<const float4 *>(kr + ((j ^ r) << 2));
+                z[4 * j] = fmaf(coef, kk.x, z[4 * j]);
+                z[4 * j + 1] = fmaf(coef, kk.y, z[4 * j + 1]);
+                z[4 * j + 2] = fmaf(coef, kk.z, z[4 * j + 2]);
+                z[4 * j + 3] = fmaf(coef, kk.w, z[4 * j + 3]);
+            }
+            if (outs && is_S) {   // uniform over the CTA: the shuffles stay inside it
+                const float o = col_dot<D, TPC>(qs[tt], z, r);
+                if (r == 0) {
+                    const int64_t oi = (tok * p.H_v + h) * D + n;
+                    if (p.dtype == HYPIC_BF16) reinterpret_cast<__nv_bfloat16 *>(p.O)[oi] = __float2bfloat16_rn(o);
+                    else reinterpret_cast<float *>(p.O)[oi] = o;
                 }
             }
-            if (outs && is_S) {
-                const float o = dot<D>(qs[tt], z);
-                const int64_t oi = (tok * p.H_v + h) * D + n;
-                if (p.dtype == HYPIC_BF16) reinterpret_cast<__nv_bfloat16 *>(p.O)[oi] = __float2bfloat16_rn(o);
-                else reinterpret_cast<float *>(p.O)[oi] = o;
-            }
-            if (n == 0 && fam != HYPIC_FAM_DIAG) lam_acc += lgs[tt];
+            if (tid == 0 && fam != HYPIC_FAM_DIAG) lam_acc += lgs[tt];
         }
-        if (fam == HYPIC_FAM_DIAG && is_S)   // lam of channel n: the chunk's log gates
-            for (int tt = 0; tt < nt; ++tt)
-                lam_acc += p.log_gate[(((int64_t)seg.start + t0 + tt) * p.H_v + h) * D + n];
     }
 
-    float *out = is_S ? p.S + unit * D * D + n : p.P + unit * D * D + (n - D);
+    float *out = (is_S ? p.S : p.P) + unit * D * D + n + (int64_t)r * RPT * D;
 #pragma unroll
-    for (int i = 0; i < D; ++i) out[(int64_t)i * D] = z[i];
+    for (int m = 0; m < RPT; ++m) out[(int64_t)m * D] = z[m];
     if (fam == HYPIC_FAM_DIAG) {
-        if (is_S) p.lam[unit * D + n] = lam_acc;
-    } else if (n == 0) {
+        if (is_S && r == 0) p.lam[unit * D + n] = lam_acc;
+    } else if (tid == 0 && is_S) {
         float lam = lam_acc;
         if (fam == HYPIC_FAM_LINEAR || fam == HYPIC_FAM_DELTA) lam = 0.f;
         else if (fam == HYPIC_FAM_SCALAR && p.log_gamma) lam = (float)seg.len * const_lg;
@@ -291,12 +296,12 @@ cudaError_t launch_build_gated_simt(const BuildParams &p, cudaStream_t s) {
 }
 
 cudaError_t launch_build_seq(const BuildParams &p, cudaStream_t s) {
-    const int blocks = p.n_seg * p.H_v;
     const bool dense = p.family == HYPIC_FAM_DELTA || p.family == HYPIC_FAM_GDN || p.family == HYPIC_FAM_KDA;
-    switch (p.D) {
-    case 32: return launch_1d(build_seq_kernel<32>, blocks, dense ? 64 : 32, p, s);
-    case 64: return launch_1d(build_seq_kernel<64>, blocks, dense ? 128 : 64, p, s);
-    case 128: return launch_1d(build_seq_kernel<128>, blocks, dense ? 256 : 128, p, s);
+    const int blocks = p.n_seg * p.H_v * (dense ? 2 : 1);   // the S and P halves of a unit apart
+    switch (p.D) {   // 32 state rows per thread
+    case 32: return launch_1d(build_seq_kernel<32, 1>, blocks, 32, p, s);
+    case 64: return launch_1d(build_seq_kernel<64, 2>, blocks, 128, p, s);
+    case 128: return launch_1d(build_seq_kernel<128, 4>, blocks, 512, p, s);
     }
     return cudaErrorInvalidValue;
 }
