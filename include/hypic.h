@@ -151,8 +151,10 @@ typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  *                     outputs of the segment reused after that prefix state; T_C does not
  *                     change. (S_init is indexed by segment and head, stride H_v, whatever
  *                     out_seg_stride is.)
- *   A call with O or S_init, and every KDA call, runs the exact CUDA-core path (fp32
- *   arithmetic, one thread per state column); the tensor-core builds compute neither.
+ *   The DeltaNet / GDN tensor-core build (bf16, d = 128) computes O itself: a second CTA per
+ *   (segment, value head) runs the S half again with the outputs, and no segment is split
+ *   into pieces. Every other call with O, every call with S_init and every KDA call runs the
+ *   exact CUDA-core path (fp32 arithmetic).
  */
 typedef struct {
     int32_t family;

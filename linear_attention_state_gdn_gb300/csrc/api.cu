@@ -122,9 +122,11 @@ enum class ComposePath { None, Scaled, DenseSimt, DenseTc };
 // Kernel selection for a build (shape/family/dtype only; no pointer checks).
 BuildPath pick_build(const hypic_build_args *a) {
     if (a->n_seg == 0) return BuildPath::None;
-    // the segment outputs, a start state and the channel-gated delta rule: the exact path
-    if (a->O || a->S_init || a->family == HYPIC_FAM_KDA) return BuildPath::Seq;
+    // start states and the channel-gated delta rule: the exact path; the segment outputs too,
+    // except on the tensor-core DeltaNet / GDN build, whose outputs instance computes them
+    if (a->S_init || a->family == HYPIC_FAM_KDA) return BuildPath::Seq;
     const bool delta = a->family == HYPIC_FAM_DELTA || a->family == HYPIC_FAM_GDN;
+    if (a->O && !delta) return BuildPath::Seq;
     BuildParams q{};
     q.family = a->family;
     q.dtype = a->dtype;
@@ -168,7 +170,7 @@ constexpr int kMaxPieces = 8;
 
 int gdn_split_m(const hypic_build_args *a) {
     const int64_t units = (int64_t)a->n_seg * a->H_v;
-    if (units == 0) return 1;
+    if (units == 0 || a->O) return 1;   // a piece's outputs would need the state before it
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -207,6 +209,7 @@ struct SplitLayout {
 // the trailing segments to halve, or 0 (see above)
 int gdn_tail_split(const hypic_build_args *a, int *first) {
     if (a->family != HYPIC_FAM_DELTA && a->family != HYPIC_FAM_GDN) return 0;
+    if (a->O) return 0;
     if (a->out_seg_stride != 0 && a->out_seg_stride != a->H_v) return 0;
     const int64_t units = (int64_t)a->n_seg * a->H_v;
     int dev = 0, sms = 0;

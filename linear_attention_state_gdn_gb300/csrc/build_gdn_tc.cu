@@ -43,6 +43,17 @@
 //     warp 14, per chunk c:  d_P(c): D_P = Z_P^T (-W^T);   f_P(c): Z_P^T += D_P^T K
 // Two issuers keep the tensor pipe fed: it queues only a few instructions, so while one half
 // waits for its operands the other half's products run.
+//
+// Outputs instance. When the call asks for the segment outputs o_t = S_t^T q_t, a second set of
+// CTAs (blockIdx >= units) runs the S~ half again without the P half and computes, per chunk,
+//     O^T = S~^T Q^T + D_S^T A^T,   A = the masked Q K^T (A_ts = q_t . k_s for s <= t),
+//     o_t = exp(Lam + c_t) O^T[:, t]
+// (with Delta = exp(Lam) D_S the chunk's delta values, o_t = e^{c_t} (S_before^T q_t +
+// sum_{s<=t} (q_t . k_s) Delta_s)): the S~ issuer adds Q S~ (A = the bf16 Z_S^T already in TMEM,
+// B = the q chunk) before d_S and the intra-chunk product (A = the bf16 D_S^T, B = A) after f_S,
+// into the Z_P columns [128,192); the P issuer computes Q K^T (M = 64) into the D_P columns;
+// the P-half warps turn it into the bf16 operand A (masked) and read the outputs out, scaled
+// with the chunk's gate slot (three slots, so that the slot outlives the read-out).
 // Every wait is bounded; a wait that runs out sets the status word and the CTA drains.
 #include <algorithm>
 
@@ -77,8 +88,14 @@ constexpr uint32_t kOffVR = kKSlots * kKV;    // {v, M2} ring: 3 x 24 KB
 constexpr uint32_t kOffWop = kOffVR + kVSlots * kVR;  // -W^T bf16: 2 slots x [128 rows i][128 B]
 constexpr uint32_t kOffM1 = kOffWop + 2 * kKV;  // M1: 2 slots x 8 KB
 constexpr uint32_t kSmemBytes = kOffM1 + 2 * kRec + 1024;
+// outputs instance only: a ring of two q chunks and two slots of the masked Q K^T (bf16)
+constexpr uint32_t kOffQ = kOffM1 + 2 * kRec;
+constexpr uint32_t kOffAq = kOffQ + 2 * kKV;
+constexpr uint32_t kSmemBytesOut = kOffAq + 2 * kRec + 1024;
+constexpr int kSlots = 3;   // per-chunk gate slots
 
 constexpr uint32_t kTZ = 0, kTD = 256, kTZK = 384;
+constexpr uint32_t kTO = 128, kTAq = 320;   // outputs instance: O^T and Q K^T (the P half's columns)
 
 struct Slot {   // per-chunk values from the operand warps (two slots)
     float ex[C];      // exp(-Lam_start - c_t)
@@ -99,6 +116,9 @@ struct Bars {
     uint64_t m1ready[2];          // M1 (and the slot) of a chunk, one barrier per slot
     uint64_t zready[2], dfull[2], dready[2], zfull[2];   // per half
     uint64_t fin[2];
+    // outputs instance: the q ring (emptied by Q S~ and Q K^T), Q K^T in TMEM (written by the
+    // P issuer, read by the output warps), its bf16 slots, and the output accumulator
+    uint64_t qfull[2], qempty[2], aqfull, aqfree, aqready[2], ofull, ofree;
 };
 
 // Named barrier of the 128 operand-warp threads, and the same with an AND of a predicate
@@ -144,20 +164,24 @@ __device__ __forceinline__ void st_bf16x64(uint32_t taddr, const uint32_t (&z)[6
 
 __global__ void __launch_bounds__(kThreads, 1)
 build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmR) {
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmR,
+                    const __grid_constant__ CUtensorMap tmQ) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-aligned base, derived by offsetting the shared array itself so that the
     // compiler keeps the shared address space (plain ld/st.shared, not generic accesses)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ Bars bars;
-    __shared__ __align__(16) Slot slots[2];
+    __shared__ __align__(16) Slot slots[kSlots];
     __shared__ uint32_t tslot;
     __shared__ volatile int abort_flag;
     __shared__ float scan_tmp[2];
 
     const int warp = warp_id(), lane = lane_id();
-    const SegEntry seg = p.seg[blockIdx.x / p.H_v];
-    const int h = blockIdx.x % p.H_v;
+    const int units = p.n_seg * p.H_v;
+    const bool outm = (int)blockIdx.x >= units;   // the outputs instance of unit blockIdx - units
+    const int ux = outm ? (int)blockIdx.x - units : (int)blockIdx.x;
+    const SegEntry seg = p.seg[ux / p.H_v];
+    const int h = ux % p.H_v;
     const int hk = h / p.gqa;
     const int nch = (seg.len + C - 1) / C;
     const bool gdn = p.family == HYPIC_FAM_GDN;
@@ -183,6 +207,15 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
         mbar_init(&bars.wfull, 1);
         mbar_init(&bars.fin[0], 1);
         mbar_init(&bars.fin[1], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars.qfull[s], 1);
+            mbar_init(&bars.qempty[s], 2);   // Q S~ (S~ issuer) and Q K^T (P issuer)
+            mbar_init(&bars.aqready[s], 128);
+        }
+        mbar_init(&bars.aqfull, 1);
+        mbar_init(&bars.aqfree, 128);
+        mbar_init(&bars.ofull, 1);
+        mbar_init(&bars.ofree, 128);
         abort_flag = 0;
         fence_mbar_init();
         // the kernel after this one (the merge of split segments) may launch and set up on SMs
@@ -206,7 +239,8 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
             prefetch_tmap(&tmR);
-            int c = 0, kc = 0;   // chunks whose {v, M2} / k loads were issued
+            if (outm) prefetch_tmap(&tmQ);
+            int c = 0, kc = 0, qc = 0;   // chunks whose {v, M2} / k / q loads were issued
             for (; c < nch; ++c) {
                 const int32_t t0 = seg.start + c * C;
                 const int ks = c % kKSlots, kuse = c / kKSlots;
@@ -228,12 +262,23 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 tma_load_3d(vt, &tmV, &bars.vfull[vs], 0, h, t0);
                 tma_load_3d(vt + kHalf, &tmV, &bars.vfull[vs], 64, h, t0);
                 tma_load_2d(vt + kKV, &tmR, &bars.vfull[vs], 0, rrow);
+                if (outm) {
+                    const int qs = c & 1, quse = c >> 1;
+                    if (quse >= 1 && !wait(&bars.qempty[qs], (quse - 1) & 1)) break;
+                    uint8_t *qt = smem + kOffQ + qs * kKV;
+                    mbar_arrive_expect_tx(&bars.qfull[qs], kKV);
+                    tma_load_3d(qt, &tmQ, &bars.qfull[qs], 0, hk, t0);
+                    tma_load_3d(qt + kHalf, &tmQ, &bars.qfull[qs], 64, hk, t0);
+                    qc = c + 1;
+                }
             }
             if (abort_flag) {   // let the loads in flight land before the CTA exits
                 for (int q = (kc > kKSlots ? kc - kKSlots : 0); q < kc; ++q)
                     mbar_wait(&bars.kfull[q % kKSlots], (q / kKSlots) & 1, p.err, kErrTimeout);
                 for (int q = (c > kVSlots ? c - kVSlots : 0); q < c; ++q)
                     mbar_wait(&bars.vfull[q % kVSlots], (q / kVSlots) & 1, p.err, kErrTimeout);
+                for (int q = (qc > 2 ? qc - 2 : 0); q < qc; ++q)
+                    mbar_wait(&bars.qfull[q & 1], (q >> 1) & 1, p.err, kErrTimeout);
             }
         }
     } else if (warp == kMmaWarpS || warp == kMmaWarpP) {
@@ -255,6 +300,11 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             const uint64_t dR = sdesc(sb + kOffVR + kKV, 16, 1024, kSwizzle128B);     // K-major
             const uint64_t dW = sdesc(sb + kOffWop, kHalf, 1024, kSwizzle128B);       // MN-major
             const uint64_t dM = sdesc(sb + kOffM1, 16, 1024, kSwizzle128B);           // K-major
+            const uint64_t dQ = sdesc(sb + kOffQ, 16, 1024, kSwizzle128B);            // K-major
+            const uint64_t dKk = sdesc(sb + kOffK, 16, 1024, kSwizzle128B);           // K-major
+            const uint64_t dAq = sdesc(sb + kOffAq, 16, 1024, kSwizzle128B);          // K-major
+            constexpr uint32_t idO = idesc(kFmtBF16, kFmtBF16, false, false, 128, 64);
+            constexpr uint32_t idQK = idesc(kFmtBF16, kFmtBF16, false, false, 64, 64);
             constexpr uint64_t kRow16 = 2048 >> 4;   // 16 rows of 128 B (MN-major K step)
             constexpr uint64_t kCol16 = 32 >> 4;     // 16 bf16 columns (K-major K step)
             const int hf = warp == kMmaWarpS ? 0 : 1;
@@ -274,8 +324,25 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 const uint32_t d = tmem + kTZ + 128 * hf, a = tmem + kTD + 64 * hf;
 #pragma unroll
                 for (int s = 0; s < 4; ++s) mma_bf16_ta(d, a + 8 * s, b + s * kRow16, idF, 1u);
-                mma_commit(&bars.zfull[hf]);
-                mma_commit(&bars.kempty[c % kKSlots]);
+                if (!outm) {
+                    mma_commit(&bars.zfull[hf]);
+                    mma_commit(&bars.kempty[c % kKSlots]);
+                }
+            };
+            // outputs instance: O^T = S~^T Q^T (A = the bf16 Z_S^T of d_S, B = the q chunk,
+            // K-major, 64-channel halves), and O^T += D_S^T A^T (A = the bf16 D_S^T of f_S,
+            // B = the masked Q K^T of the chunk, K-major)
+            auto issue_qs = [&](int c) {
+                const uint64_t b = dQ + (((c & 1) * kKV) >> 4);
+#pragma unroll
+                for (int s = 0; s < 8; ++s)
+                    mma_bf16_ta(tmem + kTO, tmem + kTZK + 8 * s, b + (((s >> 2) * kHalf) >> 4) + (s & 3) * kCol16,
+                                idO, s > 0 ? 1u : 0u);
+            };
+            auto issue_intra = [&](int c) {
+                const uint64_t b = dAq + (((c & 1) * kRec) >> 4);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) mma_bf16_ta(tmem + kTO, tmem + kTD + 8 * s, b + s * kCol16, idO, 1u);
             };
             bool ok = true;
             if (hf == 0) {
@@ -312,8 +379,13 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 for (int c = 0; ok && c < nch; ++c) {
                     const bool more = c + 1 < nch;
                     if (!(ok = wait(&bars.wready[c & 1], (c >> 1) & 1) && wait(&bars.zready[0], c & 1))) break;
+                    if (outm && !(ok = wait(&bars.qfull[c & 1], (c >> 1) & 1) &&
+                                       (c < 1 || wait(&bars.ofree, (c - 1) & 1))))
+                        break;
                     tc_fence_after();
+                    if (outm) issue_qs(c);
                     issue_d(c);
+                    if (outm) mma_commit(&bars.qempty[c & 1]);
                     if (more) {
                         if (!(ok = wait(&bars.dfull[0], c & 1) && wait(&bars.kfull[(c + 1) % kKSlots], ((c + 1) / kKSlots) & 1) &&
                                    wait(&bars.vfull[(c + 1) % kVSlots], ((c + 1) / kVSlots) & 1)))
@@ -324,12 +396,39 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                     if (!(ok = wait(&bars.dready[0], c & 1))) break;
                     tc_fence_after();
                     issue_f(c);
+                    if (outm) {
+                        if (!(ok = wait(&bars.aqready[c & 1], (c >> 1) & 1))) break;
+                        tc_fence_after();
+                        issue_intra(c);
+                        mma_commit(&bars.zfull[0]);
+                        mma_commit(&bars.kempty[c % kKSlots]);
+                        mma_commit(&bars.ofull);
+                    }
                     if (more) {
                         if (!(ok = wait(&bars.zfull[0], c & 1) && wait(&bars.m1ready[(c + 1) & 1], ((c + 1) >> 1) & 1)))
                             break;
                         tc_fence_after();
                         issue_u(c + 1);
                     }
+                }
+            } else if (outm) {
+                // outputs instance: Q K^T of every chunk (M = 64: A the q chunk, B the k chunk,
+                // both K-major) into the D_P columns, once the output warps have read the last
+                for (int c = 0; ok && c < nch; ++c) {
+                    if (!(ok = wait(&bars.qfull[c & 1], (c >> 1) & 1) &&
+                               wait(&bars.kfull[c % kKSlots], (c / kKSlots) & 1) &&
+                               (c < 1 || wait(&bars.aqfree, (c - 1) & 1))))
+                        break;
+                    tc_fence_after();
+                    const uint64_t a = dQ + (((c & 1) * kKV) >> 4), b = dKk + (((c % kKSlots) * kKV) >> 4);
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        const uint64_t o = (((s >> 2) * kHalf) >> 4) + (s & 3) * kCol16;
+                        mma_bf16(tmem + kTAq, a + o, b + o, idQK, s > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&bars.aqfull);
+                    mma_commit(&bars.qempty[c & 1]);
+                    mma_commit(&bars.kempty[c % kKSlots]);
                 }
             } else {
                 // per chunk: d_P(c) (frees the -W^T slot for the operand warps), f_P(c).
@@ -360,7 +459,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             la_next = q < min(C, seg.len) ? p.log_gate[tok * p.H_v + h] : 0.f;
         }
         for (int c = 0; c < nch; ++c) {
-            Slot &sl = slots[c & 1];
+            Slot &sl = slots[c % kSlots];
             // (1) gates: prefix sums c_t, chunk total c_C, the log-scale bookkeeping.
             //     Slot c % 2 was last read for chunk c - 2, whose W product has been issued.
             float x = la_next;
@@ -422,7 +521,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             //     slot was last read by d_S(c-2) (ordered before W(c) by its issuer) and by
             //     d_P(c-2), whose completion is signalled on wfree.
             if (!bar_aux_and(wait(&bars.wfull, c & 1) &&
-                             (c < 2 || wait(&bars.wfree[c & 1], ((c - 2) >> 1) & 1))))
+                             (outm || c < 2 || wait(&bars.wfree[c & 1], ((c - 2) >> 1) & 1))))
                 break;
             tc_fence_after();
             {
@@ -443,6 +542,55 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             fence_async_shared();
             tc_fence_before();
             mbar_arrive(&bars.wready[c & 1]);
+        }
+    } else if (outm && warp >= 4) {   // warps 4-7 (warps 8 and up took the branches above)
+        // ---------------------------------------------------------------- output warps 4-7
+        // Per chunk c: (a) the masked Q K^T (M = 64 accumulator: rows 16 (warp % 4) + lane in
+        // lanes 0-15) -> bf16 rows t of the K-major B operand, columns s <= t; (b) the outputs,
+        // o_t[n] = O^T[n][t] / ex_t with ex_t = exp(-Lam - c_t) from the chunk's gate slot.
+        const int n = threadIdx.x & 127;   // state column = TMEM lane
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        __nv_bfloat16 *Ob = static_cast<__nv_bfloat16 *>(p.O);
+        for (int c = 0; c < nch; ++c) {
+            if (!wwait(&bars.aqfull, c & 1)) break;
+            tc_fence_after();
+            {
+                uint32_t z[64];
+                ld64(tmem + lane_off + kTAq, z);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&bars.aqfree);
+                if (lane < 16) {
+                    const int t = 16 * (warp & 3) + lane;
+                    uint8_t *aq = smem + kOffAq + (c & 1) * kRec;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float f[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) f[e] = (8 * j + e <= t) ? __uint_as_float(z[8 * j + e]) : 0.f;
+                        *reinterpret_cast<uint4 *>(aq + sw128((uint32_t)t, 16u * j)) =
+                            make_uint4(bf2(f[0], f[1]), bf2(f[2], f[3]), bf2(f[4], f[5]), bf2(f[6], f[7]));
+                    }
+                }
+                fence_async_shared();
+                mbar_arrive(&bars.aqready[c & 1]);
+            }
+            if (!wwait(&bars.ofull, c & 1)) break;
+            tc_fence_after();
+            {
+                uint32_t z[64];
+                ld64(tmem + lane_off + kTO, z);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&bars.ofree);
+                const Slot &sl = slots[c % kSlots];
+                const int nv = min(C, seg.len - c * C);
+                const int64_t tok0 = (int64_t)seg.start + (int64_t)c * C;
+#pragma unroll
+                for (int t = 0; t < C; ++t)
+                    if (t < nv)
+                        Ob[((tok0 + t) * p.H_v + h) * D + n] = __float2bfloat16_rn(__uint_as_float(z[t]) / sl.ex[t]);
+            }
         }
     } else {
         // ---------------------------------------------------------------- chain warps 0-7
@@ -471,8 +619,8 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             if (hf == 0) {
                 if (!(ok = wwait(&bars.m1ready[c & 1], (c >> 1) & 1) && wwait(&bars.wready[c & 1], (c >> 1) & 1)))
                     break;
-                renorm = slots[c & 1].renorm != 0;
-                rs = slots[c & 1].rscale;
+                renorm = slots[c % kSlots].renorm != 0;
+                rs = slots[c % kSlots].rscale;
             }
             tc_fence_after();
 #pragma unroll
@@ -506,23 +654,27 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             tc_fence_before();
             mbar_arrive(&bars.dready[hf]);
         }
-        // outputs: S = exp(Lam) S~ (column n) or P (column n), and lam
+        // outputs: S = exp(Lam) S~ (column n) or P (column n), and lam (the outputs instance
+        // writes only O)
         if (ok && nch > 0) ok = wwait(&bars.zfull[hf], (nch - 1) & 1);
         tc_fence_after();
-        // a piece of a split segment writes its own slot; a whole segment the caller's output
-        const bool piece = seg.idx < 0;
-        const int64_t unit = piece ? (int64_t)(-1 - seg.idx) * p.H_v + h : (int64_t)seg.idx * p.seg_stride + h;
-        float *O = (hf == 0 ? (piece ? p.S_piece : p.S) : (piece ? p.P_piece : p.P)) + unit * D * D + n;
-        const float sc = (hf == 0 && nch > 0) ? expf(slots[(nch - 1) & 1].lam_after) : 1.f;
+
+        if (!outm) {
+            // a piece of a split segment writes its own slot; a whole segment the caller's output
+            const bool piece = seg.idx < 0;
+            const int64_t unit = piece ? (int64_t)(-1 - seg.idx) * p.H_v + h : (int64_t)seg.idx * p.seg_stride + h;
+            float *O = (hf == 0 ? (piece ? p.S_piece : p.S) : (piece ? p.P_piece : p.P)) + unit * D * D + n;
+            const float sc = (hf == 0 && nch > 0) ? expf(slots[(nch - 1) % kSlots].lam_after) : 1.f;
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-            uint32_t z[32];
-            tmem_ld32(tmem + lane_off + zcol + c0, z);
-            tmem_ld_wait();
+            for (int c0 = 0; c0 < 128; c0 += 32) {
+                uint32_t z[32];
+                tmem_ld32(tmem + lane_off + zcol + c0, z);
+                tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) O[(int64_t)(c0 + j) * D] = __uint_as_float(z[j]) * sc;
+                for (int j = 0; j < 32; ++j) O[(int64_t)(c0 + j) * D] = __uint_as_float(z[j]) * sc;
+            }
+            if (hf == 0 && n == 0) (piece ? p.lam_piece : p.lam)[unit] = nch > 0 ? slots[(nch - 1) % kSlots].lam_sum : 0.f;
         }
-        if (hf == 0 && n == 0) (piece ? p.lam_piece : p.lam)[unit] = nch > 0 ? slots[(nch - 1) & 1].lam_sum : 0.f;
     }
 
     tc_fence_before();
@@ -541,17 +693,25 @@ bool build_gdn_tc_supported(const BuildParams &p) {
 }
 
 cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s) {
-    const int blocks = p.n_seg * p.H_v;
+    // with the segment outputs, a second CTA per unit runs the outputs instance
+    const int blocks = p.n_seg * p.H_v * (p.O ? 2 : 1);
     if (blocks == 0) return cudaSuccess;
     int64_t records = 0;
     for (int r = 0; r < p.n_seg; ++r) records += (int64_t)p.H_v * ((p.seg[r].len + C - 1) / C);
     const int64_t N = p.n_tok > 0 ? p.n_tok : 1;
-    CUtensorMap tmK, tmV, tmR;
+    CUtensorMap tmK, tmV, tmR, tmQ;
     if (!make_tmap_3d(&tmK, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_k, N, (uint64_t)D * 2,
                       (uint64_t)p.H_k * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_3d(&tmV, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_v, N, (uint64_t)D * 2,
                       (uint64_t)p.H_v * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
+    if (p.O) {
+        if (!make_tmap_3d(&tmQ, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_k, N, (uint64_t)D * 2,
+                          (uint64_t)p.H_k * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    } else {
+        tmQ = tmK;   // no outputs instance: never read
+    }
     if (records > 0) {
         if (!p.workspace ||
             !make_tmap_2d(&tmR, p.workspace, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 64, (uint64_t)records * 64,
@@ -562,10 +722,11 @@ cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s) {
     }
     cudaError_t e = launch_build_gdn_prep(p, s);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(build_gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    const uint32_t smem = p.O ? kSmemBytesOut : kSmemBytes;
+    e = cudaFuncSetAttribute(build_gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (records == 0) {
-        build_gdn_tc_kernel<<<blocks, kThreads, kSmemBytes, s>>>(p, tmK, tmV, tmR);
+        build_gdn_tc_kernel<<<blocks, kThreads, smem, s>>>(p, tmK, tmV, tmR, tmQ);
         return cudaGetLastError();
     }
     // launched as a programmatic dependent of the preparation kernel: CTAs may start (set-up,
@@ -574,14 +735,14 @@ cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, build_gdn_tc_kernel, p, tmK, tmV, tmR);
+    return cudaLaunchKernelEx(&cfg, build_gdn_tc_kernel, p, tmK, tmV, tmR, tmQ);
 }
 
 }  // namespace hypic

@@ -276,11 +276,18 @@ def test_kda_needs_gates_beta_and_P(lib):
         assert call_build(lib, a) == 1
 
 
-def test_kda_and_outputs_take_the_exact_path(lib):
+def test_path_of_kda_outputs_and_start_states(lib):
     a = good_build(family=5)
     assert lib.hypic_build_kernel_name(ctypes.byref(a)) == b"build_seq"
     a = good_build(family=4)
     assert lib.hypic_build_kernel_name(ctypes.byref(a)) == b"build_gdn_tc"
-    a.q, a.O = FAKE + 0x8000000, FAKE + 0x9000000
+    recs = lib.hypic_build_workspace_bytes(ctypes.byref(a))
+    a.q, a.O = FAKE + 0x8000000, FAKE + 0x9000000   # GDN outputs: the tensor-core build
+    assert lib.hypic_build_kernel_name(ctypes.byref(a)) == b"build_gdn_tc"
+    assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == recs
+    a.S_init = FAKE + 0xA000000                      # start states: the exact path
     assert lib.hypic_build_kernel_name(ctypes.byref(a)) == b"build_seq"
     assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == 0
+    b = good_build(family=2)                         # outputs of the other families: exact path
+    b.q, b.O = FAKE + 0x8000000, FAKE + 0x9000000
+    assert lib.hypic_build_kernel_name(ctypes.byref(b)) == b"build_seq"

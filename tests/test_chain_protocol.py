@@ -34,9 +34,14 @@ class _Bar:
             self.done += 1
 
 
-def _run(nch, seed, mistake=None):
+def _run(nch, seed, mistake=None, out=False):
+    """One unit of nch chunks. out: the outputs instance of the kernel, whose P-half issuer
+    computes the masked Q K^T of every chunk (Q by TMA into a two-slot ring) and whose P-half
+    warps turn it into the bf16 operand of the intra-chunk product and read the outputs out;
+    the S-half issuer adds Q S~ before d_S and the intra-chunk product after f_S."""
     rnd = random.Random(seed)
     KS = VS = 3
+    SL = 3   # per-chunk gate slots
     B = {}
     for s in range(KS):
         B[f"kfull{s}"], B[f"kempty{s}"] = _Bar(), _Bar(2)
@@ -48,9 +53,14 @@ def _run(nch, seed, mistake=None):
         for n in ("dfull", "zfull", "wfree"):
             B[f"{n}{s}"] = _Bar()
     B["wfull"] = _Bar()
+    for s_ in range(2):
+        B[f"qfull{s_}"], B[f"qempty{s_}"] = _Bar(), _Bar(2)   # qempty: Q S~ and Q K^T
+        B[f"aqready{s_}"] = _Bar()
+    for n_ in ("aqfull", "aqfree", "ofull", "ofree"):
+        B[n_] = _Bar()
     # buffer contents (versions)
     m = dict(ZK0=None, ZK1=None, D0=None, D1=None, Z0=("Z", -1), Z1=("Z", -1), k={}, vr={},
-             wop={}, m1={}, slot={}, w_read=set())
+             wop={}, m1={}, slot={}, w_read=set(), q={}, aq={}, AQ=None, O=None)
     queues = {0: [], 1: []}   # per issuer: pending MMAs and commits, in issue order
 
     def wait(name, phase):
@@ -75,6 +85,13 @@ def _run(nch, seed, mistake=None):
             touches_inflight([("vr", vs)], True, "{v, M2} load")
             m["vr"][vs] = c
             B[f"vfull{vs}"].arrive()
+            if out:
+                qs, quse = c % 2, c // 2
+                if quse >= 1 and mistake != "q_without_qempty":
+                    yield from wait(f"qempty{qs}", quse - 1)
+                touches_inflight([("q", qs)], True, "q load")
+                m["q"][qs] = c
+                B[f"qfull{qs}"].arrive()
             yield
 
     # ---------------------------------------------------------------- MMA issuers
@@ -98,8 +115,15 @@ def _run(nch, seed, mistake=None):
             more = c + 1 < nch
             yield from wait(f"wready{c & 1}", c >> 1)
             yield from wait("zready0", c)
+            if out:
+                yield from wait(f"qfull{c % 2}", c // 2)
+                if c >= 1 and mistake != "qs_without_ofree":
+                    yield from wait("ofree", c - 1)
+                issue(0, dict(kind="QS", c=c, q=c % 2))
             issue(0, dict(kind="dS", c=c, wop=c & 1))
             commit(0, "dfull0")
+            if out:
+                commit(0, f"qempty{c % 2}")
             yield
             if more:
                 if mistake != "w_before_dS_done":
@@ -110,8 +134,13 @@ def _run(nch, seed, mistake=None):
                 commit(0, "wfull")
             yield from wait("dready0", c)
             issue(0, dict(kind="fS", c=c, k=c % KS))
+            if out:
+                yield from wait(f"aqready{c & 1}", c >> 1)
+                issue(0, dict(kind="intra", c=c, aq=c & 1))
             commit(0, "zfull0")
             commit(0, f"kempty{c % KS}")
+            if out:
+                commit(0, "ofull")
             yield
             if more:
                 yield from wait("zfull0", c)
@@ -120,6 +149,18 @@ def _run(nch, seed, mistake=None):
                 commit(0, f"vempty{(c + 1) % VS}")
 
     def issuer_p():
+        if out:   # Q K^T of every chunk into its TMEM accumulator
+            for c in range(nch):
+                yield from wait(f"qfull{c % 2}", c // 2)
+                yield from wait(f"kfull{c % KS}", c // KS)
+                if c >= 1 and mistake != "qk_without_aqfree":
+                    yield from wait("aqfree", c - 1)
+                issue(1, dict(kind="QK", c=c, q=c % 2, k=c % KS))
+                commit(1, "aqfull")
+                commit(1, f"qempty{c % 2}")
+                commit(1, f"kempty{c % KS}")
+                yield
+            return
         for c in range(nch):
             yield from wait(f"wready{c & 1}", c >> 1)
             yield from wait("zready1", c)
@@ -149,6 +190,12 @@ def _run(nch, seed, mistake=None):
             return {("vr", op["vr"]): c, ("m1", op["m1"]): c}, {"D0": ("U", c)}
         if kind == "dS":
             return {"ZK0": ("Z", c), ("wop", op["wop"]): c, "D0": ("U", c)}, {"D0": ("d", c)}
+        if kind == "QS":
+            return {"ZK0": ("Z", c), ("q", op["q"]): c}, {"O": ("QS", c)}
+        if kind == "QK":
+            return {("q", op["q"]): c, ("k", op["k"]): c}, {"AQ": ("AQ", c)}
+        if kind == "intra":
+            return {"D0": ("Dbf", c), ("aq", op["aq"]): c, "O": ("QS", c)}, {"O": ("O", c)}
         if kind == "dP":
             return {"ZK1": ("Z", c), ("wop", op["wop"]): c}, {"D1": ("d", c)}
         hf = 0 if kind == "fS" else 1
@@ -156,7 +203,8 @@ def _run(nch, seed, mistake=None):
 
     def chained(x, y):
         """y may overlap x: the same accumulator, accumulated in issue order by one issuer."""
-        return x["kind"] == "U" and y["kind"] == "dS" and x["c"] == y["c"]
+        return ((x["kind"] == "U" and y["kind"] == "dS") or (x["kind"] == "QS" and y["kind"] == "intra")) \
+            and x["c"] == y["c"]
 
     def touches_inflight(keys, writing, who):
         for q in inflight.values():
@@ -217,7 +265,7 @@ def _run(nch, seed, mistake=None):
     # ---------------------------------------------------------------- operand warps
     def operand():
         for c in range(nch):
-            m["slot"][c & 1] = c
+            m["slot"][c % SL] = c
             yield
             yield from wait(f"vfull{c % VS}", c // VS)
             if m["vr"].get(c % VS) != c:
@@ -227,7 +275,7 @@ def _run(nch, seed, mistake=None):
             B[f"m1ready{c & 1}"].arrive()
             yield
             yield from wait("wfull", c)
-            if c >= 2 and mistake != "no_wfree":
+            if c >= 2 and mistake != "no_wfree" and not out:   # d_P's read of the slot
                 yield from wait(f"wfree{c & 1}", (c - 2) >> 1)
             if m["ZK0"] != ("W", c):
                 raise Hazard(f"W read-out finds {m['ZK0']}")
@@ -246,7 +294,7 @@ def _run(nch, seed, mistake=None):
                 yield from wait(f"m1ready{c & 1}", c >> 1)
                 if mistake != "no_wready_before_z":
                     yield from wait(f"wready{c & 1}", c >> 1)
-                if m["slot"].get(c & 1) != c:
+                if m["slot"].get(c % SL) != c:
                     raise Hazard("gate slot of another chunk")
                 if c >= 1 and c not in m["w_read"] and m["ZK0"] == ("W", c):
                     raise Hazard("Z copy written over W before its read-out")
@@ -271,8 +319,34 @@ def _run(nch, seed, mistake=None):
             if m[f"Z{hf}"] != ("Z", nch - 1):
                 raise Hazard("output reads a stale state")
 
+    # ---------------------------------------------------------------- output warps (out)
+    # the P-half warps of the outputs instance: the masked Q K^T into the bf16 B operand of the
+    # intra-chunk product, then the outputs read out and scaled with the chunk's gate slot
+    def outwarps():
+        for c in range(nch):
+            yield from wait("aqfull", c)
+            if m["AQ"] != ("AQ", c):
+                raise Hazard(f"Q K^T read-out at chunk {c} finds {m['AQ']}")
+            touches_inflight(["AQ"], False, "Q K^T read-out")
+            B["aqfree"].arrive()
+            yield
+            touches_inflight([("aq", c & 1)], True, "masked Q K^T write")
+            m["aq"][c & 1] = c
+            B[f"aqready{c & 1}"].arrive()
+            yield
+            yield from wait("ofull", c)
+            if m["O"] != ("O", c):
+                raise Hazard(f"output read-out at chunk {c} finds {m['O']}")
+            touches_inflight(["O"], False, "output read-out")
+            B["ofree"].arrive()
+            if m["slot"].get(c % SL) != c:
+                raise Hazard("output scale read from the gate slot of another chunk")
+            yield
+
+    if mistake == "two_gate_slots":
+        SL = 2
     actors = {"tma": tma(), "s": issuer_s(), "p": issuer_p(), "pipe": pipe(), "op": operand(),
-              "c0": conversion(0), "c1": conversion(1)}
+              "c0": conversion(0), "c1": outwarps() if out else conversion(1)}
     # per-run speeds: some runs starve one agent, so that the others run ahead as far as the
     # protocol lets them
     speed = {k: rnd.choice((0.05, 1.0, 1.0, 4.0)) for k in actors}
@@ -302,6 +376,26 @@ def test_chain_protocol_interleavings(nch):
         assert _run(nch, seed) == "ok"
 
 
+@pytest.mark.parametrize("nch", [1, 2, 3, 4, 7])
+def test_outputs_instance_protocol_interleavings(nch):
+    for seed in range(25):
+        assert _run(nch, seed, out=True) == "ok"
+
+
+@pytest.mark.parametrize("mistake", ["q_without_qempty", "qs_without_ofree", "qk_without_aqfree",
+                                     "two_gate_slots"])
+def test_outputs_instance_model_catches_planted_mistakes(mistake):
+    hits = 0
+    for seed in range(80):
+        try:
+            r = _run(6, seed, mistake, out=True)
+        except Hazard:
+            hits += 1
+            continue
+        hits += r != "ok"
+    assert hits > 0
+
+
 @pytest.mark.parametrize("mistake", ["no_wready_before_z", "no_wfree", "w_before_dS_done"])
 def test_chain_protocol_model_catches_planted_mistakes(mistake):
     """Dropping any one of these waits lets some interleaving read or overwrite a buffer in the
@@ -318,7 +412,7 @@ def test_chain_protocol_model_catches_planted_mistakes(mistake):
 
 
 # The kernel source this model was last checked against (code only; comments do not count).
-MODELLED_SOURCE = ("build_gdn_tc.cu", "9702cefe1f3e")
+MODELLED_SOURCE = ("build_gdn_tc.cu", "294b7f765937")
 
 
 def test_model_is_checked_against_the_current_kernel_source():

@@ -107,3 +107,24 @@ def test_workload_gdn_outputs():
     inp = synth.make_workload("gdn", with_q=True)
     S, lam, P, O = gpu_build_out(inp)
     assert out_errors(inp, f64(O), oracle_outputs(inp)) <= TOL[inp.dtype]
+
+
+@pytest.mark.parametrize("family", ["gdn", "delta"])
+def test_tensor_core_outputs_over_many_units_and_key_sharing(family):
+    """The tensor-core build's outputs instance over more (segment, head) units than SMs,
+    ragged segments (empty, one-token, partial chunks), grouped-query keys (4 value heads per
+    key head), and one long segment that is not split into pieces when outputs are asked for."""
+    hy = _hy()
+    lens = [int(x) for x in np.random.default_rng(98).integers(0, 300, size=60)]
+    lens[:5] = [0, 1, 64, 65, 2000]
+    inp = synth.make_inputs(family, 1, 4, 128, lens, torch.bfloat16, seed=99, with_q=True,
+                            alpha_scale=0.05)
+    d = to_dev(inp)
+    assert hy.hypic_build_kernel_name(family, d["k"], d["v"], inp.seg_offsets,
+                                      log_gate=d.get("log_gate"), beta=d["beta"], q=d["q"],
+                                      O=torch.empty_like(d["v"])) == "build_gdn_tc"
+    S, lam, P, O = gpu_build_out(inp)
+    assert out_errors(inp, f64(O), oracle_outputs(inp)) <= 2e-2
+    So, To = oracle_build(inp)
+    assert_close(f64(S), So, 2e-2, "S")
+    assert_close(gpu_T(family, lam, P, 128), To, 2e-2, "T")
