@@ -55,6 +55,9 @@ GDN_FLOP_PER_TOKEN_HEAD = 6 * CHUNK * 128 + 8 * 128 * 128   # 180,224
 SEQ_D = 128
 SEQ_FLOP_PER_TOKEN_HEAD = {"kda": 2 * 5 * SEQ_D * SEQ_D, "gdn": (5 + 4) * SEQ_D * SEQ_D}
 SEQ_OUT_FLOP = 2 * SEQ_D * SEQ_D
+# the segment outputs on the chunked form, per token per value head: Q S 2d^2, the chunk's
+# Q K^T 2Cd and its masked product with the delta values 2Cd
+GDN_OUT_FLOP_PER_TOKEN_HEAD = 2 * 128 * 128 + 4 * CHUNK * 128   # 65,536
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -354,8 +357,9 @@ def section_family(name, flush, peak, steps=20, warmup=3, oracle_budget_s=0.0):
 
 def section_outputs(name, flush, peak, steps=10, warmup=3, oracle_budget_s=0.0):
     """The build of a workload that also returns the segment outputs O(C|0) (queries drawn
-    with the workload): the exact sequential path, against the fp32 FFMA peak; the oracle
-    leg times oracle.outputs on a sample of heads and reports the parity of O there."""
+    with the workload), against the roofline of the path it takes (the tensor-core GDN build:
+    the bf16 peak; the exact sequential path: the fp32 FFMA peak); the oracle leg times
+    oracle.outputs on a sample of heads and reports the parity of O there."""
     import linear_attention_state_gdn_gb300 as hy
     from linear_attention_state_gdn_gb300 import synth
     inp = synth.make_workload(name, with_q=True)
@@ -367,14 +371,19 @@ def section_outputs(name, flush, peak, steps=10, warmup=3, oracle_budget_s=0.0):
                                         lam=lam, P=P, q=dev["q"], O=O, **kw)
     (tb,), _ = time_loop([f], steps, warmup, flush)
     ms = statistics.mean(tb)
-    flop = (SEQ_FLOP_PER_TOKEN_HEAD[inp.family] + SEQ_OUT_FLOP) * inp.n_tok * inp.H_v
-    tf = flop / (ms * 1e-3) / 1e12
-    alu = fp32_alu_peak_tflops(peak["sm_max_mhz"])
     bk = hy.hypic_build_kernel_name(inp.family, dev["k"], dev["v"], inp.seg_offsets, S=S, lam=lam,
                                     P=P, q=dev["q"], O=O, **kw)
-    out = {"build_kernel": bk, "build_ms": round(ms, 4), "build_tokens_per_s": round(inp.n_tok / ms * 1e3, 1),
-           "build_tflops": round(tf, 2), "build_alu_frac": round(tf / alu, 4),
-           "alu_peak_tflops": round(alu, 1)}
+    out = {"build_kernel": bk, "build_ms": round(ms, 4), "build_tokens_per_s": round(inp.n_tok / ms * 1e3, 1)}
+    if bk == "build_gdn_tc":   # the chunked form's flops (S, T and O) against the bf16 peak
+        flop = (GDN_FLOP_PER_TOKEN_HEAD + GDN_OUT_FLOP_PER_TOKEN_HEAD) * inp.n_tok * inp.H_v
+        tf = flop / (ms * 1e-3) / 1e12
+        out.update({"build_tflops": round(tf, 1), "build_tensor_frac": round(tf / peak["bf16_tflops"], 4)})
+    else:                      # the sequential form against the FFMA peak
+        flop = (SEQ_FLOP_PER_TOKEN_HEAD[inp.family] + SEQ_OUT_FLOP) * inp.n_tok * inp.H_v
+        tf = flop / (ms * 1e-3) / 1e12
+        alu = fp32_alu_peak_tflops(peak["sm_max_mhz"])
+        out.update({"build_tflops": round(tf, 2), "build_alu_frac": round(tf / alu, 4),
+                    "alu_peak_tflops": round(alu, 1)})
     if oracle_budget_s:
         torch.cuda.synchronize()
         out["cpu_baseline"] = outputs_cpu_baseline(inp, O, oracle_budget_s)

@@ -92,7 +92,6 @@ constexpr uint32_t kSmemBytes = kOffM1 + 2 * kRec + 1024;
 constexpr uint32_t kOffQ = kOffM1 + 2 * kRec;
 constexpr uint32_t kOffAq = kOffQ + 2 * kKV;
 constexpr uint32_t kSmemBytesOut = kOffAq + 2 * kRec + 1024;
-constexpr int kSlots = 3;   // per-chunk gate slots
 
 constexpr uint32_t kTZ = 0, kTD = 256, kTZK = 384;
 constexpr uint32_t kTO = 128, kTAq = 320;   // outputs instance: O^T and Q K^T (the P half's columns)
@@ -162,6 +161,9 @@ __device__ __forceinline__ void st_bf16x64(uint32_t taddr, const uint32_t (&z)[6
     }
 }
 
+// OUT: the instance launched when the call asks for the segment outputs (both kinds of CTA);
+// the plain build compiles without any of the outputs code
+template <bool OUT>
 __global__ void __launch_bounds__(kThreads, 1)
 build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmR,
@@ -171,6 +173,9 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
     // compiler keeps the shared address space (plain ld/st.shared, not generic accesses)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ Bars bars;
+    // per-chunk gate slots: the outputs instance reads a chunk's slot after its last product,
+    // so it keeps three (a slot is rewritten three chunks later)
+    constexpr int kSlots = OUT ? 3 : 2;
     __shared__ __align__(16) Slot slots[kSlots];
     __shared__ uint32_t tslot;
     __shared__ volatile int abort_flag;
@@ -178,7 +183,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
 
     const int warp = warp_id(), lane = lane_id();
     const int units = p.n_seg * p.H_v;
-    const bool outm = (int)blockIdx.x >= units;   // the outputs instance of unit blockIdx - units
+    const bool outm = OUT && (int)blockIdx.x >= units;   // the outputs instance of unit blockIdx - units
     const int ux = outm ? (int)blockIdx.x - units : (int)blockIdx.x;
     const SegEntry seg = p.seg[ux / p.H_v];
     const int h = ux % p.H_v;
@@ -581,15 +586,18 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 uint32_t z[64];
                 ld64(tmem + lane_off + kTO, z);
                 tmem_ld_wait();
+                // scaled with the chunk's gate slot before the accumulator is freed: freeing
+                // it lets the next chunks run on, and the slot is rewritten three chunks later
+                const Slot &sl = slots[c % kSlots];
+#pragma unroll
+                for (int t = 0; t < C; ++t) z[t] = __float_as_uint(__uint_as_float(z[t]) / sl.ex[t]);
                 tc_fence_before();
                 mbar_arrive(&bars.ofree);
-                const Slot &sl = slots[c % kSlots];
                 const int nv = min(C, seg.len - c * C);
                 const int64_t tok0 = (int64_t)seg.start + (int64_t)c * C;
 #pragma unroll
                 for (int t = 0; t < C; ++t)
-                    if (t < nv)
-                        Ob[((tok0 + t) * p.H_v + h) * D + n] = __float2bfloat16_rn(__uint_as_float(z[t]) / sl.ex[t]);
+                    if (t < nv) Ob[((tok0 + t) * p.H_v + h) * D + n] = __float2bfloat16_rn(__uint_as_float(z[t]));
             }
         }
     } else {
@@ -723,10 +731,11 @@ cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s) {
     cudaError_t e = launch_build_gdn_prep(p, s);
     if (e != cudaSuccess) return e;
     const uint32_t smem = p.O ? kSmemBytesOut : kSmemBytes;
-    e = cudaFuncSetAttribute(build_gdn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    auto kern = p.O ? build_gdn_tc_kernel<true> : build_gdn_tc_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (records == 0) {
-        build_gdn_tc_kernel<<<blocks, kThreads, smem, s>>>(p, tmK, tmV, tmR, tmQ);
+        kern<<<blocks, kThreads, smem, s>>>(p, tmK, tmV, tmR, tmQ);
         return cudaGetLastError();
     }
     // launched as a programmatic dependent of the preparation kernel: CTAs may start (set-up,
@@ -742,7 +751,7 @@ cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, build_gdn_tc_kernel, p, tmK, tmV, tmR, tmQ);
+    return cudaLaunchKernelEx(&cfg, kern, p, tmK, tmV, tmR, tmQ);
 }
 
 }  // namespace hypic

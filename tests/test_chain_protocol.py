@@ -338,10 +338,16 @@ def _run(nch, seed, mistake=None, out=False):
             if m["O"] != ("O", c):
                 raise Hazard(f"output read-out at chunk {c} finds {m['O']}")
             touches_inflight(["O"], False, "output read-out")
-            B["ofree"].arrive()
-            if m["slot"].get(c % SL) != c:
-                raise Hazard("output scale read from the gate slot of another chunk")
-            yield
+            # the outputs are scaled with the chunk's gate slot, read over some time; the
+            # accumulator is freed after that (freeing it first lets the slot be rewritten)
+            if mistake == "slot_read_after_ofree":
+                B["ofree"].arrive()
+            for _ in range(2):
+                if m["slot"].get(c % SL) != c:
+                    raise Hazard("output scale read from the gate slot of another chunk")
+                yield
+            if mistake != "slot_read_after_ofree":
+                B["ofree"].arrive()
 
     if mistake == "two_gate_slots":
         SL = 2
@@ -383,7 +389,7 @@ def test_outputs_instance_protocol_interleavings(nch):
 
 
 @pytest.mark.parametrize("mistake", ["q_without_qempty", "qs_without_ofree", "qk_without_aqfree",
-                                     "two_gate_slots"])
+                                     "two_gate_slots", "slot_read_after_ofree"])
 def test_outputs_instance_model_catches_planted_mistakes(mistake):
     hits = 0
     for seed in range(80):
@@ -412,7 +418,7 @@ def test_chain_protocol_model_catches_planted_mistakes(mistake):
 
 
 # The kernel source this model was last checked against (code only; comments do not count).
-MODELLED_SOURCE = ("build_gdn_tc.cu", "294b7f765937")
+MODELLED_SOURCE = ("build_gdn_tc.cu", "89cdbe262dca")
 
 
 def test_model_is_checked_against_the_current_kernel_source():
