@@ -92,6 +92,7 @@ bool compose_dense_tc_supported(const ComposeParams &p);
 cudaError_t launch_build_gated_tc(const BuildParams &p, cudaStream_t s);
 bool build_gated_tc_supported(const BuildParams &p);
 cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s);
+cudaError_t launch_build_gdn_tc_outputs(const BuildParams &p, cudaStream_t s);
 cudaError_t launch_build_gdn_prep(const BuildParams &p, cudaStream_t s);
 bool build_gdn_tc_supported(const BuildParams &p);
 
