@@ -590,7 +590,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 // it lets the next chunks run on, and the slot is rewritten three chunks later
                 const Slot &sl = slots[c % kSlots];
 #pragma unroll
-                for (int t = 0; t < C; ++t) z[t] = __float_as_uint(__uint_as_float(z[t]) / sl.ex[t]);
+                for (int t = 0; t < C; ++t) z[t] = __float_as_uint(__fdividef(__uint_as_float(z[t]), sl.ex[t]));
                 tc_fence_before();
                 mbar_arrive(&bars.ofree);
                 const int nv = min(C, seg.len - c * C);

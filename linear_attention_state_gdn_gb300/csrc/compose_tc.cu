@@ -7,9 +7,8 @@
 // the final state from the segments' results).
 //
 // Precision. fp32-accurate products from three tf32 MMAs (hi/lo split of both operands:
-// A_hi B_hi + A_lo B_hi + A_hi B_lo, error ~2^-22 relative), fp32 accumulation. Both parts
-// are rounded to tf32 explicitly (to nearest), so the result does not depend on how the
-// tensor core reads fp32 operands, and the split carries no bias.
+// A_hi B_hi + A_lo B_hi + A_hi B_lo, error ~2^-21 relative), fp32 accumulation. The hi parts
+// are rounded to tf32 explicitly (to nearest), so that the lo parts carry no bias.
 //
 // Data flow of one CTA (persistent over units, one unit at a time):
 //   * the transposed running state prefix_{j-1}^T, scaled by exp(lam_j) and split into
@@ -77,10 +76,11 @@ struct Bars {
 __device__ __forceinline__ int exponent_of(float x) { return (int)((__float_as_uint(x) >> 23) & 0xFFu) - 127; }
 
 // x rounded to the nearest tf32 value, ties away from zero (sign-magnitude: adding half a tf32
-// unit to the magnitude bits, then clearing the 13 low mantissa bits). Both parts of every
-// split are rounded this way, so that the MMA sees exact tf32 values and neither part carries a
-// bias: truncated parts all err toward zero, and over long chains of products (a composed
-// transition of 64 segments) that bias accumulates.
+// unit to the magnitude bits, then clearing the 13 low mantissa bits). The hi part of every
+// split is rounded this way, so that the lo part x - hi (exact in fp32) takes either sign and
+// the tensor core's reading of it (it keeps tf32 bits only) errs both ways: a truncated hi
+// made every lo part the same sign as x, and that bias accumulated over long chains of
+// products.
 __device__ __forceinline__ float tf32_rna(float x) {
     return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
@@ -255,10 +255,10 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                     const int idx = t + kEpi * q;
                     const float4 x = src[idx];
                     float4 h, l;
-                    h.x = tf32_rna(x.x); l.x = tf32_rna(x.x - h.x);
-                    h.y = tf32_rna(x.y); l.y = tf32_rna(x.y - h.y);
-                    h.z = tf32_rna(x.z); l.z = tf32_rna(x.z - h.z);
-                    h.w = tf32_rna(x.w); l.w = tf32_rna(x.w - h.w);
+                    h.x = tf32_rna(x.x); l.x = x.x - h.x;
+                    h.y = tf32_rna(x.y); l.y = x.y - h.y;
+                    h.z = tf32_rna(x.z); l.z = x.z - h.z;
+                    h.w = tf32_rna(x.w); l.w = x.w - h.w;
                     src[idx] = h;
                     dst[idx] = l;
                 }
@@ -288,7 +288,7 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                         const float x = s0[(16 * c + i) * D] * sc0;
                         const float h = tf32_rna(x);
                         hi[i] = __float_as_uint(h);
-                        lo[i] = __float_as_uint(tf32_rna(x - h));
+                        lo[i] = __float_as_uint(x - h);
                     }
                     tmem_st16(tA_hi + lane_off + 16 * c, hi);
                     tmem_st16(tA_lo + lane_off + 16 * c, lo);
@@ -363,7 +363,7 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                             const float x = v * scale_next;
                             const float h = tf32_rna(x);
                             hi[i] = __float_as_uint(h);
-                            lo[i] = __float_as_uint(tf32_rna(x - h));
+                            lo[i] = __float_as_uint(x - h);
                         }
                         if (next) {
                             tmem_st16(tA_hi + lane_off + 16 * c, hi);
