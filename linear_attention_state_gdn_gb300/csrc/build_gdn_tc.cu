@@ -51,9 +51,11 @@
 // (with Delta = exp(Lam) D_S the chunk's delta values, o_t = e^{c_t} (S_before^T q_t +
 // sum_{s<=t} (q_t . k_s) Delta_s)): the S~ issuer adds Q S~ (A = the bf16 Z_S^T already in TMEM,
 // B = the q chunk) before d_S and the intra-chunk product (A = the bf16 D_S^T, B = A) after f_S,
-// into the Z_P columns [128,192); the P issuer computes Q K^T (M = 64) into the D_P columns;
+// into the Z_P columns (two 64-column buffers by chunk parity, so that a chunk's products do
+// not wait for the previous chunk's read-out); the P issuer computes Q K^T (M = 64) into the
+// D_P columns;
 // the P-half warps turn it into the bf16 operand A (masked) and read the outputs out, scaled
-// with the chunk's gate slot (three slots, so that the slot outlives the read-out).
+// with the chunk's gate slot (four slots, so that the slot outlives the read-out).
 // Every wait is bounded; a wait that runs out sets the status word and the CTA drains.
 #include <algorithm>
 
@@ -94,7 +96,7 @@ constexpr uint32_t kOffAq = kOffQ + 2 * kKV;
 constexpr uint32_t kSmemBytesOut = kOffAq + 2 * kRec + 1024;
 
 constexpr uint32_t kTZ = 0, kTD = 256, kTZK = 384;
-constexpr uint32_t kTO = 128, kTAq = 320;   // outputs instance: O^T and Q K^T (the P half's columns)
+constexpr uint32_t kTO = 128, kTAq = 320;   // outputs instance: O^T (two buffers) and Q K^T (the P half's columns)
 
 struct Slot {   // per-chunk values from the operand warps (two slots)
     float ex[C];      // exp(-Lam_start - c_t)
@@ -117,7 +119,7 @@ struct Bars {
     uint64_t fin[2];
     // outputs instance: the q ring (emptied by Q S~ and Q K^T), Q K^T in TMEM (written by the
     // P issuer, read by the output warps), its bf16 slots, and the output accumulator
-    uint64_t qfull[2], qempty[2], aqfull, aqfree, aqready[2], ofull, ofree;
+    uint64_t qfull[2], qempty[2], aqfull, aqfree, aqready[2], ofull[2], ofree[2];   // O: two buffers
 };
 
 // Named barrier of the 128 operand-warp threads, and the same with an AND of a predicate
@@ -173,9 +175,9 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
     // compiler keeps the shared address space (plain ld/st.shared, not generic accesses)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ Bars bars;
-    // per-chunk gate slots: the outputs instance reads a chunk's slot after its last product,
-    // so it keeps three (a slot is rewritten three chunks later)
-    constexpr int kSlots = OUT ? 3 : 2;
+    // per-chunk gate slots: the outputs instance reads a chunk's slot after its last product
+    // while its S~ issuer runs up to two chunks ahead (two output buffers), so it keeps four
+    constexpr int kSlots = OUT ? 4 : 2;
     __shared__ __align__(16) Slot slots[kSlots];
     __shared__ uint32_t tslot;
     __shared__ volatile int abort_flag;
@@ -219,8 +221,10 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
         }
         mbar_init(&bars.aqfull, 1);
         mbar_init(&bars.aqfree, 128);
-        mbar_init(&bars.ofull, 1);
-        mbar_init(&bars.ofree, 128);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars.ofull[s], 1);
+            mbar_init(&bars.ofree[s], 128);
+        }
         abort_flag = 0;
         fence_mbar_init();
         // the kernel after this one (the merge of split segments) may launch and set up on SMs
@@ -339,15 +343,17 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             // B = the masked Q K^T of the chunk, K-major)
             auto issue_qs = [&](int c) {
                 const uint64_t b = dQ + (((c & 1) * kKV) >> 4);
+                const uint32_t d = tmem + kTO + 64 * (c & 1);
 #pragma unroll
                 for (int s = 0; s < 8; ++s)
-                    mma_bf16_ta(tmem + kTO, tmem + kTZK + 8 * s, b + (((s >> 2) * kHalf) >> 4) + (s & 3) * kCol16,
+                    mma_bf16_ta(d, tmem + kTZK + 8 * s, b + (((s >> 2) * kHalf) >> 4) + (s & 3) * kCol16,
                                 idO, s > 0 ? 1u : 0u);
             };
             auto issue_intra = [&](int c) {
                 const uint64_t b = dAq + (((c & 1) * kRec) >> 4);
+                const uint32_t d = tmem + kTO + 64 * (c & 1);
 #pragma unroll
-                for (int s = 0; s < 4; ++s) mma_bf16_ta(tmem + kTO, tmem + kTD + 8 * s, b + s * kCol16, idO, 1u);
+                for (int s = 0; s < 4; ++s) mma_bf16_ta(d, tmem + kTD + 8 * s, b + s * kCol16, idO, 1u);
             };
             bool ok = true;
             if (hf == 0) {
@@ -385,7 +391,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                     const bool more = c + 1 < nch;
                     if (!(ok = wait(&bars.wready[c & 1], (c >> 1) & 1) && wait(&bars.zready[0], c & 1))) break;
                     if (outm && !(ok = wait(&bars.qfull[c & 1], (c >> 1) & 1) &&
-                                       (c < 1 || wait(&bars.ofree, (c - 1) & 1))))
+                                       (c < 2 || wait(&bars.ofree[c & 1], ((c - 2) >> 1) & 1))))
                         break;
                     tc_fence_after();
                     if (outm) issue_qs(c);
@@ -407,7 +413,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                         issue_intra(c);
                         mma_commit(&bars.zfull[0]);
                         mma_commit(&bars.kempty[c % kKSlots]);
-                        mma_commit(&bars.ofull);
+                        mma_commit(&bars.ofull[c & 1]);
                     }
                     if (more) {
                         if (!(ok = wait(&bars.zfull[0], c & 1) && wait(&bars.m1ready[(c + 1) & 1], ((c + 1) >> 1) & 1)))
@@ -580,19 +586,19 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 fence_async_shared();
                 mbar_arrive(&bars.aqready[c & 1]);
             }
-            if (!wwait(&bars.ofull, c & 1)) break;
+            if (!wwait(&bars.ofull[c & 1], (c >> 1) & 1)) break;
             tc_fence_after();
             {
                 uint32_t z[64];
-                ld64(tmem + lane_off + kTO, z);
+                ld64(tmem + lane_off + kTO + 64 * (c & 1), z);
                 tmem_ld_wait();
                 // scaled with the chunk's gate slot before the accumulator is freed: freeing
-                // it lets the next chunks run on, and the slot is rewritten three chunks later
+                // it lets the next chunks run on, and the slot is rewritten four chunks later
                 const Slot &sl = slots[c % kSlots];
 #pragma unroll
                 for (int t = 0; t < C; ++t) z[t] = __float_as_uint(__fdividef(__uint_as_float(z[t]), sl.ex[t]));
                 tc_fence_before();
-                mbar_arrive(&bars.ofree);
+                mbar_arrive(&bars.ofree[c & 1]);
                 const int nv = min(C, seg.len - c * C);
                 const int64_t tok0 = (int64_t)seg.start + (int64_t)c * C;
 #pragma unroll

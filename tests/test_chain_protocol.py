@@ -41,7 +41,7 @@ def _run(nch, seed, mistake=None, out=False):
     the S-half issuer adds Q S~ before d_S and the intra-chunk product after f_S."""
     rnd = random.Random(seed)
     KS = VS = 3
-    SL = 3   # per-chunk gate slots
+    SL = 4 if out else 2   # per-chunk gate slots, as in the kernel
     B = {}
     for s in range(KS):
         B[f"kfull{s}"], B[f"kempty{s}"] = _Bar(), _Bar(2)
@@ -56,11 +56,13 @@ def _run(nch, seed, mistake=None, out=False):
     for s_ in range(2):
         B[f"qfull{s_}"], B[f"qempty{s_}"] = _Bar(), _Bar(2)   # qempty: Q S~ and Q K^T
         B[f"aqready{s_}"] = _Bar()
-    for n_ in ("aqfull", "aqfree", "ofull", "ofree"):
+    for n_ in ("aqfull", "aqfree"):
         B[n_] = _Bar()
+    for s_ in range(2):   # two output accumulators, by chunk parity
+        B[f"ofull{s_}"], B[f"ofree{s_}"] = _Bar(), _Bar()
     # buffer contents (versions)
     m = dict(ZK0=None, ZK1=None, D0=None, D1=None, Z0=("Z", -1), Z1=("Z", -1), k={}, vr={},
-             wop={}, m1={}, slot={}, w_read=set(), q={}, aq={}, AQ=None, O=None)
+             wop={}, m1={}, slot={}, w_read=set(), q={}, aq={}, AQ=None, O0=None, O1=None)
     queues = {0: [], 1: []}   # per issuer: pending MMAs and commits, in issue order
 
     def wait(name, phase):
@@ -117,8 +119,8 @@ def _run(nch, seed, mistake=None, out=False):
             yield from wait("zready0", c)
             if out:
                 yield from wait(f"qfull{c % 2}", c // 2)
-                if c >= 1 and mistake != "qs_without_ofree":
-                    yield from wait("ofree", c - 1)
+                if c >= 2 and mistake != "qs_without_ofree":
+                    yield from wait(f"ofree{c & 1}", (c - 2) >> 1)
                 issue(0, dict(kind="QS", c=c, q=c % 2))
             issue(0, dict(kind="dS", c=c, wop=c & 1))
             commit(0, "dfull0")
@@ -140,7 +142,7 @@ def _run(nch, seed, mistake=None, out=False):
             commit(0, "zfull0")
             commit(0, f"kempty{c % KS}")
             if out:
-                commit(0, "ofull")
+                commit(0, f"ofull{c & 1}")
             yield
             if more:
                 yield from wait("zfull0", c)
@@ -190,12 +192,13 @@ def _run(nch, seed, mistake=None, out=False):
             return {("vr", op["vr"]): c, ("m1", op["m1"]): c}, {"D0": ("U", c)}
         if kind == "dS":
             return {"ZK0": ("Z", c), ("wop", op["wop"]): c, "D0": ("U", c)}, {"D0": ("d", c)}
+        ob = 0 if mistake == "one_output_buffer" else c & 1
         if kind == "QS":
-            return {"ZK0": ("Z", c), ("q", op["q"]): c}, {"O": ("QS", c)}
+            return {"ZK0": ("Z", c), ("q", op["q"]): c}, {f"O{ob}": ("QS", c)}
         if kind == "QK":
             return {("q", op["q"]): c, ("k", op["k"]): c}, {"AQ": ("AQ", c)}
         if kind == "intra":
-            return {"D0": ("Dbf", c), ("aq", op["aq"]): c, "O": ("QS", c)}, {"O": ("O", c)}
+            return {"D0": ("Dbf", c), ("aq", op["aq"]): c, f"O{ob}": ("QS", c)}, {f"O{ob}": ("O", c)}
         if kind == "dP":
             return {"ZK1": ("Z", c), ("wop", op["wop"]): c}, {"D1": ("d", c)}
         hf = 0 if kind == "fS" else 1
@@ -334,23 +337,21 @@ def _run(nch, seed, mistake=None, out=False):
             m["aq"][c & 1] = c
             B[f"aqready{c & 1}"].arrive()
             yield
-            yield from wait("ofull", c)
-            if m["O"] != ("O", c):
-                raise Hazard(f"output read-out at chunk {c} finds {m['O']}")
-            touches_inflight(["O"], False, "output read-out")
-            # the outputs are scaled with the chunk's gate slot, read over some time; the
-            # accumulator is freed after that (freeing it first lets the slot be rewritten)
-            if mistake == "slot_read_after_ofree":
-                B["ofree"].arrive()
+            yield from wait(f"ofull{c & 1}", c >> 1)
+            ob = 0 if mistake == "one_output_buffer" else c & 1
+            if m[f"O{ob}"] != ("O", c):
+                raise Hazard(f"output read-out at chunk {c} finds {m[f'O{ob}']}")
+            touches_inflight([f"O{ob}"], False, "output read-out")
+            # the outputs are scaled with the chunk's gate slot, read over some time, and the
+            # accumulator freed after that
             for _ in range(2):
                 if m["slot"].get(c % SL) != c:
                     raise Hazard("output scale read from the gate slot of another chunk")
                 yield
-            if mistake != "slot_read_after_ofree":
-                B["ofree"].arrive()
+            B[f"ofree{c & 1}"].arrive()
 
-    if mistake == "two_gate_slots":
-        SL = 2
+    if mistake == "three_gate_slots":
+        SL = 3
     actors = {"tma": tma(), "s": issuer_s(), "p": issuer_p(), "pipe": pipe(), "op": operand(),
               "c0": conversion(0), "c1": outwarps() if out else conversion(1)}
     # per-run speeds: some runs starve one agent, so that the others run ahead as far as the
@@ -388,8 +389,8 @@ def test_outputs_instance_protocol_interleavings(nch):
         assert _run(nch, seed, out=True) == "ok"
 
 
-@pytest.mark.parametrize("mistake", ["q_without_qempty", "qs_without_ofree", "qk_without_aqfree",
-                                     "two_gate_slots", "slot_read_after_ofree"])
+@pytest.mark.parametrize("mistake", ["q_without_qempty", "one_output_buffer", "qk_without_aqfree",
+                                     "three_gate_slots"])
 def test_outputs_instance_model_catches_planted_mistakes(mistake):
     hits = 0
     for seed in range(80):
@@ -418,7 +419,7 @@ def test_chain_protocol_model_catches_planted_mistakes(mistake):
 
 
 # The kernel source this model was last checked against (code only; comments do not count).
-MODELLED_SOURCE = ("build_gdn_tc.cu", "3b73ecdc748b")
+MODELLED_SOURCE = ("build_gdn_tc.cu", "2e36fd3241ba")
 
 
 def test_model_is_checked_against_the_current_kernel_source():
