@@ -559,52 +559,56 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
         // Per chunk c: (a) the masked Q K^T (M = 64 accumulator: rows 16 (warp % 4) + lane in
         // lanes 0-15) -> bf16 rows t of the K-major B operand, columns s <= t; (b) the outputs,
         // o_t[n] = O^T[n][t] / ex_t with ex_t = exp(-Lam - c_t) from the chunk's gate slot.
+        // The masked Q K^T of chunk c + 1 is prepared before the outputs of chunk c are read
+        // out and stored, so that the S~ issuer's intra-chunk product of c + 1 does not wait
+        // for chunk c's stores.
         const int n = threadIdx.x & 127;   // state column = TMEM lane
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         __nv_bfloat16 *Ob = static_cast<__nv_bfloat16 *>(p.O);
-        for (int c = 0; c < nch; ++c) {
-            if (!wwait(&bars.aqfull, c & 1)) break;
+        auto prep_aq = [&](int c) -> bool {
+            if (!wwait(&bars.aqfull, c & 1)) return false;
             tc_fence_after();
-            {
-                uint32_t z[64];
-                ld64(tmem + lane_off + kTAq, z);
-                tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&bars.aqfree);
-                if (lane < 16) {
-                    const int t = 16 * (warp & 3) + lane;
-                    uint8_t *aq = smem + kOffAq + (c & 1) * kRec;
+            uint32_t z[64];
+            ld64(tmem + lane_off + kTAq, z);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&bars.aqfree);
+            if (lane < 16) {
+                const int t = 16 * (warp & 3) + lane;
+                uint8_t *aq = smem + kOffAq + (c & 1) * kRec;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float f[8];
+                for (int j = 0; j < 8; ++j) {
+                    float f[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] = (8 * j + e <= t) ? __uint_as_float(z[8 * j + e]) : 0.f;
-                        *reinterpret_cast<uint4 *>(aq + sw128((uint32_t)t, 16u * j)) =
-                            make_uint4(bf2(f[0], f[1]), bf2(f[2], f[3]), bf2(f[4], f[5]), bf2(f[6], f[7]));
-                    }
+                    for (int e = 0; e < 8; ++e) f[e] = (8 * j + e <= t) ? __uint_as_float(z[8 * j + e]) : 0.f;
+                    *reinterpret_cast<uint4 *>(aq + sw128((uint32_t)t, 16u * j)) =
+                        make_uint4(bf2(f[0], f[1]), bf2(f[2], f[3]), bf2(f[4], f[5]), bf2(f[6], f[7]));
                 }
-                fence_async_shared();
-                mbar_arrive(&bars.aqready[c & 1]);
             }
-            if (!wwait(&bars.ofull[c & 1], (c >> 1) & 1)) break;
+            fence_async_shared();
+            mbar_arrive(&bars.aqready[c & 1]);
+            return true;
+        };
+        bool ok = nch == 0 || prep_aq(0);
+        for (int c = 0; ok && c < nch; ++c) {
+            if (c + 1 < nch && !(ok = prep_aq(c + 1))) break;
+            if (!(ok = wwait(&bars.ofull[c & 1], (c >> 1) & 1))) break;
             tc_fence_after();
-            {
-                uint32_t z[64];
-                ld64(tmem + lane_off + kTO + 64 * (c & 1), z);
-                tmem_ld_wait();
-                // scaled with the chunk's gate slot before the accumulator is freed: freeing
-                // it lets the next chunks run on, and the slot is rewritten four chunks later
-                const Slot &sl = slots[c % kSlots];
+            uint32_t z[64];
+            ld64(tmem + lane_off + kTO + 64 * (c & 1), z);
+            tmem_ld_wait();
+            // scaled with the chunk's gate slot before the accumulator is freed: freeing it
+            // lets the next chunks run on, and the slot is rewritten four chunks later
+            const Slot &sl = slots[c % kSlots];
 #pragma unroll
-                for (int t = 0; t < C; ++t) z[t] = __float_as_uint(__fdividef(__uint_as_float(z[t]), sl.ex[t]));
-                tc_fence_before();
-                mbar_arrive(&bars.ofree[c & 1]);
-                const int nv = min(C, seg.len - c * C);
-                const int64_t tok0 = (int64_t)seg.start + (int64_t)c * C;
+            for (int t = 0; t < C; ++t) z[t] = __float_as_uint(__fdividef(__uint_as_float(z[t]), sl.ex[t]));
+            tc_fence_before();
+            mbar_arrive(&bars.ofree[c & 1]);
+            const int nv = min(C, seg.len - c * C);
+            const int64_t tok0 = (int64_t)seg.start + (int64_t)c * C;
 #pragma unroll
-                for (int t = 0; t < C; ++t)
-                    if (t < nv) Ob[((tok0 + t) * p.H_v + h) * D + n] = __float2bfloat16_rn(__uint_as_float(z[t]));
-            }
+            for (int t = 0; t < C; ++t)
+                if (t < nv) Ob[((tok0 + t) * p.H_v + h) * D + n] = __float2bfloat16_rn(__uint_as_float(z[t]));
         }
     } else {
         // ---------------------------------------------------------------- chain warps 0-7
