@@ -600,15 +600,30 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             // scaled with the chunk's gate slot before the accumulator is freed: freeing it
             // lets the next chunks run on, and the slot is rewritten four chunks later
             const Slot &sl = slots[c % kSlots];
+            {
+                const float4 *ex4 = reinterpret_cast<const float4 *>(sl.ex);
 #pragma unroll
-            for (int t = 0; t < C; ++t) z[t] = __float_as_uint(__fdividef(__uint_as_float(z[t]), sl.ex[t]));
+                for (int t4 = 0; t4 < C / 4; ++t4) {
+                    const float4 e = ex4[t4];
+                    z[4 * t4] = __float_as_uint(__fdividef(__uint_as_float(z[4 * t4]), e.x));
+                    z[4 * t4 + 1] = __float_as_uint(__fdividef(__uint_as_float(z[4 * t4 + 1]), e.y));
+                    z[4 * t4 + 2] = __float_as_uint(__fdividef(__uint_as_float(z[4 * t4 + 2]), e.z));
+                    z[4 * t4 + 3] = __float_as_uint(__fdividef(__uint_as_float(z[4 * t4 + 3]), e.w));
+                }
+            }
             tc_fence_before();
             mbar_arrive(&bars.ofree[c & 1]);
             const int nv = min(C, seg.len - c * C);
             const int64_t tok0 = (int64_t)seg.start + (int64_t)c * C;
+            {
+                __nv_bfloat16 *op = Ob + ((tok0 * p.H_v + h) * D + n);
+                const int64_t st = (int64_t)p.H_v * D;
 #pragma unroll
-            for (int t = 0; t < C; ++t)
-                if (t < nv) Ob[((tok0 + t) * p.H_v + h) * D + n] = __float2bfloat16_rn(__uint_as_float(z[t]));
+                for (int t = 0; t < C; ++t) {
+                    if (t < nv) *op = __float2bfloat16_rn(__uint_as_float(z[t]));
+                    op += st;
+                }
+            }
         }
     } else {
         // ---------------------------------------------------------------- chain warps 0-7

@@ -426,7 +426,7 @@ def test_chain_protocol_model_catches_planted_mistakes(mistake):
 
 
 # The kernel source this model was last checked against (code only; comments do not count).
-MODELLED_SOURCE = ("build_gdn_tc.cu", "7bee20911041")
+MODELLED_SOURCE = ("build_gdn_tc.cu", "b89dd608e6c9")
 
 
 def test_model_is_checked_against_the_current_kernel_source():
