@@ -245,7 +245,10 @@ hypic_status hypic_build_segments(const hypic_build_args *args, void *stream);
 hypic_status hypic_build_segments_static_ws(const hypic_build_args *args, void *stream);
 
 /* Inclusive prefix scan of the composition over n_seg segments for n_units units, and
- * optionally the transition of all of them composed (lam_total, P_total). */
+ * optionally the transition of all of them composed (lam_total, P_total). Units are scanned
+ * side by side; the dense d = 128 scan without totals of at most (SMs / 4) units splits each
+ * unit's state columns over four CTAs (columns compose independently), every other dense
+ * d = 128 call takes one CTA per unit. */
 hypic_status hypic_compose_scan(const hypic_compose_args *args, void *stream);
 
 /* Device scratch bytes hypic_build_segments needs for these arguments (host-only query;
@@ -254,8 +257,9 @@ hypic_status hypic_compose_scan(const hypic_compose_args *args, void *stream);
 size_t hypic_build_workspace_bytes(const hypic_build_args *args);
 
 /* Name of the kernel hypic_build_segments / hypic_compose_scan would launch for these
- * arguments (host-only query, no device access; "none" for an empty request, NULL for
- * arguments the call would reject on shape or family). Static strings. */
+ * arguments (host-only query: reads the shapes and, for a dense compose, the current
+ * device's SM count; touches no tensor; "none" for an empty request, NULL for arguments the
+ * call would reject on shape or family). Static strings. */
 const char *hypic_build_kernel_name(const hypic_build_args *args);
 const char *hypic_compose_kernel_name(const hypic_compose_args *args);
 

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhypic.so")
-SOURCES = ["api.cu", "build_simt.cu", "compose.cu", "compose_tc.cu", "build_gated_tc.cu", "build_gdn_prep.cu",
+SOURCES = ["api.cu", "build_simt.cu", "compose.cu", "compose_tc.cu", "compose_cols.cu", "build_gated_tc.cu", "build_gdn_prep.cu",
            "build_gdn_tc.cu", "build_gdn_tc_out.cu"]
 HEADERS = [os.path.join(ROOT, "include", "hypic.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -117,7 +117,7 @@ hypic_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HYPIC_OK : HYP
 enum class BuildPath { None, GatedSimt, GatedTc, Seq, GdnTc };
 
 bool dense_family(int fam) { return fam == HYPIC_FAM_DELTA || fam == HYPIC_FAM_GDN || fam == HYPIC_FAM_KDA; }
-enum class ComposePath { None, Scaled, DenseSimt, DenseTc };
+enum class ComposePath { None, Scaled, DenseSimt, DenseTc, DenseCols };
 
 // Kernel selection for a build (shape/family/dtype only; no pointer checks).
 BuildPath pick_build(const hypic_build_args *a) {
@@ -143,6 +143,10 @@ ComposePath pick_compose(const hypic_compose_args *a) {
     q.D = a->d_k;
     q.n_seg = a->n_seg;
     q.n_units = a->n_units;
+    q.lam_total = a->lam_total;
+    q.P_total = a->P_total;
+    // a plain scan of few units: four CTAs per unit, each carrying a block of state columns
+    if (compose_dense_cols_supported(q)) return ComposePath::DenseCols;
     return compose_dense_tc_supported(q) ? ComposePath::DenseTc : ComposePath::DenseSimt;
 }
 
@@ -608,6 +612,7 @@ hypic_status hypic_compose_scan(const hypic_compose_args *a, void *stream) {
     cudaError_t e = cudaSuccess;
     switch (pick_compose(a)) {
     case ComposePath::DenseTc: e = launch_compose_dense_tc(p, s); break;
+    case ComposePath::DenseCols: e = launch_compose_dense_cols(p, s); break;
     case ComposePath::DenseSimt: e = launch_compose_dense_simt(p, s); break;
     case ComposePath::Scaled: e = launch_compose_scaled(p, s); break;
     case ComposePath::None: break;
@@ -644,6 +649,7 @@ const char *hypic_compose_kernel_name(const hypic_compose_args *a) {
     if (!compose_shape_ok(a)) return nullptr;
     switch (pick_compose(a)) {
     case ComposePath::DenseTc: return "compose_dense_tc";
+    case ComposePath::DenseCols: return "compose_dense_cols";
     case ComposePath::DenseSimt: return "compose_dense_simt";
     case ComposePath::Scaled: return "compose_scaled";
     case ComposePath::None: break;

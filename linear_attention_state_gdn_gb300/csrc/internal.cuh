@@ -89,6 +89,8 @@ cudaError_t launch_compose_lam_total(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_dense_simt(const ComposeParams &p, cudaStream_t s);
 cudaError_t launch_compose_dense_tc(const ComposeParams &p, cudaStream_t s);
 bool compose_dense_tc_supported(const ComposeParams &p);
+cudaError_t launch_compose_dense_cols(const ComposeParams &p, cudaStream_t s);
+bool compose_dense_cols_supported(const ComposeParams &p);
 cudaError_t launch_build_gated_tc(const BuildParams &p, cudaStream_t s);
 bool build_gated_tc_supported(const BuildParams &p);
 cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s);

@@ -184,6 +184,25 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, uint64_
         : "memory");
 }
 
+// 2D tiled tensor store from shared memory, tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, const void *src, int32_t c0, int32_t c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(tmap), "r"(smem_u32(src)), "r"(c0), "r"(c1)
+                 : "memory");
+}
+
+// Close the thread's current bulk group; wait until at most N of its groups are still
+// reading shared memory (_read) or still in flight at all.
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -164,6 +164,28 @@ def test_compose_parity(family, d, with_S0):
     assert_close(f64(pref) - f64(c.S), ref - f64(c.S), COMPOSE_TOL, "carried term")
 
 
+@pytest.mark.parametrize("which", ["two", "most", "over"])
+@pytest.mark.parametrize("with_S0", [False, True])
+def test_compose_few_units_column_blocks(which, with_S0):
+    """A plain d = 128 scan of few units runs four CTAs per unit, each carrying 32 state
+    columns, while all of them fit on the SMs at once; one unit more and the one-CTA-per-unit
+    kernel takes over. 16 segments, prefix and carried term at the compose bound."""
+    hy = _hy()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    units = {"two": 2, "most": sms // 4, "over": sms // 4 + 1}[which]
+    c = synth.make_compose_inputs("gdn", 16, units, 128, seed=55 + units, with_S0=with_S0)
+    dev = lambda t: None if t is None else t.cuda()
+    expect = "compose_dense_tc" if which == "over" else "compose_dense_cols"
+    assert hy.hypic_compose_kernel_name("gdn", dev(c.S), dev(c.lam), dev(c.P), dev(c.S0)) == expect
+    pref = hy.hypic_compose_scan("gdn", dev(c.S), dev(c.lam), dev(c.P), dev(c.S0))
+    torch.cuda.synchronize()
+    assert hy.hypic_get_device_status() == 0
+    T = oracle.materialize_T("gdn", f64(c.lam), f64(c.P))
+    ref = oracle.compose_scan(T, f64(c.S), f64(c.S0))
+    assert_close(f64(pref), ref, COMPOSE_TOL, "prefix")
+    assert_close(f64(pref) - f64(c.S), ref - f64(c.S), COMPOSE_TOL, "carried term")
+
+
 def test_compose_single_segment_is_S_plus_carry():
     hy = _hy()
     c = synth.make_compose_inputs("gdn", 1, 3, 128, seed=51)
@@ -410,12 +432,13 @@ def test_build_kernel_selection(family, dtype, d, expect):
     assert name == expect
 
 
-@pytest.mark.parametrize("family,d,expect", [("gdn", 128, "compose_dense_tc"),
-                                             ("delta", 64, "compose_dense_simt"),
-                                             ("diag", 128, "compose_scaled")])
-def test_compose_kernel_selection(family, d, expect):
+@pytest.mark.parametrize("family,d,units,expect", [("gdn", 128, 2, "compose_dense_cols"),
+                                                   ("gdn", 128, 200, "compose_dense_tc"),
+                                                   ("delta", 64, 2, "compose_dense_simt"),
+                                                   ("diag", 128, 2, "compose_scaled")])
+def test_compose_kernel_selection(family, d, units, expect):
     hy = _hy()
-    c = synth.make_compose_inputs(family, 2, 2, d, seed=91)
+    c = synth.make_compose_inputs(family, 2, units, d, seed=91)
     assert hy.hypic_compose_kernel_name(family, c.S) == expect
 
 
