@@ -164,16 +164,18 @@ def test_compose_parity(family, d, with_S0):
     assert_close(f64(pref) - f64(c.S), ref - f64(c.S), COMPOSE_TOL, "carried term")
 
 
-@pytest.mark.parametrize("which", ["two", "most", "over"])
+@pytest.mark.parametrize("which,n_seg", [("two", 16), ("most", 16), ("over", 16), ("two", 1),
+                                          ("two", 64), ("most", 3)])
 @pytest.mark.parametrize("with_S0", [False, True])
-def test_compose_few_units_column_blocks(which, with_S0):
+def test_compose_few_units_column_blocks(which, n_seg, with_S0):
     """A plain d = 128 scan of few units runs four CTAs per unit, each carrying 32 state
     columns, while all of them fit on the SMs at once; one unit more and the one-CTA-per-unit
-    kernel takes over. 16 segments, prefix and carried term at the compose bound."""
+    kernel takes over. One to 64 segments (more steps than the kernel's rings have slots),
+    prefix and carried term at the compose bound."""
     hy = _hy()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     units = {"two": 2, "most": sms // 4, "over": sms // 4 + 1}[which]
-    c = synth.make_compose_inputs("gdn", 16, units, 128, seed=55 + units, with_S0=with_S0)
+    c = synth.make_compose_inputs("gdn", n_seg, units, 128, seed=55 + units + n_seg, with_S0=with_S0)
     dev = lambda t: None if t is None else t.cuda()
     expect = "compose_dense_tc" if which == "over" else "compose_dense_cols"
     assert hy.hypic_compose_kernel_name("gdn", dev(c.S), dev(c.lam), dev(c.P), dev(c.S0)) == expect
