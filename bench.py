@@ -8,7 +8,7 @@ tokens (bf16 k L2-normalised, bf16 v, fp32 gates and beta), built into all 512
 second launch. `value` is build+compose tokens/s of that step with the inputs resident in
 device memory; `e2e` is the same metric through the public API with the inputs copied in
 from pinned host memory and every output copied back, inside the timed region (the segments
-in four groups, so that each group's copies overlap the previous group's build).
+in eight groups, so that each group's copies overlap the previous group's build and compose).
 
 The other workloads (RetNet scalar build + compose, GLA diagonal build + compose, the same
 GDN prompt cached as one 32768-token segment, the RetNet prompt as one 16384-token segment,
@@ -647,13 +647,15 @@ def workload_config():
 
 # ----------------------------------------------------------------------------- main arm
 
-def e2e_measure(inp, steps=5, warmup=2, groups=4):
+def e2e_measure(inp, steps=5, warmup=2, groups=8):
     """Through the public API from pinned host buffers, inside the events: H2D of k, v, log a,
     beta; build; compose; D2H of S, lam, P and the prefix states. The prompt's segments go in
     `groups` consecutive groups so that transfers overlap compute: group g's inputs copy in on
-    one stream while group g - 1 builds, and each group's S, lam, P copy out on a third stream
-    as soon as it is built (each unit's result does not depend on the grouping). The compose
-    over all segments follows the last build; its prefix states copy out last."""
+    one stream while group g - 1 builds; each group is composed as soon as it is built,
+    starting from the last prefix state of the group before (the scan's own recurrence, so the
+    prefix states are the ones one scan over all segments gives); and each group's S, lam, P
+    and prefix states copy out on a third stream (each unit's result does not depend on the
+    grouping)."""
     import linear_attention_state_gdn_gb300 as hy
     host = {n: t.pin_memory() for n, t in inp.tensors().items()}
     dev = {n: torch.empty_like(t, device="cuda") for n, t in host.items()}
@@ -692,19 +694,16 @@ def e2e_measure(inp, steps=5, warmup=2, groups=4):
                                     log_gate=d.get("log_gate"), log_gamma=dev.get("log_gamma"),
                                     beta=d.get("beta"), S=S[s0:s1], lam=lam[s0:s1], P=P[s0:s1],
                                     workspace=workspace)
+            hy.hypic_compose_scan(inp.family, S[s0:s1], lam[s0:s1], None if P is None else P[s0:s1],
+                                  S0=prefix[s0 - 1] if s0 > 0 else None, prefix=prefix[s0:s1])
             built = torch.cuda.Event()
             built.record(comp)
             cout.wait_event(built)
             with torch.cuda.stream(cout):
-                for h, t in zip(host_out[:3], outs[:3]):
+                for h, t in zip(host_out, outs):
                     if t is not None:
                         h[s0:s1].copy_(t[s0:s1], non_blocking=True)
-        hy.hypic_compose_scan(inp.family, S, lam, P, prefix=prefix)
-        composed = torch.cuda.Event()
-        composed.record(comp)
-        cout.wait_event(composed)
         with torch.cuda.stream(cout):
-            host_out[3].copy_(prefix, non_blocking=True)
             done = torch.cuda.Event()
             done.record(cout)
         comp.wait_event(done)
