@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhypic.so")
 SOURCES = ["api.cu", "build_simt.cu", "compose.cu", "compose_tc.cu", "compose_cols.cu", "build_gated_tc.cu", "build_gdn_prep.cu",
-           "build_gdn_tc.cu", "build_gdn_tc_out.cu"]
+           "build_gdn_tc.cu", "build_gdn_tc_out.cu", "build_gdn_tc_kda.cu"]
 HEADERS = [os.path.join(ROOT, "include", "hypic.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -27,9 +27,9 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
 # Translation units compiled as relocatable device code (-rdc=true) and device-linked into
 # the library. Chosen by measurement on GB300: the GDN chain kernel runs 10% faster compiled
 # this way; the gated build runs 30% slower, and the other units are unaffected.
-RDC_SOURCES = {"build_gdn_tc.cu", "build_gdn_tc_out.cu"}
+RDC_SOURCES = {"build_gdn_tc.cu", "build_gdn_tc_out.cu", "build_gdn_tc_kda.cu"}
 # translation units that include another .cu file (rebuilt when it changes)
-CU_DEPS = {"build_gdn_tc_out.cu": ["build_gdn_tc.cu"]}
+CU_DEPS = {"build_gdn_tc_out.cu": ["build_gdn_tc.cu"], "build_gdn_tc_kda.cu": ["build_gdn_tc.cu"]}
 
 
 def _flags(src: str):

@@ -122,11 +122,11 @@ enum class ComposePath { None, Scaled, DenseSimt, DenseTc, DenseCols };
 // Kernel selection for a build (shape/family/dtype only; no pointer checks).
 BuildPath pick_build(const hypic_build_args *a) {
     if (a->n_seg == 0) return BuildPath::None;
-    // start states and the channel-gated delta rule: the exact path; the segment outputs too,
-    // except on the tensor-core DeltaNet / GDN build, whose outputs instance computes them
-    if (a->S_init || a->family == HYPIC_FAM_KDA) return BuildPath::Seq;
-    const bool delta = a->family == HYPIC_FAM_DELTA || a->family == HYPIC_FAM_GDN;
-    if (a->O && !delta) return BuildPath::Seq;
+    // start states: the exact path; the segment outputs too, except on the tensor-core
+    // DeltaNet / GDN build, whose outputs instance computes them
+    if (a->S_init) return BuildPath::Seq;
+    const bool delta = dense_family(a->family);
+    if (a->O && (!delta || a->family == HYPIC_FAM_KDA)) return BuildPath::Seq;
     BuildParams q{};
     q.family = a->family;
     q.dtype = a->dtype;
@@ -150,8 +150,8 @@ ComposePath pick_compose(const hypic_compose_args *a) {
     return compose_dense_tc_supported(q) ? ComposePath::DenseTc : ComposePath::DenseSimt;
 }
 
-// Workspace records of the GDN / DeltaNet tensor-core build: one per (segment, value head,
-// 64-token chunk). Negative segment lengths count as empty (they are rejected elsewhere).
+// Workspace records of the GDN / DeltaNet / KDA tensor-core build: one per (segment, value
+// head, 64-token chunk). Negative segment lengths count as empty (they are rejected elsewhere).
 int64_t gdn_records(const hypic_build_args *a) {
     int64_t records = 0;
     for (int j = 0; j < a->n_seg; ++j) {
@@ -159,6 +159,14 @@ int64_t gdn_records(const hypic_build_args *a) {
         if (len > 0) records += (int64_t)a->H_v * ((len + kGdnChunk - 1) / kGdnChunk);
     }
     return records;
+}
+
+// Bytes of the records: M2 per record, the tail (ticket counter), and for KDA the gated keys
+// and log-decays (kKdaExtraBytes per record) after the tail.
+size_t gdn_records_bytes(const hypic_build_args *a) {
+    const size_t r = (size_t)gdn_records(a);
+    return r * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail +
+           (a->family == HYPIC_FAM_KDA ? r * (size_t)kKdaExtraBytes : 0);
 }
 
 // Intra-segment split of the tensor-core builds (DeltaNet / GDN, and the linear / scalar /
@@ -212,7 +220,7 @@ struct SplitLayout {
 
 // the trailing segments to halve, or 0 (see above)
 int gdn_tail_split(const hypic_build_args *a, int *first) {
-    if (a->family != HYPIC_FAM_DELTA && a->family != HYPIC_FAM_GDN) return 0;
+    if (!dense_family(a->family)) return 0;
     if (a->O) return 0;
     if (a->out_seg_stride != 0 && a->out_seg_stride != a->H_v) return 0;
     const int64_t units = (int64_t)a->n_seg * a->H_v;
@@ -265,7 +273,7 @@ SplitLayout gdn_split_layout(const hypic_build_args *a, size_t base) {
     }
     const size_t unit = (size_t)a->d_k * a->d_k * sizeof(float);
     const size_t su = (size_t)L.slots * a->H_v;
-    const bool dense = a->family == HYPIC_FAM_DELTA || a->family == HYPIC_FAM_GDN;
+    const bool dense = dense_family(a->family);
     const size_t nl = a->family == HYPIC_FAM_DIAG ? (size_t)a->d_k : 1;
     L.off_S = base;
     L.off_P = L.off_S + su * unit;
@@ -313,9 +321,8 @@ size_t hypic_build_workspace_bytes(const hypic_build_args *a) {
     const BuildPath path = pick_build(a);
     if (path == BuildPath::GatedTc) return gdn_split_layout(a, 0).bytes;   // 0 without a split
     if (path != BuildPath::GdnTc) return 0;
-    const int64_t records = gdn_records(a);
-    if (records == 0) return 0;
-    const size_t base = (size_t)records * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail;
+    if (gdn_records(a) == 0) return 0;
+    const size_t base = gdn_records_bytes(a);
     return base + gdn_split_layout(a, base).bytes;
 }
 
@@ -424,9 +431,14 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
     // a segment with n chunks in pj pieces covers chunks [k n / pj, (k + 1) n / pj))
     SplitLayout split;
     if (path == BuildPath::GdnTc || path == BuildPath::GatedTc) {
-        const size_t base = path == BuildPath::GdnTc
-                                ? (size_t)gdn_records(a) * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail
-                                : 0;
+        const size_t base = path == BuildPath::GdnTc ? gdn_records_bytes(a) : 0;
+        if (path == BuildPath::GdnTc && fam == HYPIC_FAM_KDA) {
+            const size_t r = (size_t)gdn_records(a);
+            uint8_t *x = static_cast<uint8_t *>(a->workspace) + r * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail;
+            p.kda_kt = x;
+            p.kda_kb = x + r * (size_t)kKdaTileBytes;
+            p.kda_side = reinterpret_cast<float *>(x + 2 * r * (size_t)kKdaTileBytes);
+        }
         split = gdn_split_layout(a, base);
         if (split.slots > 0) {
             uint8_t *ws = static_cast<uint8_t *>(a->workspace);
@@ -636,7 +648,7 @@ hypic_status hypic_probe_wait_timeout(uint32_t limit_us, void *stream) {
 const char *hypic_build_kernel_name(const hypic_build_args *a) {
     if (!build_shape_ok(a)) return nullptr;
     switch (pick_build(a)) {
-    case BuildPath::GdnTc: return "build_gdn_tc";
+    case BuildPath::GdnTc: return a->family == HYPIC_FAM_KDA ? "build_kda_tc" : "build_gdn_tc";
     case BuildPath::Seq: return "build_seq";
     case BuildPath::GatedTc: return "build_gated_tc";
     case BuildPath::GatedSimt: return "build_gated_simt";

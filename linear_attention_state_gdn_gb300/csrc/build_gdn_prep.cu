@@ -403,6 +403,260 @@ cudaError_t launch_prep(const BuildParams &p, int64_t total, const CUtensorMap &
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------------------------ KDA
+// The channel-gated delta rule: S_t = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} + b_t k_t v_t^T with
+// one decay per key channel, a_t in (0, 1]^{d_k} (KDA is among the linear layers "Cut First-Token
+// Latency by 3.25x ..." (besthub.dev), paragraph "For linear layers", names). Inside a chunk let
+// c_t = sum_{s<=t} log a_s per channel (valid tokens only) and, elementwise,
+//     kt_t = e^{c_t} k_t,   kh_s = e^{-c_s} k_s,   kb_s = e^{c_C - c_s} k_s.
+// The chunk's delta values Delta (S_t = Diag(e^{c_t})(S0 + sum_{s<=t} kh_s Delta_s^T)) solve
+// (I + A) Delta = Diag(b)(V - Kt S0) with A_ts = b_t (kt_t . kh_s) for s < t, and the state after
+// the chunk is Diag(e^{c_C}) S0 + Kb^T Delta. The gates do not factor out of A here (they differ
+// per channel), so the inverse is taken of the gated gram: M2 = (I + Diag(b) L)^-1 Diag(b) with
+// L the strictly lower part of Kt Kh^T, by the same blocked algorithm as above. One record per
+// (segment, value head, chunk): M2 (bf16 8 KB), Kt and Kb (bf16 64 x 128, written by bulk
+// tensor stores), c_C (128 fp32) and m = max_i c_C[i]. |c_t| <= |c_C| <= 60 keeps e^{-c_t}
+// within the range of bf16; a chunk below that sets the range status.
+constexpr float kKdaMinChunkLogDecay = -60.f;
+
+struct KdaGeo {
+    static constexpr uint32_t kOffK = 0;                  // k tile, then Kt in place, 16 KB
+    static constexpr uint32_t kOffH = 16384;              // Kh (B operand of the gram)
+    static constexpr uint32_t kOffB = 32768;              // Kb
+    static constexpr uint32_t kOffG32 = 49152;            // the gram, 10 blocks
+    static constexpr uint32_t kOffN32 = kOffG32 + kTri * 4;
+    static constexpr uint32_t kOffT = kOffN32 + kTri * 4;
+    static constexpr uint32_t kSmemBytes = kOffT + 4 * 16 * kLDT * 4 + 1024;
+    static constexpr int kCtasPerSm = 3;
+};
+
+__global__ void __launch_bounds__(kThreads, KdaGeo::kCtasPerSm)
+build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmKb) {
+    using G = KdaGeo;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    __shared__ uint64_t kfull, gfull;
+    __shared__ uint32_t tslot;
+    __shared__ Walk s_n2[2];
+    __shared__ float s_max[4];
+    __shared__ __align__(16) float vb[kVb];
+
+    const int64_t total = total_records(p);
+    unsigned *tickets = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(p.workspace) + total * kGdnRecordBytes);
+    Walk cur = decode<1>(p, blockIdx.x, total);
+    if (cur.r >= p.n_seg) return;   // uniform: the whole CTA leaves before any set-up
+    const int q = threadIdx.x, warp = q >> 5, lane = q & 31;
+    uint8_t *tK = smem + G::kOffK, *tH = smem + G::kOffH, *tB = smem + G::kOffB;
+    float *G32 = reinterpret_cast<float *>(smem + G::kOffG32);
+    float *N32 = reinterpret_cast<float *>(smem + G::kOffN32);
+    float *Tw = reinterpret_cast<float *>(smem + G::kOffT) + warp * 16 * kLDT;
+
+    if (q == 0) {
+        mbar_init(&kfull, 1);
+        mbar_init(&gfull, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&tslot, 64);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tslot;
+    constexpr uint32_t idG = idesc(kFmtBF16, kFmtBF16, false, false, 64, 64);
+    int kiss = 0, giss = 0, kwait = 0, gwait = 0;   // issued by thread kCtl; waited by every thread
+    bool stored = false;                             // thread kCtl: a group of record stores issued
+    auto load_k = [&](const Walk &w) {   // thread kCtl
+        ++kiss;
+        const int32_t t0 = p.seg[w.r].start + w.c * C;
+        mbar_arrive_expect_tx(&kfull, 16384);
+        tma_load_3d(tK, &tmK, &kfull, 0, w.h / p.gqa, t0);
+        tma_load_3d(tK + 8192, &tmK, &kfull, 64, w.h / p.gqa, t0);
+    };
+    bool ok = true;
+    int64_t ticket = 0;   // thread kCtl
+    Walk nxt = decode<1>(p, (int64_t)gridDim.x + blockIdx.x, total);
+    if (q == kCtl) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmKt);
+        prefetch_tmap(&tmKb);
+        load_k(cur);
+    }
+    // element (t, channel q) of a 64 x 128 bf16 tile held as two 128B-swizzled 64-channel halves
+    const uint32_t hoff = (uint32_t)(q >> 6) * 8192u, qb = 2u * (uint32_t)(q & 63);
+    for (int i = 0; cur.r < p.n_seg; ++i) {
+        const SegEntry seg = p.seg[cur.r];
+        const int nch = (seg.len + C - 1) / C;
+        const int nv = min(C, seg.len - cur.c * C);
+        const int64_t tok0 = (int64_t)seg.start + (int64_t)cur.c * C;
+        const int64_t rec = (int64_t)seg.wsb + (int64_t)cur.h * nch + cur.c;
+        // (1) the log-gates of channel q over the chunk's valid tokens, and b
+        float g[C];
+        {
+            const float *gp = p.log_gate + (tok0 * p.H_v + cur.h) * D + q;
+            const int64_t gs = (int64_t)p.H_v * D;
+#pragma unroll
+            for (int t = 0; t < C; ++t) g[t] = t < nv ? __ldg(gp + t * gs) : 0.f;
+        }
+        if (q < C) vb[vbi(q)] = q < nv ? p.beta[(tok0 + q) * p.H_v + cur.h] : 0.f;
+        if (q == kCtl && nxt.r < p.n_seg) ticket = 2 * (int64_t)gridDim.x + atomicAdd(tickets, 1u);
+        ok = ok && mbar_wait(&kfull, kwait & 1, p.err, kErrTimeout);
+        ++kwait;
+        if (!__syncthreads_and(ok)) break;   // uniform
+        // (2) channel q of Kt (over k), Kh and Kb, token by token
+        float cC = 0.f;
+#pragma unroll
+        for (int t = 0; t < C; ++t) cC += g[t];
+        {
+            float c = 0.f;
+#pragma unroll
+            for (int t = 0; t < C; ++t) {
+                c += g[t];
+                const uint32_t off = hoff + sw128((uint32_t)t, qb);
+                const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tK + off));
+                *reinterpret_cast<__nv_bfloat16 *>(tK + off) = __float2bfloat16_rn(kv * expf(c));
+                *reinterpret_cast<__nv_bfloat16 *>(tH + off) = __float2bfloat16_rn(kv * expf(-c));
+                *reinterpret_cast<__nv_bfloat16 *>(tB + off) = __float2bfloat16_rn(kv * expf(cC - c));
+            }
+        }
+        if (cC < kKdaMinChunkLogDecay) atomicOr(p.err, kErrRange);
+        float mx = cC;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) s_max[warp] = mx;
+        fence_async_shared();   // Kt, Kh and Kb are read by the tensor core and the bulk stores
+        __syncthreads();
+        if (q == kCtl) {
+            tc_fence_after();
+            // the gram Kt Kh^T (M = 64) into TMEM; the read-out below waits for it
+            const uint32_t a0 = smem_u32(tK), b0 = smem_u32(tH);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t o = (s >> 2) * 8192 + (s & 3) * 32;
+                mma_bf16(tmem, sdesc(a0 + o, 16, 1024, kSwizzle128B), sdesc(b0 + o, 16, 1024, kSwizzle128B), idG,
+                         s > 0);
+            }
+            mma_commit(&gfull);
+            ++giss;
+            // Kt and Kb to their records (64 rows each, two 64-channel boxes)
+            const int32_t row = (int32_t)(rec * C);
+            tma_store_2d(&tmKt, tK, 0, row);
+            tma_store_2d(&tmKt, tK + 8192, 64, row);
+            tma_store_2d(&tmKb, tB, 0, row);
+            tma_store_2d(&tmKb, tB + 8192, 64, row);
+            bulk_commit();
+            stored = true;
+        }
+        {
+            const float m = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
+            float *side = p.kda_side + rec * kKdaSide;
+            side[q] = cC;
+            if (q == 0) side[128] = m;
+        }
+        ok = ok && mbar_wait(&gfull, gwait & 1, p.err, kErrTimeout);
+        ++gwait;
+        if (!__syncthreads_and(ok)) break;   // uniform
+        tc_fence_after();
+        {   // gram rows into G32 (as in the GDN preparation, one TMEM buffer)
+            const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
+            const int r = lane & 15;
+#pragma unroll
+            for (int hc = 0; hc < 2; ++hc) {
+                if (hc == 1 && warp < 2) break;   // uniform
+                uint32_t gr[32];
+                tmem_ld32(taddr + 32 * hc, gr);
+                tmem_ld_wait();
+                if (lane < 16) {
+#pragma unroll
+                    for (int s4 = 0; s4 < 8; ++s4) {
+                        const int k = 2 * hc + (s4 >> 2), cb = 4 * (s4 & 3);
+                        if (k > warp) break;   // uniform
+                        float4 g4 = make_float4(__uint_as_float(gr[4 * s4]), __uint_as_float(gr[4 * s4 + 1]),
+                                                __uint_as_float(gr[4 * s4 + 2]), __uint_as_float(gr[4 * s4 + 3]));
+                        if (k < warp) g4 = make_float4(tf32r(g4.x), tf32r(g4.y), tf32r(g4.z), tf32r(g4.w));
+                        *reinterpret_cast<float4 *>(G32 + blk(warp, k) + 16 * r + (cb ^ sw(r))) = g4;
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+        // the next k tile: the gram has read the tile, and the stores must have read Kt and Kb
+        // (the next tile lands over Kt; Kb is rewritten after that tile has landed)
+        if (q == kCtl && nxt.r < p.n_seg) {
+            bulk_wait_read<0>();
+            load_k(nxt);
+        }
+        // diagonal blocks by forward substitution, lane j < 16 of warp a: column j of block a
+        if (lane < 16) {
+            const int a = warp, j = lane;
+            const float *Gd = G32 + blk(a, a);
+            float *Nd = N32 + blk(a, a);
+            float x[16];
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) {
+                float gr[16];
+#pragma unroll
+                for (int s4 = 0; s4 < 4; ++s4) {
+                    const float4 t4 = *reinterpret_cast<const float4 *>(Gd + 16 * rr + ((4 * s4) ^ sw(rr)));
+                    gr[4 * s4] = t4.x, gr[4 * s4 + 1] = t4.y, gr[4 * s4 + 2] = t4.z, gr[4 * s4 + 3] = t4.w;
+                }
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int s = 0; s < rr; ++s) acc[s & 3] = fmaf(gr[s], x[s], acc[s & 3]);
+                x[rr] = fmaf(-vb[vbi(16 * a + rr)], (acc[0] + acc[1]) + (acc[2] + acc[3]), (rr == j) ? 1.f : 0.f);
+            }
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) Nd[16 * rr + (j ^ sw(rr))] = tf32r(x[rr]);
+        }
+        __syncthreads();
+        half_block(G32, N32, Tw, vb, 1 + (warp >> 1), warp >> 1, warp & 1, lane);
+        if (warp >= 2) half_block(G32, N32, Tw, vb, 3, 2, warp & 1, lane);
+        __syncthreads();
+        half_block(G32, N32, Tw, vb, 2 + (warp >> 1), warp >> 1, warp & 1, lane);
+        __syncthreads();
+        if (warp < 2) half_block(G32, N32, Tw, vb, 3, 0, warp, lane);
+        if (q == kCtl) s_n2[i & 1] = nxt.r < p.n_seg ? decode<1>(p, ticket, total) : nxt;
+        __syncthreads();
+        const Walk n2 = s_n2[i & 1];
+        if (n2.r >= p.n_seg) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        // the record: N Diag(b) as bf16 rows t' (blocks above the diagonal are zero)
+        uint8_t *dst = static_cast<uint8_t *>(p.workspace) + rec * kGdnRecordBytes;
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) {
+            const int e8 = q + 128 * mm;
+            const int tp = e8 >> 3, s8 = (e8 & 7) * 8;
+            const int ba = tp >> 4, bb = s8 >> 4, r = tp & 15;
+            uint4 pk = make_uint4(0u, 0u, 0u, 0u);
+            if (bb <= ba) {
+                const int h0 = 4 * ((bb & 1) ^ ((sw(r) >> 2) & 1)), h1 = h0 ^ 4;
+                const float *src = N32 + blk(ba, bb) + 16 * r;
+                const float4 x0 = *reinterpret_cast<const float4 *>(src + (((s8 & 15) + h0) ^ sw(r)));
+                const float4 x1 = *reinterpret_cast<const float4 *>(src + (((s8 & 15) + h1) ^ sw(r)));
+                const float4 b0 = *reinterpret_cast<const float4 *>(vb + vbi(s8 + h0));
+                const float4 b1 = *reinterpret_cast<const float4 *>(vb + vbi(s8 + h1));
+                const uint32_t p0 = pack_bf16x2(x0.x * b0.x, x0.y * b0.y), p1 = pack_bf16x2(x0.z * b0.z, x0.w * b0.w);
+                const uint32_t p2 = pack_bf16x2(x1.x * b1.x, x1.y * b1.y), p3 = pack_bf16x2(x1.z * b1.z, x1.w * b1.w);
+                pk = h0 == 0 ? make_uint4(p0, p1, p2, p3) : make_uint4(p2, p3, p0, p1);
+            }
+            *reinterpret_cast<uint4 *>(dst + tp * 128 + s8 * 2) = pk;
+        }
+        __syncthreads();   // every read of vb, G32 and N32 done before the next unit rewrites them
+        cur = nxt;
+        nxt = n2;
+    }
+    if (q == kCtl) {   // the record stores complete; after a wait gave up, every copy and MMA lands
+        if (stored) bulk_wait<0>();
+        for (; kwait < kiss; ++kwait) mbar_wait(&kfull, kwait & 1, nullptr, 0);
+        for (; gwait < giss; ++gwait) mbar_wait(&gfull, gwait & 1, nullptr, 0);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 64);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_build_gdn_prep(const BuildParams &p, cudaStream_t s) {
@@ -425,6 +679,34 @@ cudaError_t launch_build_gdn_prep(const BuildParams &p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     // pairs of value heads share a key head when the grouped-query factor is even
     return p.gqa % 2 == 0 ? launch_prep<2>(p, total, tmK, sms, s) : launch_prep<1>(p, total, tmK, sms, s);
+}
+
+cudaError_t launch_build_kda_prep(const BuildParams &p, cudaStream_t s) {
+    if (p.n_seg == 0) return cudaSuccess;
+    const SegEntry &l = p.seg[p.n_seg - 1];
+    const int64_t total = (int64_t)l.wsb + (int64_t)p.H_v * ((l.len + C - 1) / C);
+    if (total == 0) return cudaSuccess;
+    if (total > INT32_MAX / C) return cudaErrorInvalidValue;
+    const int64_t N = p.n_tok > 0 ? p.n_tok : 1;
+    CUtensorMap tmK, tmKt, tmKb;
+    if (!make_tmap_3d(&tmK, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_k, N, (uint64_t)D * 2,
+                      (uint64_t)p.H_k * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&tmKt, p.kda_kt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)total * C, D * 2, 64, C,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&tmKb, p.kda_kb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)total * C, D * 2, 64, C,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    int dev = 0, sms = 0;
+    cudaError_t e;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    e = cudaMemsetAsync(static_cast<uint8_t *>(p.workspace) + total * kGdnRecordBytes, 0, sizeof(unsigned), s);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(build_kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KdaGeo::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int grid = (int)std::min<int64_t>(total, (int64_t)sms * KdaGeo::kCtasPerSm);
+    build_kda_prep_kernel<<<grid, kThreads, KdaGeo::kSmemBytes, s>>>(p, tmK, tmKt, tmKb);
+    return cudaGetLastError();
 }
 
 }  // namespace hypic

@@ -56,6 +56,15 @@
 // D_P columns;
 // the P-half warps turn it into the bf16 operand A (masked) and read the outputs out, scaled
 // with the chunk's gate slot (four slots, so that the slot outlives the read-out).
+// KDA instance (the channel-gated delta rule, one decay per key channel; build_gdn_prep.cu
+// derives its chunk form). The preparation leaves per chunk M2 (of the gated gram), the gated
+// keys Kt = e^{c} k and Kb = e^{c_C - c} k, and the per-channel log-decay c_C with its maximum m.
+// The chain is the same with W = M2 Kt, U = M2 V (no M1), the update Z += Kb^T D, and instead of
+// the running log-scale a per-chunk rescale of the state in the Z pass: the conversion warps
+// write the bf16 copy of Z, then Z scaled by Diag(e^{c_C}) (S half) or Diag(e^{c_C - m}) (P half,
+// whose D is scaled by e^{-m} too) back over it, so that the transition is stored as
+// exp(sum m) P with P in range. Kt and Kb share the k ring's slot; the gate values of a chunk
+// sit in one of four slots in the M1 area, each with its own barrier.
 // Every wait is bounded; a wait that runs out sets the status word and the CTA drains.
 #include <algorithm>
 
@@ -94,6 +103,8 @@ constexpr uint32_t kSmemBytes = kOffM1 + 2 * kRec + 1024;
 constexpr uint32_t kOffQ = kOffM1 + 2 * kRec;
 constexpr uint32_t kOffAq = kOffQ + 2 * kKV;
 constexpr uint32_t kSmemBytesOut = kOffAq + 2 * kRec + 1024;
+// KDA instance: k-ring slots of two tiles (Kt, Kb); the gate slots take the M1 area
+constexpr uint32_t kSmemBytesKda = kKSlots * 2 * kKV + kVSlots * kVR + 2 * kKV + 2 * kRec + 1024;
 
 constexpr uint32_t kTZ = 0, kTD = 256, kTZK = 384;
 constexpr uint32_t kTO = 128, kTAq = 320;   // outputs instance: O^T (two buffers) and Q K^T (the P half's columns)
@@ -105,6 +116,14 @@ struct Slot {   // per-chunk values from the operand warps (two slots)
     float lam_after;  // Lam after this chunk
     float lam_sum;    // sum of c_C up to and including this chunk
 };
+
+// KDA: the chunk's per-channel scales of the S and P halves, e^{-m} and the running sum of m
+struct KdaSlot {
+    float gs[D], gp[D];
+    float em, lam_sum, pad[2];
+};
+constexpr int kKdaSlots = 4;
+static_assert(kKdaSlots * sizeof(KdaSlot) <= 2 * kRec, "KDA gate slots exceed the M1 area");
 
 struct Bars {
     uint64_t kfull[kKSlots], kempty[kKSlots];   // k ring
@@ -120,6 +139,7 @@ struct Bars {
     // outputs instance: the q ring (emptied by Q S~ and Q K^T), Q K^T in TMEM (written by the
     // P issuer, read by the output warps), its bf16 slots, and the output accumulator
     uint64_t qfull[2], qempty[2], aqfull, aqfree, aqready[2], ofull[2], ofree[2];   // O: two buffers
+    uint64_t gready[kKdaSlots];   // KDA: a chunk's gate slot written (operand warps)
 };
 
 // Named barrier of the 128 operand-warp threads, and the same with an AND of a predicate
@@ -164,8 +184,8 @@ __device__ __forceinline__ void st_bf16x64(uint32_t taddr, const uint32_t (&z)[6
 }
 
 // OUT: the instance launched when the call asks for the segment outputs (both kinds of CTA);
-// the plain build compiles without any of the outputs code
-template <bool OUT>
+// the plain build compiles without any of the outputs code. KDA: the channel-gated instance.
+template <bool OUT, bool KDA>
 __global__ void __launch_bounds__(kThreads, 1)
 build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmR,
@@ -192,6 +212,12 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
     const int hk = h / p.gqa;
     const int nch = (seg.len + C - 1) / C;
     const bool gdn = p.family == HYPIC_FAM_GDN;
+    // shared-memory map of this instance (KDA: two tiles per k-ring slot, gate slots over M1)
+    constexpr uint32_t kKSl = KDA ? 2 * kKV : kKV;
+    constexpr uint32_t oVR = kKSlots * kKSl;
+    constexpr uint32_t oWop = oVR + kVSlots * kVR;
+    constexpr uint32_t oM1 = oWop + 2 * kKV;
+    KdaSlot *kslots = reinterpret_cast<KdaSlot *>(smem + oM1);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kKSlots; ++s) {
@@ -221,6 +247,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
         }
         mbar_init(&bars.aqfull, 1);
         mbar_init(&bars.aqfree, 128);
+        for (int s = 0; s < kKdaSlots; ++s) mbar_init(&bars.gready[s], 128);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars.ofull[s], 1);
             mbar_init(&bars.ofree[s], 128);
@@ -254,19 +281,28 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 const int32_t t0 = seg.start + c * C;
                 const int ks = c % kKSlots, kuse = c / kKSlots;
                 if (kuse >= 1 && !wait(&bars.kempty[ks], (kuse - 1) & 1)) break;
-                uint8_t *kt = smem + kOffK + ks * kKV;
-                mbar_arrive_expect_tx(&bars.kfull[ks], kKV);
-                tma_load_3d(kt, &tmK, &bars.kfull[ks], 0, hk, t0);
-                tma_load_3d(kt + kHalf, &tmK, &bars.kfull[ks], 64, hk, t0);
+                uint8_t *kt = smem + kOffK + ks * kKSl;
+                const int32_t rrow = (seg.wsb + h * nch + c) * 64;
+                if constexpr (KDA) {   // Kt and Kb: records of the preparation (see below)
+                    if (c == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+                    mbar_arrive_expect_tx(&bars.kfull[ks], 2 * kKV);
+                    tma_load_2d(kt, &tmK, &bars.kfull[ks], 0, rrow);
+                    tma_load_2d(kt + kHalf, &tmK, &bars.kfull[ks], 64, rrow);
+                    tma_load_2d(kt + kKV, &tmQ, &bars.kfull[ks], 0, rrow);
+                    tma_load_2d(kt + kKV + kHalf, &tmQ, &bars.kfull[ks], 64, rrow);
+                } else {
+                    mbar_arrive_expect_tx(&bars.kfull[ks], kKV);
+                    tma_load_3d(kt, &tmK, &bars.kfull[ks], 0, hk, t0);
+                    tma_load_3d(kt + kHalf, &tmK, &bars.kfull[ks], 64, hk, t0);
+                }
                 kc = c + 1;
                 // the records are written by the preparation kernel, which may still be
                 // running (this grid is a programmatic dependent launch): wait for it to
                 // complete before the first record load (k and v above are inputs)
-                if (c == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+                if (!KDA && c == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
                 const int vs = c % kVSlots, vuse = c / kVSlots;
                 if (vuse >= 1 && !wait(&bars.vempty[vs], (vuse - 1) & 1)) break;
-                uint8_t *vt = smem + kOffVR + vs * kVR;
-                const int32_t rrow = (seg.wsb + h * nch + c) * 64;
+                uint8_t *vt = smem + oVR + vs * kVR;
                 mbar_arrive_expect_tx(&bars.vfull[vs], kVR);
                 tma_load_3d(vt, &tmV, &bars.vfull[vs], 0, h, t0);
                 tma_load_3d(vt + kHalf, &tmV, &bars.vfull[vs], 64, h, t0);
@@ -305,10 +341,10 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             constexpr uint32_t idF = idesc(kFmtBF16, kFmtBF16, false, true, 128, 128);
             const uint32_t sb = smem_u32(smem);
             const uint64_t dK = sdesc(sb + kOffK, kHalf, 1024, kSwizzle128B);         // MN-major
-            const uint64_t dV = sdesc(sb + kOffVR, kHalf, 1024, kSwizzle128B);        // MN-major
-            const uint64_t dR = sdesc(sb + kOffVR + kKV, 16, 1024, kSwizzle128B);     // K-major
-            const uint64_t dW = sdesc(sb + kOffWop, kHalf, 1024, kSwizzle128B);       // MN-major
-            const uint64_t dM = sdesc(sb + kOffM1, 16, 1024, kSwizzle128B);           // K-major
+            const uint64_t dV = sdesc(sb + oVR, kHalf, 1024, kSwizzle128B);           // MN-major
+            const uint64_t dR = sdesc(sb + oVR + kKV, 16, 1024, kSwizzle128B);        // K-major
+            const uint64_t dW = sdesc(sb + oWop, kHalf, 1024, kSwizzle128B);          // MN-major
+            const uint64_t dM = sdesc(sb + oM1, 16, 1024, kSwizzle128B);              // K-major
             const uint64_t dQ = sdesc(sb + kOffQ, 16, 1024, kSwizzle128B);            // K-major
             const uint64_t dKk = sdesc(sb + kOffK, 16, 1024, kSwizzle128B);           // K-major
             const uint64_t dAq = sdesc(sb + kOffAq, 16, 1024, kSwizzle128B);          // K-major
@@ -328,8 +364,8 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             };
             // Z^T(hf) += D^T(hf) K(c) with A = bf16 D^T in TMEM; with the other half's update
             // it frees the k slot
-            auto issue_f = [&](int c) {
-                const uint64_t b = dK + (((c % kKSlots) * kKV) >> 4);
+            auto issue_f = [&](int c) {   // KDA: B = Kb, the slot's second tile
+                const uint64_t b = dK + (((c % kKSlots) * kKSl + (KDA ? kKV : 0)) >> 4);
                 const uint32_t d = tmem + kTZ + 128 * hf, a = tmem + kTD + 64 * hf;
 #pragma unroll
                 for (int s = 0; s < 4; ++s) mma_bf16_ta(d, a + 8 * s, b + s * kRow16, idF, 1u);
@@ -359,8 +395,8 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             if (hf == 0) {
                 // W^T(c) = K^T M2^T into the S~ half's bf16-Z^T columns (A: the k chunk read
                 // MN-major, B: the M2 record K-major)
-                auto issue_w = [&](int c) {
-                    const uint64_t a = dK + (((c % kKSlots) * kKV) >> 4), b = dR + (((c % kVSlots) * kVR) >> 4);
+                auto issue_w = [&](int c) {   // KDA: A = Kt
+                    const uint64_t a = dK + (((c % kKSlots) * kKSl) >> 4), b = dR + (((c % kVSlots) * kVR) >> 4);
                     mma_bf16(tmem + kTZK, a, b, idA, 0u);
 #pragma unroll
                     for (int s = 1; s < 4; ++s) mma_bf16(tmem + kTZK, a + s * kRow16, b + s * kCol16, idA, 1u);
@@ -368,8 +404,9 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 };
                 // D_S^T(c) = V^T M1^T (A: the v chunk read MN-major, B: M1 K-major); frees the
                 // {v, M2} slot of chunk c
-                auto issue_u = [&](int c) {
-                    const uint64_t a = dV + (((c % kVSlots) * kVR) >> 4), b = dM + (((c & 1) * kRec) >> 4);
+                auto issue_u = [&](int c) {   // KDA: B = the M2 record itself
+                    const uint64_t a = dV + (((c % kVSlots) * kVR) >> 4);
+                    const uint64_t b = KDA ? dR + (((c % kVSlots) * kVR) >> 4) : dM + (((c & 1) * kRec) >> 4);
                     mma_bf16(tmem + kTD, a, b, idA, 0u);
 #pragma unroll
                     for (int s = 1; s < 4; ++s) mma_bf16(tmem + kTD, a + s * kRow16, b + s * kCol16, idA, 1u);
@@ -470,6 +507,26 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             la_next = q < min(C, seg.len) ? p.log_gate[tok * p.H_v + h] : 0.f;
         }
         for (int c = 0; c < nch; ++c) {
+            if constexpr (KDA) {
+                // (1) the chunk's scales from the preparation's record: S half e^{c_C}, P half
+                //     e^{c_C - m}, D_P e^{-m}. Slot c % 4 was last read for chunk c - 4: the
+                //     waits of chunk c - 1 below (W(c - 1) complete, hence d_S(c - 2); d_P(c - 3)
+                //     complete) imply that both halves are done with chunk c - 4.
+                if (c == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+                const float *side = p.kda_side + ((int64_t)seg.wsb + (int64_t)h * nch + c) * kKdaSide;
+                const float cq = side[q], mC = side[128];
+                KdaSlot &ks = kslots[c % kKdaSlots];
+                ks.gs[q] = expf(cq);
+                ks.gp[q] = expf(cq - mC);
+                lam_sum += mC;
+                if (q == 0) {
+                    ks.em = expf(-mC);
+                    ks.lam_sum = lam_sum;
+                }
+                mbar_arrive(&bars.gready[c % kKdaSlots]);
+                // (2) no M1: U reads the record itself
+                mbar_arrive(&bars.m1ready[c & 1]);
+            } else {
             Slot &sl = slots[c % kSlots];
             // (1) gates: prefix sums c_t, chunk total c_C, the log-scale bookkeeping.
             //     Slot c % 2 was last read for chunk c - 2, whose W product has been issued.
@@ -504,8 +561,8 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             // (2) M1[t'][t] = M2[t'][t] exp(-Lam_start - c_t), same swizzled layout
             if (!bar_aux_and(wait(&bars.vfull[c % kVSlots], (c / kVSlots) & 1))) break;
             {
-                const uint8_t *rec = smem + kOffVR + (c % kVSlots) * kVR + kKV;
-                uint8_t *m1 = smem + kOffM1 + (c & 1) * kRec;
+                const uint8_t *rec = smem + oVR + (c % kVSlots) * kVR + kKV;
+                uint8_t *m1 = smem + oM1 + (c & 1) * kRec;
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int e = q + 128 * m;   // 16-byte piece: row t', columns 8 t8 .. 8 t8 + 7
@@ -528,6 +585,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             }
             fence_async_shared();
             mbar_arrive(&bars.m1ready[c & 1]);
+            }
             // (3) W^T(c) -> -W^T bf16, MN-major B operand (row i = this thread's lane). The
             //     slot was last read by d_S(c-2) (ordered before W(c) by its issuer) and by
             //     d_P(c-2), whose completion is signalled on wfree.
@@ -539,7 +597,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 uint32_t z[64];
                 ld64(tmem + lane_off + kTZK, z);
                 tmem_ld_wait();
-                uint8_t *wop = smem + kOffWop + (c & 1) * kKV;
+                uint8_t *wop = smem + oWop + (c & 1) * kKV;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     uint4 pk;
@@ -649,7 +707,11 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             if (c >= 1 && !(ok = wwait(&bars.zfull[hf], (c - 1) & 1))) break;
             bool renorm = false;
             float rs = 1.f;
-            if (hf == 0) {
+            if constexpr (KDA) {   // both halves read the chunk's gate slot
+                if (!(ok = wwait(&bars.gready[c % kKdaSlots], (c / kKdaSlots) & 1) &&
+                           (hf == 1 || wwait(&bars.wready[c & 1], (c >> 1) & 1))))
+                    break;
+            } else if (hf == 0) {
                 if (!(ok = wwait(&bars.m1ready[c & 1], (c >> 1) & 1) && wwait(&bars.wready[c & 1], (c >> 1) & 1)))
                     break;
                 renorm = slots[c % kSlots].renorm != 0;
@@ -661,6 +723,24 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 uint32_t z[64];
                 ld64(tmem + lane_off + zcol + 64 * cb, z);
                 tmem_ld_wait();
+                if constexpr (KDA) {
+                    // the bf16 copy of Z for d, then Z scaled per key row for the update
+                    st_bf16x64(tmem + lane_off + zkcol + 32 * cb, z);
+                    const float4 *g4 = reinterpret_cast<const float4 *>(
+                        (hf == 0 ? kslots[c % kKdaSlots].gs : kslots[c % kKdaSlots].gp) + 64 * cb);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float4 gg = g4[j];
+                        z[4 * j] = __float_as_uint(__uint_as_float(z[4 * j]) * gg.x);
+                        z[4 * j + 1] = __float_as_uint(__uint_as_float(z[4 * j + 1]) * gg.y);
+                        z[4 * j + 2] = __float_as_uint(__uint_as_float(z[4 * j + 2]) * gg.z);
+                        z[4 * j + 3] = __float_as_uint(__uint_as_float(z[4 * j + 3]) * gg.w);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        tmem_st16(tmem + lane_off + zcol + 64 * cb + 16 * j, *reinterpret_cast<uint32_t(*)[16]>(&z[16 * j]));
+                    continue;
+                }
                 if (renorm) {
 #pragma unroll
                     for (int j = 0; j < 64; ++j) z[j] = __float_as_uint(__uint_as_float(z[j]) * rs);
@@ -681,6 +761,11 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 uint32_t z[64];
                 ld64(tmem + lane_off + dcol, z);
                 tmem_ld_wait();
+                if (KDA && hf == 1) {   // D_P e^{-m}: the transition is carried as exp(sum m) P
+                    const float em = kslots[c % kKdaSlots].em;
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) z[j] = __float_as_uint(__uint_as_float(z[j]) * em);
+                }
                 st_bf16x64(tmem + lane_off + dcol, z);
             }
             tmem_st_wait();
@@ -697,7 +782,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             const bool piece = seg.idx < 0;
             const int64_t unit = piece ? (int64_t)(-1 - seg.idx) * p.H_v + h : (int64_t)seg.idx * p.seg_stride + h;
             float *O = (hf == 0 ? (piece ? p.S_piece : p.S) : (piece ? p.P_piece : p.P)) + unit * D * D + n;
-            const float sc = (hf == 0 && nch > 0) ? expf(slots[(nch - 1) % kSlots].lam_after) : 1.f;
+            const float sc = (!KDA && hf == 0 && nch > 0) ? expf(slots[(nch - 1) % kSlots].lam_after) : 1.f;
 #pragma unroll
             for (int c0 = 0; c0 < 128; c0 += 32) {
                 uint32_t z[32];
@@ -706,7 +791,9 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
 #pragma unroll
                 for (int j = 0; j < 32; ++j) O[(int64_t)(c0 + j) * D] = __uint_as_float(z[j]) * sc;
             }
-            if (hf == 0 && n == 0) (piece ? p.lam_piece : p.lam)[unit] = nch > 0 ? slots[(nch - 1) % kSlots].lam_sum : 0.f;
+            if (hf == 0 && n == 0)
+                (piece ? p.lam_piece : p.lam)[unit] =
+                    nch == 0 ? 0.f : KDA ? kslots[(nch - 1) % kKdaSlots].lam_sum : slots[(nch - 1) % kSlots].lam_sum;
         }
     }
 
@@ -720,16 +807,16 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
 
 }  // namespace
 
-#ifndef HYPIC_GDN_TC_OUTPUTS
+#if !defined(HYPIC_GDN_TC_OUTPUTS) && !defined(HYPIC_GDN_TC_KDA)
 bool build_gdn_tc_supported(const BuildParams &p) {
     return p.D == D && p.dtype == HYPIC_BF16 &&
-           (p.family == HYPIC_FAM_GDN || p.family == HYPIC_FAM_DELTA);
+           (p.family == HYPIC_FAM_GDN || p.family == HYPIC_FAM_DELTA || p.family == HYPIC_FAM_KDA);
 }
 #endif
 
 namespace {
 
-template <bool OUT>
+template <bool OUT, bool KDA>
 cudaError_t launch_chain(const BuildParams &p, cudaStream_t s) {
     // with the segment outputs, a second CTA per unit runs the outputs instance
     const int blocks = p.n_seg * p.H_v * (p.O ? 2 : 1);
@@ -743,7 +830,15 @@ cudaError_t launch_chain(const BuildParams &p, cudaStream_t s) {
         !make_tmap_3d(&tmV, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_v, N, (uint64_t)D * 2,
                       (uint64_t)p.H_v * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    if (p.O) {
+    if (KDA) {   // the gated keys Kt (in tmK's place) and Kb (in tmQ's), [records x 64 rows][128]
+        if (records > 0 &&
+            (!make_tmap_2d(&tmK, p.kda_kt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)records * 64, D * 2, 64,
+                           64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+             !make_tmap_2d(&tmQ, p.kda_kb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)records * 64, D * 2, 64,
+                           64, CU_TENSOR_MAP_SWIZZLE_128B)))
+            return cudaErrorInvalidValue;
+        if (records == 0) tmQ = tmK;
+    } else if (p.O) {
         if (!make_tmap_3d(&tmQ, p.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_k, N, (uint64_t)D * 2,
                           (uint64_t)p.H_k * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
@@ -758,10 +853,10 @@ cudaError_t launch_chain(const BuildParams &p, cudaStream_t s) {
     } else {
         tmR = tmK;   // no chunk anywhere: the kernel issues no load
     }
-    cudaError_t e = launch_build_gdn_prep(p, s);
+    cudaError_t e = KDA ? launch_build_kda_prep(p, s) : launch_build_gdn_prep(p, s);
     if (e != cudaSuccess) return e;
-    const uint32_t smem = OUT ? kSmemBytesOut : kSmemBytes;
-    auto kern = build_gdn_tc_kernel<OUT>;
+    const uint32_t smem = KDA ? kSmemBytesKda : OUT ? kSmemBytesOut : kSmemBytes;
+    auto kern = build_gdn_tc_kernel<OUT, KDA>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (records == 0) {
@@ -786,15 +881,19 @@ cudaError_t launch_chain(const BuildParams &p, cudaStream_t s) {
 
 }  // namespace
 
-// The two instances are compiled in separate translation units (this file, and
-// build_gdn_tc_out.cu, which includes it with HYPIC_GDN_TC_OUTPUTS defined): with both in one
-// unit the plain chain measured 6.5% slower on GB300 (0.311 against 0.292 ms per build call).
-#ifndef HYPIC_GDN_TC_OUTPUTS
-cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s) {
-    return p.O ? launch_build_gdn_tc_outputs(p, s) : launch_chain<false>(p, s);
-}
+// The instances are compiled in separate translation units (this file; build_gdn_tc_out.cu and
+// build_gdn_tc_kda.cu, which include it with HYPIC_GDN_TC_OUTPUTS or HYPIC_GDN_TC_KDA defined):
+// with two in one unit the plain chain measured 6.5% slower on GB300 (0.311 against 0.292 ms
+// per build call).
+#if defined(HYPIC_GDN_TC_KDA)
+cudaError_t launch_build_kda_tc(const BuildParams &p, cudaStream_t s) { return launch_chain<false, true>(p, s); }
+#elif defined(HYPIC_GDN_TC_OUTPUTS)
+cudaError_t launch_build_gdn_tc_outputs(const BuildParams &p, cudaStream_t s) { return launch_chain<true, false>(p, s); }
 #else
-cudaError_t launch_build_gdn_tc_outputs(const BuildParams &p, cudaStream_t s) { return launch_chain<true>(p, s); }
+cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s) {
+    if (p.family == HYPIC_FAM_KDA) return launch_build_kda_tc(p, s);
+    return p.O ? launch_build_gdn_tc_outputs(p, s) : launch_chain<false, false>(p, s);
+}
 #endif
 
 }  // namespace hypic

@@ -29,6 +29,12 @@ struct SegEntry {
 constexpr int kGdnChunk = 64;
 constexpr int64_t kGdnRecordBytes = kGdnChunk * kGdnChunk * 2;
 constexpr int64_t kGdnWorkspaceTail = 256;   // after the records: the preparation's ticket counter
+// The channel-gated delta rule (KDA) adds, per record, the chunk's gated keys Kt and Kb (bf16
+// 64 x 128 each, row-major) and its per-channel log-decay c_C (128 fp32) plus their maximum m,
+// in three arrays after the tail: [records][64][128], [records][64][128], [records][kKdaSide].
+constexpr int64_t kKdaTileBytes = kGdnChunk * 128 * 2;
+constexpr int kKdaSide = 132;
+constexpr int64_t kKdaExtraBytes = 2 * kKdaTileBytes + kKdaSide * 4;
 
 struct BuildParams {
     int32_t family;
@@ -60,6 +66,9 @@ struct BuildParams {
     const void *q;        // segment outputs (exact path only): queries, outputs, start states
     void *O;
     const float *S_init;
+    void *kda_kt;         // KDA tensor-core build: the gated-key and log-decay records above
+    void *kda_kb;
+    float *kda_side;
     SegEntry seg[HYPIC_MAX_SEGMENTS];
 };
 
@@ -96,6 +105,8 @@ bool build_gated_tc_supported(const BuildParams &p);
 cudaError_t launch_build_gdn_tc(const BuildParams &p, cudaStream_t s);
 cudaError_t launch_build_gdn_tc_outputs(const BuildParams &p, cudaStream_t s);
 cudaError_t launch_build_gdn_prep(const BuildParams &p, cudaStream_t s);
+cudaError_t launch_build_kda_tc(const BuildParams &p, cudaStream_t s);
+cudaError_t launch_build_kda_prep(const BuildParams &p, cudaStream_t s);
 bool build_gdn_tc_supported(const BuildParams &p);
 
 // fp32 view of one input element (bf16 or fp32 storage).

@@ -277,7 +277,15 @@ def test_kda_needs_gates_beta_and_P(lib):
 
 
 def test_path_of_kda_outputs_and_start_states(lib):
+    a = good_build(family=5)   # bf16, d = 128: the tensor-core build of the channel-gated rule
+    assert lib.hypic_build_kernel_name(ctypes.byref(a)) == b"build_kda_tc"
+    # 8 records: M2 (8 KB), the ticket tail, then per record Kt, Kb (16 KB each) and 132 floats
+    assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == 8 * 8192 + 256 + 8 * (2 * 16384 + 132 * 4)
+    a.q, a.O = FAKE + 0x8000000, FAKE + 0x9000000   # KDA outputs: the exact path
+    assert lib.hypic_build_kernel_name(ctypes.byref(a)) == b"build_seq"
+    assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == 0
     a = good_build(family=5)
+    a.dtype = 1                                      # fp32 inputs: the exact path
     assert lib.hypic_build_kernel_name(ctypes.byref(a)) == b"build_seq"
     a = good_build(family=4)
     assert lib.hypic_build_kernel_name(ctypes.byref(a)) == b"build_gdn_tc"

@@ -5,7 +5,9 @@ Roles, as in the kernel: the TMA warp (k chunks into a 3-slot ring, {v chunk, M2
 another), the two MMA issuers (the S~ half: W, U, d_S, f_S; the P half: d_P, f_P), the operand
 warps (gates, M1 = M2 scaled, the read-out of W into the -W^T operand), and the conversion warps
 of each half (bf16 copies of Z and of D in TMEM). Each group of warps that arrives and waits
-together is one agent. Issued MMAs complete in issue order per issuer, in any interleaving
+together is one agent. The KDA instance (kda=True) is the same protocol with four gate slots,
+each with its own barrier, that both halves read (their Z passes rescale the state per key row,
+the P half's D pass scales D), no M1 (U reads the record), and a state write in both Z passes. Issued MMAs complete in issue order per issuer, in any interleaving
 between the two issuers; a commit fires when its issuer's earlier MMAs have completed.
 
 Every run checks for deadlock, for parity aliasing (the kernel waits on parities), and that each
@@ -34,15 +36,19 @@ class _Bar:
             self.done += 1
 
 
-def _run(nch, seed, mistake=None, out=False):
+def _run(nch, seed, mistake=None, out=False, kda=False):
     """One unit of nch chunks. out: the outputs instance of the kernel, whose P-half issuer
     computes the masked Q K^T of every chunk (Q by TMA into a two-slot ring) and whose P-half
     warps turn it into the bf16 operand of the intra-chunk product and read the outputs out;
     the S-half issuer adds Q S~ before d_S and the intra-chunk product after f_S."""
     rnd = random.Random(seed)
     KS = VS = 3
-    SL = 4 if out else 2   # per-chunk gate slots, as in the kernel
+    SL = 4 if out or kda else 2   # per-chunk gate slots, as in the kernel
+    if mistake == "kda_two_slots":
+        SL = 2
     B = {}
+    for s_ in range(4):
+        B[f"gready{s_}"] = _Bar()   # KDA: one per gate slot
     for s in range(KS):
         B[f"kfull{s}"], B[f"kempty{s}"] = _Bar(), _Bar(2)
     for s in range(VS):
@@ -62,7 +68,8 @@ def _run(nch, seed, mistake=None, out=False):
         B[f"ofull{s_}"], B[f"ofree{s_}"] = _Bar(), _Bar()
     # buffer contents (versions)
     m = dict(ZK0=None, ZK1=None, D0=None, D1=None, Z0=("Z", -1), Z1=("Z", -1), k={}, vr={},
-             wop={}, m1={}, slot={}, w_read=set(), q={}, aq={}, AQ=None, O0=None, O1=None)
+             wop={}, m1={}, slot={}, w_read=set(), q={}, aq={}, AQ=None, O0=None, O1=None,
+             slot_readers=set())
     queues = {0: [], 1: []}   # per issuer: pending MMAs and commits, in issue order
 
     def wait(name, phase):
@@ -189,6 +196,8 @@ def _run(nch, seed, mistake=None, out=False):
         if kind == "W":
             return {("k", op["k"]): c, ("vr", op["vr"]): c}, {"ZK0": ("W", c)}
         if kind == "U":
+            if kda:   # B is the M2 record itself
+                return {("vr", op["vr"]): c}, {"D0": ("U", c)}
             return {("vr", op["vr"]): c, ("m1", op["m1"]): c}, {"D0": ("U", c)}
         if kind == "dS":
             return {"ZK0": ("Z", c), ("wop", op["wop"]): c, "D0": ("U", c)}, {"D0": ("d", c)}
@@ -268,15 +277,22 @@ def _run(nch, seed, mistake=None, out=False):
     # ---------------------------------------------------------------- operand warps
     def operand():
         for c in range(nch):
+            if kda and any(r[0] == c % SL for r in m["slot_readers"]):
+                raise Hazard("gate slot rewritten while a half reads it")
             m["slot"][c % SL] = c
             yield
-            yield from wait(f"vfull{c % VS}", c // VS)
-            if m["vr"].get(c % VS) != c:
-                raise Hazard("M1 built from a stale record")
-            touches_inflight([("m1", c & 1)], True, "M1 write")
-            m["m1"][c & 1] = c
-            B[f"m1ready{c & 1}"].arrive()
-            yield
+            if kda:
+                B[f"gready{c % SL}"].arrive()
+                B[f"m1ready{c & 1}"].arrive()   # no M1: U reads the record
+                yield
+            else:
+                yield from wait(f"vfull{c % VS}", c // VS)
+                if m["vr"].get(c % VS) != c:
+                    raise Hazard("M1 built from a stale record")
+                touches_inflight([("m1", c & 1)], True, "M1 write")
+                m["m1"][c & 1] = c
+                B[f"m1ready{c & 1}"].arrive()
+                yield
             yield from wait("wfull", c)
             if c >= 2 and mistake != "no_wfree" and not out:   # d_P's read of the slot
                 yield from wait(f"wfree{c & 1}", (c - 2) >> 1)
@@ -289,11 +305,28 @@ def _run(nch, seed, mistake=None, out=False):
             B[f"wready{c & 1}"].arrive()
 
     # ---------------------------------------------------------------- conversion warps
+    def read_slot(hf, c, what):
+        # a half reads the gate slot of chunk c over some time
+        m["slot_readers"].add((c % SL, hf))
+        for _ in range(2):
+            if m["slot"].get(c % SL) != c:
+                raise Hazard(f"{what} reads the gate slot of another chunk")
+            yield
+        m["slot_readers"].discard((c % SL, hf))
+
     def conversion(hf):
         for c in range(nch):
             if c >= 1:
                 yield from wait(f"zfull{hf}", c - 1)
-            if hf == 0:
+            if kda:
+                if hf == 0 or mistake != "kda_p_without_gready":
+                    yield from wait(f"gready{c % SL}", c // SL)
+                if hf == 0:
+                    yield from wait(f"wready{c & 1}", c >> 1)
+                    if c >= 1 and c not in m["w_read"] and m["ZK0"] == ("W", c):
+                        raise Hazard("Z copy written over W before its read-out")
+                yield from read_slot(hf, c, f"Z pass {hf}")
+            elif hf == 0:
                 yield from wait(f"m1ready{c & 1}", c >> 1)
                 if mistake != "no_wready_before_z":
                     yield from wait(f"wready{c & 1}", c >> 1)
@@ -305,7 +338,7 @@ def _run(nch, seed, mistake=None, out=False):
                     raise Hazard("Z copy written under the in-flight W")
             if m[f"Z{hf}"] != ("Z", c - 1):
                 raise Hazard(f"Z conversion {hf} at chunk {c} reads {m[f'Z{hf}']}")
-            touches_inflight([f"Z{hf}"], hf == 0, "Z conversion")   # the S~ half may rescale Z
+            touches_inflight([f"Z{hf}"], hf == 0 or kda, "Z conversion")   # a rescale writes Z
             touches_inflight([f"ZK{hf}"], True, "Z copy")
             m[f"ZK{hf}"] = ("Z", c)
             B[f"zready{hf}"].arrive()
@@ -313,6 +346,8 @@ def _run(nch, seed, mistake=None, out=False):
             yield from wait(f"dfull{hf}", c)
             if m[f"D{hf}"] != ("d", c):
                 raise Hazard(f"D conversion {hf} at chunk {c} reads {m[f'D{hf}']}")
+            if kda and hf == 1:   # D_P scaled by e^{-m} of the chunk
+                yield from read_slot(hf, c, "D pass")
             touches_inflight([f"D{hf}"], True, "D conversion")
             m[f"D{hf}"] = ("Dbf", c)
             B[f"dready{hf}"].arrive()
@@ -321,6 +356,8 @@ def _run(nch, seed, mistake=None, out=False):
             yield from wait(f"zfull{hf}", nch - 1)
             if m[f"Z{hf}"] != ("Z", nch - 1):
                 raise Hazard("output reads a stale state")
+            if kda and hf == 0:   # lam from the last chunk's slot
+                yield from read_slot(hf, nch - 1, "lam output")
 
     # ---------------------------------------------------------------- output warps (out)
     # the P-half warps of the outputs instance: the masked Q K^T into the bf16 B operand of the
@@ -396,6 +433,25 @@ def test_outputs_instance_protocol_interleavings(nch):
         assert _run(nch, seed, out=True) == "ok"
 
 
+@pytest.mark.parametrize("nch", [1, 2, 3, 4, 7, 9])
+def test_kda_instance_protocol_interleavings(nch):
+    for seed in range(25):
+        assert _run(nch, seed, kda=True) == "ok"
+
+
+@pytest.mark.parametrize("mistake", ["kda_two_slots", "kda_p_without_gready"])
+def test_kda_instance_model_catches_planted_mistakes(mistake):
+    hits = 0
+    for seed in range(80):
+        try:
+            r = _run(7, seed, mistake, kda=True)
+        except Hazard:
+            hits += 1
+            continue
+        hits += r != "ok"
+    assert hits > 0
+
+
 @pytest.mark.parametrize("mistake", ["q_without_qempty", "one_output_buffer", "qk_without_aqfree",
                                      "three_gate_slots"])
 def test_outputs_instance_model_catches_planted_mistakes(mistake):
@@ -426,7 +482,7 @@ def test_chain_protocol_model_catches_planted_mistakes(mistake):
 
 
 # The kernel source this model was last checked against (code only; comments do not count).
-MODELLED_SOURCE = ("build_gdn_tc.cu", "b89dd608e6c9")
+MODELLED_SOURCE = ("build_gdn_tc.cu", "ae9bade53942")
 
 
 def test_model_is_checked_against_the_current_kernel_source():

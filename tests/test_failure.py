@@ -64,6 +64,19 @@ def test_gate_out_of_range_reports_range_status():
     assert torch.equal(S0, S1) and torch.equal(P0, P1) and torch.equal(l0, l1)
 
 
+def test_kda_channel_gate_out_of_range_reports_range_status():
+    """KDA: one key channel of one chunk decays below -60 (the others stay in range)."""
+    hy = _hy()
+    inp = synth.make_inputs("kda", 1, 2, 128, [200, 64, 130], torch.bfloat16, seed=85, alpha_scale=0.05)
+    lg = inp.log_gate.clone()
+    lg[200:264, 1, 17] = -1.25
+    d = to_dev(inp)
+    hy.hypic_build_segments("kda", d["k"], d["v"], inp.seg_offsets, log_gate=lg.cuda(), beta=d["beta"])
+    assert hy.hypic_get_device_status() == HYPIC_ERR_RANGE
+    hy.hypic_build_segments("kda", d["k"], d["v"], inp.seg_offsets, log_gate=d["log_gate"], beta=d["beta"])
+    assert hy.hypic_get_device_status() == 0
+
+
 def test_exact_path_has_no_gate_range_limit():
     """The exact fp32 path steps token by token in fp32 and has no chunk log-decay limit."""
     hy = _hy()

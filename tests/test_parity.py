@@ -44,17 +44,17 @@ def test_build_parity_ragged(family, dtype, d):
     check_build(inp)
 
 
-@pytest.mark.parametrize("family", ["gdn", "delta"])
+@pytest.mark.parametrize("family", ["gdn", "delta", "kda"])
 @pytest.mark.parametrize("H_k,H_v", [(3, 3), (1, 4), (2, 6)])
 def test_build_key_head_sharing(family, H_k, H_v):
     """Grouped-query factors 1, 4 and 3: the tensor-core build's chunk preparation handles
     the value heads of one key head two at a time when the factor is even, one at a time
-    otherwise."""
+    otherwise (KDA: one at a time, its gram depends on the value head's gates)."""
     inp = synth.make_inputs(family, H_k, H_v, 128, RAGGED, torch.bfloat16, seed=47, alpha_scale=0.05)
     check_build(inp)
 
 
-@pytest.mark.parametrize("family", ["gdn", "delta"])
+@pytest.mark.parametrize("family", ["gdn", "delta", "kda"])
 def test_build_more_units_than_sms(family):
     """More (segment, head) units than SMs, in several rounds per SM: 180 ragged segments
     (empty, one-token, one-chunk and multi-chunk) x 2 value heads through the tensor-core
@@ -65,7 +65,7 @@ def test_build_more_units_than_sms(family):
     check_build(inp)
 
 
-@pytest.mark.parametrize("family,per_token", [("gdn", False), ("delta", False), ("linear", False),
+@pytest.mark.parametrize("family,per_token", [("gdn", False), ("delta", False), ("kda", False), ("linear", False),
                                               ("scalar", False), ("scalar", True), ("diag", False)])
 @pytest.mark.parametrize("lens", [[3000], [2500, 100, 0, 65]])
 def test_build_split_segments(family, per_token, lens):
@@ -80,17 +80,30 @@ def test_build_split_segments(family, per_token, lens):
                                           log_gate=d.get("log_gate"), log_gamma=d.get("log_gamma"),
                                           beta=d.get("beta"))
     chunks = sum((n + 63) // 64 for n in lens)
-    records = chunks * 2 * 8192 + 256 if family in ("gdn", "delta") else 0
+    records = chunks * 2 * 8192 + 256 if family in ("gdn", "delta", "kda") else 0
     assert need > records      # (records and tail, and) the pieces' scratch
     check_build(inp)
 
 
-@pytest.mark.parametrize("family", ["gdn", "delta"])
+@pytest.mark.parametrize("family", ["gdn", "delta", "kda"])
 def test_build_halved_trailing_segments(family):
     """A call whose units take two rounds of SMs with a nearly empty second round (80 equal
     segments x 2 heads = 160 units): its last segments are built as halves and composed back
     in one batched launch."""
     inp = synth.make_inputs(family, 1, 2, 128, [130] * 80, torch.bfloat16, seed=48, alpha_scale=0.05)
+    check_build(inp)
+
+
+@pytest.mark.parametrize("alpha_scale", [0.3, 0.6])
+def test_build_kda_strong_channel_gates(alpha_scale):
+    """The channel-gated delta rule on the tensor cores with strong per-channel decays (chunk
+    log-decays of -20 to -45 per channel at 0.6): the gated keys e^{c} k and e^{-c} k of the
+    chunk's gram span a wide range, and the transition is carried as exp(sum m) P."""
+    inp = synth.make_inputs("kda", 2, 4, 128, RAGGED, torch.bfloat16, seed=49, alpha_scale=alpha_scale)
+    lg, offs = f64(inp.log_gate), inp.seg_offsets
+    sums = [lg[a:min(a + 64, offs[j + 1])].sum(0) for j in range(len(offs) - 1)
+            for a in range(int(offs[j]), int(offs[j + 1]), 64)]
+    assert min(float(x.min()) for x in sums) > -60   # inside the supported range
     check_build(inp)
 
 
@@ -420,7 +433,8 @@ def test_workload_gdn_compose_full_size_with_totals():
     ("scalar", torch.bfloat16, 64, "build_gated_simt"), ("gdn", torch.float32, 32, "build_seq"),
     ("gdn", torch.bfloat16, 128, "build_gdn_tc"), ("delta", torch.bfloat16, 128, "build_gdn_tc"),
     ("gdn", torch.float32, 128, "build_seq"), ("gdn", torch.bfloat16, 64, "build_seq"),
-    ("kda", torch.bfloat16, 128, "build_seq"), ("kda", torch.float32, 32, "build_seq"),
+    ("kda", torch.bfloat16, 128, "build_kda_tc"), ("kda", torch.float32, 32, "build_seq"),
+    ("kda", torch.bfloat16, 64, "build_seq"),
 ])
 def test_build_kernel_selection(family, dtype, d, expect):
     """bf16 inputs with d = 128 run on the tensor cores; fp32 inputs and smaller heads run the

@@ -132,6 +132,22 @@ def test_record_stage_is_conflict_free():
                 assert wavefronts(ab, 4) <= 4
 
 
+def sw128(row, byte):
+    return row * 128 + (byte ^ ((row & 7) << 4))
+
+
+def test_kda_tile_pass_is_conflict_free():
+    """The KDA preparation's pass over a chunk: thread q (one key channel) reads element (t, q)
+    of the k tile and writes it into the three gated tiles, all 64 x 128 bf16 as two
+    128B-swizzled 64-channel halves of 8 KB, token by token: each warp-wide access is one
+    wavefront (two lanes per word)."""
+    for w in range(4):
+        for t in range(64):
+            addrs = [(((32 * w + l) >> 6) * 8192 + sw128(t, 2 * ((32 * w + l) & 63))) // 4 for l in range(32)]
+            assert len(set(addrs)) == 16
+            assert wavefronts(addrs, 1) == 1
+
+
 def test_planted_unswizzled_layout_conflicts():
     worst = max(wavefronts(addrs, width) - {1: 1, 2: 2}[width]
                 for _, addrs, width in fragment_accesses(swizzle=lambda r: 0))
@@ -139,7 +155,7 @@ def test_planted_unswizzled_layout_conflicts():
 
 
 # The kernel source this model was last checked against (code only; comments do not count).
-MODELLED_SOURCE = ("build_gdn_prep.cu", "e619cdf67e60")
+MODELLED_SOURCE = ("build_gdn_prep.cu", "f12bf11e6580")
 
 
 def test_model_is_checked_against_the_current_kernel_source():
