@@ -131,6 +131,8 @@ BuildPath pick_build(const hypic_build_args *a) {
     q.family = a->family;
     q.dtype = a->dtype;
     q.D = a->d_k;
+    // the KDA preparation reads the per-channel log-gates of a channel pair as one 8-byte word
+    if (a->family == HYPIC_FAM_KDA && (reinterpret_cast<uintptr_t>(a->log_gate) & 7u)) return BuildPath::Seq;
     if (delta) return build_gdn_tc_supported(q) ? BuildPath::GdnTc : BuildPath::Seq;
     return build_gated_tc_supported(q) ? BuildPath::GatedTc : BuildPath::GatedSimt;
 }
@@ -436,7 +438,7 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
             const size_t r = (size_t)gdn_records(a);
             uint8_t *x = static_cast<uint8_t *>(a->workspace) + r * (size_t)kGdnRecordBytes + (size_t)kGdnWorkspaceTail;
             p.kda_kt = x;
-            p.kda_kb = x + r * (size_t)kKdaTileBytes;
+            p.kda_kh = x + r * (size_t)kKdaTileBytes;
             p.kda_side = reinterpret_cast<float *>(x + 2 * r * (size_t)kKdaTileBytes);
         }
         split = gdn_split_layout(a, base);

@@ -408,31 +408,40 @@ cudaError_t launch_prep(const BuildParams &p, int64_t total, const CUtensorMap &
 // one decay per key channel, a_t in (0, 1]^{d_k} (KDA is among the linear layers "Cut First-Token
 // Latency by 3.25x ..." (besthub.dev), paragraph "For linear layers", names). Inside a chunk let
 // c_t = sum_{s<=t} log a_s per channel (valid tokens only) and, elementwise,
-//     kt_t = e^{c_t} k_t,   kh_s = e^{-c_s} k_s,   kb_s = e^{c_C - c_s} k_s.
+//     kt_t = e^{c_t} k_t,   kh_s = e^{-c_s} k_s.
 // The chunk's delta values Delta (S_t = Diag(e^{c_t})(S0 + sum_{s<=t} kh_s Delta_s^T)) solve
 // (I + A) Delta = Diag(b)(V - Kt S0) with A_ts = b_t (kt_t . kh_s) for s < t, and the state after
-// the chunk is Diag(e^{c_C}) S0 + Kb^T Delta. The gates do not factor out of A here (they differ
-// per channel), so the inverse is taken of the gated gram: M2 = (I + Diag(b) L)^-1 Diag(b) with
-// L the strictly lower part of Kt Kh^T, by the same blocked algorithm as above. One record per
-// (segment, value head, chunk): M2 (bf16 8 KB), Kt and Kb (bf16 64 x 128, written by bulk
-// tensor stores), c_C (128 fp32) and m = max_i c_C[i]. |c_t| <= |c_C| <= 60 keeps e^{-c_t}
-// within the range of bf16; a chunk below that sets the range status.
+// the chunk is Diag(e^{c_C}) (S0 + Kh^T Delta). The gates do not factor out of A here (they
+// differ per channel), so the inverse is taken of the gated gram: M2 = (I + Diag(b) L)^-1 Diag(b)
+// with L the strictly lower part of Kt Kh^T, by the same blocked algorithm as above. One record
+// per (segment, value head, chunk): M2 (bf16 8 KB), Kt and Kh (bf16 64 x 128, written by bulk
+// tensor stores from the gram's operand tiles), c_C (128 fp32) and m = max_i c_C[i].
+// c_C <= c_t <= 0 and c_C >= -60 keep e^{-c_t} within the range of bf16; a chunk below that
+// sets the range status.
 constexpr float kKdaMinChunkLogDecay = -60.f;
 
+// 2^x by the hardware's approximate base-2 exponential (relative error about 2^-22 on the
+// arguments used here, |x| <= 87: far below the bf16 rounding of every value it scales)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Four CTAs per SM: the two operand tiles, G and N (the level products' 16 x 8 scratch sits in
+// the Kh tile once its store has read it; the token halves' gate sums at the start of G).
 struct KdaGeo {
     static constexpr uint32_t kOffK = 0;                  // k tile, then Kt in place, 16 KB
-    static constexpr uint32_t kOffH = 16384;              // Kh (B operand of the gram)
-    static constexpr uint32_t kOffB = 32768;              // Kb
-    static constexpr uint32_t kOffG32 = 49152;            // the gram, 10 blocks
+    static constexpr uint32_t kOffH = 16384;              // Kh, then the scratch
+    static constexpr uint32_t kOffG32 = 32768;            // the gram, 10 blocks
     static constexpr uint32_t kOffN32 = kOffG32 + kTri * 4;
-    static constexpr uint32_t kOffT = kOffN32 + kTri * 4;
-    static constexpr uint32_t kSmemBytes = kOffT + 4 * 16 * kLDT * 4 + 1024;
-    static constexpr int kCtasPerSm = 3;
+    static constexpr uint32_t kSmemBytes = kOffN32 + kTri * 4 + 1024;
+    static constexpr int kCtasPerSm = 4;
 };
 
 __global__ void __launch_bounds__(kThreads, KdaGeo::kCtasPerSm)
 build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmKb) {
+                      const __grid_constant__ CUtensorMap tmKt, const __grid_constant__ CUtensorMap tmKh) {
     using G = KdaGeo;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -447,10 +456,11 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     Walk cur = decode<1>(p, blockIdx.x, total);
     if (cur.r >= p.n_seg) return;   // uniform: the whole CTA leaves before any set-up
     const int q = threadIdx.x, warp = q >> 5, lane = q & 31;
-    uint8_t *tK = smem + G::kOffK, *tH = smem + G::kOffH, *tB = smem + G::kOffB;
+    uint8_t *tK = smem + G::kOffK, *tH = smem + G::kOffH;
     float *G32 = reinterpret_cast<float *>(smem + G::kOffG32);
     float *N32 = reinterpret_cast<float *>(smem + G::kOffN32);
-    float *Tw = reinterpret_cast<float *>(smem + G::kOffT) + warp * 16 * kLDT;
+    float *Tw = reinterpret_cast<float *>(tH) + warp * 16 * kLDT;
+    float2 (*s_part)[64] = reinterpret_cast<float2 (*)[64]>(G32);   // [token half][channel pair]
 
     if (q == 0) {
         mbar_init(&kfull, 1);
@@ -478,52 +488,71 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     if (q == kCtl) {
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmKt);
-        prefetch_tmap(&tmKb);
+        prefetch_tmap(&tmKh);
         load_k(cur);
     }
-    // element (t, channel q) of a 64 x 128 bf16 tile held as two 128B-swizzled 64-channel halves
-    const uint32_t hoff = (uint32_t)(q >> 6) * 8192u, qb = 2u * (uint32_t)(q & 63);
+    // Thread q takes the key channels 2 pc, 2 pc + 1 (pc = q % 64) over the tokens of one half
+    // of the chunk, th = q / 64: the pair's bf16 elements of a token are one word of a 64 x 128
+    // bf16 tile held as two 128B-swizzled 64-channel halves.
+    const int pc = q & 63, th = q >> 6;
+    const uint32_t hoff = (uint32_t)(pc >> 5) * 8192u, qb = 4u * (uint32_t)(pc & 31);
+    // the pair's log-gates over the half's valid tokens (0 past the segment end) and b of token
+    // q < 64, loaded a unit ahead so that their latency overlaps the previous inverse
+    constexpr int CH = C / 2;
+    float2 g[CH];
+    float beta_cur = 0.f;
+    auto load_gates = [&](const Walk &w) {
+        const SegEntry sg = p.seg[w.r];
+        const int nvw = min(C, sg.len - w.c * C);
+        const int64_t t0 = (int64_t)sg.start + (int64_t)w.c * C;
+        const float2 *gp = reinterpret_cast<const float2 *>(p.log_gate + ((t0 + CH * th) * p.H_v + w.h) * D) + pc;
+        const int64_t gs = (int64_t)p.H_v * (D / 2);
+#pragma unroll
+        for (int t = 0; t < CH; ++t) g[t] = CH * th + t < nvw ? __ldg(gp + t * gs) : make_float2(0.f, 0.f);
+        beta_cur = q < nvw ? p.beta[(t0 + q) * p.H_v + w.h] : 0.f;
+    };
+    load_gates(cur);
     for (int i = 0; cur.r < p.n_seg; ++i) {
         const SegEntry seg = p.seg[cur.r];
         const int nch = (seg.len + C - 1) / C;
-        const int nv = min(C, seg.len - cur.c * C);
-        const int64_t tok0 = (int64_t)seg.start + (int64_t)cur.c * C;
         const int64_t rec = (int64_t)seg.wsb + (int64_t)cur.h * nch + cur.c;
-        // (1) the log-gates of channel q over the chunk's valid tokens, and b
-        float g[C];
+        // (1) b of the unit; the pair's log-decay over this token half
+        if (q < C) vb[vbi(q)] = beta_cur;
         {
-            const float *gp = p.log_gate + (tok0 * p.H_v + cur.h) * D + q;
-            const int64_t gs = (int64_t)p.H_v * D;
+            float2 sh = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int t = 0; t < C; ++t) g[t] = t < nv ? __ldg(gp + t * gs) : 0.f;
+            for (int t = 0; t < CH; ++t) sh.x += g[t].x, sh.y += g[t].y;
+            s_part[th][pc] = sh;
         }
-        if (q < C) vb[vbi(q)] = q < nv ? p.beta[(tok0 + q) * p.H_v + cur.h] : 0.f;
         if (q == kCtl && nxt.r < p.n_seg) ticket = 2 * (int64_t)gridDim.x + atomicAdd(tickets, 1u);
         ok = ok && mbar_wait(&kfull, kwait & 1, p.err, kErrTimeout);
         ++kwait;
         if (!__syncthreads_and(ok)) break;   // uniform
-        // (2) channel q of Kt (over k), Kh and Kb, token by token
-        float cC = 0.f;
-#pragma unroll
-        for (int t = 0; t < C; ++t) cC += g[t];
+        // (2) the pair's elements of Kt (over k) and Kh, token by token
+        const float2 p0 = s_part[0][pc], p1 = s_part[1][pc];
+        const float2 cC = make_float2(p0.x + p1.x, p0.y + p1.y);
         {
-            float c = 0.f;
+            constexpr float kLog2e = 1.4426950408889634f;
+            float cx = th ? p0.x : 0.f, cy = th ? p0.y : 0.f;
 #pragma unroll
-            for (int t = 0; t < C; ++t) {
-                c += g[t];
-                const uint32_t off = hoff + sw128((uint32_t)t, qb);
-                const float kv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tK + off));
-                *reinterpret_cast<__nv_bfloat16 *>(tK + off) = __float2bfloat16_rn(kv * expf(c));
-                *reinterpret_cast<__nv_bfloat16 *>(tH + off) = __float2bfloat16_rn(kv * expf(-c));
-                *reinterpret_cast<__nv_bfloat16 *>(tB + off) = __float2bfloat16_rn(kv * expf(cC - c));
+            for (int t = 0; t < CH; ++t) {
+                cx += g[t].x;
+                cy += g[t].y;
+                const uint32_t off = hoff + sw128((uint32_t)(CH * th + t), qb);
+                const uint32_t kw = *reinterpret_cast<const uint32_t *>(tK + off);
+                const float kx = __uint_as_float(kw << 16), ky = __uint_as_float(kw & 0xffff0000u);
+                *reinterpret_cast<uint32_t *>(tK + off) =
+                    pack_bf16x2(kx * ex2_approx(cx * kLog2e), ky * ex2_approx(cy * kLog2e));
+                *reinterpret_cast<uint32_t *>(tH + off) =
+                    pack_bf16x2(kx * ex2_approx(-cx * kLog2e), ky * ex2_approx(-cy * kLog2e));
             }
         }
-        if (cC < kKdaMinChunkLogDecay) atomicOr(p.err, kErrRange);
-        float mx = cC;
+        if (fminf(cC.x, cC.y) < kKdaMinChunkLogDecay) atomicOr(p.err, kErrRange);
+        float mx = fmaxf(cC.x, cC.y);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         if (lane == 0) s_max[warp] = mx;
-        fence_async_shared();   // Kt, Kh and Kb are read by the tensor core and the bulk stores
+        fence_async_shared();   // Kt and Kh are read by the tensor core and the bulk stores
         __syncthreads();
         if (q == kCtl) {
             tc_fence_after();
@@ -537,19 +566,19 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
             }
             mma_commit(&gfull);
             ++giss;
-            // Kt and Kb to their records (64 rows each, two 64-channel boxes)
+            // Kt and Kh to their records (64 rows each, two 64-channel boxes)
             const int32_t row = (int32_t)(rec * C);
             tma_store_2d(&tmKt, tK, 0, row);
             tma_store_2d(&tmKt, tK + 8192, 64, row);
-            tma_store_2d(&tmKb, tB, 0, row);
-            tma_store_2d(&tmKb, tB + 8192, 64, row);
+            tma_store_2d(&tmKh, tH, 0, row);
+            tma_store_2d(&tmKh, tH + 8192, 64, row);
             bulk_commit();
             stored = true;
         }
         {
             const float m = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
             float *side = p.kda_side + rec * kKdaSide;
-            side[q] = cC;
+            if (th == 0) reinterpret_cast<float2 *>(side)[pc] = cC;
             if (q == 0) side[128] = m;
         }
         ok = ok && mbar_wait(&gfull, gwait & 1, p.err, kErrTimeout);
@@ -580,12 +609,14 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         }
         tc_fence_before();
         __syncthreads();
-        // the next k tile: the gram has read the tile, and the stores must have read Kt and Kb
-        // (the next tile lands over Kt; Kb is rewritten after that tile has landed)
-        if (q == kCtl && nxt.r < p.n_seg) {
+        // the stores must have read Kt and Kh before the next k tile lands over Kt and the
+        // level products' scratch is written over Kh (after the barrier below); the next unit's
+        // gates
+        if (q == kCtl) {
             bulk_wait_read<0>();
-            load_k(nxt);
+            if (nxt.r < p.n_seg) load_k(nxt);
         }
+        if (nxt.r < p.n_seg) load_gates(nxt);
         // diagonal blocks by forward substitution, lane j < 16 of warp a: column j of block a
         if (lane < 16) {
             const int a = warp, j = lane;
@@ -640,7 +671,7 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
             }
             *reinterpret_cast<uint4 *>(dst + tp * 128 + s8 * 2) = pk;
         }
-        __syncthreads();   // every read of vb, G32 and N32 done before the next unit rewrites them
+        __syncthreads();   // every read of vb, G32, N32 and the scratch done before the next unit
         cur = nxt;
         nxt = n2;
     }
@@ -688,12 +719,12 @@ cudaError_t launch_build_kda_prep(const BuildParams &p, cudaStream_t s) {
     if (total == 0) return cudaSuccess;
     if (total > INT32_MAX / C) return cudaErrorInvalidValue;
     const int64_t N = p.n_tok > 0 ? p.n_tok : 1;
-    CUtensorMap tmK, tmKt, tmKb;
+    CUtensorMap tmK, tmKt, tmKh;
     if (!make_tmap_3d(&tmK, p.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_k, N, (uint64_t)D * 2,
                       (uint64_t)p.H_k * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_2d(&tmKt, p.kda_kt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)total * C, D * 2, 64, C,
                       CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_2d(&tmKb, p.kda_kb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)total * C, D * 2, 64, C,
+        !make_tmap_2d(&tmKh, p.kda_kh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)total * C, D * 2, 64, C,
                       CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     int dev = 0, sms = 0;
@@ -705,7 +736,7 @@ cudaError_t launch_build_kda_prep(const BuildParams &p, cudaStream_t s) {
     e = cudaFuncSetAttribute(build_kda_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, KdaGeo::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int grid = (int)std::min<int64_t>(total, (int64_t)sms * KdaGeo::kCtasPerSm);
-    build_kda_prep_kernel<<<grid, kThreads, KdaGeo::kSmemBytes, s>>>(p, tmK, tmKt, tmKb);
+    build_kda_prep_kernel<<<grid, kThreads, KdaGeo::kSmemBytes, s>>>(p, tmK, tmKt, tmKh);
     return cudaGetLastError();
 }
 

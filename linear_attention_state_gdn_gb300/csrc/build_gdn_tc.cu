@@ -58,13 +58,14 @@
 // with the chunk's gate slot (four slots, so that the slot outlives the read-out).
 // KDA instance (the channel-gated delta rule, one decay per key channel; build_gdn_prep.cu
 // derives its chunk form). The preparation leaves per chunk M2 (of the gated gram), the gated
-// keys Kt = e^{c} k and Kb = e^{c_C - c} k, and the per-channel log-decay c_C with its maximum m.
-// The chain is the same with W = M2 Kt, U = M2 V (no M1), the update Z += Kb^T D, and instead of
-// the running log-scale a per-chunk rescale of the state in the Z pass: the conversion warps
-// write the bf16 copy of Z, then Z scaled by Diag(e^{c_C}) (S half) or Diag(e^{c_C - m}) (P half,
-// whose D is scaled by e^{-m} too) back over it, so that the transition is stored as
-// exp(sum m) P with P in range. Kt and Kb share the k ring's slot; the gate values of a chunk
-// sit in one of four slots in the M1 area, each with its own barrier.
+// keys Kt = e^{c} k and Kh = e^{-c} k, and the per-channel log-decay c_C with its maximum m.
+// The chunk maps the state to Diag(e^{c_C}) (Z + Kh^T D), so the chain is the same with
+// W = M2 Kt, U = M2 V (no M1), the update Z += Kh^T D, and instead of the running log-scale the
+// chunk's row scaling applied in the next Z pass: the conversion warps scale Z by Diag(e^{c_C})
+// (S half) or Diag(e^{c_C - m}) (P half) of the previous chunk, write it back and take the bf16
+// copy of the scaled state; the outputs get the last chunk's scaling. The transition is stored as
+// exp(sum m) P with P in range. Kt and Kh share the k ring's slot; the scales of a chunk sit in
+// one of four slots in the M1 area, each with its own barrier.
 // Every wait is bounded; a wait that runs out sets the status word and the CTA drains.
 #include <algorithm>
 
@@ -103,7 +104,7 @@ constexpr uint32_t kSmemBytes = kOffM1 + 2 * kRec + 1024;
 constexpr uint32_t kOffQ = kOffM1 + 2 * kRec;
 constexpr uint32_t kOffAq = kOffQ + 2 * kKV;
 constexpr uint32_t kSmemBytesOut = kOffAq + 2 * kRec + 1024;
-// KDA instance: k-ring slots of two tiles (Kt, Kb); the gate slots take the M1 area
+// KDA instance: k-ring slots of two tiles (Kt, Kh); the gate slots take the M1 area
 constexpr uint32_t kSmemBytesKda = kKSlots * 2 * kKV + kVSlots * kVR + 2 * kKV + 2 * kRec + 1024;
 
 constexpr uint32_t kTZ = 0, kTD = 256, kTZK = 384;
@@ -117,10 +118,10 @@ struct Slot {   // per-chunk values from the operand warps (two slots)
     float lam_sum;    // sum of c_C up to and including this chunk
 };
 
-// KDA: the chunk's per-channel scales of the S and P halves, e^{-m} and the running sum of m
+// KDA: the chunk's per-channel scales of the S and P halves and the running sum of m
 struct KdaSlot {
     float gs[D], gp[D];
-    float em, lam_sum, pad[2];
+    float lam_sum, pad[3];
 };
 constexpr int kKdaSlots = 4;
 static_assert(kKdaSlots * sizeof(KdaSlot) <= 2 * kRec, "KDA gate slots exceed the M1 area");
@@ -283,7 +284,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 if (kuse >= 1 && !wait(&bars.kempty[ks], (kuse - 1) & 1)) break;
                 uint8_t *kt = smem + kOffK + ks * kKSl;
                 const int32_t rrow = (seg.wsb + h * nch + c) * 64;
-                if constexpr (KDA) {   // Kt and Kb: records of the preparation (see below)
+                if constexpr (KDA) {   // Kt and Kh: records of the preparation (see below)
                     if (c == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
                     mbar_arrive_expect_tx(&bars.kfull[ks], 2 * kKV);
                     tma_load_2d(kt, &tmK, &bars.kfull[ks], 0, rrow);
@@ -364,7 +365,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             };
             // Z^T(hf) += D^T(hf) K(c) with A = bf16 D^T in TMEM; with the other half's update
             // it frees the k slot
-            auto issue_f = [&](int c) {   // KDA: B = Kb, the slot's second tile
+            auto issue_f = [&](int c) {   // KDA: B = Kh, the slot's second tile
                 const uint64_t b = dK + (((c % kKSlots) * kKSl + (KDA ? kKV : 0)) >> 4);
                 const uint32_t d = tmem + kTZ + 128 * hf, a = tmem + kTD + 64 * hf;
 #pragma unroll
@@ -509,9 +510,9 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
         for (int c = 0; c < nch; ++c) {
             if constexpr (KDA) {
                 // (1) the chunk's scales from the preparation's record: S half e^{c_C}, P half
-                //     e^{c_C - m}, D_P e^{-m}. Slot c % 4 was last read for chunk c - 4: the
-                //     waits of chunk c - 1 below (W(c - 1) complete, hence d_S(c - 2); d_P(c - 3)
-                //     complete) imply that both halves are done with chunk c - 4.
+                //     e^{c_C - m}. Slot c % 4 was last read (for chunk c - 4) in the Z passes of
+                //     chunk c - 3: the waits of chunk c - 1 below (W(c - 1) complete, hence
+                //     d_S(c - 2); d_P(c - 3) complete) imply that both halves are done with them.
                 if (c == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
                 const float *side = p.kda_side + ((int64_t)seg.wsb + (int64_t)h * nch + c) * kKdaSide;
                 const float cq = side[q], mC = side[128];
@@ -519,10 +520,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 ks.gs[q] = expf(cq);
                 ks.gp[q] = expf(cq - mC);
                 lam_sum += mC;
-                if (q == 0) {
-                    ks.em = expf(-mC);
-                    ks.lam_sum = lam_sum;
-                }
+                if (q == 0) ks.lam_sum = lam_sum;
                 mbar_arrive(&bars.gready[c % kKdaSlots]);
                 // (2) no M1: U reads the record itself
                 mbar_arrive(&bars.m1ready[c & 1]);
@@ -707,8 +705,8 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             if (c >= 1 && !(ok = wwait(&bars.zfull[hf], (c - 1) & 1))) break;
             bool renorm = false;
             float rs = 1.f;
-            if constexpr (KDA) {   // both halves read the chunk's gate slot
-                if (!(ok = wwait(&bars.gready[c % kKdaSlots], (c / kKdaSlots) & 1) &&
+            if constexpr (KDA) {   // both halves read the previous chunk's gate slot
+                if (!(ok = (c == 0 || wwait(&bars.gready[(c - 1) % kKdaSlots], ((c - 1) / kKdaSlots) & 1)) &&
                            (hf == 1 || wwait(&bars.wready[c & 1], (c >> 1) & 1))))
                     break;
             } else if (hf == 0) {
@@ -723,11 +721,10 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 uint32_t z[64];
                 ld64(tmem + lane_off + zcol + 64 * cb, z);
                 tmem_ld_wait();
-                if constexpr (KDA) {
-                    // the bf16 copy of Z for d, then Z scaled per key row for the update
-                    st_bf16x64(tmem + lane_off + zkcol + 32 * cb, z);
-                    const float4 *g4 = reinterpret_cast<const float4 *>(
-                        (hf == 0 ? kslots[c % kKdaSlots].gs : kslots[c % kKdaSlots].gp) + 64 * cb);
+                if (KDA && c > 0) {
+                    // the previous chunk's row scaling, written back, then the bf16 copy for d
+                    const KdaSlot &ks = kslots[(c - 1) % kKdaSlots];
+                    const float4 *g4 = reinterpret_cast<const float4 *>((hf == 0 ? ks.gs : ks.gp) + 64 * cb);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const float4 gg = g4[j];
@@ -739,7 +736,6 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         tmem_st16(tmem + lane_off + zcol + 64 * cb + 16 * j, *reinterpret_cast<uint32_t(*)[16]>(&z[16 * j]));
-                    continue;
                 }
                 if (renorm) {
 #pragma unroll
@@ -761,11 +757,6 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
                 uint32_t z[64];
                 ld64(tmem + lane_off + dcol, z);
                 tmem_ld_wait();
-                if (KDA && hf == 1) {   // D_P e^{-m}: the transition is carried as exp(sum m) P
-                    const float em = kslots[c % kKdaSlots].em;
-#pragma unroll
-                    for (int j = 0; j < 64; ++j) z[j] = __float_as_uint(__uint_as_float(z[j]) * em);
-                }
                 st_bf16x64(tmem + lane_off + dcol, z);
             }
             tmem_st_wait();
@@ -775,6 +766,8 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
         // outputs: S = exp(Lam) S~ (column n) or P (column n), and lam (the outputs instance
         // writes only O)
         if (ok && nch > 0) ok = wwait(&bars.zfull[hf], (nch - 1) & 1);
+        // KDA: the last chunk's row scaling is applied here
+        if (KDA && ok && nch > 0) ok = wwait(&bars.gready[(nch - 1) % kKdaSlots], ((nch - 1) / kKdaSlots) & 1);
         tc_fence_after();
 
         if (!outm) {
@@ -783,13 +776,16 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             const int64_t unit = piece ? (int64_t)(-1 - seg.idx) * p.H_v + h : (int64_t)seg.idx * p.seg_stride + h;
             float *O = (hf == 0 ? (piece ? p.S_piece : p.S) : (piece ? p.P_piece : p.P)) + unit * D * D + n;
             const float sc = (!KDA && hf == 0 && nch > 0) ? expf(slots[(nch - 1) % kSlots].lam_after) : 1.f;
+            const float *gl = nullptr;
+            if (KDA && nch > 0) gl = hf == 0 ? kslots[(nch - 1) % kKdaSlots].gs : kslots[(nch - 1) % kKdaSlots].gp;
 #pragma unroll
             for (int c0 = 0; c0 < 128; c0 += 32) {
                 uint32_t z[32];
                 tmem_ld32(tmem + lane_off + zcol + c0, z);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) O[(int64_t)(c0 + j) * D] = __uint_as_float(z[j]) * sc;
+                for (int j = 0; j < 32; ++j)
+                    O[(int64_t)(c0 + j) * D] = __uint_as_float(z[j]) * (KDA && gl ? gl[c0 + j] : sc);
             }
             if (hf == 0 && n == 0)
                 (piece ? p.lam_piece : p.lam)[unit] =
@@ -830,11 +826,11 @@ cudaError_t launch_chain(const BuildParams &p, cudaStream_t s) {
         !make_tmap_3d(&tmV, p.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, p.H_v, N, (uint64_t)D * 2,
                       (uint64_t)p.H_v * D * 2, 64, 1, C, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    if (KDA) {   // the gated keys Kt (in tmK's place) and Kb (in tmQ's), [records x 64 rows][128]
+    if (KDA) {   // the gated keys Kt (in tmK's place) and Kh (in tmQ's), [records x 64 rows][128]
         if (records > 0 &&
             (!make_tmap_2d(&tmK, p.kda_kt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)records * 64, D * 2, 64,
                            64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-             !make_tmap_2d(&tmQ, p.kda_kb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)records * 64, D * 2, 64,
+             !make_tmap_2d(&tmQ, p.kda_kh, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, D, (uint64_t)records * 64, D * 2, 64,
                            64, CU_TENSOR_MAP_SWIZZLE_128B)))
             return cudaErrorInvalidValue;
         if (records == 0) tmQ = tmK;

@@ -29,7 +29,7 @@ struct SegEntry {
 constexpr int kGdnChunk = 64;
 constexpr int64_t kGdnRecordBytes = kGdnChunk * kGdnChunk * 2;
 constexpr int64_t kGdnWorkspaceTail = 256;   // after the records: the preparation's ticket counter
-// The channel-gated delta rule (KDA) adds, per record, the chunk's gated keys Kt and Kb (bf16
+// The channel-gated delta rule (KDA) adds, per record, the chunk's gated keys Kt and Kh (bf16
 // 64 x 128 each, row-major) and its per-channel log-decay c_C (128 fp32) plus their maximum m,
 // in three arrays after the tail: [records][64][128], [records][64][128], [records][kKdaSide].
 constexpr int64_t kKdaTileBytes = kGdnChunk * 128 * 2;
@@ -67,7 +67,7 @@ struct BuildParams {
     void *O;
     const float *S_init;
     void *kda_kt;         // KDA tensor-core build: the gated-key and log-decay records above
-    void *kda_kb;
+    void *kda_kh;
     float *kda_side;
     SegEntry seg[HYPIC_MAX_SEGMENTS];
 };

@@ -6,8 +6,9 @@ another), the two MMA issuers (the S~ half: W, U, d_S, f_S; the P half: d_P, f_P
 warps (gates, M1 = M2 scaled, the read-out of W into the -W^T operand), and the conversion warps
 of each half (bf16 copies of Z and of D in TMEM). Each group of warps that arrives and waits
 together is one agent. The KDA instance (kda=True) is the same protocol with four gate slots,
-each with its own barrier, that both halves read (their Z passes rescale the state per key row,
-the P half's D pass scales D), no M1 (U reads the record), and a state write in both Z passes. Issued MMAs complete in issue order per issuer, in any interleaving
+each with its own barrier, that both halves read (the Z pass of chunk c rescales the state per key
+row with the slot of chunk c - 1, the outputs with that of the last chunk), no M1 (U reads the
+record), and a state write in both Z passes. Issued MMAs complete in issue order per issuer, in any interleaving
 between the two issuers; a commit fires when its issuer's earlier MMAs have completed.
 
 Every run checks for deadlock, for parity aliasing (the kernel waits on parities), and that each
@@ -319,13 +320,14 @@ def _run(nch, seed, mistake=None, out=False, kda=False):
             if c >= 1:
                 yield from wait(f"zfull{hf}", c - 1)
             if kda:
-                if hf == 0 or mistake != "kda_p_without_gready":
-                    yield from wait(f"gready{c % SL}", c // SL)
-                if hf == 0:
+                if c >= 1:
+                    yield from wait(f"gready{(c - 1) % SL}", (c - 1) // SL)
+                if hf == 0 and mistake != "no_wready_before_z":
                     yield from wait(f"wready{c & 1}", c >> 1)
                     if c >= 1 and c not in m["w_read"] and m["ZK0"] == ("W", c):
                         raise Hazard("Z copy written over W before its read-out")
-                yield from read_slot(hf, c, f"Z pass {hf}")
+                if c >= 1:
+                    yield from read_slot(hf, c - 1, f"Z pass {hf}")
             elif hf == 0:
                 yield from wait(f"m1ready{c & 1}", c >> 1)
                 if mistake != "no_wready_before_z":
@@ -346,8 +348,6 @@ def _run(nch, seed, mistake=None, out=False, kda=False):
             yield from wait(f"dfull{hf}", c)
             if m[f"D{hf}"] != ("d", c):
                 raise Hazard(f"D conversion {hf} at chunk {c} reads {m[f'D{hf}']}")
-            if kda and hf == 1:   # D_P scaled by e^{-m} of the chunk
-                yield from read_slot(hf, c, "D pass")
             touches_inflight([f"D{hf}"], True, "D conversion")
             m[f"D{hf}"] = ("Dbf", c)
             B[f"dready{hf}"].arrive()
@@ -356,8 +356,9 @@ def _run(nch, seed, mistake=None, out=False, kda=False):
             yield from wait(f"zfull{hf}", nch - 1)
             if m[f"Z{hf}"] != ("Z", nch - 1):
                 raise Hazard("output reads a stale state")
-            if kda and hf == 0:   # lam from the last chunk's slot
-                yield from read_slot(hf, nch - 1, "lam output")
+            if kda:   # the last chunk's scaling (and lam)
+                yield from wait(f"gready{(nch - 1) % SL}", (nch - 1) // SL)
+                yield from read_slot(hf, nch - 1, "output")
 
     # ---------------------------------------------------------------- output warps (out)
     # the P-half warps of the outputs instance: the masked Q K^T into the bf16 B operand of the
@@ -439,7 +440,7 @@ def test_kda_instance_protocol_interleavings(nch):
         assert _run(nch, seed, kda=True) == "ok"
 
 
-@pytest.mark.parametrize("mistake", ["kda_two_slots", "kda_p_without_gready"])
+@pytest.mark.parametrize("mistake", ["kda_two_slots", "no_wready_before_z", "w_before_dS_done"])
 def test_kda_instance_model_catches_planted_mistakes(mistake):
     hits = 0
     for seed in range(80):
@@ -482,7 +483,7 @@ def test_chain_protocol_model_catches_planted_mistakes(mistake):
 
 
 # The kernel source this model was last checked against (code only; comments do not count).
-MODELLED_SOURCE = ("build_gdn_tc.cu", "ae9bade53942")
+MODELLED_SOURCE = ("build_gdn_tc.cu", "aa1de184f466")
 
 
 def test_model_is_checked_against_the_current_kernel_source():

@@ -137,14 +137,18 @@ def sw128(row, byte):
 
 
 def test_kda_tile_pass_is_conflict_free():
-    """The KDA preparation's pass over a chunk: thread q (one key channel) reads element (t, q)
-    of the k tile and writes it into the three gated tiles, all 64 x 128 bf16 as two
-    128B-swizzled 64-channel halves of 8 KB, token by token: each warp-wide access is one
-    wavefront (two lanes per word)."""
+    """The KDA preparation's pass over a chunk: thread q takes the key channels 2 pc, 2 pc + 1
+    (pc = q % 64) over the token half q / 64 and reads, then writes, their bf16 pair (one word)
+    of the k tile and the three gated tiles, all 64 x 128 bf16 as two 128B-swizzled 64-channel
+    halves of 8 KB, token by token: each warp-wide access is one wavefront."""
     for w in range(4):
-        for t in range(64):
-            addrs = [(((32 * w + l) >> 6) * 8192 + sw128(t, 2 * ((32 * w + l) & 63))) // 4 for l in range(32)]
-            assert len(set(addrs)) == 16
+        for t in range(32):
+            addrs = []
+            for l in range(32):
+                q = 32 * w + l
+                pc, th = q & 63, q >> 6
+                addrs.append(((pc >> 5) * 8192 + sw128(32 * th + t, 4 * (pc & 31))) // 4)
+            assert len(set(addrs)) == 32
             assert wavefronts(addrs, 1) == 1
 
 
@@ -155,7 +159,7 @@ def test_planted_unswizzled_layout_conflicts():
 
 
 # The kernel source this model was last checked against (code only; comments do not count).
-MODELLED_SOURCE = ("build_gdn_prep.cu", "f12bf11e6580")
+MODELLED_SOURCE = ("build_gdn_prep.cu", "35a2cc300d12")
 
 
 def test_model_is_checked_against_the_current_kernel_source():
