@@ -47,7 +47,8 @@ CHUNK = 64
 L2_FLUSH_BYTES = 256 << 20
 
 # algorithmic work per token per value head of the chunked (C = 64) WY/UT GDN build:
-# gram 2Cd + W 2Cd + U 2Cd + X = W[S|P] 2d(2d) + state update 2d(2d)
+# gram 2Cd + W 2Cd + U 2Cd + X = W[S|P] 2d(2d) + state update 2d(2d); the channel-gated (KDA)
+# chunked build has the same products (its gram, of the gated keys, per value head)
 GDN_FLOP_PER_TOKEN_HEAD = 6 * CHUNK * 128 + 8 * 128 * 128   # 180,224
 # the exact sequential form (one thread per state column), per token per value head, d = 128:
 # the gate d^2 (a product per state element; KDA also on P), k^T z 2d^2 and the rank-1
@@ -333,7 +334,7 @@ def section_family(name, flush, peak, steps=20, warmup=3, oracle_budget_s=0.0):
     bk, ck = st.kernel_names()
     b_gbs, c_gbs = b_bytes / b_ms / 1e6, c_bytes / c_ms / 1e6
     extra = {}
-    if bk == "build_gdn_tc":   # tensor-bound: the chunked-form flops against the measured bf16 peak
+    if bk in ("build_gdn_tc", "build_kda_tc"):   # tensor-bound: the chunked-form flops against the bf16 peak
         tf = GDN_FLOP_PER_TOKEN_HEAD * n_tok * inp.H_v / (b_ms * 1e-3) / 1e12
         extra = {"build_tflops": round(tf, 1), "build_tensor_frac": round(tf / peak["bf16_tflops"], 4)}
     elif bk == "build_seq":    # fp32 CUDA-core bound: the sequential form against the FFMA peak

@@ -48,8 +48,10 @@
  *   DIAG             lam = sum_t log g_t (per key channel)      [seg][head][d_k]
  *   DELTA / GDN      lam = sum_t log a_t (0 for DELTA)          [seg][head]
  *                    P = prod_t (I - b_t k_t k_t^T), gate-free  [seg][head][d_k][d_k] fp32
- *   KDA              lam = sum_t max_i log a_t[i]              [seg][head]
+ *   KDA              lam = a log-scale that keeps P in range   [seg][head]
  *                    P = exp(-lam) T_C                          [seg][head][d_k][d_k] fp32
+ *                    (exact path: lam = sum_t max_i log a_t[i]; tensor-core path: the sum
+ *                    over 64-token chunks of max_i sum_{t in chunk} log a_t[i])
  *
  * Conventions shared by every call:
  *   - Ownership: the caller allocates and owns every buffer. The library allocates no
@@ -123,10 +125,12 @@ typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  *   P                 out DELTA / GDN / KDA: [n_seg][H_v][d_k][d_k] fp32; else NULL
  *   workspace         device scratch, at least hypic_build_workspace_bytes() bytes, 16-byte
  *                     aligned (NULL when that is 0). What it holds:
- *                     - DELTA / GDN with bf16 k, v and d = 128: 8 KB per (segment, value
- *                       head, 64-token chunk), the chunk matrices (I + Diag(b) L)^-1 Diag(b)
- *                       that the chain kernel reads back, and 256 bytes of work-distribution
- *                       counter set by the call itself.
+ *                     - DELTA / GDN / KDA with bf16 k, v and d = 128: 8 KB per (segment,
+ *                       value head, 64-token chunk), the chunk matrices (I + Diag(b) L)^-1
+ *                       Diag(b) that the chain kernel reads back, and 256 bytes of
+ *                       work-distribution counter set by the call itself; KDA adds 33,296
+ *                       bytes per chunk (its gated keys e^{c} k and e^{-c} k in bf16, and the
+ *                       chunk's per-channel log-decays).
  *                     - Any bf16, d = 128 build whose (segment, value head) units fill at most
  *                       half of the current device's SMs: each segment is built as up to 8
  *                       chunk-aligned pieces that are then composed back into its entry. A
@@ -153,8 +157,11 @@ typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  *                     out_seg_stride is.)
  *   The DeltaNet / GDN tensor-core build (bf16, d = 128) computes O itself: a second CTA per
  *   (segment, value head) runs the S half again with the outputs, and no segment is split
- *   into pieces. Every other call with O, every call with S_init and every KDA call runs the
- *   exact CUDA-core path (fp32 arithmetic).
+ *   into pieces. Every other call with O, every call with S_init, and KDA with fp32 inputs,
+ *   d < 128 or a log_gate pointer that is not 8-byte aligned runs the exact CUDA-core path
+ *   (fp32 arithmetic). KDA on the tensor cores supports chunks whose log-decay
+ *   sum_{t in chunk} log a_t[i] is at least -60 on every channel i (HYPIC_ERR_RANGE in the
+ *   device status otherwise), as GDN does for its scalar gate.
  */
 typedef struct {
     int32_t family;
@@ -252,7 +259,7 @@ hypic_status hypic_build_segments_static_ws(const hypic_build_args *args, void *
 hypic_status hypic_compose_scan(const hypic_compose_args *args, void *stream);
 
 /* Device scratch bytes hypic_build_segments needs for these arguments (host-only query;
- * reads the shapes and seg_offsets, never the tensors). 0 means no workspace; 0 also for
+ * reads the shapes, seg_offsets and, for KDA, the alignment of log_gate, never the tensors). 0 means no workspace; 0 also for
  * NULL or malformed arguments, which hypic_build_segments then rejects. */
 size_t hypic_build_workspace_bytes(const hypic_build_args *args);
 
@@ -284,7 +291,7 @@ const char *hypic_status_string(hypic_status status);
 
 /* Library ABI version (incremented on any change to the structs above or to the meaning of
  * their fields). 3: P_total needs lam_total and may carry a power-of-two scale. 4: KDA; the
- * build's q, O and S_init. */
+ * build's q, O and S_init. 5: KDA on the tensor cores (its workspace, its lam). */
 int32_t hypic_abi_version(void);
 
 #ifdef __cplusplus

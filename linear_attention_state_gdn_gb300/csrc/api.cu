@@ -303,7 +303,7 @@ bool compose_shape_ok(const hypic_compose_args *a) {
 
 extern "C" {
 
-int32_t hypic_abi_version(void) { return 4; }
+int32_t hypic_abi_version(void) { return 5; }
 
 const char *hypic_status_string(hypic_status s) {
     switch (s) {

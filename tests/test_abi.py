@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings_and_version(lib):
-    assert lib.hypic_abi_version() == 4
+    assert lib.hypic_abi_version() == 5
     assert lib.hypic_status_string(0) == b"ok"
     assert lib.hypic_status_string(2) == b"misaligned tensor pointer"
     assert lib.hypic_status_string(99) == b"unknown status"
