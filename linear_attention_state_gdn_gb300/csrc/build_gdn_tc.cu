@@ -203,6 +203,8 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
     __shared__ uint32_t tslot;
     __shared__ volatile int abort_flag;
     __shared__ float scan_tmp[2];
+    // outputs instance: exp(Lam_start + c_t), the outputs' scale, per gate slot
+    __shared__ __align__(16) float s_oscale[OUT ? kSlots : 1][C];
 
     const int warp = warp_id(), lane = lane_id();
     const int units = p.n_seg * p.H_v;
@@ -546,6 +548,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             const bool renorm = Lam + cC < kRenormBelow;
             const float lam0 = renorm ? 0.f : Lam;
             if (q < C) sl.ex[q] = expf(-lam0 - (q >= 32 ? x + scan_tmp[0] : x));
+            if (OUT && q < C) s_oscale[c % kSlots][q] = expf(lam0 + (q >= 32 ? x + scan_tmp[0] : x));
             if (q == 0) {
                 sl.renorm = renorm ? 1 : 0;
                 sl.rscale = expf(Lam);
@@ -614,7 +617,7 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
         // ---------------------------------------------------------------- output warps 4-7
         // Per chunk c: (a) the masked Q K^T (M = 64 accumulator: rows 16 (warp % 4) + lane in
         // lanes 0-15) -> bf16 rows t of the K-major B operand, columns s <= t; (b) the outputs,
-        // o_t[n] = O^T[n][t] / ex_t with ex_t = exp(-Lam - c_t) from the chunk's gate slot.
+        // o_t[n] = O^T[n][t] exp(Lam + c_t), the scale written with the chunk's gate slot.
         // The masked Q K^T of chunk c + 1 is prepared before the outputs of chunk c are read
         // out and stored, so that the S~ issuer's intra-chunk product of c + 1 does not wait
         // for chunk c's stores.
@@ -655,16 +658,15 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             tmem_ld_wait();
             // scaled with the chunk's gate slot before the accumulator is freed: freeing it
             // lets the next chunks run on, and the slot is rewritten four chunks later
-            const Slot &sl = slots[c % kSlots];
             {
-                const float4 *ex4 = reinterpret_cast<const float4 *>(sl.ex);
+                const float4 *os4 = reinterpret_cast<const float4 *>(s_oscale[c % kSlots]);
 #pragma unroll
                 for (int t4 = 0; t4 < C / 4; ++t4) {
-                    const float4 e = ex4[t4];
-                    z[4 * t4] = __float_as_uint(__fdividef(__uint_as_float(z[4 * t4]), e.x));
-                    z[4 * t4 + 1] = __float_as_uint(__fdividef(__uint_as_float(z[4 * t4 + 1]), e.y));
-                    z[4 * t4 + 2] = __float_as_uint(__fdividef(__uint_as_float(z[4 * t4 + 2]), e.z));
-                    z[4 * t4 + 3] = __float_as_uint(__fdividef(__uint_as_float(z[4 * t4 + 3]), e.w));
+                    const float4 e = os4[t4];
+                    z[4 * t4] = __float_as_uint(__uint_as_float(z[4 * t4]) * e.x);
+                    z[4 * t4 + 1] = __float_as_uint(__uint_as_float(z[4 * t4 + 1]) * e.y);
+                    z[4 * t4 + 2] = __float_as_uint(__uint_as_float(z[4 * t4 + 2]) * e.z);
+                    z[4 * t4 + 3] = __float_as_uint(__uint_as_float(z[4 * t4 + 3]) * e.w);
                 }
             }
             tc_fence_before();
