@@ -285,6 +285,10 @@ def test_path_of_kda_outputs_and_start_states(lib):
     assert lib.hypic_build_kernel_name(ctypes.byref(a)) == b"build_seq"
     assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == 0
     a = good_build(family=5)
+    a.log_gate = FAKE + 0x5000004                    # gates not 8-byte aligned: the exact path
+    assert lib.hypic_build_kernel_name(ctypes.byref(a)) == b"build_seq"
+    assert lib.hypic_build_workspace_bytes(ctypes.byref(a)) == 0
+    a = good_build(family=5)
     a.dtype = 1                                      # fp32 inputs: the exact path
     assert lib.hypic_build_kernel_name(ctypes.byref(a)) == b"build_seq"
     a = good_build(family=4)
