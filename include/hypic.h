@@ -89,7 +89,8 @@ typedef enum {
     HYPIC_ERR_UNSUPPORTED = 3,  /* valid request outside what is built (head size, dtype)   */
     HYPIC_ERR_RANGE = 4,        /* a gate outside the supported range (device-detected)     */
     HYPIC_ERR_CUDA = 5,         /* a CUDA runtime call failed (launch, attribute query)     */
-    HYPIC_ERR_TIMEOUT = 6       /* a kernel wait ran out of its iteration limit             */
+    HYPIC_ERR_TIMEOUT = 6,      /* a kernel wait ran out of its iteration limit             */
+    HYPIC_ERR_BOUNDS = 7        /* an index check failed (debug-bounds builds only)         */
 } hypic_status;
 
 typedef enum {
@@ -271,7 +272,9 @@ const char *hypic_build_kernel_name(const hypic_build_args *args);
 const char *hypic_compose_kernel_name(const hypic_compose_args *args);
 
 /* Synchronise `stream`, then read and clear the current device's status word: HYPIC_OK,
- * HYPIC_ERR_TIMEOUT or HYPIC_ERR_RANGE; HYPIC_ERR_CUDA if the synchronisation failed. */
+ * HYPIC_ERR_TIMEOUT or HYPIC_ERR_RANGE (HYPIC_ERR_BOUNDS, before both, in a library built with
+ * HYPIC_DEBUG_BOUNDS: an index check in a kernel failed and that kernel skipped the access and
+ * its remaining work); HYPIC_ERR_CUDA if the synchronisation failed. */
 hypic_status hypic_get_device_status(void *stream);
 
 /* Diagnostic for the kernels' failure path, so that it can be exercised on a GPU without
@@ -291,7 +294,8 @@ const char *hypic_status_string(hypic_status status);
 
 /* Library ABI version (incremented on any change to the structs above or to the meaning of
  * their fields). 3: P_total needs lam_total and may carry a power-of-two scale. 4: KDA; the
- * build's q, O and S_init. 5: KDA on the tensor cores (its workspace, its lam). */
+ * build's q, O and S_init. 5: KDA on the tensor cores (its workspace, its lam);
+ * HYPIC_ERR_BOUNDS. */
 int32_t hypic_abi_version(void);
 
 #ifdef __cplusplus

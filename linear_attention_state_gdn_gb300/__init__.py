@@ -19,7 +19,8 @@ import numpy as np
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libhypic.so")
+# HYPIC_LIBRARY selects another build of the library (the debug-bounds build libhypic_dbg.so)
+LIB_PATH = os.environ.get("HYPIC_LIBRARY") or os.path.join(_PKG, "libhypic.so")
 
 FAMILY = {"linear": 0, "scalar": 1, "diag": 2, "delta": 3, "gdn": 4, "kda": 5}
 DENSE = ("delta", "gdn", "kda")

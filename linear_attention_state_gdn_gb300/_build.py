@@ -16,6 +16,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhypic.so")
+# the debug-bounds build: every kernel's index checks compiled in (HYPIC_DEBUG_BOUNDS); a failing
+# check is reported as HYPIC_ERR_BOUNDS by hypic_get_device_status (no trap, no fault)
+OBJ_DBG = os.path.join(PKG, "_build_dbg")
+LIB_DBG = os.path.join(PKG, "libhypic_dbg.so")
 SOURCES = ["api.cu", "build_simt.cu", "compose.cu", "compose_tc.cu", "compose_cols.cu", "build_gated_tc.cu", "build_gdn_prep.cu",
            "build_gdn_tc.cu", "build_gdn_tc_out.cu", "build_gdn_tc_kda.cu"]
 HEADERS = [os.path.join(ROOT, "include", "hypic.h")]
@@ -56,10 +60,13 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(OBJ, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug_bounds: bool = False) -> str:
+    obj_dir, lib = (OBJ_DBG, LIB_DBG) if debug_bounds else (OBJ, LIB)
+    if debug_bounds:
+        extra_flags = list(extra_flags) + ["-DHYPIC_DEBUG_BOUNDS"]
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
-    stamp = os.path.join(OBJ, "flags.txt")   # objects built with other flags are rebuilt
+    stamp = os.path.join(obj_dir, "flags.txt")   # objects built with other flags are rebuilt
     flags = " ".join(NVCC_FLAGS + list(extra_flags) + sorted(RDC_SOURCES))
     if not os.path.exists(stamp) or open(stamp).read() != flags:
         force = True
@@ -67,7 +74,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     objs, jobs = [], []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(OBJ, src.replace(".cu", ".o"))
+        o = os.path.join(obj_dir, src.replace(".cu", ".o"))
         objs.append(o)
         deps = [s] + headers + [os.path.join(CSRC, d) for d in CU_DEPS.get(src, [])]
         if force or _stale(o, deps):
@@ -83,15 +90,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
-        run([cc, *ARCH, "-rdc=true", "-shared", "-o", tmp, *objs, "-Xlinker", "-soname,libhypic.so"])
-        os.replace(tmp, LIB)
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
+        run([cc, *ARCH, "-rdc=true", "-shared", "-o", tmp, *objs, "-Xlinker", "-soname," + os.path.basename(lib)])
+        os.replace(tmp, lib)
     with open(stamp, "w") as f:
         f.write(flags)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug_bounds="--debug-bounds" in sys.argv))

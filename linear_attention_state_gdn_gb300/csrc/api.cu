@@ -314,6 +314,7 @@ const char *hypic_status_string(hypic_status s) {
     case HYPIC_ERR_RANGE: return "gate outside the supported range";
     case HYPIC_ERR_CUDA: return "CUDA runtime error";
     case HYPIC_ERR_TIMEOUT: return "device wait timed out";
+    case HYPIC_ERR_BOUNDS: return "device index check failed";
     }
     return "unknown status";
 }
@@ -683,6 +684,7 @@ hypic_status hypic_get_device_status(void *stream) {
         if (cudaMemcpy(w, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
             return HYPIC_ERR_CUDA;
     }
+    if (v & kErrBounds) return HYPIC_ERR_BOUNDS;
     if (v & kErrTimeout) return HYPIC_ERR_TIMEOUT;
     if (v & kErrRange) return HYPIC_ERR_RANGE;
     return HYPIC_OK;

@@ -102,6 +102,7 @@ build_gated_tc_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     __shared__ float scan_tmp[2];
 
     const int warp = warp_id(), lane = lane_id();
+    if (!in_bounds((int)(blockIdx.x / p.H_v) < p.n_seg, p.err)) return;   // uniform, before any set-up
     const SegEntry seg = p.seg[blockIdx.x / p.H_v];
     const int h = blockIdx.x % p.H_v;
     const int hk = h / p.gqa;

@@ -252,6 +252,10 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         const int b = i & 1;
         const SegEntry seg = p.seg[cur.r];
         const int nch = nch_of(cur.r);
+        // every thread decodes the same unit: a failing check leaves the loop uniformly
+        if (!in_bounds(cur.c < nch && cur.h + R <= p.H_v &&
+                           (int64_t)seg.wsb + (int64_t)(cur.h + R - 1) * nch + cur.c < total, p.err))
+            break;
         if (q < R * C) vb[b][q / C][vbi(q & (C - 1))] = beta_cur;
         const float beta_next = load_beta(nxt);
         // gram(i) done: the k tile is free for the next record
@@ -516,6 +520,7 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         const SegEntry seg = p.seg[cur.r];
         const int nch = (seg.len + C - 1) / C;
         const int64_t rec = (int64_t)seg.wsb + (int64_t)cur.h * nch + cur.c;
+        if (!in_bounds(cur.c < nch && cur.h < p.H_v && rec < total, p.err)) break;   // uniform
         // (1) b of the unit; the pair's log-decay over this token half
         if (q < C) vb[vbi(q)] = beta_cur;
         {

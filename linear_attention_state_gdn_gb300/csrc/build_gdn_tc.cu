@@ -280,8 +280,15 @@ build_gdn_tc_kernel(const __grid_constant__ BuildParams p, const __grid_constant
             prefetch_tmap(&tmR);
             if (outm) prefetch_tmap(&tmQ);
             int c = 0, kc = 0, qc = 0;   // chunks whose {v, M2} / k / q loads were issued
+            const SegEntry &last = p.seg[p.n_seg - 1];
+            const int64_t records = (int64_t)last.wsb + (int64_t)p.H_v * ((last.len + C - 1) / C);
             for (; c < nch; ++c) {
                 const int32_t t0 = seg.start + c * C;
+                if (!in_bounds((int64_t)seg.wsb + (int64_t)h * nch + c < records &&
+                                   seg.start + (int64_t)c * C < (int64_t)p.n_tok, p.err)) {
+                    abort_flag = 1;   // the other roles give up their waits; the loads drain below
+                    break;
+                }
                 const int ks = c % kKSlots, kuse = c / kKSlots;
                 if (kuse >= 1 && !wait(&bars.kempty[ks], (kuse - 1) & 1)) break;
                 uint8_t *kt = smem + kOffK + ks * kKSl;

@@ -29,6 +29,7 @@ build_gated_simt_kernel(const __grid_constant__ BuildParams p) {
     __shared__ __align__(16) float vs[kGatedChunk][D];
     __shared__ __align__(16) float gs[kGatedChunk][D];
 
+    if (!in_bounds((int)(blockIdx.x / p.H_v) < p.n_seg, p.err)) return;
     const SegEntry seg = p.seg[blockIdx.x / p.H_v];
     const int h = blockIdx.x % p.H_v;
     const int hk = h / p.gqa;
@@ -159,6 +160,7 @@ build_seq_kernel(const __grid_constant__ BuildParams p) {
     const int halves = delta ? 2 : 1;
     const int ux = blockIdx.x / halves;                       // (segment rank, value head)
     const bool is_S = blockIdx.x % halves == 0;               // the S half, else the P half
+    if (!in_bounds(ux / p.H_v < p.n_seg, p.err)) return;      // uniform, before any set-up
     const SegEntry seg = p.seg[ux / p.H_v];
     const int h = ux % p.H_v;
     const int hk = h / p.gqa;

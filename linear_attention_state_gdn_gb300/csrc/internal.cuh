@@ -11,7 +11,7 @@
 namespace hypic {
 
 // Device status word bits (set by kernels, read by hypic_get_device_status).
-enum : unsigned { kErrTimeout = 1u, kErrRange = 2u };
+enum : unsigned { kErrTimeout = 1u, kErrRange = 2u, kErrBounds = 4u };
 
 // One segment of the launch table. The table is ordered longest first (LPT order:
 // "Hypic: Position-Independent KV Caching ..." episode companion, "Segment parallelism:
@@ -119,5 +119,17 @@ __device__ __forceinline__ float load_in(const void *base, int64_t idx, int dtyp
 __device__ __forceinline__ void raise_error(unsigned *err, unsigned bit) {
     if (err) atomicOr(err, bit);
 }
+
+// Index checks of a debug-bounds build (compiled with -DHYPIC_DEBUG_BOUNDS, in place of a memory
+// checker): a failing check sets kErrBounds in the status word and the caller skips the access
+// (and the work after it). In a release build every check is the constant true.
+#ifdef HYPIC_DEBUG_BOUNDS
+__device__ __forceinline__ bool in_bounds(bool ok, unsigned *err) {
+    if (!ok) raise_error(err, kErrBounds);
+    return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(bool, unsigned *) { return true; }
+#endif
 
 }  // namespace hypic

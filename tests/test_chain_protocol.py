@@ -483,7 +483,7 @@ def test_chain_protocol_model_catches_planted_mistakes(mistake):
 
 
 # The kernel source this model was last checked against (code only; comments do not count).
-MODELLED_SOURCE = ("build_gdn_tc.cu", "af2c6a89798e")
+MODELLED_SOURCE = ("build_gdn_tc.cu", "36b00f4cb906")
 
 
 def test_model_is_checked_against_the_current_kernel_source():
