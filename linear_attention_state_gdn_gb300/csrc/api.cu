@@ -9,6 +9,8 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.cuh"
 #include "ptx.cuh"
 
@@ -113,6 +115,15 @@ bool head_size_ok(int d_k, int d_v) {
 }
 
 hypic_status from_cuda(cudaError_t e) { return e == cudaSuccess ? HYPIC_OK : HYPIC_ERR_CUDA; }
+
+// A named NVTX range around an entry point: the call's launches show under its name in a
+// profiler's timeline; without a profiler attached the push and pop return at once.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 enum class BuildPath { None, GatedSimt, GatedTc, Seq, GdnTc };
 
@@ -330,6 +341,7 @@ size_t hypic_build_workspace_bytes(const hypic_build_args *a) {
 }
 
 hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
+    NvtxRange range("hypic_build_segments");
     if (!a) return HYPIC_ERR_INVALID_ARG;
     const int fam = a->family;
     if (fam < HYPIC_FAM_LINEAR || fam > HYPIC_FAM_KDA) return HYPIC_ERR_INVALID_ARG;
@@ -565,6 +577,7 @@ hypic_status hypic_build_segments_static_ws(const hypic_build_args *a, void *str
 }
 
 hypic_status hypic_compose_scan(const hypic_compose_args *a, void *stream) {
+    NvtxRange range("hypic_compose_scan");
     if (!a) return HYPIC_ERR_INVALID_ARG;
     const int fam = a->family;
     if (fam < HYPIC_FAM_LINEAR || fam > HYPIC_FAM_KDA) return HYPIC_ERR_INVALID_ARG;
