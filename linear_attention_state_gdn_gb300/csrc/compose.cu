@@ -6,7 +6,7 @@
 //
 // compose_scaled: scalar and diagonal transitions, T_j = exp(lam_j) (per unit or per row).
 //   A pure element-wise stream: each thread carries 4 consecutive state elements of one
-//   unit through all segments, with the next segments' S loads issued ahead.
+//   unit through all segments, the S loads (and log-scales) of up to 16 segments in flight.
 // compose_dense_simt: dense transitions T_j = exp(lam_j) P_j on CUDA cores, used for head
 //   sizes below 128 (the d = 128 case runs on the tensor cores, compose_tc.cu). With P_total
 //   requested, units U .. 2U-1 of the grid carry the transition chain P_j ... P_0 instead.
@@ -18,7 +18,7 @@ namespace hypic {
 namespace {
 
 constexpr int kScaledThreads = 256;
-constexpr int kAhead = 4;
+constexpr int kAhead = 16;   // segments whose S loads are in flight at once
 
 __device__ __forceinline__ float4 ldg_stream(const float *p) {
     float4 r;
@@ -50,22 +50,27 @@ compose_scaled_kernel(const __grid_constant__ ComposeParams p) {
     float4 cur = make_float4(0.f, 0.f, 0.f, 0.f);
     if (p.S0) cur = ldg_stream(p.S0 + u * DD + e4 * 4);
 
+    // a batch of up to kAhead segments: every S load of the batch is issued before the first is
+    // used (the scan is short: one memory latency per batch instead of one per few segments)
+    // (with the batch's log-scales: a load after a store of the loop below would wait for it)
     float4 ring[kAhead];
-#pragma unroll
-    for (int a = 0; a < kAhead; ++a)
-        if (a < p.n_seg) ring[a] = ldg_stream(p.S + ((int64_t)a * p.n_units + u) * DD + e4 * 4);
-
+    float lv[kAhead];
     for (int j0 = 0; j0 < p.n_seg; j0 += kAhead) {
 #pragma unroll
         for (int a = 0; a < kAhead; ++a) {
             const int j = j0 + a;
             if (j < p.n_seg) {
+                ring[a] = ldg_stream(p.S + ((int64_t)j * p.n_units + u) * DD + e4 * 4);
+                lv[a] = !has_lam ? 0.f
+                        : diag ? p.lam[((int64_t)j * p.n_units + u) * D + row] : p.lam[(int64_t)j * p.n_units + u];
+            }
+        }
+#pragma unroll
+        for (int a = 0; a < kAhead; ++a) {
+            const int j = j0 + a;
+            if (j < p.n_seg) {
                 const float4 x = ring[a];
-                const int jn = j + kAhead;
-                if (jn < p.n_seg) ring[a] = ldg_stream(p.S + ((int64_t)jn * p.n_units + u) * DD + e4 * 4);
-                float sc = 1.f;
-                if (has_lam) sc = expf(diag ? p.lam[((int64_t)j * p.n_units + u) * D + row]
-                                            : p.lam[(int64_t)j * p.n_units + u]);
+                const float sc = has_lam ? expf(lv[a]) : 1.f;
                 cur.x = fmaf(sc, cur.x, x.x);
                 cur.y = fmaf(sc, cur.y, x.y);
                 cur.z = fmaf(sc, cur.z, x.z);
