@@ -212,9 +212,9 @@ int seg_pieces(int64_t len, int m) {
     return (int)std::max<int64_t>(1, std::min<int64_t>(m, nch));
 }
 
-// Workspace of the split: piece outputs S, P (dense families only) [slots][H_v][d][d], lam
-// [slots][H_v] ([slots][H_v][d] for diagonal gates; rounded to 256 bytes), and for the scaled
-// families one scan buffer [max pieces][H_v][d][d] for the composition.
+// Workspace of the split: piece outputs S, P (dense families only) [slots][H_v][d][d] and lam
+// [slots][H_v] ([slots][H_v][d] for diagonal gates). The pieces are composed straight into the
+// outputs (the last state, the summed lam and, dense, the product).
 //
 // A second, narrower case: a DeltaNet / GDN call whose units take several rounds of SMs with
 // a last round at most half full (16 segments x 32 heads on 152 SMs: 56 units in round four).
@@ -224,7 +224,7 @@ int seg_pieces(int64_t len, int m) {
 struct SplitLayout {
     int m = 1, slots = 0, max_pieces = 1;
     int tail_first = -1, tail_count = 0;   // batched halving of segments [first, first + count)
-    size_t off_S = 0, off_P = 0, off_lam = 0, off_prefix = 0, bytes = 0;
+    size_t off_S = 0, off_P = 0, off_lam = 0, bytes = 0;
     int pieces(const hypic_build_args *a, int j) const {
         if (tail_count > 0) return j >= tail_first && j < tail_first + tail_count ? 2 : 1;
         return m > 1 ? seg_pieces(a->seg_offsets[j + 1] - a->seg_offsets[j], m) : 1;
@@ -262,14 +262,12 @@ int gdn_tail_split(const hypic_build_args *a, int *first) {
 SplitLayout gdn_split_layout(const hypic_build_args *a, size_t base) {
     SplitLayout L;
     L.m = gdn_split_m(a);
-    size_t prefix_units = 0;
     if (L.m <= 1) {
         L.m = 1;
         L.tail_count = gdn_tail_split(a, &L.tail_first);
         if (L.tail_count == 0) return L;
         L.slots = 2 * L.tail_count;
         L.max_pieces = 2;
-        prefix_units = (size_t)L.slots * a->H_v;
     } else {
         for (int j = 0; j < a->n_seg; ++j) {
             const int pj = seg_pieces(a->seg_offsets[j + 1] - a->seg_offsets[j], L.m);
@@ -282,7 +280,6 @@ SplitLayout gdn_split_layout(const hypic_build_args *a, size_t base) {
             L.m = 1;
             return L;
         }
-        prefix_units = (size_t)L.max_pieces * a->H_v;
     }
     const size_t unit = (size_t)a->d_k * a->d_k * sizeof(float);
     const size_t su = (size_t)L.slots * a->H_v;
@@ -291,10 +288,7 @@ SplitLayout gdn_split_layout(const hypic_build_args *a, size_t base) {
     L.off_S = base;
     L.off_P = L.off_S + su * unit;
     L.off_lam = L.off_P + (dense ? su * unit : 0);
-    L.off_prefix = L.off_lam + ((su * nl * sizeof(float) + 255) & ~(size_t)255);
-    // dense pieces are composed straight into the outputs; only the scaled compose needs a
-    // scan buffer
-    L.bytes = L.off_prefix + (dense ? 0 : prefix_units * unit) - base;
+    L.bytes = L.off_lam + ((su * nl * sizeof(float) + 255) & ~(size_t)255) - base;
     return L;
 }
 
@@ -504,7 +498,6 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
         const size_t unit = (size_t)a->d_k * a->d_k;
         const size_t nl = fam == HYPIC_FAM_DIAG ? (size_t)a->d_k : 1;
         const int64_t stride = p.seg_stride;
-        float *prefix = reinterpret_cast<float *>(static_cast<uint8_t *>(a->workspace) + split.off_prefix);
         if (split.tail_count > 0) {   // one launch for all halved segments (adjacent outputs)
             const int64_t nu = (int64_t)split.tail_count * a->H_v;
             ComposeParams q;
@@ -535,20 +528,12 @@ hypic_status hypic_build_segments(const hypic_build_args *a, void *stream) {
             q.S = p.S_piece + (size_t)slot0 * a->H_v * unit;
             q.lam = p.lam_piece + (size_t)slot0 * a->H_v * nl;
             q.P = dense ? p.P_piece + (size_t)slot0 * a->H_v * unit : nullptr;
-            q.prefix = prefix;
             q.lam_total = a->lam + (size_t)j * stride * nl;
             q.P_total = dense ? a->P + (size_t)j * stride * unit : nullptr;
             q.err = err;
-            if (dense) {   // one launch: the last state straight into S, lam_total summed inside
-                q.prefix_last = a->S + (size_t)j * stride * unit;
-                e = launch_compose_dense_tc(q, s);
-            } else {
-                e = launch_compose_scaled(q, s);
-                if (e == cudaSuccess) e = launch_compose_lam_total(q, s);
-                if (e == cudaSuccess)
-                    e = cudaMemcpyAsync(a->S + (size_t)j * stride * unit, prefix + (size_t)(pj - 1) * a->H_v * unit,
-                                        (size_t)a->H_v * unit * sizeof(float), cudaMemcpyDeviceToDevice, s);
-            }
+            // one launch: the last state straight into S, lam_total summed inside
+            q.prefix_last = a->S + (size_t)j * stride * unit;
+            e = dense ? launch_compose_dense_tc(q, s) : launch_compose_scaled(q, s);
             slot0 += pj;
         }
         return from_cuda(e);
@@ -645,8 +630,10 @@ hypic_status hypic_compose_scan(const hypic_compose_args *a, void *stream) {
     case ComposePath::Scaled: e = launch_compose_scaled(p, s); break;
     case ComposePath::None: break;
     }
-    // the dense tensor-core kernel sums lam_total itself
-    if (e == cudaSuccess && a->lam_total && pick_compose(a) != ComposePath::DenseTc) e = launch_compose_lam_total(p, s);
+    // the dense tensor-core and the scaled kernels sum lam_total themselves (when they run)
+    const ComposePath path = pick_compose(a);
+    if (e == cudaSuccess && a->lam_total && path != ComposePath::DenseTc && path != ComposePath::Scaled)
+        e = launch_compose_lam_total(p, s);
     return from_cuda(e);
 }
 

@@ -121,6 +121,9 @@ build_gated_tc_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         mbar_init(&bars.fin, 1);
         abort_flag = 0;
         fence_mbar_init();
+        // the kernel after this one (the merge of split segments) may launch and set up on SMs
+        // this grid has left; it waits for this grid's completion before any access
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     }
     if (warp == 0) tmem_alloc(&tslot, kTmemCols);
     tc_fence_before();

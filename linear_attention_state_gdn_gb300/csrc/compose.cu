@@ -7,6 +7,10 @@
 // compose_scaled: scalar and diagonal transitions, T_j = exp(lam_j) (per unit or per row).
 //   A pure element-wise stream: each thread carries 4 consecutive state elements of one
 //   unit through all segments, the S loads (and log-scales) of up to 16 segments in flight.
+//   It also sums lam_total when asked (the first thread of each unit, or of each row for
+//   diagonal gates) and, with prefix_last (a build composing the pieces of its segments),
+//   writes only the last state. It is a programmatic dependent launch: it waits for the
+//   kernel before it on the stream (the build of the pieces) before any global access.
 // compose_dense_simt: dense transitions T_j = exp(lam_j) P_j on CUDA cores, used for head
 //   sizes below 128 (the d = 128 case runs on the tensor cores, compose_tc.cu). With P_total
 //   requested, units U .. 2U-1 of the grid carry the transition chain P_j ... P_0 instead.
@@ -36,6 +40,7 @@ __device__ __forceinline__ void stg_stream(float *p, float4 v) {
 
 __global__ void __launch_bounds__(kScaledThreads)
 compose_scaled_kernel(const __grid_constant__ ComposeParams p) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int D = p.D;
     const int n4 = D * D / 4;
     const int bpu = (n4 + kScaledThreads - 1) / kScaledThreads;   // blocks per unit
@@ -55,6 +60,7 @@ compose_scaled_kernel(const __grid_constant__ ComposeParams p) {
     // (with the batch's log-scales: a load after a store of the loop below would wait for it)
     float4 ring[kAhead];
     float lv[kAhead];
+    float lsum = 0.f;
     for (int j0 = 0; j0 < p.n_seg; j0 += kAhead) {
 #pragma unroll
         for (int a = 0; a < kAhead; ++a) {
@@ -71,13 +77,20 @@ compose_scaled_kernel(const __grid_constant__ ComposeParams p) {
             if (j < p.n_seg) {
                 const float4 x = ring[a];
                 const float sc = has_lam ? expf(lv[a]) : 1.f;
+                lsum += lv[a];
                 cur.x = fmaf(sc, cur.x, x.x);
                 cur.y = fmaf(sc, cur.y, x.y);
                 cur.z = fmaf(sc, cur.z, x.z);
                 cur.w = fmaf(sc, cur.w, x.w);
-                stg_stream(p.prefix + ((int64_t)j * p.n_units + u) * DD + e4 * 4, cur);
+                if (!p.prefix_last)
+                    stg_stream(p.prefix + ((int64_t)j * p.n_units + u) * DD + e4 * 4, cur);
             }
         }
+    }
+    if (p.prefix_last) stg_stream(p.prefix_last + u * DD + e4 * 4, cur);
+    if (p.lam_total) {   // the segments' lam in order, as compose_lam_total sums them
+        if (diag && (e4 * 4) % D == 0) p.lam_total[u * D + row] = lsum;
+        if (!diag && e4 == 0) p.lam_total[u] = lsum;
     }
 }
 
@@ -196,9 +209,16 @@ cudaError_t launch_dense(const ComposeParams &p, cudaStream_t s) {
 cudaError_t launch_compose_scaled(const ComposeParams &p, cudaStream_t s) {
     if (p.n_seg == 0 || p.n_units == 0) return cudaSuccess;
     const int n4 = p.D * p.D / 4;
-    dim3 grid((unsigned)(p.n_units * ((n4 + kScaledThreads - 1) / kScaledThreads)));
-    compose_scaled_kernel<<<grid, kScaledThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.n_units * ((n4 + kScaledThreads - 1) / kScaledThreads)));
+    cfg.blockDim = dim3(kScaledThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, compose_scaled_kernel, p);
 }
 
 cudaError_t launch_compose_lam_total(const ComposeParams &p, cudaStream_t s) {
