@@ -219,3 +219,88 @@ def materialize_T(family, lam, P=None, d_k=None):
     if rc != 0:
         raise RuntimeError(f"oracle_materialize_T failed ({rc})")
     return out
+
+
+# ------------------------------------------------------------------ convolution-state warm-up
+# "Cut First-Token Latency by 3.25x: Introducing HYPIC ..." (besthub.dev), paragraph "For linear
+# layers": for convolutional variants HYPIC adds a "convolution state warm-up" patch to keep
+# cached segments aligned. The pages do not define the convolution; the reading here is the
+# short convolution of the Gated DeltaNet layer ("Gated Delta Networks: Improving Mamba2 with
+# Delta Rule", reference 7 of the episode-companion page): a causal depthwise convolution of
+# width K over the token axis, then SiLU, on k and v, with k L2-normalised per token and head
+# afterwards for the delta-rule families. A segment's tokens from K-1 on have their whole
+# window inside the segment, so their entry (the "rest") is position-independent and cached; the
+# first K-1 tokens (the "head") see the preceding segment's last raw tokens and are rebuilt in
+# context, then composed before the rest: T = T_rest T_head, S = T_rest S_head + S_rest.
+
+DELTA_FAMILIES = ("delta", "gdn", "kda")
+
+
+def silu(x):
+    """x * sigmoid(x), fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / (1.0 + np.exp(-x))
+
+
+def short_conv(x, w, start=0, stop=None, normalize=False):
+    """The convolved (then SiLU, then optionally L2-normalised) value of tokens [start, stop) of
+    a token stream x [N, H, D]: y[t, h, c] = silu(sum_{tau < K} w[h D + c, tau] x[t - K + 1 + tau,
+    h, c]), with x taken as 0 before token 0. w [H D, K] fp64 (tap K-1 on the token itself).
+    Returns [stop - start, H, D]. Plain loops over taps and tokens."""
+    x = _f64(x)
+    w = _f64(w)
+    N, H, D = x.shape
+    K = w.shape[1]
+    stop = N if stop is None else stop
+    out = np.zeros((stop - start, H, D))
+    wk = w.reshape(H, D, K)
+    for t in range(start, stop):
+        acc = np.zeros((H, D))
+        for tau in range(K):
+            s = t - (K - 1) + tau
+            if s >= 0:
+                acc += wk[:, :, tau] * x[s]
+        y = silu(acc)
+        if normalize:
+            n = np.sqrt((y * y).sum(axis=1, keepdims=True))
+            y = np.where(n > 0, y / np.where(n > 0, n, 1.0), 0.0)
+        out[t - start] = y
+    return out
+
+
+def head_lengths(seg_offsets, K):
+    """Tokens of each segment rebuilt in context: min(K - 1, length)."""
+    offs = np.asarray(seg_offsets, dtype=np.int64)
+    return np.minimum(K - 1, offs[1:] - offs[:-1])
+
+
+def conv_warmup(family, seg_offsets, k_raw, v_raw, wk, wv, K, S_rest, lam_rest, P_rest=None,
+                log_gate=None, log_gamma=None, beta=None):
+    """Entries of the prompt's segments in context, from the cached entries of their rests,
+    fp64. k_raw [N, H_k, d], v_raw [N, H_v, d]: the prompt's raw (pre-convolution) inputs in
+    order; wk [H_k d, K], wv [H_v d, K]; log_gate / log_gamma / beta as for build_segments, over
+    the prompt's tokens; S_rest [n_seg, H_v, d, d], lam_rest, P_rest: the entries of each
+    segment's tokens from its head length on. Returns (S [n_seg, H_v, d, d], T [n_seg, H_v, d, d])
+    with T dense."""
+    fam = family
+    offs = np.asarray(seg_offsets, dtype=np.int64)
+    n_seg = len(offs) - 1
+    hl = head_lengths(offs, K)
+    # 1. the heads' tokens, convolved over the prompt's stream (their windows reach back into
+    #    the preceding segment), and their gates
+    rows = [int(offs[j]) + i for j in range(n_seg) for i in range(int(hl[j]))]
+    Hk, Hv, d = k_raw.shape[1], v_raw.shape[1], v_raw.shape[2]
+    kh = np.zeros((len(rows), Hk, d))
+    vh = np.zeros((len(rows), Hv, d))
+    for r, t in enumerate(rows):
+        kh[r] = short_conv(k_raw, wk, t, t + 1, normalize=fam in DELTA_FAMILIES)[0]
+        vh[r] = short_conv(v_raw, wv, t, t + 1)[0]
+    pick = lambda a: None if a is None else _f64(a)[rows]
+    head_offs = np.concatenate([[0], np.cumsum(hl)]).astype(np.int64)
+    # 2. the heads' entries (from a zero state)
+    S_h, T_h = build_segments(fam, head_offs, kh, vh, pick(log_gate), log_gamma, pick(beta))
+    # 3. composed before the rests
+    T_r = materialize_T(fam, lam_rest, P_rest, d_k=d)
+    S = np.einsum("suij,sujk->suik", T_r, S_h) + _f64(S_rest)
+    T = np.einsum("suij,sujk->suik", T_r, T_h)
+    return S, T

@@ -587,3 +587,90 @@ def test_outputs_after_a_prefix_state_are_corrected_by_the_transition(family):
         for h in range(4):
             np.testing.assert_allclose(dO[t, h], (T[0, h] @ S0[0, h]).T @ q[t, h // 2],
                                        rtol=1e-10, atol=1e-12)
+
+
+# ------------------------------------------------------------------ convolution-state warm-up
+
+def _conv_case(family, lens, K, seed, d=6, H_k=1, H_v=2):
+    rng = np.random.default_rng(seed)
+    inp = synth.make_inputs(family, H_k, H_v, d, lens, torch.float64, seed=seed, alpha_scale=0.3,
+                            gla_div=4.0, k_scale=0.7)
+    k_raw, v_raw = inp.k.numpy(), inp.v.numpy()
+    wk = rng.standard_normal((H_k * d, K)) * 0.6
+    wv = rng.standard_normal((H_v * d, K)) * 0.6
+    f = lambda t: None if t is None else t.numpy()
+    return inp, k_raw, v_raw, wk, wv, f(inp.log_gate), f(inp.log_gamma), f(inp.beta)
+
+
+def _segment_local_conv(x, w, offs, normalize):
+    """Each segment convolved on its own (zeros before its first token): the values a cached
+    segment was built from."""
+    return np.concatenate([oracle.short_conv(x[offs[j]:offs[j + 1]], w, normalize=normalize)
+                           for j in range(len(offs) - 1)])
+
+
+def test_short_conv_is_numpy_convolve_then_silu():
+    rng = np.random.default_rng(170)
+    x = rng.standard_normal((11, 2, 3))
+    w = rng.standard_normal((6, 4))
+    y = oracle.short_conv(x, w)
+    for h in range(2):
+        for c in range(3):
+            ref = np.convolve(x[:, h, c], w[h * 3 + c, ::-1])[:11]
+            np.testing.assert_allclose(y[:, h, c], ref / (1 + np.exp(-ref)), rtol=1e-13, atol=1e-14)
+    yn = oracle.short_conv(x, w, normalize=True)
+    np.testing.assert_allclose(np.linalg.norm(yn, axis=2), 1.0, rtol=1e-13)
+    np.testing.assert_allclose(oracle.short_conv(x, w, 4, 9), y[4:9], rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("family", ["linear", "scalar", "diag", "delta", "gdn", "kda"])
+@pytest.mark.parametrize("K", [2, 4])
+def test_conv_warmup_is_recomputation_of_the_whole_prompt(family, K):
+    """The defining property: each segment's entry from its cached rest plus the head rebuilt
+    in context equals the entry built from the whole prompt convolved in one pass (segments of
+    length 0, 1 and below K - 1 included)."""
+    lens = [9, 1, 0, 2, 7, 12]
+    inp, k_raw, v_raw, wk, wv, lg, lgam, beta = _conv_case(family, lens, K, seed=171 + K)
+    offs = inp.seg_offsets
+    delta = family in oracle.DELTA_FAMILIES
+    # the cached rests: each segment convolved alone, its tokens from the head length on
+    kl = _segment_local_conv(k_raw, wk, offs, delta)
+    vl = _segment_local_conv(v_raw, wv, offs, False)
+    hl = oracle.head_lengths(offs, K)
+    rest = [(int(offs[j] + hl[j]), int(offs[j + 1])) for j in range(len(lens))]
+    keep = np.concatenate([np.arange(a, b) for a, b in rest]).astype(np.int64)
+    r_offs = np.concatenate([[0], np.cumsum([b - a for a, b in rest])]).astype(np.int64)
+    g = lambda a: None if a is None else a[keep]
+    S_r, T_r = oracle.build_segments(family, r_offs, kl[keep], vl[keep], g(lg), lgam, g(beta))
+    # (lam, P) of the rests as the library stores them: here lam = 0 and P = T (any pair with
+    # exp(lam) P = T is an entry)
+    d = v_raw.shape[2]
+    if family in ("delta", "gdn", "kda"):
+        lam_r, P_r = np.zeros(S_r.shape[:2]), T_r
+    elif family == "diag":
+        lam_r, P_r = np.log(np.diagonal(T_r, axis1=2, axis2=3)), None
+    elif family == "scalar":
+        lam_r, P_r = np.log(T_r[:, :, 0, 0]), None
+    else:
+        lam_r, P_r = np.zeros(S_r.shape[:2]), None
+    S, T = oracle.conv_warmup(family, offs, k_raw, v_raw, wk, wv, K, S_r, lam_r, P_r, lg, lgam, beta)
+    kf = oracle.short_conv(k_raw, wk, normalize=delta)
+    vf = oracle.short_conv(v_raw, wv)
+    S_w, T_w = oracle.build_segments(family, offs, kf, vf, lg, lgam, beta)
+    np.testing.assert_allclose(S, S_w, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(T, T_w, rtol=1e-10, atol=1e-12)
+    # the pin is sensitive to the window: segment-local heads (a zero convolution state) differ
+    S_0, _ = oracle.build_segments(family, offs, kl, vl, lg, lgam, beta)
+    assert max(np.abs(S_0[j] - S_w[j]).max() for j in (3, 4, 5)) > 1e-3
+
+
+def test_conv_warmup_without_window_is_the_rest():
+    """K = 1: no token sees another, the heads are empty and the entry is the cached one."""
+    inp, k_raw, v_raw, wk, wv, lg, lgam, beta = _conv_case("gdn", [5, 3], 1, seed=175)
+    S_r = np.random.default_rng(1).standard_normal((2, 2, 6, 6))
+    P_r = np.random.default_rng(2).standard_normal((2, 2, 6, 6))
+    lam_r = np.full((2, 2), -0.5)
+    S, T = oracle.conv_warmup("gdn", inp.seg_offsets, k_raw, v_raw, wk, wv, 1, S_r, lam_r, P_r, lg,
+                              lgam, beta)
+    np.testing.assert_allclose(S, S_r, rtol=0, atol=0)
+    np.testing.assert_allclose(T, np.exp(-0.5) * P_r, rtol=1e-15)
