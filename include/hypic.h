@@ -259,6 +259,69 @@ hypic_status hypic_build_segments_static_ws(const hypic_build_args *args, void *
  * d = 128 call takes one CTA per unit. */
 hypic_status hypic_compose_scan(const hypic_compose_args *args, void *stream);
 
+/* ---------------------------------------------------------------- convolution-state warm-up
+ * "Cut First-Token Latency by 3.25x: Introducing HYPIC ..." (besthub.dev), paragraph "For linear
+ * layers": for convolutional variants HYPIC adds a "convolution state warm-up" patch. The pages
+ * do not define the convolution; this library reads it as the short convolution of the Gated
+ * DeltaNet layer ("Gated Delta Networks: Improving Mamba2 with Delta Rule", reference 7 of the
+ * episode-companion page): per channel, a causal convolution of width K over the tokens,
+ *     y_t[c] = silu(sum_{tau < K} w[c][tau] x_{t-K+1+tau}[c]),   silu(z) = z / (1 + e^-z),
+ * on the raw keys and values (x taken as 0 before the prompt's first token), the keys then
+ * L2-normalised per token and head for DELTA / GDN / KDA. A segment's tokens from min(K - 1,
+ * length) on (its "rest") have their whole window inside the segment: their entry is
+ * position-independent and is what a cache of a convolutional layer keeps (build it with
+ * hypic_build_segments from the segment's own convolution, over the offsets shifted by the
+ * head length). On reuse, the first min(K - 1, length) tokens (the "head") see the raw tokens
+ * of the segment before in this prompt, so the call rebuilds them in context and composes the
+ * head before the rest (T = T_rest T_head, S = T_rest S_head + S_rest), every segment at once:
+ * a convolution kernel for the heads' tokens, the exact (fp32) build of the heads, and one
+ * composition launch with totals.
+ *
+ *   family, dtype, n_seg, H_k, H_v, d_k, d_v   as in hypic_build_args (dtype of k_raw, v_raw)
+ *   conv_k         K, the convolution's width, 1 <= K <= 8 (K = 1: empty heads)
+ *   seg_offsets    HOST [n_seg + 1] int64: this prompt's segments, in order
+ *   k_raw, v_raw   [N_tok][H_k][d_k], [N_tok][H_v][d_v] dtype, 16-byte aligned: the raw inputs
+ *                  of the convolution for the whole prompt
+ *   conv_wk, conv_wv  [H_k d_k][K], [H_v d_v][K] fp32, 4-byte aligned: the taps, tap K - 1 on
+ *                  the token itself
+ *   log_gate, log_gamma, beta   as in hypic_build_args, over the prompt's tokens
+ *   S_rest, lam_rest, P_rest    the rests' cached entries, layouts of hypic_build_args' S,
+ *                  lam, P with segment stride H_v (P_rest: DELTA / GDN / KDA only)
+ *   S, lam, P      out: the segments' entries in this context, the same layouts; they may not
+ *                  overlap any input
+ *   workspace      at least hypic_warmup_workspace_bytes() bytes, 16-byte aligned
+ * Errors: those of hypic_build_segments and hypic_compose_scan; K outside [1, 8] or a missing
+ * rest entry is HYPIC_ERR_INVALID_ARG. Asynchronous on `stream`. */
+typedef struct {
+    int32_t family;
+    int32_t dtype;
+    int32_t n_seg;
+    int32_t H_k;
+    int32_t H_v;
+    int32_t d_k;
+    int32_t d_v;
+    int32_t conv_k;
+    const int64_t *seg_offsets;
+    const void *k_raw;
+    const void *v_raw;
+    const float *conv_wk;
+    const float *conv_wv;
+    const float *log_gate;
+    const float *log_gamma;
+    const float *beta;
+    const float *S_rest;
+    const float *lam_rest;
+    const float *P_rest;
+    float *S;
+    float *lam;
+    float *P;
+    void *workspace;
+    size_t workspace_bytes;
+} hypic_warmup_args;
+
+size_t hypic_warmup_workspace_bytes(const hypic_warmup_args *args);
+hypic_status hypic_conv_warmup(const hypic_warmup_args *args, void *stream);
+
 /* Device scratch bytes hypic_build_segments needs for these arguments (host-only query;
  * reads the shapes, seg_offsets and, for KDA, the alignment of log_gate, never the tensors). 0 means no workspace; 0 also for
  * NULL or malformed arguments, which hypic_build_segments then rejects. */
@@ -295,7 +358,7 @@ const char *hypic_status_string(hypic_status status);
 /* Library ABI version (incremented on any change to the structs above or to the meaning of
  * their fields). 3: P_total needs lam_total and may carry a power-of-two scale. 4: KDA; the
  * build's q, O and S_init. 5: KDA on the tensor cores (its workspace, its lam);
- * HYPIC_ERR_BOUNDS. */
+ * HYPIC_ERR_BOUNDS; the convolution-state warm-up (hypic_warmup_args). */
 int32_t hypic_abi_version(void);
 
 #ifdef __cplusplus

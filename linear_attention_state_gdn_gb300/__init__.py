@@ -57,6 +57,18 @@ class ComposeArgs(ctypes.Structure):
                 ("lam_total", ctypes.c_void_p), ("P_total", ctypes.c_void_p)]
 
 
+class WarmupArgs(ctypes.Structure):
+    _fields_ = [("family", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("n_seg", ctypes.c_int32), ("H_k", ctypes.c_int32), ("H_v", ctypes.c_int32),
+                ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32), ("conv_k", ctypes.c_int32),
+                ("seg_offsets", ctypes.c_void_p), ("k_raw", ctypes.c_void_p), ("v_raw", ctypes.c_void_p),
+                ("conv_wk", ctypes.c_void_p), ("conv_wv", ctypes.c_void_p), ("log_gate", ctypes.c_void_p),
+                ("log_gamma", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("S_rest", ctypes.c_void_p),
+                ("lam_rest", ctypes.c_void_p), ("P_rest", ctypes.c_void_p), ("S", ctypes.c_void_p),
+                ("lam", ctypes.c_void_p), ("P", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -89,6 +101,10 @@ def load_library(path: str = LIB_PATH):
                 f.restype = ctypes.c_char_p
             lib.hypic_probe_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
             lib.hypic_probe_wait_timeout.restype = ctypes.c_int
+            lib.hypic_warmup_workspace_bytes.argtypes = [ctypes.POINTER(WarmupArgs)]
+            lib.hypic_warmup_workspace_bytes.restype = ctypes.c_size_t
+            lib.hypic_conv_warmup.argtypes = [ctypes.POINTER(WarmupArgs), ctypes.c_void_p]
+            lib.hypic_conv_warmup.restype = ctypes.c_int
             lib.hypic_abi_version.argtypes = []
             lib.hypic_abi_version.restype = ctypes.c_int32
             _lib = lib
@@ -228,6 +244,61 @@ def hypic_build_segments_static_ws(family, k, v, seg_offsets, log_gate=None, log
 
 
 STATIC_WS_BYTES = 64 << 20   # HYPIC_STATIC_WS_BYTES in include/hypic.h
+
+
+def make_warmup_args(family, seg_offsets, k_raw, v_raw, conv_wk, conv_wv, S_rest, lam_rest,
+                     P_rest=None, log_gate=None, log_gamma=None, beta=None, S=None, lam=None,
+                     P=None, workspace=None):
+    """Fill a WarmupArgs struct (and keep the host offsets array alive with it)."""
+    offs = _offsets(seg_offsets)
+    a = WarmupArgs()
+    a.family = FAMILY[family] if isinstance(family, str) else int(family)
+    a.dtype = DTYPE[k_raw.dtype]
+    a.n_seg = len(offs) - 1
+    a.H_k, a.d_k = k_raw.shape[1], k_raw.shape[2]
+    a.H_v, a.d_v = v_raw.shape[1], v_raw.shape[2]
+    a.conv_k = conv_wk.shape[1]
+    a.seg_offsets = offs.ctypes.data
+    a.k_raw, a.v_raw = _ptr(k_raw), _ptr(v_raw)
+    a.conv_wk, a.conv_wv = _ptr(conv_wk), _ptr(conv_wv)
+    a.log_gate, a.log_gamma, a.beta = _ptr(log_gate), _ptr(log_gamma), _ptr(beta)
+    a.S_rest, a.lam_rest, a.P_rest = _ptr(S_rest), _ptr(lam_rest), _ptr(P_rest)
+    a.S, a.lam, a.P = _ptr(S), _ptr(lam), _ptr(P)
+    if workspace is not None:
+        a.workspace, a.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    a._keep = offs
+    return a
+
+
+def hypic_warmup_workspace_bytes(family, seg_offsets, k_raw, v_raw, conv_wk, conv_wv, S_rest,
+                                 lam_rest, **kw) -> int:
+    lib = load_library()
+    a = make_warmup_args(family, seg_offsets, k_raw, v_raw, conv_wk, conv_wv, S_rest, lam_rest, **kw)
+    return int(lib.hypic_warmup_workspace_bytes(ctypes.byref(a)))
+
+
+def hypic_conv_warmup(family, seg_offsets, k_raw, v_raw, conv_wk, conv_wv, S_rest, lam_rest,
+                      P_rest=None, log_gate=None, log_gamma=None, beta=None, S=None, lam=None,
+                      P=None, workspace=None, stream=None):
+    """Entries (S, lam, P) of this prompt's segments in context, from the cached entries of
+    their rests (each segment's tokens from min(K - 1, length) on) and the raw, pre-convolution
+    k_raw [N, H_k, d], v_raw [N, H_v, d] of the whole prompt; conv_wk [H_k d, K] and
+    conv_wv [H_v d, K] fp32 are the short convolution's taps. Outputs are allocated when not
+    given (shapes of S_rest, lam_rest, P_rest). Asynchronous on `stream`."""
+    lib = load_library()
+    if S is None:
+        S, lam = torch.empty_like(S_rest), torch.empty_like(lam_rest)
+        P = None if P_rest is None else torch.empty_like(P_rest)
+    a = make_warmup_args(family, seg_offsets, k_raw, v_raw, conv_wk, conv_wv, S_rest, lam_rest,
+                         P_rest, log_gate, log_gamma, beta, S, lam, P)
+    need = int(lib.hypic_warmup_workspace_bytes(ctypes.byref(a)))
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=S_rest.device)
+    if workspace is not None:
+        a.workspace = _ptr(workspace)
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.hypic_conv_warmup(ctypes.byref(a), _stream(stream)), "hypic_conv_warmup")
+    return S, lam, P
 
 
 def make_compose_args(family, S, lam, P=None, S0=None, prefix=None, lam_total=None, P_total=None):

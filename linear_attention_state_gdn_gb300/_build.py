@@ -21,7 +21,7 @@ LIB = os.path.join(PKG, "libhypic.so")
 OBJ_DBG = os.path.join(PKG, "_build_dbg")
 LIB_DBG = os.path.join(PKG, "libhypic_dbg.so")
 SOURCES = ["api.cu", "build_simt.cu", "compose.cu", "compose_tc.cu", "compose_cols.cu", "build_gated_tc.cu", "build_gdn_prep.cu",
-           "build_gdn_tc.cu", "build_gdn_tc_out.cu", "build_gdn_tc_kda.cu"]
+           "build_gdn_tc.cu", "build_gdn_tc_out.cu", "build_gdn_tc_kda.cu", "conv.cu"]
 HEADERS = [os.path.join(ROOT, "include", "hypic.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

@@ -304,6 +304,43 @@ bool compose_shape_ok(const hypic_compose_args *a) {
            a->n_units >= 0 && head_size_ok(a->d_k, a->d_v);
 }
 
+// The convolution-state warm-up's workspace: the heads' convolved k, v (fp32), their gathered
+// gates and b, then the two composition pieces of every (segment, value head) unit (the head
+// entries, built here, and copies of the cached rests) and, for a dense scan that cannot write
+// its last state directly (d < 128), the scan's prefix states.
+struct WarmupLayout {
+    int64_t rows = 0;
+    size_t off_kh = 0, off_vh = 0, off_gh = 0, off_bh = 0, off_S = 0, off_lam = 0, off_P = 0, off_pre = 0,
+           bytes = 0;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool warmup_shape_ok(const hypic_warmup_args *a) {
+    return a && a->family >= HYPIC_FAM_LINEAR && a->family <= HYPIC_FAM_KDA &&
+           (a->dtype == HYPIC_BF16 || a->dtype == HYPIC_F32) && a->n_seg >= 0 &&
+           a->n_seg <= HYPIC_MAX_SEGMENTS && a->H_k > 0 && a->H_v > 0 && a->H_v % a->H_k == 0 &&
+           head_size_ok(a->d_k, a->d_v) && a->conv_k >= 1 && a->conv_k <= 8;
+}
+
+WarmupLayout warmup_layout(const hypic_warmup_args *a) {
+    WarmupLayout L;
+    for (int j = 0; j < a->n_seg; ++j)
+        L.rows += std::max<int64_t>(0, std::min<int64_t>(a->conv_k - 1, a->seg_offsets[j + 1] - a->seg_offsets[j]));
+    const size_t D = (size_t)a->d_k, U = (size_t)a->n_seg * a->H_v, R = (size_t)L.rows;
+    const bool chan = a->family == HYPIC_FAM_DIAG || a->family == HYPIC_FAM_KDA;
+    const bool dense = dense_family(a->family);
+    L.off_vh = align256(R * a->H_k * D * 4);
+    L.off_gh = L.off_vh + align256(R * a->H_v * D * 4);
+    L.off_bh = L.off_gh + align256(a->log_gate ? R * a->H_v * (chan ? D : 1) * 4 : 0);
+    L.off_S = L.off_bh + align256(a->beta ? R * a->H_v * 4 : 0);
+    L.off_lam = L.off_S + align256(2 * U * D * D * 4);
+    L.off_P = L.off_lam + align256(2 * U * (a->family == HYPIC_FAM_DIAG ? D : 1) * 4);
+    L.off_pre = L.off_P + align256(dense ? 2 * U * D * D * 4 : 0);
+    L.bytes = L.off_pre + align256(dense && D != 128 ? 2 * U * D * D * 4 : 0);
+    return L;
+}
+
 }  // namespace
 
 extern "C" {
@@ -646,6 +683,173 @@ hypic_status hypic_probe_wait_timeout(uint32_t limit_us, void *stream) {
         return HYPIC_ERR_CUDA;
     wait_probe_kernel<<<sms, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, (uint64_t)limit_us * 1000u);
     return from_cuda(cudaGetLastError());
+}
+
+size_t hypic_warmup_workspace_bytes(const hypic_warmup_args *a) {
+    if (!warmup_shape_ok(a) || a->n_seg == 0 || !a->seg_offsets) return 0;
+    for (int j = 0; j < a->n_seg; ++j)
+        if (a->seg_offsets[j + 1] < a->seg_offsets[j]) return 0;
+    return warmup_layout(a).bytes;
+}
+
+hypic_status hypic_conv_warmup(const hypic_warmup_args *a, void *stream) {
+    NvtxRange range("hypic_conv_warmup");
+    if (!a) return HYPIC_ERR_INVALID_ARG;
+    const int fam = a->family;
+    if (fam < HYPIC_FAM_LINEAR || fam > HYPIC_FAM_KDA) return HYPIC_ERR_INVALID_ARG;
+    if (a->dtype != HYPIC_BF16 && a->dtype != HYPIC_F32) return HYPIC_ERR_INVALID_ARG;
+    if (a->n_seg < 0 || a->n_seg > HYPIC_MAX_SEGMENTS) return HYPIC_ERR_INVALID_ARG;
+    if (a->H_k <= 0 || a->H_v <= 0 || a->H_v % a->H_k != 0) return HYPIC_ERR_INVALID_ARG;
+    if (a->d_k <= 0 || a->d_v <= 0) return HYPIC_ERR_INVALID_ARG;
+    if (a->conv_k < 1 || a->conv_k > 8) return HYPIC_ERR_INVALID_ARG;
+    if (!head_size_ok(a->d_k, a->d_v)) return HYPIC_ERR_UNSUPPORTED;
+    if (a->n_seg == 0) return HYPIC_OK;
+    if (!a->seg_offsets || a->seg_offsets[0] != 0) return HYPIC_ERR_INVALID_ARG;
+    for (int j = 0; j < a->n_seg; ++j)
+        if (a->seg_offsets[j + 1] < a->seg_offsets[j]) return HYPIC_ERR_INVALID_ARG;
+    const int64_t n_tok = a->seg_offsets[a->n_seg];
+    if (n_tok > INT32_MAX) return HYPIC_ERR_UNSUPPORTED;
+    const bool dense = dense_family(fam);
+    const bool need_gate = fam == HYPIC_FAM_DIAG || fam == HYPIC_FAM_GDN || fam == HYPIC_FAM_KDA;
+    if (!a->S_rest || !a->lam_rest || !a->S || !a->lam || !a->conv_wk || !a->conv_wv) return HYPIC_ERR_INVALID_ARG;
+    if (dense && (!a->P_rest || !a->P || !a->beta)) return HYPIC_ERR_INVALID_ARG;
+    if (need_gate && !a->log_gate) return HYPIC_ERR_INVALID_ARG;
+    if (fam == HYPIC_FAM_SCALAR && (!a->log_gate) == (!a->log_gamma)) return HYPIC_ERR_INVALID_ARG;
+    if (n_tok > 0 && (!a->k_raw || !a->v_raw)) return HYPIC_ERR_INVALID_ARG;
+    const void *v16[] = {a->k_raw, a->v_raw, a->S_rest, a->P_rest, a->S, a->P};
+    for (const void *p : v16)
+        if (p && !aligned(p, 16)) return HYPIC_ERR_ALIGNMENT;
+    const void *v4[] = {a->conv_wk, a->conv_wv, a->log_gate, a->log_gamma, a->beta, a->lam_rest, a->lam};
+    for (const void *p : v4)
+        if (p && !aligned(p, 4)) return HYPIC_ERR_ALIGNMENT;
+    const void *dev[] = {a->conv_wk, a->conv_wv, a->log_gamma, a->S_rest, a->lam_rest, a->P_rest,
+                         a->S, a->lam, a->P};
+    for (const void *p : dev)
+        if (p && !on_device(p)) return HYPIC_ERR_INVALID_ARG;
+    if (n_tok > 0) {
+        const void *in[] = {a->k_raw, a->v_raw, a->log_gate, a->beta};
+        for (const void *p : in)
+            if (p && !on_device(p)) return HYPIC_ERR_INVALID_ARG;
+    }
+    // the outputs overlap no input and no other output
+    const size_t D = (size_t)a->d_k, U = (size_t)a->n_seg * a->H_v, el = a->dtype == HYPIC_BF16 ? 2 : 4;
+    const bool chan = fam == HYPIC_FAM_DIAG || fam == HYPIC_FAM_KDA;
+    const size_t nS = U * D * D * 4, nl = U * (fam == HYPIC_FAM_DIAG ? D : 1) * 4;
+    const struct { const void *p; size_t n; } ins[] = {
+        {a->k_raw, (size_t)n_tok * a->H_k * D * el}, {a->v_raw, (size_t)n_tok * a->H_v * D * el},
+        {a->conv_wk, (size_t)a->H_k * D * a->conv_k * 4}, {a->conv_wv, (size_t)a->H_v * D * a->conv_k * 4},
+        {a->log_gate, (size_t)n_tok * a->H_v * (chan ? D : 1) * 4}, {a->log_gamma, (size_t)a->H_v * 4},
+        {a->beta, (size_t)n_tok * a->H_v * 4}, {a->S_rest, nS}, {a->lam_rest, nl}, {a->P_rest, dense ? nS : 0}};
+    const struct { const void *p; size_t n; } outs[] = {{a->S, nS}, {a->lam, nl}, {a->P, dense ? nS : 0}};
+    for (const auto &o : outs) {
+        for (const auto &i : ins)
+            if (overlaps(o.p, o.n, i.p, i.n)) return HYPIC_ERR_INVALID_ARG;
+        for (const auto &o2 : outs)
+            if (&o != &o2 && overlaps(o.p, o.n, o2.p, o2.n)) return HYPIC_ERR_INVALID_ARG;
+    }
+    const WarmupLayout L = warmup_layout(a);
+    if (!a->workspace) return HYPIC_ERR_INVALID_ARG;
+    if (!aligned(a->workspace, 16)) return HYPIC_ERR_ALIGNMENT;
+    if (!on_device(a->workspace)) return HYPIC_ERR_INVALID_ARG;
+    if (L.bytes > a->workspace_bytes) return HYPIC_ERR_INVALID_ARG;
+    unsigned *err = status_word(nullptr);
+    if (!err) return HYPIC_ERR_CUDA;
+    uint8_t *ws = static_cast<uint8_t *>(a->workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // (1) the heads' tokens convolved over the prompt's raw stream, with their gates and b
+    static thread_local ConvHeadParams cp;   // ~8 KB: kept off the stack
+    std::memset(&cp, 0, sizeof(cp));
+    std::vector<int64_t> head_offs(a->n_seg + 1, 0);
+    for (int j = 0; j < a->n_seg; ++j) {
+        const int64_t hl = std::min<int64_t>(a->conv_k - 1, a->seg_offsets[j + 1] - a->seg_offsets[j]);
+        cp.seg_start[j] = (int32_t)a->seg_offsets[j];
+        cp.head_off[j] = (int32_t)head_offs[j];
+        head_offs[j + 1] = head_offs[j] + hl;
+    }
+    cp.head_off[a->n_seg] = (int32_t)head_offs[a->n_seg];
+    cp.family = fam;
+    cp.dtype = a->dtype;
+    cp.n_seg = a->n_seg;
+    cp.H_k = a->H_k;
+    cp.H_v = a->H_v;
+    cp.D = a->d_k;
+    cp.K = a->conv_k;
+    cp.n_rows = (int32_t)L.rows;
+    cp.k_raw = a->k_raw;
+    cp.v_raw = a->v_raw;
+    cp.wk = a->conv_wk;
+    cp.wv = a->conv_wv;
+    cp.log_gate = a->log_gate;
+    cp.beta = a->beta;
+    cp.k_head = reinterpret_cast<float *>(ws + L.off_kh);
+    cp.v_head = reinterpret_cast<float *>(ws + L.off_vh);
+    cp.g_head = a->log_gate ? reinterpret_cast<float *>(ws + L.off_gh) : nullptr;
+    cp.b_head = a->beta ? reinterpret_cast<float *>(ws + L.off_bh) : nullptr;
+    cp.err = err;
+    cudaError_t e = launch_conv_heads(cp, s);
+    if (e != cudaSuccess) return HYPIC_ERR_CUDA;
+
+    // (2) the heads' entries from a zero state (fp32 inputs: the exact path, no workspace),
+    //     into the first composition piece
+    float *Sp = reinterpret_cast<float *>(ws + L.off_S);
+    float *lp = reinterpret_cast<float *>(ws + L.off_lam);
+    float *Pp = dense ? reinterpret_cast<float *>(ws + L.off_P) : nullptr;
+    hypic_build_args b;
+    std::memset(&b, 0, sizeof(b));
+    b.family = fam;
+    b.dtype = HYPIC_F32;
+    b.n_seg = a->n_seg;
+    b.H_k = a->H_k;
+    b.H_v = a->H_v;
+    b.d_k = a->d_k;
+    b.d_v = a->d_v;
+    b.seg_offsets = head_offs.data();
+    b.k = cp.k_head;
+    b.v = cp.v_head;
+    b.log_gate = cp.g_head;
+    b.log_gamma = a->log_gamma;
+    b.beta = cp.b_head;
+    b.S = Sp;
+    b.lam = lp;
+    b.P = Pp;
+    const hypic_status st = hypic_build_segments(&b, stream);
+    if (st != HYPIC_OK) return st;
+
+    // (3) the cached rests as the second piece, then one composition: the last state (S), the
+    //     summed lam and, dense, the product P_rest P_head
+    const size_t nls = U * (fam == HYPIC_FAM_DIAG ? D : 1) * 4;
+    e = cudaMemcpyAsync(Sp + U * D * D, a->S_rest, nS, cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(reinterpret_cast<uint8_t *>(lp) + nls, a->lam_rest, nls,
+                                              cudaMemcpyDeviceToDevice, s);
+    if (e == cudaSuccess && dense) e = cudaMemcpyAsync(Pp + U * D * D, a->P_rest, nS, cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return HYPIC_ERR_CUDA;
+    ComposeParams q;
+    std::memset(&q, 0, sizeof(q));
+    q.family = fam;
+    q.n_seg = 2;
+    q.n_units = (int64_t)U;
+    q.D = a->d_k;
+    q.S = Sp;
+    q.lam = lp;
+    q.P = Pp;
+    q.lam_total = a->lam;
+    q.P_total = dense ? a->P : nullptr;
+    q.err = err;
+    if (!dense) {
+        q.prefix_last = a->S;
+        e = launch_compose_scaled(q, s);
+    } else if (compose_dense_tc_supported(q)) {
+        q.prefix_last = a->S;
+        e = launch_compose_dense_tc(q, s);
+    } else {
+        float *pre = reinterpret_cast<float *>(ws + L.off_pre);
+        q.prefix = pre;
+        e = launch_compose_dense_simt(q, s);
+        if (e == cudaSuccess) e = launch_compose_lam_total(q, s);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(a->S, pre + U * D * D, nS, cudaMemcpyDeviceToDevice, s);
+    }
+    return from_cuda(e);
 }
 
 const char *hypic_build_kernel_name(const hypic_build_args *a) {

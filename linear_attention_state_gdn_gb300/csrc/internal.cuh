@@ -90,6 +90,33 @@ struct ComposeParams {
     unsigned *err;
 };
 
+// The convolution of the warm-up's head tokens (conv.cu): head row r is token
+// seg_start[j] + r - head_off[j] of the prompt, for the segment j with head_off[j] <= r <
+// head_off[j + 1].
+struct ConvHeadParams {
+    int32_t family;
+    int32_t dtype;
+    int32_t n_seg;
+    int32_t H_k;
+    int32_t H_v;
+    int32_t D;          // d_k == d_v
+    int32_t K;          // the convolution's width
+    int32_t n_rows;     // head tokens of all segments
+    const void *k_raw;
+    const void *v_raw;
+    const float *wk;
+    const float *wv;
+    const float *log_gate;   // gathered per head row into g_head when not NULL
+    const float *beta;       // gathered into b_head when not NULL
+    float *k_head;      // [n_rows][H_k][D]
+    float *v_head;      // [n_rows][H_v][D]
+    float *g_head;      // [n_rows][H_v] (DIAG, KDA: [n_rows][H_v][D])
+    float *b_head;      // [n_rows][H_v]
+    unsigned *err;
+    int32_t seg_start[HYPIC_MAX_SEGMENTS];
+    int32_t head_off[HYPIC_MAX_SEGMENTS + 1];
+};
+
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_build_gated_simt(const BuildParams &p, cudaStream_t s);
 cudaError_t launch_build_seq(const BuildParams &p, cudaStream_t s);
@@ -107,6 +134,7 @@ cudaError_t launch_build_gdn_tc_outputs(const BuildParams &p, cudaStream_t s);
 cudaError_t launch_build_gdn_prep(const BuildParams &p, cudaStream_t s);
 cudaError_t launch_build_kda_tc(const BuildParams &p, cudaStream_t s);
 cudaError_t launch_build_kda_prep(const BuildParams &p, cudaStream_t s);
+cudaError_t launch_conv_heads(const ConvHeadParams &p, cudaStream_t s);
 bool build_gdn_tc_supported(const BuildParams &p);
 
 // fp32 view of one input element (bf16 or fp32 storage).

@@ -54,7 +54,7 @@ def test_python_names_match_the_abi():
 
 # ------------------------------------------------------------------ host-side validation
 
-from linear_attention_state_gdn_gb300 import BuildArgs, ComposeArgs  # noqa: E402
+from linear_attention_state_gdn_gb300 import BuildArgs, ComposeArgs, WarmupArgs  # noqa: E402
 
 FAKE = 0x7f0000000000   # 16-byte aligned, never dereferenced
 
@@ -303,3 +303,50 @@ def test_path_of_kda_outputs_and_start_states(lib):
     b = good_build(family=2)                         # outputs of the other families: exact path
     b.q, b.O = FAKE + 0x8000000, FAKE + 0x9000000
     assert lib.hypic_build_kernel_name(ctypes.byref(b)) == b"build_seq"
+
+
+# ------------------------------------------------------------------ convolution-state warm-up
+
+def good_warmup(family=4, lens=(64, 2, 0, 70), K=4):
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    a = WarmupArgs()
+    a.family, a.dtype, a.n_seg, a.conv_k = family, 0, len(lens), K
+    a.H_k, a.H_v, a.d_k, a.d_v = 2, 4, 128, 128
+    a.seg_offsets = offs.ctypes.data
+    a.k_raw, a.v_raw = FAKE, FAKE + 0x1000000
+    a.conv_wk, a.conv_wv = FAKE + 0x2000000, FAKE + 0x2100000
+    a.log_gate, a.beta = FAKE + 0x5000000, FAKE + 0x6000000
+    a.S_rest, a.lam_rest, a.P_rest = FAKE + 0x7000000, FAKE + 0x8000000, FAKE + 0x9000000
+    a.S, a.lam, a.P = FAKE + 0xA000000, FAKE + 0xB000000, FAKE + 0xC000000
+    a._keep = offs
+    return a
+
+
+def test_warmup_struct_layout():
+    assert ctypes.sizeof(WarmupArgs) == 8 * 4 + 16 * 8
+
+
+@pytest.mark.parametrize("field,value", [("conv_k", 0), ("conv_k", 9), ("family", 6), ("dtype", 3),
+                                         ("H_k", 3), ("S_rest", None), ("lam_rest", None),
+                                         ("P_rest", None), ("beta", None), ("log_gate", None),
+                                         ("conv_wk", None), ("S", None)])
+def test_warmup_rejects_bad_arguments(lib, field, value):
+    a = good_warmup()
+    setattr(a, field, value)
+    assert lib.hypic_conv_warmup(ctypes.byref(a), None) == 1
+
+
+def test_warmup_empty_call_and_workspace(lib):
+    a = good_warmup(lens=())
+    assert lib.hypic_conv_warmup(ctypes.byref(a), None) == 0
+    # heads of 3, 2, 0, 3 tokens (K = 4): convolved k (2 heads) and v (4 heads), gathered gates
+    # and b, then two composition pieces of S, lam and P for 4 x 4 units (256-byte rounding)
+    a = good_warmup()
+    r, U, d = 8, 16, 128
+    rnd = lambda x: (x + 255) // 256 * 256
+    want = (rnd(r * 2 * d * 4) + rnd(r * 4 * d * 4) + rnd(r * 4 * 4) + rnd(r * 4 * 4) +
+            rnd(2 * U * d * d * 4) + rnd(2 * U * 4) + rnd(2 * U * d * d * 4))
+    assert lib.hypic_warmup_workspace_bytes(ctypes.byref(a)) == want
+    a = good_warmup(K=1)
+    assert lib.hypic_warmup_workspace_bytes(ctypes.byref(a)) == rnd(2 * U * d * d * 4) + rnd(2 * U * 4) + \
+        rnd(2 * U * d * d * 4)
