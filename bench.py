@@ -392,6 +392,93 @@ def section_outputs(name, flush, peak, steps=10, warmup=3, oracle_budget_s=0.0):
     return out
 
 
+def section_conv_warmup(flush, peak, steps=20, warmup=3, oracle_heads=0, K=4):
+    """The convolution-state warm-up on the GDN workload's prompt (16 x 2048 tokens, 32 value /
+    16 key heads, d = 128) with a width-4 short convolution. Outside the timed region: each
+    segment's rest (its tokens from K - 1 on) is built from the segment's own convolution
+    (torch's grouped conv1d prepares the cache's inputs) with the library's build. Timed: the
+    hypic_conv_warmup call, which convolves the 16 x 3 head tokens in context, builds their
+    entries and composes each before its rest. Its algorithmic bytes: the rests' entries read,
+    the entries in context written, the head tokens' raw k, v and the taps. The oracle leg runs
+    oracle.conv_warmup on the first key head's value heads from the same rests."""
+    import torch.nn.functional as F
+    import linear_attention_state_gdn_gb300 as hy
+    from linear_attention_state_gdn_gb300 import synth
+    inp = synth.make_workload("gdn")
+    dev = {n: t.cuda() for n, t in inp.tensors().items()}
+    d, Hk, Hv, n_seg = inp.d_k, inp.H_k, inp.H_v, inp.n_seg
+    offs = [int(x) for x in inp.seg_offsets]
+    g = torch.Generator().manual_seed(2026)
+    wk = (torch.randn(Hk * d, K, generator=g) * 0.5).cuda()
+    wv = (torch.randn(Hv * d, K, generator=g) * 0.5).cuda()
+
+    def local_conv(x, w, H, normalize):   # each segment convolved on its own (zeros before it)
+        out = torch.empty(x.shape, dtype=torch.float32, device="cuda")
+        for j in range(n_seg):
+            a, b = offs[j], offs[j + 1]
+            seg = x[a:b].float().reshape(b - a, H * d).t().unsqueeze(0)
+            y = F.silu(F.conv1d(F.pad(seg, (K - 1, 0)), w.unsqueeze(1), groups=H * d))[0].t()
+            y = y.reshape(b - a, H, d)
+            if normalize:
+                n = y.norm(dim=2, keepdim=True)
+                y = torch.where(n > 0, y / torch.where(n > 0, n, torch.ones_like(n)), torch.zeros_like(y))
+            out[a:b] = y
+        return out
+
+    kl = local_conv(dev["k"], wk, Hk, True)
+    vl = local_conv(dev["v"], wv, Hv, False)
+    hl = [min(K - 1, offs[j + 1] - offs[j]) for j in range(n_seg)]
+    keep = torch.cat([torch.arange(offs[j] + hl[j], offs[j + 1]) for j in range(n_seg)]).cuda()
+    r_offs = np.concatenate([[0], np.cumsum([offs[j + 1] - offs[j] - hl[j] for j in range(n_seg)])])
+    S_r, lam_r, P_r = hy.hypic_build_segments("gdn", kl[keep].to(torch.bfloat16).contiguous(),
+                                              vl[keep].to(torch.bfloat16).contiguous(), r_offs,
+                                              log_gate=dev["log_gate"][keep].contiguous(),
+                                              beta=dev["beta"][keep].contiguous())
+    del kl, vl
+    S, lam, P = torch.empty_like(S_r), torch.empty_like(lam_r), torch.empty_like(P_r)
+    need = hy.hypic_warmup_workspace_bytes("gdn", offs, dev["k"], dev["v"], wk, wv, S_r, lam_r,
+                                           P_rest=P_r, log_gate=dev["log_gate"], beta=dev["beta"],
+                                           S=S, lam=lam, P=P)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    f = lambda: hy.hypic_conv_warmup("gdn", offs, dev["k"], dev["v"], wk, wv, S_r, lam_r, P_r,
+                                     log_gate=dev["log_gate"], beta=dev["beta"], S=S, lam=lam, P=P,
+                                     workspace=ws)
+    (tw,), _ = time_loop([f], steps, warmup, flush)
+    ms = statistics.mean(tw)
+    units = n_seg * Hv
+    rows = sum(hl)
+    nbytes = 2 * units * (2 * d * d * 4 + 4) + rows * (Hk + Hv) * d * 2 + (Hk + Hv) * d * K * 4
+    gbs = nbytes / ms / 1e6
+    out = {"kernels": "conv_heads + build_seq (heads) + compose_dense_tc (head before rest)",
+           "conv_k": K, "units": units, "head_tokens": rows, "warmup_ms": round(ms, 4),
+           "warmup_bytes": nbytes, "warmup_gbs": round(gbs, 1),
+           "warmup_hbm_frac": round(gbs / peak["hbm_gbs"], 4),
+           "note": "the pieces go through the workspace (a copy of each rest's entry), so DRAM "
+                   "traffic exceeds these algorithmic bytes"}
+    if oracle_heads:
+        import oracle
+        torch.cuda.synchronize()
+        hv = sample_heads(inp, oracle_heads)
+        hk = hv // (Hv // Hk)
+        f64 = lambda t: t.double().cpu().numpy()
+        t0 = time.perf_counter()
+        S_o, T_o = oracle.conv_warmup(
+            "gdn", offs, f64(inp.k[:, :hk]), f64(inp.v[:, :hv]), f64(wk[:hk * d]), f64(wv[:hv * d]), K,
+            f64(S_r[:, :hv]), f64(lam_r[:, :hv]), f64(P_r[:, :hv]),
+            log_gate=f64(inp.log_gate[:, :hv]), beta=f64(inp.beta[:, :hv]))
+        secs = time.perf_counter() - t0
+        e_S = rel_frob_max(f64(S[:, :hv]), S_o)
+        e_T = rel_frob_max(oracle.materialize_T("gdn", f64(lam[:, :hv]), f64(P[:, :hv])), T_o)
+        out["cpu_baseline"] = {"value": round(secs * Hv / hv * 1e3, 1), "unit": "ms per call (scaled)",
+                               "cores": oracle.default_threads(), "kind": "oracle",
+                               "sample": f"oracle.conv_warmup of all {n_seg} segments x {hv} of {Hv} "
+                                         f"value heads from the same rests; ms scaled by {Hv}/{hv}"}
+        out["parity"] = {"S": float(f"{e_S:.4g}"), "T": float(f"{e_T:.4g}"), "tol": 1e-4,
+                         "ok": bool(e_S <= 1e-4 and e_T <= 1e-4),
+                         "units": f"{n_seg} segments x {hv} of {Hv} value heads"}
+    return out
+
+
 def section_gdn_compose(flush, peak, steps=10, warmup=3, layers=48, oracle_units=0):
     import linear_attention_state_gdn_gb300 as hy
     S, lam, P, info = build_gdn_compose_cache(layers)
@@ -849,6 +936,7 @@ def run_main(args):
         sections["gdn_outputs"] = section_outputs("gdn", flush, pk, oracle_budget_s=4.0 if oracle_leg else 0.0)
         sections["gdn_compose"] = section_gdn_compose(flush, pk, layers=args.compose_layers,
                                                       oracle_units=96 if oracle_leg else 0)
+        sections["conv_warmup"] = section_conv_warmup(flush, pk, oracle_heads=2 if oracle_leg else 0)
         line["sections"] = sections
         if oracle_leg:
             line["cpu_baseline"] = cpu_baseline(inp, gpu=gpu_out)
@@ -874,6 +962,8 @@ def run_only(args):
                                   layers=args.compose_layers)
     elif args.only == "gdn_outputs":
         out = section_outputs("gdn", flush, pk, steps=args.steps, warmup=args.warmup)
+    elif args.only == "conv_warmup":
+        out = section_conv_warmup(flush, pk, steps=args.steps, warmup=args.warmup, oracle_heads=2)
     else:
         out = section_family(args.only, flush, pk, steps=args.steps, warmup=args.warmup)
     assert hy.hypic_get_device_status() == 0
@@ -891,7 +981,7 @@ def main(argv=None):
                     help="main timed region only (no e2e, sections or CPU baseline)")
     ap.add_argument("--compose-layers", type=int, default=48)
     ap.add_argument("--only", choices=["gdn", "retnet", "gla", "gdn_tiny", "gdn_compose", "gdn_one_segment",
-                                       "retnet_one_segment", "kda", "gdn_outputs"],
+                                       "retnet_one_segment", "kda", "gdn_outputs", "conv_warmup"],
                     help="time one workload's launches alone (profiling helper; no contract line)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
