@@ -18,32 +18,39 @@
 // Persistent CTAs of 128 threads. A unit of work is R records of one (segment, chunk): with
 // an even grouped-query factor R = 2, the two value heads of one key head, which share the k
 // tile, the gram and its shared-memory copy, and whose two inverses run side by side;
-// otherwise R = 1. Four CTAs per SM (all 512 TMEM columns, about 52 KB of shared memory and at
+// otherwise R = 1. Four CTAs per SM (all 512 TMEM columns, about 50 KB of shared memory and at
 // most 128 registers each). Units are handed out as tickets: a CTA
 // starts with two fixed units and takes each further one from a counter in the workspace
 // (zeroed before the launch), so CTAs that run faster take more units and all CTAs finish
 // within about one unit of each other. The k tile of the next unit is requested as soon as
-// the current gram has read the single k buffer, its gram is issued while the current
-// inverses finish (two TMEM buffers), and b is loaded a unit ahead, so loads and grams
-// overlap the inversions. A CTA that has drawn its last ticket lets the chain
-// kernel launch (programmatic dependent launch); the chain waits for this grid's completion
-// before it reads any record.
+// the current gram has read the single k buffer, its gram is issued once the current diagonal
+// blocks are solved (two TMEM buffers), and b is loaded a unit ahead, so loads and grams
+// overlap the inversions. A CTA that is on its last unit lets the chain kernel launch
+// (programmatic dependent launch); the chain waits for this grid's completion before it reads
+// any record. Three CTA barriers per unit:
 //   1. TMA the chunk's k (two 128B-swizzled 64-channel halves); b masked past the segment end.
 //   2. One thread issues the gram K K^T (M = 64 tcgen05 MMA, fp32 accumulator in TMEM).
-//   3. The raw gram G = K K^T in shared memory, 16 x 16 blocks: the blocks left of the
-//      diagonal rounded to tf32 once (they are only ever MMA operands), the diagonal blocks
-//      exact (forward substitution); the blocks right of the diagonal are not stored.
+//   3. Warp w reads block row w of the raw gram G = K K^T into shared memory as 16 x 16 blocks:
+//      the blocks left of the diagonal rounded to tf32 once (they are only ever MMA operands),
+//      the diagonal block exact (forward substitution); the blocks right of it are not stored.
 //      A = Diag(b) L is never formed: b scales rows inside the consumers, and the strictly
 //      lower mask is the consumers' index range.
-//   4. N by 16 x 16 blocks: the four diagonal blocks by forward substitution (one warp each;
-//      lanes 0-15 solve the first record's columns, lanes 16-31 the second's),
-//      then the blocks below level by level, N_ab = -N_aa Diag(b_a) sum_{k=b}^{a-1} G_ak N_kb,
-//      as 16 x 8 half-blocks spread over the four warps. The 16 x 16 x 16 products run on
-//      the warp-level tensor-core MMA (m16n8k8, tf32 inputs, fp32 accumulation): tcgen05's
-//      smallest tile (M = 64) would waste most of its work on products this small and each
-//      would need a round trip through TMEM. Every MMA operand in shared memory is stored
-//      already rounded to tf32, so the fragments are loaded without conversions.
-//   5. Columns scaled by b_t, rounded to bf16, stored (16-byte coalesced stores).
+//   4. N by 16 x 16 blocks. (i) Warp a solves diagonal block a by forward substitution (lanes
+//      0-15 the first record's columns, lanes 16-31 the second's); it needs only its own gram
+//      rows, so no CTA barrier precedes it. (ii) The blocks (1,0) and (3,2), which complete the
+//      inverses N11 and N22 of the two 32 x 32 diagonal halves: N_ab = -N_aa Diag(b_a) G_ab N_bb.
+//      (iii) The lower-left 32 x 32 quarter, N21 = -N22 Diag(b) G21 N11, by columns: a warp
+//      takes 8 columns of one record and forms both T = Diag(b) G21 N11 rows and both N21 rows
+//      for them with nothing but its own scratch, so no barrier separates the two products.
+//      All products are 16 x 8 x 16 pieces on the warp-level tensor-core MMA (m16n8k8, tf32
+//      inputs, fp32 accumulation): tcgen05's smallest tile (M = 64) would waste most of its
+//      work on products this small and each would need a round trip through TMEM. Operands
+//      come by ldmatrix: A operands from row-major blocks, B operands from transposed copies
+//      (a block is stored in the orientations its consumers need), all already rounded to
+//      tf32.
+//   5. Every block of N is scaled by b over its columns, rounded to bf16 and stored into the
+//      record straight from the registers that computed it; warps 0-1 write the blocks above the
+//      diagonal as zeros after their diagonal solves.
 // Tokens past the segment end have b = 0, so their rows and columns of M2 are zero.
 #include <algorithm>
 
@@ -59,21 +66,25 @@ using namespace ptx;
 constexpr int D = 128;
 constexpr int C = kGdnChunk;
 constexpr int kThreads = 128;
-// Shared-memory layout of G and N: only the ten 16 x 16 blocks on and below the diagonal are
-// stored, block (a, b) at word kBlk (a (a + 1) / 2 + b), and element (r, c) of a block at
-// 16 r + (c ^ sw(r)). The swizzle makes the warp-level MMA's A fragments (8 rows x 4 columns),
-// its B fragments (4 rows x 8 columns), the 16 x 8 result stores and the row-wise accesses
-// each touch 32 distinct banks. The 8 words after each block put the blocks of one row in
-// different banks (record stage) and start N's second record 16 banks after the first (the two
-// records' diagonal solves store side by side). The per-warp 16 x 8 scratch (a B operand) has
-// unpadded rows of 8.
-constexpr int kBlk = 264;
-constexpr int kTri = 10 * kBlk;   // one matrix
-constexpr int kLDT = 8;
+// Shared-memory layout. G keeps its ten 16 x 16 blocks on and below the diagonal, block (a, b)
+// at word 256 (a (a + 1) / 2 + b), row-major with element (r, c) at 16 r + (c ^ sw(r)). N keeps,
+// per record, the blocks its products read: row-major (the same swizzle) N11, N22, N32, N33 (A
+// operands) and transposed, with element (r, c) at kLdT c + r, N00, N10, N11, N22 (B operands).
+// The swizzle and the transposed row stride of 20 words make every ldmatrix phase (8 rows of 16
+// bytes), the diagonal solves' stores and the result stores touch 32 distinct banks. A record's
+// N takes kNRec words, 16 more than its blocks, so that the second record's row-major blocks sit
+// 16 banks after the first's (the two records' diagonal solves store side by side). Each warp
+// has two 16 x 8 scratch tiles T, held transposed (8 rows of stride kLdT).
+constexpr int kLdT = 20;
+constexpr int kN11 = 0, kN22 = 256, kN32 = 512, kN33 = 768;                 // row-major
+constexpr int kT00 = 1024, kT10 = kT00 + 16 * kLdT, kT11 = kT10 + 16 * kLdT, kT22 = kT11 + 16 * kLdT;
+constexpr int kNRec = kT22 + 16 * kLdT + 16;
+constexpr int kGWords = 10 * 256;
+constexpr int kTile = 8 * kLdT;   // one transposed 16 x 8 T tile
 __device__ __forceinline__ int sw(int r) { return ((r << 2) & 8) | (r & 4); }
-__device__ __forceinline__ int blk(int a, int b) { return kBlk * (a * (a + 1) / 2 + b); }
+__host__ __device__ constexpr int gblk(int a, int b) { return 256 * (a * (a + 1) / 2 + b); }
 // b of a record: entry e at vbi(e), 16 words of padding after the first 32 entries, so that the
-// record stage's loads of b touch distinct banks
+// diagonal solves' loads of b touch distinct banks
 constexpr int kVb = 80;
 __device__ __forceinline__ int vbi(int e) { return e + ((e >> 5) << 4); }
 // R records per iteration: the value heads h, h + 1 that share a key head (R = 2, when the
@@ -83,12 +94,12 @@ template <int R>
 struct PrepGeo {
     static constexpr uint32_t kOffK = 0;                              // k tile, 16 KB
     static constexpr uint32_t kOffG32 = 16384;                        // the gram K K^T, 10 blocks
-    static constexpr uint32_t kOffN32 = kOffG32 + kTri * 4;           // R x N (tf32-rounded), 10 blocks each
-    static constexpr uint32_t kOffT = kOffN32 + R * kTri * 4;         // 4 warps x 16 x 8 fp32
-    static constexpr uint32_t kSmemBytes = kOffT + 4 * 16 * kLDT * 4 + 1024;
+    static constexpr uint32_t kOffN32 = kOffG32 + kGWords * 4;        // R x N (tf32-rounded)
+    static constexpr uint32_t kOffT = kOffN32 + R * kNRec * 4;        // 4 warps x 2 tiles
+    static constexpr uint32_t kSmemBytes = kOffT + 4 * 2 * kTile * 4 + 1024;
     static constexpr int kCtasPerSm = 4;                              // 4 x 128 TMEM columns
 };
-constexpr int kCtl = 96;   // warp 3 lane 0 issues loads and grams (warp 3 has the least level work)
+constexpr int kCtl = 0;   // warp 0 lane 0 issues loads and grams (warp 0 reads the fewest gram rows)
 
 __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
@@ -99,50 +110,231 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
 // x rounded to tf32 (round to nearest), kept as a float with the low 13 mantissa bits zero
 __device__ __forceinline__ float tf32r(float x) { return __uint_as_float(to_tf32(x)); }
 
-// c (16 x 8, m16n8 accumulator layout) += X (16 x 16) * Y[:, yc .. yc + 7] (16 x 8), holding
-// tf32-rounded values: X a swizzled block; Y a swizzled block (YS) or the unswizzled 16 x 8
-// scratch (row stride kLDT, yc = 0).
-template <bool YS>
-__device__ __forceinline__ void mma16x8x16(float (&c)[4], const float *X, const float *Y, int yc, int lane) {
-    const int g = lane >> 2, t = lane & 3;
-    const int sx = sw(g);   // rows g and g + 8 share it
-    constexpr int ldy = YS ? 16 : kLDT;
+// four 8 x 8 b16 matrices; read as 32-bit words, lane l receives word (l / 4, l % 4) of each
+// matrix's 8 rows of 16 bytes, which is how a tf32 MMA fragment is laid out
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mma_m16n8k8(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// A lane's byte offsets of the ldmatrix row addresses, and its place (g, t) in the m16n8
+// accumulator: rows g, g + 8, columns 2 t, 2 t + 1.
+struct Lanes {
+    uint32_t a0, a1;   // A fragments, k-steps 0 and 1, of a row-major 16 x 16 block
+    uint32_t b;        // B fragments, both k-steps, of rows 0-7 of a transposed block or a T tile
+    int g, t;
+};
+
+__device__ __forceinline__ Lanes lanes_of(int lane) {
+    Lanes L;
+    // matrices 0-3 of an A fragment: rows 0-7 and 8-15 of k-columns 8 ks .. + 3, then + 4 .. + 7
+    const int r = (lane & 7) | (lane & 8), c = 4 * (lane >> 4);
+    L.a0 = 4u * (uint32_t)(16 * r + (c ^ sw(r)));
+    L.a1 = 4u * (uint32_t)(16 * r + ((8 + c) ^ sw(r)));
+    // matrices 0-3 of a B fragment: columns 0-7 of k-rows 0-3, 4-7, 8-11, 12-15
+    L.b = 4u * (uint32_t)(kLdT * (lane & 7) + 4 * (lane >> 3));
+    L.g = lane >> 2;
+    L.t = lane & 3;
+    return L;
+}
+
+// c += X Y for a row-major 16 x 16 block X (shared address) and the B fragments of a 16 x 8 Y
+__device__ __forceinline__ void mma16(float (&c)[4], uint32_t X, const uint32_t (&y)[4], const Lanes &L) {
+    uint32_t a[4], a2[4];
+    ldsm4(a, X + L.a0);
+    ldsm4(a2, X + L.a1);
+    mma_m16n8k8(c, a, y[0], y[1]);
+    mma_m16n8k8(c, a2, y[2], y[3]);
+}
+
+// T = Diag(b_lo rows, b_hi rows) c, rounded to tf32, into a transposed tile (element (m, n) at
+// kLdT n + m)
+__device__ __forceinline__ void put_t(float *Tt, const float (&c)[4], float b_lo, float b_hi, const Lanes &L) {
+    float *o = Tt + kLdT * (2 * L.t) + L.g;
+    o[0] = tf32r(c[0] * b_lo);
+    o[kLdT] = tf32r(c[1] * b_lo);
+    o[8] = tf32r(c[2] * b_hi);
+    o[kLdT + 8] = tf32r(c[3] * b_hi);
+}
+
+// the record's entries (row0 + g, col0 + 2 t, + 1) and (row0 + g + 8, ...) from N values -d:
+// M2 = N Diag(b), bf16, rows of 128 bytes
+__device__ __forceinline__ void put_rec(uint8_t *rec, int row0, int col0, const float (&d)[4], const float *bv,
+                                        const Lanes &L) {
+    const int r = row0 + L.g, c = col0 + 2 * L.t;
+    const float2 bc = *reinterpret_cast<const float2 *>(bv + vbi(c));
+    *reinterpret_cast<uint32_t *>(rec + r * 128 + c * 2) = pack_bf16x2(-d[0] * bc.x, -d[1] * bc.y);
+    *reinterpret_cast<uint32_t *>(rec + (r + 8) * 128 + c * 2) = pack_bf16x2(-d[2] * bc.x, -d[3] * bc.y);
+}
+
+// Step 4 (i): diagonal block `warp` of each record. Lane j < 16 solves column j of record 0
+// (lanes 16-31 that of record 1 when R = 2) by forward substitution,
+// x_r = [r == j] - b_r sum_{s<r} G_rs x_s (A = Diag(b) L restricted to the block), then stores
+// the column into the copies the products read and into the record.
+template <int R>
+__device__ __forceinline__ void diag_blocks(const float *G32, float *N32, const float (*vb)[kVb],
+                                            uint8_t *const (&rec)[R], int warp, int lane) {
+    if (R == 2 || lane < 16) {
+        const int a = warp, j = lane & 15, rr_ = R == 2 ? lane >> 4 : 0;
+        const float *bv = vb[rr_];
+        const float *Gd = G32 + gblk(a, a);
+        float x[16];
 #pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-        const int c0 = (8 * ks + t) ^ sx, c1 = (8 * ks + t + 4) ^ sx;
-        const int r0 = 8 * ks + t, r1 = r0 + 4;
-        const uint32_t a0 = __float_as_uint(X[g * 16 + c0]);
-        const uint32_t a1 = __float_as_uint(X[(g + 8) * 16 + c0]);
-        const uint32_t a2 = __float_as_uint(X[g * 16 + c1]);
-        const uint32_t a3 = __float_as_uint(X[(g + 8) * 16 + c1]);
-        const uint32_t b0 = __float_as_uint(Y[r0 * ldy + ((yc + g) ^ (YS ? sw(r0) : 0))]);
-        const uint32_t b1 = __float_as_uint(Y[r1 * ldy + ((yc + g) ^ (YS ? sw(r1) : 0))]);
-        asm volatile(
-            "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-            "{%0,%1,%2,%3};"
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+        for (int rr = 0; rr < 16; ++rr) {
+            float gr[16];
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+                const float4 t4 = *reinterpret_cast<const float4 *>(Gd + 16 * rr + ((4 * s4) ^ sw(rr)));
+                gr[4 * s4] = t4.x, gr[4 * s4 + 1] = t4.y, gr[4 * s4 + 2] = t4.z, gr[4 * s4 + 3] = t4.w;
+            }
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int s = 0; s < rr; ++s) acc[s & 3] = fmaf(gr[s], x[s], acc[s & 3]);
+            x[rr] = fmaf(-bv[vbi(16 * a + rr)], (acc[0] + acc[1]) + (acc[2] + acc[3]), (rr == j) ? 1.f : 0.f);
+        }
+        float *Nr = N32 + rr_ * kNRec;
+        if (a >= 1) {   // row-major copy: N11, N22, N33
+            float *Nd = Nr + (a == 1 ? kN11 : a == 2 ? kN22 : kN33);
+#pragma unroll
+            for (int rr = 0; rr < 16; ++rr) Nd[16 * rr + (j ^ sw(rr))] = tf32r(x[rr]);
+        }
+        if (a <= 2) {   // transposed copy: N00, N11, N22 (column j is row j)
+            float *Td = Nr + (a == 0 ? kT00 : a == 1 ? kT11 : kT22) + kLdT * j;
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4)
+                *reinterpret_cast<float4 *>(Td + 4 * s4) = make_float4(
+                    tf32r(x[4 * s4]), tf32r(x[4 * s4 + 1]), tf32r(x[4 * s4 + 2]), tf32r(x[4 * s4 + 3]));
+        }
+        const float bj = bv[vbi(16 * a + j)];
+        uint8_t *dst = (rr_ ? rec[R - 1] : rec[0]) + (16 * a) * 128 + (16 * a + j) * 2;
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr)
+            *reinterpret_cast<uint16_t *>(dst + rr * 128) = (uint16_t)pack_bf16x2(x[rr] * bj, 0.f);
     }
 }
 
-// Half-block (a, b, hh) of N: columns 16 b + 8 hh .. + 7 of block row a, from the blocks of
-// N already computed: T = Diag(b_a) sum_{k=b}^{a-1} G_ak N_kb[:, half], N_ab[:, half] =
-// -N_aa T (bv: the chunk's b).
-__device__ __forceinline__ void half_block(const float *G32, float *N32, float *Tw, const float *bv, int a,
-                                           int b, int hh, int lane) {
-    const int g = lane >> 2, t = lane & 3;
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k = b; k < a; ++k) mma16x8x16<true>(c, G32 + blk(a, k), N32 + blk(k, b), 8 * hh, lane);
-    const float b0 = bv[vbi(16 * a + g)], b1 = bv[vbi(16 * a + g + 8)];
-    *reinterpret_cast<float2 *>(Tw + g * kLDT + 2 * t) = make_float2(tf32r(c[0] * b0), tf32r(c[1] * b0));
-    *reinterpret_cast<float2 *>(Tw + (g + 8) * kLDT + 2 * t) = make_float2(tf32r(c[2] * b1), tf32r(c[3] * b1));
+// Step 4 (ii): columns 8 h .. 8 h + 7 of block (1,0) (B32 = false) or (3,2) (true) of each of the
+// unit's R records, N_ab = -N_aa Diag(b_a) G_ab N_bb; the records share the G fragments and run
+// side by side (record rr in scratch tile rr). N10 is stored transposed (a B operand of step
+// (iii)), N32 row-major (an A operand).
+template <bool B32, int R>
+__device__ __forceinline__ void level_one(uint32_t sG, float *N32, float *Tw, const float (*vb)[kVb],
+                                          uint8_t *const (&rec)[R], int h, const Lanes &L) {
+    constexpr int a = B32 ? 3 : 1, b = B32 ? 2 : 0;
+    const uint32_t sN = smem_u32(N32), sT = smem_u32(Tw);
+    uint32_t ga[4], ga2[4], y[R][4];
+    ldsm4(ga, sG + 4u * gblk(a, b) + L.a0);
+    ldsm4(ga2, sG + 4u * gblk(a, b) + L.a1);
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr)
+        ldsm4(y[rr], sN + 4u * (uint32_t)(rr * kNRec + (B32 ? kT22 : kT00) + 8 * kLdT * h) + L.b);
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_m16n8k8(c, ga, y[rr][0], y[rr][1]);
+        mma_m16n8k8(c, ga2, y[rr][2], y[rr][3]);
+        put_t(Tw + rr * kTile, c, vb[rr][vbi(16 * a + L.g)], vb[rr][vbi(16 * a + L.g + 8)], L);
+    }
     __syncwarp();
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
-    mma16x8x16<false>(d, N32 + blk(a, a), Tw, 0, lane);
-    float *o = N32 + blk(a, b) + ((8 * hh + 2 * t) ^ sw(g));   // rows g and g + 8 share the swizzle
-    *reinterpret_cast<float2 *>(o + g * 16) = make_float2(tf32r(-d[0]), tf32r(-d[1]));
-    *reinterpret_cast<float2 *>(o + (g + 8) * 16) = make_float2(tf32r(-d[2]), tf32r(-d[3]));
-    __syncwarp();   // Tw is reused by this warp's next half-block
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) ldsm4(y[rr], sT + 4u * (uint32_t)(rr * kTile) + L.b);
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        float *Nr = N32 + rr * kNRec;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16(d, sN + 4u * (uint32_t)(rr * kNRec + (B32 ? kN33 : kN11)), y[rr], L);
+        if (B32) {
+            float *o = Nr + kN32 + ((8 * h + 2 * L.t) ^ sw(L.g));   // rows g and g + 8 share the swizzle
+            *reinterpret_cast<float2 *>(o + 16 * L.g) = make_float2(tf32r(-d[0]), tf32r(-d[1]));
+            *reinterpret_cast<float2 *>(o + 16 * (L.g + 8)) = make_float2(tf32r(-d[2]), tf32r(-d[3]));
+        } else {
+            float *o = Nr + kT10 + kLdT * (8 * h + 2 * L.t) + L.g;
+            o[0] = tf32r(-d[0]);
+            o[kLdT] = tf32r(-d[1]);
+            o[8] = tf32r(-d[2]);
+            o[kLdT + 8] = tf32r(-d[3]);
+        }
+        put_rec(rec[rr], 16 * a, 16 * b + 8 * h, d, vb[rr], L);
+    }
+    __syncwarp();   // the scratch tiles are rewritten by this warp's next piece
+}
+
+// Step 4 (iii): columns 16 X + 8 h .. + 7 of the lower-left quarter of one record:
+// T2, T3 = Diag(b) (G21 N11) rows 32-47, 48-63 (N11's block column X: blocks 0-1 for X = 0,
+// block 1 for X = 1), then N(2,X) = -N22 T2 and N(3,X) = -(N32 T2 + N33 T3), straight into the
+// record.
+template <int X>
+__device__ __forceinline__ void level_two(uint32_t sG, const float *Nr, float *Tw, const float *bv, uint8_t *rec,
+                                          int h, const Lanes &L) {
+    const uint32_t sN = smem_u32(Nr), sT = smem_u32(Tw), hoff = 4u * (uint32_t)(8 * kLdT * h);
+    float c2[4] = {0.f, 0.f, 0.f, 0.f}, c3[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t y[4];
+    if (X == 0) {
+        ldsm4(y, sN + 4u * kT00 + hoff + L.b);
+        mma16(c2, sG + 4u * gblk(2, 0), y, L);
+        mma16(c3, sG + 4u * gblk(3, 0), y, L);
+        ldsm4(y, sN + 4u * kT10 + hoff + L.b);
+    } else {
+        ldsm4(y, sN + 4u * kT11 + hoff + L.b);
+    }
+    mma16(c2, sG + 4u * gblk(2, 1), y, L);
+    mma16(c3, sG + 4u * gblk(3, 1), y, L);
+    put_t(Tw, c2, bv[vbi(32 + L.g)], bv[vbi(40 + L.g)], L);
+    put_t(Tw + kTile, c3, bv[vbi(48 + L.g)], bv[vbi(56 + L.g)], L);
+    __syncwarp();
+    float d2[4] = {0.f, 0.f, 0.f, 0.f}, d3[4] = {0.f, 0.f, 0.f, 0.f};
+    ldsm4(y, sT + L.b);
+    mma16(d2, sN + 4u * kN22, y, L);
+    mma16(d3, sN + 4u * kN32, y, L);
+    ldsm4(y, sT + 4u * kTile + L.b);
+    mma16(d3, sN + 4u * kN33, y, L);
+    put_rec(rec, 32, 16 * X + 8 * h, d2, bv, L);
+    put_rec(rec, 48, 16 * X + 8 * h, d3, bv, L);
+    __syncwarp();   // T is rewritten by this warp's next piece
+}
+
+// The record's blocks above the diagonal, as zeros: 192 pieces of 16 bytes per record (block
+// row 0 from column 16, row 1 from 32, row 2 from 48), by threads q < NT.
+template <int R, int NT>
+__device__ __forceinline__ void zero_upper(uint8_t *const (&rec)[R], int q) {
+#pragma unroll
+    for (int id = q; id < 192 * R; id += NT) {
+        const int rr = R == 2 ? (id >= 192) : 0, z = id - 192 * rr;
+        int row, piece;
+        if (z < 96) row = z / 6, piece = 2 + z % 6;
+        else if (z < 160) row = 16 + (z - 96) / 4, piece = 4 + (z - 96) % 4;
+        else row = 32 + (z - 160) / 2, piece = 6 + (z - 160) % 2;
+        *reinterpret_cast<uint4 *>((rr ? rec[R - 1] : rec[0]) + row * 128 + piece * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// Steps 4 (ii) and (iii) for the unit's R records, with one CTA barrier between them. Step
+// (ii): warps 0-1 take the halves of (1,0), warps 2-3 those of (3,2), for every record. Step
+// (iii): warp w takes
+// column half h = w % 2 of block column w / 2 of record 0 and, when R = 2, of the other block
+// column of record 1, so that every warp has the same work.
+template <int R>
+__device__ __forceinline__ void off_diagonal(uint32_t sG, float *N32, float *Tw, const float (*vb)[kVb],
+                                             uint8_t *const (&rec)[R], int warp, const Lanes &L) {
+    const int h = warp & 1;
+    if (warp < 2) level_one<false, R>(sG, N32, Tw, vb, rec, h, L);
+    else level_one<true, R>(sG, N32, Tw, vb, rec, h, L);
+    __syncthreads();
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        if ((warp >> 1) == rr) level_two<0>(sG, N32 + rr * kNRec, Tw, vb[rr], rec[rr], h, L);
+        else level_two<1>(sG, N32 + rr * kNRec, Tw, vb[rr], rec[rr], h, L);
+    }
 }
 
 // Work units (R records each) are numbered in the order (segment rank, chunk, value heads
@@ -184,7 +376,7 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     __shared__ uint64_t kfull, gfull[2];
     __shared__ uint32_t tslot;
     __shared__ int s_ok;
-    __shared__ Walk s_n2[2];   // the unit after `nxt`, drawn by thread kCtl (two slots)
+    __shared__ Walk s_walk[2];   // the unit after the next, drawn by thread kCtl (two slots)
     __shared__ __align__(16) float vb[2][R][kVb];   // the records' b at vbi(token)
 
     const int64_t total = total_records(p), units = total / R;
@@ -194,8 +386,10 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     if (cur.r >= p.n_seg) return;   // uniform: the whole CTA leaves before any set-up
     const int q = threadIdx.x, warp = q >> 5, lane = q & 31;
     float *G32 = reinterpret_cast<float *>(smem + G::kOffG32);
-    float *N32 = reinterpret_cast<float *>(smem + G::kOffN32);   // record rr at N32 + rr * kTri
-    float *Tw = reinterpret_cast<float *>(smem + G::kOffT) + warp * 16 * kLDT;
+    float *N32 = reinterpret_cast<float *>(smem + G::kOffN32);   // record rr at N32 + rr * kNRec
+    float *Tw = reinterpret_cast<float *>(smem + G::kOffT) + warp * 2 * kTile;
+    const uint32_t sG = smem_u32(G32);
+    const Lanes L = lanes_of(lane);
 
     if (q == 0) {
         mbar_init(&kfull, 1);
@@ -241,12 +435,17 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     };
     bool ok = true;
     int64_t ticket = 0;   // thread kCtl
+    // every thread decodes unit 1; later units come through s_walk. Thread kCtl keeps its own
+    // copy `kn`: the unit after the current one at the top of an iteration (its k tile is
+    // requested there), the unit after that once its ticket is decoded.
     Walk nxt = decode<R>(p, (int64_t)gridDim.x + blockIdx.x, units);
+    Walk kn = nxt;
     float beta_cur = load_beta(cur);
     if (q == kCtl) {
         prefetch_tmap(&tmK);
         load_k(cur);
         ok = gram(0);
+        s_walk[1] = nxt;
     }
     for (int i = 0; cur.r < p.n_seg; ++i) {
         const int b = i & 1;
@@ -256,22 +455,29 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         if (!in_bounds(cur.c < nch && cur.h + R <= p.H_v &&
                            (int64_t)seg.wsb + (int64_t)(cur.h + R - 1) * nch + cur.c < total, p.err))
             break;
+        uint8_t *rec[R];
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr)
+            rec[rr] = static_cast<uint8_t *>(p.workspace) +
+                      ((int64_t)seg.wsb + (int64_t)(cur.h + rr) * nch + cur.c) * (int64_t)kGdnRecordBytes;
         if (q < R * C) vb[b][q / C][vbi(q & (C - 1))] = beta_cur;
-        const float beta_next = load_beta(nxt);
-        // gram(i) done: the k tile is free for the next record
+        // gram(i) done: the k tile is free for the next unit
         if (q == kCtl) {
             ok = ok && mbar_wait(&gfull[b], gwait[b] & 1, p.err, kErrTimeout);
             if (ok) {
                 ++gwait[b];
-                if (nxt.r < p.n_seg) load_k(nxt);
+                if (kn.r < p.n_seg) load_k(kn);
             }
             s_ok = ok ? 1 : 0;
-            // the ticket of the record after `nxt` (the counter's answer is used only at
-            // level 3 below, so its latency overlaps this record's inverse)
-            if (nxt.r < p.n_seg) ticket = 2 * (int64_t)gridDim.x + atomicAdd(tickets, 1u);
+            // the ticket of the unit after the next (the counter's answer is used only once
+            // this unit's diagonal blocks are solved, so its latency overlaps them)
+            if (kn.r < p.n_seg) ticket = 2 * (int64_t)gridDim.x + atomicAdd(tickets, 1u);
         }
         __syncthreads();
         if (!s_ok) break;   // uniform
+        nxt = s_walk[(i + 1) & 1];
+        if (nxt.r >= p.n_seg) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        const float beta_next = load_beta(nxt);
         tc_fence_after();
         {   // gram rows 16 warp + lane (lanes < 16, M = 64 accumulator layout): row `lane` of
             // block row `warp`; its blocks left of the diagonal are stored tf32-rounded, its
@@ -293,94 +499,26 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
                         float4 g4 = make_float4(__uint_as_float(gr[4 * s4]), __uint_as_float(gr[4 * s4 + 1]),
                                                 __uint_as_float(gr[4 * s4 + 2]), __uint_as_float(gr[4 * s4 + 3]));
                         if (k < warp) g4 = make_float4(tf32r(g4.x), tf32r(g4.y), tf32r(g4.z), tf32r(g4.w));
-                        *reinterpret_cast<float4 *>(G32 + blk(warp, k) + 16 * r + (cb ^ sw(r))) = g4;
+                        *reinterpret_cast<float4 *>(G32 + gblk(warp, k) + 16 * r + (cb ^ sw(r))) = g4;
                     }
                 }
             }
         }
+        __syncwarp();   // the diagonal block's rows were stored by this warp
+        diag_blocks<R>(G32, N32, vb[b], rec, warp, lane);
+        if (warp < 2) zero_upper<R, 64>(rec, q);   // warps 0-1 read the fewest gram rows
+        // the next unit's gram (its k tile was requested at the top of this unit) into the other
+        // TMEM buffer, last read a unit ago, and the walk of the unit after it
+        if (q == kCtl) {
+            if (ok && kn.r < p.n_seg) ok = gram(b ^ 1);
+            const Walk w2 = kn.r < p.n_seg ? decode<R>(p, ticket, units) : kn;
+            s_walk[b] = w2;
+            kn = w2;
+        }
         tc_fence_before();
         __syncthreads();
-        // diagonal block `warp`: lane j < 16 solves column j of record 0 (lanes 16-31 that of
-        // record 1 when R = 2) by forward substitution,
-        // x_r = [r == j] - b_r sum_{s<r} G_rs x_s (A = Diag(b) L restricted to the block)
-        if (R == 2 || lane < 16) {
-            const int a = warp, j = lane & 15, rr_ = lane >> 4;
-            const float *bv = vb[b][rr_];
-            const float *Gd = G32 + blk(a, a);
-            float *Nd = N32 + rr_ * kTri + blk(a, a);
-            float x[16];
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) {
-                float gr[16];
-#pragma unroll
-                for (int s4 = 0; s4 < 4; ++s4) {
-                    const float4 t4 = *reinterpret_cast<const float4 *>(Gd + 16 * rr + ((4 * s4) ^ sw(rr)));
-                    gr[4 * s4] = t4.x, gr[4 * s4 + 1] = t4.y, gr[4 * s4 + 2] = t4.z, gr[4 * s4 + 3] = t4.w;
-                }
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int s = 0; s < rr; ++s) acc[s & 3] = fmaf(gr[s], x[s], acc[s & 3]);
-                x[rr] = fmaf(-bv[vbi(16 * a + rr)], (acc[0] + acc[1]) + (acc[2] + acc[3]), (rr == j) ? 1.f : 0.f);
-            }
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) Nd[16 * rr + (j ^ sw(rr))] = tf32r(x[rr]);
-        }
-        __syncthreads();
-        // level 1: (1,0), (2,1), (3,2) as six half-blocks; level 2: (2,0), (3,1); level 3: (3,0).
-        // Warps 0-1 take one half-block per level, warps 2-3 two in level 1 and none in level 3.
-        // Each half-block is done for every record of the unit.
-#pragma unroll
-        for (int rr = 0; rr < R; ++rr) {
-            half_block(G32, N32 + rr * kTri, Tw, vb[b][rr], 1 + (warp >> 1), warp >> 1, warp & 1, lane);
-            if (warp >= 2) half_block(G32, N32 + rr * kTri, Tw, vb[b][rr], 3, 2, warp & 1, lane);
-        }
-        __syncthreads();
-#pragma unroll
-        for (int rr = 0; rr < R; ++rr)
-            half_block(G32, N32 + rr * kTri, Tw, vb[b][rr], 2 + (warp >> 1), warp >> 1, warp & 1, lane);
-        __syncthreads();
-        if (warp < 2) {
-#pragma unroll
-            for (int rr = 0; rr < R; ++rr) half_block(G32, N32 + rr * kTri, Tw, vb[b][rr], 3, 0, warp, lane);
-        }
-        // warps 2-3 have no level-3 work: the next record's gram (its k tile was requested at
-        // the top of this iteration) into the other TMEM buffer, last read a record ago
-        // and the ticket of the record after it
-        if (q == kCtl) {
-            if (ok && nxt.r < p.n_seg) ok = gram(b ^ 1);
-            s_n2[b] = nxt.r < p.n_seg ? decode<R>(p, ticket, units) : nxt;
-        }
-        __syncthreads();
-        const Walk n2 = s_n2[b];   // slot b is written again two records later
-        if (n2.r >= p.n_seg) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        // records: N Diag(b) as bf16 rows t' (blocks above the diagonal are zero)
-#pragma unroll
-        for (int m = 0; m < 4 * R; ++m) {
-            const int rr = m / 4;
-            uint8_t *dst = static_cast<uint8_t *>(p.workspace) +
-                           ((int64_t)seg.wsb + (int64_t)(cur.h + rr) * nch + cur.c) * (int64_t)kGdnRecordBytes;
-            const float *Nr = N32 + rr * kTri;
-            const int e8 = q + 128 * (m & 3);   // 8 consecutive entries of row t'
-            const int tp = e8 >> 3, s8 = (e8 & 7) * 8;
-            const int ba = tp >> 4, bb = s8 >> 4, r = tp & 15;   // block (ba, bb), row r in it
-            uint4 pk = make_uint4(0u, 0u, 0u, 0u);
-            if (bb <= ba) {
-                // the eight lanes of a row read the two halves of their 8 entries in an order
-                // chosen per lane, so that each load of N and of b touches distinct banks
-                const int h0 = 4 * ((bb & 1) ^ ((sw(r) >> 2) & 1)), h1 = h0 ^ 4;
-                const float *src = Nr + blk(ba, bb) + 16 * r;
-                const float4 x0 = *reinterpret_cast<const float4 *>(src + (((s8 & 15) + h0) ^ sw(r)));
-                const float4 x1 = *reinterpret_cast<const float4 *>(src + (((s8 & 15) + h1) ^ sw(r)));
-                const float4 b0 = *reinterpret_cast<const float4 *>(vb[b][rr] + vbi(s8 + h0));
-                const float4 b1 = *reinterpret_cast<const float4 *>(vb[b][rr] + vbi(s8 + h1));
-                const uint32_t p0 = pack_bf16x2(x0.x * b0.x, x0.y * b0.y), p1 = pack_bf16x2(x0.z * b0.z, x0.w * b0.w);
-                const uint32_t p2 = pack_bf16x2(x1.x * b1.x, x1.y * b1.y), p3 = pack_bf16x2(x1.z * b1.z, x1.w * b1.w);
-                pk = h0 == 0 ? make_uint4(p0, p1, p2, p3) : make_uint4(p2, p3, p0, p1);
-            }
-            *reinterpret_cast<uint4 *>(dst + tp * 128 + s8 * 2) = pk;
-        }
+        off_diagonal<R>(sG, N32, Tw, vb[b], rec, warp, L);
         cur = nxt;
-        nxt = n2;
         beta_cur = beta_next;
     }
     if (q == kCtl) {   // after a wait gave up: let every copy and MMA in flight land first
@@ -432,16 +570,20 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// Four CTAs per SM: the two operand tiles, G and N (the level products' 16 x 8 scratch sits in
-// the Kh tile once its store has read it; the token halves' gate sums at the start of G).
+// Four CTAs per SM: the two operand tiles, G and N (the level products' scratch tiles sit in the
+// Kh tile once its store has read it).
 struct KdaGeo {
     static constexpr uint32_t kOffK = 0;                  // k tile, then Kt in place, 16 KB
     static constexpr uint32_t kOffH = 16384;              // Kh, then the scratch
     static constexpr uint32_t kOffG32 = 32768;            // the gram, 10 blocks
-    static constexpr uint32_t kOffN32 = kOffG32 + kTri * 4;
-    static constexpr uint32_t kSmemBytes = kOffN32 + kTri * 4 + 1024;
+    static constexpr uint32_t kOffN32 = kOffG32 + kGWords * 4;
+    static constexpr uint32_t kSmemBytes = kOffN32 + kNRec * 4 + 1024;
     static constexpr int kCtasPerSm = 4;
 };
+static_assert(4 * 2 * kTile * 4 <= 16384, "the scratch tiles fit in the Kh tile");
+// warp 3 lane 0 issues loads, grams and the operand stores: its wait for the stores' reads comes
+// after its diagonal solve, which its larger share of gram rows delays anyway
+constexpr int kKdaCtl = 96;
 
 __global__ void __launch_bounds__(kThreads, KdaGeo::kCtasPerSm)
 build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_constant__ CUtensorMap tmK,
@@ -451,9 +593,10 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ uint64_t kfull, gfull;
     __shared__ uint32_t tslot;
-    __shared__ Walk s_n2[2];
+    __shared__ Walk s_walk[2];
     __shared__ float s_max[4];
-    __shared__ __align__(16) float vb[kVb];
+    __shared__ float2 s_part[2][64];                  // [token half][channel pair]
+    __shared__ __align__(16) float vb[2][1][kVb];     // two units' b
 
     const int64_t total = total_records(p);
     unsigned *tickets = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(p.workspace) + total * kGdnRecordBytes);
@@ -463,8 +606,9 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     uint8_t *tK = smem + G::kOffK, *tH = smem + G::kOffH;
     float *G32 = reinterpret_cast<float *>(smem + G::kOffG32);
     float *N32 = reinterpret_cast<float *>(smem + G::kOffN32);
-    float *Tw = reinterpret_cast<float *>(tH) + warp * 16 * kLDT;
-    float2 (*s_part)[64] = reinterpret_cast<float2 (*)[64]>(G32);   // [token half][channel pair]
+    float *Tw = reinterpret_cast<float *>(tH) + warp * 2 * kTile;
+    const uint32_t sG = smem_u32(G32);
+    const Lanes L = lanes_of(lane);
 
     if (q == 0) {
         mbar_init(&kfull, 1);
@@ -477,9 +621,9 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     tc_fence_after();
     const uint32_t tmem = tslot;
     constexpr uint32_t idG = idesc(kFmtBF16, kFmtBF16, false, false, 64, 64);
-    int kiss = 0, giss = 0, kwait = 0, gwait = 0;   // issued by thread kCtl; waited by every thread
-    bool stored = false;                             // thread kCtl: a group of record stores issued
-    auto load_k = [&](const Walk &w) {   // thread kCtl
+    int kiss = 0, giss = 0, kwait = 0, gwait = 0;   // issued by thread kKdaCtl; waited by every thread
+    bool stored = false;                             // thread kKdaCtl: a group of record stores issued
+    auto load_k = [&](const Walk &w) {   // thread kKdaCtl
         ++kiss;
         const int32_t t0 = p.seg[w.r].start + w.c * C;
         mbar_arrive_expect_tx(&kfull, 16384);
@@ -487,9 +631,9 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         tma_load_3d(tK + 8192, &tmK, &kfull, 64, w.h / p.gqa, t0);
     };
     bool ok = true;
-    int64_t ticket = 0;   // thread kCtl
+    int64_t ticket = 0;   // thread kKdaCtl
     Walk nxt = decode<1>(p, (int64_t)gridDim.x + blockIdx.x, total);
-    if (q == kCtl) {
+    if (q == kKdaCtl) {
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmKt);
         prefetch_tmap(&tmKh);
@@ -517,19 +661,22 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     };
     load_gates(cur);
     for (int i = 0; cur.r < p.n_seg; ++i) {
+        const int b = i & 1;
         const SegEntry seg = p.seg[cur.r];
         const int nch = (seg.len + C - 1) / C;
-        const int64_t rec = (int64_t)seg.wsb + (int64_t)cur.h * nch + cur.c;
-        if (!in_bounds(cur.c < nch && cur.h < p.H_v && rec < total, p.err)) break;   // uniform
+        const int64_t rec_i = (int64_t)seg.wsb + (int64_t)cur.h * nch + cur.c;
+        if (!in_bounds(cur.c < nch && cur.h < p.H_v && rec_i < total, p.err)) break;   // uniform
+        uint8_t *const rec[1] = {static_cast<uint8_t *>(p.workspace) + rec_i * kGdnRecordBytes};
         // (1) b of the unit; the pair's log-decay over this token half
-        if (q < C) vb[vbi(q)] = beta_cur;
+        if (q < C) vb[b][0][vbi(q)] = beta_cur;
         {
             float2 sh = make_float2(0.f, 0.f);
 #pragma unroll
             for (int t = 0; t < CH; ++t) sh.x += g[t].x, sh.y += g[t].y;
             s_part[th][pc] = sh;
         }
-        if (q == kCtl && nxt.r < p.n_seg) ticket = 2 * (int64_t)gridDim.x + atomicAdd(tickets, 1u);
+        if (q == kKdaCtl && nxt.r < p.n_seg) ticket = 2 * (int64_t)gridDim.x + atomicAdd(tickets, 1u);
+        zero_upper<1, kThreads>(rec, q);
         ok = ok && mbar_wait(&kfull, kwait & 1, p.err, kErrTimeout);
         ++kwait;
         if (!__syncthreads_and(ok)) break;   // uniform
@@ -559,7 +706,7 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         if (lane == 0) s_max[warp] = mx;
         fence_async_shared();   // Kt and Kh are read by the tensor core and the bulk stores
         __syncthreads();
-        if (q == kCtl) {
+        if (q == kKdaCtl) {
             tc_fence_after();
             // the gram Kt Kh^T (M = 64) into TMEM; the read-out below waits for it
             const uint32_t a0 = smem_u32(tK), b0 = smem_u32(tH);
@@ -572,7 +719,7 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
             mma_commit(&gfull);
             ++giss;
             // Kt and Kh to their records (64 rows each, two 64-channel boxes)
-            const int32_t row = (int32_t)(rec * C);
+            const int32_t row = (int32_t)(rec_i * C);
             tma_store_2d(&tmKt, tK, 0, row);
             tma_store_2d(&tmKt, tK + 8192, 64, row);
             tma_store_2d(&tmKh, tH, 0, row);
@@ -582,7 +729,7 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
         }
         {
             const float m = fmaxf(fmaxf(s_max[0], s_max[1]), fmaxf(s_max[2], s_max[3]));
-            float *side = p.kda_side + rec * kKdaSide;
+            float *side = p.kda_side + rec_i * kKdaSide;
             if (th == 0) reinterpret_cast<float2 *>(side)[pc] = cC;
             if (q == 0) side[128] = m;
         }
@@ -607,80 +754,31 @@ build_kda_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
                         float4 g4 = make_float4(__uint_as_float(gr[4 * s4]), __uint_as_float(gr[4 * s4 + 1]),
                                                 __uint_as_float(gr[4 * s4 + 2]), __uint_as_float(gr[4 * s4 + 3]));
                         if (k < warp) g4 = make_float4(tf32r(g4.x), tf32r(g4.y), tf32r(g4.z), tf32r(g4.w));
-                        *reinterpret_cast<float4 *>(G32 + blk(warp, k) + 16 * r + (cb ^ sw(r))) = g4;
+                        *reinterpret_cast<float4 *>(G32 + gblk(warp, k) + 16 * r + (cb ^ sw(r))) = g4;
                     }
                 }
             }
         }
-        tc_fence_before();
-        __syncthreads();
+        __syncwarp();   // the diagonal block's rows were stored by this warp
+        diag_blocks<1>(G32, N32, vb[b], rec, warp, lane);
         // the stores must have read Kt and Kh before the next k tile lands over Kt and the
         // level products' scratch is written over Kh (after the barrier below); the next unit's
-        // gates
-        if (q == kCtl) {
+        // gates and walk
+        if (q == kKdaCtl) {
             bulk_wait_read<0>();
             if (nxt.r < p.n_seg) load_k(nxt);
+            s_walk[b] = nxt.r < p.n_seg ? decode<1>(p, ticket, total) : nxt;
         }
         if (nxt.r < p.n_seg) load_gates(nxt);
-        // diagonal blocks by forward substitution, lane j < 16 of warp a: column j of block a
-        if (lane < 16) {
-            const int a = warp, j = lane;
-            const float *Gd = G32 + blk(a, a);
-            float *Nd = N32 + blk(a, a);
-            float x[16];
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) {
-                float gr[16];
-#pragma unroll
-                for (int s4 = 0; s4 < 4; ++s4) {
-                    const float4 t4 = *reinterpret_cast<const float4 *>(Gd + 16 * rr + ((4 * s4) ^ sw(rr)));
-                    gr[4 * s4] = t4.x, gr[4 * s4 + 1] = t4.y, gr[4 * s4 + 2] = t4.z, gr[4 * s4 + 3] = t4.w;
-                }
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int s = 0; s < rr; ++s) acc[s & 3] = fmaf(gr[s], x[s], acc[s & 3]);
-                x[rr] = fmaf(-vb[vbi(16 * a + rr)], (acc[0] + acc[1]) + (acc[2] + acc[3]), (rr == j) ? 1.f : 0.f);
-            }
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) Nd[16 * rr + (j ^ sw(rr))] = tf32r(x[rr]);
-        }
+        tc_fence_before();
         __syncthreads();
-        half_block(G32, N32, Tw, vb, 1 + (warp >> 1), warp >> 1, warp & 1, lane);
-        if (warp >= 2) half_block(G32, N32, Tw, vb, 3, 2, warp & 1, lane);
-        __syncthreads();
-        half_block(G32, N32, Tw, vb, 2 + (warp >> 1), warp >> 1, warp & 1, lane);
-        __syncthreads();
-        if (warp < 2) half_block(G32, N32, Tw, vb, 3, 0, warp, lane);
-        if (q == kCtl) s_n2[i & 1] = nxt.r < p.n_seg ? decode<1>(p, ticket, total) : nxt;
-        __syncthreads();
-        const Walk n2 = s_n2[i & 1];
+        const Walk n2 = s_walk[b];   // slot b is written again two units later
         if (n2.r >= p.n_seg) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-        // the record: N Diag(b) as bf16 rows t' (blocks above the diagonal are zero)
-        uint8_t *dst = static_cast<uint8_t *>(p.workspace) + rec * kGdnRecordBytes;
-#pragma unroll
-        for (int mm = 0; mm < 4; ++mm) {
-            const int e8 = q + 128 * mm;
-            const int tp = e8 >> 3, s8 = (e8 & 7) * 8;
-            const int ba = tp >> 4, bb = s8 >> 4, r = tp & 15;
-            uint4 pk = make_uint4(0u, 0u, 0u, 0u);
-            if (bb <= ba) {
-                const int h0 = 4 * ((bb & 1) ^ ((sw(r) >> 2) & 1)), h1 = h0 ^ 4;
-                const float *src = N32 + blk(ba, bb) + 16 * r;
-                const float4 x0 = *reinterpret_cast<const float4 *>(src + (((s8 & 15) + h0) ^ sw(r)));
-                const float4 x1 = *reinterpret_cast<const float4 *>(src + (((s8 & 15) + h1) ^ sw(r)));
-                const float4 b0 = *reinterpret_cast<const float4 *>(vb + vbi(s8 + h0));
-                const float4 b1 = *reinterpret_cast<const float4 *>(vb + vbi(s8 + h1));
-                const uint32_t p0 = pack_bf16x2(x0.x * b0.x, x0.y * b0.y), p1 = pack_bf16x2(x0.z * b0.z, x0.w * b0.w);
-                const uint32_t p2 = pack_bf16x2(x1.x * b1.x, x1.y * b1.y), p3 = pack_bf16x2(x1.z * b1.z, x1.w * b1.w);
-                pk = h0 == 0 ? make_uint4(p0, p1, p2, p3) : make_uint4(p2, p3, p0, p1);
-            }
-            *reinterpret_cast<uint4 *>(dst + tp * 128 + s8 * 2) = pk;
-        }
-        __syncthreads();   // every read of vb, G32, N32 and the scratch done before the next unit
+        off_diagonal<1>(sG, N32, Tw, vb[b], rec, warp, L);
         cur = nxt;
         nxt = n2;
     }
-    if (q == kCtl) {   // the record stores complete; after a wait gave up, every copy and MMA lands
+    if (q == kKdaCtl) {   // the record stores complete; after a wait gave up, every copy and MMA lands
         if (stored) bulk_wait<0>();
         for (; kwait < kiss; ++kwait) mbar_wait(&kfull, kwait & 1, nullptr, 0);
         for (; gwait < giss; ++gwait) mbar_wait(&gfull, gwait & 1, nullptr, 0);
