@@ -27,7 +27,8 @@
 // blocks are solved (two TMEM buffers), and b is loaded a unit ahead, so loads and grams
 // overlap the inversions. A CTA that is on its last unit lets the chain kernel launch
 // (programmatic dependent launch); the chain waits for this grid's completion before it reads
-// any record. Three CTA barriers per unit:
+// any record. Three CTA barriers per unit: at its top, after the diagonal solves, and between
+// steps 4 (ii) and (iii). Per unit:
 //   1. TMA the chunk's k (two 128B-swizzled 64-channel halves); b masked past the segment end.
 //   2. One thread issues the gram K K^T (M = 64 tcgen05 MMA, fp32 accumulator in TMEM).
 //   3. Warp w reads block row w of the raw gram G = K K^T into shared memory as 16 x 16 blocks:
