@@ -69,17 +69,18 @@ constexpr int C = kGdnChunk;
 constexpr int kThreads = 128;
 // Shared-memory layout. G keeps its ten 16 x 16 blocks on and below the diagonal, block (a, b)
 // at word 256 (a (a + 1) / 2 + b), row-major with element (r, c) at 16 r + (c ^ sw(r)). N keeps,
-// per record, the blocks its products read: row-major (the same swizzle) N11, N22, N32, N33 (A
-// operands) and transposed, with element (r, c) at kLdT c + r, N00, N10, N11, N22 (B operands).
-// The swizzle and the transposed row stride of 20 words make every ldmatrix phase (8 rows of 16
-// bytes), the diagonal solves' stores and the result stores touch 32 distinct banks. A record's
-// N takes kNRec words, 16 more than its blocks, so that the second record's row-major blocks sit
+// per record, the blocks its products read: row-major N11, N22, N32, N33 (A operands) and
+// transposed N00, N10, N11, N22 (B operands: element (r, c) at 16 c + (r ^ sw(c))). The swizzle
+// makes every ldmatrix phase (8 rows of 16 bytes), the gram's and the diagonal solves' stores
+// and the step (ii) stores of N32 touch 32 distinct banks (those of N10 touch 16). A record's N
+// takes kNRec words, 16 more than its blocks, so that the second record's row-major blocks sit
 // 16 banks after the first's (the two records' diagonal solves store side by side). Each warp
-// has two 16 x 8 scratch tiles T, held transposed (8 rows of stride kLdT).
+// has 2 R scratch tiles T (16 x 8), held transposed as 8 rows of stride kLdT = 20 words, which
+// keeps both their stores from the accumulators and their ldmatrix reads conflict-free.
 constexpr int kLdT = 20;
 constexpr int kN11 = 0, kN22 = 256, kN32 = 512, kN33 = 768;                 // row-major
-constexpr int kT00 = 1024, kT10 = kT00 + 16 * kLdT, kT11 = kT10 + 16 * kLdT, kT22 = kT11 + 16 * kLdT;
-constexpr int kNRec = kT22 + 16 * kLdT + 16;
+constexpr int kT00 = 1024, kT10 = 1280, kT11 = 1536, kT22 = 1792;           // transposed
+constexpr int kNRec = 2048 + 16;
 constexpr int kGWords = 10 * 256;
 constexpr int kTile = 8 * kLdT;   // one transposed 16 x 8 T tile
 __device__ __forceinline__ int sw(int r) { return ((r << 2) & 8) | (r & 4); }
@@ -96,8 +97,8 @@ struct PrepGeo {
     static constexpr uint32_t kOffK = 0;                              // k tile, 16 KB
     static constexpr uint32_t kOffG32 = 16384;                        // the gram K K^T, 10 blocks
     static constexpr uint32_t kOffN32 = kOffG32 + kGWords * 4;        // R x N (tf32-rounded)
-    static constexpr uint32_t kOffT = kOffN32 + R * kNRec * 4;        // 4 warps x 2 tiles
-    static constexpr uint32_t kSmemBytes = kOffT + 4 * 2 * kTile * 4 + 1024;
+    static constexpr uint32_t kOffT = kOffN32 + R * kNRec * 4;        // 4 warps x 2 R tiles
+    static constexpr uint32_t kSmemBytes = kOffT + 4 * 2 * R * kTile * 4 + 1024;
     static constexpr int kCtasPerSm = 4;                              // 4 x 128 TMEM columns
 };
 constexpr int kCtl = 0;   // warp 0 lane 0 issues loads and grams (warp 0 reads the fewest gram rows)
@@ -132,7 +133,8 @@ __device__ __forceinline__ void mma_m16n8k8(float (&c)[4], const uint32_t (&a)[4
 // accumulator: rows g, g + 8, columns 2 t, 2 t + 1.
 struct Lanes {
     uint32_t a0, a1;   // A fragments, k-steps 0 and 1, of a row-major 16 x 16 block
-    uint32_t b;        // B fragments, both k-steps, of rows 0-7 of a transposed block or a T tile
+    uint32_t bn;       // B fragments, both k-steps, of rows 0-7 of a transposed block of N
+    uint32_t b;        // B fragments, both k-steps, of a T tile
     int g, t;
 };
 
@@ -142,7 +144,9 @@ __device__ __forceinline__ Lanes lanes_of(int lane) {
     const int r = (lane & 7) | (lane & 8), c = 4 * (lane >> 4);
     L.a0 = 4u * (uint32_t)(16 * r + (c ^ sw(r)));
     L.a1 = 4u * (uint32_t)(16 * r + ((8 + c) ^ sw(r)));
-    // matrices 0-3 of a B fragment: columns 0-7 of k-rows 0-3, 4-7, 8-11, 12-15
+    // matrices 0-3 of a B fragment: columns 0-7 of k-rows 0-3, 4-7, 8-11, 12-15 (rows 8-15 of a
+    // transposed block share the swizzle of rows 0-7)
+    L.bn = 4u * (uint32_t)(16 * (lane & 7) + ((4 * (lane >> 3)) ^ sw(lane & 7)));
     L.b = 4u * (uint32_t)(kLdT * (lane & 7) + 4 * (lane >> 3));
     L.g = lane >> 2;
     L.t = lane & 3;
@@ -210,10 +214,10 @@ __device__ __forceinline__ void diag_blocks(const float *G32, float *N32, const 
             for (int rr = 0; rr < 16; ++rr) Nd[16 * rr + (j ^ sw(rr))] = tf32r(x[rr]);
         }
         if (a <= 2) {   // transposed copy: N00, N11, N22 (column j is row j)
-            float *Td = Nr + (a == 0 ? kT00 : a == 1 ? kT11 : kT22) + kLdT * j;
+            float *Td = Nr + (a == 0 ? kT00 : a == 1 ? kT11 : kT22) + 16 * j;
 #pragma unroll
             for (int s4 = 0; s4 < 4; ++s4)
-                *reinterpret_cast<float4 *>(Td + 4 * s4) = make_float4(
+                *reinterpret_cast<float4 *>(Td + ((4 * s4) ^ sw(j))) = make_float4(
                     tf32r(x[4 * s4]), tf32r(x[4 * s4 + 1]), tf32r(x[4 * s4 + 2]), tf32r(x[4 * s4 + 3]));
         }
         const float bj = bv[vbi(16 * a + j)];
@@ -238,7 +242,7 @@ __device__ __forceinline__ void level_one(uint32_t sG, float *N32, float *Tw, co
     ldsm4(ga2, sG + 4u * gblk(a, b) + L.a1);
 #pragma unroll
     for (int rr = 0; rr < R; ++rr)
-        ldsm4(y[rr], sN + 4u * (uint32_t)(rr * kNRec + (B32 ? kT22 : kT00) + 8 * kLdT * h) + L.b);
+        ldsm4(y[rr], sN + 4u * (uint32_t)(rr * kNRec + (B32 ? kT22 : kT00) + 128 * h) + L.bn);
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {
         float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -258,50 +262,67 @@ __device__ __forceinline__ void level_one(uint32_t sG, float *N32, float *Tw, co
             float *o = Nr + kN32 + ((8 * h + 2 * L.t) ^ sw(L.g));   // rows g and g + 8 share the swizzle
             *reinterpret_cast<float2 *>(o + 16 * L.g) = make_float2(tf32r(-d[0]), tf32r(-d[1]));
             *reinterpret_cast<float2 *>(o + 16 * (L.g + 8)) = make_float2(tf32r(-d[2]), tf32r(-d[3]));
-        } else {
-            float *o = Nr + kT10 + kLdT * (8 * h + 2 * L.t) + L.g;
-            o[0] = tf32r(-d[0]);
-            o[kLdT] = tf32r(-d[1]);
-            o[8] = tf32r(-d[2]);
-            o[kLdT + 8] = tf32r(-d[3]);
+        } else {   // N10 transposed: rows n = 8 h + 2 t, + 1 (the same swizzle), columns g, g + 8
+            const int n = 8 * h + 2 * L.t;
+            float *o = Nr + kT10 + 16 * n;
+            o[L.g ^ sw(n)] = tf32r(-d[0]);
+            o[16 + (L.g ^ sw(n + 1))] = tf32r(-d[1]);
+            o[(L.g + 8) ^ sw(n)] = tf32r(-d[2]);
+            o[16 + ((L.g + 8) ^ sw(n + 1))] = tf32r(-d[3]);
         }
         put_rec(rec[rr], 16 * a, 16 * b + 8 * h, d, vb[rr], L);
     }
     __syncwarp();   // the scratch tiles are rewritten by this warp's next piece
 }
 
-// Step 4 (iii): columns 16 X + 8 h .. + 7 of the lower-left quarter of one record:
-// T2, T3 = Diag(b) (G21 N11) rows 32-47, 48-63 (N11's block column X: blocks 0-1 for X = 0,
-// block 1 for X = 1), then N(2,X) = -N22 T2 and N(3,X) = -(N32 T2 + N33 T3), straight into the
-// record.
-template <int X>
-__device__ __forceinline__ void level_two(uint32_t sG, const float *Nr, float *Tw, const float *bv, uint8_t *rec,
-                                          int h, const Lanes &L) {
-    const uint32_t sN = smem_u32(Nr), sT = smem_u32(Tw), hoff = 4u * (uint32_t)(8 * kLdT * h);
-    float c2[4] = {0.f, 0.f, 0.f, 0.f}, c3[4] = {0.f, 0.f, 0.f, 0.f};
-    uint32_t y[4];
-    if (X == 0) {
-        ldsm4(y, sN + 4u * kT00 + hoff + L.b);
-        mma16(c2, sG + 4u * gblk(2, 0), y, L);
-        mma16(c3, sG + 4u * gblk(3, 0), y, L);
-        ldsm4(y, sN + 4u * kT10 + hoff + L.b);
-    } else {
-        ldsm4(y, sN + 4u * kT11 + hoff + L.b);
+// Step 4 (iii): columns 16 X + 8 h .. + 7 of the lower-left quarter of R records (record rr takes
+// block column X ^ rr, in scratch tiles 2 rr and 2 rr + 1; the records' products run side by
+// side): T2, T3 = Diag(b) (G21 N11) rows 32-47, 48-63 (N11's block column: blocks 0-1 for column
+// 0, block 1 for column 1), then N(2,.) = -N22 T2 and N(3,.) = -(N32 T2 + N33 T3), straight into
+// the record.
+template <int X, int R>
+__device__ __forceinline__ void level_two(uint32_t sG, const float *N32, float *Tw, const float (*vb)[kVb],
+                                          uint8_t *const (&rec)[R], int h, const Lanes &L) {
+    const uint32_t sN = smem_u32(N32), sT = smem_u32(Tw), hoff = 4u * (uint32_t)(128 * h);
+    float c2[R][4], c3[R][4];
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        const int x = X ^ rr;
+        const uint32_t nb = sN + 4u * (uint32_t)(rr * kNRec) + hoff + L.bn;
+        uint32_t y[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) c2[rr][i] = c3[rr][i] = 0.f;
+        if (x == 0) {
+            ldsm4(y, nb + 4u * kT00);
+            mma16(c2[rr], sG + 4u * gblk(2, 0), y, L);
+            mma16(c3[rr], sG + 4u * gblk(3, 0), y, L);
+            ldsm4(y, nb + 4u * kT10);
+        } else {
+            ldsm4(y, nb + 4u * kT11);
+        }
+        mma16(c2[rr], sG + 4u * gblk(2, 1), y, L);
+        mma16(c3[rr], sG + 4u * gblk(3, 1), y, L);
     }
-    mma16(c2, sG + 4u * gblk(2, 1), y, L);
-    mma16(c3, sG + 4u * gblk(3, 1), y, L);
-    put_t(Tw, c2, bv[vbi(32 + L.g)], bv[vbi(40 + L.g)], L);
-    put_t(Tw + kTile, c3, bv[vbi(48 + L.g)], bv[vbi(56 + L.g)], L);
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        put_t(Tw + 2 * rr * kTile, c2[rr], vb[rr][vbi(32 + L.g)], vb[rr][vbi(40 + L.g)], L);
+        put_t(Tw + (2 * rr + 1) * kTile, c3[rr], vb[rr][vbi(48 + L.g)], vb[rr][vbi(56 + L.g)], L);
+    }
     __syncwarp();
-    float d2[4] = {0.f, 0.f, 0.f, 0.f}, d3[4] = {0.f, 0.f, 0.f, 0.f};
-    ldsm4(y, sT + L.b);
-    mma16(d2, sN + 4u * kN22, y, L);
-    mma16(d3, sN + 4u * kN32, y, L);
-    ldsm4(y, sT + 4u * kTile + L.b);
-    mma16(d3, sN + 4u * kN33, y, L);
-    put_rec(rec, 32, 16 * X + 8 * h, d2, bv, L);
-    put_rec(rec, 48, 16 * X + 8 * h, d3, bv, L);
-    __syncwarp();   // T is rewritten by this warp's next piece
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        const uint32_t na = sN + 4u * (uint32_t)(rr * kNRec);
+        float d2[4] = {0.f, 0.f, 0.f, 0.f}, d3[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t y[4];
+        ldsm4(y, sT + 4u * (uint32_t)(2 * rr * kTile) + L.b);
+        mma16(d2, na + 4u * kN22, y, L);
+        mma16(d3, na + 4u * kN32, y, L);
+        ldsm4(y, sT + 4u * (uint32_t)((2 * rr + 1) * kTile) + L.b);
+        mma16(d3, na + 4u * kN33, y, L);
+        put_rec(rec[rr], 32, 16 * (X ^ rr) + 8 * h, d2, vb[rr], L);
+        put_rec(rec[rr], 48, 16 * (X ^ rr) + 8 * h, d3, vb[rr], L);
+    }
+    __syncwarp();   // the scratch tiles are rewritten by this warp's next piece
 }
 
 // The record's blocks above the diagonal, as zeros: 192 pieces of 16 bytes per record (block
@@ -323,7 +344,7 @@ __device__ __forceinline__ void zero_upper(uint8_t *const (&rec)[R], int q) {
 // (ii): warps 0-1 take the halves of (1,0), warps 2-3 those of (3,2), for every record. Step
 // (iii): warp w takes
 // column half h = w % 2 of block column w / 2 of record 0 and, when R = 2, of the other block
-// column of record 1, so that every warp has the same work.
+// column of record 1, so that every warp has the same work; the two records' pieces interleave.
 template <int R>
 __device__ __forceinline__ void off_diagonal(uint32_t sG, float *N32, float *Tw, const float (*vb)[kVb],
                                              uint8_t *const (&rec)[R], int warp, const Lanes &L) {
@@ -331,11 +352,8 @@ __device__ __forceinline__ void off_diagonal(uint32_t sG, float *N32, float *Tw,
     if (warp < 2) level_one<false, R>(sG, N32, Tw, vb, rec, h, L);
     else level_one<true, R>(sG, N32, Tw, vb, rec, h, L);
     __syncthreads();
-#pragma unroll
-    for (int rr = 0; rr < R; ++rr) {
-        if ((warp >> 1) == rr) level_two<0>(sG, N32 + rr * kNRec, Tw, vb[rr], rec[rr], h, L);
-        else level_two<1>(sG, N32 + rr * kNRec, Tw, vb[rr], rec[rr], h, L);
-    }
+    if (warp < 2) level_two<0, R>(sG, N32, Tw, vb, rec, h, L);
+    else level_two<1, R>(sG, N32, Tw, vb, rec, h, L);
 }
 
 // Work units (R records each) are numbered in the order (segment rank, chunk, value heads
@@ -388,7 +406,7 @@ build_gdn_prep_kernel(const __grid_constant__ BuildParams p, const __grid_consta
     const int q = threadIdx.x, warp = q >> 5, lane = q & 31;
     float *G32 = reinterpret_cast<float *>(smem + G::kOffG32);
     float *N32 = reinterpret_cast<float *>(smem + G::kOffN32);   // record rr at N32 + rr * kNRec
-    float *Tw = reinterpret_cast<float *>(smem + G::kOffT) + warp * 2 * kTile;
+    float *Tw = reinterpret_cast<float *>(smem + G::kOffT) + warp * 2 * R * kTile;
     const uint32_t sG = smem_u32(G32);
     const Lanes L = lanes_of(lane);
 

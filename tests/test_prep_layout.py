@@ -4,9 +4,9 @@
 G (the chunk's gram) keeps its ten 16 x 16 blocks on and below the diagonal, block (a, b) at word
 256 (a (a + 1) / 2 + b), row-major with element (r, c) at 16 r + (c ^ sw(r)), sw(r) = 8 bit1(r) +
 4 bit2(r). N keeps, per record, the row-major blocks N11, N22, N32, N33 (A operands, the same
-swizzle) and the transposed blocks N00, N10, N11, N22 (B operands: element (r, c) at 20 c + r).
-The products' scratch tiles T (16 x 8) are transposed too. The b values of a record sit at
-e + 16 (e >> 5). The tests restate those index functions and every access of the kernel, and
+swizzle) and the transposed blocks N00, N10, N11, N22 (B operands: element (r, c) at
+16 c + (r ^ sw(c))). The products' scratch tiles T (16 x 8) are transposed, element (m, n) at
+20 n + m. The b values of a record sit at e + 16 (e >> 5). The tests restate those index functions and every access of the kernel, and
 check that
 
 - the ldmatrix row addresses deliver each lane exactly the elements of the m16n8k8 tf32 A and B
@@ -27,8 +27,8 @@ import pytest
 
 LDT = 20
 N11, N22, N32, N33 = 0, 256, 512, 768
-T00, T10, T11, T22 = 1024, 1024 + 16 * LDT, 1024 + 32 * LDT, 1024 + 48 * LDT
-NREC = T22 + 16 * LDT + 16
+T00, T10, T11, T22 = 1024, 1280, 1536, 1792
+NREC = 2048 + 16
 GW = 10 * 256
 TILE = 8 * LDT
 KDA_SCRATCH = 16384   # the Kh tile the KDA preparation's scratch tiles sit in
@@ -47,7 +47,13 @@ def el_rm(base, r, c, swizzle=sw):
 
 
 def el_t(base, r, c):
-    return base + LDT * c + r
+    """Element (r, c) of a block of N stored transposed."""
+    return base + 16 * c + (r ^ sw(c))
+
+
+def el_tile(base, m, n):
+    """Element (m, n) of a 16 x 8 scratch tile (stored transposed)."""
+    return base + LDT * n + m
 
 
 def vbi(e):
@@ -99,7 +105,13 @@ def a_addrs(base, ks, swizzle=sw):
 
 
 def b_addrs(base, h):
-    return [base + LDT * (8 * h + (l & 7)) + 4 * (l >> 3) for l in range(32)]
+    """B fragments of columns 8 h .. 8 h + 7 of a transposed block of N."""
+    return [base + 16 * (8 * h + (l & 7)) + ((4 * (l >> 3)) ^ sw(l & 7)) for l in range(32)]
+
+
+def tile_addrs(base):
+    """B fragments of a scratch tile."""
+    return [base + LDT * (l & 7) + 4 * (l >> 3) for l in range(32)]
 
 
 def test_a_fragments_hold_the_mma_layout():
@@ -113,22 +125,32 @@ def test_a_fragments_hold_the_mma_layout():
 
 
 def test_b_fragments_hold_the_mma_layout():
-    """B (16 x 8) = columns 8 h .. 8 h + 7 of a transposed block (or a T tile, h = 0): lane (g, t)
-    needs k-rows t, t + 4 (k-step 0) and 8 + t, 12 + t (k-step 1) of column g."""
+    """B (16 x 8) = columns 8 h .. 8 h + 7 of a transposed block, or a T tile: lane (g, t) needs
+    k-rows t, t + 4 (k-step 0) and 8 + t, 12 + t (k-step 1) of column g."""
     for h in range(2):
         got = ldsm_words(b_addrs(0, h))
         for l in range(32):
             g, t = l >> 2, l & 3
             want = [el_t(0, k, 8 * h + g) for k in (t, t + 4, 8 + t, 12 + t)]
             assert got[l] == want, (h, l)
+    got = ldsm_words(tile_addrs(0))
+    for l in range(32):
+        g, t = l >> 2, l & 3
+        assert got[l] == [el_tile(0, k, g) for k in (t, t + 4, 8 + t, 12 + t)], l
 
 
 def test_planted_transposed_operand_is_caught():
-    """Reading an A operand as if it were stored transposed delivers other elements."""
+    """A B operand read from a row-major block (the transposed copy forgotten) delivers N[g][k]
+    instead of N[k][g]: every lane off the diagonal gets other elements."""
     got = ldsm_words(b_addrs(0, 0))
-    l = 5
-    g, t = l >> 2, l & 3
-    assert got[l][0] != el_rm(0, g, t)
+    wrong = 0
+    for l in range(32):
+        g, t = l >> 2, l & 3
+        for i, k in enumerate((t, t + 4, 8 + t, 12 + t)):
+            if k != g:
+                wrong += got[l][i] != el_rm(0, k, g)
+    assert wrong == sum(1 for l in range(32) for k in ((l & 3), (l & 3) + 4, 8 + (l & 3), 12 + (l & 3))
+                        if k != (l >> 2))
 
 
 def test_ldmatrix_reads_are_conflict_free():
@@ -139,8 +161,8 @@ def test_ldmatrix_reads_are_conflict_free():
     for base in (T00, T10, T11, T22):
         for h in range(2):
             assert ldsm_wavefronts(b_addrs(base, h)) == 4, (base, h)
-    for tile in range(2):
-        assert ldsm_wavefronts(b_addrs(tile * TILE, 0)) == 4
+    for tile in range(4):
+        assert ldsm_wavefronts(tile_addrs(tile * TILE)) == 4
 
 
 def test_planted_unswizzled_layout_conflicts():
@@ -148,12 +170,13 @@ def test_planted_unswizzled_layout_conflicts():
 
 
 def result_store_addrs(kind, base, h):
-    """The four 4-byte stores of a 16 x 8 result piece (put_t, or N10 transposed), or the two
-    8-byte stores of N32 (row-major)."""
+    """The four 4-byte stores of a 16 x 8 result piece (put_t into a tile, or N10 transposed),
+    or the two 8-byte stores of N32 (row-major)."""
     out = []
-    if kind == "transposed":
+    if kind in ("tile", "transposed"):
+        el = el_tile if kind == "tile" else el_t
         for dm, dn in ((0, 0), (0, 1), (8, 0), (8, 1)):
-            out.append(([el_t(base, (l >> 2) + dm, 8 * h + 2 * (l & 3) + dn) for l in range(32)], 1))
+            out.append(([el(base, (l >> 2) + dm, 8 * h + 2 * (l & 3) + dn) for l in range(32)], 1))
     else:
         for dm in (0, 8):
             out.append(([el_rm(base, (l >> 2) + dm, 8 * h + 2 * (l & 3)) for l in range(32)], 2))
@@ -161,12 +184,14 @@ def result_store_addrs(kind, base, h):
 
 
 def test_result_stores_are_conflict_free():
-    for tile in range(2):
-        for addrs, width in result_store_addrs("transposed", tile * TILE, 0):
+    """The scratch tiles' and N32's stores take the minimum wavefronts; N10's (four stores of a
+    step (ii) piece) take two."""
+    for tile in range(4):
+        for addrs, width in result_store_addrs("tile", tile * TILE, 0):
             assert wavefronts(addrs, width) == width
     for h in range(2):
         for addrs, width in result_store_addrs("transposed", T10, h):
-            assert wavefronts(addrs, width) == width
+            assert wavefronts(addrs, width) <= 2
         for addrs, width in result_store_addrs("row-major", N32, h):
             assert wavefronts(addrs, width) == width
             assert all(el_rm(N32, r, c) + 1 == el_rm(N32, r, c + 1) for r in range(16) for c in range(0, 16, 2))
@@ -189,8 +214,11 @@ def test_diagonal_solve_stores_are_conflict_free():
             assert wavefronts(addrs, 1) == 1
     for base in (T00, T11, T22):
         for s4 in range(4):
-            addrs = [(l >> 4) * NREC + base + LDT * (l & 15) + 4 * s4 for l in range(32)]
+            addrs = [(l >> 4) * NREC + base + 16 * (l & 15) + ((4 * s4) ^ sw(l & 15)) for l in range(32)]
             assert wavefronts(addrs, 4) == 4
+            for l in range(16):   # the 16-byte piece is elements 4 s4 .. 4 s4 + 3 of row l, in order
+                assert [el_t(base, 4 * s4 + e, l) for e in range(4)] == list(
+                    range(base + 16 * l + ((4 * s4) ^ sw(l)), base + 16 * l + ((4 * s4) ^ sw(l)) + 4))
     for a in range(4):
         for rr in range(16):
             assert wavefronts([(l >> 4) * 80 + vbi(16 * a + rr) for l in range(32)], 1) == 1
@@ -210,13 +238,13 @@ def test_every_word_is_its_own_and_inside_the_allocation():
     assert NREC % 32 == 16 and NREC % 4 == 0   # record 1's row-major blocks 16 banks over
     g = {el_rm(gblk(a, b), r, c) for a in range(4) for b in range(a + 1) for r in range(16) for c in range(16)}
     assert len(g) == 10 * 256 and max(g) < GW
-    t = {tile * TILE + el_t(0, m, n) for tile in range(2) for m in range(16) for n in range(8)}
-    assert len(t) == 2 * 128 and max(t) < 2 * TILE
-    assert 4 * 2 * TILE * 4 <= KDA_SCRATCH
+    t = {tile * TILE + el_tile(0, m, n) for tile in range(4) for m in range(16) for n in range(8)}
+    assert len(t) == 4 * 128 and max(t) < 4 * TILE
+    assert 4 * 2 * TILE * 4 <= KDA_SCRATCH   # the KDA preparation (one record): two tiles a warp
     assert len({vbi(e) for e in range(64)}) == 64 and vbi(63) < 80
     # the GDN preparation's shared memory at R = 2, four CTAs per SM (the static part measured
     # by the compiler: 1344 bytes)
-    dyn = 16384 + GW * 4 + 2 * NREC * 4 + 4 * 2 * TILE * 4 + 1024
+    dyn = 16384 + GW * 4 + 2 * NREC * 4 + 4 * 4 * TILE * 4 + 1024
     assert 4 * (dyn + 1344 + 1024) <= 228 * 1024
 
 
@@ -347,7 +375,7 @@ def test_kda_tile_pass_is_conflict_free():
 
 
 # The kernel source this model was last checked against (code only; comments do not count).
-MODELLED_SOURCE = ("build_gdn_prep.cu", "189cba36e8d8")
+MODELLED_SOURCE = ("build_gdn_prep.cu", "87c7e3551c14")
 
 
 def test_model_is_checked_against_the_current_kernel_source():
