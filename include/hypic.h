@@ -137,8 +137,7 @@ typedef enum { HYPIC_BF16 = 0, HYPIC_F32 = 1 } hypic_dtype;
  *                       chunk-aligned pieces that are then composed back into its entry. A
  *                       DELTA / GDN build whose last round of units fills at most half of the
  *                       SMs builds its trailing equal-length segments as two halves each. The
- *                       pieces' S, (P,) lam follow, and for LINEAR / SCALAR / DIAG one scan
- *                       buffer.
+ *                       pieces' S, (P,) lam follow.
  *                     No part needs to start at zero. The caller owns it; its contents are
  *                     undefined after the call and it may be reused by the next call on the
  *                     same stream, but not by a call still running on another stream. It must
