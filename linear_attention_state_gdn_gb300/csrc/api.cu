@@ -305,9 +305,9 @@ bool compose_shape_ok(const hypic_compose_args *a) {
 }
 
 // The convolution-state warm-up's workspace: the heads' convolved k, v (fp32), their gathered
-// gates and b, then the two composition pieces of every (segment, value head) unit (the head
-// entries, built here, and copies of the cached rests) and, for a dense scan that cannot write
-// its last state directly (d < 128), the scan's prefix states.
+// gates and b, then the head entries of every (segment, value head) unit, built here (the
+// composition reads the cached rests where the caller keeps them), and, for a dense scan that
+// cannot write its last state directly (d < 128), the scan's prefix states.
 struct WarmupLayout {
     int64_t rows = 0;
     size_t off_kh = 0, off_vh = 0, off_gh = 0, off_bh = 0, off_S = 0, off_lam = 0, off_P = 0, off_pre = 0,
@@ -334,9 +334,9 @@ WarmupLayout warmup_layout(const hypic_warmup_args *a) {
     L.off_gh = L.off_vh + align256(R * a->H_v * D * 4);
     L.off_bh = L.off_gh + align256(a->log_gate ? R * a->H_v * (chan ? D : 1) * 4 : 0);
     L.off_S = L.off_bh + align256(a->beta ? R * a->H_v * 4 : 0);
-    L.off_lam = L.off_S + align256(2 * U * D * D * 4);
-    L.off_P = L.off_lam + align256(2 * U * (a->family == HYPIC_FAM_DIAG ? D : 1) * 4);
-    L.off_pre = L.off_P + align256(dense ? 2 * U * D * D * 4 : 0);
+    L.off_lam = L.off_S + align256(U * D * D * 4);
+    L.off_P = L.off_lam + align256(U * (a->family == HYPIC_FAM_DIAG ? D : 1) * 4);
+    L.off_pre = L.off_P + align256(dense ? U * D * D * 4 : 0);
     L.bytes = L.off_pre + align256(dense && D != 128 ? 2 * U * D * D * 4 : 0);
     return L;
 }
@@ -816,14 +816,9 @@ hypic_status hypic_conv_warmup(const hypic_warmup_args *a, void *stream) {
     const hypic_status st = hypic_build_segments(&b, stream);
     if (st != HYPIC_OK) return st;
 
-    // (3) the cached rests as the second piece, then one composition: the last state (S), the
-    //     summed lam and, dense, the product P_rest P_head
-    const size_t nls = U * (fam == HYPIC_FAM_DIAG ? D : 1) * 4;
-    e = cudaMemcpyAsync(Sp + U * D * D, a->S_rest, nS, cudaMemcpyDeviceToDevice, s);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(reinterpret_cast<uint8_t *>(lp) + nls, a->lam_rest, nls,
-                                              cudaMemcpyDeviceToDevice, s);
-    if (e == cudaSuccess && dense) e = cudaMemcpyAsync(Pp + U * D * D, a->P_rest, nS, cudaMemcpyDeviceToDevice, s);
-    if (e != cudaSuccess) return HYPIC_ERR_CUDA;
+    // (3) one composition of the head entries (segment 0) with the cached rests (segment 1, read
+    //     where the caller keeps them): the last state (S), the summed lam and, dense, the
+    //     product P_rest P_head
     ComposeParams q;
     std::memset(&q, 0, sizeof(q));
     q.family = fam;
@@ -833,6 +828,9 @@ hypic_status hypic_conv_warmup(const hypic_warmup_args *a, void *stream) {
     q.S = Sp;
     q.lam = lp;
     q.P = Pp;
+    q.S1 = a->S_rest;
+    q.lam1 = a->lam_rest;
+    q.P1 = dense ? a->P_rest : nullptr;
     q.lam_total = a->lam;
     q.P_total = dense ? a->P : nullptr;
     q.err = err;

@@ -66,9 +66,10 @@ compose_scaled_kernel(const __grid_constant__ ComposeParams p) {
         for (int a = 0; a < kAhead; ++a) {
             const int j = j0 + a;
             if (j < p.n_seg) {
-                ring[a] = ldg_stream(p.S + ((int64_t)j * p.n_units + u) * DD + e4 * 4);
+                ring[a] = ldg_stream(compose_seg(p.S, p.S1, j, p.n_units, u, DD) + e4 * 4);
                 lv[a] = !has_lam ? 0.f
-                        : diag ? p.lam[((int64_t)j * p.n_units + u) * D + row] : p.lam[(int64_t)j * p.n_units + u];
+                        : diag ? compose_seg(p.lam, p.lam1, j, p.n_units, u, D)[row]
+                               : *compose_seg(p.lam, p.lam1, j, p.n_units, u, 1);
             }
         }
 #pragma unroll
@@ -127,7 +128,9 @@ compose_dense_simt_kernel(const __grid_constant__ ComposeParams p) {
     }
 
     for (int j = trans ? 1 : 0; j < p.n_seg; ++j) {
-        const int64_t base = ((int64_t)j * p.n_units + u) * DD;
+        const int64_t base = ((int64_t)j * p.n_units + u) * DD;   // of prefix_j
+        const float *Pj = compose_seg(p.P, p.P1, j, p.n_units, u, DD);
+        const float *Sj = compose_seg(p.S, p.S1, j, p.n_units, u, DD);
         float acc[RPT][4];
 #pragma unroll
         for (int r = 0; r < RPT; ++r)
@@ -137,7 +140,7 @@ compose_dense_simt_kernel(const __grid_constant__ ComposeParams p) {
             __syncthreads();
             for (int e = tid; e < D * D / 4; e += kDenseThreads) {
                 const int r = (e * 4) / D, c = (e * 4) % D;
-                const float4 a = *reinterpret_cast<const float4 *>(p.P + base + (int64_t)r * D + c);
+                const float4 a = *reinterpret_cast<const float4 *>(Pj + (int64_t)r * D + c);
                 *reinterpret_cast<float4 *>(&A[r * LDA + c]) = a;
             }
             __syncthreads();
@@ -154,18 +157,19 @@ compose_dense_simt_kernel(const __grid_constant__ ComposeParams p) {
                 }
             }
         }
-        const float sc = trans ? 1.f : have_state ? expf(p.lam[(int64_t)j * p.n_units + u]) : 0.f;
+        const float sc = trans ? 1.f : have_state ? expf(*compose_seg(p.lam, p.lam1, j, p.n_units, u, 1)) : 0.f;
         __syncthreads();   // every thread is done reading X
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
             const int row = ty * RPT + r;
             const int64_t off = base + (int64_t)row * D + cb + tx * 4;
+            const int64_t in_off = (int64_t)row * D + cb + tx * 4;
             if (trans) {
                 *reinterpret_cast<float4 *>(&X[row * kDenseCols + tx * 4]) =
                     make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
                 continue;
             }
-            const float4 s = *reinterpret_cast<const float4 *>(p.S + off);
+            const float4 s = *reinterpret_cast<const float4 *>(Sj + in_off);
             float4 o;
             o.x = fmaf(sc, acc[r][0], s.x);
             o.y = fmaf(sc, acc[r][1], s.y);
@@ -189,7 +193,8 @@ __global__ void __launch_bounds__(256) compose_lam_total_kernel(const __grid_con
     if (i >= p.n_units * nl) return;
     float acc = 0.f;
     if (p.family != HYPIC_FAM_LINEAR)
-        for (int j = 0; j < p.n_seg; ++j) acc += p.lam[(int64_t)j * p.n_units * nl + i];
+        for (int j = 0; j < p.n_seg; ++j)
+            acc += (j == 1 && p.lam1) ? p.lam1[i] : p.lam[(int64_t)j * p.n_units * nl + i];
     p.lam_total[i] = acc;
 }
 

@@ -369,7 +369,7 @@ int sm_count() {
 // Plain scans (no totals, no merge) of d = 128 whose (unit, column block) tiles all fit on the
 // SMs at once.
 bool compose_dense_cols_supported(const ComposeParams &p) {
-    if (p.D != D || p.lam_total || p.P_total || p.prefix_last) return false;
+    if (p.D != D || p.lam_total || p.P_total || p.prefix_last || p.S1) return false;
     if ((int64_t)p.n_seg * p.n_units * D > INT32_MAX) return false;
     const int sms = sm_count();
     return sms > 0 && p.n_units * kCols <= sms;

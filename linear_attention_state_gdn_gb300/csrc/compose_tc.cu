@@ -96,7 +96,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                         const __grid_constant__ CUtensorMap tmP,
                         const __grid_constant__ CUtensorMap tmS,
-                        const __grid_constant__ CUtensorMap tmQ) {
+                        const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmP1,
+                        const __grid_constant__ CUtensorMap tmS1) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-aligned base, derived by offsetting the shared array itself so that the
     // compiler keeps the shared address space (plain ld/st.shared, not generic accesses)
@@ -144,12 +146,18 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
             prefetch_tmap(&tmP);
             prefetch_tmap(&tmS);
             prefetch_tmap(&tmQ);
+            if (FUSED && p.S1) {
+                prefetch_tmap(&tmP1);
+                prefetch_tmap(&tmS1);
+            }
             uint32_t pc = 0, sc = 0;
             for (int ux = blockIdx.x; ux < UT && !abort_flag; ux += gridDim.x) {
                 const bool tr = ux >= U;
                 const int u = tr ? ux - U : ux;
                 for (int j = 0; j < NS; ++j) {
-                    const int32_t row = (int32_t)(((int64_t)j * U + u) * D);
+                    // segment 1 in arrays of its own (fused instance only)
+                    const bool sep = FUSED && j == 1 && p.S1 != nullptr;
+                    const int32_t row = sep ? (int32_t)((int64_t)u * D) : (int32_t)(((int64_t)j * U + u) * D);
                     if (j > 0 || (has_s0 && !tr)) {
                         const uint32_t st = pc & 1, use = pc >> 1;
                         if (use >= 1 && !mbar_wait_or_abort(&bars.p_empty[st], (use - 1) & 1, p.err,
@@ -157,8 +165,8 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                             goto producer_done;
                         mbar_arrive_expect_tx(&bars.p_full[st], kTile);
                         for (int b = 0; b < 4; ++b)
-                            tma_load_2d(smem + kOffP + st * kTile + b * kBlock, &tmP, &bars.p_full[st],
-                                        32 * b, row);
+                            tma_load_2d(smem + kOffP + st * kTile + b * kBlock, sep ? &tmP1 : &tmP,
+                                        &bars.p_full[st], 32 * b, row);
                         ++pc;
                     }
                     if (tr && j > 0) continue;   // the transition chain adds no S
@@ -166,7 +174,7 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                                                        kErrTimeout, &abort_flag))
                         goto producer_done;
                     mbar_arrive_expect_tx(&bars.s_full, kTile);
-                    tma_load_2d(smem + kOffS, tr ? &tmQ : &tmS, &bars.s_full, 0, row);   // Q_0 = P_0
+                    tma_load_2d(smem + kOffS, tr ? &tmQ : sep ? &tmS1 : &tmS, &bars.s_full, 0, row);   // Q_0 = P_0
                     ++sc;
                 }
             }
@@ -339,8 +347,11 @@ compose_dense_tc_kernel(const __grid_constant__ ComposeParams p,
                     ++sc;
                 }
                 const bool next = j + 1 < NS;
-                const float scale_next = !next ? 0.f : tr ? s_pow : expf(p.lam[(int64_t)(j + 1) * U + u]);
-                if (FUSED && t == 0 && p.lam_total) lsum += p.lam[(int64_t)j * U + u];
+                const float scale_next =
+                    !next ? 0.f
+                    : tr  ? s_pow
+                          : expf(FUSED && j == 0 && p.lam1 ? p.lam1[u] : p.lam[(int64_t)(j + 1) * U + u]);
+                if (FUSED && t == 0 && p.lam_total) lsum += j == 1 && p.lam1 ? p.lam1[u] : p.lam[(int64_t)j * U + u];
                 // prefix_j (only the last one with prefix_last), or for the transition chain
                 // only its last state, P_total
                 float *out = tr ? (next ? nullptr : p.P_total + (int64_t)u * D * D + n)
@@ -422,7 +433,18 @@ cudaError_t launch_compose_dense_tc(const ComposeParams &p, cudaStream_t s) {
         !make_tmap_2d(&tmQ, pbase, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, rows, D * 4, 128, 128,
                       CU_TENSOR_MAP_SWIZZLE_NONE))   // P_0 read whole, like an S tile
         return cudaErrorInvalidValue;
-    const bool fused = p.lam_total != nullptr || p.prefix_last != nullptr;
+    // segment 1 in arrays of its own ([n_units] rows of d x d): its own maps, else unused copies
+    CUtensorMap tmP1 = tmP, tmS1 = tmS;
+    if (p.S1) {
+        if (p.n_seg != 2 || !p.P1 || !p.lam1) return cudaErrorInvalidValue;
+        const uint64_t rows1 = (uint64_t)p.n_units * D;
+        if (!make_tmap_2d(&tmP1, p.P1, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, rows1, D * 4, 32, 128,
+                          CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_tmap_2d(&tmS1, p.S1, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, D, rows1, D * 4, 128, 128,
+                          CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
+    const bool fused = p.lam_total != nullptr || p.prefix_last != nullptr || p.S1 != nullptr;
     auto kern = fused ? compose_dense_tc_kernel<true> : compose_dense_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kern,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -441,7 +463,7 @@ cudaError_t launch_compose_dense_tc(const ComposeParams &p, cudaStream_t s) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, p, tmP, tmS, tmQ);
+    return cudaLaunchKernelEx(&cfg, kern, p, tmP, tmS, tmQ, tmP1, tmS1);
 }
 
 }  // namespace hypic

@@ -87,8 +87,20 @@ struct ComposeParams {
     float *P_total;     // optional, dense families: P_{n-1} ... P_0 per unit
     float *prefix_last; // dense tensor-core compose, internal use: write only the last state,
                         // [n_units][d][d], instead of prefix
+    // internal use (the convolution warm-up): with two segments, segment 1's S, lam and P in
+    // arrays of their own ([n_units][d][d], [n_units] ([n_units][d] for DIAG)); NULL: segment
+    // 1 follows segment 0 in S, lam and P
+    const float *S1;
+    const float *lam1;
+    const float *P1;
     unsigned *err;
 };
+
+// Segment j of unit u in a [segment][unit][per] array, or in segment 1's own [unit][per] array
+__host__ __device__ __forceinline__ const float *compose_seg(const float *a, const float *a1, int64_t j,
+                                                             int64_t n_units, int64_t u, int64_t per) {
+    return (j == 1 && a1) ? a1 + u * per : a + (j * n_units + u) * per;
+}
 
 // The convolution of the warm-up's head tokens (conv.cu): head row r is token
 // seg_start[j] + r - head_off[j] of the prompt, for the segment j with head_off[j] <= r <

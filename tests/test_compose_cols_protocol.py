@@ -277,7 +277,7 @@ def test_compose_cols_model_catches_planted_mistakes(mistake):
     assert hits > 0
 
 
-MODELLED_SOURCE = ("compose_cols.cu", "97818d77c561")
+MODELLED_SOURCE = ("compose_cols.cu", "670a280bf16c")
 
 
 def test_model_is_checked_against_the_current_kernel_source():

@@ -235,7 +235,7 @@ def test_compose_protocol_model_catches_planted_mistakes(mistake, expect):
 
 
 # The kernel source this model was last checked against (code only; comments do not count).
-MODELLED_SOURCE = ("compose_tc.cu", "d0f3c0788ed9")
+MODELLED_SOURCE = ("compose_tc.cu", "1fc5103a21f7")
 
 
 def test_model_is_checked_against_the_current_kernel_source():
