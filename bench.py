@@ -453,8 +453,8 @@ def section_conv_warmup(flush, peak, steps=20, warmup=3, oracle_heads=0, K=4):
            "conv_k": K, "units": units, "head_tokens": rows, "warmup_ms": round(ms, 4),
            "warmup_bytes": nbytes, "warmup_gbs": round(gbs, 1),
            "warmup_hbm_frac": round(gbs / peak["hbm_gbs"], 4),
-           "note": "the pieces go through the workspace (a copy of each rest's entry), so DRAM "
-                   "traffic exceeds these algorithmic bytes"}
+           "note": "the head entries go through the workspace (written by the head build, read "
+                   "by the composition), so DRAM traffic exceeds these algorithmic bytes"}
     if oracle_heads:
         import oracle
         torch.cuda.synchronize()
