@@ -6,7 +6,8 @@ segment's rest (its tokens from min(K - 1, length) on, convolved within the segm
 of a convolutional layer holds them) with the library's build, runs the warm-up, and compares
 each segment's entry in context with the oracle's entry of the same segment built from the
 whole prompt convolved in one pass: relative Frobenius error <= 1e-4 (fp32 inputs), 2e-2 (bf16
-inputs), on S and on T = exp(lam) P."""
+inputs), on S and on T = exp(lam) P. The cached rests, which the composition reads in place,
+must come back bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -49,11 +50,15 @@ def _case(family, dtype, d, K, lens, seed):
         family, dev(kl[keep], dtype), dev(vl[keep], dtype), r_offs,
         log_gate=None if lg is None else dev(lg[keep]), log_gamma=dev(lgam),
         beta=None if beta is None else dev(beta[keep]))
+    rests = [None if t is None else t.clone() for t in (S_r, lam_r, P_r)]
     S, lam, P = hy.hypic_conv_warmup(
         family, offs, inp.k.cuda(), inp.v.cuda(), dev(wk), dev(wv), S_r, lam_r, P_r,
         log_gate=dev(lg), log_gamma=dev(lgam), beta=dev(beta))
     torch.cuda.synchronize()
     assert hy.hypic_get_device_status() == 0
+    # the cached rests are read where they are and left as they were
+    for before, after in zip(rests, (S_r, lam_r, P_r)):
+        assert before is None or torch.equal(before, after)
     # the oracle: the whole prompt convolved in one pass, every segment built from it
     kf = oracle.short_conv(k_raw, wk, normalize=delta)
     vf = oracle.short_conv(v_raw, wv)
