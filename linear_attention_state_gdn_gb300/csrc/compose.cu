@@ -213,6 +213,7 @@ cudaError_t launch_dense(const ComposeParams &p, cudaStream_t s) {
 
 cudaError_t launch_compose_scaled(const ComposeParams &p, cudaStream_t s) {
     if (p.n_seg == 0 || p.n_units == 0) return cudaSuccess;
+    if (p.S1 && (p.n_seg != 2 || !p.lam1)) return cudaErrorInvalidValue;   // segment 1 of a two-segment scan
     const int n4 = p.D * p.D / 4;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.n_units * ((n4 + kScaledThreads - 1) / kScaledThreads)));
@@ -228,6 +229,7 @@ cudaError_t launch_compose_scaled(const ComposeParams &p, cudaStream_t s) {
 
 cudaError_t launch_compose_lam_total(const ComposeParams &p, cudaStream_t s) {
     if (p.n_units == 0 || !p.lam_total) return cudaSuccess;
+    if (p.lam1 && p.n_seg != 2) return cudaErrorInvalidValue;
     const int64_t n = p.n_units * (p.family == HYPIC_FAM_DIAG ? p.D : 1);
     compose_lam_total_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(p);
     return cudaGetLastError();
@@ -235,6 +237,7 @@ cudaError_t launch_compose_lam_total(const ComposeParams &p, cudaStream_t s) {
 
 cudaError_t launch_compose_dense_simt(const ComposeParams &p, cudaStream_t s) {
     if (p.n_seg == 0 || p.n_units == 0) return cudaSuccess;
+    if (p.S1 && (p.n_seg != 2 || !p.lam1 || !p.P1)) return cudaErrorInvalidValue;   // segment 1 of a two-segment scan
     switch (p.D) {
     case 32: return launch_dense<32>(p, s);
     case 64: return launch_dense<64>(p, s);
